@@ -97,11 +97,11 @@ void kvo_attention(int Hq, int Hkv, int d, int64_t L, const uint16_t* q,
             sum += p[i];
         }
         for (int64_t i = 0; i < L; ++i) p[i] /= sum;
-        for (int c = 0; c < d; ++c) {
-            double acc = 0.0;
-            for (int64_t i = 0; i < L; ++i)
-                acc += p[i] * bf16_to_double(v[((int64_t)g * ld + i) * d + c]);
-            out[h * d + c] = acc;
+        /* out[h][c] = sum_i p_i v_i[c], accumulated in ascending i for every c */
+        for (int c = 0; c < d; ++c) out[h * d + c] = 0.0;
+        for (int64_t i = 0; i < L; ++i) {
+            const uint16_t* vr = v + ((int64_t)g * ld + i) * d;
+            for (int c = 0; c < d; ++c) out[h * d + c] += p[i] * bf16_to_double(vr[c]);
         }
     }
 }
