@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 decode-time KV-eviction pass.
+
+Workload (one "step" = one whole eviction pass): Llama-3.1-8B attention
+geometry (32 layers, 32 query / 8 KV heads, head_dim 128, bf16), batch 1, a
+32768-token prefilled cache plus the appended token (L = 32769), budget 3277
+(10%), EMA alpha 0.05, beta 0.001, access-clock ages, full refresh: append,
+split-K attention with probability capture, combine, scoring (probabilities,
+head sum, 32-layer EMA, priority), selection, compaction.  Each timed step
+re-runs decode step 1 on the untouched prefill buffer (compaction writes the
+other ping-pong buffer), after resetting the per-token state on the device.
+
+Metric: algorithmic K/V bytes per step (every live row read once by the
+attention, plus the retained rows read and written by the compaction) over
+the device step time, in GB/s; the same over the end-to-end time of the
+host-buffer entry point (kvev_step_host) is the "e2e" figure.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvev|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the pass has no cross-GPU exchange at batch 1); the value is the sum over
+ranks of the bytes processed over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "eviction decode-step us & KV GB/s vs HBM peak (Llama-8B shape, 32k ctx, 10%)"
+WORKLOAD = dict(workload="llama3.1-8b-shape eviction step, 32k ctx, 10% budget",
+                n_layers=32, n_q_heads=32, n_kv_heads=8, head_dim=128, batch=1,
+                prefill=32768, budget=3277, alpha=0.05, beta=0.001,
+                age="since last access", refresh="full", step=1)
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def kv_bytes(n_layers, n_kv, d, L, budget, batch=1):
+    """(algorithmic bytes of one step, of which attention reads)."""
+    row = 2 * d * 2 * n_kv * n_layers          # K and V of one token, all layers/heads
+    attn = L * row * batch
+    comp = (2 * min(L, budget) * row * batch) if L > budget else 0
+    return attn + comp, attn
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel_file: str, units: float):
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    summary, if it was taken on the current source; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)["attention"]
+        src = open(os.path.join(ROOT, "decoding_kv_cache_split_gb300", "csrc", kernel_file),
+                   "rb").read()
+        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return float(rec["bytes_per_token_layer"]) * units
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    smax = float(f[2])
+                    power.append(float(f[3]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, f[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["no samples"]}
+        busy = [s for s, p in zip(sm, power) if p > 1.5 * min(power)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def to_dev(bits, torch):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def cpu_baseline(wl, n_layers_sample: int):
+    """The fp64 oracle (single thread) on the first `n_layers_sample` layers
+    of the same step; returns (GB/s, seconds, sample description)."""
+    import oracle as O
+    K, V = wl.prefill()
+    L0, W = wl.L0, WORKLOAD
+    st = O.SequenceState.from_prefill(K[:n_layers_sample, 0], V[:n_layers_sample, 0], L0, L0 + 2)
+    q, kn, vn = wl.step_inputs(1)
+    P = O.OracleParams(n_layers_sample, W["n_q_heads"], W["n_kv_heads"], W["head_dim"],
+                       W["budget"], W["alpha"], W["beta"], O.AGE_SINCE_ACCESS)
+    t0 = time.perf_counter()
+    O.step(P, st, 1, True, q[0, :n_layers_sample], kn[0, :n_layers_sample],
+           vn[0, :n_layers_sample], L0, want_probs=False)
+    dt = time.perf_counter() - t0
+    nbytes, _ = kv_bytes(n_layers_sample, W["n_kv_heads"], W["head_dim"], L0 + 1, W["budget"])
+    return nbytes / dt / 1e9, dt, (f"step 1 of the same workload restricted to its first "
+                                   f"{n_layers_sample} of 32 layers (all 32769 tokens)")
+
+
+def reference_arm(args, rank, world):
+    """The oracle, timed on the host cores on a bounded sample per step."""
+    if rank != 0:
+        return
+    import oracle as O
+    from workloads import llama8b_workload
+    W = WORKLOAD
+    # sample: one layer, a token prefix sized so that warmup + steps fit ~2 min
+    per_step_s = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    tokens = int(min(W["prefill"], max(512, per_step_s / 25e-6)))
+    wl = llama8b_workload(0, prefill_len=tokens, n_layers=1)
+    K, V = wl.prefill()
+    st = O.SequenceState.from_prefill(K[:, 0], V[:, 0], tokens, tokens + 2)
+    q, kn, vn = wl.step_inputs(1)
+    budget = max(1, (tokens * W["budget"]) // W["prefill"])
+    P = O.OracleParams(1, W["n_q_heads"], W["n_kv_heads"], W["head_dim"], budget, W["alpha"],
+                       W["beta"], O.AGE_SINCE_ACCESS)
+
+    def one():
+        O.step(P, st, 1, True, q[0], kn[0], vn[0], tokens, want_probs=False)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    nbytes, _ = kv_bytes(1, W["n_kv_heads"], W["head_dim"], tokens + 1, budget)
+    val = nbytes / dt / 1e9
+    sample = (f"1 of 32 layers, {tokens}-token prefill + 1, budget {budget} "
+              f"(same geometry, alpha, beta, access clock)")
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(W, sample=sample),
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvev", choices=["kvev", "reference"])
+    ap.add_argument("--cpu-layers", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+
+    from decoding_kv_cache_split_gb300 import build as kbuild
+    if not os.path.exists(kbuild.LIB):
+        kbuild.build()
+    from decoding_kv_cache_split_gb300 import kvev
+    from workloads import llama8b_workload
+
+    W = WORKLOAD
+    L0, B = W["prefill"], W["budget"]
+    max_ctx = L0 + 64
+    wl = llama8b_workload(0, prefill_len=L0)
+    ep = kvev.EvictionPass(W["n_layers"], W["n_q_heads"], W["n_kv_heads"], W["head_dim"],
+                           W["batch"], max_ctx, B, W["alpha"], W["beta"],
+                           age_mode=kvev.KVEV_AGE_SINCE_ACCESS)
+    for layer in range(W["n_layers"]):
+        k, v = wl.prefill_layer(layer)
+        ep.k[0][layer, :, :, :L0].copy_(torch.from_numpy(k.view(np.int16)).view(torch.bfloat16))
+        ep.v[0][layer, :, :, :L0].copy_(torch.from_numpy(v.view(np.int16)).view(torch.bfloat16))
+    q, kn, vn = wl.step_inputs(1)
+    qd, knd, vnd = to_dev(q, torch), to_dev(kn, torch), to_dev(vn, torch)
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        ep.begin(L0, stream)
+        ep.step(qd, knd, vnd, stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    kvev.kvev_sync(ep.ctx)
+
+    # ---------------------------------------------------------- device timing
+    kvev.kvev_profile(ep.ctx, True)
+    kvev.kvev_profile_read(ep.ctx)          # reset accumulators
+    n0 = kvev.kvev_launch_count(ep.ctx)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    kvev.kvev_sync(ep.ctx)
+    prof = kvev.kvev_profile_read(ep.ctx)
+    kvev.kvev_profile(ep.ctx, False)
+    launches = kvev.kvev_launch_count(ep.ctx) - n0
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    nbytes, attn_bytes = kv_bytes(W["n_layers"], W["n_kv_heads"], W["head_dim"], L0 + 1, B)
+    value = world * nbytes / (ms * 1e-3) / 1e9
+
+    # -------------------------------------------------- end to end (host API)
+    qh = torch.from_numpy(q.view(np.int16)).pin_memory()
+    knh = torch.from_numpy(kn.view(np.int16)).pin_memory()
+    vnh = torch.from_numpy(vn.view(np.int16)).pin_memory()
+    outh = torch.empty((1, W["n_layers"], W["n_q_heads"], W["head_dim"]),
+                       dtype=torch.float32).pin_memory()
+    reth = torch.empty((1, B), dtype=torch.int32).pin_memory()
+    nreth = torch.empty((1,), dtype=torch.int32).pin_memory()
+    h2d = qh.numel() * 2 + knh.numel() * 2 + vnh.numel() * 2
+    d2h = outh.numel() * 4 + reth.numel() * 4 + nreth.numel() * 4
+
+    def one_e2e(step_no=1):
+        ep.begin(L0, stream)
+        kvev.kvev_step_host(ep.ctx, qh, knh, vnh, ep.cache, ep.state, step_no, outh, reth, nreth,
+                            stream)
+
+    for _ in range(args.warmup):
+        one_e2e()
+    n_e2e = max(10, min(args.steps, 500))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        one_e2e()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+    if dist:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = world * nbytes / (e2e_ms * 1e-3) / 1e9
+    assert int(nreth[0]) == B
+
+    # --------------------------------------------------------------- roofline
+    peak, peak_kind = measured_peak()
+    att_ms, att_n = prof.get("attention", (0.0, 0))
+    att_avg = att_ms / max(1, att_n)
+    attn_achieved = attn_bytes / (att_avg * 1e-3) / 1e9 if att_avg > 0 else None
+    tokens_layers = (L0 + 1) * W["n_layers"]
+    traffic = ncu_traffic("attn.cu", tokens_layers)
+    kernels_us = {k: round(v[0] / max(1, v[1]) * 1e3, 2) for k, v in prof.items()}
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            val, secs, sample = cpu_baseline(wl, args.cpu_layers)
+            cpu = {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": sample, "seconds": round(secs, 2)}
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "us_per_step": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(W, parallelism=f"replicas{world}",
+                           l2="inputs larger than L2 (4.3 GB of K/V per step)"),
+            "frac_of_peak": {"measured": round(value / world / peak, 4),
+                             "nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+                             "peak_kind": peak_kind},
+            "kv_tokens_per_s": round(world * (L0 + 1) / (ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "kernel": "attention",
+                         "achieved": round(attn_achieved, 2) if attn_achieved else None,
+                         "peak": peak, "unit": "GB/s",
+                         "frac": round(attn_achieved / peak, 4) if attn_achieved else None,
+                         "traffic": traffic, "algorithmic_bytes": attn_bytes,
+                         "peak_kind": f"{peak_kind} (copy bandwidth)"},
+            "kernels_us": kernels_us,
+            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    ep.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,584 @@
+// C ABI of the eviction pass: argument checking, scratch ownership and the
+// per-step launch sequence (append -> attention -> combine -> score ->
+// select -> compact) on the caller's stream.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "kvev_internal.h"
+
+namespace kvev {
+int attn_warps_per_cta();
+}
+
+using namespace kvev;
+
+namespace {
+
+thread_local char g_err[512] = "no error";
+
+kvev_status fail(kvev_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+kvev_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(KVEV_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+enum { kProfAppend = 0, kProfAttn, kProfCombine, kProfScore, kProfSelect, kProfCompact, kProfInit };
+
+struct Workspace {
+    float* logits = nullptr;
+    float* part_o = nullptr;
+    float* part_ml = nullptr;
+    float* lse2 = nullptr;
+    uint32_t* keys = nullptr;
+    float* m_s = nullptr;
+    int32_t* tref_s = nullptr;
+    int32_t* tins_s = nullptr;
+    int32_t* pos_s = nullptr;
+    float* msum_part = nullptr;
+    uint32_t* status = nullptr;
+    uint16_t* stg_q = nullptr;
+    uint16_t* stg_k = nullptr;
+    uint16_t* stg_v = nullptr;
+    float* stg_out = nullptr;
+    int32_t* stg_ret = nullptr;
+    int32_t* stg_nret = nullptr;
+    size_t bytes = 0;
+};
+
+// Lays out (or, with base == nullptr, only sizes) the context's scratch.
+Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base) {
+    Workspace w;
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char* {
+        char* p = base ? base + off : nullptr;
+        off += align_up(bytes, 256);
+        return p;
+    };
+    const size_t rows = (size_t)L.n_layers * L.batch * L.n_kv_heads;
+    const size_t G = (size_t)(L.n_q_heads / L.n_kv_heads);
+    const size_t ctx = (size_t)L.batch * L.max_ctx;
+    const size_t nblk = (size_t)((L.max_ctx + kScoreThreads - 1) / kScoreThreads);
+    w.logits = (float*)take(rows * L.max_ctx * G * 4);
+    w.part_o = (float*)take((size_t)slots * G * L.head_dim * 4);
+    w.part_ml = (float*)take((size_t)slots * G * 2 * 4);
+    w.lse2 = (float*)take(rows * G * 4);
+    w.keys = (uint32_t*)take(ctx * 4);
+    w.m_s = (float*)take(ctx * 4);
+    w.tref_s = (int32_t*)take(ctx * 4);
+    w.tins_s = (int32_t*)take(ctx * 4);
+    w.pos_s = (int32_t*)take(ctx * 4);
+    w.msum_part = (float*)take((size_t)L.batch * nblk * 4);
+    w.status = (uint32_t*)take(4);
+    const size_t qn = (size_t)L.batch * L.n_layers * L.n_q_heads * L.head_dim;
+    const size_t kn = (size_t)L.batch * L.n_layers * L.n_kv_heads * L.head_dim;
+    w.stg_q = (uint16_t*)take(qn * 2);
+    w.stg_k = (uint16_t*)take(kn * 2);
+    w.stg_v = (uint16_t*)take(kn * 2);
+    w.stg_out = (float*)take(qn * 4);
+    w.stg_ret = (int32_t*)take((size_t)L.batch * budget * 4);
+    w.stg_nret = (int32_t*)take((size_t)L.batch * 4);
+    w.bytes = off;
+    return w;
+}
+
+kvev_status check_layout(const kvev_layout* L, int64_t budget) {
+    if (!L) return fail(KVEV_EINVAL, "layout is NULL");
+    if (L->n_layers < 1 || L->n_q_heads < 1 || L->n_kv_heads < 1 || L->batch < 1)
+        return fail(KVEV_EINVAL, "layout: n_layers, n_q_heads, n_kv_heads, batch must be >= 1");
+    if (L->n_q_heads % L->n_kv_heads != 0)
+        return fail(KVEV_EINVAL, "layout: n_q_heads (%d) must be a multiple of n_kv_heads (%d)",
+                    L->n_q_heads, L->n_kv_heads);
+    if (L->head_dim != 64 && L->head_dim != 128)
+        return fail(KVEV_EUNSUPPORTED, "layout: head_dim %d (supported: 64, 128)", L->head_dim);
+    if (L->n_q_heads / L->n_kv_heads != 4)
+        return fail(KVEV_EUNSUPPORTED, "layout: query heads per KV head %d (supported: 4)",
+                    L->n_q_heads / L->n_kv_heads);
+    if (L->max_ctx < 2) return fail(KVEV_EINVAL, "layout: max_ctx must be >= 2");
+    if (L->page_tokens != 1)
+        return fail(KVEV_EUNSUPPORTED, "layout: page_tokens %d (supported: 1)", L->page_tokens);
+    if (L->kv_dtype != KVEV_BF16) return fail(KVEV_EUNSUPPORTED, "layout: kv_dtype must be BF16");
+    if (budget < 1 || budget >= L->max_ctx)
+        return fail(KVEV_EINVAL, "budget %lld must be in [1, max_ctx)", (long long)budget);
+    return KVEV_OK;
+}
+
+int64_t attn_grid_for_device(int num_sms, const kvev_layout& L) {
+    const int per_sm = attn_ctas_per_sm(L.head_dim, L.n_q_heads / L.n_kv_heads);
+    return (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
+}
+
+}  // namespace
+
+struct kvev_ctx {
+    kvev_layout lay{};
+    int64_t budget = 0;
+    float alpha = 0.f, beta = 0.f;
+    int32_t refresh_mode = KVEV_REFRESH_FULL, refresh_period = 1;
+    int32_t age_mode = KVEV_AGE_SINCE_INSERT, pool = KVEV_POOL_SUM;
+    int32_t group = 4;
+    int32_t len = 0, prefill_len = 0;
+    int64_t step = 0;
+    bool begun = false;
+    int device = 0, num_sms = 0;
+    int attn_grid = 0, attn_warps = 0;
+    char* ws_base = nullptr;
+    Workspace ws;
+    float* dbg_probs = nullptr;
+    float* dbg_prio = nullptr;
+    bool prof = false;
+    std::vector<cudaEvent_t> ev_pool;
+    std::vector<int> ev_kind;   // kernel slot of each recorded start/end pair
+    size_t ev_used = 0;
+    float prof_ms[KVEV_PROFILE_SLOTS] = {};
+    int64_t prof_n[KVEV_PROFILE_SLOTS] = {};
+    int64_t launches = 0;
+};
+
+namespace {
+
+cudaEvent_t next_event(kvev_ctx* c) {
+    if (c->ev_used == c->ev_pool.size()) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        c->ev_pool.push_back(e);
+    }
+    return c->ev_pool[c->ev_used++];
+}
+
+kvev_status harvest_profile(kvev_ctx* c) {
+    for (size_t k = 0; k + 1 < c->ev_used; k += 2) {
+        cudaError_t e = cudaEventSynchronize(c->ev_pool[k + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "profile event");
+        float ms = 0.f;
+        e = cudaEventElapsedTime(&ms, c->ev_pool[k], c->ev_pool[k + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "profile elapsed");
+        const int slot = c->ev_kind[k / 2];
+        c->prof_ms[slot] += ms;
+        c->prof_n[slot] += 1;
+    }
+    c->ev_used = 0;
+    c->ev_kind.clear();
+    return KVEV_OK;
+}
+
+// Launch helper: optional event pair around the launch, launch counting.
+template <typename F>
+kvev_status timed_launch(kvev_ctx* c, int slot, cudaStream_t s, const char* what, F&& f) {
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (c->prof) {
+        if (c->ev_used + 2 > (1u << 16)) {
+            kvev_status st = harvest_profile(c);
+            if (st != KVEV_OK) return st;
+        }
+        e0 = next_event(c);
+        e1 = next_event(c);
+        if (!e0 || !e1) return fail(KVEV_ENOMEM, "cannot create profiling events");
+        cudaEventRecord(e0, s);
+    }
+    cudaError_t e = f();
+    c->launches += 1;
+    if (e != cudaSuccess) {
+        if (c->prof) c->ev_used -= 2;
+        return cuda_fail(e, what);
+    }
+    if (c->prof) {
+        cudaEventRecord(e1, s);
+        c->ev_kind.push_back(slot);
+    }
+    return KVEV_OK;
+}
+
+kvev_status check_status_word(kvev_ctx* c, cudaStream_t s) {
+    uint32_t host = 0;
+    cudaError_t e = cudaMemcpyAsync(&host, c->ws.status, 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "device status");
+    if (host & kStatusTimeout) {
+        cudaMemsetAsync(c->ws.status, 0, 4, s);
+        cudaStreamSynchronize(s);
+        return fail(KVEV_ETIMEOUT, "a device wait exceeded its iteration limit");
+    }
+    return KVEV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvev_last_error(const kvev_ctx*) { return g_err; }
+
+kvev_status kvev_workspace_size(const kvev_layout* layout, int64_t budget, size_t* bytes) {
+    kvev_status st = check_layout(layout, budget);
+    if (st != KVEV_OK) return st;
+    if (!bytes) return fail(KVEV_EINVAL, "bytes is NULL");
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    const int64_t W = attn_grid_for_device(sms, *layout) * attn_warps_per_cta();
+    const int64_t rows = (int64_t)layout->n_layers * layout->batch * layout->n_kv_heads;
+    *bytes = carve(*layout, budget, W + rows, nullptr).bytes;
+    return KVEV_OK;
+}
+
+kvev_status kvev_create(const kvev_layout* layout, int64_t budget, int32_t granularity,
+                        float alpha, float beta, const void* regions, kvev_ctx** out) {
+    if (!out) return fail(KVEV_EINVAL, "out is NULL");
+    *out = nullptr;
+    kvev_status st = check_layout(layout, budget);
+    if (st != KVEV_OK) return st;
+    if (granularity != layout->page_tokens)
+        return fail(KVEV_EINVAL, "granularity %d != layout.page_tokens %d", granularity,
+                    layout->page_tokens);
+    if (!(alpha > 0.f && alpha <= 1.f)) return fail(KVEV_EINVAL, "alpha must be in (0, 1]");
+    if (!(beta >= 0.f)) return fail(KVEV_EINVAL, "beta must be >= 0 (+inf allowed)");
+    if (regions) return fail(KVEV_EUNSUPPORTED, "a region table needs page-granular eviction");
+
+    kvev_ctx* c = new (std::nothrow) kvev_ctx;
+    if (!c) return fail(KVEV_ENOMEM, "host allocation failed");
+    c->lay = *layout;
+    c->budget = budget;
+    c->alpha = alpha;
+    c->beta = beta;
+    c->group = layout->n_q_heads / layout->n_kv_heads;
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e != cudaSuccess) {
+        delete c;
+        return cuda_fail(e, "device query");
+    }
+    c->attn_grid = (int)attn_grid_for_device(c->num_sms, *layout);
+    c->attn_warps = c->attn_grid * attn_warps_per_cta();
+    const int64_t rows = (int64_t)layout->n_layers * layout->batch * layout->n_kv_heads;
+    const size_t bytes = carve(*layout, budget, c->attn_warps + rows, nullptr).bytes;
+    e = cudaMalloc(&c->ws_base, bytes);
+    if (e != cudaSuccess) {
+        delete c;
+        cudaGetLastError();
+        return fail(KVEV_ENOMEM, "cudaMalloc of %zu bytes of scratch failed", bytes);
+    }
+    c->ws = carve(*layout, budget, c->attn_warps + rows, c->ws_base);
+    e = cudaMemset(c->ws.status, 0, 4);
+    if (e != cudaSuccess) {
+        cudaFree(c->ws_base);
+        delete c;
+        return cuda_fail(e, "scratch init");
+    }
+    *out = c;
+    return KVEV_OK;
+}
+
+void kvev_destroy(kvev_ctx* c) {
+    if (!c) return;
+    for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+    if (c->ws_base) cudaFree(c->ws_base);
+    delete c;
+}
+
+kvev_status kvev_refresh_mode(kvev_ctx* c, int32_t mode, int32_t period) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (mode != KVEV_REFRESH_FULL && mode != KVEV_REFRESH_LAZY && mode != KVEV_REFRESH_FROZEN)
+        return fail(KVEV_EINVAL, "unknown refresh mode %d", mode);
+    if (mode == KVEV_REFRESH_LAZY && period < 1)
+        return fail(KVEV_EINVAL, "lazy refresh period must be >= 1");
+    c->refresh_mode = mode;
+    c->refresh_period = mode == KVEV_REFRESH_LAZY ? period : 1;
+    return KVEV_OK;
+}
+
+kvev_status kvev_configure(kvev_ctx* c, int32_t age_mode, int32_t pool) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (age_mode != KVEV_AGE_SINCE_INSERT && age_mode != KVEV_AGE_SINCE_ACCESS)
+        return fail(KVEV_EINVAL, "unknown age mode %d", age_mode);
+    if (pool != KVEV_POOL_SUM && pool != KVEV_POOL_MEAN)
+        return fail(KVEV_EINVAL, "unknown pooling %d", pool);
+    c->age_mode = age_mode;
+    c->pool = pool;
+    return KVEV_OK;
+}
+
+kvev_status kvev_begin(kvev_ctx* c, int32_t prefill_len) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (prefill_len < 0 || prefill_len >= c->lay.max_ctx)
+        return fail(KVEV_EINVAL, "prefill_len %d must be in [0, max_ctx)", prefill_len);
+    c->len = prefill_len;
+    c->prefill_len = prefill_len;
+    c->step = 0;
+    c->begun = true;
+    return KVEV_OK;
+}
+
+kvev_status kvev_length(const kvev_ctx* c, int32_t* len) {
+    if (!c || !len) return fail(KVEV_EINVAL, "NULL argument");
+    *len = c->len;
+    return KVEV_OK;
+}
+
+kvev_status kvev_init_state(kvev_ctx* c, const kvev_state* st, void* stream) {
+    if (!c || !st) return fail(KVEV_EINVAL, "NULL argument");
+    if (!st->score || !st->t_ins || !st->t_ref || !st->pos)
+        return fail(KVEV_EINVAL, "state has a NULL array");
+    if (!c->begun) return fail(KVEV_ESTATE, "kvev_begin must come first");
+    cudaStream_t s = (cudaStream_t)stream;
+    const int len = c->len;
+    return timed_launch(c, kProfInit, s, "init_state", [&] {
+        return launch_init_state(*st, c->lay.batch, c->lay.max_ctx, len, s);
+    });
+}
+
+kvev_status kvev_set_debug(kvev_ctx* c, float* probs, float* priority) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    c->dbg_probs = probs;
+    c->dbg_prio = priority;
+    return KVEV_OK;
+}
+
+kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void* v_new,
+                      kvev_cache* cache, const kvev_state* st, int64_t step, float* out,
+                      int32_t* retained_idx, int32_t* n_retained, void* stream) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (!q || !k_new || !v_new || !cache || !st || !out || !retained_idx || !n_retained)
+        return fail(KVEV_EINVAL, "NULL argument");
+    if (!cache->k[0] || !cache->k[1] || !cache->v[0] || !cache->v[1])
+        return fail(KVEV_EINVAL, "cache has a NULL buffer");
+    if (cache->cur != 0 && cache->cur != 1) return fail(KVEV_EINVAL, "cache.cur must be 0 or 1");
+    if (!st->score || !st->t_ins || !st->t_ref || !st->pos)
+        return fail(KVEV_EINVAL, "state has a NULL array");
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(cache->k[0]) ||
+        !aligned16(cache->k[1]) || !aligned16(cache->v[0]) || !aligned16(cache->v[1]) ||
+        !aligned16(out))
+        return fail(KVEV_EINVAL, "q, k_new, v_new, out and the cache buffers must be 16-byte aligned");
+    if (!c->begun) return fail(KVEV_ESTATE, "kvev_begin must come before the first step");
+    if (step != c->step + 1)
+        return fail(KVEV_ESTATE, "step %lld out of order (expected %lld)", (long long)step,
+                    (long long)(c->step + 1));
+    if (c->len + 1 > c->lay.max_ctx)
+        return fail(KVEV_EINVAL, "cache full: %d live tokens, max_ctx %d", c->len, c->lay.max_ctx);
+
+    cudaStream_t s = (cudaStream_t)stream;
+    const kvev_layout& Ly = c->lay;
+    const int G = c->group;
+    const int t = (int)step;
+    const int L = c->len + 1;
+    const int cur = cache->cur;
+    bool refresh = true;
+    if (c->refresh_mode == KVEV_REFRESH_LAZY) refresh = (t - 1) % c->refresh_period == 0;
+    if (c->refresh_mode == KVEV_REFRESH_FROZEN) refresh = t == 1;
+    const int rows = Ly.n_layers * Ly.batch * Ly.n_kv_heads;
+    const int tiles_per_row = (L + kTile - 1) / kTile;
+    const int n_keep = L < c->budget ? L : (int)c->budget;
+    const bool identity = L <= c->budget;
+    kvev_status rc;
+
+    AppendArgs ap{};
+    ap.k = (uint16_t*)cache->k[cur];
+    ap.v = (uint16_t*)cache->v[cur];
+    ap.k_new = (const uint16_t*)k_new;
+    ap.v_new = (const uint16_t*)v_new;
+    ap.st = *st;
+    ap.slot = c->len;
+    ap.t = t;
+    ap.pos = c->prefill_len + t - 1;
+    ap.n_layers = Ly.n_layers;
+    ap.batch = Ly.batch;
+    ap.n_kv = Ly.n_kv_heads;
+    ap.max_ctx = Ly.max_ctx;
+    ap.head_dim = Ly.head_dim;
+    rc = timed_launch(c, kProfAppend, s, "append", [&] { return launch_append(ap, s); });
+    if (rc != KVEV_OK) return rc;
+
+    AttnArgs at{};
+    at.k = (const uint16_t*)cache->k[cur];
+    at.v = (const uint16_t*)cache->v[cur];
+    at.q = (const uint16_t*)q;
+    at.logits = c->ws.logits;
+    at.part_o = c->ws.part_o;
+    at.part_ml = c->ws.part_ml;
+    at.status = c->ws.status;
+    at.n_tiles_total = (int64_t)rows * tiles_per_row;
+    at.tiles_per_row = tiles_per_row;
+    at.L = L;
+    at.max_ctx = Ly.max_ctx;
+    at.n_layers = Ly.n_layers;
+    at.batch = Ly.batch;
+    at.n_kv = Ly.n_kv_heads;
+    at.n_q = Ly.n_q_heads;
+    at.total_warps = c->attn_warps;
+    at.write_logits = refresh ? 1 : 0;
+    at.q_scale = (float)(1.4426950408889634 / sqrt((double)Ly.head_dim));
+    rc = timed_launch(c, kProfAttn, s, "attention", [&] {
+        return launch_attention(at, Ly.head_dim, G, c->attn_grid, s);
+    });
+    if (rc != KVEV_OK) return rc;
+
+    CombineArgs cb{};
+    cb.part_o = c->ws.part_o;
+    cb.part_ml = c->ws.part_ml;
+    cb.out = out;
+    cb.lse2 = c->ws.lse2;
+    cb.n_tiles_total = at.n_tiles_total;
+    cb.tiles_per_row = tiles_per_row;
+    cb.total_warps = c->attn_warps;
+    cb.n_layers = Ly.n_layers;
+    cb.batch = Ly.batch;
+    cb.n_kv = Ly.n_kv_heads;
+    cb.n_q = Ly.n_q_heads;
+    rc = timed_launch(c, kProfCombine, s, "combine",
+                      [&] { return launch_combine(cb, Ly.head_dim, G, s); });
+    if (rc != KVEV_OK) return rc;
+
+    ScoreArgs sc{};
+    sc.logits = c->ws.logits;
+    sc.lse2 = c->ws.lse2;
+    sc.st = *st;
+    sc.m_s = c->ws.m_s;
+    sc.tref_s = c->ws.tref_s;
+    sc.tins_s = c->ws.tins_s;
+    sc.pos_s = c->ws.pos_s;
+    sc.keys = c->ws.keys;
+    sc.msum_part = c->ws.msum_part;
+    sc.dbg_probs = refresh ? c->dbg_probs : nullptr;
+    sc.dbg_prio = c->dbg_prio;
+    sc.L = L;
+    sc.max_ctx = Ly.max_ctx;
+    sc.n_layers = Ly.n_layers;
+    sc.batch = Ly.batch;
+    sc.n_kv = Ly.n_kv_heads;
+    sc.n_q = Ly.n_q_heads;
+    sc.refresh = refresh ? 1 : 0;
+    sc.age_mode = c->age_mode;
+    sc.pool_mean = c->pool == KVEV_POOL_MEAN ? 1 : 0;
+    sc.t = t;
+    sc.alpha = c->alpha;
+    sc.beta = c->beta;
+    sc.access_thr = (float)(2.0 * Ly.n_q_heads * Ly.n_layers / (double)L);
+    int n_part = 0;
+    rc = timed_launch(c, kProfScore, s, "score", [&] { return launch_score(sc, G, &n_part, s); });
+    if (rc != KVEV_OK) return rc;
+
+    SelectArgs se{};
+    se.keys = c->ws.keys;
+    se.m_s = c->ws.m_s;
+    se.msum_part = c->ws.msum_part;
+    se.n_part = n_part;
+    se.retained = retained_idx;
+    se.n_retained = n_retained;
+    se.L = L;
+    se.max_ctx = Ly.max_ctx;
+    se.budget = (int)c->budget;
+    se.refresh = refresh ? 1 : 0;
+    rc = timed_launch(c, kProfSelect, s, "select",
+                      [&] { return launch_select(se, Ly.batch, s); });
+    if (rc != KVEV_OK) return rc;
+
+    CompactArgs cp{};
+    cp.k_src = (const uint16_t*)cache->k[cur];
+    cp.v_src = (const uint16_t*)cache->v[cur];
+    cp.k_dst = (uint16_t*)cache->k[cur ^ 1];
+    cp.v_dst = (uint16_t*)cache->v[cur ^ 1];
+    cp.retained = retained_idx;
+    cp.m_s = c->ws.m_s;
+    cp.tref_s = c->ws.tref_s;
+    cp.tins_s = c->ws.tins_s;
+    cp.pos_s = c->ws.pos_s;
+    cp.st = *st;
+    cp.n_keep = n_keep;
+    cp.identity = identity ? 1 : 0;
+    cp.rows = rows;
+    cp.batch = Ly.batch;
+    cp.n_kv = Ly.n_kv_heads;
+    cp.max_ctx = Ly.max_ctx;
+    cp.budget = (int)c->budget;
+    cp.head_dim = Ly.head_dim;
+    rc = timed_launch(c, kProfCompact, s, "compact",
+                      [&] { return launch_compact(cp, c->num_sms, s); });
+    if (rc != KVEV_OK) return rc;
+
+    if (!identity) cache->cur = cur ^ 1;
+    c->len = n_keep;
+    c->step = step;
+    return KVEV_OK;
+}
+
+kvev_status kvev_step_host(kvev_ctx* c, const void* q_host, const void* k_new_host,
+                           const void* v_new_host, kvev_cache* cache, const kvev_state* st,
+                           int64_t step, float* out_host, int32_t* retained_idx_host,
+                           int32_t* n_retained_host, void* stream) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (!q_host || !k_new_host || !v_new_host || !out_host || !retained_idx_host ||
+        !n_retained_host)
+        return fail(KVEV_EINVAL, "NULL argument");
+    cudaStream_t s = (cudaStream_t)stream;
+    const kvev_layout& Ly = c->lay;
+    const size_t qb = (size_t)Ly.batch * Ly.n_layers * Ly.n_q_heads * Ly.head_dim * 2;
+    const size_t kb = (size_t)Ly.batch * Ly.n_layers * Ly.n_kv_heads * Ly.head_dim * 2;
+    cudaError_t e = cudaMemcpyAsync(c->ws.stg_q, q_host, qb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->ws.stg_k, k_new_host, kb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(c->ws.stg_v, v_new_host, kb, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    kvev_status rc = kvev_step(c, c->ws.stg_q, c->ws.stg_k, c->ws.stg_v, cache, st, step,
+                               c->ws.stg_out, c->ws.stg_ret, c->ws.stg_nret, stream);
+    if (rc != KVEV_OK) return rc;
+    e = cudaMemcpyAsync(out_host, c->ws.stg_out, qb * 2, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(retained_idx_host, c->ws.stg_ret, (size_t)Ly.batch * c->budget * 4,
+                            cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(n_retained_host, c->ws.stg_nret, (size_t)Ly.batch * 4,
+                            cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    return check_status_word(c, s);
+}
+
+kvev_status kvev_profile(kvev_ctx* c, int32_t enable) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    c->prof = enable != 0;
+    return KVEV_OK;
+}
+
+kvev_status kvev_profile_read(kvev_ctx* c, float* ms, int64_t* launches) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    kvev_status st = harvest_profile(c);
+    if (st != KVEV_OK) return st;
+    for (int k = 0; k < KVEV_PROFILE_SLOTS; ++k) {
+        if (ms) ms[k] = c->prof_ms[k];
+        if (launches) launches[k] = c->prof_n[k];
+        c->prof_ms[k] = 0.f;
+        c->prof_n[k] = 0;
+    }
+    return KVEV_OK;
+}
+
+kvev_status kvev_launch_count(const kvev_ctx* c, int64_t* launches) {
+    if (!c || !launches) return fail(KVEV_EINVAL, "NULL argument");
+    *launches = c->launches;
+    return KVEV_OK;
+}
+
+kvev_status kvev_sync(kvev_ctx* c, void* stream) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "pending CUDA error");
+    return check_status_word(c, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,113 @@
+// Internal declarations of the kvev CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvev.h"
+
+namespace kvev {
+
+constexpr uint32_t kWaitLimit = 1u << 22;   // iteration cap of every device spin-wait
+
+// Device status word bits (ctx->status_word); read by kvev_sync / kvev_step_host.
+enum : uint32_t { kStatusTimeout = 1u };
+
+// Work decomposition of the split-K attention: every (layer, sequence, KV head)
+// "row" of the cache is cut into tiles of kTile tokens; the tiles of all rows,
+// in row order, are dealt out to the grid's warps in equal contiguous ranges
+// (so every warp streams the same number of bytes).  Warp w's piece of row r
+// writes its softmax partial to slot w + r.
+constexpr int kTile = 16;
+
+struct AttnArgs {
+    const uint16_t* k;     // cache buffer [rows][max_ctx][D] (rows = Ly*b*Hkv)
+    const uint16_t* v;
+    const uint16_t* q;     // [b][Ly][Hq][D]
+    float* logits;         // [rows][max_ctx][G] log2-domain scaled logits (refresh)
+    float* part_o;         // [slots][G][D]
+    float* part_ml;        // [slots][G][2] running max (log2 domain), sum
+    uint32_t* status;
+    int64_t n_tiles_total; // rows * tiles_per_row
+    int32_t tiles_per_row;
+    int32_t L;             // live tokens per row (after the append)
+    int32_t max_ctx;
+    int32_t n_layers, batch, n_kv, n_q;
+    int32_t total_warps;
+    int32_t write_logits;
+    float q_scale;         // log2(e) / sqrt(D)
+};
+
+struct CombineArgs {
+    const float* part_o;
+    const float* part_ml;
+    float* out;            // [b][Ly][Hq][D]
+    float* lse2;           // [rows][G] = [Ly][b][Hq]
+    int64_t n_tiles_total;
+    int32_t tiles_per_row;
+    int32_t total_warps;
+    int32_t n_layers, batch, n_kv, n_q;
+};
+
+struct ScoreArgs {
+    const float* logits;   // [rows][max_ctx][G]
+    const float* lse2;     // [Ly][b][Hq]
+    kvev_state st;         // caller's state (read)
+    float* m_s;            // scratch [b][max_ctx] updated score
+    int32_t* tref_s;       // scratch updated t_ref
+    int32_t* tins_s;       // scratch copy of t_ins
+    int32_t* pos_s;        // scratch copy of pos
+    uint32_t* keys;        // scratch [b][max_ctx] order-preserving priority bits
+    float* msum_part;      // [b][gridDim.x] partial sums of the old tokens' scores
+    float* dbg_probs;      // [b][Ly][Hq][max_ctx] or null
+    float* dbg_prio;       // [b][max_ctx] or null
+    int32_t L, max_ctx, n_layers, batch, n_kv, n_q;
+    int32_t refresh, age_mode, pool_mean;
+    int32_t t;
+    float alpha, beta, access_thr;   // access: sum over layers of head-summed p >= access_thr
+};
+
+struct SelectArgs {
+    const uint32_t* keys;
+    float* m_s;
+    const float* msum_part;
+    int32_t n_part;
+    int32_t* retained;     // [b][budget]
+    int32_t* n_retained;   // [b]
+    float* dbg_prio;       // fix the new token's entry? (no: priority of new token is 0)
+    int32_t L, max_ctx, budget, refresh;
+};
+
+struct CompactArgs {
+    const uint16_t* k_src; const uint16_t* v_src;
+    uint16_t* k_dst; uint16_t* v_dst;
+    const int32_t* retained;   // [b][budget]
+    const float* m_s; const int32_t* tref_s; const int32_t* tins_s; const int32_t* pos_s;
+    kvev_state st;             // written
+    int32_t n_keep;            // retained per sequence (min(L, budget))
+    int32_t identity;          // 1: no eviction, state only
+    int32_t rows, batch, n_kv, max_ctx, budget, head_dim;
+};
+
+struct AppendArgs {
+    uint16_t* k; uint16_t* v;            // live buffer
+    const uint16_t* k_new; const uint16_t* v_new;   // [b][Ly][Hkv][D]
+    kvev_state st;
+    int32_t slot, t, pos, n_layers, batch, n_kv, max_ctx, head_dim;
+};
+
+// ---- launchers (return cudaGetLastError of the launch) --------------------
+int attn_ctas_per_sm(int head_dim, int group);
+size_t attn_smem_bytes(int head_dim, int group);
+cudaError_t launch_attention(const AttnArgs& a, int head_dim, int group, int grid,
+                             cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs& a, int head_dim, int group, cudaStream_t s);
+cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStream_t s);
+cudaError_t launch_select(const SelectArgs& a, int batch, cudaStream_t s);
+cudaError_t launch_compact(const CompactArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_init_state(kvev_state st, int batch, int max_ctx, int len, cudaStream_t s);
+
+constexpr int kScoreThreads = 256;
+
+}  // namespace kvev

@@ -1,0 +1,281 @@
+"""Python binding of the kvev C ABI (include/kvev.h).
+
+Argument marshalling only: every function has the C entry point's name,
+takes torch tensors (or raw integer pointers) and raises KvevError on a
+non-OK status.  Nothing here computes any part of the eviction pass; the
+library must be built (``python -m decoding_kv_cache_split_gb300.build``)
+and the binding refuses to run without it.
+
+``EvictionPass`` is a convenience owner of the device buffers (ping-pong
+cache, per-token state, outputs) for one context; it, too, only allocates
+torch tensors and forwards to the C calls.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkvev.so")
+
+KVEV_OK, KVEV_EINVAL, KVEV_ENOMEM, KVEV_ECUDA, KVEV_ESTATE, KVEV_ETIMEOUT, KVEV_EUNSUPPORTED = range(7)
+STATUS_NAMES = ["OK", "EINVAL", "ENOMEM", "ECUDA", "ESTATE", "ETIMEOUT", "EUNSUPPORTED"]
+KVEV_REFRESH_FULL, KVEV_REFRESH_LAZY, KVEV_REFRESH_FROZEN = 0, 1, 2
+KVEV_AGE_SINCE_INSERT, KVEV_AGE_SINCE_ACCESS = 0, 1
+KVEV_POOL_SUM, KVEV_POOL_MEAN = 0, 1
+KVEV_BF16 = 0
+KVEV_PROFILE_SLOTS = 8
+PROFILE_NAMES = ["append", "attention", "combine", "score", "select", "compact", "init_state", "-"]
+
+# every entry point declared in include/kvev.h
+EXPORTS = ["kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_size",
+           "kvev_refresh_mode", "kvev_configure", "kvev_begin", "kvev_length",
+           "kvev_init_state", "kvev_step", "kvev_step_host", "kvev_set_debug",
+           "kvev_profile", "kvev_profile_read", "kvev_launch_count", "kvev_sync"]
+
+
+class KvevError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"KVEV_{name}: {message}")
+
+
+class kvev_layout(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("batch", ctypes.c_int32), ("max_ctx", ctypes.c_int32),
+                ("page_tokens", ctypes.c_int32), ("kv_dtype", ctypes.c_int32)]
+
+
+class kvev_cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p * 2), ("v", ctypes.c_void_p * 2), ("cur", ctypes.c_int32)]
+
+
+class kvev_state(ctypes.Structure):
+    _fields_ = [("score", ctypes.c_void_p), ("t_ins", ctypes.c_void_p),
+                ("t_ref", ctypes.c_void_p), ("pos", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA library first "
+                               "(python -m decoding_kv_cache_split_gb300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, I64, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        sig = {
+            "kvev_create": ([P, I64, I32, F, F, P, P], I32),
+            "kvev_destroy": ([P], None),
+            "kvev_last_error": ([P], ctypes.c_char_p),
+            "kvev_workspace_size": ([P, I64, P], I32),
+            "kvev_refresh_mode": ([P, I32, I32], I32),
+            "kvev_configure": ([P, I32, I32], I32),
+            "kvev_begin": ([P, I32], I32),
+            "kvev_length": ([P, P], I32),
+            "kvev_init_state": ([P, P, P], I32),
+            "kvev_step": ([P, P, P, P, P, P, I64, P, P, P, P], I32),
+            "kvev_step_host": ([P, P, P, P, P, P, I64, P, P, P, P], I32),
+            "kvev_set_debug": ([P, P, P], I32),
+            "kvev_profile": ([P, I32], I32),
+            "kvev_profile_read": ([P, P, P], I32),
+            "kvev_launch_count": ([P, P], I32),
+            "kvev_sync": ([P, P], I32),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(f"cannot pass {type(x)} as a pointer")
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, ctx=None):
+    if status != KVEV_OK:
+        raise KvevError(status, lib().kvev_last_error(ctx).decode())
+
+
+# ------------------------------------------------------------------ C calls
+def kvev_create(layout: kvev_layout, budget: int, granularity: int, alpha: float, beta: float,
+                regions=None):
+    out = ctypes.c_void_p()
+    _check(lib().kvev_create(ctypes.byref(layout), int(budget), int(granularity), float(alpha),
+                             float(beta), _ptr(regions), ctypes.byref(out)))
+    return out
+
+
+def kvev_destroy(ctx) -> None:
+    lib().kvev_destroy(ctx)
+
+
+def kvev_last_error(ctx=None) -> str:
+    return lib().kvev_last_error(ctx).decode()
+
+
+def kvev_workspace_size(layout: kvev_layout, budget: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().kvev_workspace_size(ctypes.byref(layout), int(budget), ctypes.byref(n)))
+    return n.value
+
+
+def kvev_refresh_mode(ctx, mode: int, period: int = 1) -> None:
+    _check(lib().kvev_refresh_mode(ctx, int(mode), int(period)), ctx)
+
+
+def kvev_configure(ctx, age_mode: int, pool: int) -> None:
+    _check(lib().kvev_configure(ctx, int(age_mode), int(pool)), ctx)
+
+
+def kvev_begin(ctx, prefill_len: int) -> None:
+    _check(lib().kvev_begin(ctx, int(prefill_len)), ctx)
+
+
+def kvev_length(ctx) -> int:
+    n = ctypes.c_int32()
+    _check(lib().kvev_length(ctx, ctypes.byref(n)), ctx)
+    return n.value
+
+
+def kvev_init_state(ctx, state: kvev_state, stream=None) -> None:
+    _check(lib().kvev_init_state(ctx, ctypes.byref(state), _stream(stream)), ctx)
+
+
+def kvev_step(ctx, q, k_new, v_new, cache: kvev_cache, state: kvev_state, step: int, out,
+              retained_idx, n_retained, stream=None) -> None:
+    _check(lib().kvev_step(ctx, _ptr(q), _ptr(k_new), _ptr(v_new), ctypes.byref(cache),
+                           ctypes.byref(state), int(step), _ptr(out), _ptr(retained_idx),
+                           _ptr(n_retained), _stream(stream)), ctx)
+
+
+def kvev_step_host(ctx, q, k_new, v_new, cache: kvev_cache, state: kvev_state, step: int, out,
+                   retained_idx, n_retained, stream=None) -> None:
+    _check(lib().kvev_step_host(ctx, _ptr(q), _ptr(k_new), _ptr(v_new), ctypes.byref(cache),
+                                ctypes.byref(state), int(step), _ptr(out), _ptr(retained_idx),
+                                _ptr(n_retained), _stream(stream)), ctx)
+
+
+def kvev_set_debug(ctx, probs=None, priority=None) -> None:
+    _check(lib().kvev_set_debug(ctx, _ptr(probs), _ptr(priority)), ctx)
+
+
+def kvev_profile(ctx, enable: bool) -> None:
+    _check(lib().kvev_profile(ctx, int(bool(enable))), ctx)
+
+
+def kvev_profile_read(ctx):
+    ms = (ctypes.c_float * KVEV_PROFILE_SLOTS)()
+    n = (ctypes.c_int64 * KVEV_PROFILE_SLOTS)()
+    _check(lib().kvev_profile_read(ctx, ms, n), ctx)
+    return {PROFILE_NAMES[i]: (ms[i], n[i]) for i in range(KVEV_PROFILE_SLOTS) if n[i]}
+
+
+def kvev_launch_count(ctx) -> int:
+    n = ctypes.c_int64()
+    _check(lib().kvev_launch_count(ctx, ctypes.byref(n)), ctx)
+    return n.value
+
+
+def kvev_sync(ctx, stream=None) -> None:
+    _check(lib().kvev_sync(ctx, _stream(stream)), ctx)
+
+
+# ------------------------------------------------------------- buffer owner
+class EvictionPass:
+    """Device buffers plus a context for one decode run (token granularity).
+
+    Cache buffers: k[2], v[2] each [Ly][b][Hkv][max_ctx][d] bf16; state arrays
+    [b][max_ctx]; outputs out [b][Ly][Hq][d] fp32, retained [b][budget] int32,
+    n_retained [b] int32.  All torch tensors on the current CUDA device."""
+
+    def __init__(self, n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, budget,
+                 alpha, beta, *, age_mode=KVEV_AGE_SINCE_INSERT, pool=KVEV_POOL_SUM,
+                 refresh=KVEV_REFRESH_FULL, period=1, device="cuda"):
+        import torch
+        self.torch = torch
+        self.layout = kvev_layout(n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, 1,
+                                  KVEV_BF16)
+        self.budget = int(budget)
+        self.ctx = kvev_create(self.layout, budget, 1, alpha, beta)
+        kvev_configure(self.ctx, age_mode, pool)
+        kvev_refresh_mode(self.ctx, refresh, period)
+        shape = (n_layers, batch, n_kv_heads, max_ctx, head_dim)
+        self.k = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self.v = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self.score = torch.zeros((batch, max_ctx), dtype=torch.float32, device=device)
+        self.t_ins = torch.zeros((batch, max_ctx), dtype=torch.int32, device=device)
+        self.t_ref = torch.zeros((batch, max_ctx), dtype=torch.int32, device=device)
+        self.pos = torch.zeros((batch, max_ctx), dtype=torch.int32, device=device)
+        self.out = torch.zeros((batch, n_layers, n_q_heads, head_dim), dtype=torch.float32,
+                               device=device)
+        self.retained = torch.zeros((batch, self.budget), dtype=torch.int32, device=device)
+        self.n_retained = torch.zeros((batch,), dtype=torch.int32, device=device)
+        self.cache = kvev_cache((ctypes.c_void_p * 2)(self.k[0].data_ptr(), self.k[1].data_ptr()),
+                                (ctypes.c_void_p * 2)(self.v[0].data_ptr(), self.v[1].data_ptr()),
+                                0)
+        self.state = kvev_state(self.score.data_ptr(), self.t_ins.data_ptr(),
+                                self.t_ref.data_ptr(), self.pos.data_ptr())
+        self.step_no = 0
+
+    @property
+    def cur(self) -> int:
+        return self.cache.cur
+
+    def live_k(self):
+        return self.k[self.cache.cur]
+
+    def live_v(self):
+        return self.v[self.cache.cur]
+
+    def begin(self, prefill_len: int, stream=None, cur: int = 0):
+        """Start a run over the prefill already written into buffer ``cur``."""
+        self.cache.cur = cur
+        kvev_begin(self.ctx, prefill_len)
+        kvev_init_state(self.ctx, self.state, stream)
+        self.step_no = 0
+
+    def length(self) -> int:
+        return kvev_length(self.ctx)
+
+    def step(self, q, k_new, v_new, stream=None):
+        self.step_no += 1
+        kvev_step(self.ctx, q, k_new, v_new, self.cache, self.state, self.step_no, self.out,
+                  self.retained, self.n_retained, stream)
+        return self.out, self.retained, self.n_retained
+
+    def close(self):
+        if self.ctx is not None:
+            kvev_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,209 @@
+/*
+ * kvev.h -- C ABI of the GB300 decode-time KV-cache eviction pass.
+ *
+ * One call, kvev_step, runs the whole per-decode-step pass on one CUDA
+ * stream:
+ *   1. append the new token's K/V in every layer and KV head;
+ *   2. single-query GQA attention over the live cache, every layer at once,
+ *      producing the attention output and the per-token probabilities
+ *      ("What Matters for Aggressive Decoding-Time KV Eviction?", Sec. 3.1
+ *      Eq. (1) and Appendix E "Per-step scoring");
+ *   3. head pooling of those probabilities and the EMA fold of the per-token
+ *      state, layer by layer in ascending order, kept across steps
+ *      (kv-cache-docs figure "ema-eviction", EMA table; the same paper's
+ *      Appendix E "Layer scoring");
+ *   4. the eviction priority (1 - score) * (1 - exp(-beta * age))
+ *      ("ema-eviction" figure, priority and decision matrix);
+ *   5. selection of the B lowest-priority tokens, ties to the lower slot
+ *      index, whenever the cache exceeds the budget (Sec. 3.1: evict the
+ *      lowest-utility tokens whenever |cache| > B);
+ *   6. stable compaction of the retained K/V rows and per-token state.
+ * Lazy refresh and Score-Free (Sec. 3.2, Eq. (6)) skip steps 2's
+ * probability capture and 3 on non-refresh steps.
+ *
+ * Conventions, for every entry point:
+ *   - Device pointers are CUDA device memory of the current device, owned by
+ *     the caller, contiguous, in the layouts stated; host pointers are said
+ *     to be host pointers.  The context owns only its own scratch.
+ *   - Every call returns a kvev_status.  Argument errors are reported before
+ *     anything is launched and leave every buffer untouched.  A CUDA error
+ *     raised by a launch, or an asynchronous fault of an earlier launch,
+ *     returns KVEV_ECUDA; after that the cache and state are undefined.
+ *   - kvev_last_error(ctx) gives a message for the last failing call on this
+ *     thread (ctx may be NULL, e.g. after a failed kvev_create).
+ *   - Calls taking a stream enqueue work on it asynchronously (NULL = the
+ *     legacy default stream).  A context is not thread-safe: one context per
+ *     stream.
+ *   - All floating-point arithmetic on the device is fp32; K/V are bf16.
+ */
+#ifndef KVEV_H
+#define KVEV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVEV_OK = 0,
+    KVEV_EINVAL = 1,       /* bad argument (null pointer, size, range) */
+    KVEV_ENOMEM = 2,       /* device or host allocation failed */
+    KVEV_ECUDA = 3,        /* a CUDA call failed or an earlier launch faulted */
+    KVEV_ESTATE = 4,       /* call out of order (step numbering, begin missing) */
+    KVEV_ETIMEOUT = 5,     /* a bounded device wait gave up */
+    KVEV_EUNSUPPORTED = 6  /* valid but not implemented for this layout */
+} kvev_status;
+
+typedef enum {
+    KVEV_REFRESH_FULL = 0,    /* score every step */
+    KVEV_REFRESH_LAZY = 1,    /* score at steps t with (t - 1) mod period == 0 */
+    KVEV_REFRESH_FROZEN = 2   /* Score-Free: score at step 1 only */
+} kvev_refresh;
+
+typedef enum {
+    KVEV_AGE_SINCE_INSERT = 0, /* age = t - insertion step */
+    KVEV_AGE_SINCE_ACCESS = 1  /* age = t - last access; an access is a
+                                  refresh step on which the token's attention,
+                                  averaged over heads and layers, is at least
+                                  2/L (MemDecay Sec. III-C Eq. (3), tau scaled
+                                  to the uniform level); insertion counts */
+} kvev_age_mode;
+
+typedef enum {
+    KVEV_POOL_SUM = 0,   /* s = sum over query heads of the probabilities */
+    KVEV_POOL_MEAN = 1   /* s = mean over query heads (Sec. 3.1 Eq. (1)) */
+} kvev_pool;
+
+enum { KVEV_BF16 = 0 };
+
+typedef struct {
+    int32_t n_layers;     /* Ly */
+    int32_t n_q_heads;    /* Hq; a multiple of n_kv_heads */
+    int32_t n_kv_heads;   /* Hkv; query head h reads KV head h / (Hq/Hkv) */
+    int32_t head_dim;     /* d: 64 or 128 */
+    int32_t batch;        /* b: independent sequences */
+    int32_t max_ctx;      /* slots per (layer, sequence, KV head) */
+    int32_t page_tokens;  /* 1 = token-granular eviction */
+    int32_t kv_dtype;     /* KVEV_BF16 */
+} kvev_layout;
+
+/* The KV cache: two ping-pong buffers.  Each of k[0], k[1], v[0], v[1] is
+ * [n_layers][batch][n_kv_heads][max_ctx][head_dim] bf16, 16-byte aligned.
+ * Slots [0, len) of buffer `cur` are live.  kvev_step reads buffer `cur`,
+ * appends into it, and when it evicts writes the compacted cache into the
+ * other buffer and flips `cur`. */
+typedef struct {
+    void* k[2];
+    void* v[2];
+    int32_t cur;
+} kvev_cache;
+
+/* Per-token state, each [batch][max_ctx], slot-aligned with the cache. */
+typedef struct {
+    float* score;    /* EMA state m (fp32) */
+    int32_t* t_ins;  /* step at which the token was inserted (prefill: 0) */
+    int32_t* t_ref;  /* step of the token's last access (prefill: 0) */
+    int32_t* pos;    /* logical position of the token in its sequence */
+} kvev_state;
+
+typedef struct kvev_ctx kvev_ctx;
+
+/* Create a context for `layout` with a budget of `budget` retained tokens
+ * per sequence (1 <= budget < max_ctx).  `granularity` must equal
+ * layout->page_tokens (1).  `alpha` in (0, 1] weights the new observation in
+ * the EMA; `beta` >= 0 is the recency coefficient (+INFINITY allowed: rank by
+ * score, newest token protected).  `regions` must be NULL (no region table
+ * for token-granular eviction).  Allocates the context's device scratch on
+ * the current device (kvev_workspace_size bytes).  Defaults: full refresh,
+ * age since insertion, head-sum pooling. */
+kvev_status kvev_create(const kvev_layout* layout, int64_t budget, int32_t granularity,
+                        float alpha, float beta, const void* regions, kvev_ctx** out);
+
+/* Release the context and its scratch.  NULL is a no-op. */
+void kvev_destroy(kvev_ctx* ctx);
+
+/* Message for the last failing call on this thread (never NULL). */
+const char* kvev_last_error(const kvev_ctx* ctx);
+
+/* Device scratch bytes that kvev_create allocates for this layout. */
+kvev_status kvev_workspace_size(const kvev_layout* layout, int64_t budget, size_t* bytes);
+
+/* Refresh schedule (Sec. 3.2): KVEV_REFRESH_FULL, KVEV_REFRESH_LAZY with
+ * `period` >= 1, or KVEV_REFRESH_FROZEN.  Takes effect from the next step. */
+kvev_status kvev_refresh_mode(kvev_ctx* ctx, int32_t mode, int32_t period);
+
+/* Age definition (kvev_age_mode) and head pooling (kvev_pool). */
+kvev_status kvev_configure(kvev_ctx* ctx, int32_t age_mode, int32_t pool);
+
+/* Start a decode run: every sequence holds `prefill_len` live tokens
+ * (0 <= prefill_len < max_ctx) and the next step is step 1. */
+kvev_status kvev_begin(kvev_ctx* ctx, int32_t prefill_len);
+
+/* Live tokens per sequence after the last step (or kvev_begin). */
+kvev_status kvev_length(const kvev_ctx* ctx, int32_t* len);
+
+/* Write the prefill state on `stream`: for every sequence and slot i below
+ * the prefill length, score = 0, t_ins = t_ref = 0, pos = i (Appendix E
+ * "Momentum initialization": m0 = 0). */
+kvev_status kvev_init_state(kvev_ctx* ctx, const kvev_state* state, void* stream);
+
+/* One decode step `step` (must be the previous step + 1; the first step
+ * after kvev_begin is 1).  Device inputs:
+ *   q      [batch][n_layers][n_q_heads][head_dim] bf16
+ *   k_new  [batch][n_layers][n_kv_heads][head_dim] bf16
+ *   v_new  [batch][n_layers][n_kv_heads][head_dim] bf16
+ * Device outputs:
+ *   out           [batch][n_layers][n_q_heads][head_dim] fp32 attention
+ *                 output of this step (over the cache including the new token)
+ *   retained_idx  [batch][budget] int32: the retained slots of the cache as it
+ *                 was after the append, ascending; after the call retained
+ *                 slot retained_idx[b][j] lives at slot j.  When the cache
+ *                 does not exceed the budget nothing is evicted and the list
+ *                 is 0..len-1.
+ *   n_retained    [batch] int32: entries written to retained_idx.
+ * `cache` and `state` are read and updated (cache->cur may flip). */
+kvev_status kvev_step(kvev_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                      kvev_cache* cache, const kvev_state* state, int64_t step, float* out,
+                      int32_t* retained_idx, int32_t* n_retained, void* stream);
+
+/* kvev_step with the per-step inputs and outputs in HOST memory (pinned
+ * memory gives asynchronous copies; pageable memory works too): copies
+ * q/k_new/v_new to the context's device staging, runs the step, copies
+ * out/retained_idx/n_retained back and synchronizes `stream` before
+ * returning.  Same layouts as kvev_step; the cache and state stay on the
+ * device. */
+kvev_status kvev_step_host(kvev_ctx* ctx, const void* q_host, const void* k_new_host,
+                           const void* v_new_host, kvev_cache* cache, const kvev_state* state,
+                           int64_t step, float* out_host, int32_t* retained_idx_host,
+                           int32_t* n_retained_host, void* stream);
+
+/* Optional diagnostic outputs written by later steps (NULL disables):
+ *   probs     [batch][n_layers][n_q_heads][max_ctx] fp32, the attention
+ *             probabilities of refresh steps over slots [0, L) of the cache
+ *             after the append;
+ *   priority  [batch][max_ctx] fp32, every step's eviction priority of slots
+ *             [0, L), before compaction.
+ * The pointers must stay valid while set. */
+kvev_status kvev_set_debug(kvev_ctx* ctx, float* probs, float* priority);
+
+/* Per-kernel timing with CUDA events on the step's stream.  Enable, run
+ * steps, then kvev_profile_read fills `ms[i]` (accumulated milliseconds) and
+ * `launches[i]` for kernel i in the order append, attention, combine, score,
+ * select, compact (KVEV_PROFILE_SLOTS entries each; pass NULL to skip) and
+ * resets the accumulators.  kvev_profile_read synchronizes. */
+enum { KVEV_PROFILE_SLOTS = 8 };
+kvev_status kvev_profile(kvev_ctx* ctx, int32_t enable);
+kvev_status kvev_profile_read(kvev_ctx* ctx, float* ms, int64_t* launches);
+
+/* Total kernel launches this context has made (all entry points). */
+kvev_status kvev_launch_count(const kvev_ctx* ctx, int64_t* launches);
+
+/* Block until `stream`'s work is done; returns KVEV_ECUDA on a device fault. */
+kvev_status kvev_sync(kvev_ctx* ctx, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVEV_H */

@@ -1,0 +1,86 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every entry point that include/kvev.h declares, and rejects
+bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from decoding_kv_cache_split_gb300 import build as kbuild
+from decoding_kv_cache_split_gb300 import kvev
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kvev.lib()
+
+
+def declared_entry_points():
+    text = open(os.path.join(ROOT, "include", "kvev.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvev_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_what_the_binding_wraps():
+    assert declared_entry_points() == sorted(kvev.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_entry_points():
+        assert hasattr(lib, name), name
+
+
+def layout(**kw):
+    base = dict(n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128, batch=1, max_ctx=64,
+                page_tokens=1, kv_dtype=0)
+    base.update(kw)
+    return kvev.kvev_layout(*[base[f] for f, _ in kvev.kvev_layout._fields_])
+
+
+@pytest.mark.parametrize("kw,budget,status", [
+    (dict(head_dim=96), 8, kvev.KVEV_EUNSUPPORTED),
+    (dict(n_q_heads=7), 8, kvev.KVEV_EINVAL),
+    (dict(n_q_heads=16), 8, kvev.KVEV_EUNSUPPORTED),
+    (dict(batch=0), 8, kvev.KVEV_EINVAL),
+    (dict(page_tokens=16), 8, kvev.KVEV_EUNSUPPORTED),
+    ({}, 0, kvev.KVEV_EINVAL),
+    ({}, 64, kvev.KVEV_EINVAL),
+])
+def test_create_rejects_bad_layouts(lib, kw, budget, status):
+    out = ctypes.c_void_p()
+    lay = layout(**kw)
+    rc = lib.kvev_create(ctypes.byref(lay), budget, 1, 0.05, 0.001, None, ctypes.byref(out))
+    assert rc == status
+    assert out.value is None
+    assert kvev.kvev_last_error()
+
+
+def test_create_rejects_bad_scalars(lib):
+    out = ctypes.c_void_p()
+    lay = layout()
+    assert lib.kvev_create(ctypes.byref(lay), 8, 1, 0.0, 0.001, None, ctypes.byref(out)) == kvev.KVEV_EINVAL
+    assert lib.kvev_create(ctypes.byref(lay), 8, 1, 1.5, 0.001, None, ctypes.byref(out)) == kvev.KVEV_EINVAL
+    assert lib.kvev_create(ctypes.byref(lay), 8, 1, 0.05, -1.0, None, ctypes.byref(out)) == kvev.KVEV_EINVAL
+    assert lib.kvev_create(ctypes.byref(lay), 8, 2, 0.05, 0.001, None, ctypes.byref(out)) == kvev.KVEV_EINVAL
+    assert lib.kvev_create(None, 8, 1, 0.05, 0.001, None, ctypes.byref(out)) == kvev.KVEV_EINVAL
+    assert lib.kvev_create(ctypes.byref(lay), 8, 1, 0.05, 0.001, None, None) == kvev.KVEV_EINVAL
+
+
+def test_null_context_is_rejected(lib):
+    assert lib.kvev_refresh_mode(None, 0, 1) == kvev.KVEV_EINVAL
+    assert lib.kvev_configure(None, 0, 0) == kvev.KVEV_EINVAL
+    assert lib.kvev_begin(None, 0) == kvev.KVEV_EINVAL
+    assert lib.kvev_step(None, None, None, None, None, None, 1, None, None, None, None) == kvev.KVEV_EINVAL
+    assert lib.kvev_sync(None, None) == kvev.KVEV_EINVAL
+    lib.kvev_destroy(None)   # no-op
+
+
+def test_binding_raises_with_message(lib):
+    with pytest.raises(kvev.KvevError) as ei:
+        kvev.kvev_create(layout(head_dim=80), 8, 1, 0.05, 0.001)
+    assert ei.value.status == kvev.KVEV_EUNSUPPORTED
+    assert "head_dim" in str(ei.value)

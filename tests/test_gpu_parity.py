@@ -1,0 +1,142 @@
+"""GPU parity of the eviction pass against the fp64 oracle.
+
+Every test runs the CUDA path through the C ABI (Python binding) and, at
+each step, the oracle from the device's own pre-step state (teacher
+forcing), and compares element by element (tolerances in tests/parity.py).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+from workloads import Geometry, Workload, llama8b_workload, tiny_workload
+
+from parity import (access_alternative, compare_step, load_prefill, oracle_step, snapshot,
+                    to_dev_bf16)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from decoding_kv_cache_split_gb300 import kvev  # noqa: E402
+
+AGE_NAMES = {O.AGE_SINCE_INSERT: kvev.KVEV_AGE_SINCE_INSERT,
+             O.AGE_SINCE_ACCESS: kvev.KVEV_AGE_SINCE_ACCESS}
+REFRESH = {"full": (O.REFRESH_FULL, kvev.KVEV_REFRESH_FULL),
+           "lazy": (O.REFRESH_LAZY, kvev.KVEV_REFRESH_LAZY),
+           "frozen": (O.REFRESH_FROZEN, kvev.KVEV_REFRESH_FROZEN)}
+
+
+def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int, *,
+               age_mode=O.AGE_SINCE_INSERT, refresh="full", period=8, pool_mean=False,
+               max_ctx=None, check_every=1):
+    g = wl.geom
+    max_ctx = max_ctx or max(wl.L0 + steps + 1, budget + 1)
+    mode_o, mode_d = REFRESH[refresh]
+    ep = kvev.EvictionPass(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, g.batch, max_ctx,
+                           budget, alpha, beta, age_mode=AGE_NAMES[age_mode],
+                           pool=kvev.KVEV_POOL_MEAN if pool_mean else kvev.KVEV_POOL_SUM,
+                           refresh=mode_d, period=period)
+    load_prefill(ep, wl)
+    ep.begin(wl.L0)
+    probs = torch.zeros((g.batch, g.n_layers, g.n_q_heads, max_ctx), dtype=torch.float32,
+                        device="cuda")
+    prio = torch.zeros((g.batch, max_ctx), dtype=torch.float32, device="cuda")
+    kvev.kvev_set_debug(ep.ctx, probs, prio)
+    P = O.OracleParams(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, budget, alpha, beta,
+                       age_mode, pool_mean)
+    totals = {"swaps": 0, "out_rel": 0.0, "m_abs": 0.0, "p_rel": 0.0, "steps": 0}
+    for t in range(1, steps + 1):
+        L_prev = ep.length()
+        check = (t - 1) % check_every == 0 or t == steps
+        pres = [snapshot(ep, b, L_prev) for b in range(g.batch)] if check else None
+        q, kn, vn = wl.step_inputs(t)
+        ep.step(to_dev_bf16(q), to_dev_bf16(kn), to_dev_bf16(vn))
+        kvev.kvev_sync(ep.ctx)
+        if not check:
+            continue
+        refresh_now = O.is_refresh(mode_o, period, t)
+        for b in range(g.batch):
+            res, _ = oracle_step(P, pres[b], t, refresh_now, q[b], kn[b], vn[b], wl.L0 + t - 1)
+            alt = access_alternative(res, pres[b], P) if (
+                refresh_now and age_mode == O.AGE_SINCE_ACCESS) else None
+            st = compare_step(res, ep, b, pres[b], budget, probs, prio, refresh_now, alt)
+            totals["swaps"] += st["swaps"]
+            for k in ("out_rel", "m_abs", "p_rel"):
+                totals[k] = max(totals[k], st.get(k, 0.0))
+            totals["steps"] += 1
+        assert ep.length() == min(L_prev + 1, budget)
+    ep.close()
+    return totals
+
+
+def test_tiny_token_eviction_64_steps():
+    """1 layer, 8 q / 2 KV heads, d 64, 512-token prefill with 8 heavy
+    hitters, alpha 0.05, beta 0.001, budget 128, 64 full-refresh steps."""
+    tot = run_parity(tiny_workload(0), 128, 0.05, 0.001, 64)
+    print("tiny:", tot)
+    assert tot["steps"] == 64
+
+
+@pytest.mark.parametrize("refresh", ["full", "lazy", "frozen"])
+@pytest.mark.parametrize("alpha", [0.01, 0.05, 0.15])
+def test_llama_geometry_modes(refresh, alpha):
+    """Llama-3.1-8B head geometry (32 q / 8 KV, d 128), 3 layers, 1000-token
+    prefill (ragged last tile), 10% budget, access-clock ages, 12 steps in
+    every refresh mode (lazy period 4 so non-refresh steps occur)."""
+    wl = llama8b_workload(0, prefill_len=1000, n_layers=3, needle_period=5)
+    tot = run_parity(wl, 100, alpha, 0.001, 12, age_mode=O.AGE_SINCE_ACCESS, refresh=refresh,
+                     period=4)
+    print(refresh, alpha, tot)
+
+
+def test_batch_and_ragged_lengths():
+    """Four sequences, prefill 47 (not a tile multiple), budget 20."""
+    wl = Workload(Geometry(2, 8, 2, 128, 4), 47, seed=3, outliers=4, heavy=3)
+    run_parity(wl, 20, 0.05, 0.001, 6)
+
+
+@pytest.mark.parametrize("L0,budget", [(1, 1), (15, 8), (16, 8), (17, 16), (33, 40)])
+def test_edge_lengths(L0, budget):
+    """Tiny caches around the 16-token tile: single token, exact tile, one
+    past a tile, and a budget larger than the cache (no eviction)."""
+    wl = Workload(Geometry(2, 4, 1, 64, 1), L0, seed=L0, heavy=1)
+    run_parity(wl, budget, 0.05, 0.001, 4)
+
+
+def test_beta_infinite_and_head_mean():
+    """beta = +inf (rank by score, newest token protected) with head-mean
+    pooling (Sec. 3.1 Eq. (1))."""
+    wl = Workload(Geometry(2, 8, 2, 64, 1), 300, seed=11, heavy=4)
+    run_parity(wl, 64, 0.2, math.inf, 5, pool_mean=True)
+
+
+def test_probabilities_sum_to_one():
+    """Device probabilities of every (layer, head) sum to 1 (fp32)."""
+    wl = Workload(Geometry(2, 8, 2, 128, 1), 777, seed=5, outliers=4)
+    g = wl.geom
+    ep = kvev.EvictionPass(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, 1, 800, 100, 0.05,
+                           0.001)
+    load_prefill(ep, wl)
+    ep.begin(wl.L0)
+    probs = torch.zeros((1, g.n_layers, g.n_q_heads, 800), device="cuda")
+    kvev.kvev_set_debug(ep.ctx, probs, None)
+    q, kn, vn = wl.step_inputs(1)
+    ep.step(to_dev_bf16(q), to_dev_bf16(kn), to_dev_bf16(vn))
+    kvev.kvev_sync(ep.ctx)
+    s = probs[0, :, :, :778].sum(-1).cpu().numpy()
+    assert np.allclose(s, 1.0, atol=1e-5)
+    ep.close()
+
+
+@pytest.mark.slow
+def test_llama8b_32k_step1_full_size():
+    """The full Llama-3.1-8B-shaped pass: 32 layers, 32 q / 8 KV heads, d 128,
+    32768-token prefill + 1, budget 3277, alpha 0.05, beta 0.001, access
+    clock; steps 1 and 2 against the oracle, element by element."""
+    wl = llama8b_workload(0, prefill_len=32768)
+    tot = run_parity(wl, 3277, 0.05, 0.001, 2, age_mode=O.AGE_SINCE_ACCESS, max_ctx=32768 + 64)
+    print("llama8b 32k:", tot)
