@@ -143,9 +143,13 @@ def cpu_baseline(wl, n_layers_sample: int):
     """The fp64 oracle (single thread) on the first `n_layers_sample` layers
     of the same step; returns (GB/s, seconds, sample description)."""
     import oracle as O
-    K, V = wl.prefill()
     L0, W = wl.L0, WORKLOAD
-    st = O.SequenceState.from_prefill(K[:n_layers_sample, 0], V[:n_layers_sample, 0], L0, L0 + 2)
+    kv = [wl.prefill_layer(layer) for layer in range(n_layers_sample)]
+    K = np.stack([k[0] for k, _ in kv])          # [layers][Hkv][L0][d] of sequence 0
+    V = np.stack([v[0] for _, v in kv])
+    del kv
+    st = O.SequenceState.from_prefill(K, V, L0, L0 + 2)
+    del K, V
     q, kn, vn = wl.step_inputs(1)
     P = O.OracleParams(n_layers_sample, W["n_q_heads"], W["n_kv_heads"], W["head_dim"],
                        W["budget"], W["alpha"], W["beta"], O.AGE_SINCE_ACCESS)

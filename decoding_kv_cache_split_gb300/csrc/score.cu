@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
                 const float sp = a.pool_mean ? s * inv_hq : s;
                 m = fmaf(a.alpha, sp, oma * m);
             }
-            if (a.age_mode == KVEV_AGE_SINCE_ACCESS && tot >= a.access_thr) t_ref = a.t;
+            if (tot >= a.access_thr) t_ref = a.t;   // the clock runs in every age mode
         } else if (!is_new) {
             old_m = m;
         }

@@ -89,7 +89,8 @@ def boundary_check(pr_ref: np.ndarray, kept_dev: np.ndarray, budget: int, tol: f
 
 
 def compare_step(res, ep, b: int, pre: O.SequenceState, budget: int, dbg_probs=None,
-                 dbg_prio=None, refresh: bool = True, pr_alt=None, m_atol: float = M_ATOL):
+                 dbg_prio=None, refresh: bool = True, pr_alt=None, m_atol: float = M_ATOL,
+                 access_amb=None):
     """Compare one device step of sequence b with the oracle result `res`
     computed from the same pre-step state.  Returns a dict of counters."""
     import torch
@@ -127,9 +128,9 @@ def compare_step(res, ep, b: int, pre: O.SequenceState, budget: int, dbg_probs=N
     assert np.array_equal(ep.t_ins[b, :n].cpu().numpy(), tins_full[kept]), "compacted t_ins"
     tref_dev = ep.t_ref[b, :n].cpu().numpy()
     tref_ok = tref_dev == res["t_ref_upd"][kept]
-    if pr_alt is not None:
-        tref_ok |= pr_alt[kept] != res["priority"][kept]
-    assert tref_ok.all(), "compacted t_ref"
+    if access_amb is not None:
+        tref_ok |= access_amb[kept]
+    assert tref_ok.all(), f"compacted t_ref: {(~tref_ok).sum()} differ"
     # K/V after compaction: the device's pre-step rows (plus the appended row)
     # at the device's retained indices, bit for bit
     Kd = ep.live_k()[:, b, :, :n].view(torch.int16).cpu().numpy().view(np.uint16)
@@ -152,17 +153,17 @@ def oracle_step(P, pre: O.SequenceState, t: int, refresh: bool, q, kn, vn, new_p
 
 
 def access_alternative(res, pre: O.SequenceState, P, rel: float = 1e-4):
-    """Priorities under the other access decision for slots whose head- and
-    layer-averaged attention is within `rel` of the 2/L threshold (fp32 on
-    the device and fp64 here may decide either way); None if there are none.
-    Other slots keep their oracle priority."""
+    """Slots whose head- and layer-averaged attention is within `rel` of the
+    2/L threshold, where fp32 on the device and fp64 here may decide the
+    access either way.  Returns (priorities under the other decision, or None
+    when the age does not depend on it or no slot is ambiguous; the mask)."""
     L = res["L"]
     mean_attn = res["score_sum"] / (P.n_layers * P.n_q_heads)
     thr = 2.0 / L
     amb = np.abs(mean_attn - thr) <= rel * thr
     amb[L - 1] = False                       # the new token is accessed by insertion
-    if not amb.any():
-        return None
+    if not amb.any() or P.age_mode != O.AGE_SINCE_ACCESS:
+        return None, amb
     alt = res["priority"].copy()
     t = res["t"]
     for i in np.nonzero(amb)[0]:
@@ -171,4 +172,4 @@ def access_alternative(res, pre: O.SequenceState, P, rel: float = 1e-4):
         else:
             age = 0                          # clock reset this step
         alt[i] = O.priority(res["m_upd"][i], age, P.beta)
-    return alt
+    return alt, amb

@@ -61,9 +61,9 @@ def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int,
         refresh_now = O.is_refresh(mode_o, period, t)
         for b in range(g.batch):
             res, _ = oracle_step(P, pres[b], t, refresh_now, q[b], kn[b], vn[b], wl.L0 + t - 1)
-            alt = access_alternative(res, pres[b], P) if (
-                refresh_now and age_mode == O.AGE_SINCE_ACCESS) else None
-            st = compare_step(res, ep, b, pres[b], budget, probs, prio, refresh_now, alt)
+            alt, amb = access_alternative(res, pres[b], P) if refresh_now else (None, None)
+            st = compare_step(res, ep, b, pres[b], budget, probs, prio, refresh_now, alt,
+                              access_amb=amb)
             totals["swaps"] += st["swaps"]
             for k in ("out_rel", "m_abs", "p_rel"):
                 totals[k] = max(totals[k], st.get(k, 0.0))
