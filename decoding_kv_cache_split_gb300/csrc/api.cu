@@ -124,6 +124,12 @@ int64_t attn_grid_for_device(int num_sms, const kvev_layout& L) {
 
 }  // namespace
 
+namespace kvev {
+// Lets other translation units of the library set the message that
+// kvev_last_error returns.
+kvev_status report_error(kvev_status st, const char* msg) { return fail(st, "%s", msg); }
+}  // namespace kvev
+
 struct kvev_ctx {
     kvev_layout lay{};
     int64_t budget = 0;

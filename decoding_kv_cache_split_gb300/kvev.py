@@ -32,7 +32,8 @@ PROFILE_NAMES = ["append", "attention", "combine", "score", "select", "compact",
 EXPORTS = ["kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_size",
            "kvev_refresh_mode", "kvev_configure", "kvev_begin", "kvev_length",
            "kvev_init_state", "kvev_step", "kvev_step_host", "kvev_set_debug",
-           "kvev_profile", "kvev_profile_read", "kvev_launch_count", "kvev_sync"]
+           "kvev_profile", "kvev_profile_read", "kvev_launch_count", "kvev_sync",
+           "kvev_attend_noalloc"]
 
 
 class KvevError(RuntimeError):
@@ -87,6 +88,7 @@ def lib():
             "kvev_profile_read": ([P, P, P], I32),
             "kvev_launch_count": ([P, P], I32),
             "kvev_sync": ([P, P], I32),
+            "kvev_attend_noalloc": ([P, P, P, P, I32, P, P, P], I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -204,6 +206,12 @@ def kvev_launch_count(ctx) -> int:
 
 def kvev_sync(ctx, stream=None) -> None:
     _check(lib().kvev_sync(ctx, _stream(stream)), ctx)
+
+
+def kvev_attend_noalloc(layout: kvev_layout, q, k, v, length: int, out, lse2, stream=None) -> None:
+    """Attention of the pass with no allocation (see include/kvev.h)."""
+    _check(lib().kvev_attend_noalloc(ctypes.byref(layout), _ptr(q), _ptr(k), _ptr(v), int(length),
+                                     _ptr(out), _ptr(lse2), _stream(stream)))
 
 
 # ------------------------------------------------------------- buffer owner

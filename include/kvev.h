@@ -203,6 +203,32 @@ kvev_status kvev_launch_count(const kvev_ctx* ctx, int64_t* launches);
 /* Block until `stream`'s work is done; returns KVEV_ECUDA on a device fault. */
 kvev_status kvev_sync(kvev_ctx* ctx, void* stream);
 
+/* Attention of the pass without allocating: no counterpart on the pages;
+ * it exists for callers that cannot call cudaMalloc (engines whose allocator
+ * owns all device memory, latency-critical paths that cannot take the
+ * implicit synchronisation of cudaMalloc/cudaFree).  Runs the split-K
+ * attention and split combine of kvev_step, with no context, keeping the
+ * split partials in a 16 MiB array in device memory that belongs to the
+ * library image (every GPU that loads the library holds it until exit).
+ *   q      [batch][n_layers][n_q_heads][head_dim] bf16 (device)
+ *   k, v   ONE cache buffer, [n_layers][batch][n_kv_heads][max_ctx][head_dim]
+ *          bf16 (device); slots [0, len) are attended, 1 <= len <= max_ctx
+ *   out    [batch][n_layers][n_q_heads][head_dim] fp32 (device)
+ *   lse2   [n_layers][batch][n_q_heads] fp32 (device): log2 of the softmax
+ *          normaliser, i.e. ln(sum_i exp(q.k_i/sqrt(d))) / ln 2
+ * Limits: head_dim 64 or 128, 4 query heads per KV head, and
+ * n_layers*batch*n_kv_heads at most floor((16 MiB - 256) / (16 (head_dim +
+ * 2))) - 4, i.e. 8061 at head_dim 128 and 15883 at 64; larger layouts return
+ * KVEV_EINVAL before anything is launched.  layout->page_tokens,
+ * kv_dtype are ignored (bf16 tokens).  The first call on a device looks up
+ * the array's address (make it before any stream capture).  All calls share
+ * the array: calls that overlap on the GPU race; order them on one stream.
+ * Asynchronous on `stream`; a device wait that gives up leaves `out`
+ * undefined and is not reported by this call. */
+kvev_status kvev_attend_noalloc(const kvev_layout* layout, const void* q, const void* k,
+                                const void* v, int32_t len, float* out, float* lse2,
+                                void* stream);
+
 #ifdef __cplusplus
 }
 #endif
