@@ -213,6 +213,9 @@ def main():
     ap.add_argument("--impl", default="kvev", choices=["kvev", "reference"])
     ap.add_argument("--cpu-layers", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=WORKLOAD["n_layers"],
+                    help="smaller cases for profiling; the headline uses 32")
+    ap.add_argument("--prefill", type=int, default=WORKLOAD["prefill"])
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -239,10 +242,14 @@ def main():
     from decoding_kv_cache_split_gb300 import kvev
     from workloads import llama8b_workload
 
-    W = WORKLOAD
+    W = dict(WORKLOAD)
+    if args.layers != W["n_layers"] or args.prefill != W["prefill"]:
+        W.update(workload=f"profiling case: {args.layers} layers, {args.prefill}-token prefill",
+                 n_layers=args.layers, prefill=args.prefill,
+                 budget=-(-args.prefill // 10))
     L0, B = W["prefill"], W["budget"]
     max_ctx = L0 + 64
-    wl = llama8b_workload(0, prefill_len=L0)
+    wl = llama8b_workload(0, prefill_len=L0, n_layers=W["n_layers"])
     ep = kvev.EvictionPass(W["n_layers"], W["n_q_heads"], W["n_kv_heads"], W["head_dim"],
                            W["batch"], max_ctx, B, W["alpha"], W["beta"],
                            age_mode=kvev.KVEV_AGE_SINCE_ACCESS)
@@ -339,7 +346,7 @@ def main():
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            val, secs, sample = cpu_baseline(wl, args.cpu_layers)
+            val, secs, sample = cpu_baseline(wl, min(args.cpu_layers, W["n_layers"]))
             cpu = {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                    "sample": sample, "seconds": round(secs, 2)}
         line = {
