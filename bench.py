@@ -270,8 +270,9 @@ def main():
     kvev.kvev_sync(ep.ctx)
 
     # ---------------------------------------------------------- device timing
-    kvev.kvev_profile(ep.ctx, True)
-    kvev.kvev_profile_read(ep.ctx)          # reset accumulators
+    # Headline region: the pass back to back, no per-kernel events (an event
+    # between kernels would stop each kernel's launch from overlapping the
+    # previous one's tail).
     n0 = kvev.kvev_launch_count(ep.ctx)
     clocks = ClockSampler(local_rank)
     clocks.start()
@@ -288,14 +289,22 @@ def main():
         dist.barrier()
     clk = clocks.stop()
     kvev.kvev_sync(ep.ctx)
-    prof = kvev.kvev_profile_read(ep.ctx)
-    kvev.kvev_profile(ep.ctx, False)
     launches = kvev.kvev_launch_count(ep.ctx) - n0
     ms = e0.elapsed_time(e1) / args.steps
     if dist:
         t = torch.tensor([ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
+
+    # Per-kernel region: CUDA events around every launch, on the launching stream.
+    kvev.kvev_profile(ep.ctx, True)
+    kvev.kvev_profile_read(ep.ctx)          # reset accumulators
+    n_prof = max(10, min(args.steps, 200))
+    for _ in range(n_prof):
+        one_step()
+    kvev.kvev_sync(ep.ctx)
+    prof = kvev.kvev_profile_read(ep.ctx)
+    kvev.kvev_profile(ep.ctx, False)
     nbytes, attn_bytes = kv_bytes(W["n_layers"], W["n_kv_heads"], W["head_dim"], L0 + 1, B)
     value = world * nbytes / (ms * 1e-3) / 1e9
 
@@ -341,6 +350,7 @@ def main():
     tokens_layers = (L0 + 1) * W["n_layers"]
     traffic = ncu_traffic("attn.cu", tokens_layers)
     kernels_us = {k: round(v[0] / max(1, v[1]) * 1e3, 2) for k, v in prof.items()}
+    kernels_us["profiled_steps"] = n_prof
 
     line = None
     if rank == 0:

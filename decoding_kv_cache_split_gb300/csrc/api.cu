@@ -50,6 +50,7 @@ struct Workspace {
     int32_t* tins_s = nullptr;
     int32_t* pos_s = nullptr;
     float* msum_part = nullptr;
+    int32_t* row_done = nullptr;
     uint32_t* status = nullptr;
     uint16_t* stg_q = nullptr;
     uint16_t* stg_k = nullptr;
@@ -83,6 +84,7 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base)
     w.tins_s = (int32_t*)take(ctx * 4);
     w.pos_s = (int32_t*)take(ctx * 4);
     w.msum_part = (float*)take((size_t)L.batch * nblk * 4);
+    w.row_done = (int32_t*)take(rows * 4);
     w.status = (uint32_t*)take(4);
     const size_t qn = (size_t)L.batch * L.n_layers * L.n_q_heads * L.head_dim;
     const size_t kn = (size_t)L.batch * L.n_layers * L.n_kv_heads * L.head_dim;
@@ -280,7 +282,7 @@ kvev_status kvev_create(const kvev_layout* layout, int64_t budget, int32_t granu
         return fail(KVEV_ENOMEM, "cudaMalloc of %zu bytes of scratch failed", bytes);
     }
     c->ws = carve(*layout, budget, c->attn_warps + rows, c->ws_base);
-    e = cudaMemset(c->ws.status, 0, 4);
+    e = cudaMemset(c->ws_base, 0, bytes);   // row counters and status start at zero
     if (e != cudaSuccess) {
         cudaFree(c->ws_base);
         delete c;
@@ -428,25 +430,12 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     at.total_warps = c->attn_warps;
     at.write_logits = refresh ? 1 : 0;
     at.q_scale = (float)(1.4426950408889634 / sqrt((double)Ly.head_dim));
+    at.row_done = c->ws.row_done;   // the split combine runs inside the attention kernel
+    at.out = out;
+    at.lse2 = c->ws.lse2;
     rc = timed_launch(c, kProfAttn, s, "attention", [&] {
         return launch_attention(at, Ly.head_dim, G, c->attn_grid, s);
     });
-    if (rc != KVEV_OK) return rc;
-
-    CombineArgs cb{};
-    cb.part_o = c->ws.part_o;
-    cb.part_ml = c->ws.part_ml;
-    cb.out = out;
-    cb.lse2 = c->ws.lse2;
-    cb.n_tiles_total = at.n_tiles_total;
-    cb.tiles_per_row = tiles_per_row;
-    cb.total_warps = c->attn_warps;
-    cb.n_layers = Ly.n_layers;
-    cb.batch = Ly.batch;
-    cb.n_kv = Ly.n_kv_heads;
-    cb.n_q = Ly.n_q_heads;
-    rc = timed_launch(c, kProfCombine, s, "combine",
-                      [&] { return launch_combine(cb, Ly.head_dim, G, s); });
     if (rc != KVEV_OK) return rc;
 
     ScoreArgs sc{};

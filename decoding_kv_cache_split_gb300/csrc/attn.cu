@@ -26,8 +26,10 @@
 //    into the order in which each lane visits its rows and into the slot
 //    order of its query registers.
 //  * Softmax partials (running max, sum, output) of each warp's piece of a
-//    row go to a slot; the combine kernel merges them and writes the output
-//    and the per-head log2-sum-exp.
+//    row go to a slot; the last warp to finish a row (an atomic counter per
+//    row) merges the row's partials and writes the output and the per-head
+//    log2-sum-exp.  A standalone combine kernel does the same for callers
+//    without counters.
 #include <math.h>
 
 #include "kvev_internal.h"
@@ -125,6 +127,104 @@ struct AttnCfg {
     static_assert(RPL * RPW == T && NV % LPR == 0, "tile shape");
 };
 
+// Warps of the split whose tile range is empty write no partial.
+__device__ __forceinline__ bool warp_has_tiles(int64_t w, int64_t N, int64_t W) {
+    return w * N / W != (w + 1) * N / W;
+}
+
+// Called by every warp after it wrote its partial of `row`: the last of the
+// row's warps to arrive merges all of the row's partials into the output and
+// the log2-sum-exp, then resets the row's counter for the next launch.
+struct CombineView {   // what the fused combine needs, passed by value
+    const float* part_o;
+    const float* part_ml;
+    int32_t* row_done;
+    float* out;
+    float* lse2;
+    int64_t N, W;
+    int32_t tiles_per_row, n_kv, batch, n_layers, n_q;
+};
+
+template <int D, int G>
+__device__ __noinline__ void fused_combine(const CombineView a, int64_t row, int lane) {
+    constexpr int VPL = D / 32;   // output dims per lane
+    const int64_t N = a.N, W = a.W;
+    const int64_t first = row * a.tiles_per_row, last = first + a.tiles_per_row - 1;
+    const int64_t w_lo = ((first + 1) * W - 1) / N, w_hi = ((last + 1) * W - 1) / N;
+    __threadfence();   // this warp's partial is visible before it is counted
+    __syncwarp();
+    int is_last = 0;
+    if (lane == 0) {
+        int need = 0;
+        for (int64_t w = w_lo; w <= w_hi; ++w) need += warp_has_tiles(w, N, W);
+        is_last = atomicAdd(&a.row_done[row], 1) == need - 1;
+    }
+    if (!__shfl_sync(kFull, is_last, 0)) return;
+    __threadfence();
+
+    float M[G], lsum[G], acc[G][VPL];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        M[h] = -INFINITY;
+        lsum[h] = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) acc[h][v] = 0.f;
+    }
+    for (int64_t base = w_lo; base <= w_hi; base += 32) {   // segments, 32 at a time
+        const int64_t w = base + lane;
+        const bool valid = w <= w_hi && warp_has_tiles(w, N, W);
+        float mj[G], lj[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            mj[h] = valid ? __ldcg(a.part_ml + ((w + row) * G + h) * 2) : -INFINITY;
+            lj[h] = valid ? __ldcg(a.part_ml + ((w + row) * G + h) * 2 + 1) : 0.f;
+        }
+        float Mn[G], fj[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float mm = mj[h];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(kFull, mm, o));
+            Mn[h] = fmaxf(M[h], mm);
+            const float fo = M[h] == -INFINITY ? 0.f : fast_exp2(M[h] - Mn[h]);
+            lsum[h] *= fo;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) acc[h][v] *= fo;
+            M[h] = Mn[h];
+            fj[h] = valid ? fast_exp2(mj[h] - Mn[h]) : 0.f;
+            float ls = lj[h] * fj[h];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(kFull, ls, o);
+            lsum[h] += ls;
+        }
+        unsigned vm = __ballot_sync(kFull, valid);
+        while (vm) {
+            const int j = __ffs(vm) - 1;
+            vm &= vm - 1;
+            const int64_t slot = base + j + row;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float f = __shfl_sync(kFull, fj[h], j);
+                const float* src = a.part_o + (slot * G + h) * D + lane * VPL;
+#pragma unroll
+                for (int v = 0; v < VPL; ++v) acc[h][v] += __ldcg(src + v) * f;
+            }
+        }
+    }
+    const int g = (int)(row % a.n_kv);
+    const int64_t lb = row / a.n_kv;
+    const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float* dst = a.out + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)g * G + h) * D +
+                     lane * VPL;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) dst[v] = acc[h][v] / lsum[h];
+        if (lane == 0) a.lse2[row * G + h] = M[h] + log2f(lsum[h]);
+    }
+    if (lane == 0) a.row_done[row] = 0;
+}
+
 template <int D, int G, int STAGES, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
     attn_splitk_kernel(const AttnArgs a) {
@@ -133,6 +233,8 @@ __global__ void __launch_bounds__(WARPS * 32)
                   NVF = C::NVF, TB = C::TILE_BYTES;
 
     extern __shared__ __align__(128) unsigned char smem[];
+    griddep_wait();      // the append of this step is complete and visible
+    griddep_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned char* wbuf = smem + (size_t)warp * STAGES * 2 * TB;
     uint64_t* bars =
@@ -212,6 +314,12 @@ __global__ void __launch_bounds__(WARPS * 32)
         if (lane < 2) {  // lane 0 owns heads 0..NVF-1, lane 1 heads NVF..G-1
 #pragma unroll
             for (int e = 0; e < NVF; ++e) pml[(h0 + e) * 2 + 1] = l_part[e];
+        }
+        if (a.row_done) {
+            const CombineView cv{a.part_o, a.part_ml, a.row_done, a.out, a.lse2,
+                                 a.n_tiles_total, a.total_warps, a.tiles_per_row,
+                                 a.n_kv, a.batch, a.n_layers, a.n_q};
+            fused_combine<D, G>(cv, row, lane);
         }
     };
 
@@ -380,6 +488,8 @@ __global__ void __launch_bounds__(WARPS * 32)
 
 template <int D, int G>
 __global__ void __launch_bounds__(D) combine_kernel(const CombineArgs a) {
+    griddep_wait();
+    griddep_release();
     const int row = blockIdx.x, hh = blockIdx.y, d = threadIdx.x;
     const int64_t N = a.n_tiles_total;
     const int64_t W = a.total_warps;
@@ -419,8 +529,7 @@ cudaError_t launch_attn_t(const AttnArgs& a, int grid, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kWarps * 32, C::SMEM, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kWarps * 32), C::SMEM, s, a);
 }
 
 template <int D, int G>
@@ -464,14 +573,9 @@ cudaError_t launch_attention(const AttnArgs& a, int head_dim, int group, int gri
 
 cudaError_t launch_combine(const CombineArgs& a, int head_dim, int group, cudaStream_t s) {
     const dim3 grid(a.n_layers * a.batch * a.n_kv, group);
-    if (group == 4 && head_dim == 128) {
-        combine_kernel<128, 4><<<grid, 128, 0, s>>>(a);
-    } else if (group == 4 && head_dim == 64) {
-        combine_kernel<64, 4><<<grid, 64, 0, s>>>(a);
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    if (group == 4 && head_dim == 128) return launch_pdl(combine_kernel<128, 4>, grid, dim3(128), 0, s, a);
+    if (group == 4 && head_dim == 64) return launch_pdl(combine_kernel<64, 4>, grid, dim3(64), 0, s, a);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace kvev

@@ -17,6 +17,8 @@ constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 4;
 
 __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const CompactArgs a) {
+    griddep_wait();
+    griddep_release();
     const int lpr = a.head_dim / 8;                 // 16-byte units per row
     const int rows_per_pass = kCopyThreads / lpr;
     const int chunk = rows_per_pass * kCopyUnroll;  // retained rows per CTA
@@ -59,6 +61,8 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const CompactArgs
 
 __global__ void append_kernel(const AppendArgs a) {
     // one CTA per (layer, sequence, KV head) row; threads copy 16-byte units
+    griddep_wait();
+    griddep_release();
     const int r = blockIdx.x;
     const int g = r % a.n_kv, lb = r / a.n_kv;
     const int b = lb % a.batch, l = lb / a.batch;
@@ -81,6 +85,8 @@ __global__ void append_kernel(const AppendArgs a) {
 }
 
 __global__ void init_state_kernel(kvev_state st, int batch, int max_ctx, int len) {
+    griddep_wait();
+    griddep_release();
     const int64_t n = (int64_t)batch * len;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
          e += (int64_t)gridDim.x * blockDim.x) {
@@ -100,22 +106,19 @@ cudaError_t launch_compact(const CompactArgs& a, int num_sms, cudaStream_t s) {
     const int lpr = a.head_dim / 8;
     const int chunk = (kCopyThreads / lpr) * kCopyUnroll;
     const dim3 grid((a.n_keep + chunk - 1) / chunk, a.identity ? 1 : a.rows, a.identity ? 1 : 2);
-    compact_kernel<<<grid, kCopyThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(compact_kernel, grid, dim3(kCopyThreads), 0, s, a);
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
     const int rows = a.n_layers * a.batch * a.n_kv;
-    append_kernel<<<rows, 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(append_kernel, dim3(rows), dim3(32), 0, s, a);
 }
 
 cudaError_t launch_init_state(kvev_state st, int batch, int max_ctx, int len, cudaStream_t s) {
     if (len == 0 || batch == 0) return cudaSuccess;
     const int64_t n = (int64_t)batch * len;
     const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    init_state_kernel<<<blocks, 256, 0, s>>>(st, batch, max_ctx, len);
-    return cudaGetLastError();
+    return launch_pdl(init_state_kernel, dim3(blocks), dim3(256), 0, s, st, batch, max_ctx, len);
 }
 
 }  // namespace kvev

@@ -36,6 +36,11 @@ struct AttnArgs {
     int32_t total_warps;
     int32_t write_logits;
     float q_scale;         // log2(e) / sqrt(D)
+    // Fused combine (optional): when row_done is set, the last warp to finish
+    // a row merges that row's partials into out / lse2 and resets its counter.
+    int32_t* row_done;     // [rows] zero-initialised counters, or null
+    float* out;            // [b][Ly][Hq][D]
+    float* lse2;           // [rows][G]
 };
 
 struct CombineArgs {
@@ -95,6 +100,36 @@ struct AppendArgs {
     kvev_state st;
     int32_t slot, t, pos, n_layers, batch, n_kv, max_ctx, head_dim;
 };
+
+// ---- programmatic dependent launch ----------------------------------------
+// Every kernel of the pass is launched with programmatic stream serialisation:
+// it may be scheduled while its predecessor drains, and waits in
+// griddep_wait() (before touching global memory) until the predecessor has
+// completed and its writes are visible.  griddep_release() lets the next
+// kernel start being scheduled.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_release() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 // ---- launchers (return cudaGetLastError of the launch) --------------------
 int attn_ctas_per_sm(int head_dim, int group);

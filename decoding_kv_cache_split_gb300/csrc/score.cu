@@ -37,9 +37,100 @@ __device__ __forceinline__ uint32_t order_bits(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Refresh steps.  A CTA owns 32 consecutive tokens of one sequence.  Phase 1:
+// warp w streams the logits of KV heads g = w, w+8, ... for all layers (one
+// 16-byte load per layer per token, lanes on consecutive tokens, every layer
+// in flight at once) and leaves, per layer, its share of the head sum in
+// shared memory.  Phase 2: warp 0, one lane per token, folds the layers in
+// ascending order into the EMA and forms the clock, priority and key.
+constexpr int kRefreshTokens = 32;
+constexpr int kRefreshWarps = 8;
+
+template <int G>
+__global__ void __launch_bounds__(kRefreshWarps * 32) score_refresh_kernel(const ScoreArgs a) {
+    extern __shared__ float sm[];
+    float* s_lse = sm;                                  // [Ly][Hq]
+    float* part = sm + a.n_layers * a.n_q;              // [Ly][warps][32]
+    griddep_wait();
+    griddep_release();
+    const int b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nlse = a.n_layers * a.n_q;
+    for (int k = threadIdx.x; k < nlse; k += blockDim.x) {
+        const int l = k / a.n_q, h = k % a.n_q;
+        s_lse[k] = a.lse2[((size_t)l * a.batch + b) * a.n_q + h];
+    }
+    __syncthreads();
+    const int i = blockIdx.x * kRefreshTokens + lane;
+    const bool live = i < a.L;
+
+    for (int l = 0; l < a.n_layers; ++l) part[(l * kRefreshWarps + warp) * 32 + lane] = 0.f;
+    constexpr int kBatch = 16;   // layers whose logits are in flight together
+    for (int g = warp; g < a.n_kv; g += kRefreshWarps) {
+        const float* lg = s_lse + g * G;
+        for (int l0 = 0; l0 < a.n_layers; l0 += kBatch) {
+            float4 xb[kBatch][G / 4];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {       // all loads first ...
+                const int l = l0 + k;
+                const size_t row = ((size_t)l * a.batch + b) * a.n_kv + g;
+                const float4* x = reinterpret_cast<const float4*>(a.logits + (row * a.max_ctx + i) * G);
+#pragma unroll
+                for (int c = 0; c < G / 4; ++c)
+                    xb[k][c] = (live && l < a.n_layers) ? __ldcs(x + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {       // ... then the arithmetic and stores
+                const int l = l0 + k;
+                if (!live || l >= a.n_layers) continue;
+                const float* xv = reinterpret_cast<const float*>(&xb[k][0]);
+                float s = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float p = fast_exp2(xv[hh] - lg[l * a.n_q + hh]);
+                    if (a.dbg_probs)
+                        a.dbg_probs[(((size_t)b * a.n_layers + l) * a.n_q + g * G + hh) * a.max_ctx + i] = p;
+                    s += p;
+                }
+                part[(l * kRefreshWarps + warp) * 32 + lane] += s;
+            }
+        }
+    }
+    __syncthreads();
+    if (warp != 0 || !live) return;
+
+    const size_t si = (size_t)b * a.max_ctx + i;
+    float m = a.st.score[si];
+    int t_ref = a.st.t_ref[si];
+    const int t_ins = a.st.t_ins[si];
+    const float oma = 1.0f - a.alpha;
+    const float inv_hq = 1.0f / (float)a.n_q;
+    float tot = 0.f;
+    for (int l = 0; l < a.n_layers; ++l) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kRefreshWarps; ++w) s += part[(l * kRefreshWarps + w) * 32 + lane];
+        tot += s;
+        const float sp = a.pool_mean ? s * inv_hq : s;
+        m = fmaf(a.alpha, sp, oma * m);
+    }
+    if (tot >= a.access_thr) t_ref = a.t;   // the clock runs in every age mode
+    const int age = a.t - (a.age_mode == KVEV_AGE_SINCE_ACCESS ? t_ref : t_ins);
+    const float pr = age == 0 ? 0.0f : (1.0f - m) * -expm1f(-a.beta * (float)age);
+    a.keys[si] = order_bits(pr);
+    a.m_s[si] = m;
+    a.tref_s[si] = t_ref;
+    a.tins_s[si] = t_ins;
+    a.pos_s[si] = a.st.pos[si];
+    if (a.dbg_prio) a.dbg_prio[si] = pr + 0.0f;
+}
+
+// Non-refresh steps (and the general one-thread-per-token form).
 template <int G>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a) {
     extern __shared__ float s_lse[];  // [Ly][Hq] of this sequence
+    griddep_wait();
+    griddep_release();
     const int b = blockIdx.y;
     const int nlse = a.n_layers * a.n_q;
     for (int k = threadIdx.x; k < nlse; k += blockDim.x) {
@@ -120,18 +211,28 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
 }  // namespace
 
 cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStream_t s) {
+    if (a.refresh) {
+        const int nb = (a.L + kRefreshTokens - 1) / kRefreshTokens;
+        *n_blocks = nb;
+        const dim3 grid(nb, a.batch);
+        const size_t smem = sizeof(float) * ((size_t)a.n_layers * a.n_q +
+                                             (size_t)a.n_layers * kRefreshWarps * 32);
+        auto k4 = score_refresh_kernel<4>;
+        auto k8 = score_refresh_kernel<8>;
+        auto kern = group == 4 ? k4 : group == 8 ? k8 : nullptr;
+        if (!kern) return cudaErrorInvalidValue;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(kern, grid, dim3(kRefreshWarps * 32), smem, s, a);
+    }
     const int nb = (a.L + kScoreThreads - 1) / kScoreThreads;
     *n_blocks = nb;
     const dim3 grid(nb, a.batch);
     const size_t smem = sizeof(float) * (size_t)a.n_layers * a.n_q;
-    if (group == 4) {
-        score_kernel<4><<<grid, kScoreThreads, smem, s>>>(a);
-    } else if (group == 8) {
-        score_kernel<8><<<grid, kScoreThreads, smem, s>>>(a);
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    if (group == 4) return launch_pdl(score_kernel<4>, grid, dim3(kScoreThreads), smem, s, a);
+    if (group == 8) return launch_pdl(score_kernel<8>, grid, dim3(kScoreThreads), smem, s, a);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace kvev

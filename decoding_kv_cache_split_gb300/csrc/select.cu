@@ -55,8 +55,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     __shared__ int red[32];
     __shared__ uint32_t s_digit, s_rank;
 
+    griddep_wait();
+    griddep_release();
     const int b = blockIdx.x;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    (void)lane;
     const int L = a.L, B = a.budget;
     const uint32_t* gkeys = a.keys + (size_t)b * a.max_ctx;
     int32_t* ret = a.retained + (size_t)b * B;
@@ -73,20 +76,42 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
         return;
     }
     const bool staged = L <= kSmemKeyCap;
+    if (staged) {   // stage the keys: a batch of loads in flight per thread
+        constexpr int kBatch = 8;
+        for (int i0 = 0; i0 < L; i0 += kSelThreads * kBatch) {
+            uint32_t v[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int i = i0 + k * kSelThreads + tid;
+                v[k] = i < L ? __ldcg(gkeys + i) : 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int i = i0 + k * kSelThreads + tid;
+                if (i < L) s_keys[i] = v[k];
+            }
+        }
+    }
+    const uint32_t* keys = staged ? s_keys : gkeys;
 
     uint32_t prefix = 0, pmask = 0, rank = (uint32_t)B;   // rank: 1-based within candidates
     for (int shift = 24; shift >= 0; shift -= 8) {
         for (int k = tid; k < kSelWarps * 256; k += kSelThreads) (&hist[0][0])[k] = 0;
         __syncthreads();
-        for (int i = tid; i < L; i += kSelThreads) {
-            uint32_t u;
-            if (shift == 24) {
-                u = gkeys[i];
-                if (staged) s_keys[i] = u;
-            } else {
-                u = staged ? s_keys[i] : gkeys[i];
-            }
-            if ((u & pmask) == prefix) atomicAdd(&hist[warp][(u >> shift) & 255u], 1u);
+        for (int i0 = 0; i0 < L; i0 += kSelThreads) {   // every lane runs every round
+            const int i = i0 + tid;
+            const uint32_t u = i < L ? keys[i] : 0u;
+            const bool act = i < L && (u & pmask) == prefix;
+            const uint32_t digit = (u >> shift) & 255u;
+            // Equal priorities are common (e.g. every accessed token has 0): the
+            // lanes sharing the first active lane's digit add with one atomic.
+            const unsigned am = __ballot_sync(0xffffffffu, act);
+            if (!am) continue;
+            const int leader = __ffs(am) - 1;
+            const uint32_t d0 = __shfl_sync(0xffffffffu, digit, leader);
+            const unsigned same = __ballot_sync(0xffffffffu, act && digit == d0);
+            if (lane == leader) atomicAdd(&hist[warp][d0], (uint32_t)__popc(same));
+            else if (act && digit != d0) atomicAdd(&hist[warp][digit], 1u);
         }
         __syncthreads();
         if (tid < 256) {
@@ -129,7 +154,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     const int i0 = min(L, tid * chunk), i1 = min(L, i0 + chunk);
     int n_lt = 0, n_eq = 0;
     for (int i = i0; i < i1; ++i) {
-        const uint32_t u = staged ? s_keys[i] : gkeys[i];
+        const uint32_t u = keys[i];
         n_lt += u < T;
         n_eq += u == T;
     }
@@ -139,7 +164,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     const int out0 = block_exclusive_scan(n_lt + my_eq_keep, red, &total);
     int o = out0, eqr = eq_before;
     for (int i = i0; i < i1; ++i) {
-        const uint32_t u = staged ? s_keys[i] : gkeys[i];
+        const uint32_t u = keys[i];
         bool keep = u < T;
         if (u == T) {
             keep = eqr < keep_eq;
@@ -157,8 +182,7 @@ cudaError_t launch_select(const SelectArgs& a, int batch, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(sizeof(uint32_t) * kSmemKeyCap));
     if (e != cudaSuccess) return e;
-    select_kernel<<<batch, kSelThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(select_kernel, dim3(batch), dim3(kSelThreads), smem, s, a);
 }
 
 }  // namespace kvev
