@@ -43,11 +43,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     headers = sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [
         os.path.join(HERE, "..", "include", "kvev.h")]
     cc = nvcc()
+    extra = os.environ.get("KVEV_EXTRA_NVCC_FLAGS", "").split()
     jobs = []
     for src in sources:
         obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
         if force or _needs(obj, [src] + headers):
-            cmd = [cc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+            cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
             if verbose:
                 cmd.insert(1, "-Xptxas=-v")
             jobs.append((src, cmd))

@@ -12,24 +12,25 @@
 // Appendix J "Hook-level profiling").
 //
 // Design (GB300, sm_103a):
-//  * The op is a GEMV over bf16 K/V: 4 flop per byte at GQA group 4, far
-//    below the tensor-core ridge, so it runs on the FP32 pipes with packed
-//    fma.rn.f32x2, and the goal is HBM bandwidth.
 //  * Every warp owns an equal contiguous range of 16-token tiles of the
 //    concatenated rows (no tail imbalance at any length) and streams them
-//    through its own double buffer in shared memory with cp.async.bulk
-//    (TMA bulk copies, completion on an mbarrier, L2 evict-first).  No
-//    block-level barrier exists in the main loop.
-//  * A row is read by D/8 lanes, 16 bytes each (LDS.128, conflict-free).
-//    Partial dot products are combined by a shuffle reduce-scatter; the
-//    lane-dependent index permutation that makes it select-free is folded
-//    into the order in which each lane visits its rows and into the slot
-//    order of its query registers.
+//    through its own ring of stages in shared memory with 2-D TMA
+//    (cp.async.bulk.tensor, boxes of 16 tokens x 64 dims, 128-byte swizzle,
+//    completion on an mbarrier, L2 evict-first).  No block-level barrier
+//    exists in the main loop.
+//  * The op is a GEMV over bf16 K/V (4 flop per byte at GQA group 4), so the
+//    goal is HBM bandwidth.  A first version on the FP32 pipes (packed
+//    fma.rn.f32x2 and a shuffle reduce-scatter) was issue-bound at 6.1 TB/s
+//    while a pure TMA stream of the same tiles reaches 7.4 TB/s; here the
+//    two contractions of a tile run on mma.sync m16n8k16 (bf16 in, fp32
+//    accumulate), which removes most of the per-token instructions.
 //  * Softmax partials (running max, sum, output) of each warp's piece of a
 //    row go to a slot; the last warp to finish a row (an atomic counter per
 //    row) merges the row's partials and writes the output and the per-head
 //    log2-sum-exp.  A standalone combine kernel does the same for callers
 //    without counters.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 
 #include "kvev_internal.h"
@@ -78,54 +79,12 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rc, rd;\n"
-        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
-        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// 8 bf16 (one 16-byte word) -> 4 float pairs, exactly.
-__device__ __forceinline__ void unpack8(uint4 w, float2 (&f)[4]) {
-    f[0] = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
-    f[1] = make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
-    f[2] = make_float2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u));
-    f[3] = make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
-}
 
-constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
-
-template <int D, int G, int STAGES, int WARPS>
-struct AttnCfg {
-    static constexpr int T = kTile;
-    static constexpr int LPR = D / 8;        // lanes per cache row (16 B each)
-    static constexpr int RPW = 32 / LPR;     // rows covered by one warp-wide load
-    static constexpr int RPL = T / RPW;      // rows a lane visits per tile
-    static constexpr int NV = RPL * G;       // partial dot products per lane per tile
-    static constexpr int NVF = NV / LPR;     // complete dot products per lane per tile
-    static constexpr int LOG_NVF = ilog2(NVF);
-    static constexpr int NSTEP = ilog2(LPR);
-    static constexpr int TILE_BYTES = T * D * 2;
-    static constexpr size_t SMEM = (size_t)WARPS * STAGES * 2 * TILE_BYTES +
-                                   (size_t)WARPS * STAGES * sizeof(uint64_t);
-    static_assert(NVF * 2 == G, "the lane layout splits each tile's heads into two groups");
-    static_assert(RPL * RPW == T && NV % LPR == 0, "tile shape");
-};
 
 // Warps of the split whose tile range is empty write no partial.
 __device__ __forceinline__ bool warp_has_tiles(int64_t w, int64_t N, int64_t W) {
@@ -225,26 +184,100 @@ __device__ __noinline__ void fused_combine(const CombineView a, int64_t row, int
     if (lane == 0) a.row_done[row] = 0;
 }
 
+// ---------------------------------------------------------------------------
+// The two contractions of a 16-token tile on mma.sync m16n8k16 (bf16 in,
+// fp32 accumulate):
+//   S = Q K^T : A = Q (query heads of the group in rows 0..G-1, zero rows
+//               above), B = the K tile; 2 token blocks x D/16 k-steps.
+//   O += P V  : A = P from the S accumulators (the fragment layouts line up),
+//               split into bf16 hi + lo so P keeps ~16 mantissa bits;
+//               B = the V tile through ldmatrix.trans.
+// K/V tiles arrive by 2-D TMA in boxes of 16 tokens x 64 dims with the
+// 128-byte swizzle, so every ldmatrix is conflict-free.  Each thread owns
+// one head g = lane/4 of the group (rows g >= G are padding), so the online
+// softmax needs only 4-lane shuffles and no head selects.
+template <int D, int G, int STAGES, int WARPS>
+struct MmaCfg {
+    static constexpr int T = kTile;                 // tokens per tile
+    static constexpr int BOXES = D / 64;            // 64-dim (128-byte) boxes per tile
+    static constexpr int BOX_BYTES = T * 128;       // one box: 16 rows x 128 B
+    static constexpr int TILE_BYTES = BOXES * BOX_BYTES;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K and V
+    static constexpr int NB = D / 8;                // 8-dim output blocks
+    static constexpr int KS = D / 16;               // k-steps of the QK contraction
+    static constexpr size_t SMEM = 1024 + (size_t)WARPS * STAGES * STAGE_BYTES +
+                                   (size_t)WARPS * STAGES * sizeof(uint64_t);
+    static_assert(G <= 8 && (D == 64 || D == 128), "mma tile shape");
+};
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+// D = A B + C for one 16x8x16 block; A rows 8..15 are zero (a1 = a3 = 0),
+// so only d0, d1 (rows 0..7) are used; d2, d3 are discarded.
+__device__ __forceinline__ void mma_rows8(float& c0, float& c1, uint32_t a0, uint32_t a2,
+                                          uint32_t b0, uint32_t b1) {
+    float d2, d3;   // rows 8..15: discarded
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3},"
+        " {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(c0), "=f"(c1), "=f"(d2), "=f"(d3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(0.f),
+          "f"(0.f));
+    (void)d2;
+    (void)d3;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// shared-memory byte address of 16-byte chunk c (0 .. D/8-1) of tile row r
+template <int D>
+__device__ __forceinline__ uint32_t tile_chunk(uint32_t tile, int r, int c) {
+    return tile + (c >> 3) * (kTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
 template <int D, int G, int STAGES, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
-    attn_splitk_kernel(const AttnArgs a) {
-    using C = AttnCfg<D, G, STAGES, WARPS>;
-    constexpr int T = C::T, LPR = C::LPR, RPW = C::RPW, RPL = C::RPL, NV = C::NV,
-                  NVF = C::NVF, TB = C::TILE_BYTES;
+    attn_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a) {
+    using C = MmaCfg<D, G, STAGES, WARPS>;
+    constexpr int T = C::T, NB = C::NB, KS = C::KS;
 
-    extern __shared__ __align__(128) unsigned char smem[];
-    griddep_wait();      // the append of this step is complete and visible
+    extern __shared__ unsigned char smem_raw[];
+    griddep_wait();
     griddep_release();
+    // 128-byte swizzled boxes want 1024-byte aligned destinations
+    unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    unsigned char* wbuf = smem + (size_t)warp * STAGES * 2 * TB;
-    uint64_t* bars =
-        reinterpret_cast<uint64_t*>(smem + (size_t)WARPS * STAGES * 2 * TB) + warp * STAGES;
+    unsigned char* wbuf = smem + (size_t)warp * STAGES * C::STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)WARPS * STAGES * C::STAGE_BYTES) +
+                     warp * STAGES;
 
     const int w = blockIdx.x * WARPS + warp;
     const int64_t N = a.n_tiles_total;
     const int64_t x0 = (int64_t)w * N / a.total_warps;
     const int64_t x1 = (int64_t)(w + 1) * N / a.total_warps;
-    if (x0 >= x1) return;  // this warp has no tiles (tiny problems)
+    if (x0 >= x1) return;
 
     if (lane == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
@@ -253,67 +286,51 @@ __global__ void __launch_bounds__(WARPS * 32)
     __syncwarp();
     const uint64_t pol = evict_first_policy();
 
-    auto issue = [&](int64_t x, int stage) {  // lane 0 only
-        const int64_t row = x / a.tiles_per_row;
-        const int tok0 = (int)(x - row * a.tiles_per_row) * T;
-        const int nv = min(T, a.L - tok0);
-        const uint32_t bytes = (uint32_t)nv * D * 2;
-        const size_t off = ((size_t)row * a.max_ctx + tok0) * D;
-        unsigned char* dst = wbuf + (size_t)stage * 2 * TB;
-        mbar_expect_tx(&bars[stage], 2 * bytes);
-        bulk_load(dst, a.k + off, bytes, &bars[stage], pol);
-        bulk_load(dst + TB, a.v + off, bytes, &bars[stage], pol);
+    // tiles are walked with (row, tile-in-row) counters: no divisions in the loop
+    const int tpr = a.tiles_per_row;
+    auto issue = [&](int64_t row, int tile, int stage) {  // lane 0 only
+        const int y = (int)(row * a.max_ctx + tile * T);
+        unsigned char* dst = wbuf + (size_t)stage * C::STAGE_BYTES;
+        mbar_expect_tx(&bars[stage], C::STAGE_BYTES);
+#pragma unroll
+        for (int bx = 0; bx < C::BOXES; ++bx) {
+            tma_load_2d(dst + bx * C::BOX_BYTES, &tmap_k, bx * 64, y, &bars[stage], pol);
+            tma_load_2d(dst + C::TILE_BYTES + bx * C::BOX_BYTES, &tmap_v, bx * 64, y,
+                        &bars[stage], pol);
+        }
     };
-    if (lane == 0)
-        for (int s = 0; s < STAGES && x0 + s < x1; ++s) issue(x0 + s, s);
+    int64_t prow = x0 / tpr;          // next tile to issue
+    int ptile = (int)(x0 - prow * tpr);
+    const int64_t n_issue0 = x1 - x0 < STAGES ? x1 - x0 : STAGES;
+    for (int s = 0; s < n_issue0; ++s) {
+        if (lane == 0) issue(prow, ptile, s);
+        if (++ptile == tpr) { ptile = 0; ++prow; }
+    }
+    int64_t crow = x0 / tpr;          // tile being consumed
+    int ctile = (int)(x0 - crow * tpr);
 
-    const int hl = lane % LPR, hr = lane / LPR;
-    // Reduce-scatter bookkeeping: the lane stores the partial for (local row
-    // j, head h) at index (j*G + h) ^ pmask, so each halving step keeps the
-    // lower half; afterwards it owns rows j_own = hl>>1, heads h0..h0+NVF-1.
-    const int pmask = hl << C::LOG_NVF;
-    const int pmask_r = pmask / G, h0 = pmask % G;
-    const bool odd = (hl & 1) != 0;
-
-    float2 q2[G][4];   // slot h' holds head h' ^ h0, dims hl*8 .. hl*8+7, scaled
-    float2 o2[G][4];   // running output, head h (natural order)
-    float m_run[G];    // running max per head (log2 domain), same in every lane
-    float l_part[NVF]; // this lane's share of the running sum, heads h0+e
+    const int g = lane >> 2, t = lane & 3;   // fragment row (query head) and column pair
+    const bool real = g < G;
+    uint32_t qa0[KS], qa2[KS];               // Q as the A operand, per k-step
+    float o[NB][2];                          // O[g][8j + 2t .. 2t+1]
+    float m_run = -INFINITY, l_run = 0.f;
     int64_t cur_row = -1;
 
     auto flush = [&](int64_t row) {
-        // sum the output over lanes that read different rows of the same dims
-#pragma unroll
-        for (int m = LPR; m < 32; m <<= 1)
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    o2[h][c].x += __shfl_xor_sync(kFull, o2[h][c].x, m);
-                    o2[h][c].y += __shfl_xor_sync(kFull, o2[h][c].y, m);
-                }
-#pragma unroll
-        for (int e = 0; e < NVF; ++e)
-#pragma unroll
-            for (int m = 2; m < 32; m <<= 1) l_part[e] += __shfl_xor_sync(kFull, l_part[e], m);
+        float l = l_run;
+        l += __shfl_xor_sync(kFull, l, 1);
+        l += __shfl_xor_sync(kFull, l, 2);
         const int64_t slot = (int64_t)w + row;
-        float* po = a.part_o + (size_t)slot * G * D;
-        if (hr == 0) {
+        if (real) {
+            float* po = a.part_o + ((size_t)slot * G + g) * D;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float4* dst = reinterpret_cast<float4*>(po + h * D + hl * 8);
-                dst[0] = make_float4(o2[h][0].x, o2[h][0].y, o2[h][1].x, o2[h][1].y);
-                dst[1] = make_float4(o2[h][2].x, o2[h][2].y, o2[h][3].x, o2[h][3].y);
+            for (int j = 0; j < NB; ++j)
+                *reinterpret_cast<float2*>(po + 8 * j + 2 * t) = make_float2(o[j][0], o[j][1]);
+            if (t == 0) {
+                float* pml = a.part_ml + ((size_t)slot * G + g) * 2;
+                pml[0] = m_run;
+                pml[1] = l;
             }
-        }
-        float* pml = a.part_ml + (size_t)slot * G * 2;
-        if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) pml[h * 2] = m_run[h];
-        }
-        if (lane < 2) {  // lane 0 owns heads 0..NVF-1, lane 1 heads NVF..G-1
-#pragma unroll
-            for (int e = 0; e < NVF; ++e) pml[(h0 + e) * 2 + 1] = l_part[e];
         }
         if (a.row_done) {
             const CombineView cv{a.part_o, a.part_ml, a.row_done, a.out, a.lse2,
@@ -325,154 +342,134 @@ __global__ void __launch_bounds__(WARPS * 32)
 
     bool ok = true;
     int64_t it = 0;
+    int stage = 0;
+    uint32_t parity = 0;
     for (int64_t x = x0; x < x1; ++x, ++it) {
-        const int stage = (int)(it % STAGES);
-        const uint32_t parity = (uint32_t)((it / STAGES) & 1);
-        const int64_t row = x / a.tiles_per_row;
-        const int tok0 = (int)(x - row * a.tiles_per_row) * T;
+        const int64_t row = crow;
+        const int tok0 = ctile * T;
+        if (++ctile == tpr) { ctile = 0; ++crow; }
 
         if (row != cur_row) {
             if (cur_row >= 0) flush(cur_row);
             cur_row = row;
-            const int g = (int)(row % a.n_kv);
+            const int gk = (int)(row % a.n_kv);
             const int64_t lb = row / a.n_kv;
             const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
-            const uint16_t* qrow =
-                a.q + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)g * G) * D + hl * 8;
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                a.q + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)gk * G + (real ? g : 0)) * D);
 #pragma unroll
-            for (int hs = 0; hs < G; ++hs) {
-                const uint4 qw = *reinterpret_cast<const uint4*>(qrow + (size_t)(hs ^ h0) * D);
-                float2 qf[4];
-                unpack8(qw, qf);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    q2[hs][c] = make_float2(qf[c].x * a.q_scale, qf[c].y * a.q_scale);
+            for (int s = 0; s < KS; ++s) {
+                qa0[s] = real ? qrow[8 * s + t] : 0u;       // dims 16s + 2t, +1
+                qa2[s] = real ? qrow[8 * s + 4 + t] : 0u;   // dims 16s + 8 + 2t, +1
             }
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                m_run[h] = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) o2[h][c] = make_float2(0.f, 0.f);
-            }
-#pragma unroll
-            for (int e = 0; e < NVF; ++e) l_part[e] = 0.f;
+            for (int j = 0; j < NB; ++j) o[j][0] = o[j][1] = 0.f;
+            m_run = -INFINITY;
+            l_run = 0.f;
         }
 
         if (!mbar_wait(&bars[stage], parity)) {
             ok = false;
             break;
         }
-        const unsigned char* Ks = wbuf + (size_t)stage * 2 * TB;
-        const unsigned char* Vs = Ks + TB;
+        const uint32_t ktile = smem_addr(wbuf + (size_t)stage * C::STAGE_BYTES);
+        const uint32_t vtile = ktile + C::TILE_BYTES;
         const int nvalid = min(T, a.L - tok0);
 
-        // ---- q.k for this lane's rows and slice of dims
-        float acc[NV];
+        // ---- S = Q K^T for the two 8-token blocks (even and odd k-steps in
+        //      separate accumulators: four independent MMA chains)
+        float sc[2][2];
+        {
+            float acc[2][2][2] = {};
 #pragma unroll
-        for (int rp = 0; rp < RPL; ++rp) {
-            const int j = rp ^ pmask_r;
-            const uint4 kw =
-                *reinterpret_cast<const uint4*>(Ks + ((j * RPW + hr) * D + hl * 8) * 2);
-            float2 k2[4];
-            unpack8(kw, k2);
+            for (int s = 0; s < KS; s += 2) {
 #pragma unroll
-            for (int hs = 0; hs < G; ++hs) {
-                float2 t = ffma2(q2[hs][0], k2[0], make_float2(0.f, 0.f));
-                t = ffma2(q2[hs][1], k2[1], t);
-                t = ffma2(q2[hs][2], k2[2], t);
-                t = ffma2(q2[hs][3], k2[3], t);
-                acc[rp * G + hs] = t.x + t.y;
-            }
-        }
-        // ---- reduce-scatter across the LPR lanes of a row group
-#pragma unroll
-        for (int s = 0; s < C::NSTEP; ++s) {
-            const int half = (NV >> s) >> 1;
-            const int m = LPR >> (s + 1);
-#pragma unroll
-            for (int i = 0; i < half; ++i) acc[i] += __shfl_xor_sync(kFull, acc[i + half], m);
-        }
-        // acc[e] (e < NVF) is now the full logit of tile row j_own*RPW+hr, head h0+e
-        const int tok_own = pmask_r * RPW + hr;
-        const bool own_valid = tok_own < nvalid;
-        float xv[NVF];
-#pragma unroll
-        for (int e = 0; e < NVF; ++e) xv[e] = own_valid ? acc[e] : -INFINITY;
-        if (a.write_logits && own_valid) {
-            float* dst = a.logits + ((size_t)row * a.max_ctx + tok0 + tok_own) * G + h0;
-            if constexpr (NVF == 2) {
-                *reinterpret_cast<float2*>(dst) = make_float2(xv[0], xv[1]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < NVF; ++e) dst[e] = xv[e];
-            }
-        }
-        // ---- online softmax: per-head tile max, rescale only when it grows
-        float tmo[NVF], tmx[NVF];
-#pragma unroll
-        for (int e = 0; e < NVF; ++e) {
-            float v = xv[e];
-#pragma unroll
-            for (int m = 2; m < 32; m <<= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, m));
-            tmo[e] = v;
-            tmx[e] = __shfl_xor_sync(kFull, v, 1);
-        }
-        float m_new[G];
-        bool grow = false;
-#pragma unroll
-        for (int e = 0; e < NVF; ++e) {
-            m_new[e] = fmaxf(m_run[e], odd ? tmx[e] : tmo[e]);
-            m_new[NVF + e] = fmaxf(m_run[NVF + e], odd ? tmo[e] : tmx[e]);
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) grow |= m_new[h] > m_run[h];
-        if (grow) {
-            float f[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                f[h] = fast_exp2(m_run[h] - m_new[h]);
-                m_run[h] = m_new[h];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    o2[h][c].x *= f[h];
-                    o2[h][c].y *= f[h];
+                for (int i = 0; i < 2; ++i) {
+                    uint32_t kb[4];   // b0, b1 of k-steps s and s+1
+                    ldsm_x4(tile_chunk<D>(ktile, 8 * i + (lane & 7), 2 * s + (lane >> 3)), kb);
+                    mma_rows8(acc[i][0][0], acc[i][0][1], qa0[s], qa2[s], kb[0], kb[1]);
+                    mma_rows8(acc[i][1][0], acc[i][1][1], qa0[s + 1], qa2[s + 1], kb[2], kb[3]);
                 }
             }
 #pragma unroll
-            for (int e = 0; e < NVF; ++e) l_part[e] *= odd ? f[NVF + e] : f[e];
-        }
-        float p[NVF];
-#pragma unroll
-        for (int e = 0; e < NVF; ++e) {
-            const float mh = odd ? m_run[NVF + e] : m_run[e];
-            p[e] = fast_exp2(xv[e] - mh);
-            l_part[e] += p[e];
-        }
-        // ---- p.v: every lane needs p for its rows and all G heads
-#pragma unroll
-        for (int j = 0; j < RPL; ++j) {
-            const uint4 vw =
-                *reinterpret_cast<const uint4*>(Vs + ((j * RPW + hr) * D + hl * 8) * 2);
-            float2 v2[4];
-            unpack8(vw, v2);
-            if (nvalid < T && j * RPW + hr >= nvalid) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) v2[c] = make_float2(0.f, 0.f);
+            for (int i = 0; i < 2; ++i) {
+                sc[i][0] = (acc[i][0][0] + acc[i][1][0]) * a.q_scale;
+                sc[i][1] = (acc[i][0][1] + acc[i][1][1]) * a.q_scale;
             }
+        }
+        // tokens of this thread's four logits: 8i + 2t + e
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const int vi = j * G + h;
-                const float pp = __shfl_sync(kFull, p[vi & (NVF - 1)], hr * LPR + (vi >> C::LOG_NVF));
-                const float2 pp2 = make_float2(pp, pp);
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) o2[h][c] = ffma2(pp2, v2[c], o2[h][c]);
+            for (int e = 0; e < 2; ++e)
+                if (!real || 8 * i + 2 * t + e >= nvalid) sc[i][e] = -INFINITY;
+        if (a.write_logits && real) {
+            float* lg = a.logits + ((size_t)row * a.max_ctx + tok0) * G + g;
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = 8 * i + 2 * t + e;
+                    if (tok < nvalid) lg[tok * G] = sc[i][e];
+                }
+        }
+        // ---- online softmax for head g
+        float mt = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+        if (real && mt > m_run) {
+            const float f = fast_exp2(m_run - mt);
+            m_run = mt;
+            l_run *= f;
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                o[j][0] *= f;
+                o[j][1] *= f;
             }
+        }
+        float p[2][2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                p[i][e] = real ? fast_exp2(sc[i][e] - m_run) : 0.f;
+                l_run += p[i][e];
+            }
+        const uint32_t ph0 = pack_bf16x2(p[0][0], p[0][1]);   // tokens 2t, 2t+1
+        const uint32_t ph2 = pack_bf16x2(p[1][0], p[1][1]);   // tokens 8+2t, 8+2t+1
+        const uint32_t pl0 = pack_bf16x2(p[0][0] - bf16_lo(ph0), p[0][1] - bf16_hi(ph0));
+        const uint32_t pl2 = pack_bf16x2(p[1][0] - bf16_lo(ph2), p[1][1] - bf16_hi(ph2));
+
+        // rows past the end of the cache may hold anything: zero them in V
+        if (nvalid < T) {
+            unsigned char* vt = wbuf + (size_t)stage * C::STAGE_BYTES + C::TILE_BYTES;
+            for (int u = lane; u < (T - nvalid) * (D / 8); u += 32) {
+                const int r = nvalid + u / (D / 8), c = u % (D / 8);
+                *reinterpret_cast<uint4*>(vt + (tile_chunk<D>(0, r, c))) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async();   // ordered before the next TMA write to this stage
+            __syncwarp();
+        }
+        // ---- O += P V, two 8-dim blocks per ldmatrix.x4.trans
+#pragma unroll
+        for (int jj = 0; jj < NB / 2; ++jj) {
+            uint32_t vb[4];   // b0, b1 of dim blocks 2jj and 2jj+1
+            const int mi = lane >> 3;
+            ldsm_x4_t(tile_chunk<D>(vtile, (mi & 1) * 8 + (lane & 7), 2 * jj + (mi >> 1)), vb);
+            mma_rows8(o[2 * jj][0], o[2 * jj][1], ph0, ph2, vb[0], vb[1]);
+            mma_rows8(o[2 * jj][0], o[2 * jj][1], pl0, pl2, vb[0], vb[1]);
+            mma_rows8(o[2 * jj + 1][0], o[2 * jj + 1][1], ph0, ph2, vb[2], vb[3]);
+            mma_rows8(o[2 * jj + 1][0], o[2 * jj + 1][1], pl0, pl2, vb[2], vb[3]);
         }
         __syncwarp();
-        if (lane == 0 && x + STAGES < x1) {
-            fence_proxy_async();
-            issue(x + STAGES, stage);
+        if (x + STAGES < x1) {
+            if (lane == 0) {
+                fence_proxy_async();
+                issue(prow, ptile, stage);
+            }
+            if (++ptile == tpr) { ptile = 0; ++prow; }
         }
+        if (++stage == STAGES) { stage = 0; parity ^= 1u; }
     }
     if (!ok) {
         if (lane == 0) atomicOr(a.status, kStatusTimeout);
@@ -519,23 +516,56 @@ __global__ void __launch_bounds__(D) combine_kernel(const CombineArgs a) {
     if (d == 0) a.lse2[(size_t)row * G + hh] = M + log2f(lsum);
 }
 
-constexpr int kStages = 2;
-constexpr int kWarps = 4;
+#ifndef KVEV_ATTN_STAGES
+#define KVEV_ATTN_STAGES 2
+#endif
+#ifndef KVEV_ATTN_WARPS
+#define KVEV_ATTN_WARPS 4
+#endif
+constexpr int kStages = KVEV_ATTN_STAGES;   // tiles in flight per warp
+constexpr int kWarps = KVEV_ATTN_WARPS;     // warps per CTA
+
+// 2-D view of one cache buffer: rows x max_ctx tokens of D bf16; boxes of
+// 16 tokens x 64 dims with the 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* base, int64_t n_tokens, int D) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)n_tokens};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kTile};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 template <int D, int G>
 cudaError_t launch_attn_t(const AttnArgs& a, int grid, cudaStream_t s) {
-    using C = AttnCfg<D, G, kStages, kWarps>;
-    auto kern = attn_splitk_kernel<D, G, kStages, kWarps>;
+    using C = MmaCfg<D, G, kStages, kWarps>;
+    auto kern = attn_mma_kernel<D, G, kStages, kWarps>;
+    const int64_t n_tokens = (int64_t)a.n_layers * a.batch * a.n_kv * a.max_ctx;
+    CUtensorMap mk, mv;
+    if (!encode_cache_map(&mk, a.k, n_tokens, D) || !encode_cache_map(&mv, a.v, n_tokens, D))
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(grid), dim3(kWarps * 32), C::SMEM, s, a);
+    return launch_pdl(kern, dim3(grid), dim3(kWarps * 32), C::SMEM, s, mk, mv, a);
 }
 
 template <int D, int G>
 int ctas_per_sm_t() {
-    using C = AttnCfg<D, G, kStages, kWarps>;
-    auto kern = attn_splitk_kernel<D, G, kStages, kWarps>;
+    using C = MmaCfg<D, G, kStages, kWarps>;
+    auto kern = attn_mma_kernel<D, G, kStages, kWarps>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) !=
         cudaSuccess)
         return 0;
@@ -559,8 +589,8 @@ int attn_ctas_per_sm(int head_dim, int group) {
 
 size_t attn_smem_bytes(int head_dim, int group) {
     if (group != 4) return 0;
-    if (head_dim == 128) return AttnCfg<128, 4, kStages, kWarps>::SMEM;
-    if (head_dim == 64) return AttnCfg<64, 4, kStages, kWarps>::SMEM;
+    if (head_dim == 128) return MmaCfg<128, 4, kStages, kWarps>::SMEM;
+    if (head_dim == 64) return MmaCfg<64, 4, kStages, kWarps>::SMEM;
     return 0;
 }
 
