@@ -461,12 +461,12 @@ __global__ void __launch_bounds__(WARPS * 32)
             mma_rows8(o[2 * jj + 1][0], o[2 * jj + 1][1], ph0, ph2, vb[2], vb[3]);
             mma_rows8(o[2 * jj + 1][0], o[2 * jj + 1][1], pl0, pl2, vb[2], vb[3]);
         }
+        // Every ldmatrix of this stage fed an MMA issued above, so its read is
+        // complete once the warp passes this point; only the zeroing stores of
+        // a partial tile needed a proxy fence (done there).
         __syncwarp();
         if (x + STAGES < x1) {
-            if (lane == 0) {
-                fence_proxy_async();
-                issue(prow, ptile, stage);
-            }
+            if (lane == 0) issue(prow, ptile, stage);
             if (++ptile == tpr) { ptile = 0; ++prow; }
         }
         if (++stage == STAGES) { stage = 0; parity ^= 1u; }

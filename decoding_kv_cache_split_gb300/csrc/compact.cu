@@ -47,13 +47,16 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const CompactArgs
                  (size_t)r * a.max_ctx * lpr;
     const int c = threadIdx.x % lpr, jr = threadIdx.x / lpr;
     uint4 buf[kCopyUnroll];
-    int jj[kCopyUnroll];
+    int jj[kCopyUnroll], from[kCopyUnroll];
 #pragma unroll
-    for (int u = 0; u < kCopyUnroll; ++u) {
+    for (int u = 0; u < kCopyUnroll; ++u) {       // every index load in flight first
         const int j = j0 + u * rows_per_pass + jr;
         jj[u] = j;
-        if (j < a.n_keep) buf[u] = __ldcs(src + (size_t)idx[j] * lpr + c);
+        from[u] = j < a.n_keep ? __ldg(idx + j) : 0;
     }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u)
+        if (jj[u] < a.n_keep) buf[u] = __ldcs(src + (size_t)from[u] * lpr + c);
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u)
         if (jj[u] < a.n_keep) __stcs(dst + (size_t)jj[u] * lpr + c, buf[u]);

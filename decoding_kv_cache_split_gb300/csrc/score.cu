@@ -37,83 +37,76 @@ __device__ __forceinline__ uint32_t order_bits(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Refresh steps.  A CTA owns 32 consecutive tokens of one sequence.  Phase 1:
-// warp w streams the logits of KV heads g = w, w+8, ... for all layers (one
-// 16-byte load per layer per token, lanes on consecutive tokens, every layer
-// in flight at once) and leaves, per layer, its share of the head sum in
-// shared memory.  Phase 2: warp 0, one lane per token, folds the layers in
-// ascending order into the EMA and forms the clock, priority and key.
-constexpr int kRefreshTokens = 32;
-constexpr int kRefreshWarps = 8;
+// Refresh steps: two threads per token (adjacent lanes), each summing the
+// heads of half of the KV heads; lanes cover consecutive tokens so every load
+// instruction reads two 256-byte runs.  The (layer, KV head) logit rows are
+// visited in layer order in batches whose loads are all issued before any is
+// used (kBatch 16-byte loads in flight per thread); each completed layer is
+// combined across the pair with one shuffle and folded into the EMA.
+constexpr int kRefreshThreads = 128;
 
-template <int G>
-__global__ void __launch_bounds__(kRefreshWarps * 32) score_refresh_kernel(const ScoreArgs a) {
-    extern __shared__ float sm[];
-    float* s_lse = sm;                                  // [Ly][Hq]
-    float* part = sm + a.n_layers * a.n_q;              // [Ly][warps][32]
+template <int G, int kSplit>   // kSplit threads per token (1 or 2)
+__global__ void __launch_bounds__(kRefreshThreads, 4) score_refresh_kernel(const ScoreArgs a) {
+    constexpr int V4 = G / 4;                          // float4 per (layer, KV head)
+    constexpr int kBatch = 16 / V4;                    // (layer, KV head) pairs in flight
+    extern __shared__ float s_lse[];                   // [Ly][Hq] of this sequence
     griddep_wait();
     griddep_release();
     const int b = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nlse = a.n_layers * a.n_q;
     for (int k = threadIdx.x; k < nlse; k += blockDim.x) {
         const int l = k / a.n_q, h = k % a.n_q;
         s_lse[k] = a.lse2[((size_t)l * a.batch + b) * a.n_q + h];
     }
     __syncthreads();
-    const int i = blockIdx.x * kRefreshTokens + lane;
-    const bool live = i < a.L;
+    const int half = kSplit == 2 ? (threadIdx.x & 1) : 0;
+    const int i = (blockIdx.x * kRefreshThreads + threadIdx.x) / kSplit;
+    const bool live = i < a.L;                         // both lanes of a pair agree
+    const int kv_half = a.n_kv / kSplit;               // KV heads per thread
+    const int n_pairs = a.n_layers * kv_half;
 
-    for (int l = 0; l < a.n_layers; ++l) part[(l * kRefreshWarps + warp) * 32 + lane] = 0.f;
-    constexpr int kBatch = 16;   // layers whose logits are in flight together
-    for (int g = warp; g < a.n_kv; g += kRefreshWarps) {
-        const float* lg = s_lse + g * G;
-        for (int l0 = 0; l0 < a.n_layers; l0 += kBatch) {
-            float4 xb[kBatch][G / 4];
+    const size_t si = (size_t)b * a.max_ctx + (live ? i : 0);
+    float m = live ? a.st.score[si] : 0.f;
+    const float oma = 1.0f - a.alpha;
+    const float inv_hq = 1.0f / (float)a.n_q;
+    float tot = 0.f, s = 0.f;
+    for (int k0 = 0; k0 < n_pairs; k0 += kBatch) {
+        float4 xb[kBatch][V4];
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) {       // all loads first ...
-                const int l = l0 + k;
-                const size_t row = ((size_t)l * a.batch + b) * a.n_kv + g;
-                const float4* x = reinterpret_cast<const float4*>(a.logits + (row * a.max_ctx + i) * G);
+        for (int u = 0; u < kBatch; ++u) {           // all loads of the batch first ...
+            const int k = k0 + u;
+            const int l = k / kv_half, g = half * kv_half + (k - l * kv_half);
+            const size_t row = ((size_t)l * a.batch + b) * a.n_kv + g;
+            const float4* x = reinterpret_cast<const float4*>(a.logits + (row * a.max_ctx + i) * G);
 #pragma unroll
-                for (int c = 0; c < G / 4; ++c)
-                    xb[k][c] = (live && l < a.n_layers) ? __ldcs(x + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c = 0; c < V4; ++c)
+                xb[u][c] = (live && k < n_pairs) ? __ldcs(x + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {           // ... then the arithmetic, in layer order
+            const int k = k0 + u;
+            if (k >= n_pairs) break;
+            const int l = k / kv_half, gl = k - l * kv_half, g = half * kv_half + gl;
+            const float* lg = s_lse + l * a.n_q + g * G;
+            const float* xv = reinterpret_cast<const float*>(&xb[u][0]);
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                const float p = fast_exp2(xv[hh] - lg[hh]);
+                if (a.dbg_probs && live)
+                    a.dbg_probs[(((size_t)b * a.n_layers + l) * a.n_q + g * G + hh) * a.max_ctx + i] = p;
+                s += p;
             }
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {       // ... then the arithmetic and stores
-                const int l = l0 + k;
-                if (!live || l >= a.n_layers) continue;
-                const float* xv = reinterpret_cast<const float*>(&xb[k][0]);
-                float s = 0.f;
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    const float p = fast_exp2(xv[hh] - lg[l * a.n_q + hh]);
-                    if (a.dbg_probs)
-                        a.dbg_probs[(((size_t)b * a.n_layers + l) * a.n_q + g * G + hh) * a.max_ctx + i] = p;
-                    s += p;
-                }
-                part[(l * kRefreshWarps + warp) * 32 + lane] += s;
+            if (gl == kv_half - 1) {                 // layer l complete: fold it
+                if (kSplit == 2) s += __shfl_xor_sync(0xffffffffu, s, 1);
+                tot += s;
+                m = fmaf(a.alpha, a.pool_mean ? s * inv_hq : s, oma * m);
+                s = 0.f;
             }
         }
     }
-    __syncthreads();
-    if (warp != 0 || !live) return;
-
-    const size_t si = (size_t)b * a.max_ctx + i;
-    float m = a.st.score[si];
+    if (!live || half) return;
     int t_ref = a.st.t_ref[si];
     const int t_ins = a.st.t_ins[si];
-    const float oma = 1.0f - a.alpha;
-    const float inv_hq = 1.0f / (float)a.n_q;
-    float tot = 0.f;
-    for (int l = 0; l < a.n_layers; ++l) {
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < kRefreshWarps; ++w) s += part[(l * kRefreshWarps + w) * 32 + lane];
-        tot += s;
-        const float sp = a.pool_mean ? s * inv_hq : s;
-        m = fmaf(a.alpha, sp, oma * m);
-    }
     if (tot >= a.access_thr) t_ref = a.t;   // the clock runs in every age mode
     const int age = a.t - (a.age_mode == KVEV_AGE_SINCE_ACCESS ? t_ref : t_ins);
     const float pr = age == 0 ? 0.0f : (1.0f - m) * -expm1f(-a.beta * (float)age);
@@ -212,19 +205,16 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
 
 cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStream_t s) {
     if (a.refresh) {
-        const int nb = (a.L + kRefreshTokens - 1) / kRefreshTokens;
+        const int split = a.n_kv % 2 == 0 ? 2 : 1;
+        const int nb = (a.L * split + kRefreshThreads - 1) / kRefreshThreads;
         *n_blocks = nb;
         const dim3 grid(nb, a.batch);
-        const size_t smem = sizeof(float) * ((size_t)a.n_layers * a.n_q +
-                                             (size_t)a.n_layers * kRefreshWarps * 32);
-        auto k4 = score_refresh_kernel<4>;
-        auto k8 = score_refresh_kernel<8>;
-        auto kern = group == 4 ? k4 : group == 8 ? k8 : nullptr;
+        const size_t smem = sizeof(float) * (size_t)a.n_layers * a.n_q;
+        void (*kern)(ScoreArgs) = nullptr;
+        if (group == 4) kern = split == 2 ? score_refresh_kernel<4, 2> : score_refresh_kernel<4, 1>;
+        if (group == 8) kern = split == 2 ? score_refresh_kernel<8, 2> : score_refresh_kernel<8, 1>;
         if (!kern) return cudaErrorInvalidValue;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        return launch_pdl(kern, grid, dim3(kRefreshWarps * 32), smem, s, a);
+        return launch_pdl(kern, grid, dim3(kRefreshThreads), smem, s, a);
     }
     const int nb = (a.L + kScoreThreads - 1) / kScoreThreads;
     *n_blocks = nb;

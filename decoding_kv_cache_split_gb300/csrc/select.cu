@@ -6,20 +6,43 @@
 // priority of the kv-cache-docs "ema-eviction" figure a higher priority is
 // evicted, so the B lowest priorities are retained.
 //
-// One CTA per sequence.  The keys are the order-preserving bits of the fp32
-// priorities; a 4-pass radix select (8-bit digits, per-warp shared-memory
-// histograms) finds the B-th smallest key T and how many keys equal to T
-// are kept; a final pass over contiguous per-thread chunks, with two block
-// scans, emits the kept slots in ascending order.  When the sequence's keys
-// fit in shared memory they are staged there on the first pass.
+// One thread-block cluster of kCl CTAs per sequence.  The keys are the
+// order-preserving bits of the fp32 priorities; CTA r of the cluster stages
+// the r-th contiguous chunk of a sequence's keys in shared memory.  A 4-pass
+// radix select (8-bit digits) finds the B-th smallest key T: in every pass
+// each CTA histograms its chunk, the CTAs read each other's histograms
+// through distributed shared memory after a cluster barrier, and all of them
+// take the same digit.  Then each CTA counts its keys below / equal to T,
+// the counts are exchanged the same way, and each CTA writes its kept slots
+// (all keys < T, and the first keys == T in slot order up to B) at its
+// offset, ascending.  The cluster barriers are hardware barriers
+// (barrier.cluster), there is no software spin-wait.
 #include "kvev_internal.h"
 
 namespace kvev {
 namespace {
 
+constexpr int kCl = 8;                      // CTAs per sequence (portable cluster size)
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSmemKeyCap = 40960;   // keys staged in shared memory up to this length
+constexpr int kChunkCap = 10240;            // keys per CTA staged in shared memory
+
+__device__ __forceinline__ uint32_t cta_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 32-bit load from the same shared-memory variable of CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t ld_remote(const void* local, uint32_t rank) {
+    uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(local)), ra, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+    return v;
+}
 
 // Exclusive block scan of one int per thread; also returns the total.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* red, int* total) {
@@ -49,62 +72,56 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* red, int* total)
 }
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a) {
-    extern __shared__ uint32_t s_keys[];
+    extern __shared__ uint32_t s_keys[];             // this CTA's chunk (if it fits)
     __shared__ uint32_t hist[kSelWarps][256];
-    __shared__ uint32_t tot[256];
+    __shared__ uint32_t local[2][256];               // this CTA's histogram, double-buffered
+    __shared__ uint32_t counts[2];                   // keys < T, keys == T in this chunk
     __shared__ int red[32];
     __shared__ uint32_t s_digit, s_rank;
 
     griddep_wait();
     griddep_release();
-    const int b = blockIdx.x;
+    const uint32_t rank = cta_rank();
+    const int b = blockIdx.x / kCl;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    (void)lane;
     const int L = a.L, B = a.budget;
     const uint32_t* gkeys = a.keys + (size_t)b * a.max_ctx;
     int32_t* ret = a.retained + (size_t)b * B;
 
-    if (!a.refresh && tid == 0) {
+    if (!a.refresh && rank == 0 && tid == 0) {
         // new token's score: mean of the old tokens' scores (block sums in order)
         float s = 0.f;
         for (int k = 0; k < a.n_part; ++k) s += a.msum_part[(size_t)b * a.n_part + k];
         a.m_s[(size_t)b * a.max_ctx + L - 1] = L > 1 ? s / (float)(L - 1) : 0.f;
     }
-    if (L <= B) {
-        for (int i = tid; i < L; i += kSelThreads) ret[i] = i;
-        if (tid == 0) a.n_retained[b] = L;
+    if (L <= B) {   // nothing to evict: identity (the same for every CTA: no exchange)
+        if (rank == 0) {
+            for (int i = tid; i < L; i += kSelThreads) ret[i] = i;
+            if (tid == 0) a.n_retained[b] = L;
+        }
         return;
     }
-    const bool staged = L <= kSmemKeyCap;
-    if (staged) {   // stage the keys: a batch of loads in flight per thread
-        constexpr int kBatch = 8;
-        for (int i0 = 0; i0 < L; i0 += kSelThreads * kBatch) {
-            uint32_t v[kBatch];
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int i = i0 + k * kSelThreads + tid;
-                v[k] = i < L ? __ldcg(gkeys + i) : 0u;
-            }
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int i = i0 + k * kSelThreads + tid;
-                if (i < L) s_keys[i] = v[k];
-            }
-        }
+    const int chunk = (L + kCl - 1) / kCl;
+    const int c0 = min(L, (int)rank * chunk), c1 = min(L, c0 + chunk);
+    const int n = c1 - c0;
+    const bool staged = chunk <= kChunkCap;
+    if (staged) {
+        for (int i = tid; i < n; i += kSelThreads) s_keys[i] = __ldcg(gkeys + c0 + i);
     }
-    const uint32_t* keys = staged ? s_keys : gkeys;
+    const uint32_t* keys = staged ? s_keys : gkeys + c0;
 
-    uint32_t prefix = 0, pmask = 0, rank = (uint32_t)B;   // rank: 1-based within candidates
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    uint32_t prefix = 0, pmask = 0, want = (uint32_t)B;   // want: 1-based rank within candidates
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
         for (int k = tid; k < kSelWarps * 256; k += kSelThreads) (&hist[0][0])[k] = 0;
         __syncthreads();
-        for (int i0 = 0; i0 < L; i0 += kSelThreads) {   // every lane runs every round
+        for (int i0 = 0; i0 < n; i0 += kSelThreads) {   // every lane runs every round
             const int i = i0 + tid;
-            const uint32_t u = i < L ? keys[i] : 0u;
-            const bool act = i < L && (u & pmask) == prefix;
+            const uint32_t u = i < n ? keys[i] : 0u;
+            const bool act = i < n && (u & pmask) == prefix;
             const uint32_t digit = (u >> shift) & 255u;
-            // Equal priorities are common (e.g. every accessed token has 0): the
-            // lanes sharing the first active lane's digit add with one atomic.
+            // equal priorities are common (every token accessed this step has
+            // 0): lanes sharing the first active lane's digit add once
             const unsigned am = __ballot_sync(0xffffffffu, act);
             if (!am) continue;
             const int leader = __ffs(am) - 1;
@@ -114,54 +131,71 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
             else if (act && digit != d0) atomicAdd(&hist[warp][digit], 1u);
         }
         __syncthreads();
+        uint32_t* mine = local[pass & 1];
         if (tid < 256) {
             uint32_t t = 0;
             for (int w = 0; w < kSelWarps; ++w) t += hist[w][tid];
-            tot[tid] = t;
+            mine[tid] = t;
         }
-        __syncthreads();
-        if (warp < 8) {   // exclusive scan of the 256 bins by 8 warps
-            const int lane = tid & 31;
-            uint32_t x = tot[tid];
+        cluster_sync();   // every CTA's histogram of this pass is complete
+        if (warp < 8) {   // sum over the cluster, then scan the 256 bins
+            uint32_t t = 0;
+#pragma unroll
+            for (uint32_t r = 0; r < kCl; ++r) t += ld_remote(&mine[tid], r);
+            uint32_t x = t;
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
                 const uint32_t y = __shfl_up_sync(0xffffffffu, x, m);
                 if (lane >= m) x += y;
             }
             if (lane == 31) red[warp] = (int)x;
-            __syncwarp();
             asm volatile("bar.sync 1, 256;" ::: "memory");
             uint32_t base = 0;
             for (int w = 0; w < warp; ++w) base += (uint32_t)red[w];
-            const uint32_t incl = base + x, excl = incl - tot[tid];
-            if (excl < rank && rank <= incl) {
+            const uint32_t incl = base + x, excl = incl - t;
+            if (excl < want && want <= incl) {
                 s_digit = (uint32_t)tid;
-                s_rank = rank - excl;
+                s_rank = want - excl;
             }
         }
         __syncthreads();
         prefix |= s_digit << shift;
         pmask |= 255u << shift;
-        rank = s_rank;
+        want = s_rank;
         __syncthreads();
     }
     const uint32_t T = prefix;        // the B-th smallest key
-    const int keep_eq = (int)rank;    // keys equal to T kept, lowest slots first
+    const int keep_eq = (int)want;    // keys equal to T kept, lowest slots first
 
-    // contiguous chunks; an odd chunk length keeps shared-memory reads conflict-free
-    int chunk = (L + kSelThreads - 1) / kSelThreads;
-    chunk |= 1;
-    const int i0 = min(L, tid * chunk), i1 = min(L, i0 + chunk);
+    // per-thread contiguous sub-chunks (odd length: conflict-free shared reads)
+    int sub = (n + kSelThreads - 1) / kSelThreads;
+    sub |= 1;
+    const int i0 = min(n, tid * sub), i1 = min(n, i0 + sub);
     int n_lt = 0, n_eq = 0;
     for (int i = i0; i < i1; ++i) {
         const uint32_t u = keys[i];
         n_lt += u < T;
         n_eq += u == T;
     }
-    int total;
-    const int eq_before = block_exclusive_scan(n_eq, red, &total);
-    const int my_eq_keep = max(0, min(n_eq, keep_eq - eq_before));
-    const int out0 = block_exclusive_scan(n_lt + my_eq_keep, red, &total);
+    int cta_eq, cta_lt;
+    const int eq_before_t = block_exclusive_scan(n_eq, red, &cta_eq);
+    block_exclusive_scan(n_lt, red, &cta_lt);
+    if (tid == 0) {
+        counts[0] = (uint32_t)cta_lt;
+        counts[1] = (uint32_t)cta_eq;
+    }
+    cluster_sync();   // every CTA's counts are published
+    int eq_before_c = 0, out_before_c = 0;
+    for (uint32_t r = 0; r < rank; ++r) {   // CTAs before this one, in slot order
+        const int lt_r = (int)ld_remote(&counts[0], r);
+        const int eq_r = (int)ld_remote(&counts[1], r);
+        out_before_c += lt_r + max(0, min(eq_r, keep_eq - eq_before_c));
+        eq_before_c += eq_r;
+    }
+    const int eq_before = eq_before_c + eq_before_t;
+    const int my_keep = n_lt + max(0, min(n_eq, keep_eq - eq_before));
+    int cta_kept;
+    const int out0 = out_before_c + block_exclusive_scan(my_keep, red, &cta_kept);
     int o = out0, eqr = eq_before;
     for (int i = i0; i < i1; ++i) {
         const uint32_t u = keys[i];
@@ -170,19 +204,36 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
             keep = eqr < keep_eq;
             ++eqr;
         }
-        if (keep) ret[o++] = i;
+        if (keep) ret[o++] = c0 + i;
     }
-    if (tid == 0) a.n_retained[b] = total;
+    if (rank == kCl - 1 && tid == 0) a.n_retained[b] = out_before_c + cta_kept;
+    cluster_sync();   // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, int batch, cudaStream_t s) {
-    const size_t smem = a.L <= kSmemKeyCap ? sizeof(uint32_t) * (size_t)a.L : 0;
+    const int chunk = (a.L + kCl - 1) / kCl;
+    const size_t smem = chunk <= kChunkCap ? sizeof(uint32_t) * (size_t)chunk : 0;
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(uint32_t) * kSmemKeyCap));
+                                         (int)(sizeof(uint32_t) * kChunkCap));
     if (e != cudaSuccess) return e;
-    return launch_pdl(select_kernel, dim3(batch), dim3(kSelThreads), smem, s, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCl * batch);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, select_kernel, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace kvev
