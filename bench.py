@@ -344,12 +344,15 @@ def main():
 
     # --------------------------------------------------------------- roofline
     peak, peak_kind = measured_peak()
+    # the attention of one step may be split into launches over groups of
+    # layers: the algorithmic bytes of a step over its attention time per step
     att_ms, att_n = prof.get("attention", (0.0, 0))
-    att_avg = att_ms / max(1, att_n)
-    attn_achieved = attn_bytes / (att_avg * 1e-3) / 1e9 if att_avg > 0 else None
+    att_per_step = att_ms / n_prof
+    attn_achieved = attn_bytes / (att_per_step * 1e-3) / 1e9 if att_per_step > 0 else None
     tokens_layers = (L0 + 1) * W["n_layers"]
     traffic = ncu_traffic("attn.cu", tokens_layers)
-    kernels_us = {k: round(v[0] / max(1, v[1]) * 1e3, 2) for k, v in prof.items()}
+    kernels_us = {k: round(v[0] / n_prof * 1e3, 2) for k, v in prof.items()}   # per step
+    kernels_us["launches_per_step"] = {k: v[1] // n_prof for k, v in prof.items()}
     kernels_us["profiled_steps"] = n_prof
 
     line = None
@@ -370,7 +373,7 @@ def main():
                              "nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
                              "peak_kind": peak_kind},
             "kv_tokens_per_s": round(world * (L0 + 1) / (ms * 1e-3), 1),
-            "roofline": {"bound": "hbm", "kernel": "attention",
+            "roofline": {"bound": "hbm", "kernel": "attention (all launches of a step)",
                          "achieved": round(attn_achieved, 2) if attn_achieved else None,
                          "peak": peak, "unit": "GB/s",
                          "frac": round(attn_achieved / peak, 4) if attn_achieved else None,

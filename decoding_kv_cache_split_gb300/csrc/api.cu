@@ -37,7 +37,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// token stride of a logits row: whole 128-byte lines per row
+int logit_ld(int max_ctx) { return (max_ctx + 7) / 8 * 8; }
+
 enum { kProfAppend = 0, kProfAttn, kProfCombine, kProfScore, kProfSelect, kProfCompact, kProfInit };
+
+// Target size of the logits of one group of layers (see kvev_step).
+constexpr int64_t kLogitGroupBytes = int64_t(1) << 40;
 
 struct Workspace {
     float* logits = nullptr;
@@ -50,6 +56,7 @@ struct Workspace {
     int32_t* tins_s = nullptr;
     int32_t* pos_s = nullptr;
     float* msum_part = nullptr;
+    float* tot_s = nullptr;
     int32_t* row_done = nullptr;
     uint32_t* status = nullptr;
     uint16_t* stg_q = nullptr;
@@ -74,7 +81,7 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base)
     const size_t G = (size_t)(L.n_q_heads / L.n_kv_heads);
     const size_t ctx = (size_t)L.batch * L.max_ctx;
     const size_t nblk = (size_t)((L.max_ctx + kScoreThreads - 1) / kScoreThreads);
-    w.logits = (float*)take(rows * L.max_ctx * G * 4);
+    w.logits = (float*)take(rows * (size_t)logit_ld(L.max_ctx) * G * 4);
     w.part_o = (float*)take((size_t)slots * G * L.head_dim * 4);
     w.part_ml = (float*)take((size_t)slots * G * 2 * 4);
     w.lse2 = (float*)take(rows * G * 4);
@@ -84,6 +91,7 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base)
     w.tins_s = (int32_t*)take(ctx * 4);
     w.pos_s = (int32_t*)take(ctx * 4);
     w.msum_part = (float*)take((size_t)L.batch * nblk * 4);
+    w.tot_s = (float*)take(ctx * 4);
     w.row_done = (int32_t*)take(rows * 4);
     w.status = (uint32_t*)take(4);
     const size_t qn = (size_t)L.batch * L.n_layers * L.n_q_heads * L.head_dim;
@@ -416,10 +424,10 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     at.v = (const uint16_t*)cache->v[cur];
     at.q = (const uint16_t*)q;
     at.logits = c->ws.logits;
+    at.logit_ld = logit_ld(Ly.max_ctx);
     at.part_o = c->ws.part_o;
     at.part_ml = c->ws.part_ml;
     at.status = c->ws.status;
-    at.n_tiles_total = (int64_t)rows * tiles_per_row;
     at.tiles_per_row = tiles_per_row;
     at.L = L;
     at.max_ctx = Ly.max_ctx;
@@ -433,13 +441,10 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     at.row_done = c->ws.row_done;   // the split combine runs inside the attention kernel
     at.out = out;
     at.lse2 = c->ws.lse2;
-    rc = timed_launch(c, kProfAttn, s, "attention", [&] {
-        return launch_attention(at, Ly.head_dim, G, c->attn_grid, s);
-    });
-    if (rc != KVEV_OK) return rc;
 
     ScoreArgs sc{};
     sc.logits = c->ws.logits;
+    sc.logit_ld = logit_ld(Ly.max_ctx);
     sc.lse2 = c->ws.lse2;
     sc.st = *st;
     sc.m_s = c->ws.m_s;
@@ -448,6 +453,7 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     sc.pos_s = c->ws.pos_s;
     sc.keys = c->ws.keys;
     sc.msum_part = c->ws.msum_part;
+    sc.tot_s = c->ws.tot_s;
     sc.dbg_probs = refresh ? c->dbg_probs : nullptr;
     sc.dbg_prio = c->dbg_prio;
     sc.L = L;
@@ -463,9 +469,45 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     sc.alpha = c->alpha;
     sc.beta = c->beta;
     sc.access_thr = (float)(2.0 * Ly.n_q_heads * Ly.n_layers / (double)L);
+
+    // On refresh steps the layers go in groups whose logits fit comfortably
+    // in L2 (the scoring kernel reads them right after the group's attention
+    // and drops the lines, so they need not reach HBM).
+    const int64_t rows_per_layer = (int64_t)Ly.batch * Ly.n_kv_heads;
+    const int64_t logit_bytes_per_layer = rows_per_layer * L * G * 4;
+    int group_layers = Ly.n_layers;
+    if (refresh) {
+        group_layers = (int)(kLogitGroupBytes / logit_bytes_per_layer);
+        group_layers = group_layers < 1 ? 1 : group_layers > Ly.n_layers ? Ly.n_layers : group_layers;
+        const int n_groups = (Ly.n_layers + group_layers - 1) / group_layers;
+        group_layers = (Ly.n_layers + n_groups - 1) / n_groups;   // balanced groups
+    }
     int n_part = 0;
-    rc = timed_launch(c, kProfScore, s, "score", [&] { return launch_score(sc, G, &n_part, s); });
-    if (rc != KVEV_OK) return rc;
+    for (int l0 = 0; l0 < Ly.n_layers; l0 += group_layers) {
+        const int l1 = l0 + group_layers < Ly.n_layers ? l0 + group_layers : Ly.n_layers;
+        at.row0 = (int64_t)l0 * rows_per_layer;
+        at.n_tiles_total = (int64_t)(l1 - l0) * rows_per_layer * tiles_per_row;
+        rc = timed_launch(c, kProfAttn, s, "attention", [&] {
+            return launch_attention(at, Ly.head_dim, G, c->attn_grid, s);
+        });
+        if (rc != KVEV_OK) return rc;
+        if (!refresh) continue;
+        sc.l0 = l0;
+        sc.l1 = l1;
+        sc.first_group = l0 == 0;
+        sc.last_group = l1 == Ly.n_layers;
+        rc = timed_launch(c, kProfScore, s, "score",
+                          [&] { return launch_score(sc, G, &n_part, s); });
+        if (rc != KVEV_OK) return rc;
+    }
+    if (!refresh) {
+        sc.l0 = 0;
+        sc.l1 = Ly.n_layers;
+        sc.first_group = sc.last_group = 1;
+        rc = timed_launch(c, kProfScore, s, "score",
+                          [&] { return launch_score(sc, G, &n_part, s); });
+        if (rc != KVEV_OK) return rc;
+    }
 
     SelectArgs se{};
     se.keys = c->ws.keys;

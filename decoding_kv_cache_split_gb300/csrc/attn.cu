@@ -91,16 +91,17 @@ __device__ __forceinline__ bool warp_has_tiles(int64_t w, int64_t N, int64_t W) 
     return w * N / W != (w + 1) * N / W;
 }
 
-// Called by every warp after it wrote its partial of `row`: the last of the
-// row's warps to arrive merges all of the row's partials into the output and
-// the log2-sum-exp, then resets the row's counter for the next launch.
+// Called by every warp after it wrote its partial of `row` (counted from the
+// launch's first row): the last of the row's warps to arrive merges all of
+// the row's partials into the output and the log2-sum-exp, then resets the
+// row's counter for the next launch.
 struct CombineView {   // what the fused combine needs, passed by value
     const float* part_o;
     const float* part_ml;
     int32_t* row_done;
     float* out;
     float* lse2;
-    int64_t N, W;
+    int64_t N, W, row0;
     int32_t tiles_per_row, n_kv, batch, n_layers, n_q;
 };
 
@@ -116,7 +117,7 @@ __device__ __noinline__ void fused_combine(const CombineView a, int64_t row, int
     if (lane == 0) {
         int need = 0;
         for (int64_t w = w_lo; w <= w_hi; ++w) need += warp_has_tiles(w, N, W);
-        is_last = atomicAdd(&a.row_done[row], 1) == need - 1;
+        is_last = atomicAdd(&a.row_done[a.row0 + row], 1) == need - 1;
     }
     if (!__shfl_sync(kFull, is_last, 0)) return;
     __threadfence();
@@ -170,8 +171,9 @@ __device__ __noinline__ void fused_combine(const CombineView a, int64_t row, int
             }
         }
     }
-    const int g = (int)(row % a.n_kv);
-    const int64_t lb = row / a.n_kv;
+    const int64_t arow = a.row0 + row;
+    const int g = (int)(arow % a.n_kv);
+    const int64_t lb = arow / a.n_kv;
     const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -179,9 +181,9 @@ __device__ __noinline__ void fused_combine(const CombineView a, int64_t row, int
                      lane * VPL;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) dst[v] = acc[h][v] / lsum[h];
-        if (lane == 0) a.lse2[row * G + h] = M[h] + log2f(lsum[h]);
+        if (lane == 0) a.lse2[arow * G + h] = M[h] + log2f(lsum[h]);
     }
-    if (lane == 0) a.row_done[row] = 0;
+    if (lane == 0) a.row_done[arow] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -289,7 +291,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     // tiles are walked with (row, tile-in-row) counters: no divisions in the loop
     const int tpr = a.tiles_per_row;
     auto issue = [&](int64_t row, int tile, int stage) {  // lane 0 only
-        const int y = (int)(row * a.max_ctx + tile * T);
+        const int y = (int)((a.row0 + row) * a.max_ctx + tile * T);
         unsigned char* dst = wbuf + (size_t)stage * C::STAGE_BYTES;
         mbar_expect_tx(&bars[stage], C::STAGE_BYTES);
 #pragma unroll
@@ -334,7 +336,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         }
         if (a.row_done) {
             const CombineView cv{a.part_o, a.part_ml, a.row_done, a.out, a.lse2,
-                                 a.n_tiles_total, a.total_warps, a.tiles_per_row,
+                                 a.n_tiles_total, a.total_warps, a.row0, a.tiles_per_row,
                                  a.n_kv, a.batch, a.n_layers, a.n_q};
             fused_combine<D, G>(cv, row, lane);
         }
@@ -352,8 +354,8 @@ __global__ void __launch_bounds__(WARPS * 32)
         if (row != cur_row) {
             if (cur_row >= 0) flush(cur_row);
             cur_row = row;
-            const int gk = (int)(row % a.n_kv);
-            const int64_t lb = row / a.n_kv;
+            const int gk = (int)((a.row0 + row) % a.n_kv);
+            const int64_t lb = (a.row0 + row) / a.n_kv;
             const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
             const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
                 a.q + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)gk * G + (real ? g : 0)) * D);
@@ -404,7 +406,7 @@ __global__ void __launch_bounds__(WARPS * 32)
             for (int e = 0; e < 2; ++e)
                 if (!real || 8 * i + 2 * t + e >= nvalid) sc[i][e] = -INFINITY;
         if (a.write_logits && real) {
-            float* lg = a.logits + ((size_t)row * a.max_ctx + tok0) * G + g;
+            float* lg = a.logits + ((size_t)(a.row0 + row) * a.logit_ld + tok0) * G + g;
 #pragma unroll
             for (int i = 0; i < 2; ++i)
 #pragma unroll

@@ -24,11 +24,14 @@ struct AttnArgs {
     const uint16_t* k;     // cache buffer [rows][max_ctx][D] (rows = Ly*b*Hkv)
     const uint16_t* v;
     const uint16_t* q;     // [b][Ly][Hq][D]
-    float* logits;         // [rows][max_ctx][G] log2-domain scaled logits (refresh)
+    float* logits;         // [rows][logit_ld][G] log2-domain scaled logits (refresh)
+    int32_t logit_ld;      // token stride of a logits row: max_ctx rounded up to 8, so
+                           // every 128-byte line holds 8 tokens of one row
     float* part_o;         // [slots][G][D]
     float* part_ml;        // [slots][G][2] running max (log2 domain), sum
     uint32_t* status;
-    int64_t n_tiles_total; // rows * tiles_per_row
+    int64_t n_tiles_total; // rows of this launch * tiles_per_row
+    int64_t row0;          // first (layer, sequence, KV head) row of this launch
     int32_t tiles_per_row;
     int32_t L;             // live tokens per row (after the append)
     int32_t max_ctx;
@@ -55,7 +58,8 @@ struct CombineArgs {
 };
 
 struct ScoreArgs {
-    const float* logits;   // [rows][max_ctx][G]
+    const float* logits;   // [rows][logit_ld][G]
+    int32_t logit_ld;
     const float* lse2;     // [Ly][b][Hq]
     kvev_state st;         // caller's state (read)
     float* m_s;            // scratch [b][max_ctx] updated score
@@ -70,6 +74,11 @@ struct ScoreArgs {
     int32_t refresh, age_mode, pool_mean;
     int32_t t;
     float alpha, beta, access_thr;   // access: sum over layers of head-summed p >= access_thr
+    // Refresh steps may score the layers in groups [l0, l1) (each right after
+    // the attention of its layers, while their logits are still in L2); the
+    // EMA state and the access sum are carried between groups in m_s / tot_s.
+    int32_t l0, l1, first_group, last_group;
+    float* tot_s;          // scratch [b][max_ctx]
 };
 
 struct SelectArgs {

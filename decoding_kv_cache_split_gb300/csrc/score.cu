@@ -37,74 +37,101 @@ __device__ __forceinline__ uint32_t order_bits(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Refresh steps: two threads per token (adjacent lanes), each summing the
-// heads of half of the KV heads; lanes cover consecutive tokens so every load
-// instruction reads two 256-byte runs.  The (layer, KV head) logit rows are
-// visited in layer order in batches whose loads are all issued before any is
-// used (kBatch 16-byte loads in flight per thread); each completed layer is
-// combined across the pair with one shuffle and folded into the EMA.
+// Refresh steps: one thread per token, lanes on consecutive tokens (every
+// load instruction of a warp reads 512 contiguous bytes).  The number of KV
+// heads is a template parameter so a layer's heads are an unrolled loop with
+// no index arithmetic; the loads of kLB layers are all issued before any is
+// used, and each layer is folded into the EMA as soon as it is summed.
 constexpr int kRefreshThreads = 128;
 
-template <int G, int kSplit>   // kSplit threads per token (1 or 2)
-__global__ void __launch_bounds__(kRefreshThreads, 4) score_refresh_kernel(const ScoreArgs a) {
-    constexpr int V4 = G / 4;                          // float4 per (layer, KV head)
-    constexpr int kBatch = 16 / V4;                    // (layer, KV head) pairs in flight
-    extern __shared__ float s_lse[];                   // [Ly][Hq] of this sequence
+template <int G, int NKV>
+__global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const ScoreArgs a) {
+    constexpr int V4 = G / 4;                               // float4 per (layer, KV head)
+    constexpr int kLB = NKV * V4 >= 16 ? 1 : (16 / (NKV * V4) > 4 ? 4 : 16 / (NKV * V4));  // layers in flight
+    constexpr int kPerLine = 128 / (G * 4);                 // tokens per 128-byte line
+    extern __shared__ float s_lse[];                        // [l1 - l0][NKV * G]
     griddep_wait();
     griddep_release();
     const int b = blockIdx.y;
-    const int nlse = a.n_layers * a.n_q;
+    const int n_lay = a.l1 - a.l0;
+    const int nlse = n_lay * NKV * G;
     for (int k = threadIdx.x; k < nlse; k += blockDim.x) {
-        const int l = k / a.n_q, h = k % a.n_q;
-        s_lse[k] = a.lse2[((size_t)l * a.batch + b) * a.n_q + h];
+        const int l = k / (NKV * G), h = k % (NKV * G);
+        s_lse[k] = a.lse2[((size_t)(a.l0 + l) * a.batch + b) * a.n_q + h];
     }
     __syncthreads();
-    const int half = kSplit == 2 ? (threadIdx.x & 1) : 0;
-    const int i = (blockIdx.x * kRefreshThreads + threadIdx.x) / kSplit;
-    const bool live = i < a.L;                         // both lanes of a pair agree
-    const int kv_half = a.n_kv / kSplit;               // KV heads per thread
-    const int n_pairs = a.n_layers * kv_half;
+    const int i = blockIdx.x * kRefreshThreads + threadIdx.x;
+    if (i >= a.L) return;
 
-    const size_t si = (size_t)b * a.max_ctx + (live ? i : 0);
-    float m = live ? a.st.score[si] : 0.f;
+    const size_t si = (size_t)b * a.max_ctx + i;
+    float m = a.first_group ? a.st.score[si] : a.m_s[si];
+    float tot = a.first_group ? 0.f : a.tot_s[si];
     const float oma = 1.0f - a.alpha;
     const float inv_hq = 1.0f / (float)a.n_q;
-    float tot = 0.f, s = 0.f;
-    for (int k0 = 0; k0 < n_pairs; k0 += kBatch) {
-        float4 xb[kBatch][V4];
+    const size_t head_stride = (size_t)a.logit_ld * G;                  // one (layer, KV head) row
+    const size_t layer_stride = (size_t)a.batch * NKV * head_stride;
+    const float* base = a.logits + ((size_t)a.l0 * a.batch + b) * NKV * head_stride + (size_t)i * G;
+    const bool drop = i % kPerLine == 0 && i + kPerLine <= a.L;         // this thread drops lines
+
+    for (int l0 = 0; l0 < n_lay; l0 += kLB) {
+        float4 xb[kLB][NKV][V4];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {           // all loads of the batch first ...
-            const int k = k0 + u;
-            const int l = k / kv_half, g = half * kv_half + (k - l * kv_half);
-            const size_t row = ((size_t)l * a.batch + b) * a.n_kv + g;
-            const float4* x = reinterpret_cast<const float4*>(a.logits + (row * a.max_ctx + i) * G);
+        for (int u = 0; u < kLB; ++u)                 // all loads of the batch first ...
 #pragma unroll
-            for (int c = 0; c < V4; ++c)
-                xb[u][c] = (live && k < n_pairs) ? __ldcs(x + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+            for (int g = 0; g < NKV; ++g)
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {           // ... then the arithmetic, in layer order
-            const int k = k0 + u;
-            if (k >= n_pairs) break;
-            const int l = k / kv_half, gl = k - l * kv_half, g = half * kv_half + gl;
-            const float* lg = s_lse + l * a.n_q + g * G;
-            const float* xv = reinterpret_cast<const float*>(&xb[u][0]);
+                for (int c = 0; c < V4; ++c)
+                    xb[u][g][c] = l0 + u < n_lay
+                        ? __ldcs(reinterpret_cast<const float4*>(
+                              base + (size_t)(l0 + u) * layer_stride + g * head_stride) + c)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                const float p = fast_exp2(xv[hh] - lg[hh]);
-                if (a.dbg_probs && live)
-                    a.dbg_probs[(((size_t)b * a.n_layers + l) * a.n_q + g * G + hh) * a.max_ctx + i] = p;
-                s += p;
+        for (int u = 0; u < kLB; ++u) {               // ... then the layers in order
+            const int lr = l0 + u;
+            if (lr >= n_lay) break;
+            const float4* lg = reinterpret_cast<const float4*>(s_lse + lr * NKV * G);
+            float s = 0.f;
+#pragma unroll
+            for (int g = 0; g < NKV; ++g)
+#pragma unroll
+                for (int c = 0; c < V4; ++c) {
+                    const float4 x = xb[u][g][c], e = lg[g * V4 + c];
+                    const float p0 = fast_exp2(x.x - e.x), p1 = fast_exp2(x.y - e.y);
+                    const float p2 = fast_exp2(x.z - e.z), p3 = fast_exp2(x.w - e.w);
+                    if (a.dbg_probs) {
+                        float* dp = a.dbg_probs +
+                                    (((size_t)b * a.n_layers + a.l0 + lr) * a.n_q + g * G + 4 * c) *
+                                        a.max_ctx + i;
+                        dp[0] = p0;
+                        dp[(size_t)a.max_ctx] = p1;
+                        dp[2 * (size_t)a.max_ctx] = p2;
+                        dp[3 * (size_t)a.max_ctx] = p3;
+                    }
+                    s += (p0 + p1) + (p2 + p3);
+                }
+            // The logits are dead once read: drop their L2 lines without
+            // writing them back.  A 128-byte line holds kPerLine tokens of
+            // one (layer, KV head) row (rows start on a line), all loaded by
+            // this warp's load, which has completed since its values were
+            // just used (the discard takes `s` as an operand, so it cannot
+            // move above that use).  The line's first token's thread drops it.
+            if (drop) {
+#pragma unroll
+                for (int g = 0; g < NKV; ++g)
+                    asm volatile("discard.global.L2 [%0], 128;" ::"l"(
+                                     base + (size_t)lr * layer_stride + g * head_stride),
+                                 "f"(s)
+                                 : "memory");
             }
-            if (gl == kv_half - 1) {                 // layer l complete: fold it
-                if (kSplit == 2) s += __shfl_xor_sync(0xffffffffu, s, 1);
-                tot += s;
-                m = fmaf(a.alpha, a.pool_mean ? s * inv_hq : s, oma * m);
-                s = 0.f;
-            }
+            tot += s;
+            m = fmaf(a.alpha, a.pool_mean ? s * inv_hq : s, oma * m);
         }
     }
-    if (!live || half) return;
+    if (!a.last_group) {   // carry the state to the next group of layers
+        a.m_s[si] = m;
+        a.tot_s[si] = tot;
+        return;
+    }
     int t_ref = a.st.t_ref[si];
     const int t_ins = a.st.t_ins[si];
     if (tot >= a.access_thr) t_ref = a.t;   // the clock runs in every age mode
@@ -118,86 +145,53 @@ __global__ void __launch_bounds__(kRefreshThreads, 4) score_refresh_kernel(const
     if (a.dbg_prio) a.dbg_prio[si] = pr + 0.0f;
 }
 
-// Non-refresh steps (and the general one-thread-per-token form).
 template <int G>
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a) {
-    extern __shared__ float s_lse[];  // [Ly][Hq] of this sequence
+void* refresh_kernel_for(int nkv) {
+    switch (nkv) {
+        case 1: return (void*)score_refresh_kernel<G, 1>;
+        case 2: return (void*)score_refresh_kernel<G, 2>;
+        case 4: return (void*)score_refresh_kernel<G, 4>;
+        case 8: return (void*)score_refresh_kernel<G, 8>;
+        default: return nullptr;
+    }
+}
+
+// Non-refresh steps: no probabilities, the state is frozen; one thread per
+// token forms the priority from the stale score, and each block adds up its
+// old tokens' scores (for the new token's mean, taken by the selection).
+__global__ void __launch_bounds__(kScoreThreads) score_stale_kernel(const ScoreArgs a) {
     griddep_wait();
     griddep_release();
     const int b = blockIdx.y;
-    const int nlse = a.n_layers * a.n_q;
-    for (int k = threadIdx.x; k < nlse; k += blockDim.x) {
-        const int l = k / a.n_q, h = k % a.n_q;
-        s_lse[k] = a.lse2[((size_t)l * a.batch + b) * a.n_q + h];
-    }
-    __syncthreads();
-
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const bool live = i < a.L;
     const bool is_new = i == a.L - 1;
     const size_t si = (size_t)b * a.max_ctx + i;
     float old_m = 0.f;
     if (live) {
-        float m = a.st.score[si];
-        int t_ref = a.st.t_ref[si];
+        const float m = a.st.score[si];
+        const int t_ref = a.st.t_ref[si];
         const int t_ins = a.st.t_ins[si];
-        const int pos = a.st.pos[si];
-        if (a.refresh) {
-            const float oma = 1.0f - a.alpha;
-            const float inv_hq = 1.0f / (float)a.n_q;
-            float tot = 0.f;
-            for (int l = 0; l < a.n_layers; ++l) {
-                float s = 0.f;
-                const float* lrow = s_lse + l * a.n_q;
-                for (int g = 0; g < a.n_kv; ++g) {
-                    const size_t row = ((size_t)l * a.batch + b) * a.n_kv + g;
-                    const float* x = a.logits + (row * a.max_ctx + i) * G;
-                    float xv[G];
-                    if constexpr (G == 4) {
-                        const float4 x4 = *reinterpret_cast<const float4*>(x);
-                        xv[0] = x4.x; xv[1] = x4.y; xv[2] = x4.z; xv[3] = x4.w;
-                    } else {
-#pragma unroll
-                        for (int hh = 0; hh < G; ++hh) xv[hh] = x[hh];
-                    }
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh) {
-                        const float p = fast_exp2(xv[hh] - lrow[g * G + hh]);
-                        if (a.dbg_probs)
-                            a.dbg_probs[(((size_t)b * a.n_layers + l) * a.n_q + g * G + hh) *
-                                            a.max_ctx + i] = p;
-                        s += p;
-                    }
-                }
-                tot += s;
-                const float sp = a.pool_mean ? s * inv_hq : s;
-                m = fmaf(a.alpha, sp, oma * m);
-            }
-            if (tot >= a.access_thr) t_ref = a.t;   // the clock runs in every age mode
-        } else if (!is_new) {
-            old_m = m;
-        }
+        if (!is_new) old_m = m;
         const int age = a.t - (a.age_mode == KVEV_AGE_SINCE_ACCESS ? t_ref : t_ins);
         const float pr = age == 0 ? 0.0f : (1.0f - m) * -expm1f(-a.beta * (float)age);
         a.keys[si] = order_bits(pr);
         a.m_s[si] = m;
         a.tref_s[si] = t_ref;
         a.tins_s[si] = t_ins;
-        a.pos_s[si] = pos;
+        a.pos_s[si] = a.st.pos[si];
         if (a.dbg_prio) a.dbg_prio[si] = pr + 0.0f;
     }
-    if (!a.refresh) {  // deterministic block sum of the old tokens' scores
-        __shared__ float red[kScoreThreads / 32];
-        float v = old_m;
+    __shared__ float red[kScoreThreads / 32];   // deterministic block sum
+    float v = old_m;
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float s = 0.f;
-            for (int k = 0; k < kScoreThreads / 32; ++k) s += red[k];
-            a.msum_part[(size_t)b * gridDim.x + blockIdx.x] = s;
-        }
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = 0.f;
+        for (int k = 0; k < kScoreThreads / 32; ++k) s += red[k];
+        a.msum_part[(size_t)b * gridDim.x + blockIdx.x] = s;
     }
 }
 
@@ -205,24 +199,20 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
 
 cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStream_t s) {
     if (a.refresh) {
-        const int split = a.n_kv % 2 == 0 ? 2 : 1;
-        const int nb = (a.L * split + kRefreshThreads - 1) / kRefreshThreads;
+        const int nb = (a.L + kRefreshThreads - 1) / kRefreshThreads;
         *n_blocks = nb;
         const dim3 grid(nb, a.batch);
-        const size_t smem = sizeof(float) * (size_t)a.n_layers * a.n_q;
-        void (*kern)(ScoreArgs) = nullptr;
-        if (group == 4) kern = split == 2 ? score_refresh_kernel<4, 2> : score_refresh_kernel<4, 1>;
-        if (group == 8) kern = split == 2 ? score_refresh_kernel<8, 2> : score_refresh_kernel<8, 1>;
+        const size_t smem = sizeof(float) * (size_t)(a.l1 - a.l0) * a.n_q;
+        void* kern = group == 4 ? refresh_kernel_for<4>(a.n_kv)
+                   : group == 8 ? refresh_kernel_for<8>(a.n_kv) : nullptr;
         if (!kern) return cudaErrorInvalidValue;
-        return launch_pdl(kern, grid, dim3(kRefreshThreads), smem, s, a);
+        return launch_pdl(reinterpret_cast<void (*)(ScoreArgs)>(kern), grid,
+                          dim3(kRefreshThreads), smem, s, a);
     }
     const int nb = (a.L + kScoreThreads - 1) / kScoreThreads;
     *n_blocks = nb;
-    const dim3 grid(nb, a.batch);
-    const size_t smem = sizeof(float) * (size_t)a.n_layers * a.n_q;
-    if (group == 4) return launch_pdl(score_kernel<4>, grid, dim3(kScoreThreads), smem, s, a);
-    if (group == 8) return launch_pdl(score_kernel<8>, grid, dim3(kScoreThreads), smem, s, a);
-    return cudaErrorInvalidValue;
+    (void)group;
+    return launch_pdl(score_stale_kernel, dim3(nb, a.batch), dim3(kScoreThreads), 0, s, a);
 }
 
 }  // namespace kvev
