@@ -57,7 +57,6 @@ struct Workspace {
     int32_t* pos_s = nullptr;
     float* msum_part = nullptr;
     float* tot_s = nullptr;
-    int32_t* row_done = nullptr;
     uint32_t* status = nullptr;
     uint16_t* stg_q = nullptr;
     uint16_t* stg_k = nullptr;
@@ -92,7 +91,6 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base)
     w.pos_s = (int32_t*)take(ctx * 4);
     w.msum_part = (float*)take((size_t)L.batch * nblk * 4);
     w.tot_s = (float*)take(ctx * 4);
-    w.row_done = (int32_t*)take(rows * 4);
     w.status = (uint32_t*)take(4);
     const size_t qn = (size_t)L.batch * L.n_layers * L.n_q_heads * L.head_dim;
     const size_t kn = (size_t)L.batch * L.n_layers * L.n_kv_heads * L.head_dim;
@@ -438,9 +436,6 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     at.total_warps = c->attn_warps;
     at.write_logits = refresh ? 1 : 0;
     at.q_scale = (float)(1.4426950408889634 / sqrt((double)Ly.head_dim));
-    at.row_done = c->ws.row_done;   // the split combine runs inside the attention kernel
-    at.out = out;
-    at.lse2 = c->ws.lse2;
 
     ScoreArgs sc{};
     sc.logits = c->ws.logits;
@@ -490,6 +485,23 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
         rc = timed_launch(c, kProfAttn, s, "attention", [&] {
             return launch_attention(at, Ly.head_dim, G, c->attn_grid, s);
         });
+        if (rc != KVEV_OK) return rc;
+        CombineArgs cb{};   // merge the split: outputs and per-head log2-sum-exp
+        cb.sp.part_o = c->ws.part_o;
+        cb.sp.part_ml = c->ws.part_ml;
+        cb.sp.n_tiles = at.n_tiles_total;
+        cb.sp.row0 = at.row0;
+        cb.sp.total_warps = c->attn_warps;
+        cb.sp.tiles_per_row = tiles_per_row;
+        cb.n_rows = (int32_t)((l1 - l0) * rows_per_layer);
+        cb.out = out;
+        cb.lse2 = c->ws.lse2;
+        cb.n_layers = Ly.n_layers;
+        cb.batch = Ly.batch;
+        cb.n_kv = Ly.n_kv_heads;
+        cb.n_q = Ly.n_q_heads;
+        rc = timed_launch(c, kProfCombine, s, "combine",
+                          [&] { return launch_combine(cb, Ly.head_dim, G, s); });
         if (rc != KVEV_OK) return rc;
         if (!refresh) continue;
         sc.l0 = l0;

@@ -25,10 +25,10 @@
 //    two contractions of a tile run on mma.sync m16n8k16 (bf16 in, fp32
 //    accumulate), which removes most of the per-token instructions.
 //  * Softmax partials (running max, sum, output) of each warp's piece of a
-//    row go to a slot; the last warp to finish a row (an atomic counter per
-//    row) merges the row's partials and writes the output and the per-head
-//    log2-sum-exp.  A standalone combine kernel does the same for callers
-//    without counters.
+//    row go to a slot.  On refresh steps the scoring kernel merges them (it
+//    needs the per-head log2-sum-exp anyway); otherwise the combine kernel
+//    below does.  Merging inside this kernel (last warp of a row) stalled
+//    that warp's TMA pipeline and cost ~3% of the kernel.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -85,106 +85,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-
-// Warps of the split whose tile range is empty write no partial.
-__device__ __forceinline__ bool warp_has_tiles(int64_t w, int64_t N, int64_t W) {
-    return w * N / W != (w + 1) * N / W;
-}
-
-// Called by every warp after it wrote its partial of `row` (counted from the
-// launch's first row): the last of the row's warps to arrive merges all of
-// the row's partials into the output and the log2-sum-exp, then resets the
-// row's counter for the next launch.
-struct CombineView {   // what the fused combine needs, passed by value
-    const float* part_o;
-    const float* part_ml;
-    int32_t* row_done;
-    float* out;
-    float* lse2;
-    int64_t N, W, row0;
-    int32_t tiles_per_row, n_kv, batch, n_layers, n_q;
-};
-
-template <int D, int G>
-__device__ __noinline__ void fused_combine(const CombineView a, int64_t row, int lane) {
-    constexpr int VPL = D / 32;   // output dims per lane
-    const int64_t N = a.N, W = a.W;
-    const int64_t first = row * a.tiles_per_row, last = first + a.tiles_per_row - 1;
-    const int64_t w_lo = ((first + 1) * W - 1) / N, w_hi = ((last + 1) * W - 1) / N;
-    __threadfence();   // this warp's partial is visible before it is counted
-    __syncwarp();
-    int is_last = 0;
-    if (lane == 0) {
-        int need = 0;
-        for (int64_t w = w_lo; w <= w_hi; ++w) need += warp_has_tiles(w, N, W);
-        is_last = atomicAdd(&a.row_done[a.row0 + row], 1) == need - 1;
-    }
-    if (!__shfl_sync(kFull, is_last, 0)) return;
-    __threadfence();
-
-    float M[G], lsum[G], acc[G][VPL];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        M[h] = -INFINITY;
-        lsum[h] = 0.f;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) acc[h][v] = 0.f;
-    }
-    for (int64_t base = w_lo; base <= w_hi; base += 32) {   // segments, 32 at a time
-        const int64_t w = base + lane;
-        const bool valid = w <= w_hi && warp_has_tiles(w, N, W);
-        float mj[G], lj[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            mj[h] = valid ? __ldcg(a.part_ml + ((w + row) * G + h) * 2) : -INFINITY;
-            lj[h] = valid ? __ldcg(a.part_ml + ((w + row) * G + h) * 2 + 1) : 0.f;
-        }
-        float Mn[G], fj[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float mm = mj[h];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(kFull, mm, o));
-            Mn[h] = fmaxf(M[h], mm);
-            const float fo = M[h] == -INFINITY ? 0.f : fast_exp2(M[h] - Mn[h]);
-            lsum[h] *= fo;
-#pragma unroll
-            for (int v = 0; v < VPL; ++v) acc[h][v] *= fo;
-            M[h] = Mn[h];
-            fj[h] = valid ? fast_exp2(mj[h] - Mn[h]) : 0.f;
-            float ls = lj[h] * fj[h];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(kFull, ls, o);
-            lsum[h] += ls;
-        }
-        unsigned vm = __ballot_sync(kFull, valid);
-        while (vm) {
-            const int j = __ffs(vm) - 1;
-            vm &= vm - 1;
-            const int64_t slot = base + j + row;
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float f = __shfl_sync(kFull, fj[h], j);
-                const float* src = a.part_o + (slot * G + h) * D + lane * VPL;
-#pragma unroll
-                for (int v = 0; v < VPL; ++v) acc[h][v] += __ldcg(src + v) * f;
-            }
-        }
-    }
-    const int64_t arow = a.row0 + row;
-    const int g = (int)(arow % a.n_kv);
-    const int64_t lb = arow / a.n_kv;
-    const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        float* dst = a.out + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)g * G + h) * D +
-                     lane * VPL;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) dst[v] = acc[h][v] / lsum[h];
-        if (lane == 0) a.lse2[arow * G + h] = M[h] + log2f(lsum[h]);
-    }
-    if (lane == 0) a.row_done[arow] = 0;
-}
 
 // ---------------------------------------------------------------------------
 // The two contractions of a 16-token tile on mma.sync m16n8k16 (bf16 in,
@@ -334,12 +234,6 @@ __global__ void __launch_bounds__(WARPS * 32)
                 pml[1] = l;
             }
         }
-        if (a.row_done) {
-            const CombineView cv{a.part_o, a.part_ml, a.row_done, a.out, a.lse2,
-                                 a.n_tiles_total, a.total_warps, a.row0, a.tiles_per_row,
-                                 a.n_kv, a.batch, a.n_layers, a.n_q};
-            fused_combine<D, G>(cv, row, lane);
-        }
     };
 
     bool ok = true;
@@ -485,37 +379,56 @@ __global__ void __launch_bounds__(WARPS * 32)
     flush(cur_row);
 }
 
+// Split combine: one CTA per row of the launch, thread d owns output dim d
+// of every head of the row.  All of a row's segments are loaded in batches
+// of kSeg before any is used, and merged with a running max (one pass).
 template <int D, int G>
 __global__ void __launch_bounds__(D) combine_kernel(const CombineArgs a) {
+    constexpr int kSeg = 8;
     griddep_wait();
     griddep_release();
-    const int row = blockIdx.x, hh = blockIdx.y, d = threadIdx.x;
-    const int64_t N = a.n_tiles_total;
-    const int64_t W = a.total_warps;
-    const int64_t first = (int64_t)row * a.tiles_per_row;
-    const int64_t last = first + a.tiles_per_row - 1;
-    // warp owning tile x: the largest w with floor(w*N/W) <= x
-    const int w_lo = (int)(((first + 1) * W - 1) / N);
-    const int w_hi = (int)(((last + 1) * W - 1) / N);
-    float M = -INFINITY;
-    for (int w = w_lo; w <= w_hi; ++w) {
-        if ((int64_t)w * N / W == (int64_t)(w + 1) * N / W) continue;  // empty warp
-        M = fmaxf(M, a.part_ml[(((int64_t)w + row) * G + hh) * 2]);
+    const SplitPartials& sp = a.sp;
+    const int64_t r = blockIdx.x;                 // row of the launch
+    const int d = threadIdx.x;
+    int64_t lo, hi;
+    split_warps_of_row(sp, r, &lo, &hi);
+    float M[G], Ls[G], acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) { M[h] = -INFINITY; Ls[h] = 0.f; acc[h] = 0.f; }
+    for (int64_t w0 = lo; w0 <= hi; w0 += kSeg) {
+        float m[kSeg][G], l[kSeg][G], o[kSeg][G];
+#pragma unroll
+        for (int j = 0; j < kSeg; ++j) {
+            const int64_t w = w0 + j;
+            const bool ok = w <= hi && split_warp_has_tiles(w, sp.n_tiles, sp.total_warps);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                m[j][h] = ok ? __ldcg(sp.part_ml + ((w + r) * G + h) * 2) : -INFINITY;
+                l[j][h] = ok ? __ldcg(sp.part_ml + ((w + r) * G + h) * 2 + 1) : 0.f;
+                o[j][h] = ok ? __ldcg(sp.part_o + ((w + r) * G + h) * D + d) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kSeg; ++j)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                if (m[j][h] == -INFINITY) continue;
+                const float mn = fmaxf(M[h], m[j][h]);
+                const float fo = fast_exp2(M[h] - mn), fj = fast_exp2(m[j][h] - mn);
+                Ls[h] = Ls[h] * fo + l[j][h] * fj;
+                acc[h] = acc[h] * fo + o[j][h] * fj;
+                M[h] = mn;
+            }
     }
-    float lsum = 0.f, acc = 0.f;
-    for (int w = w_lo; w <= w_hi; ++w) {
-        if ((int64_t)w * N / W == (int64_t)(w + 1) * N / W) continue;
-        const int64_t slot = (int64_t)w + row;
-        const float f = fast_exp2(a.part_ml[(slot * G + hh) * 2] - M);
-        lsum += a.part_ml[(slot * G + hh) * 2 + 1] * f;
-        acc += a.part_o[(slot * G + hh) * D + d] * f;
+    const int64_t arow = sp.row0 + r;
+    const int g = (int)(arow % a.n_kv);
+    const int64_t lb = arow / a.n_kv;
+    const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        a.out[(((size_t)b * a.n_layers + l) * a.n_q + (size_t)g * G + h) * D + d] = acc[h] / Ls[h];
+        if (d == 0) a.lse2[arow * G + h] = M[h] + log2f(Ls[h]);
     }
-    const int g = row % a.n_kv;
-    const int lb = row / a.n_kv;
-    const int b = lb % a.batch, l = lb / a.batch;
-    const int h = g * G + hh;
-    a.out[(((size_t)b * a.n_layers + l) * a.n_q + h) * D + d] = acc / lsum;
-    if (d == 0) a.lse2[(size_t)row * G + hh] = M + log2f(lsum);
 }
 
 #ifndef KVEV_ATTN_STAGES
@@ -604,7 +517,7 @@ cudaError_t launch_attention(const AttnArgs& a, int head_dim, int group, int gri
 }
 
 cudaError_t launch_combine(const CombineArgs& a, int head_dim, int group, cudaStream_t s) {
-    const dim3 grid(a.n_layers * a.batch * a.n_kv, group);
+    const dim3 grid(a.n_rows);
     if (group == 4 && head_dim == 128) return launch_pdl(combine_kernel<128, 4>, grid, dim3(128), 0, s, a);
     if (group == 4 && head_dim == 64) return launch_pdl(combine_kernel<64, 4>, grid, dim3(64), 0, s, a);
     return cudaErrorInvalidValue;

@@ -39,28 +39,45 @@ struct AttnArgs {
     int32_t total_warps;
     int32_t write_logits;
     float q_scale;         // log2(e) / sqrt(D)
-    // Fused combine (optional): when row_done is set, the last warp to finish
-    // a row merges that row's partials into out / lse2 and resets its counter.
-    int32_t* row_done;     // [rows] zero-initialised counters, or null
-    float* out;            // [b][Ly][Hq][D]
-    float* lse2;           // [rows][G]
 };
 
+// Where one attention launch left its split partials: warp w's piece of the
+// launch's row r (rows counted from row0) is slot w + r.
+struct SplitPartials {
+    const float* part_o;   // [slots][G][D]
+    const float* part_ml;  // [slots][G][2]
+    int64_t n_tiles;       // tiles of the launch
+    int64_t row0;
+    int32_t total_warps;
+    int32_t tiles_per_row;
+};
+
+// Warps of the split whose tile range is empty write no partial.
+__device__ __forceinline__ bool split_warp_has_tiles(int64_t w, int64_t N, int64_t W) {
+    return w * N / W != (w + 1) * N / W;
+}
+// The warps whose tile ranges meet launch row r: [*lo, *hi] (some may be empty).
+__device__ __forceinline__ void split_warps_of_row(const SplitPartials& p, int64_t r,
+                                                   int64_t* lo, int64_t* hi) {
+    const int64_t first = r * p.tiles_per_row, last = first + p.tiles_per_row - 1;
+    const int64_t W = p.total_warps, N = p.n_tiles;
+    *lo = ((first + 1) * W - 1) / N;   // the largest w with floor(w N / W) <= tile
+    *hi = ((last + 1) * W - 1) / N;
+}
+
 struct CombineArgs {
-    const float* part_o;
-    const float* part_ml;
+    SplitPartials sp;      // the attention launch to merge (its rows from sp.row0)
+    int32_t n_rows;        // rows of that launch
     float* out;            // [b][Ly][Hq][D]
     float* lse2;           // [rows][G] = [Ly][b][Hq]
-    int64_t n_tiles_total;
-    int32_t tiles_per_row;
-    int32_t total_warps;
     int32_t n_layers, batch, n_kv, n_q;
 };
+
 
 struct ScoreArgs {
     const float* logits;   // [rows][logit_ld][G]
     int32_t logit_ld;
-    const float* lse2;     // [Ly][b][Hq]
+    const float* lse2;     // [Ly][b][Hq] log2-sum-exp from the split combine
     kvev_state st;         // caller's state (read)
     float* m_s;            // scratch [b][max_ctx] updated score
     int32_t* tref_s;       // scratch updated t_ref

@@ -138,13 +138,15 @@ extern "C" kvev_status kvev_attend_noalloc(const kvev_layout* L, const void* q, 
     if (e != cudaSuccess) return report_error(KVEV_ECUDA, cudaGetErrorString(e));
 
     CombineArgs cb{};
-    cb.part_o = part_o;
-    cb.part_ml = part_ml;
+    cb.sp.part_o = part_o;
+    cb.sp.part_ml = part_ml;
+    cb.sp.n_tiles = at.n_tiles_total;
+    cb.sp.row0 = 0;
+    cb.sp.total_warps = at.total_warps;
+    cb.sp.tiles_per_row = tiles_per_row;
+    cb.n_rows = (int32_t)rows;
     cb.out = out;
     cb.lse2 = lse2;
-    cb.n_tiles_total = at.n_tiles_total;
-    cb.tiles_per_row = tiles_per_row;
-    cb.total_warps = at.total_warps;
     cb.n_layers = L->n_layers;
     cb.batch = L->batch;
     cb.n_kv = L->n_kv_heads;

@@ -2,8 +2,9 @@
 // access clock, eviction priority and its sortable key.
 //
 //  p_h(i)   = exp2(logit2_h(i) - lse2_h)      (the softmax of the attention
-//             kernel, from the logits it kept; "What Matters for Aggressive
-//             Decoding-Time KV Eviction?" Sec. 3.1 Eq. (1))
+//             kernel, from the logits it kept and the log2-sum-exp of the
+//             split combine; "What Matters for Aggressive Decoding-Time KV
+//             Eviction?" Sec. 3.1 Eq. (1))
 //  s_l(i)   = sum_h p_h(i)   (or the head mean, Eq. (1))
 //  m(i)    <- alpha * s_l(i) + (1 - alpha) * m(i) for l = 0 .. Ly-1 in order
 //             (kv-cache-docs "ema-eviction" EMA table; Appendix E "Layer
