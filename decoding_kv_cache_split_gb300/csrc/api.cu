@@ -40,7 +40,10 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // token stride of a logits row: whole 128-byte lines per row
 int logit_ld(int max_ctx) { return (max_ctx + 7) / 8 * 8; }
 
-enum { kProfAppend = 0, kProfAttn, kProfCombine, kProfScore, kProfSelect, kProfCompact, kProfInit };
+enum {
+    kProfAppend = 0, kProfAttn, kProfCombine, kProfScore, kProfSelect, kProfCompact, kProfInit,
+    kProfReadmit
+};
 
 // Target size of the logits of one group of layers (see kvev_step).
 constexpr int64_t kLogitGroupBytes = int64_t(1) << 40;
@@ -64,6 +67,13 @@ struct Workspace {
     float* stg_out = nullptr;
     int32_t* stg_ret = nullptr;
     int32_t* stg_nret = nullptr;
+    // block-granular mode: scratch copies of the block state, [batch][pps]
+    int32_t* lid_s = nullptr;
+    int32_t* len_s = nullptr;
+    int32_t* page_s = nullptr;
+    int32_t* tokens = nullptr;        // [batch] live tokens after the append
+    int32_t* sel = nullptr;           // [batch][budget] kept block slots
+    int32_t* readmit_page = nullptr;  // [1]
     size_t bytes = 0;
 };
 
@@ -100,6 +110,13 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base)
     w.stg_out = (float*)take(qn * 4);
     w.stg_ret = (int32_t*)take((size_t)L.batch * budget * 4);
     w.stg_nret = (int32_t*)take((size_t)L.batch * 4);
+    const size_t units = (size_t)L.batch * (L.max_ctx / L.page_tokens);
+    w.lid_s = (int32_t*)take(units * 4);
+    w.len_s = (int32_t*)take(units * 4);
+    w.page_s = (int32_t*)take(units * 4);
+    w.tokens = (int32_t*)take((size_t)L.batch * 4);
+    w.sel = (int32_t*)take((size_t)L.batch * budget * 4);
+    w.readmit_page = (int32_t*)take(4);
     w.bytes = off;
     return w;
 }
@@ -117,11 +134,17 @@ kvev_status check_layout(const kvev_layout* L, int64_t budget) {
         return fail(KVEV_EUNSUPPORTED, "layout: query heads per KV head %d (supported: 4)",
                     L->n_q_heads / L->n_kv_heads);
     if (L->max_ctx < 2) return fail(KVEV_EINVAL, "layout: max_ctx must be >= 2");
-    if (L->page_tokens != 1)
-        return fail(KVEV_EUNSUPPORTED, "layout: page_tokens %d (supported: 1)", L->page_tokens);
+    if (L->page_tokens != 1 && L->page_tokens != kTile)
+        return fail(KVEV_EUNSUPPORTED, "layout: page_tokens %d (supported: 1, %d)", L->page_tokens,
+                    kTile);
     if (L->kv_dtype != KVEV_BF16) return fail(KVEV_EUNSUPPORTED, "layout: kv_dtype must be BF16");
-    if (budget < 1 || budget >= L->max_ctx)
-        return fail(KVEV_EINVAL, "budget %lld must be in [1, max_ctx)", (long long)budget);
+    if (L->max_ctx % L->page_tokens != 0)
+        return fail(KVEV_EINVAL, "layout: max_ctx %d must be a multiple of page_tokens %d",
+                    L->max_ctx, L->page_tokens);
+    const int64_t units = L->max_ctx / L->page_tokens;   // tokens, or pages per sequence
+    if (budget < 1 || budget >= units)
+        return fail(KVEV_EINVAL, "budget %lld must be in [1, %lld)", (long long)budget,
+                    (long long)units);
     return KVEV_OK;
 }
 
@@ -146,6 +169,7 @@ struct kvev_ctx {
     int32_t age_mode = KVEV_AGE_SINCE_INSERT, pool = KVEV_POOL_SUM;
     int32_t group = 4;
     int32_t len = 0, prefill_len = 0;
+    std::vector<int32_t> ub_blocks;   // block mode: upper bound of each sequence's live blocks
     int64_t step = 0;
     bool begun = false;
     int device = 0, num_sms = 0;
@@ -222,11 +246,14 @@ kvev_status check_status_word(kvev_ctx* c, cudaStream_t s) {
     cudaError_t e = cudaMemcpyAsync(&host, c->ws.status, 4, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "device status");
-    if (host & kStatusTimeout) {
+    if (host != 0) {
         cudaMemsetAsync(c->ws.status, 0, 4, s);
         cudaStreamSynchronize(s);
-        return fail(KVEV_ETIMEOUT, "a device wait exceeded its iteration limit");
     }
+    if (host & kStatusTimeout)
+        return fail(KVEV_ETIMEOUT, "a device wait exceeded its iteration limit");
+    if (host & kStatusNoPage)
+        return fail(KVEV_ESTATE, "a sequence had no free page for a new or re-admitted block");
     return KVEV_OK;
 }
 
@@ -329,6 +356,8 @@ kvev_status kvev_configure(kvev_ctx* c, int32_t age_mode, int32_t pool) {
 
 kvev_status kvev_begin(kvev_ctx* c, int32_t prefill_len) {
     if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (c->lay.page_tokens != 1)
+        return fail(KVEV_ESTATE, "a block-granular context starts with kvev_paged_begin");
     if (prefill_len < 0 || prefill_len >= c->lay.max_ctx)
         return fail(KVEV_EINVAL, "prefill_len %d must be in [0, max_ctx)", prefill_len);
     c->len = prefill_len;
@@ -379,6 +408,8 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
         !aligned16(out))
         return fail(KVEV_EINVAL, "q, k_new, v_new, out and the cache buffers must be 16-byte aligned");
     if (!c->begun) return fail(KVEV_ESTATE, "kvev_begin must come before the first step");
+    if (c->lay.page_tokens != 1)
+        return fail(KVEV_ESTATE, "a block-granular context steps with kvev_paged_step");
     if (step != c->step + 1)
         return fail(KVEV_ESTATE, "step %lld out of order (expected %lld)", (long long)step,
                     (long long)(c->step + 1));
@@ -436,6 +467,7 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     at.total_warps = c->attn_warps;
     at.write_logits = refresh ? 1 : 0;
     at.q_scale = (float)(1.4426950408889634 / sqrt((double)Ly.head_dim));
+    at.view_tokens = (int64_t)Ly.n_layers * Ly.batch * Ly.n_kv_heads * Ly.max_ctx;
 
     ScoreArgs sc{};
     sc.logits = c->ws.logits;
@@ -593,6 +625,246 @@ kvev_status kvev_step_host(kvev_ctx* c, const void* q_host, const void* k_new_ho
                             cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
     return check_status_word(c, s);
+}
+
+// ---- block-granular (paged) mode ------------------------------------------
+
+}  // extern "C"
+
+namespace {
+
+kvev_status check_paged(kvev_ctx* c, const kvev_paged_cache* pc, const kvev_block_state* bs) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (c->lay.page_tokens == 1)
+        return fail(KVEV_ESTATE, "a token-granular context: use kvev_begin / kvev_step");
+    if (!pc || !bs) return fail(KVEV_EINVAL, "NULL argument");
+    if (!pc->k_pool || !pc->v_pool || !pc->block_table || !pc->n_blocks || !pc->free_pages ||
+        !pc->n_free || !pc->next_lid)
+        return fail(KVEV_EINVAL, "paged cache has a NULL array");
+    if (!aligned16(pc->k_pool) || !aligned16(pc->v_pool))
+        return fail(KVEV_EINVAL, "the page pools must be 16-byte aligned");
+    if (pc->pages_per_seq != c->lay.max_ctx / c->lay.page_tokens)
+        return fail(KVEV_EINVAL, "pages_per_seq %d != max_ctx / page_tokens = %d", pc->pages_per_seq,
+                    c->lay.max_ctx / c->lay.page_tokens);
+    if (pc->n_backing < 0) return fail(KVEV_EINVAL, "n_backing must be >= 0");
+    if (pc->n_backing > 0 && (!pc->backing_k || !pc->backing_v || !aligned16(pc->backing_k) ||
+                              !aligned16(pc->backing_v)))
+        return fail(KVEV_EINVAL, "backing tier: NULL or unaligned buffer");
+    if (!bs->score || !bs->t_ins || !bs->t_ref || !bs->lid || !bs->len || !bs->table)
+        return fail(KVEV_EINVAL, "block state has a NULL array");
+    if (bs->table_len < pc->n_backing || bs->table_len < 1)
+        return fail(KVEV_EINVAL, "table_len %d must be >= max(1, n_backing %d)", bs->table_len,
+                    pc->n_backing);
+    return KVEV_OK;
+}
+
+PagedArgs paged_args(kvev_ctx* c, const kvev_paged_cache* pc, const kvev_block_state* bs, int t,
+                     bool refresh) {
+    PagedArgs a{};
+    a.c = *pc;
+    a.st = *bs;
+    a.tokens = c->ws.tokens;
+    a.m_s = c->ws.m_s;
+    a.tref_s = c->ws.tref_s;
+    a.tins_s = c->ws.tins_s;
+    a.lid_s = c->ws.lid_s;
+    a.len_s = c->ws.len_s;
+    a.page_s = c->ws.page_s;
+    a.keys = c->ws.keys;
+    a.sel = c->ws.sel;
+    a.readmit_page = c->ws.readmit_page;
+    a.status = c->ws.status;
+    a.batch = c->lay.batch;
+    a.n_layers = c->lay.n_layers;
+    a.n_kv = c->lay.n_kv_heads;
+    a.n_q = c->lay.n_q_heads;
+    a.head_dim = c->lay.head_dim;
+    a.page = c->lay.page_tokens;
+    a.budget = (int)c->budget;
+    a.t = t;
+    a.refresh = refresh ? 1 : 0;
+    a.age_mode = c->age_mode;
+    a.pool_mean = c->pool == KVEV_POOL_MEAN ? 1 : 0;
+    a.alpha = c->alpha;
+    a.beta = c->beta;
+    a.dbg_prio = c->dbg_prio;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvev_status kvev_paged_begin(kvev_ctx* c, const kvev_paged_cache* pc, const kvev_block_state* bs,
+                             int32_t prefill_tokens, void* stream) {
+    kvev_status rc = check_paged(c, pc, bs);
+    if (rc != KVEV_OK) return rc;
+    const int P = c->lay.page_tokens, pps = pc->pages_per_seq;
+    if (prefill_tokens <= 0 || prefill_tokens % P != 0)
+        return fail(KVEV_EINVAL, "prefill_tokens %d must be a positive multiple of %d",
+                    prefill_tokens, P);
+    const int nb0 = prefill_tokens / P;
+    if (nb0 + 1 > pps)
+        return fail(KVEV_EINVAL, "%d prefill blocks leave no free page (pages_per_seq %d)", nb0,
+                    pps);
+    cudaStream_t s = (cudaStream_t)stream;
+    const PagedArgs a = paged_args(c, pc, bs, 0, true);
+    rc = timed_launch(c, kProfInit, s, "paged begin", [&] { return launch_paged_begin(a, nb0, s); });
+    if (rc != KVEV_OK) return rc;
+    c->len = prefill_tokens;
+    c->prefill_len = prefill_tokens;
+    c->ub_blocks.assign(c->lay.batch, nb0);
+    c->step = 0;
+    c->begun = true;
+    return KVEV_OK;
+}
+
+kvev_status kvev_paged_step(kvev_ctx* c, const void* q, const void* k_new, const void* v_new,
+                            const kvev_paged_cache* pc, const kvev_block_state* bs, int64_t step,
+                            float* out, int32_t* retained_lid, int32_t* n_retained,
+                            void* stream) {
+    kvev_status rc = check_paged(c, pc, bs);
+    if (rc != KVEV_OK) return rc;
+    if (!q || !k_new || !v_new || !out || !retained_lid || !n_retained)
+        return fail(KVEV_EINVAL, "NULL argument");
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out))
+        return fail(KVEV_EINVAL, "q, k_new, v_new and out must be 16-byte aligned");
+    if (!c->begun) return fail(KVEV_ESTATE, "kvev_paged_begin must come before the first step");
+    if (step != c->step + 1)
+        return fail(KVEV_ESTATE, "step %lld out of order (expected %lld)", (long long)step,
+                    (long long)(c->step + 1));
+    const int pps = pc->pages_per_seq;
+    int ub = 0;   // live blocks of any sequence after the append, at most
+    for (int b = 0; b < c->lay.batch; ++b) {
+        if (c->ub_blocks[b] + 1 > pps)
+            return fail(KVEV_EINVAL, "sequence %d may hold %d blocks: no page left for a new one",
+                        b, c->ub_blocks[b]);
+        ub = c->ub_blocks[b] + 1 > ub ? c->ub_blocks[b] + 1 : ub;
+    }
+
+    cudaStream_t s = (cudaStream_t)stream;
+    const kvev_layout& Ly = c->lay;
+    const int G = c->group;
+    const int t = (int)step;
+    bool refresh = true;
+    if (c->refresh_mode == KVEV_REFRESH_LAZY) refresh = (t - 1) % c->refresh_period == 0;
+    if (c->refresh_mode == KVEV_REFRESH_FROZEN) refresh = t == 1;
+    PagedArgs pa = paged_args(c, pc, bs, t, refresh);
+    pa.sel = c->ws.sel;
+    pa.n_sel = n_retained;
+    pa.retained_lid = retained_lid;
+
+    rc = timed_launch(c, kProfAppend, s, "paged append", [&] {
+        return launch_paged_append(pa, (const uint16_t*)k_new, (const uint16_t*)v_new, s);
+    });
+    if (rc != KVEV_OK) return rc;
+
+    const int64_t rows = (int64_t)Ly.n_layers * Ly.batch * Ly.n_kv_heads;
+    AttnArgs at{};
+    at.k = (const uint16_t*)pc->k_pool;
+    at.v = (const uint16_t*)pc->v_pool;
+    at.q = (const uint16_t*)q;
+    at.logits = c->ws.logits;
+    at.logit_ld = logit_ld(Ly.max_ctx);
+    at.part_o = c->ws.part_o;
+    at.part_ml = c->ws.part_ml;
+    at.status = c->ws.status;
+    at.row0 = 0;
+    at.tiles_per_row = ub;
+    at.n_tiles_total = rows * ub;
+    at.L = ub * kTile;
+    at.max_ctx = Ly.max_ctx;
+    at.n_layers = Ly.n_layers;
+    at.batch = Ly.batch;
+    at.n_kv = Ly.n_kv_heads;
+    at.n_q = Ly.n_q_heads;
+    at.total_warps = c->attn_warps;
+    at.write_logits = refresh ? 1 : 0;
+    at.q_scale = (float)(1.4426950408889634 / sqrt((double)Ly.head_dim));
+    at.view_tokens = (int64_t)Ly.batch * pps * Ly.n_layers * Ly.n_kv_heads * Ly.page_tokens;
+    at.block_table = pc->block_table;
+    at.n_blocks = pc->n_blocks;
+    at.blk_len = bs->len;
+    at.pps = pps;
+    rc = timed_launch(c, kProfAttn, s, "attention",
+                      [&] { return launch_attention(at, Ly.head_dim, G, c->attn_grid, s); });
+    if (rc != KVEV_OK) return rc;
+    CombineArgs cb{};
+    cb.sp.part_o = c->ws.part_o;
+    cb.sp.part_ml = c->ws.part_ml;
+    cb.sp.n_tiles = at.n_tiles_total;
+    cb.sp.row0 = 0;
+    cb.sp.total_warps = c->attn_warps;
+    cb.sp.tiles_per_row = ub;
+    cb.n_rows = (int32_t)rows;
+    cb.out = out;
+    cb.lse2 = c->ws.lse2;
+    cb.n_layers = Ly.n_layers;
+    cb.batch = Ly.batch;
+    cb.n_kv = Ly.n_kv_heads;
+    cb.n_q = Ly.n_q_heads;
+    rc = timed_launch(c, kProfCombine, s, "combine",
+                      [&] { return launch_combine(cb, Ly.head_dim, G, s); });
+    if (rc != KVEV_OK) return rc;
+
+    ScoreArgs sc{};
+    sc.logits = c->ws.logits;
+    sc.logit_ld = logit_ld(Ly.max_ctx);
+    sc.lse2 = c->ws.lse2;
+    sc.dbg_probs = refresh ? c->dbg_probs : nullptr;
+    sc.max_ctx = Ly.max_ctx;
+    sc.n_layers = Ly.n_layers;
+    sc.batch = Ly.batch;
+    sc.n_kv = Ly.n_kv_heads;
+    sc.n_q = Ly.n_q_heads;
+    sc.refresh = refresh ? 1 : 0;
+    sc.alpha = c->alpha;
+    rc = timed_launch(c, kProfScore, s, "paged score",
+                      [&] { return launch_paged_score(sc, pa, G, ub, s); });
+    if (rc != KVEV_OK) return rc;
+
+    SelectArgs se{};
+    se.n_units = pc->n_blocks;
+    se.keys = c->ws.keys;
+    se.retained = c->ws.sel;
+    se.n_retained = n_retained;
+    se.L = ub;
+    se.max_ctx = pps;
+    se.budget = (int)c->budget;
+    se.refresh = 1;   // a new block's score was set by the append
+    rc = timed_launch(c, kProfSelect, s, "select",
+                      [&] { return launch_select(se, Ly.batch, s); });
+    if (rc != KVEV_OK) return rc;
+    rc = timed_launch(c, kProfCompact, s, "paged compact",
+                      [&] { return launch_paged_compact(pa, s); });
+    if (rc != KVEV_OK) return rc;
+
+    for (int32_t& u : c->ub_blocks) u = u + 1 < c->budget ? u + 1 : (int32_t)c->budget;
+    c->step = step;
+    return KVEV_OK;
+}
+
+kvev_status kvev_readmit(kvev_ctx* c, const kvev_paged_cache* pc, const kvev_block_state* bs,
+                         int32_t seq, int32_t lid, int32_t persist, void* stream) {
+    kvev_status rc = check_paged(c, pc, bs);
+    if (rc != KVEV_OK) return rc;
+    if (!c->begun) return fail(KVEV_ESTATE, "kvev_paged_begin must come first");
+    if (seq < 0 || seq >= c->lay.batch)
+        return fail(KVEV_EINVAL, "seq %d out of [0, %d)", seq, c->lay.batch);
+    if (lid < 0 || lid >= pc->n_backing)
+        return fail(KVEV_EINVAL, "lid %d is not a block of the backing tier [0, %d)", lid,
+                    pc->n_backing);
+    if (c->ub_blocks[seq] + 2 > pc->pages_per_seq)
+        return fail(KVEV_EINVAL, "sequence %d may hold %d blocks: no page left for a re-admission "
+                    "and the next step's new block", seq, c->ub_blocks[seq]);
+    cudaStream_t s = (cudaStream_t)stream;
+    const PagedArgs a = paged_args(c, pc, bs, (int)(c->step + 1), true);
+    rc = timed_launch(c, kProfReadmit, s, "readmit",
+                      [&] { return launch_readmit(a, seq, lid, persist != 0 ? 1 : 0, s); });
+    if (rc != KVEV_OK) return rc;
+    c->launches += 1;   // the copy kernel
+    c->ub_blocks[seq] += 1;
+    return KVEV_OK;
 }
 
 kvev_status kvev_profile(kvev_ctx* c, int32_t enable) {

@@ -108,7 +108,7 @@ struct MmaCfg {
     static constexpr int NB = D / 8;                // 8-dim output blocks
     static constexpr int KS = D / 16;               // k-steps of the QK contraction
     static constexpr size_t SMEM = 1024 + (size_t)WARPS * STAGES * STAGE_BYTES +
-                                   (size_t)WARPS * STAGES * sizeof(uint64_t);
+                                   (size_t)WARPS * STAGES * (sizeof(uint64_t) + sizeof(int));
     static_assert(G <= 8 && (D == 64 || D == 128), "mma tile shape");
 };
 
@@ -158,7 +158,11 @@ __device__ __forceinline__ uint32_t tile_chunk(uint32_t tile, int r, int c) {
     return tile + (c >> 3) * (kTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-template <int D, int G, int STAGES, int WARPS>
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+template <int D, int G, int STAGES, int WARPS, bool PAGED>
 __global__ void __launch_bounds__(WARPS * 32)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a) {
@@ -174,6 +178,10 @@ __global__ void __launch_bounds__(WARPS * 32)
     unsigned char* wbuf = smem + (size_t)warp * STAGES * C::STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)WARPS * STAGES * C::STAGE_BYTES) +
                      warp * STAGES;
+    // valid tokens of the tile in each stage (written by lane 0 at issue)
+    int* stage_nv = reinterpret_cast<int*>(reinterpret_cast<uint64_t*>(
+                        smem + (size_t)WARPS * STAGES * C::STAGE_BYTES) + WARPS * STAGES) +
+                    warp * STAGES;
 
     const int w = blockIdx.x * WARPS + warp;
     const int64_t N = a.n_tiles_total;
@@ -191,7 +199,27 @@ __global__ void __launch_bounds__(WARPS * 32)
     // tiles are walked with (row, tile-in-row) counters: no divisions in the loop
     const int tpr = a.tiles_per_row;
     auto issue = [&](int64_t row, int tile, int stage) {  // lane 0 only
-        const int y = (int)((a.row0 + row) * a.max_ctx + tile * T);
+        int y = 0, nv;
+        if constexpr (PAGED) {
+            const int64_t arow = a.row0 + row;
+            const int gk = (int)(arow % a.n_kv);
+            const int64_t lb = arow / a.n_kv;
+            const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
+            nv = 0;
+            if (tile < a.n_blocks[b]) {
+                const int page = a.block_table[(size_t)b * a.pps + tile];
+                nv = a.blk_len[(size_t)b * a.pps + tile];
+                y = (int)((((int64_t)page * a.n_layers + l) * a.n_kv + gk) * T);
+            }
+        } else {
+            y = (int)((a.row0 + row) * a.max_ctx + tile * T);
+            nv = min(T, a.L - tile * T);
+        }
+        stage_nv[stage] = nv;
+        if (nv == 0) {   // empty tile: complete the phase with no data
+            mbar_arrive(&bars[stage]);
+            return;
+        }
         unsigned char* dst = wbuf + (size_t)stage * C::STAGE_BYTES;
         mbar_expect_tx(&bars[stage], C::STAGE_BYTES);
 #pragma unroll
@@ -270,7 +298,16 @@ __global__ void __launch_bounds__(WARPS * 32)
         }
         const uint32_t ktile = smem_addr(wbuf + (size_t)stage * C::STAGE_BYTES);
         const uint32_t vtile = ktile + C::TILE_BYTES;
-        const int nvalid = min(T, a.L - tok0);
+        const int nvalid = PAGED ? stage_nv[stage] : min(T, a.L - tok0);
+        if (PAGED && nvalid == 0) {   // past the sequence's live blocks: nothing to do
+            __syncwarp();
+            if (x + STAGES < x1) {
+                if (lane == 0) issue(prow, ptile, stage);
+                if (++ptile == tpr) { ptile = 0; ++prow; }
+            }
+            if (++stage == STAGES) { stage = 0; parity ^= 1u; }
+            continue;
+        }
 
         // ---- S = Q K^T for the two 8-token blocks (even and odd k-steps in
         //      separate accumulators: four independent MMA chains)
@@ -463,13 +500,12 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int64_t n_tokens, int 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int G>
+template <int D, int G, bool PAGED>
 cudaError_t launch_attn_t(const AttnArgs& a, int grid, cudaStream_t s) {
     using C = MmaCfg<D, G, kStages, kWarps>;
-    auto kern = attn_mma_kernel<D, G, kStages, kWarps>;
-    const int64_t n_tokens = (int64_t)a.n_layers * a.batch * a.n_kv * a.max_ctx;
+    auto kern = attn_mma_kernel<D, G, kStages, kWarps, PAGED>;
     CUtensorMap mk, mv;
-    if (!encode_cache_map(&mk, a.k, n_tokens, D) || !encode_cache_map(&mv, a.v, n_tokens, D))
+    if (!encode_cache_map(&mk, a.k, a.view_tokens, D) || !encode_cache_map(&mv, a.v, a.view_tokens, D))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::SMEM);
@@ -480,7 +516,7 @@ cudaError_t launch_attn_t(const AttnArgs& a, int grid, cudaStream_t s) {
 template <int D, int G>
 int ctas_per_sm_t() {
     using C = MmaCfg<D, G, kStages, kWarps>;
-    auto kern = attn_mma_kernel<D, G, kStages, kWarps>;
+    auto kern = attn_mma_kernel<D, G, kStages, kWarps, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) !=
         cudaSuccess)
         return 0;
@@ -511,8 +547,11 @@ size_t attn_smem_bytes(int head_dim, int group) {
 
 cudaError_t launch_attention(const AttnArgs& a, int head_dim, int group, int grid,
                              cudaStream_t s) {
-    if (group == 4 && head_dim == 128) return launch_attn_t<128, 4>(a, grid, s);
-    if (group == 4 && head_dim == 64) return launch_attn_t<64, 4>(a, grid, s);
+    const bool paged = a.block_table != nullptr;
+    if (group == 4 && head_dim == 128)
+        return paged ? launch_attn_t<128, 4, true>(a, grid, s) : launch_attn_t<128, 4, false>(a, grid, s);
+    if (group == 4 && head_dim == 64)
+        return paged ? launch_attn_t<64, 4, true>(a, grid, s) : launch_attn_t<64, 4, false>(a, grid, s);
     return cudaErrorInvalidValue;
 }
 

@@ -39,6 +39,14 @@ struct AttnArgs {
     int32_t total_warps;
     int32_t write_logits;
     float q_scale;         // log2(e) / sqrt(D)
+    int64_t view_tokens;   // rows of the 2-D (token x D) view of k / v for the tensor maps
+    // Block-granular cache (block_table non-null): k / v are page pools
+    // [pages][Ly][Hkv][kTile][D]; tile j of a row is the sequence's j-th live
+    // block (tiles at or past n_blocks[b] are empty); L is unused.
+    const int32_t* block_table;   // [batch][pps]
+    const int32_t* n_blocks;      // [batch]
+    const int32_t* blk_len;       // [batch][pps]
+    int32_t pps;
 };
 
 // Where one attention launch left its split partials: warp w's piece of the
@@ -99,14 +107,14 @@ struct ScoreArgs {
 };
 
 struct SelectArgs {
+    const int32_t* n_units;   // [b] units per sequence on the device (paged mode), or null: L
     const uint32_t* keys;
     float* m_s;
     const float* msum_part;
     int32_t n_part;
     int32_t* retained;     // [b][budget]
     int32_t* n_retained;   // [b]
-    float* dbg_prio;       // fix the new token's entry? (no: priority of new token is 0)
-    int32_t L, max_ctx, budget, refresh;
+    int32_t L, max_ctx, budget, refresh;   // L: upper bound of n_units when n_units is set
 };
 
 struct CompactArgs {
@@ -125,6 +133,30 @@ struct AppendArgs {
     const uint16_t* k_new; const uint16_t* v_new;   // [b][Ly][Hkv][D]
     kvev_state st;
     int32_t slot, t, pos, n_layers, batch, n_kv, max_ctx, head_dim;
+};
+
+// Block-granular (paged) mode: the caller's structures plus this context's
+// per-block scratch (slot-indexed [b][pps], written by the scorer).
+struct PagedArgs {
+    kvev_paged_cache c;
+    kvev_block_state st;
+    int32_t* tokens;       // [b] live tokens (for the access threshold)
+    float* m_s;            // scratch copies of the block state after scoring
+    int32_t* tref_s;
+    int32_t* tins_s;
+    int32_t* lid_s;
+    int32_t* len_s;
+    int32_t* page_s;
+    uint32_t* keys;        // [b][pps]
+    const int32_t* sel;    // [b][budget] kept slots from the selection
+    const int32_t* n_sel;  // [b]
+    int32_t* retained_lid; // [b][budget] user output
+    int32_t* readmit_page; // [1] page chosen by the last re-admission (-1: none)
+    uint32_t* status;
+    int32_t batch, n_layers, n_kv, n_q, head_dim, page, budget;
+    int32_t t, refresh, age_mode, pool_mean;
+    float alpha, beta;
+    float* dbg_prio;       // [b][pps] or null
 };
 
 // ---- programmatic dependent launch ----------------------------------------
@@ -168,6 +200,15 @@ cudaError_t launch_select(const SelectArgs& a, int batch, cudaStream_t s);
 cudaError_t launch_compact(const CompactArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_init_state(kvev_state st, int batch, int max_ctx, int len, cudaStream_t s);
+cudaError_t launch_paged_begin(const PagedArgs& a, int prefill_blocks, cudaStream_t s);
+cudaError_t launch_paged_append(const PagedArgs& a, const uint16_t* k_new, const uint16_t* v_new,
+                                cudaStream_t s);
+cudaError_t launch_paged_score(const ScoreArgs& sc, const PagedArgs& a, int group, int ub_blocks,
+                               cudaStream_t s);
+cudaError_t launch_paged_compact(const PagedArgs& a, cudaStream_t s);
+cudaError_t launch_readmit(const PagedArgs& a, int seq, int lid, int persist, cudaStream_t s);
+
+enum : uint32_t { kStatusNoPage = 2u };   // a sequence ran out of free pages
 
 constexpr int kScoreThreads = 256;
 

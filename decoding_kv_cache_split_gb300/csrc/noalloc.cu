@@ -134,6 +134,7 @@ extern "C" kvev_status kvev_attend_noalloc(const kvev_layout* L, const void* q, 
     at.total_warps = (int32_t)(grid * wpc);
     at.write_logits = 0;
     at.q_scale = (float)(1.4426950408889634 / sqrt((double)L->head_dim));
+    at.view_tokens = rows * L->max_ctx;
     e = launch_attention(at, L->head_dim, G, (int)grid, s);
     if (e != cudaSuccess) return report_error(KVEV_ECUDA, cudaGetErrorString(e));
 

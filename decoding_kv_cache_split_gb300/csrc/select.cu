@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     const uint32_t rank = cta_rank();
     const int b = blockIdx.x / kCl;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int L = a.L, B = a.budget;
+    const int L = a.n_units ? min(a.n_units[blockIdx.x / kCl], a.L) : a.L, B = a.budget;
     const uint32_t* gkeys = a.keys + (size_t)b * a.max_ctx;
     int32_t* ret = a.retained + (size_t)b * B;
 

@@ -26,14 +26,15 @@ KVEV_AGE_SINCE_INSERT, KVEV_AGE_SINCE_ACCESS = 0, 1
 KVEV_POOL_SUM, KVEV_POOL_MEAN = 0, 1
 KVEV_BF16 = 0
 KVEV_PROFILE_SLOTS = 8
-PROFILE_NAMES = ["append", "attention", "combine", "score", "select", "compact", "init_state", "-"]
+PROFILE_NAMES = ["append", "attention", "combine", "score", "select", "compact", "init_state",
+                 "readmit"]
 
 # every entry point declared in include/kvev.h
 EXPORTS = ["kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_size",
            "kvev_refresh_mode", "kvev_configure", "kvev_begin", "kvev_length",
            "kvev_init_state", "kvev_step", "kvev_step_host", "kvev_set_debug",
            "kvev_profile", "kvev_profile_read", "kvev_launch_count", "kvev_sync",
-           "kvev_attend_noalloc"]
+           "kvev_paged_begin", "kvev_paged_step", "kvev_readmit", "kvev_attend_noalloc"]
 
 
 class KvevError(RuntimeError):
@@ -57,6 +58,21 @@ class kvev_cache(ctypes.Structure):
 class kvev_state(ctypes.Structure):
     _fields_ = [("score", ctypes.c_void_p), ("t_ins", ctypes.c_void_p),
                 ("t_ref", ctypes.c_void_p), ("pos", ctypes.c_void_p)]
+
+
+class kvev_paged_cache(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("pages_per_seq", ctypes.c_int32), ("block_table", ctypes.c_void_p),
+                ("n_blocks", ctypes.c_void_p), ("free_pages", ctypes.c_void_p),
+                ("n_free", ctypes.c_void_p), ("next_lid", ctypes.c_void_p),
+                ("backing_k", ctypes.c_void_p), ("backing_v", ctypes.c_void_p),
+                ("n_backing", ctypes.c_int32)]
+
+
+class kvev_block_state(ctypes.Structure):
+    _fields_ = [("score", ctypes.c_void_p), ("t_ins", ctypes.c_void_p),
+                ("t_ref", ctypes.c_void_p), ("lid", ctypes.c_void_p), ("len", ctypes.c_void_p),
+                ("table", ctypes.c_void_p), ("table_len", ctypes.c_int32)]
 
 
 _lib = None
@@ -88,6 +104,9 @@ def lib():
             "kvev_profile_read": ([P, P, P], I32),
             "kvev_launch_count": ([P, P], I32),
             "kvev_sync": ([P, P], I32),
+            "kvev_paged_begin": ([P, P, P, I32, P], I32),
+            "kvev_paged_step": ([P, P, P, P, P, P, I64, P, P, P, P], I32),
+            "kvev_readmit": ([P, P, P, I32, I32, I32, P], I32),
             "kvev_attend_noalloc": ([P, P, P, P, I32, P, P, P], I32),
         }
         for name, (args, res) in sig.items():
@@ -208,6 +227,25 @@ def kvev_sync(ctx, stream=None) -> None:
     _check(lib().kvev_sync(ctx, _stream(stream)), ctx)
 
 
+def kvev_paged_begin(ctx, cache: kvev_paged_cache, state: kvev_block_state, prefill_tokens: int,
+                     stream=None) -> None:
+    _check(lib().kvev_paged_begin(ctx, ctypes.byref(cache), ctypes.byref(state),
+                                  int(prefill_tokens), _stream(stream)), ctx)
+
+
+def kvev_paged_step(ctx, q, k_new, v_new, cache: kvev_paged_cache, state: kvev_block_state,
+                    step: int, out, retained_lid, n_retained, stream=None) -> None:
+    _check(lib().kvev_paged_step(ctx, _ptr(q), _ptr(k_new), _ptr(v_new), ctypes.byref(cache),
+                                 ctypes.byref(state), int(step), _ptr(out), _ptr(retained_lid),
+                                 _ptr(n_retained), _stream(stream)), ctx)
+
+
+def kvev_readmit(ctx, cache: kvev_paged_cache, state: kvev_block_state, seq: int, lid: int,
+                 persist: bool = True, stream=None) -> None:
+    _check(lib().kvev_readmit(ctx, ctypes.byref(cache), ctypes.byref(state), int(seq), int(lid),
+                              int(bool(persist)), _stream(stream)), ctx)
+
+
 def kvev_attend_noalloc(layout: kvev_layout, q, k, v, length: int, out, lse2, stream=None) -> None:
     """Attention of the pass with no allocation (see include/kvev.h)."""
     _check(lib().kvev_attend_noalloc(ctypes.byref(layout), _ptr(q), _ptr(k), _ptr(v), int(length),
@@ -276,6 +314,86 @@ class EvictionPass:
         kvev_step(self.ctx, q, k_new, v_new, self.cache, self.state, self.step_no, self.out,
                   self.retained, self.n_retained, stream)
         return self.out, self.retained, self.n_retained
+
+    def close(self):
+        if self.ctx is not None:
+            kvev_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class PagedEvictionPass:
+    """Device buffers plus a context for one block-granular run.
+
+    Page pools k_pool, v_pool [batch * pps][Ly][Hkv][P][d] bf16; block table,
+    free stack and per-block state [batch][pps]; persisted scores
+    [batch][table_len]; the backing tier (prefill blocks, for re-admission)
+    [batch][n_backing][Ly][Hkv][P][d] bf16.  All torch tensors on the
+    current CUDA device."""
+
+    def __init__(self, n_layers, n_q_heads, n_kv_heads, head_dim, batch, pages_per_seq, page,
+                 budget, alpha, beta, *, n_backing=0, table_len=None,
+                 age_mode=KVEV_AGE_SINCE_ACCESS, pool=KVEV_POOL_SUM, refresh=KVEV_REFRESH_FULL,
+                 period=1, device="cuda"):
+        import torch
+        self.torch = torch
+        self.page, self.pps, self.budget = int(page), int(pages_per_seq), int(budget)
+        self.layout = kvev_layout(n_layers, n_q_heads, n_kv_heads, head_dim, batch,
+                                  self.pps * self.page, self.page, KVEV_BF16)
+        self.ctx = kvev_create(self.layout, budget, self.page, alpha, beta)
+        kvev_configure(self.ctx, age_mode, pool)
+        kvev_refresh_mode(self.ctx, refresh, period)
+        pshape = (batch * self.pps, n_layers, n_kv_heads, self.page, head_dim)
+        self.k_pool = torch.zeros(pshape, dtype=torch.bfloat16, device=device)
+        self.v_pool = torch.zeros(pshape, dtype=torch.bfloat16, device=device)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.block_table = torch.zeros((batch, self.pps), **i32)
+        self.n_blocks = torch.zeros((batch,), **i32)
+        self.free_pages = torch.zeros((batch, self.pps), **i32)
+        self.n_free = torch.zeros((batch,), **i32)
+        self.next_lid = torch.zeros((batch,), **i32)
+        bshape = (batch, max(int(n_backing), 1), n_layers, n_kv_heads, self.page, head_dim)
+        self.backing_k = torch.zeros(bshape, dtype=torch.bfloat16, device=device)
+        self.backing_v = torch.zeros(bshape, dtype=torch.bfloat16, device=device)
+        self.score = torch.zeros((batch, self.pps), dtype=torch.float32, device=device)
+        self.t_ins = torch.zeros((batch, self.pps), **i32)
+        self.t_ref = torch.zeros((batch, self.pps), **i32)
+        self.lid = torch.zeros((batch, self.pps), **i32)
+        self.len = torch.zeros((batch, self.pps), **i32)
+        self.table_len = int(table_len if table_len is not None else max(int(n_backing), 1))
+        self.table = torch.zeros((batch, self.table_len), dtype=torch.float32, device=device)
+        self.out = torch.zeros((batch, n_layers, n_q_heads, head_dim), dtype=torch.float32,
+                               device=device)
+        self.retained_lid = torch.zeros((batch, self.budget), **i32)
+        self.n_retained = torch.zeros((batch,), **i32)
+        self.cache = kvev_paged_cache(
+            self.k_pool.data_ptr(), self.v_pool.data_ptr(), self.pps, self.block_table.data_ptr(),
+            self.n_blocks.data_ptr(), self.free_pages.data_ptr(), self.n_free.data_ptr(),
+            self.next_lid.data_ptr(), self.backing_k.data_ptr(), self.backing_v.data_ptr(),
+            int(n_backing))
+        self.state = kvev_block_state(self.score.data_ptr(), self.t_ins.data_ptr(),
+                                      self.t_ref.data_ptr(), self.lid.data_ptr(),
+                                      self.len.data_ptr(), self.table.data_ptr(), self.table_len)
+        self.step_no = 0
+
+    def begin(self, prefill_tokens: int, stream=None):
+        """Start a run over the prefill already written into pages b*pps + j."""
+        kvev_paged_begin(self.ctx, self.cache, self.state, prefill_tokens, stream)
+        self.step_no = 0
+
+    def step(self, q, k_new, v_new, stream=None):
+        self.step_no += 1
+        kvev_paged_step(self.ctx, q, k_new, v_new, self.cache, self.state, self.step_no, self.out,
+                        self.retained_lid, self.n_retained, stream)
+        return self.out, self.retained_lid, self.n_retained
+
+    def readmit(self, seq: int, lid: int, persist: bool = True, stream=None):
+        kvev_readmit(self.ctx, self.cache, self.state, seq, lid, persist, stream)
 
     def close(self):
         if self.ctx is not None:

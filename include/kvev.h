@@ -85,7 +85,7 @@ typedef struct {
     int32_t head_dim;     /* d: 64 or 128 */
     int32_t batch;        /* b: independent sequences */
     int32_t max_ctx;      /* slots per (layer, sequence, KV head) */
-    int32_t page_tokens;  /* 1 = token-granular eviction */
+    int32_t page_tokens;  /* 1 = token-granular eviction; 16 = paged blocks */
     int32_t kv_dtype;     /* KVEV_BF16 */
 } kvev_layout;
 
@@ -112,7 +112,8 @@ typedef struct kvev_ctx kvev_ctx;
 
 /* Create a context for `layout` with a budget of `budget` retained tokens
  * per sequence (1 <= budget < max_ctx).  `granularity` must equal
- * layout->page_tokens (1).  `alpha` in (0, 1] weights the new observation in
+ * layout->page_tokens (1, or 16 for block-granular eviction, where the budget
+ * counts blocks).  `alpha` in (0, 1] weights the new observation in
  * the EMA; `beta` >= 0 is the recency coefficient (+INFINITY allowed: rank by
  * score, newest token protected).  `regions` must be NULL (no region table
  * for token-granular eviction).  Allocates the context's device scratch on
@@ -191,7 +192,8 @@ kvev_status kvev_set_debug(kvev_ctx* ctx, float* probs, float* priority);
 /* Per-kernel timing with CUDA events on the step's stream.  Enable, run
  * steps, then kvev_profile_read fills `ms[i]` (accumulated milliseconds) and
  * `launches[i]` for kernel i in the order append, attention, combine, score,
- * select, compact (KVEV_PROFILE_SLOTS entries each; pass NULL to skip) and
+ * select, compact, state set-up (kvev_init_state, kvev_paged_begin),
+ * re-admission (KVEV_PROFILE_SLOTS entries each; pass NULL to skip) and
  * resets the accumulators.  kvev_profile_read synchronizes. */
 enum { KVEV_PROFILE_SLOTS = 8 };
 kvev_status kvev_profile(kvev_ctx* ctx, int32_t enable);
@@ -202,6 +204,80 @@ kvev_status kvev_launch_count(const kvev_ctx* ctx, int64_t* launches);
 
 /* Block until `stream`'s work is done; returns KVEV_ECUDA on a device fault. */
 kvev_status kvev_sync(kvev_ctx* ctx, void* stream);
+
+/* ---- Block-granular eviction with score persistence ----------------------
+ * layout->page_tokens = P > 1 (16 in the paged workloads), budget = blocks.
+ * The LRFU policy per (sequence, token block) of the kv-cache-docs figure
+ * "ema-eviction": per layer a block's new score is the max over its tokens of
+ * the head-summed probability, folded into the block's EMA (layers in
+ * ascending order); the priority (1 - score)(1 - exp(-beta age)) is per
+ * block; the B blocks of lowest priority are kept, ties to the lower slot.
+ * When a block is evicted its score is stored under (sequence, logical
+ * block) and restored when the block is re-admitted.  K/V rows never move:
+ * eviction only frees pages.  Slot order is ascending logical block id
+ * (prefill blocks 0.., then blocks opened by decoding); new tokens fill the
+ * last block while it has room, else open a new one. */
+typedef struct {
+    void* k_pool;            /* [n_pages][n_layers][n_kv_heads][P][head_dim] bf16,
+                                n_pages = batch * pages_per_seq, 16-byte aligned */
+    void* v_pool;
+    int32_t pages_per_seq;   /* sequence b owns pages [b*pps, (b+1)*pps) */
+    int32_t* block_table;    /* [batch][pps] page of each live block, slot order */
+    int32_t* n_blocks;       /* [batch] live blocks */
+    int32_t* free_pages;     /* [batch][pps] stack of free pages */
+    int32_t* n_free;         /* [batch] */
+    int32_t* next_lid;       /* [batch] logical id of the next block decoding opens */
+    const void* backing_k;   /* [batch][n_backing][n_layers][n_kv_heads][P][head_dim]
+                                bf16: the prefill blocks, for re-admission (may be NULL) */
+    const void* backing_v;
+    int32_t n_backing;
+} kvev_paged_cache;
+
+/* Per live block, each [batch][pps], slot-aligned with block_table. */
+typedef struct {
+    float* score;            /* EMA state of the block */
+    int32_t* t_ins;          /* step the block was opened (prefill: 0) */
+    int32_t* t_ref;          /* step of its last access (insertion, re-admission,
+                                or a token of it accessed: KVEV_AGE_SINCE_ACCESS) */
+    int32_t* lid;            /* logical block id */
+    int32_t* len;            /* tokens in the block (1..P) */
+    float* table;            /* [batch][table_len] persisted score per logical block
+                                (NaN = never stored) */
+    int32_t table_len;       /* > every logical id used */
+} kvev_block_state;
+
+/* Start a paged run.  `prefill_tokens` (a multiple of P, > 0) per sequence
+ * are already in the pool: block j of sequence b at page b*pps + j.  Sets
+ * the block tables, free lists, per-block state (score 0, t_ins = t_ref = 0,
+ * lid j, len P), empties the persisted table; the next step is 1. */
+kvev_status kvev_paged_begin(kvev_ctx* ctx, const kvev_paged_cache* cache,
+                             const kvev_block_state* state, int32_t prefill_tokens, void* stream);
+
+/* One paged decode step `step` (previous + 1).  q, k_new, v_new, out as in
+ * kvev_step.  retained_lid [batch][budget] int32 (device): logical ids of the
+ * kept blocks in slot order; n_retained [batch] int32 (device).  Launches
+ * append, attention, combine, block scoring, selection and compaction.  The
+ * host keeps an upper bound of each sequence's live blocks; a step whose
+ * new block could find no free page returns KVEV_EINVAL before launching.
+ * Debug outputs (kvev_set_debug) are indexed by block slot: probabilities
+ * [batch][n_layers][n_q_heads][max_ctx] at slot j*P + k for token k of
+ * block j, priorities [batch][pps]. */
+kvev_status kvev_paged_step(kvev_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                            const kvev_paged_cache* cache, const kvev_block_state* state,
+                            int64_t step, float* out, int32_t* retained_lid,
+                            int32_t* n_retained, void* stream);
+
+/* Re-admit prefill block `lid` (0 <= lid < n_backing) of sequence `seq`
+ * before the next step (a no-op when it is resident): a free page receives
+ * the block's K/V from the backing tier, the block returns to its slot
+ * (ascending logical id), its score is the persisted one (persist != 0 and
+ * one was stored) or 0, its insertion step 0 and its access time the next
+ * step.  Rejected (KVEV_EINVAL) when the sequence could be left without a
+ * page for the next step's new block; KVEV_ESTATE at the next kvev_sync if
+ * no page was free on the device. */
+kvev_status kvev_readmit(kvev_ctx* ctx, const kvev_paged_cache* cache,
+                         const kvev_block_state* state, int32_t seq, int32_t lid,
+                         int32_t persist, void* stream);
 
 /* Attention of the pass without allocating: no counterpart on the pages;
  * it exists for callers that cannot call cudaMalloc (engines whose allocator

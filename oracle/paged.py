@@ -96,9 +96,14 @@ def readmit(seq: PagedSequence, lid: int, t: int, persist: bool = True) -> bool:
 
 
 def step(P: O.OracleParams, seq: PagedSequence, t: int, refresh: bool, q_bits, knew_bits,
-         vnew_bits, want_probs: bool = False, forced_access=None):
+         vnew_bits, want_probs: bool = False, forced_access=None, kept=None):
     """One decode step of one sequence.  P.budget counts blocks.  Returns the
-    result dict; `seq` is updated in place (append, scores, eviction)."""
+    result dict; `seq` is updated in place (append, scores, eviction).
+
+    forced_access: per token, -1 = the threshold decides, 0/1 = the decision
+    taken instead; kept: the block slots to keep instead of this function's
+    own selection.  Both let a caller continue along another admissible
+    outcome where the decision sits within rounding of a tie."""
     Ly, Hq, Hkv, d = P.n_layers, P.n_q_heads, P.n_kv_heads, P.head_dim
     page = seq.page
     kn = np.ascontiguousarray(knew_bits, dtype=np.uint16).reshape(Ly, Hkv, 1, d)
@@ -153,7 +158,9 @@ def step(P: O.OracleParams, seq: PagedSequence, t: int, refresh: bool, q_bits, k
             b.t_ref = t
     pr = np.array([O.priority(b.m, t - (b.t_ref if P.age_mode == O.AGE_SINCE_ACCESS else b.t_ins),
                               P.beta) for b in seq.blocks])
-    kept = O.select(pr, P.budget)
+    if kept is None:
+        kept = O.select(pr, P.budget)
+    kept = np.asarray(kept, dtype=np.int64)
     evicted = [j for j in range(nb) if j not in set(kept.tolist())]
     for j in evicted:
         seq.table[seq.blocks[j].lid] = seq.blocks[j].m

@@ -46,14 +46,17 @@ def layout(**kw):
     (dict(n_q_heads=7), 8, kvev.KVEV_EINVAL),
     (dict(n_q_heads=16), 8, kvev.KVEV_EUNSUPPORTED),
     (dict(batch=0), 8, kvev.KVEV_EINVAL),
-    (dict(page_tokens=16), 8, kvev.KVEV_EUNSUPPORTED),
+    (dict(page_tokens=8), 4, kvev.KVEV_EUNSUPPORTED),
+    (dict(page_tokens=16), 4, kvev.KVEV_EINVAL),                # budget counts pages: 4 of 4
+    (dict(page_tokens=16, max_ctx=72), 2, kvev.KVEV_EINVAL),    # not whole pages
     ({}, 0, kvev.KVEV_EINVAL),
     ({}, 64, kvev.KVEV_EINVAL),
 ])
 def test_create_rejects_bad_layouts(lib, kw, budget, status):
     out = ctypes.c_void_p()
     lay = layout(**kw)
-    rc = lib.kvev_create(ctypes.byref(lay), budget, 1, 0.05, 0.001, None, ctypes.byref(out))
+    rc = lib.kvev_create(ctypes.byref(lay), budget, lay.page_tokens, 0.05, 0.001, None,
+                         ctypes.byref(out))
     assert rc == status
     assert out.value is None
     assert kvev.kvev_last_error()

@@ -12,4 +12,6 @@ from .gen import (  # noqa: F401
     f32_to_bf16_bits,
     tiny_workload,
     llama8b_workload,
+    needle_blocks,
+    paged_workload,
 )

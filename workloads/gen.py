@@ -179,3 +179,19 @@ def llama8b_workload(seed: int = 0, prefill_len: int = 32768, *, n_layers: int =
     return Workload(Geometry(n_layers, 32, 8, 128, batch), prefill_len, seed,
                     outliers=4, outlier_sigma=8.0, needle=16,
                     needle_period=needle_period, needle_weight=0.5)
+
+
+def paged_workload(seed: int = 0, prefill_len: int = 8192, *, n_layers: int = 32,
+                   batch: int = 64, needle_period: int = 200) -> Workload:
+    """Block-granular workload: Llama-3.1-8B attention geometry, keys with 4
+    outlier channels, queries drawn toward a 16-position needle set that is
+    re-drawn every ``needle_period`` steps (the blocks holding the new set
+    are the ones a caller re-admits when they were evicted)."""
+    return Workload(Geometry(n_layers, 32, 8, 128, batch), prefill_len, seed,
+                    outliers=4, outlier_sigma=8.0, needle=16,
+                    needle_period=needle_period, needle_weight=0.5)
+
+
+def needle_blocks(wl: Workload, step: int, page: int) -> np.ndarray:
+    """Logical ids of the prefill blocks holding step ``step``'s needle set."""
+    return np.unique(wl.needle_positions(step) // page)
