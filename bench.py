@@ -44,6 +44,12 @@ WORKLOAD = dict(workload="llama3.1-8b-shape eviction step, 32k ctx, 10% budget",
                 n_layers=32, n_q_heads=32, n_kv_heads=8, head_dim=128, batch=1,
                 prefill=32768, budget=3277, alpha=0.05, beta=0.001,
                 age="since last access", refresh="full", step=1)
+PAGED = dict(workload="paged block eviction with score persistence, 64 x 8192 tokens, "
+                      "25% of blocks",
+             n_layers=32, n_q_heads=32, n_kv_heads=8, head_dim=128, batch=64, prefill=8192,
+             page=16, budget_blocks=128, alpha=0.05, beta=0.001, age="since last access",
+             refresh="full", needle_blocks=4, needle_period=200, readmit="needle blocks at "
+             "t = 1 + 200k, k >= 1", persistence=True)
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -216,6 +222,10 @@ def main():
     ap.add_argument("--layers", type=int, default=WORKLOAD["n_layers"],
                     help="smaller cases for profiling; the headline uses 32")
     ap.add_argument("--prefill", type=int, default=WORKLOAD["prefill"])
+    ap.add_argument("--workload", default="llama8b-32k", choices=["llama8b-32k", "paged"],
+                    help="the headline token-granular step, or the block-granular run")
+    ap.add_argument("--batch", type=int, default=PAGED["batch"],
+                    help="paged workload: sequences (profiling cases only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -225,6 +235,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         reference_arm(args, rank, world)
+        return
+
+    if args.workload == "paged":
+        bench_paged(args, rank, world, local_rank)
         return
 
     import torch
@@ -388,6 +402,209 @@ def main():
         }
         print(json.dumps(line), flush=True)
     ep.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def bench_paged(args, rank, world, local_rank):
+    """Block-granular run: 64 sequences of 8192 tokens in 16-token blocks,
+    budget 128 blocks; step 1 evicts from 513 to 128 blocks per sequence,
+    later steps attend over ~2049 tokens per sequence; the needle blocks are
+    re-admitted (scores restored) when the needle is re-drawn.  Timed: K
+    consecutive decode steps after step 1 (readmissions included); step 1
+    alone is timed separately (re-run on the untouched prefill pages)."""
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from decoding_kv_cache_split_gb300 import build as kbuild
+    if not os.path.exists(kbuild.LIB):
+        kbuild.build()
+    from decoding_kv_cache_split_gb300 import kvev
+    from workloads.device import PagedDeviceWorkload
+
+    W = dict(PAGED)
+    if args.layers != WORKLOAD["n_layers"] or args.batch != W["batch"] or \
+            args.prefill != WORKLOAD["prefill"]:
+        pre = args.prefill if args.prefill != WORKLOAD["prefill"] else W["prefill"]
+        W.update(workload=f"profiling case: {args.layers} layers, {args.batch} x {pre} tokens",
+                 n_layers=args.layers, batch=args.batch, prefill=pre,
+                 budget_blocks=max(1, pre // W["page"] // 4))
+    Ly, b, P, B = W["n_layers"], W["batch"], W["page"], W["budget_blocks"]
+    nb0 = W["prefill"] // P
+    pps = nb0 + 8
+    wl = PagedDeviceWorkload(0, n_layers=Ly, batch=b, prefill=W["prefill"], page=P,
+                             needle_blocks=W["needle_blocks"], needle_period=W["needle_period"])
+    pp = kvev.PagedEvictionPass(Ly, W["n_q_heads"], W["n_kv_heads"], W["head_dim"], b, pps, P,
+                                B, W["alpha"], W["beta"], n_backing=nb0, table_len=nb0,
+                                age_mode=kvev.KVEV_AGE_SINCE_ACCESS)
+    wl.fill(torch, pp.k_pool, pp.v_pool, pps, pp.backing_k, pp.backing_v)
+    n_steps = args.steps
+    last = max(n_steps + 1, args.warmup)
+    inputs = [wl.step_inputs(torch, t, pp.backing_k) for t in range(1, last + 1)]
+    readmits = {}
+    for t in range(1 + W["needle_period"], last + 1, W["needle_period"]):
+        nd = wl.needle(t)
+        readmits[t] = [(s, int(x)) for s in range(b) for x in nd[s]]
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def run_step(t):
+        for (s, lid) in readmits.get(t, ()):
+            pp.readmit(s, lid, True, stream)
+        q, kn, vn = inputs[t - 1]
+        pp.step(q, kn, vn, stream)
+
+    # warm-up: the first W steps of a run
+    pp.begin(W["prefill"], stream)
+    for t in range(1, args.warmup + 1):
+        run_step(t)
+    kvev.kvev_sync(pp.ctx)
+
+    # timed: steps 2 .. K+1 of a fresh run
+    pp.begin(W["prefill"], stream)
+    run_step(1)
+    n0 = kvev.kvev_launch_count(pp.ctx)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for t in range(2, n_steps + 2):
+        run_step(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    kvev.kvev_sync(pp.ctx)
+    launches = kvev.kvev_launch_count(pp.ctx) - n0
+    ms = e0.elapsed_time(e1) / n_steps
+    if dist:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # replay with per-kernel events; count the live tokens each step attends
+    row = 2 * W["head_dim"] * 2 * W["n_kv_heads"] * Ly        # bytes of one token, all layers
+    kvev.kvev_profile(pp.ctx, True)
+    pp.begin(W["prefill"], stream)
+    run_step(1)
+    kvev.kvev_sync(pp.ctx)
+    kvev.kvev_profile_read(pp.ctx)
+    def live_tokens():
+        nb, lens = pp.n_blocks.cpu().numpy(), pp.len.cpu().numpy()
+        return int(sum(lens[s, :nb[s]].sum() for s in range(b)))
+
+    tokens_after = live_tokens()               # after step 1's compaction
+    attn_tokens = 0
+    readmit_blocks = 0
+    for t in range(2, n_steps + 2):
+        if t in readmits:                          # readmitted blocks are attended too
+            before = live_tokens()
+            for (s, lid) in readmits[t]:
+                pp.readmit(s, lid, True, stream)
+            kvev.kvev_sync(pp.ctx)
+            readmit_blocks += (live_tokens() - before) // P
+            tokens_after = live_tokens()
+        q, kn, vn = inputs[t - 1]
+        pp.step(q, kn, vn, stream)
+        kvev.kvev_sync(pp.ctx)
+        attn_tokens += tokens_after + b            # previous live tokens + the new ones
+        tokens_after = live_tokens()
+    prof = kvev.kvev_profile_read(pp.ctx)
+    kvev.kvev_profile(pp.ctx, False)
+    attn_bytes_total = attn_tokens * row
+    # pages never move; a re-admission copies one block (all layers) from the backing tier
+    nbytes_total = attn_bytes_total + readmit_blocks * P * row * 2
+    att_ms = prof.get("attention", (0.0, 0))[0]
+    value = world * nbytes_total / n_steps / (ms * 1e-3) / 1e9
+    attn_achieved = attn_bytes_total / (att_ms * 1e-3) / 1e9 if att_ms > 0 else None
+    kernels_us = {k: round(v[0] / n_steps * 1e3, 2) for k, v in prof.items()}
+    kernels_us["launches_per_step"] = {k: round(v[1] / n_steps, 2) for k, v in prof.items()}
+
+    # step 1 alone: 64 x 8193 tokens, eviction to 128 blocks
+    n1 = 10
+    pp.begin(W["prefill"], stream)
+    run_step(1)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(n1):
+        pp.begin(W["prefill"], stream)
+        run_step(1)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    kvev.kvev_sync(pp.ctx)
+    step1_ms = s0.elapsed_time(s1) / n1
+    step1_bytes = b * (W["prefill"] + 1) * row
+
+    # end to end: host inputs (pinned) in, outputs out, every step
+    n_e2e = min(n_steps, 64)
+    host_in = [tuple(x.view(torch.int16).cpu().pin_memory() for x in inputs[t - 1])
+               for t in range(2, n_e2e + 2)]
+    dev_in = [torch.empty_like(x) for x in inputs[0]]
+    out_h = torch.empty(pp.out.shape, dtype=torch.float32).pin_memory()
+    ret_h = torch.empty(pp.retained_lid.shape, dtype=torch.int32).pin_memory()
+    nret_h = torch.empty(pp.n_retained.shape, dtype=torch.int32).pin_memory()
+    h2d = sum(x.numel() * 2 for x in host_in[0])
+    d2h = out_h.numel() * 4 + ret_h.numel() * 4 + nret_h.numel() * 4
+    pp.begin(W["prefill"], stream)
+    run_step(1)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i, t in enumerate(range(2, n_e2e + 2)):
+        for d, h in zip(dev_in, host_in[i]):
+            d.view(torch.int16).copy_(h, non_blocking=True)
+        for (s, lid) in readmits.get(t, ()):
+            pp.readmit(s, lid, True, stream)
+        pp.step(*dev_in, stream)
+        out_h.copy_(pp.out, non_blocking=True)
+        ret_h.copy_(pp.retained_lid, non_blocking=True)
+        nret_h.copy_(pp.n_retained, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+    kvev.kvev_sync(pp.ctx)
+    e2e_val = world * (attn_bytes_total / n_steps) / (e2e_ms * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peak()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": n_steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "us_per_step": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (device Philox)",
+            "config": dict(W, parallelism=f"replicas{world}", timed="decode steps 2..K+1",
+                           l2="inputs larger than L2 (~17 GB of K/V per step)"),
+            "frac_of_peak": {"measured": round(value / world / peak, 4),
+                             "nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+                             "peak_kind": peak_kind},
+            "kv_tokens_per_s": round(world * attn_tokens / n_steps / (ms * 1e-3), 1),
+            "step1": {"us": round(step1_ms * 1e3, 2), "bytes": step1_bytes,
+                      "GB/s": round(step1_bytes / (step1_ms * 1e-3) / 1e9, 2),
+                      "frac_measured": round(step1_bytes / (step1_ms * 1e-3) / 1e9 / peak, 4)},
+            "readmitted_blocks": readmit_blocks,
+            "roofline": {"bound": "hbm", "kernel": "attention (paged)",
+                         "achieved": round(attn_achieved, 2) if attn_achieved else None,
+                         "peak": peak, "unit": "GB/s",
+                         "frac": round(attn_achieved / peak, 4) if attn_achieved else None,
+                         "traffic": None, "algorithmic_bytes": attn_bytes_total // n_steps,
+                         "peak_kind": f"{peak_kind} (copy bandwidth)"},
+            "kernels_us": kernels_us,
+            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "cpu_baseline": None,
+        }
+        print(json.dumps(line), flush=True)
+    pp.close()
     if dist:
         dist.destroy_process_group()
 

@@ -76,7 +76,8 @@ def check_state(pp, b, seq, amb_lids=()):
     nb = len(seq.blocks)
     m = pp.score[b, :nb].cpu().numpy().astype(np.float64)
     ref = np.array([blk.m for blk in seq.blocks])
-    assert np.abs(m - ref).max(initial=0.0) <= M_ATOL, "block EMA scores"
+    m_abs = float(np.abs(m - ref).max(initial=0.0))
+    assert m_abs <= M_ATOL, "block EMA scores"
     assert list(pp.t_ins[b, :nb].cpu().numpy()) == [blk.t_ins for blk in seq.blocks], "t_ins"
     tref = pp.t_ref[b, :nb].cpu().numpy()
     for j, blk in enumerate(seq.blocks):
@@ -89,6 +90,7 @@ def check_state(pp, b, seq, amb_lids=()):
             assert abs(tab[lid] - seq.table[lid]) <= M_ATOL, f"persisted score of {lid}"
         else:
             assert math.isnan(tab[lid]), f"table entry {lid} written without an eviction"
+    return m_abs
 
 
 def ambiguous_blocks(res, P):
@@ -105,6 +107,47 @@ def ambiguous_blocks(res, P):
         own = res["owner"] == j
         amb[j] = near[own].any() and not above[own].any()
     return amb
+
+
+def step_and_compare(pp, P, seqs, b, t, ref_now, q, kn, vn, probs, prio, stats):
+    """Run the oracle's step t on sequence b and compare the device's."""
+    budget, beta, age_mode = P.budget, P.beta, P.age_mode
+    pre = seqs[b].copy()
+    res = PG.step(P, seqs[b], t, ref_now, q, kn, vn, want_probs=True)
+    out = pp.out[b].cpu().numpy().astype(np.float64)
+    err = np.abs(out - res["out"]).max(-1) / np.abs(res["out"]).max(-1)
+    assert err.max() <= OUT_RTOL, f"step {t} seq {b}: output rel err {err.max():.2e}"
+    stats["out_rel"] = max(stats["out_rel"], float(err.max()))
+    # slot of every oracle token in the device's block-major layout
+    owner = res["owner"]
+    first = np.searchsorted(owner, np.arange(len(res["lids_before"])))
+    slot = owner * PAGE + (np.arange(res["L"]) - first[owner])
+    if ref_now:
+        p = probs[b].cpu().numpy().astype(np.float64)[:, :, slot]
+        bad = np.abs(p - res["probs"]) > P_RTOL * res["probs"] + P_ATOL
+        assert not bad.any(), f"step {t} seq {b}: {bad.sum()} probabilities"
+    nbb = len(res["lids_before"])
+    pr = prio[b, :nbb].cpu().numpy().astype(np.float64)
+    amb = ambiguous_blocks(res, P) if ref_now else np.zeros(nbb, dtype=bool)
+    alt = res["priority"].copy()
+    for j in np.nonzero(amb)[0] if age_mode == O.AGE_SINCE_ACCESS else []:
+        blk_tref = pre.blocks[j].t_ref if j < len(pre.blocks) else t
+        age = (t - blk_tref) if res["accessed"][j] else 0
+        alt[j] = O.priority(res["m_upd"][j], age, beta)
+    ok = (np.abs(pr - res["priority"]) <= PR_ATOL) | (amb & (np.abs(pr - alt) <= PR_ATOL))
+    assert ok.all(), f"step {t} seq {b}: {(~ok).sum()} block priorities"
+    n = int(pp.n_retained[b])
+    kept_lids = list(pp.retained_lid[b, :n].cpu().numpy())
+    if kept_lids != [res["lids_before"][j] for j in res["kept"]]:
+        dev_slots = np.array([res["lids_before"].index(x) for x in kept_lids])
+        stats["swaps"] += boundary_check(res["priority"], dev_slots, budget, PR_ATOL,
+                                         alt if amb.any() else None)
+        seqs[b] = pre.copy()        # continue along the device's admissible choice
+        res = PG.step(P, seqs[b], t, ref_now, q, kn, vn, kept=dev_slots)
+    stats["amb"] += int(amb.sum())
+    amb_lids = {res["lids_before"][j] for j in np.nonzero(amb)[0]}
+    check_pages(pp, b, seqs[b])
+    stats["m_abs"] = max(stats["m_abs"], check_state(pp, b, seqs[b], amb_lids))
 
 
 def run_paged(wl, budget, alpha, beta, steps, *, pps, age_mode=O.AGE_SINCE_ACCESS,
@@ -144,42 +187,7 @@ def run_paged(wl, budget, alpha, beta, steps, *, pps, age_mode=O.AGE_SINCE_ACCES
         kvev.kvev_sync(pp.ctx)
         ref_now = O.is_refresh(refresh_o, period, t)
         for b in range(g.batch):
-            pre = seqs[b].copy()
-            res = PG.step(P, seqs[b], t, ref_now, q[b], kn[b], vn[b], want_probs=True)
-            out = pp.out[b].cpu().numpy().astype(np.float64)
-            err = np.abs(out - res["out"]).max(-1) / np.abs(res["out"]).max(-1)
-            assert err.max() <= OUT_RTOL, f"step {t} seq {b}: output rel err {err.max():.2e}"
-            stats["out_rel"] = max(stats["out_rel"], float(err.max()))
-            # slot of every oracle token in the device's block-major layout
-            owner = res["owner"]
-            first = np.searchsorted(owner, np.arange(len(res["lids_before"])))
-            slot = owner * PAGE + (np.arange(res["L"]) - first[owner])
-            if ref_now:
-                p = probs[b].cpu().numpy().astype(np.float64)[:, :, slot]
-                bad = np.abs(p - res["probs"]) > P_RTOL * res["probs"] + P_ATOL
-                assert not bad.any(), f"step {t} seq {b}: {bad.sum()} probabilities"
-            nbb = len(res["lids_before"])
-            pr = prio[b, :nbb].cpu().numpy().astype(np.float64)
-            amb = ambiguous_blocks(res, P) if ref_now else np.zeros(nbb, dtype=bool)
-            alt = res["priority"].copy()
-            for j in np.nonzero(amb)[0] if age_mode == O.AGE_SINCE_ACCESS else []:
-                blk_tref = pre.blocks[j].t_ref if j < len(pre.blocks) else t
-                age = (t - blk_tref) if res["accessed"][j] else 0
-                alt[j] = O.priority(res["m_upd"][j], age, beta)
-            ok = (np.abs(pr - res["priority"]) <= PR_ATOL) | (amb & (np.abs(pr - alt) <= PR_ATOL))
-            assert ok.all(), f"step {t} seq {b}: {(~ok).sum()} block priorities"
-            n = int(pp.n_retained[b])
-            kept_lids = list(pp.retained_lid[b, :n].cpu().numpy())
-            if kept_lids != [res["lids_before"][j] for j in res["kept"]]:
-                dev_slots = np.array([res["lids_before"].index(x) for x in kept_lids])
-                stats["swaps"] += boundary_check(res["priority"], dev_slots, budget, PR_ATOL,
-                                                 alt if amb.any() else None)
-                seqs[b] = pre.copy()        # continue along the device's admissible choice
-                res = PG.step(P, seqs[b], t, ref_now, q[b], kn[b], vn[b], kept=dev_slots)
-            stats["amb"] += int(amb.sum())
-            amb_lids = {res["lids_before"][j] for j in np.nonzero(amb)[0]}
-            check_pages(pp, b, seqs[b])
-            check_state(pp, b, seqs[b], amb_lids)
+            step_and_compare(pp, P, seqs, b, t, ref_now, q[b], kn[b], vn[b], probs, prio, stats)
     pp.close()
     return stats
 
@@ -219,3 +227,40 @@ def test_paged_edge_sizes(L0, budget):
 def test_paged_beta_infinite():
     wl = paged_workload(3, prefill_len=256, n_layers=2, batch=1, needle_period=50)
     run_paged(wl, 4, 0.2, math.inf, 6, pps=20)
+
+
+@pytest.mark.slow
+def test_paged_full_size_steps_1_2():
+    """The full block-granular workload on the device: 32 layers, 64
+    sequences of 8192 tokens (512 blocks), budget 128 blocks; steps 1 and 2
+    of sequences 0 and 63 against the oracle, element by element."""
+    from workloads.device import PagedDeviceWorkload
+    wl = PagedDeviceWorkload(0)
+    Ly, b, nb0 = wl.n_layers, wl.batch, wl.n_blocks
+    pps, budget = nb0 + 8, 128
+    pp = kvev.PagedEvictionPass(Ly, 32, 8, 128, b, pps, PAGE, budget, 0.05, 0.001,
+                                n_backing=nb0, table_len=nb0,
+                                age_mode=kvev.KVEV_AGE_SINCE_ACCESS)
+    wl.fill(torch, pp.k_pool, pp.v_pool, pps, pp.backing_k, pp.backing_v)
+    pp.begin(wl.prefill)
+    probs = torch.zeros((b, Ly, 32, pps * PAGE), device="cuda")
+    prio = torch.zeros((b, pps), device="cuda")
+    kvev.kvev_set_debug(pp.ctx, probs, prio)
+    sample = (0, b - 1)
+    seqs = {}
+    for s in sample:
+        K = _bits(pp.backing_k[s, :nb0]).transpose(1, 2, 0, 3, 4).reshape(Ly, 8, -1, 128)
+        V = _bits(pp.backing_v[s, :nb0]).transpose(1, 2, 0, 3, 4).reshape(Ly, 8, -1, 128)
+        seqs[s] = PG.PagedSequence.from_prefill(np.ascontiguousarray(K),
+                                                np.ascontiguousarray(V), PAGE)
+    P = O.OracleParams(Ly, 32, 8, 128, budget, 0.05, 0.001, O.AGE_SINCE_ACCESS, False)
+    stats = {"swaps": 0, "amb": 0, "out_rel": 0.0, "m_abs": 0.0}
+    for t in (1, 2):
+        q, kn, vn = wl.step_inputs(torch, t, pp.backing_k)
+        pp.step(q, kn, vn)
+        kvev.kvev_sync(pp.ctx)
+        for s in sample:
+            step_and_compare(pp, P, seqs, s, t, True, _bits(q[s]), _bits(kn[s]), _bits(vn[s]),
+                             probs, prio, stats)
+    print("paged full size:", stats)
+    pp.close()

@@ -1,0 +1,104 @@
+"""Seeded synthetic inputs drawn on the GPU, for workloads too large to draw
+on the host (the 64-sequence, 8192-token block-granular workload holds
+68.7 GB of K/V).
+
+Values come from torch's CUDA generator (Philox), one generator per tensor
+family and index, seeded from ``SeedSequence(entropy=seed, spawn_key=(family,
+index))`` so any sequence's prefill or any step's inputs can be drawn alone.
+Draws are fp32 N(0,1) rounded to bf16 by torch's round-to-nearest-even.  The
+tensors land directly in the layouts the block-granular entry points take;
+tests copy them to the host for the oracle.  Like ``gen``, this module holds
+none of the eviction method's arithmetic.
+
+Layouts:
+  page pools    [batch * pps][n_layers][n_kv_heads][page][head_dim] bf16;
+                prefill block j of sequence b at page b * pps + j
+  backing tier  [batch][n_blocks][n_layers][n_kv_heads][page][head_dim] bf16
+  q             [batch][n_layers][n_q_heads][head_dim] bf16
+  k_new, v_new  [batch][n_layers][n_kv_heads][head_dim] bf16
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# stream families of this module (part of the seed key; never reorder)
+_D_K, _D_V, _D_NEEDLE, _D_Q, _D_KNEW, _D_VNEW = range(100, 106)
+
+
+def _seed(seed: int, family: int, index: int) -> int:
+    ss = np.random.SeedSequence(entropy=seed, spawn_key=(family, index))
+    return int(ss.generate_state(1, np.uint64)[0] & np.uint64((1 << 63) - 1))
+
+
+class PagedDeviceWorkload:
+    """Block-granular workload: every sequence has ``prefill`` tokens of
+    N(0,1) keys and values in ``page``-token blocks; each step's query is
+    N(0,1) plus ``needle_weight`` times the mean prefill key of the sequence's
+    needle blocks (``needle_blocks`` distinct prefill blocks, re-drawn at
+    steps 1, 1 + P, 1 + 2P, ... with P = ``needle_period``); new keys and
+    values are N(0,1)."""
+
+    def __init__(self, seed: int = 0, *, n_layers: int = 32, n_q_heads: int = 32,
+                 n_kv_heads: int = 8, head_dim: int = 128, batch: int = 64,
+                 prefill: int = 8192, page: int = 16, needle_blocks: int = 4,
+                 needle_period: int = 200, needle_weight: float = 0.5):
+        if prefill % page:
+            raise ValueError("prefill must be whole blocks")
+        self.seed = int(seed)
+        self.n_layers, self.n_q_heads, self.n_kv_heads = n_layers, n_q_heads, n_kv_heads
+        self.head_dim, self.batch, self.prefill, self.page = head_dim, batch, prefill, page
+        self.n_blocks = prefill // page
+        self.needle_blocks_n = int(needle_blocks)
+        self.needle_period = int(needle_period)
+        self.needle_weight = float(needle_weight)
+
+    # ------------------------------------------------------------- prefill
+    def _normal(self, torch, shape, family, index, device):
+        g = torch.Generator(device=device)
+        g.manual_seed(_seed(self.seed, family, index))
+        return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(
+            torch.bfloat16)
+
+    def prefill_sequence(self, torch, b: int, device="cuda"):
+        """(K, V) of sequence b: [n_blocks][n_layers][n_kv_heads][page][head_dim] bf16."""
+        shape = (self.n_blocks, self.n_layers, self.n_kv_heads, self.page, self.head_dim)
+        return (self._normal(torch, shape, _D_K, b, device),
+                self._normal(torch, shape, _D_V, b, device))
+
+    def fill(self, torch, k_pool, v_pool, pps: int, backing_k=None, backing_v=None):
+        """Write every sequence's prefill into its pages (and the backing tier)."""
+        for b in range(self.batch):
+            k, v = self.prefill_sequence(torch, b, k_pool.device)
+            k_pool[b * pps:b * pps + self.n_blocks].copy_(k)
+            v_pool[b * pps:b * pps + self.n_blocks].copy_(v)
+            if backing_k is not None:
+                backing_k[b, :self.n_blocks].copy_(k)
+                backing_v[b, :self.n_blocks].copy_(v)
+            del k, v
+
+    # -------------------------------------------------------------- decode
+    def needle(self, step: int) -> np.ndarray:
+        """[batch][needle_blocks] sorted logical ids of step ``step``'s needle."""
+        epoch = (step - 1) // self.needle_period
+        out = np.empty((self.batch, self.needle_blocks_n), dtype=np.int64)
+        for b in range(self.batch):
+            rng = np.random.Generator(np.random.PCG64(
+                np.random.SeedSequence(entropy=self.seed, spawn_key=(_D_NEEDLE, epoch, b))))
+            out[b] = np.sort(rng.choice(self.n_blocks, size=self.needle_blocks_n,
+                                        replace=False))
+        return out
+
+    def step_inputs(self, torch, step: int, backing_k, device="cuda"):
+        """(q, k_new, v_new) bf16 device tensors of decode step ``step``; the
+        needle's mean key is taken from the backing tier (the original
+        prefill keys, evicted or not)."""
+        g = self.n_q_heads // self.n_kv_heads
+        q = self._normal(torch, (self.batch, self.n_layers, self.n_q_heads, self.head_dim),
+                         _D_Q, step, device).float()
+        idx = torch.from_numpy(self.needle(step)).to(device)
+        sel = backing_k[torch.arange(self.batch, device=device)[:, None], idx]
+        mean = sel.float().mean(dim=(1, 4))                # [b][Ly][Hkv][d]
+        q = q + self.needle_weight * mean.repeat_interleave(g, dim=2)
+        kv = (self.batch, self.n_layers, self.n_kv_heads, self.head_dim)
+        return (q.to(torch.bfloat16), self._normal(torch, kv, _D_KNEW, step, device),
+                self._normal(torch, kv, _D_VNEW, step, device))
