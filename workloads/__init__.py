@@ -14,4 +14,11 @@ from .gen import (  # noqa: F401
     llama8b_workload,
     needle_blocks,
     paged_workload,
+    memdecay_workload,
+    region_labels,
+    region_spans,
+    REGION_NAMES,
+    REGION_HALF_LIVES,
+    REGION_PINNED,
+    DECODE_REGION,
 )

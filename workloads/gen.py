@@ -195,3 +195,32 @@ def paged_workload(seed: int = 0, prefill_len: int = 8192, *, n_layers: int = 32
 def needle_blocks(wl: Workload, step: int, page: int) -> np.ndarray:
     """Logical ids of the prefill blocks holding step ``step``'s needle set."""
     return np.unique(wl.needle_positions(step) // page)
+
+
+# Region-aware workload: labelled contiguous spans of an agent context, in
+# this order, each floor(fraction * n) tokens, the remainder scratchpad;
+# half-lives in decode steps; the system span is pinned and decoded tokens
+# are scratchpad.
+REGION_NAMES = ("system", "plan", "user", "tool", "retrieved", "scratchpad")
+REGION_FRACTIONS = (0.05, 0.05, 0.10, 0.30, 0.30)
+REGION_HALF_LIVES = (160.0, 80.0, 60.0, 30.0, 40.0, 15.0)
+REGION_PINNED = (True, False, False, False, False, False)
+DECODE_REGION = 5
+
+
+def region_spans(n: int):
+    """Token counts of the six spans of an n-token context."""
+    counts = [int(np.floor(f * n)) for f in REGION_FRACTIONS]
+    return counts + [n - sum(counts)]
+
+
+def region_labels(n: int) -> np.ndarray:
+    """[n] uint8 region label of every prefill position."""
+    return np.repeat(np.arange(len(REGION_NAMES), dtype=np.uint8), region_spans(n))
+
+
+def memdecay_workload(seed: int = 0, prefill_len: int = 1700, *, n_layers: int = 36,
+                      batch: int = 32) -> Workload:
+    """Qwen2.5-3B attention geometry (16 q / 2 KV heads, head_dim 128); q, K,
+    V ~ N(0,1); labels from ``region_labels``."""
+    return Workload(Geometry(n_layers, 16, 2, 128, batch), prefill_len, seed)
