@@ -50,6 +50,11 @@ PAGED = dict(workload="paged block eviction with score persistence, 64 x 8192 to
              page=16, budget_blocks=128, alpha=0.05, beta=0.001, age="since last access",
              refresh="full", needle_blocks=4, needle_period=200, readmit="needle blocks at "
              "t = 1 + 200k, k >= 1", persistence=True)
+MEMDECAY = dict(workload="region-aware (MemDecay) page eviction, 32 x 16384 tokens, 30% budget",
+                n_layers=36, n_q_heads=16, n_kv_heads=2, head_dim=128, batch=32, prefill=16384,
+                page=16, budget_tokens=4915, regions="system 5% (pinned), plan 5%, user 10%, "
+                "tool 30%, retrieved 30%, scratchpad 20%; half-lives 160/80/60/30/40/15 steps",
+                rho=0.9, attn_weight=0.5, tau="2/|K_t|", refresh="full (observation every step)")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -222,7 +227,8 @@ def main():
     ap.add_argument("--layers", type=int, default=WORKLOAD["n_layers"],
                     help="smaller cases for profiling; the headline uses 32")
     ap.add_argument("--prefill", type=int, default=WORKLOAD["prefill"])
-    ap.add_argument("--workload", default="llama8b-32k", choices=["llama8b-32k", "paged"],
+    ap.add_argument("--workload", default="llama8b-32k",
+                    choices=["llama8b-32k", "paged", "memdecay"],
                     help="the headline token-granular step, or the block-granular run")
     ap.add_argument("--batch", type=int, default=PAGED["batch"],
                     help="paged workload: sequences (profiling cases only)")
@@ -237,7 +243,7 @@ def main():
         reference_arm(args, rank, world)
         return
 
-    if args.workload == "paged":
+    if args.workload in ("paged", "memdecay"):
         bench_paged(args, rank, world, local_rank)
         return
 
@@ -407,12 +413,14 @@ def main():
 
 
 def bench_paged(args, rank, world, local_rank):
-    """Block-granular run: 64 sequences of 8192 tokens in 16-token blocks,
-    budget 128 blocks; step 1 evicts from 513 to 128 blocks per sequence,
-    later steps attend over ~2049 tokens per sequence; the needle blocks are
-    re-admitted (scores restored) when the needle is re-drawn.  Timed: K
-    consecutive decode steps after step 1 (readmissions included); step 1
-    alone is timed separately (re-run on the untouched prefill pages)."""
+    """Block-granular runs.  "paged": 64 sequences of 8192 tokens in 16-token
+    blocks, budget 128 blocks; step 1 evicts from 513 to 128 blocks per
+    sequence, later steps attend over ~2049 tokens per sequence; the needle
+    blocks are re-admitted (scores restored) when the needle is re-drawn.
+    "memdecay": Qwen2.5-3B geometry, 32 sequences of 16384 region-labelled
+    tokens, MemDecay page scores, budget 4915 tokens.  Timed: K consecutive
+    decode steps after step 1 (readmissions included); step 1 alone is timed
+    separately (re-run on the untouched prefill pages)."""
     import torch
     dist = None
     if world > 1:
@@ -427,27 +435,53 @@ def bench_paged(args, rank, world, local_rank):
     from decoding_kv_cache_split_gb300 import kvev
     from workloads.device import PagedDeviceWorkload
 
-    W = dict(PAGED)
-    if args.layers != WORKLOAD["n_layers"] or args.batch != W["batch"] or \
+    md = args.workload == "memdecay"
+    W = dict(MEMDECAY if md else PAGED)
+    if args.layers != WORKLOAD["n_layers"] or args.batch != PAGED["batch"] or \
             args.prefill != WORKLOAD["prefill"]:
         pre = args.prefill if args.prefill != WORKLOAD["prefill"] else W["prefill"]
         W.update(workload=f"profiling case: {args.layers} layers, {args.batch} x {pre} tokens",
-                 n_layers=args.layers, batch=args.batch, prefill=pre,
-                 budget_blocks=max(1, pre // W["page"] // 4))
-    Ly, b, P, B = W["n_layers"], W["batch"], W["page"], W["budget_blocks"]
-    nb0 = W["prefill"] // P
+                 n_layers=args.layers, batch=args.batch, prefill=pre)
+        if md:
+            W.update(budget_tokens=max(1, (3 * pre) // 10))
+        else:
+            W.update(budget_blocks=max(1, pre // W["page"] // 4))
+    Ly, b, P = W["n_layers"], W["batch"], W["page"]
+    nb0 = -(-W["prefill"] // P)
     pps = nb0 + 8
-    wl = PagedDeviceWorkload(0, n_layers=Ly, batch=b, prefill=W["prefill"], page=P,
-                             needle_blocks=W["needle_blocks"], needle_period=W["needle_period"])
-    pp = kvev.PagedEvictionPass(Ly, W["n_q_heads"], W["n_kv_heads"], W["head_dim"], b, pps, P,
-                                B, W["alpha"], W["beta"], n_backing=nb0, table_len=nb0,
-                                age_mode=kvev.KVEV_AGE_SINCE_ACCESS)
-    wl.fill(torch, pp.k_pool, pp.v_pool, pps, pp.backing_k, pp.backing_v)
+    if md:
+        import math
+        from workloads import (DECODE_REGION, REGION_HALF_LIVES, REGION_PINNED,
+                               region_labels)
+        wl = PagedDeviceWorkload(0, n_layers=Ly, n_q_heads=W["n_q_heads"],
+                                 n_kv_heads=W["n_kv_heads"], batch=b, prefill=W["prefill"],
+                                 page=P, needle_blocks=0)
+        table = kvev.region_table([1.0] * len(REGION_HALF_LIVES),
+                                  [math.log(2.0) / h for h in REGION_HALF_LIVES], REGION_PINNED,
+                                  score_kind=kvev.KVEV_SCORE_MEMDECAY, rho=W["rho"],
+                                  attn_weight=W["attn_weight"], tau_scale=2.0,
+                                  decode_region=DECODE_REGION)
+        pp = kvev.PagedEvictionPass(Ly, W["n_q_heads"], W["n_kv_heads"], W["head_dim"], b, pps,
+                                    P, W["budget_tokens"], 0.05, 0.001, regions=table)
+        wl.fill(torch, pp.k_pool, pp.v_pool, pps)
+        lab = np.zeros(nb0 * P, np.uint8)
+        lab[:W["prefill"]] = region_labels(W["prefill"])
+        lab_t = torch.from_numpy(lab).cuda()
+        for s_ in range(b):
+            pp.region[s_ * pps * P:s_ * pps * P + nb0 * P].copy_(lab_t)
+    else:
+        wl = PagedDeviceWorkload(0, n_layers=Ly, batch=b, prefill=W["prefill"], page=P,
+                                 needle_blocks=W["needle_blocks"],
+                                 needle_period=W["needle_period"])
+        pp = kvev.PagedEvictionPass(Ly, W["n_q_heads"], W["n_kv_heads"], W["head_dim"], b, pps,
+                                    P, W["budget_blocks"], W["alpha"], W["beta"], n_backing=nb0,
+                                    table_len=nb0, age_mode=kvev.KVEV_AGE_SINCE_ACCESS)
+        wl.fill(torch, pp.k_pool, pp.v_pool, pps, pp.backing_k, pp.backing_v)
     n_steps = args.steps
     last = max(n_steps + 1, args.warmup)
     inputs = [wl.step_inputs(torch, t, pp.backing_k) for t in range(1, last + 1)]
     readmits = {}
-    for t in range(1 + W["needle_period"], last + 1, W["needle_period"]):
+    for t in range(1 + W.get("needle_period", last + 1), last + 1, W.get("needle_period", 1)):
         nd = wl.needle(t)
         readmits[t] = [(s, int(x)) for s in range(b) for x in nd[s]]
     stream = torch.cuda.current_stream()
@@ -534,15 +568,16 @@ def bench_paged(args, rank, world, local_rank):
     pp.begin(W["prefill"], stream)
     run_step(1)
     torch.cuda.synchronize()
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-    for _ in range(n1):
+    step1_ms = 0.0
+    for _ in range(n1):   # events around the step only (kvev_paged_begin may synchronize)
         pp.begin(W["prefill"], stream)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
         run_step(1)
-    s1.record(stream)
-    torch.cuda.synchronize()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        step1_ms += s0.elapsed_time(s1) / n1
     kvev.kvev_sync(pp.ctx)
-    step1_ms = s0.elapsed_time(s1) / n1
     step1_bytes = b * (W["prefill"] + 1) * row
 
     # end to end: host inputs (pinned) in, outputs out, every step
@@ -581,7 +616,7 @@ def bench_paged(args, rank, world, local_rank):
             "us_per_step": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (device Philox)",
             "config": dict(W, parallelism=f"replicas{world}", timed="decode steps 2..K+1",
-                           l2="inputs larger than L2 (~17 GB of K/V per step)"),
+                           l2="inputs larger than L2 (>= 5 GB of K/V per step)"),
             "frac_of_peak": {"measured": round(value / world / peak, 4),
                              "nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
                              "peak_kind": peak_kind},
@@ -590,7 +625,7 @@ def bench_paged(args, rank, world, local_rank):
                       "GB/s": round(step1_bytes / (step1_ms * 1e-3) / 1e9, 2),
                       "frac_measured": round(step1_bytes / (step1_ms * 1e-3) / 1e9 / peak, 4)},
             "readmitted_blocks": readmit_blocks,
-            "roofline": {"bound": "hbm", "kernel": "attention (paged)",
+            "roofline": {"bound": "hbm", "kernel": "attention (block table)",
                          "achieved": round(attn_achieved, 2) if attn_achieved else None,
                          "peak": peak, "unit": "GB/s",
                          "frac": round(attn_achieved / peak, 4) if attn_achieved else None,

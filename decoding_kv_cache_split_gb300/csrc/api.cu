@@ -72,7 +72,8 @@ struct Workspace {
     int32_t* len_s = nullptr;
     int32_t* page_s = nullptr;
     int32_t* tokens = nullptr;        // [batch] live tokens after the append
-    int32_t* sel = nullptr;           // [batch][budget] kept block slots
+    int32_t* sel = nullptr;           // [batch][units] kept block slots
+    int32_t* budgets = nullptr;       // [batch] blocks kept (region-aware selection)
     int32_t* readmit_page = nullptr;  // [1]
     size_t bytes = 0;
 };
@@ -115,13 +116,16 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base)
     w.len_s = (int32_t*)take(units * 4);
     w.page_s = (int32_t*)take(units * 4);
     w.tokens = (int32_t*)take((size_t)L.batch * 4);
-    w.sel = (int32_t*)take((size_t)L.batch * budget * 4);
+    w.sel = (int32_t*)take(units * 4);
+    w.budgets = (int32_t*)take((size_t)L.batch * 4);
     w.readmit_page = (int32_t*)take(4);
     w.bytes = off;
     return w;
 }
 
-kvev_status check_layout(const kvev_layout* L, int64_t budget) {
+// budget_tokens: the budget counts tokens even at block granularity
+// (region-aware MemDecay selection).
+kvev_status check_layout(const kvev_layout* L, int64_t budget, bool budget_tokens = false) {
     if (!L) return fail(KVEV_EINVAL, "layout is NULL");
     if (L->n_layers < 1 || L->n_q_heads < 1 || L->n_kv_heads < 1 || L->batch < 1)
         return fail(KVEV_EINVAL, "layout: n_layers, n_q_heads, n_kv_heads, batch must be >= 1");
@@ -130,8 +134,8 @@ kvev_status check_layout(const kvev_layout* L, int64_t budget) {
                     L->n_q_heads, L->n_kv_heads);
     if (L->head_dim != 64 && L->head_dim != 128)
         return fail(KVEV_EUNSUPPORTED, "layout: head_dim %d (supported: 64, 128)", L->head_dim);
-    if (L->n_q_heads / L->n_kv_heads != 4)
-        return fail(KVEV_EUNSUPPORTED, "layout: query heads per KV head %d (supported: 4)",
+    if (L->n_q_heads / L->n_kv_heads != 4 && L->n_q_heads / L->n_kv_heads != 8)
+        return fail(KVEV_EUNSUPPORTED, "layout: query heads per KV head %d (supported: 4, 8)",
                     L->n_q_heads / L->n_kv_heads);
     if (L->max_ctx < 2) return fail(KVEV_EINVAL, "layout: max_ctx must be >= 2");
     if (L->page_tokens != 1 && L->page_tokens != kTile)
@@ -141,7 +145,7 @@ kvev_status check_layout(const kvev_layout* L, int64_t budget) {
     if (L->max_ctx % L->page_tokens != 0)
         return fail(KVEV_EINVAL, "layout: max_ctx %d must be a multiple of page_tokens %d",
                     L->max_ctx, L->page_tokens);
-    const int64_t units = L->max_ctx / L->page_tokens;   // tokens, or pages per sequence
+    const int64_t units = budget_tokens ? L->max_ctx : L->max_ctx / L->page_tokens;
     if (budget < 1 || budget >= units)
         return fail(KVEV_EINVAL, "budget %lld must be in [1, %lld)", (long long)budget,
                     (long long)units);
@@ -168,6 +172,8 @@ struct kvev_ctx {
     int32_t refresh_mode = KVEV_REFRESH_FULL, refresh_period = 1;
     int32_t age_mode = KVEV_AGE_SINCE_INSERT, pool = KVEV_POOL_SUM;
     int32_t group = 4;
+    RegionParams rp{};
+    std::vector<int32_t> pin_blocks;  // per sequence: prefill blocks holding a pinned token
     int32_t len = 0, prefill_len = 0;
     std::vector<int32_t> ub_blocks;   // block mode: upper bound of each sequence's live blocks
     int64_t step = 0;
@@ -278,17 +284,47 @@ kvev_status kvev_workspace_size(const kvev_layout* layout, int64_t budget, size_
 }
 
 kvev_status kvev_create(const kvev_layout* layout, int64_t budget, int32_t granularity,
-                        float alpha, float beta, const void* regions, kvev_ctx** out) {
+                        float alpha, float beta, const kvev_region_table* regions,
+                        kvev_ctx** out) {
     if (!out) return fail(KVEV_EINVAL, "out is NULL");
     *out = nullptr;
-    kvev_status st = check_layout(layout, budget);
+    const bool memdecay = regions && regions->score_kind == KVEV_SCORE_MEMDECAY;
+    kvev_status st = check_layout(layout, budget, memdecay);
     if (st != KVEV_OK) return st;
     if (granularity != layout->page_tokens)
         return fail(KVEV_EINVAL, "granularity %d != layout.page_tokens %d", granularity,
                     layout->page_tokens);
     if (!(alpha > 0.f && alpha <= 1.f)) return fail(KVEV_EINVAL, "alpha must be in (0, 1]");
     if (!(beta >= 0.f)) return fail(KVEV_EINVAL, "beta must be >= 0 (+inf allowed)");
-    if (regions) return fail(KVEV_EUNSUPPORTED, "a region table needs page-granular eviction");
+    RegionParams rp{};
+    if (regions) {
+        const kvev_region_table& R = *regions;
+        if (layout->page_tokens == 1)
+            return fail(KVEV_EUNSUPPORTED, "a region table needs block granularity");
+        if (R.n_regions < 1 || R.n_regions > KVEV_MAX_REGIONS)
+            return fail(KVEV_EINVAL, "n_regions %d out of [1, %d]", R.n_regions, KVEV_MAX_REGIONS);
+        if (R.score_kind != KVEV_SCORE_LRFU && R.score_kind != KVEV_SCORE_MEMDECAY)
+            return fail(KVEV_EINVAL, "unknown score_kind %d", R.score_kind);
+        if (R.decode_region < 0 || R.decode_region >= R.n_regions)
+            return fail(KVEV_EINVAL, "decode_region %d out of range", R.decode_region);
+        if (!(R.rho >= 0.f && R.rho < 1.f) || !(R.attn_weight >= 0.f) || !(R.tau_scale >= 0.f))
+            return fail(KVEV_EINVAL, "rho must be in [0, 1), attn_weight and tau_scale >= 0");
+        rp.on = 1;
+        rp.memdecay = memdecay ? 1 : 0;
+        rp.decode_region = R.decode_region;
+        for (int r = 0; r < R.n_regions; ++r) {
+            if (!(R.base_priority[r] >= 0.f) || !(R.decay_lambda[r] >= 0.f))
+                return fail(KVEV_EINVAL, "region %d: base_priority and decay_lambda must be >= 0",
+                            r);
+            rp.base[r] = R.base_priority[r];
+            rp.lam[r] = R.decay_lambda[r];
+            if (R.pinned[r]) rp.pinned_mask |= 1u << r;
+        }
+        rp.rho = R.rho;
+        rp.attn_w = R.attn_weight;
+        rp.tau_scale = R.tau_scale;
+        rp.budget_tokens = (int32_t)budget;
+    }
 
     kvev_ctx* c = new (std::nothrow) kvev_ctx;
     if (!c) return fail(KVEV_ENOMEM, "host allocation failed");
@@ -297,6 +333,7 @@ kvev_status kvev_create(const kvev_layout* layout, int64_t budget, int32_t granu
     c->alpha = alpha;
     c->beta = beta;
     c->group = layout->n_q_heads / layout->n_kv_heads;
+    c->rp = rp;
     cudaError_t e = cudaGetDevice(&c->device);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
@@ -655,6 +692,9 @@ kvev_status check_paged(kvev_ctx* c, const kvev_paged_cache* pc, const kvev_bloc
     if (bs->table_len < pc->n_backing || bs->table_len < 1)
         return fail(KVEV_EINVAL, "table_len %d must be >= max(1, n_backing %d)", bs->table_len,
                     pc->n_backing);
+    if (c->rp.on && !bs->region) return fail(KVEV_EINVAL, "a region table needs state.region");
+    if (c->rp.memdecay && (!bs->tok_a || !bs->tok_t_ref))
+        return fail(KVEV_EINVAL, "MemDecay scoring needs state.tok_a and state.tok_t_ref");
     return KVEV_OK;
 }
 
@@ -688,6 +728,9 @@ PagedArgs paged_args(kvev_ctx* c, const kvev_paged_cache* pc, const kvev_block_s
     a.alpha = c->alpha;
     a.beta = c->beta;
     a.dbg_prio = c->dbg_prio;
+    a.sel_ld = c->rp.on ? pc->pages_per_seq : (int)c->budget;
+    a.budgets = c->ws.budgets;
+    a.rp = c->rp;
     return a;
 }
 
@@ -700,17 +743,38 @@ kvev_status kvev_paged_begin(kvev_ctx* c, const kvev_paged_cache* pc, const kvev
     kvev_status rc = check_paged(c, pc, bs);
     if (rc != KVEV_OK) return rc;
     const int P = c->lay.page_tokens, pps = pc->pages_per_seq;
-    if (prefill_tokens <= 0 || prefill_tokens % P != 0)
-        return fail(KVEV_EINVAL, "prefill_tokens %d must be a positive multiple of %d",
-                    prefill_tokens, P);
-    const int nb0 = prefill_tokens / P;
+    if (prefill_tokens <= 0)
+        return fail(KVEV_EINVAL, "prefill_tokens %d must be > 0", prefill_tokens);
+    if (!c->rp.memdecay && prefill_tokens % P != 0)
+        return fail(KVEV_EINVAL, "prefill_tokens %d must be a multiple of %d", prefill_tokens, P);
+    const int nb0 = (prefill_tokens + P - 1) / P;
     if (nb0 + 1 > pps)
         return fail(KVEV_EINVAL, "%d prefill blocks leave no free page (pages_per_seq %d)", nb0,
                     pps);
     cudaStream_t s = (cudaStream_t)stream;
     const PagedArgs a = paged_args(c, pc, bs, 0, true);
-    rc = timed_launch(c, kProfInit, s, "paged begin", [&] { return launch_paged_begin(a, nb0, s); });
+    rc = timed_launch(c, kProfInit, s, "paged begin",
+                      [&] { return launch_paged_begin(a, prefill_tokens, s); });
     if (rc != KVEV_OK) return rc;
+    c->pin_blocks.assign(c->lay.batch, 0);
+    if (c->rp.on && c->rp.pinned_mask) {   // bound the blocks no eviction can remove
+        std::vector<uint8_t> lab((size_t)c->lay.batch * pps * P);
+        cudaError_t e = cudaMemcpyAsync(lab.data(), bs->region, lab.size(),
+                                        cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "reading the prefill region labels");
+        for (int b = 0; b < c->lay.batch; ++b) {
+            const uint8_t* lb = lab.data() + (size_t)b * pps * P;
+            int n = 0;
+            for (int j = 0; j < nb0; ++j) {
+                bool pin = false;
+                for (int k = 0; k < P && j * P + k < prefill_tokens; ++k)
+                    pin |= ((c->rp.pinned_mask >> lb[(size_t)j * P + k]) & 1u) != 0;
+                n += pin;
+            }
+            c->pin_blocks[b] = n;
+        }
+    }
     c->len = prefill_tokens;
     c->prefill_len = prefill_tokens;
     c->ub_blocks.assign(c->lay.batch, nb0);
@@ -819,9 +883,19 @@ kvev_status kvev_paged_step(kvev_ctx* c, const void* q, const void* k_new, const
     sc.n_q = Ly.n_q_heads;
     sc.refresh = refresh ? 1 : 0;
     sc.alpha = c->alpha;
-    rc = timed_launch(c, kProfScore, s, "paged score",
-                      [&] { return launch_paged_score(sc, pa, G, ub, s); });
+    if (c->rp.memdecay) {
+        rc = timed_launch(c, kProfScore, s, "memdecay score",
+                          [&] { return launch_memdecay_score(sc, pa, G, ub, s); });
+    } else {
+        rc = timed_launch(c, kProfScore, s, "paged score",
+                          [&] { return launch_paged_score(sc, pa, G, ub, s); });
+    }
     if (rc != KVEV_OK) return rc;
+    if (c->rp.on) {
+        rc = timed_launch(c, kProfSelect, s, "block budget",
+                          [&] { return launch_block_budget(pa, s); });
+        if (rc != KVEV_OK) return rc;
+    }
 
     SelectArgs se{};
     se.n_units = pc->n_blocks;
@@ -830,7 +904,9 @@ kvev_status kvev_paged_step(kvev_ctx* c, const void* q, const void* k_new, const
     se.n_retained = n_retained;
     se.L = ub;
     se.max_ctx = pps;
-    se.budget = (int)c->budget;
+    se.budget = c->rp.on ? pps : (int)c->budget;
+    se.budgets = c->rp.on ? c->ws.budgets : nullptr;
+    se.ret_ld = pa.sel_ld;
     se.refresh = 1;   // a new block's score was set by the append
     rc = timed_launch(c, kProfSelect, s, "select",
                       [&] { return launch_select(se, Ly.batch, s); });
@@ -839,7 +915,18 @@ kvev_status kvev_paged_step(kvev_ctx* c, const void* q, const void* k_new, const
                       [&] { return launch_paged_compact(pa, s); });
     if (rc != KVEV_OK) return rc;
 
-    for (int32_t& u : c->ub_blocks) u = u + 1 < c->budget ? u + 1 : (int32_t)c->budget;
+    for (int b = 0; b < c->lay.batch; ++b) {
+        int32_t& u = c->ub_blocks[b];
+        // blocks kept at most: the budget, or (MemDecay) as many as hold the
+        // budget's tokens with all but the last full; more only when pinned
+        // blocks alone exceed it
+        int cap = c->rp.memdecay ? (int)(c->budget / c->lay.page_tokens) + 1 : (int)c->budget;
+        if (c->rp.on) {
+            if ((c->rp.pinned_mask >> c->rp.decode_region) & 1u) cap = pps;
+            else if (c->pin_blocks[b] > cap) cap = c->pin_blocks[b];
+        }
+        u = u + 1 < cap ? u + 1 : cap;
+    }
     c->step = step;
     return KVEV_OK;
 }
@@ -849,6 +936,7 @@ kvev_status kvev_readmit(kvev_ctx* c, const kvev_paged_cache* pc, const kvev_blo
     kvev_status rc = check_paged(c, pc, bs);
     if (rc != KVEV_OK) return rc;
     if (!c->begun) return fail(KVEV_ESTATE, "kvev_paged_begin must come first");
+    if (c->rp.memdecay) return fail(KVEV_EUNSUPPORTED, "re-admission needs LRFU scoring");
     if (seq < 0 || seq >= c->lay.batch)
         return fail(KVEV_EINVAL, "seq %d out of [0, %d)", seq, c->lay.batch);
     if (lid < 0 || lid >= pc->n_backing)

@@ -531,15 +531,17 @@ int ctas_per_sm_t() {
 
 int attn_warps_per_cta() { return kWarps; }
 
+// Instantiated shapes: head_dim 64 / 128, query heads per KV head 4 / 8.
 int attn_ctas_per_sm(int head_dim, int group) {
-    if (group != 4) return 0;
-    if (head_dim == 128) return ctas_per_sm_t<128, 4>();
-    if (head_dim == 64) return ctas_per_sm_t<64, 4>();
+    if (head_dim == 128 && group == 4) return ctas_per_sm_t<128, 4>();
+    if (head_dim == 64 && group == 4) return ctas_per_sm_t<64, 4>();
+    if (head_dim == 128 && group == 8) return ctas_per_sm_t<128, 8>();
+    if (head_dim == 64 && group == 8) return ctas_per_sm_t<64, 8>();
     return 0;
 }
 
 size_t attn_smem_bytes(int head_dim, int group) {
-    if (group != 4) return 0;
+    if (group != 4 && group != 8) return 0;
     if (head_dim == 128) return MmaCfg<128, 4, kStages, kWarps>::SMEM;
     if (head_dim == 64) return MmaCfg<64, 4, kStages, kWarps>::SMEM;
     return 0;
@@ -552,6 +554,10 @@ cudaError_t launch_attention(const AttnArgs& a, int head_dim, int group, int gri
         return paged ? launch_attn_t<128, 4, true>(a, grid, s) : launch_attn_t<128, 4, false>(a, grid, s);
     if (group == 4 && head_dim == 64)
         return paged ? launch_attn_t<64, 4, true>(a, grid, s) : launch_attn_t<64, 4, false>(a, grid, s);
+    if (group == 8 && head_dim == 128)
+        return paged ? launch_attn_t<128, 8, true>(a, grid, s) : launch_attn_t<128, 8, false>(a, grid, s);
+    if (group == 8 && head_dim == 64)
+        return paged ? launch_attn_t<64, 8, true>(a, grid, s) : launch_attn_t<64, 8, false>(a, grid, s);
     return cudaErrorInvalidValue;
 }
 
@@ -559,6 +565,8 @@ cudaError_t launch_combine(const CombineArgs& a, int head_dim, int group, cudaSt
     const dim3 grid(a.n_rows);
     if (group == 4 && head_dim == 128) return launch_pdl(combine_kernel<128, 4>, grid, dim3(128), 0, s, a);
     if (group == 4 && head_dim == 64) return launch_pdl(combine_kernel<64, 4>, grid, dim3(64), 0, s, a);
+    if (group == 8 && head_dim == 128) return launch_pdl(combine_kernel<128, 8>, grid, dim3(128), 0, s, a);
+    if (group == 8 && head_dim == 64) return launch_pdl(combine_kernel<64, 8>, grid, dim3(64), 0, s, a);
     return cudaErrorInvalidValue;
 }
 

@@ -115,6 +115,8 @@ struct SelectArgs {
     int32_t* retained;     // [b][budget]
     int32_t* n_retained;   // [b]
     int32_t L, max_ctx, budget, refresh;   // L: upper bound of n_units when n_units is set
+    const int32_t* budgets;   // [b] per-sequence kept count (null: budget)
+    int32_t ret_ld;           // row stride of retained (0: budget)
 };
 
 struct CompactArgs {
@@ -133,6 +135,18 @@ struct AppendArgs {
     const uint16_t* k_new; const uint16_t* v_new;   // [b][Ly][Hkv][D]
     kvev_state st;
     int32_t slot, t, pos, n_layers, batch, n_kv, max_ctx, head_dim;
+};
+
+// Region table as the kernels take it (by value).
+struct RegionParams {
+    int32_t on;             // a region table is set
+    int32_t memdecay;       // KVEV_SCORE_MEMDECAY
+    int32_t decode_region;
+    uint32_t pinned_mask;   // bit r: region r pinned
+    float base[KVEV_MAX_REGIONS];
+    float lam[KVEV_MAX_REGIONS];
+    float rho, attn_w, tau_scale;
+    int32_t budget_tokens;  // MemDecay budget in tokens
 };
 
 // Block-granular (paged) mode: the caller's structures plus this context's
@@ -157,6 +171,9 @@ struct PagedArgs {
     int32_t t, refresh, age_mode, pool_mean;
     float alpha, beta;
     float* dbg_prio;       // [b][pps] or null
+    int32_t sel_ld;        // row stride of sel and retained_lid (budget, or pps)
+    int32_t* budgets;      // [b] with a region table: blocks the selection keeps
+    RegionParams rp;
 };
 
 // ---- programmatic dependent launch ----------------------------------------
@@ -200,13 +217,16 @@ cudaError_t launch_select(const SelectArgs& a, int batch, cudaStream_t s);
 cudaError_t launch_compact(const CompactArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_init_state(kvev_state st, int batch, int max_ctx, int len, cudaStream_t s);
-cudaError_t launch_paged_begin(const PagedArgs& a, int prefill_blocks, cudaStream_t s);
+cudaError_t launch_paged_begin(const PagedArgs& a, int prefill_tokens, cudaStream_t s);
 cudaError_t launch_paged_append(const PagedArgs& a, const uint16_t* k_new, const uint16_t* v_new,
                                 cudaStream_t s);
 cudaError_t launch_paged_score(const ScoreArgs& sc, const PagedArgs& a, int group, int ub_blocks,
                                cudaStream_t s);
 cudaError_t launch_paged_compact(const PagedArgs& a, cudaStream_t s);
 cudaError_t launch_readmit(const PagedArgs& a, int seq, int lid, int persist, cudaStream_t s);
+cudaError_t launch_memdecay_score(const ScoreArgs& sc, const PagedArgs& a, int group,
+                                  int ub_blocks, cudaStream_t s);
+cudaError_t launch_block_budget(const PagedArgs& a, cudaStream_t s);
 
 enum : uint32_t { kStatusNoPage = 2u };   // a sequence ran out of free pages
 

@@ -84,10 +84,11 @@ __device__ __forceinline__ int block_scan_excl(int v, int* red, int* total) {
 }
 
 // ---------------------------------------------------------------- begin
-__global__ void __launch_bounds__(kBookThreads) paged_begin_kernel(const PagedArgs a, int nb0) {
+__global__ void __launch_bounds__(kBookThreads) paged_begin_kernel(const PagedArgs a, int n0) {
     griddep_wait();
     griddep_release();
     const int b = blockIdx.x, pps = a.c.pages_per_seq;
+    const int nb0 = (n0 + a.page - 1) / a.page;   // the last prefill block may be partial
     const size_t base = (size_t)b * pps;
     for (int j = threadIdx.x; j < pps; j += blockDim.x) {
         a.c.block_table[base + j] = j < nb0 ? b * pps + j : -1;
@@ -95,17 +96,24 @@ __global__ void __launch_bounds__(kBookThreads) paged_begin_kernel(const PagedAr
         a.st.t_ins[base + j] = 0;
         a.st.t_ref[base + j] = 0;
         a.st.lid[base + j] = j < nb0 ? j : -1;
-        a.st.len[base + j] = j < nb0 ? a.page : 0;
+        a.st.len[base + j] = j < nb0 ? min(a.page, n0 - j * a.page) : 0;
         // free stack: popping from the top yields the lowest free page first
         if (j < pps - nb0) a.c.free_pages[base + j] = b * pps + (pps - 1 - j);
     }
     for (int j = threadIdx.x; j < a.st.table_len; j += blockDim.x)
         a.st.table[(size_t)b * a.st.table_len + j] = __int_as_float(0x7fc00000);   // NaN
+    if (a.rp.memdecay) {   // prefill tokens: importance 0, clock at insertion (step 0)
+        for (int i = threadIdx.x; i < nb0 * a.page; i += blockDim.x) {
+            const size_t ti = ((size_t)b * pps) * a.page + i;   // page b*pps + i/P, token i%P
+            a.st.tok_a[ti] = 0.f;
+            a.st.tok_t_ref[ti] = 0;
+        }
+    }
     if (threadIdx.x == 0) {
         a.c.n_blocks[b] = nb0;
         a.c.n_free[b] = pps - nb0;
         a.c.next_lid[b] = nb0;
-        a.tokens[b] = nb0 * a.page;
+        a.tokens[b] = n0;
     }
 }
 
@@ -154,6 +162,14 @@ __global__ void __launch_bounds__(256) paged_append_kernel(const PagedArgs a,
             a.st.len[base + j] = tok + 1;
             a.st.t_ref[base + j] = a.t;   // insertion counts as an access
             s_tok = tok;
+            if (a.rp.on) {                // the new token's label and MemDecay state
+                const size_t ti = (size_t)page * a.page + tok;
+                a.st.region[ti] = (uint8_t)a.rp.decode_region;
+                if (a.rp.memdecay) {
+                    a.st.tok_a[ti] = 0.f;
+                    a.st.tok_t_ref[ti] = a.t;
+                }
+            }
         }
         s_page = page;
     }
@@ -257,13 +273,20 @@ __global__ void __launch_bounds__(kPagedThreads) score_paged_kernel(const ScoreA
         const unsigned bal = __ballot_sync(0xffffffffu, acc_tok);
         acc_blk = ((bal >> (threadIdx.x & 16)) & 0xffffu) != 0;
     }
+    bool pinned = false;
+    if (a.rp.on) {   // a block holding a token of a pinned region is never evicted
+        const int pg = blk_live ? a.c.block_table[base + j] : 0;
+        const bool pin_tok = live && ((a.rp.pinned_mask >> a.st.region[(size_t)pg * a.page + k]) & 1u);
+        const unsigned pb = __ballot_sync(0xffffffffu, pin_tok);
+        pinned = ((pb >> (threadIdx.x & 16)) & 0xffffu) != 0;
+    }
     if (k != 0 || !blk_live) return;
     int t_ref = a.st.t_ref[base + j];
     const int t_ins = a.st.t_ins[base + j];
     if (acc_blk) t_ref = a.t;
     const int age = a.t - (a.age_mode == KVEV_AGE_SINCE_ACCESS ? t_ref : t_ins);
     const float pr = age == 0 ? 0.0f : (1.0f - m) * -expm1f(-a.beta * (float)age);
-    a.keys[base + j] = order_bits(pr);
+    a.keys[base + j] = pinned ? 0u : order_bits(pr);
     a.m_s[base + j] = m;
     a.tref_s[base + j] = t_ref;
     a.tins_s[base + j] = t_ins;
@@ -286,7 +309,7 @@ __global__ void __launch_bounds__(kBookThreads) paged_compact_kernel(const Paged
     const size_t base = (size_t)b * pps;
     const int nb = a.c.n_blocks[b];
     const int nk = a.n_sel[b];
-    const int32_t* sel = a.sel + (size_t)b * a.budget;
+    const int32_t* sel = a.sel + (size_t)b * a.sel_ld;
     for (int j = threadIdx.x; j < nb; j += blockDim.x) s_kept[j] = 0;
     __syncthreads();
     for (int j = threadIdx.x; j < nk; j += blockDim.x) s_kept[sel[j]] = 1;
@@ -299,7 +322,7 @@ __global__ void __launch_bounds__(kBookThreads) paged_compact_kernel(const Paged
         a.st.t_ref[dst] = a.tref_s[src];
         a.st.lid[dst] = a.lid_s[src];
         a.st.len[dst] = a.len_s[src];
-        a.retained_lid[(size_t)b * a.budget + j] = a.lid_s[src];
+        a.retained_lid[(size_t)b * a.sel_ld + j] = a.lid_s[src];
     }
     int nf = a.c.n_free[b];
     for (int j0 = 0; j0 < nb; j0 += blockDim.x) {   // evicted: persist, free the page
@@ -309,7 +332,7 @@ __global__ void __launch_bounds__(kBookThreads) paged_compact_kernel(const Paged
         const int before = block_scan_excl(ev ? 1 : 0, red, &total);
         if (ev) {
             const int lid = a.lid_s[base + j];
-            if (lid >= 0 && lid < a.st.table_len)
+            if (!a.rp.memdecay && lid >= 0 && lid < a.st.table_len)
                 a.st.table[(size_t)b * a.st.table_len + lid] = a.m_s[base + j];
             a.c.free_pages[base + nf + before] = a.page_s[base + j];
         }
@@ -411,6 +434,163 @@ __global__ void readmit_copy_kernel(const PagedArgs a, int seq, int lid) {
     }
 }
 
+// ---------------------------------------------------------- region-aware
+// MemDecay scoring ("MemDecay: Region-Aware KV Cache Eviction ...", Sec.
+// III-C/D): one thread per token slot, 16 lanes = one block.  On refresh
+// (observation) steps the token's attention averaged over heads and layers
+// updates its importance (Eq. (2)) and may reset its decay clock (Eq. (3));
+// every step the token's retention score (Eq. (4)) is averaged over the
+// block (Eq. (5)).  Per-token state is indexed by page, so it never moves.
+// Key: 0 for a pinned block (always kept), else the order bits of -S_p
+// (the selection keeps the smallest keys: the highest page scores).
+template <int G, int NKV>
+__global__ void __launch_bounds__(kPagedThreads) score_memdecay_kernel(const ScoreArgs sc,
+                                                                       const PagedArgs a) {
+    constexpr int V4 = G / 4;
+    extern __shared__ float s_lse[];   // [Ly][NKV * G]
+    griddep_wait();
+    griddep_release();
+    const int b = blockIdx.y, pps = a.c.pages_per_seq;
+    const size_t base = (size_t)b * pps;
+    if (sc.refresh) {
+        const int nlse = sc.n_layers * NKV * G;
+        for (int k = threadIdx.x; k < nlse; k += blockDim.x) {
+            const int l = k / (NKV * G), h = k % (NKV * G);
+            s_lse[k] = sc.lse2[((size_t)l * sc.batch + b) * sc.n_q + h];
+        }
+    }
+    __syncthreads();
+    const int slot = blockIdx.x * kPagedThreads + threadIdx.x;
+    const int j = slot / a.page, k = slot % a.page;
+    const int nb = a.c.n_blocks[b];
+    const bool blk_live = j < nb;
+    const int len = blk_live ? a.st.len[base + j] : 0;
+    const bool live = k < len;
+    float s = 0.f;
+    bool pin = false;
+    if (live) {
+        const size_t ti = (size_t)a.c.block_table[base + j] * a.page + k;
+        float av = a.st.tok_a[ti];
+        int tref = a.st.tok_t_ref[ti];
+        const int r = a.st.region[ti];
+        if (sc.refresh) {
+            const size_t head_stride = (size_t)sc.logit_ld * G;
+            const size_t layer_stride = (size_t)sc.batch * NKV * head_stride;
+            const float* lbase = sc.logits + ((size_t)b * NKV) * head_stride + (size_t)slot * G;
+            float tot = 0.f;
+            for (int l = 0; l < sc.n_layers; ++l) {
+                float4 xb[NKV][V4];
+#pragma unroll
+                for (int g = 0; g < NKV; ++g)
+#pragma unroll
+                    for (int c = 0; c < V4; ++c)
+                        xb[g][c] = __ldcs(reinterpret_cast<const float4*>(
+                                              lbase + (size_t)l * layer_stride + g * head_stride) +
+                                          c);
+                const float4* lg = reinterpret_cast<const float4*>(s_lse + l * NKV * G);
+                float sl = 0.f;
+#pragma unroll
+                for (int g = 0; g < NKV; ++g)
+#pragma unroll
+                    for (int c = 0; c < V4; ++c) {
+                        const float4 x = xb[g][c], e = lg[g * V4 + c];
+                        const float p0 = fast_exp2(x.x - e.x), p1 = fast_exp2(x.y - e.y);
+                        const float p2 = fast_exp2(x.z - e.z), p3 = fast_exp2(x.w - e.w);
+                        if (sc.dbg_probs) {
+                            float* dp = sc.dbg_probs +
+                                        (((size_t)b * sc.n_layers + l) * sc.n_q + g * G + 4 * c) *
+                                            sc.max_ctx + slot;
+                            dp[0] = p0;
+                            dp[(size_t)sc.max_ctx] = p1;
+                            dp[2 * (size_t)sc.max_ctx] = p2;
+                            dp[3 * (size_t)sc.max_ctx] = p3;
+                        }
+                        sl += (p0 + p1) + (p2 + p3);
+                    }
+                tot += sl;
+            }
+            const float A = tot / (float)(sc.n_q * sc.n_layers);
+            av = fmaf(a.rp.rho, av, (1.0f - a.rp.rho) * A);
+            if (A >= a.rp.tau_scale / (float)a.tokens[b]) tref = a.t;
+            a.st.tok_a[ti] = av;
+            a.st.tok_t_ref[ti] = tref;
+        }
+        s = fmaf(a.rp.attn_w, av, a.rp.base[r] * expf(-a.rp.lam[r] * (float)(a.t - tref)));
+        pin = (a.rp.pinned_mask >> r) & 1u;
+    }
+    float sum = s;   // block sum over the 16 lanes of this block
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const unsigned pb = __ballot_sync(0xffffffffu, pin);
+    const bool pinned = ((pb >> (threadIdx.x & 16)) & 0xffffu) != 0;
+    if (k != 0 || !blk_live) return;
+    const float S = sum / (float)len;
+    a.keys[base + j] = pinned ? 0u : max(order_bits(-S), 1u);
+    a.m_s[base + j] = S;
+    a.tref_s[base + j] = a.st.t_ref[base + j];
+    a.tins_s[base + j] = a.st.t_ins[base + j];
+    a.lid_s[base + j] = a.st.lid[base + j];
+    a.len_s[base + j] = len;
+    a.page_s[base + j] = a.c.block_table[base + j];
+    if (a.dbg_prio) a.dbg_prio[base + j] = S;
+}
+
+// Blocks the selection keeps per sequence when a region table is set.
+// LRFU: the budget, or every pinned block when they are more.  MemDecay:
+// evicting the blocks of least S_p one by one until the tokens fit the
+// budget removes the j largest keys, j the least count whose blocks hold at
+// least the excess.  Every block but the last is full, so j is
+// ceil(excess / P), plus one when the partial last block is among those and
+// falls short.
+__global__ void __launch_bounds__(256) block_budget_kernel(const PagedArgs a) {
+    __shared__ int red[32];
+    griddep_wait();
+    griddep_release();
+    const int b = blockIdx.x, pps = a.c.pages_per_seq;
+    const size_t base = (size_t)b * pps;
+    const int nb = a.c.n_blocks[b];
+    if (!a.rp.memdecay) {
+        int pinned = 0;
+        for (int j = threadIdx.x; j < nb; j += blockDim.x) pinned += a.keys[base + j] == 0u;
+        pinned = block_sum_int(pinned, red);
+        if (threadIdx.x == 0) a.budgets[b] = max(a.budget, pinned);
+        return;
+    }
+    const int excess = a.tokens[b] - a.rp.budget_tokens;
+    if (excess <= 0 || nb == 0) {          // the same in every thread
+        if (threadIdx.x == 0) a.budgets[b] = nb;
+        return;
+    }
+    const int last = nb - 1;
+    const uint32_t kl = a.keys[base + last];
+    const int rl = a.len_s[base + last];
+    int n_free = 0, ahead = 0;   // evictable blocks; blocks ranked before the last one
+    for (int j = threadIdx.x; j < nb; j += blockDim.x) {
+        const uint32_t kj = a.keys[base + j];
+        n_free += kj != 0u;
+        ahead += j < last && kj <= kl;
+    }
+    n_free = block_sum_int(n_free, red);
+    ahead = block_sum_int(ahead, red);
+    if (threadIdx.x == 0) {
+        int j0 = min((excess + a.page - 1) / a.page, n_free);
+        const bool last_goes = kl != 0u && ahead >= nb - j0;
+        if (rl < a.page && last_goes && a.page * (j0 - 1) + rl < excess && j0 < n_free) ++j0;
+        a.budgets[b] = nb - j0;
+    }
+}
+
+template <int G>
+void* memdecay_score_for(int nkv) {
+    switch (nkv) {
+        case 1: return (void*)score_memdecay_kernel<G, 1>;
+        case 2: return (void*)score_memdecay_kernel<G, 2>;
+        case 4: return (void*)score_memdecay_kernel<G, 4>;
+        case 8: return (void*)score_memdecay_kernel<G, 8>;
+        default: return nullptr;
+    }
+}
+
 template <int G>
 void* paged_score_for(int nkv) {
     switch (nkv) {
@@ -424,9 +604,9 @@ void* paged_score_for(int nkv) {
 
 }  // namespace
 
-cudaError_t launch_paged_begin(const PagedArgs& a, int prefill_blocks, cudaStream_t s) {
+cudaError_t launch_paged_begin(const PagedArgs& a, int prefill_tokens, cudaStream_t s) {
     return launch_pdl(paged_begin_kernel, dim3(a.batch), dim3(kBookThreads), 0, s, a,
-                      prefill_blocks);
+                      prefill_tokens);
 }
 
 cudaError_t launch_paged_append(const PagedArgs& a, const uint16_t* k_new, const uint16_t* v_new,
@@ -444,6 +624,22 @@ cudaError_t launch_paged_score(const ScoreArgs& sc, const PagedArgs& a, int grou
     const size_t smem = sizeof(float) * (size_t)sc.n_layers * sc.n_q;
     return launch_pdl(reinterpret_cast<void (*)(ScoreArgs, PagedArgs)>(kern), grid,
                       dim3(kPagedThreads), smem, s, sc, a);
+}
+
+cudaError_t launch_memdecay_score(const ScoreArgs& sc, const PagedArgs& a, int group,
+                                  int ub_blocks, cudaStream_t s) {
+    void* kern = group == 4 ? memdecay_score_for<4>(sc.n_kv)
+                 : group == 8 ? memdecay_score_for<8>(sc.n_kv) : nullptr;
+    if (!kern || a.page != 16) return cudaErrorInvalidValue;
+    const int slots = ub_blocks * a.page;
+    const dim3 grid((slots + kPagedThreads - 1) / kPagedThreads, a.batch);
+    const size_t smem = sizeof(float) * (size_t)sc.n_layers * sc.n_q;
+    return launch_pdl(reinterpret_cast<void (*)(ScoreArgs, PagedArgs)>(kern), grid,
+                      dim3(kPagedThreads), smem, s, sc, a);
+}
+
+cudaError_t launch_block_budget(const PagedArgs& a, cudaStream_t s) {
+    return launch_pdl(block_budget_kernel, dim3(a.batch), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_paged_compact(const PagedArgs& a, cudaStream_t s) {

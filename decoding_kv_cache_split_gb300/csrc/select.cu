@@ -84,15 +84,20 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     const uint32_t rank = cta_rank();
     const int b = blockIdx.x / kCl;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int L = a.n_units ? min(a.n_units[blockIdx.x / kCl], a.L) : a.L, B = a.budget;
+    const int L = a.n_units ? min(a.n_units[blockIdx.x / kCl], a.L) : a.L;
+    const int B = a.budgets ? a.budgets[b] : a.budget;
     const uint32_t* gkeys = a.keys + (size_t)b * a.max_ctx;
-    int32_t* ret = a.retained + (size_t)b * B;
+    int32_t* ret = a.retained + (size_t)b * (a.ret_ld ? a.ret_ld : a.budget);
 
     if (!a.refresh && rank == 0 && tid == 0) {
         // new token's score: mean of the old tokens' scores (block sums in order)
         float s = 0.f;
         for (int k = 0; k < a.n_part; ++k) s += a.msum_part[(size_t)b * a.n_part + k];
         a.m_s[(size_t)b * a.max_ctx + L - 1] = L > 1 ? s / (float)(L - 1) : 0.f;
+    }
+    if (B <= 0) {   // keep nothing (the same for every CTA: no exchange)
+        if (rank == 0 && tid == 0) a.n_retained[b] = 0;
+        return;
     }
     if (L <= B) {   // nothing to evict: identity (the same for every CTA: no exchange)
         if (rank == 0) {

@@ -25,6 +25,8 @@ KVEV_REFRESH_FULL, KVEV_REFRESH_LAZY, KVEV_REFRESH_FROZEN = 0, 1, 2
 KVEV_AGE_SINCE_INSERT, KVEV_AGE_SINCE_ACCESS = 0, 1
 KVEV_POOL_SUM, KVEV_POOL_MEAN = 0, 1
 KVEV_BF16 = 0
+KVEV_MAX_REGIONS = 16
+KVEV_SCORE_LRFU, KVEV_SCORE_MEMDECAY = 0, 1
 KVEV_PROFILE_SLOTS = 8
 PROFILE_NAMES = ["append", "attention", "combine", "score", "select", "compact", "init_state",
                  "readmit"]
@@ -72,7 +74,34 @@ class kvev_paged_cache(ctypes.Structure):
 class kvev_block_state(ctypes.Structure):
     _fields_ = [("score", ctypes.c_void_p), ("t_ins", ctypes.c_void_p),
                 ("t_ref", ctypes.c_void_p), ("lid", ctypes.c_void_p), ("len", ctypes.c_void_p),
-                ("table", ctypes.c_void_p), ("table_len", ctypes.c_int32)]
+                ("table", ctypes.c_void_p), ("table_len", ctypes.c_int32),
+                ("region", ctypes.c_void_p), ("tok_a", ctypes.c_void_p),
+                ("tok_t_ref", ctypes.c_void_p)]
+
+
+class kvev_region_table(ctypes.Structure):
+    _fields_ = [("n_regions", ctypes.c_int32),
+                ("base_priority", ctypes.c_float * KVEV_MAX_REGIONS),
+                ("decay_lambda", ctypes.c_float * KVEV_MAX_REGIONS),
+                ("pinned", ctypes.c_uint8 * KVEV_MAX_REGIONS),
+                ("score_kind", ctypes.c_int32), ("rho", ctypes.c_float),
+                ("attn_weight", ctypes.c_float), ("tau_scale", ctypes.c_float),
+                ("decode_region", ctypes.c_int32)]
+
+
+def region_table(base, lam, pinned, *, score_kind=KVEV_SCORE_MEMDECAY, rho=0.9,
+                 attn_weight=0.5, tau_scale=2.0, decode_region=0) -> kvev_region_table:
+    """A kvev_region_table from per-region lists."""
+    n = len(base)
+    t = kvev_region_table()
+    t.n_regions = n
+    for r in range(n):
+        t.base_priority[r] = float(base[r])
+        t.decay_lambda[r] = float(lam[r])
+        t.pinned[r] = 1 if pinned[r] else 0
+    t.score_kind, t.rho, t.attn_weight = int(score_kind), float(rho), float(attn_weight)
+    t.tau_scale, t.decode_region = float(tau_scale), int(decode_region)
+    return t
 
 
 _lib = None
@@ -147,8 +176,9 @@ def _check(status: int, ctx=None):
 def kvev_create(layout: kvev_layout, budget: int, granularity: int, alpha: float, beta: float,
                 regions=None):
     out = ctypes.c_void_p()
+    reg = ctypes.byref(regions) if isinstance(regions, kvev_region_table) else _ptr(regions)
     _check(lib().kvev_create(ctypes.byref(layout), int(budget), int(granularity), float(alpha),
-                             float(beta), _ptr(regions), ctypes.byref(out)))
+                             float(beta), reg, ctypes.byref(out)))
     return out
 
 
@@ -339,13 +369,14 @@ class PagedEvictionPass:
     def __init__(self, n_layers, n_q_heads, n_kv_heads, head_dim, batch, pages_per_seq, page,
                  budget, alpha, beta, *, n_backing=0, table_len=None,
                  age_mode=KVEV_AGE_SINCE_ACCESS, pool=KVEV_POOL_SUM, refresh=KVEV_REFRESH_FULL,
-                 period=1, device="cuda"):
+                 period=1, regions=None, device="cuda"):
         import torch
         self.torch = torch
         self.page, self.pps, self.budget = int(page), int(pages_per_seq), int(budget)
         self.layout = kvev_layout(n_layers, n_q_heads, n_kv_heads, head_dim, batch,
                                   self.pps * self.page, self.page, KVEV_BF16)
-        self.ctx = kvev_create(self.layout, budget, self.page, alpha, beta)
+        self.regions = regions
+        self.ctx = kvev_create(self.layout, budget, self.page, alpha, beta, regions)
         kvev_configure(self.ctx, age_mode, pool)
         kvev_refresh_mode(self.ctx, refresh, period)
         pshape = (batch * self.pps, n_layers, n_kv_heads, self.page, head_dim)
@@ -369,7 +400,12 @@ class PagedEvictionPass:
         self.table = torch.zeros((batch, self.table_len), dtype=torch.float32, device=device)
         self.out = torch.zeros((batch, n_layers, n_q_heads, head_dim), dtype=torch.float32,
                                device=device)
-        self.retained_lid = torch.zeros((batch, self.budget), **i32)
+        ntok = batch * self.pps * self.page
+        self.region = torch.zeros((ntok,), dtype=torch.uint8, device=device)
+        self.tok_a = torch.zeros((ntok,), dtype=torch.float32, device=device)
+        self.tok_t_ref = torch.zeros((ntok,), **i32)
+        self.retained_lid = torch.zeros((batch, self.pps if regions is not None else self.budget),
+                                        **i32)
         self.n_retained = torch.zeros((batch,), **i32)
         self.cache = kvev_paged_cache(
             self.k_pool.data_ptr(), self.v_pool.data_ptr(), self.pps, self.block_table.data_ptr(),
@@ -378,7 +414,9 @@ class PagedEvictionPass:
             int(n_backing))
         self.state = kvev_block_state(self.score.data_ptr(), self.t_ins.data_ptr(),
                                       self.t_ref.data_ptr(), self.lid.data_ptr(),
-                                      self.len.data_ptr(), self.table.data_ptr(), self.table_len)
+                                      self.len.data_ptr(), self.table.data_ptr(), self.table_len,
+                                      self.region.data_ptr(), self.tok_a.data_ptr(),
+                                      self.tok_t_ref.data_ptr())
         self.step_no = 0
 
     def begin(self, prefill_tokens: int, stream=None):

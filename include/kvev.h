@@ -110,17 +110,53 @@ typedef struct {
 
 typedef struct kvev_ctx kvev_ctx;
 
+/* Region table (block granularity only): every cached token carries a
+ * region label (uint8, < n_regions) supplied by the caller for the prefill;
+ * decoded tokens take `decode_region`.  A block holding a token of a pinned
+ * region is never evicted ("MemDecay: Region-Aware KV Cache Eviction ...",
+ * Sec. III-A and IV-A: pinning protects whole pages).
+ *   score_kind KVEV_SCORE_LRFU: the LRFU block priority of kvev_paged_step,
+ *     with pinning; base_priority, decay_lambda, rho, attn_weight, tau_scale
+ *     are unused.
+ *   score_kind KVEV_SCORE_MEMDECAY: the MemDecay policy replaces the block
+ *     EMA and priority.  Per token, at refresh (observation) steps:
+ *       a <- rho a + (1 - rho) A,  A = the token's attention averaged over
+ *            heads and layers                                     (Eq. (2))
+ *       t_ref <- t  when A >= tau_scale / |K_t|                   (Eq. (3))
+ *     and every step, for block p of the cache:
+ *       s = base_priority[r] exp(-decay_lambda[r] (t - t_ref)) + attn_weight a
+ *                                                                  (Eq. (4))
+ *       S_p = mean of s over the block's tokens                   (Eq. (5))
+ *     and while the cache holds more than `budget` TOKENS, the non-pinned
+ *     block of least S_p is evicted (Algorithm 1; equal S_p: the later slot
+ *     goes first).  kvev_create's alpha and beta are unused. */
+enum { KVEV_MAX_REGIONS = 16 };
+typedef enum { KVEV_SCORE_LRFU = 0, KVEV_SCORE_MEMDECAY = 1 } kvev_score_kind;
+typedef struct {
+    int32_t n_regions;                        /* 1 .. KVEV_MAX_REGIONS */
+    float base_priority[KVEV_MAX_REGIONS];    /* b_r >= 0 */
+    float decay_lambda[KVEV_MAX_REGIONS];     /* lambda_r >= 0, per decode step */
+    uint8_t pinned[KVEV_MAX_REGIONS];         /* != 0: never evicted */
+    int32_t score_kind;                       /* kvev_score_kind */
+    float rho;                                /* in [0, 1) */
+    float attn_weight;                        /* alpha of Eq. (4), >= 0 */
+    float tau_scale;                          /* tau = tau_scale / |K_t|, >= 0 */
+    int32_t decode_region;                    /* label of decoded tokens */
+} kvev_region_table;
+
 /* Create a context for `layout` with a budget of `budget` retained tokens
  * per sequence (1 <= budget < max_ctx).  `granularity` must equal
  * layout->page_tokens (1, or 16 for block-granular eviction, where the budget
- * counts blocks).  `alpha` in (0, 1] weights the new observation in
- * the EMA; `beta` >= 0 is the recency coefficient (+INFINITY allowed: rank by
- * score, newest token protected).  `regions` must be NULL (no region table
- * for token-granular eviction).  Allocates the context's device scratch on
- * the current device (kvev_workspace_size bytes).  Defaults: full refresh,
- * age since insertion, head-sum pooling. */
+ * counts blocks, or tokens under KVEV_SCORE_MEMDECAY).  `alpha` in (0, 1]
+ * weights the new observation in the EMA; `beta` >= 0 is the recency
+ * coefficient (+INFINITY allowed: rank by score, newest token protected).
+ * `regions` is a kvev_region_table (copied) or NULL; it needs block
+ * granularity.  Allocates the context's device scratch on the current
+ * device (kvev_workspace_size bytes).  Defaults: full refresh, age since
+ * insertion, head-sum pooling. */
 kvev_status kvev_create(const kvev_layout* layout, int64_t budget, int32_t granularity,
-                        float alpha, float beta, const void* regions, kvev_ctx** out);
+                        float alpha, float beta, const kvev_region_table* regions,
+                        kvev_ctx** out);
 
 /* Release the context and its scratch.  NULL is a no-op. */
 void kvev_destroy(kvev_ctx* ctx);
@@ -244,30 +280,42 @@ typedef struct {
     float* table;            /* [batch][table_len] persisted score per logical block
                                 (NaN = never stored) */
     int32_t table_len;       /* > every logical id used */
+    /* Per token, indexed [page][P] (pages never move), with a region table: */
+    uint8_t* region;         /* region label; the caller writes the prefill's */
+    float* tok_a;            /* KVEV_SCORE_MEMDECAY: importance a */
+    int32_t* tok_t_ref;      /* KVEV_SCORE_MEMDECAY: decay clock t_ref */
 } kvev_block_state;
 
-/* Start a paged run.  `prefill_tokens` (a multiple of P, > 0) per sequence
- * are already in the pool: block j of sequence b at page b*pps + j.  Sets
- * the block tables, free lists, per-block state (score 0, t_ins = t_ref = 0,
- * lid j, len P), empties the persisted table; the next step is 1. */
+/* Start a paged run.  `prefill_tokens` (> 0) per sequence are already in
+ * the pool: block j of sequence b at page b*pps + j, the last one partial
+ * when P does not divide prefill_tokens.  Sets the block tables, free lists,
+ * per-block state (score 0, t_ins = t_ref = 0, lid j), empties the persisted
+ * table, and with KVEV_SCORE_MEMDECAY sets tok_a = 0, tok_t_ref = 0 for the
+ * prefill tokens; the next step is 1.  With a region table it reads the
+ * prefill labels back to the host (to bound the pinned blocks) and
+ * synchronizes `stream`. */
 kvev_status kvev_paged_begin(kvev_ctx* ctx, const kvev_paged_cache* cache,
                              const kvev_block_state* state, int32_t prefill_tokens, void* stream);
 
 /* One paged decode step `step` (previous + 1).  q, k_new, v_new, out as in
- * kvev_step.  retained_lid [batch][budget] int32 (device): logical ids of the
- * kept blocks in slot order; n_retained [batch] int32 (device).  Launches
+ * kvev_step.  retained_lid [batch][budget] int32 (device; [batch][pps] with a
+ * region table): logical ids of the kept blocks in slot order; n_retained
+ * [batch] int32 (device).  With a region table and LRFU scoring, every
+ * pinned block is kept even when they outnumber the budget.  Launches
  * append, attention, combine, block scoring, selection and compaction.  The
  * host keeps an upper bound of each sequence's live blocks; a step whose
  * new block could find no free page returns KVEV_EINVAL before launching.
  * Debug outputs (kvev_set_debug) are indexed by block slot: probabilities
  * [batch][n_layers][n_q_heads][max_ctx] at slot j*P + k for token k of
- * block j, priorities [batch][pps]. */
+ * block j, priorities [batch][pps] (the page score S_p under
+ * KVEV_SCORE_MEMDECAY). */
 kvev_status kvev_paged_step(kvev_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                             const kvev_paged_cache* cache, const kvev_block_state* state,
                             int64_t step, float* out, int32_t* retained_lid,
                             int32_t* n_retained, void* stream);
 
-/* Re-admit prefill block `lid` (0 <= lid < n_backing) of sequence `seq`
+/* Re-admit prefill block `lid` (0 <= lid < n_backing, a full block) of
+ * sequence `seq` (LRFU scoring only)
  * before the next step (a no-op when it is resident): a free page receives
  * the block's K/V from the backing tier, the block returns to its slot
  * (ascending logical id), its score is the persisted one (persist != 0 and

@@ -44,7 +44,7 @@ def layout(**kw):
 @pytest.mark.parametrize("kw,budget,status", [
     (dict(head_dim=96), 8, kvev.KVEV_EUNSUPPORTED),
     (dict(n_q_heads=7), 8, kvev.KVEV_EINVAL),
-    (dict(n_q_heads=16), 8, kvev.KVEV_EUNSUPPORTED),
+    (dict(n_q_heads=32), 8, kvev.KVEV_EUNSUPPORTED),             # 16 query heads per KV head
     (dict(batch=0), 8, kvev.KVEV_EINVAL),
     (dict(page_tokens=8), 4, kvev.KVEV_EUNSUPPORTED),
     (dict(page_tokens=16), 4, kvev.KVEV_EINVAL),                # budget counts pages: 4 of 4
@@ -87,3 +87,37 @@ def test_binding_raises_with_message(lib):
         kvev.kvev_create(layout(head_dim=80), 8, 1, 0.05, 0.001)
     assert ei.value.status == kvev.KVEV_EUNSUPPORTED
     assert "head_dim" in str(ei.value)
+
+
+def _table(**kw):
+    t = kvev.region_table([1.0, 1.0], [0.1, 0.2], [True, False], decode_region=1)
+    for k, v in kw.items():
+        setattr(t, k, v)
+    return t
+
+
+@pytest.mark.parametrize("lay_kw,table_kw,status", [
+    ({}, {}, kvev.KVEV_EUNSUPPORTED),                                  # token granularity
+    (dict(page_tokens=16), dict(n_regions=0), kvev.KVEV_EINVAL),
+    (dict(page_tokens=16), dict(n_regions=17), kvev.KVEV_EINVAL),
+    (dict(page_tokens=16), dict(decode_region=2), kvev.KVEV_EINVAL),
+    (dict(page_tokens=16), dict(rho=1.0), kvev.KVEV_EINVAL),
+    (dict(page_tokens=16), dict(score_kind=7), kvev.KVEV_EINVAL),
+])
+def test_create_rejects_bad_region_tables(lib, lay_kw, table_kw, status):
+    out = ctypes.c_void_p()
+    lay = layout(max_ctx=256, **lay_kw)
+    t = _table(**table_kw)
+    rc = lib.kvev_create(ctypes.byref(lay), 8, lay.page_tokens, 0.05, 0.001, ctypes.byref(t),
+                         ctypes.byref(out))
+    assert rc == status
+    assert out.value is None
+
+
+def test_region_table_layout_matches_the_header():
+    """Field offsets of the ctypes mirror (the C struct has no padding
+    before score_kind: 4 + 64 + 64 + 16 bytes)."""
+    T = kvev.kvev_region_table
+    assert T.base_priority.offset == 4 and T.decay_lambda.offset == 68
+    assert T.pinned.offset == 132 and T.score_kind.offset == 148
+    assert ctypes.sizeof(T) == 168

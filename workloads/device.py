@@ -32,22 +32,21 @@ def _seed(seed: int, family: int, index: int) -> int:
 
 class PagedDeviceWorkload:
     """Block-granular workload: every sequence has ``prefill`` tokens of
-    N(0,1) keys and values in ``page``-token blocks; each step's query is
+    N(0,1) keys and values in ``page``-token blocks (rows past the prefill in
+    a partial last block are drawn too and never read); each step's query is
     N(0,1) plus ``needle_weight`` times the mean prefill key of the sequence's
     needle blocks (``needle_blocks`` distinct prefill blocks, re-drawn at
-    steps 1, 1 + P, 1 + 2P, ... with P = ``needle_period``); new keys and
-    values are N(0,1)."""
+    steps 1, 1 + P, 1 + 2P, ... with P = ``needle_period``; none when 0); new
+    keys and values are N(0,1)."""
 
     def __init__(self, seed: int = 0, *, n_layers: int = 32, n_q_heads: int = 32,
                  n_kv_heads: int = 8, head_dim: int = 128, batch: int = 64,
                  prefill: int = 8192, page: int = 16, needle_blocks: int = 4,
                  needle_period: int = 200, needle_weight: float = 0.5):
-        if prefill % page:
-            raise ValueError("prefill must be whole blocks")
         self.seed = int(seed)
         self.n_layers, self.n_q_heads, self.n_kv_heads = n_layers, n_q_heads, n_kv_heads
         self.head_dim, self.batch, self.prefill, self.page = head_dim, batch, prefill, page
-        self.n_blocks = prefill // page
+        self.n_blocks = -(-prefill // page)   # the last block may be partial
         self.needle_blocks_n = int(needle_blocks)
         self.needle_period = int(needle_period)
         self.needle_weight = float(needle_weight)
@@ -95,10 +94,11 @@ class PagedDeviceWorkload:
         g = self.n_q_heads // self.n_kv_heads
         q = self._normal(torch, (self.batch, self.n_layers, self.n_q_heads, self.head_dim),
                          _D_Q, step, device).float()
-        idx = torch.from_numpy(self.needle(step)).to(device)
-        sel = backing_k[torch.arange(self.batch, device=device)[:, None], idx]
-        mean = sel.float().mean(dim=(1, 4))                # [b][Ly][Hkv][d]
-        q = q + self.needle_weight * mean.repeat_interleave(g, dim=2)
+        if self.needle_blocks_n:
+            idx = torch.from_numpy(self.needle(step)).to(device)
+            sel = backing_k[torch.arange(self.batch, device=device)[:, None], idx]
+            mean = sel.float().mean(dim=(1, 4))                # [b][Ly][Hkv][d]
+            q = q + self.needle_weight * mean.repeat_interleave(g, dim=2)
         kv = (self.batch, self.n_layers, self.n_kv_heads, self.head_dim)
         return (q.to(torch.bfloat16), self._normal(torch, kv, _D_KNEW, step, device),
                 self._normal(torch, kv, _D_VNEW, step, device))
