@@ -1,0 +1,167 @@
+"""Pins for the two-tier (QEvict) window-routing oracle and its INT2 codec."""
+import numpy as np
+import pytest
+
+from oracle import qevict as QE
+from workloads import f32_to_bf16_bits
+
+
+def _bits(x):
+    return f32_to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def _params(**kw):
+    base = dict(n_layers=1, n_q_heads=1, n_kv_heads=1, head_dim=32, k_full=1, k_quant=1,
+                alpha=0.05, window=32, n_sink=1, n_recent=2, omega=1, group=32)
+    base.update(kw)
+    return QE.QParams(**base)
+
+
+def test_tier_capacities_worked_example():
+    """Sec. 4.5: B_hist 100 MB, q = 0.70, 1 MB full and ~0.131 MB INT2 per
+    window give K_f = 30 and K_q = 534."""
+    assert QE.capacities(100.0, 0.70, 1.0, 0.131) == (30, 534)
+
+
+def test_int2_footprint_per_token_layer():
+    """Llama-8B geometry: bf16 K+V is 4096 B per token-layer; the INT2 tier
+    holds 512 B of codes plus 256 B of fp16 scale/zero (groups of 32)."""
+    assert QE.int2_bytes_per_token_layer(8, 128) == 768
+    assert QE.int2_bytes_per_token_layer(8, 128, group=64) == 640
+
+
+def test_codec_exact_on_representable_groups():
+    """Values zero + code * scale with fp16-exact zero and scale come back
+    bit for bit; the group's min codes to 0 and its max to 3."""
+    x = np.array([[1.0, 1.5, 2.0, 2.5] * 8], dtype=np.float32)      # one group of 32
+    codes, scale, zero = QE.quantize_groups(x, axis=1)
+    assert float(zero[0]) == 1.0 and float(scale[0]) == 0.5
+    assert codes[0].tolist() == [0, 1, 2, 3] * 8
+    assert np.array_equal(QE.dequantize(codes, scale, zero, axis=1), x)
+
+
+def test_codec_error_bound_and_constant_groups():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((64, 32)).astype(np.float32) * 3
+    codes, scale, zero = QE.quantize_groups(x, axis=1)
+    assert codes.min() >= 0 and codes.max() <= 3
+    xh = QE.dequantize(codes, scale, zero, axis=1)
+    s = scale.astype(np.float32)[:, None]
+    slack = np.abs(zero.astype(np.float32) - x.min(axis=1))[:, None] + 1e-6 * np.abs(x)
+    assert np.all(np.abs(x - xh) <= 0.5 * s + slack + 1e-6)
+    c = np.full((2, 32), 0.75, np.float32)                            # max = min: scale 0
+    codes, scale, zero = QE.quantize_groups(c, axis=1)
+    assert np.all(scale == 0) and np.all(codes == 0)
+    assert np.array_equal(QE.dequantize(codes, scale, zero, axis=1), c)
+
+
+def test_keys_per_channel_values_per_token():
+    """Keys constant along tokens within a channel and values constant along
+    channels within a token quantize with scale 0 and come back exactly;
+    the other orientation would spread each group over distinct values."""
+    W, d = 64, 64
+    k = np.tile(np.arange(d, dtype=np.float32) / 8, (W, 1))           # varies by channel
+    v = np.tile(np.arange(W, dtype=np.float32)[:, None] / 8, (1, d))  # varies by token
+    led = QE.quantize_window(_bits(k)[None, None], _bits(v)[None, None], group=32)
+    assert np.all(led["ks"] == 0) and np.all(led["vs"] == 0)
+    kd, vd = QE.dequantize_window(led)
+    assert np.array_equal(kd[0, 0], k) and np.array_equal(vd[0, 0], v)
+
+
+def test_window_partition():
+    """Sinks [0, 5), windows of 128 from position 5, the rest is the tail:
+    131072 tokens make 1023 windows and a 123-token tail."""
+    P = _params(window=128, n_sink=5)
+    z = np.zeros((1, 1, 5 + 128 * 3 + 10, 32), np.uint16)
+    seq = QE.QSequence.from_prefill(P, z, z)
+    assert len(seq.windows) == 3 and seq.K_tail.shape[2] == 10 and seq.K_sink.shape[2] == 5
+    assert (131072 - 5) // 128 == 1023 and (131072 - 5) % 128 == 123
+
+
+def test_window_score_is_a_layer_sequential_ema_of_head_mean_mass():
+    """Uniform attention (zero keys): every token gets 1/n in every head, so
+    a window's per-layer mass is W/n and after one step over Ly layers its
+    score is (1 - (1 - alpha)^Ly) W / n."""
+    P = _params(n_layers=3, n_q_heads=2, n_kv_heads=1, alpha=0.2, omega=100)
+    z = np.zeros((3, 1, 1 + 32 * 2 + 3, 32), np.uint16)
+    seq = QE.QSequence.from_prefill(P, z, z)
+    zq = np.zeros((3, 2, 32), np.uint16)
+    zk = np.zeros((3, 1, 32), np.uint16)
+    res = QE.step(P, seq, 1, zq, zk, zk)
+    n = 1 + 64 + 4
+    want = (1 - 0.8 ** 3) * 32 / n
+    assert res["m"][0] == pytest.approx(want, rel=1e-12)
+    assert res["m"][1] == pytest.approx(want, rel=1e-12)
+
+
+def _seq_with_scores(P, scores, tail=3):
+    nw = len(scores)
+    rng = np.random.default_rng(1)
+    K = _bits(rng.standard_normal((1, 1, P.n_sink + P.window * nw + tail, P.head_dim)))
+    seq = QE.QSequence.from_prefill(P, K, K.copy())
+    for w, m in zip(seq.windows, scores):
+        w.m = m
+    return seq
+
+
+def test_routing_top_k_full_next_k_quantized_rest_evicted():
+    """Eq. (5): rank candidates by score (ties: lower index first); the top
+    K_f are Full, the next K_q Quantized, the rest Evicted; a window not yet
+    aged out of the recent region is no candidate."""
+    P = _params(k_full=2, k_quant=1, n_recent=34)
+    seq = _seq_with_scores(P, [0.1, 0.5, 0.3, 0.3, 0.9, 0.0, 0.7], tail=3)
+    # L = 1 + 7*32 + 3 = 228, horizon 194: window 6 (ends at 225) is not aged;
+    # windows 2 and 3 tie and the lower index takes the one quantized slot
+    QE.route(P, seq)
+    assert seq.tiers() == ["E", "F", "Q", "E", "F", "E", "U"]
+    QE.route(P, seq)                                # evicted windows never come back
+    assert seq.tiers()[0] == "E" and seq.tiers()[3] == "E" and seq.tiers()[5] == "E"
+    assert seq.windows[2].ledger is not None and seq.windows[2].K is None
+
+
+def test_ledger_is_reused_across_migrations():
+    """A window is quantized on its first demotion only; promoted, it holds
+    the bf16 rounding of its dequantized values; demoted again it keeps the
+    ledger entry of the first demotion."""
+    P = _params(k_full=1, k_quant=1, n_recent=1)
+    seq = _seq_with_scores(P, [0.2, 0.8], tail=1)
+    QE.route(P, seq)                                # window 0 -> Q (first quantization)
+    led = seq.windows[0].ledger
+    first = {k: v.copy() for k, v in led.items() if isinstance(v, np.ndarray)}
+    assert seq.windows[0].K is None                 # the full-precision copy is dropped
+    seq.windows[0].m, seq.windows[1].m = 0.9, 0.1
+    QE.route(P, seq)                                # promote 0, demote 1
+    w0 = seq.windows[0]
+    kd, vd = QE.dequantize_window(w0.ledger)
+    assert w0.tier == "F" and np.array_equal(w0.K, _bits(kd)) and np.array_equal(w0.V, _bits(vd))
+    seq.windows[0].m, seq.windows[1].m = 0.1, 0.9
+    QE.route(P, seq)                                # demote 0 again: same codes
+    assert seq.windows[0].ledger is led             # the ledger entry itself is reused
+    for k in first:
+        assert np.array_equal(seq.windows[0].ledger[k], first[k])
+
+
+def test_evicted_window_no_longer_attended_and_quantized_one_is():
+    """A window whose keys would take nearly all attention stops affecting
+    the output once evicted; a quantized window with fp16-exact values is
+    attended exactly as its dequantized values say."""
+    P = _params(k_full=0, k_quant=1, n_recent=1, omega=1)
+    d = 32
+    K = np.zeros((1, 1, 1 + 64 + 1, d), np.float32)
+    V = np.zeros_like(K)
+    K[0, 0, 1:33, 0] = 20.0                         # window 0: dominant keys
+    V[0, 0, 1:33, 1] = 7.0
+    V[0, 0, 33:65, 2] = np.tile([0.75, 1.5, 3.0, 6.0], 8)   # window 1: val/3 fp16-exact
+    seq = QE.QSequence.from_prefill(P, _bits(K), _bits(V))
+    seq.windows[0].m, seq.windows[1].m = 0.0, 1.0
+    QE.route(P, seq)
+    assert seq.tiers() == ["E", "Q"]
+    q = np.zeros((1, 1, d), np.float32)
+    q[0, 0, 0] = 1.0
+    z = np.zeros((1, 1, d), np.float32)
+    res = QE.step(P, seq, 3, _bits(q), _bits(z), _bits(z))
+    out = res["out"][0, 0]
+    # accessible: sink (0), window 1 (32 tokens), tail token, new token: all logits 0
+    n = 1 + 32 + 2
+    assert out[1] == pytest.approx(0.0, abs=1e-15)
+    assert out[2] == pytest.approx(np.tile([0.75, 1.5, 3.0, 6.0], 8).sum() / n, rel=1e-12)
