@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 #include <vector>
 
@@ -75,11 +76,34 @@ struct Workspace {
     int32_t* sel = nullptr;           // [batch][units] kept block slots
     int32_t* budgets = nullptr;       // [batch] blocks kept (region-aware selection)
     int32_t* readmit_page = nullptr;  // [1]
+    // two-tier mode (page_tokens = window)
+    int32_t* t_bt = nullptr;          // [batch][bt_ld] attention block list
+    int32_t* t_bpos = nullptr;
+    int32_t* t_blen = nullptr;
+    int32_t* t_nblk = nullptr;        // [batch]
+    int32_t* t_qlist = nullptr;       // [batch][max_windows]
+    int32_t* t_nq = nullptr;
+    int32_t* t_seq_len = nullptr;
+    int32_t* t_quant = nullptr;       // [batch][max_windows] routing lists + counts
+    int32_t* t_nquant = nullptr;
+    int32_t* t_prom = nullptr;
+    int32_t* t_nprom = nullptr;
+    int32_t* t_free = nullptr;
+    int32_t* t_nfree = nullptr;
+    float2* t_stats = nullptr;        // [rows][stats_tiles][G]
+    float* part_o2 = nullptr;         // INT2 attention partials
+    float* part_ml2 = nullptr;
     size_t bytes = 0;
 };
 
 // Lays out (or, with base == nullptr, only sizes) the context's scratch.
-Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base) {
+int tier_max_windows(const kvev_layout& L) { return (L.max_ctx - kTierSinks) / kTierW; }
+int tier_bt_ld(const kvev_layout& L) { return tier_max_windows(L) * (kTierW / kTile) + 10; }
+int tier_stats_tiles(const kvev_layout& L) { return tier_max_windows(L) * (kTierW / kTile) + 8; }
+
+// slots2: softmax partial slots of the INT2 attention (two-tier mode only).
+Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
+                int64_t slots2 = 0) {
     Workspace w;
     size_t off = 0;
     auto take = [&](size_t bytes) -> char* {
@@ -119,6 +143,26 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base)
     w.sel = (int32_t*)take(units * 4);
     w.budgets = (int32_t*)take((size_t)L.batch * 4);
     w.readmit_page = (int32_t*)take(4);
+    if (L.page_tokens == kTierW) {
+        const size_t B = (size_t)L.batch, MW = (size_t)tier_max_windows(L);
+        const size_t bt = B * tier_bt_ld(L);
+        w.t_bt = (int32_t*)take(bt * 4);
+        w.t_bpos = (int32_t*)take(bt * 4);
+        w.t_blen = (int32_t*)take(bt * 4);
+        w.t_nblk = (int32_t*)take(B * 4);
+        w.t_qlist = (int32_t*)take(B * MW * 4);
+        w.t_nq = (int32_t*)take(B * 4);
+        w.t_seq_len = (int32_t*)take(B * 4);
+        w.t_quant = (int32_t*)take(B * MW * 4);
+        w.t_nquant = (int32_t*)take(B * 4);
+        w.t_prom = (int32_t*)take(B * MW * 4);
+        w.t_nprom = (int32_t*)take(B * 4);
+        w.t_free = (int32_t*)take(B * MW * 4);
+        w.t_nfree = (int32_t*)take(B * 4);
+        w.t_stats = (float2*)take(rows * (size_t)tier_stats_tiles(L) * G * sizeof(float2));
+        w.part_o2 = (float*)take((size_t)slots2 * G * L.head_dim * 4);
+        w.part_ml2 = (float*)take((size_t)slots2 * G * 2 * 4);
+    }
     w.bytes = off;
     return w;
 }
@@ -138,10 +182,22 @@ kvev_status check_layout(const kvev_layout* L, int64_t budget, bool budget_token
         return fail(KVEV_EUNSUPPORTED, "layout: query heads per KV head %d (supported: 4, 8)",
                     L->n_q_heads / L->n_kv_heads);
     if (L->max_ctx < 2) return fail(KVEV_EINVAL, "layout: max_ctx must be >= 2");
-    if (L->page_tokens != 1 && L->page_tokens != kTile)
-        return fail(KVEV_EUNSUPPORTED, "layout: page_tokens %d (supported: 1, %d)", L->page_tokens,
-                    kTile);
+    if (L->page_tokens != 1 && L->page_tokens != kTile && L->page_tokens != kTierW)
+        return fail(KVEV_EUNSUPPORTED, "layout: page_tokens %d (supported: 1, %d, %d)",
+                    L->page_tokens, kTile, kTierW);
     if (L->kv_dtype != KVEV_BF16) return fail(KVEV_EUNSUPPORTED, "layout: kv_dtype must be BF16");
+    if (L->page_tokens == kTierW) {   // two-tier windows: budget = K_f windows
+        if (L->head_dim != 128 || L->n_q_heads / L->n_kv_heads != 4)
+            return fail(KVEV_EUNSUPPORTED, "two-tier windows: head_dim 128 and 4 query heads per "
+                        "KV head only");
+        const int mw = (L->max_ctx - kTierSinks) / kTierW;
+        if (mw < 1 || mw > kTierRouteCap)
+            return fail(KVEV_EINVAL, "layout: max_ctx %d gives %d windows (1 .. %d)", L->max_ctx,
+                        mw, kTierRouteCap);
+        if (budget < 0 || budget > mw)
+            return fail(KVEV_EINVAL, "budget (K_f) %lld must be in [0, %d]", (long long)budget, mw);
+        return KVEV_OK;
+    }
     if (L->max_ctx % L->page_tokens != 0)
         return fail(KVEV_EINVAL, "layout: max_ctx %d must be a multiple of page_tokens %d",
                     L->max_ctx, L->page_tokens);
@@ -154,6 +210,12 @@ kvev_status check_layout(const kvev_layout* L, int64_t budget, bool budget_token
 
 int64_t attn_grid_for_device(int num_sms, const kvev_layout& L) {
     const int per_sm = attn_ctas_per_sm(L.head_dim, L.n_q_heads / L.n_kv_heads);
+    return (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
+}
+
+int64_t int2_grid_for_device(int num_sms, const kvev_layout& L) {
+    if (L.page_tokens != kTierW) return 0;
+    const int per_sm = int2_ctas_per_sm(L.head_dim, L.n_q_heads / L.n_kv_heads);
     return (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
 }
 
@@ -174,6 +236,12 @@ struct kvev_ctx {
     int32_t group = 4;
     RegionParams rp{};
     std::vector<int32_t> pin_blocks;  // per sequence: prefill blocks holding a pinned token
+    // two-tier mode: capacities, routing interval, INT2 attention grid, and the
+    // host's exact copy of the window counts (the same for every sequence:
+    // windows form by position and routing fills the tiers by capacity)
+    int k_full = 0, k_quant = 0, omega = 8;
+    int int2_grid = 0, int2_warps = 0;
+    int t_nw = 0, t_tl = 0, t_first_u = 0, t_nf = 0, t_nq = 0;
     int32_t len = 0, prefill_len = 0;
     std::vector<int32_t> ub_blocks;   // block mode: upper bound of each sequence's live blocks
     int64_t step = 0;
@@ -278,8 +346,9 @@ kvev_status kvev_workspace_size(const kvev_layout* layout, int64_t budget, size_
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "device query");
     const int64_t W = attn_grid_for_device(sms, *layout) * attn_warps_per_cta();
+    const int64_t W2 = int2_grid_for_device(sms, *layout) * int2_warps_per_cta();
     const int64_t rows = (int64_t)layout->n_layers * layout->batch * layout->n_kv_heads;
-    *bytes = carve(*layout, budget, W + rows, nullptr).bytes;
+    *bytes = carve(*layout, budget, W + rows, nullptr, W2 ? W2 + rows : 0).bytes;
     return KVEV_OK;
 }
 
@@ -299,8 +368,8 @@ kvev_status kvev_create(const kvev_layout* layout, int64_t budget, int32_t granu
     RegionParams rp{};
     if (regions) {
         const kvev_region_table& R = *regions;
-        if (layout->page_tokens == 1)
-            return fail(KVEV_EUNSUPPORTED, "a region table needs block granularity");
+        if (layout->page_tokens != kTile)
+            return fail(KVEV_EUNSUPPORTED, "a region table needs %d-token blocks", kTile);
         if (R.n_regions < 1 || R.n_regions > KVEV_MAX_REGIONS)
             return fail(KVEV_EINVAL, "n_regions %d out of [1, %d]", R.n_regions, KVEV_MAX_REGIONS);
         if (R.score_kind != KVEV_SCORE_LRFU && R.score_kind != KVEV_SCORE_MEMDECAY)
@@ -343,15 +412,19 @@ kvev_status kvev_create(const kvev_layout* layout, int64_t budget, int32_t granu
     }
     c->attn_grid = (int)attn_grid_for_device(c->num_sms, *layout);
     c->attn_warps = c->attn_grid * attn_warps_per_cta();
+    c->int2_grid = (int)int2_grid_for_device(c->num_sms, *layout);
+    c->int2_warps = c->int2_grid * int2_warps_per_cta();
     const int64_t rows = (int64_t)layout->n_layers * layout->batch * layout->n_kv_heads;
-    const size_t bytes = carve(*layout, budget, c->attn_warps + rows, nullptr).bytes;
+    const int64_t slots2 = c->int2_warps ? c->int2_warps + rows : 0;
+    const size_t bytes = carve(*layout, budget, c->attn_warps + rows, nullptr, slots2).bytes;
     e = cudaMalloc(&c->ws_base, bytes);
     if (e != cudaSuccess) {
         delete c;
         cudaGetLastError();
         return fail(KVEV_ENOMEM, "cudaMalloc of %zu bytes of scratch failed", bytes);
     }
-    c->ws = carve(*layout, budget, c->attn_warps + rows, c->ws_base);
+    c->ws = carve(*layout, budget, c->attn_warps + rows, c->ws_base, slots2);
+    c->k_full = (int)budget;
     e = cudaMemset(c->ws_base, 0, bytes);   // row counters and status start at zero
     if (e != cudaSuccess) {
         cudaFree(c->ws_base);
@@ -952,6 +1025,282 @@ kvev_status kvev_readmit(kvev_ctx* c, const kvev_paged_cache* pc, const kvev_blo
     if (rc != KVEV_OK) return rc;
     c->launches += 1;   // the copy kernel
     c->ub_blocks[seq] += 1;
+    return KVEV_OK;
+}
+
+// ---- two-tier windows with an INT2 tier -----------------------------------
+
+}  // extern "C"
+
+namespace {
+
+kvev_status check_tier(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_tier_state* ts) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (c->lay.page_tokens != kTierW)
+        return fail(KVEV_ESTATE, "not a two-tier context (layout.page_tokens must be %d)", kTierW);
+    if (!tc || !ts) return fail(KVEV_EINVAL, "NULL argument");
+    if (!tc->k_pool || !tc->v_pool || !tc->free_pages || !tc->n_free || !tc->ledger)
+        return fail(KVEV_EINVAL, "tier cache has a NULL array");
+    if (!aligned16(tc->k_pool) || !aligned16(tc->v_pool) || !aligned16(tc->ledger))
+        return fail(KVEV_EINVAL, "pools and ledger must be 16-byte aligned");
+    if (tc->max_windows != tier_max_windows(c->lay))
+        return fail(KVEV_EINVAL, "max_windows %d != (max_ctx - 5) / 128 = %d", tc->max_windows,
+                    tier_max_windows(c->lay));
+    if (tc->pages_per_seq < 2) return fail(KVEV_EINVAL, "pages_per_seq must be >= 2");
+    if (!ts->score || !ts->tier || !ts->has_codes || !ts->win_pages || !ts->n_windows ||
+        !ts->tail_pages || !ts->tail_len)
+        return fail(KVEV_EINVAL, "tier state has a NULL array");
+    return KVEV_OK;
+}
+
+TierArgs tier_args(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_tier_state* ts, int t) {
+    TierArgs a{};
+    a.c = *tc;
+    a.st = *ts;
+    a.bt = c->ws.t_bt;
+    a.bpos = c->ws.t_bpos;
+    a.blen = c->ws.t_blen;
+    a.nblk = c->ws.t_nblk;
+    a.bt_ld = tier_bt_ld(c->lay);
+    a.qlist = c->ws.t_qlist;
+    a.nq = c->ws.t_nq;
+    a.seq_len = c->ws.t_seq_len;
+    a.quant_list = c->ws.t_quant;
+    a.n_quant = c->ws.t_nquant;
+    a.prom_list = c->ws.t_prom;
+    a.n_prom = c->ws.t_nprom;
+    a.free_list = c->ws.t_free;
+    a.n_freeing = c->ws.t_nfree;
+    a.tile_stats = c->ws.t_stats;
+    a.stats_tiles = tier_stats_tiles(c->lay);
+    a.lse2 = c->ws.lse2;
+    a.status = c->ws.status;
+    a.batch = c->lay.batch;
+    a.n_layers = c->lay.n_layers;
+    a.n_kv = c->lay.n_kv_heads;
+    a.n_q = c->lay.n_q_heads;
+    a.head_dim = c->lay.head_dim;
+    a.k_full = c->k_full;
+    a.k_quant = c->k_quant;
+    a.t = t;
+    a.alpha = c->alpha;
+    return a;
+}
+
+// bf16 pages a sequence holds (sink page, unrouted and Full windows, tail)
+int tier_used_pages(const kvev_ctx* c) {
+    const int n_u = c->t_nw - c->t_first_u;
+    return 1 + (kTierW / kTile) * (n_u + c->t_nf) + (c->t_tl + kTile - 1) / kTile;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvev_status kvev_set_tiers(kvev_ctx* c, int64_t k_full, int64_t k_quant, int32_t omega) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (c->lay.page_tokens != kTierW)
+        return fail(KVEV_ESTATE, "not a two-tier context (layout.page_tokens must be %d)", kTierW);
+    const int mw = tier_max_windows(c->lay);
+    if (k_full < 0 || k_quant < 0 || k_full > mw || k_quant > mw || omega < 1)
+        return fail(KVEV_EINVAL, "K_f, K_q must be in [0, %d] and omega >= 1", mw);
+    c->k_full = (int)k_full;
+    c->k_quant = (int)k_quant;
+    c->omega = omega;
+    return KVEV_OK;
+}
+
+kvev_status kvev_tier_begin(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_tier_state* ts,
+                            int32_t prefill_tokens, void* stream) {
+    kvev_status rc = check_tier(c, tc, ts);
+    if (rc != KVEV_OK) return rc;
+    if (prefill_tokens < kTierSinks || prefill_tokens >= c->lay.max_ctx)
+        return fail(KVEV_EINVAL, "prefill_tokens %d must be in [%d, max_ctx)", prefill_tokens,
+                    kTierSinks);
+    const int hist = prefill_tokens - kTierSinks;
+    const int used = 1 + (hist + kTile - 1) / kTile;
+    if (used + 1 > tc->pages_per_seq)
+        return fail(KVEV_EINVAL, "pages_per_seq %d too small for a %d-token prefill",
+                    tc->pages_per_seq, prefill_tokens);
+    cudaStream_t s = (cudaStream_t)stream;
+    const TierArgs a = tier_args(c, tc, ts, 0);
+    rc = timed_launch(c, kProfInit, s, "tier begin",
+                      [&] { return launch_tier_begin(a, prefill_tokens, s); });
+    if (rc != KVEV_OK) return rc;
+    c->t_nw = hist / kTierW;
+    c->t_tl = hist % kTierW;
+    c->t_first_u = 0;
+    c->t_nf = c->t_nq = 0;
+    c->len = prefill_tokens;
+    c->prefill_len = prefill_tokens;
+    c->step = 0;
+    c->begun = true;
+    return KVEV_OK;
+}
+
+kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const void* v_new,
+                           const kvev_tier_cache* tc, const kvev_tier_state* ts, int64_t step,
+                           float* out, void* stream) {
+    kvev_status rc = check_tier(c, tc, ts);
+    if (rc != KVEV_OK) return rc;
+    if (!q || !k_new || !v_new || !out) return fail(KVEV_EINVAL, "NULL argument");
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out))
+        return fail(KVEV_EINVAL, "q, k_new, v_new and out must be 16-byte aligned");
+    if (!c->begun) return fail(KVEV_ESTATE, "kvev_tier_begin must come before the first step");
+    if (step != c->step + 1)
+        return fail(KVEV_ESTATE, "step %lld out of order (expected %lld)", (long long)step,
+                    (long long)(c->step + 1));
+    if (c->len + 1 > c->lay.max_ctx)
+        return fail(KVEV_EINVAL, "max_ctx %d positions reached", c->lay.max_ctx);
+    const int pps = tc->pages_per_seq, PW = kTierW / kTile;
+    const int t = (int)step;
+    // host copy of the counts after the append
+    int nw = c->t_nw, tl = c->t_tl + 1;
+    if (tl == kTierW) {
+        ++nw;
+        tl = 0;
+    }
+    const int L = c->len + 1;
+    const bool routing = t % c->omega == 0;
+    int n_aged = 0, n_cand = 0, nf2 = c->t_nf, nq2 = c->t_nq;
+    if (routing) {   // windows whose last token is below the recent region
+        const int horizon = L - kTierRecent;
+        const int aged_total = horizon >= kTierSinks + kTierW ? (horizon - kTierSinks) / kTierW : 0;
+        n_aged = std::max(0, std::min(nw, aged_total) - c->t_first_u);
+        n_cand = c->t_nf + c->t_nq + n_aged;
+        nf2 = std::min(c->k_full, n_cand);
+        nq2 = std::min(c->k_quant, n_cand - nf2);
+    }
+    {
+        int saved_nw = c->t_nw, saved_tl = c->t_tl;
+        c->t_nw = nw;
+        c->t_tl = tl;
+        const int used = tier_used_pages(c);
+        c->t_nw = saved_nw;
+        c->t_tl = saved_tl;
+        const int prom = routing ? std::min(c->t_nq, nf2) : 0;
+        if (used + PW * prom > pps)
+            return fail(KVEV_EINVAL, "pages_per_seq %d too small: %d bf16 pages needed", pps,
+                        used + PW * prom);
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const kvev_layout& Ly = c->lay;
+    const int G = c->group;
+    TierArgs ta = tier_args(c, tc, ts, t);
+    rc = timed_launch(c, kProfAppend, s, "tier append", [&] {
+        return launch_tier_append(ta, (const uint16_t*)k_new, (const uint16_t*)v_new, s);
+    });
+    if (rc != KVEV_OK) return rc;
+
+    const int64_t rows = (int64_t)Ly.n_layers * Ly.batch * Ly.n_kv_heads;
+    const int n_bf = 1 + PW * (nw - c->t_first_u + c->t_nf) + (tl + kTile - 1) / kTile;
+    AttnArgs at{};
+    at.k = (const uint16_t*)tc->k_pool;
+    at.v = (const uint16_t*)tc->v_pool;
+    at.q = (const uint16_t*)q;
+    at.part_o = c->ws.part_o;
+    at.part_ml = c->ws.part_ml;
+    at.status = c->ws.status;
+    at.row0 = 0;
+    at.tiles_per_row = n_bf;
+    at.n_tiles_total = rows * n_bf;
+    at.L = n_bf * kTile;
+    at.max_ctx = Ly.max_ctx;
+    at.n_layers = Ly.n_layers;
+    at.batch = Ly.batch;
+    at.n_kv = Ly.n_kv_heads;
+    at.n_q = Ly.n_q_heads;
+    at.total_warps = c->attn_warps;
+    at.write_logits = 0;
+    at.q_scale = (float)(1.4426950408889634 / sqrt((double)Ly.head_dim));
+    at.view_tokens = (int64_t)Ly.batch * pps * Ly.n_layers * Ly.n_kv_heads * kTile;
+    at.block_table = c->ws.t_bt;
+    at.n_blocks = c->ws.t_nblk;
+    at.blk_len = c->ws.t_blen;
+    at.pps = tier_bt_ld(Ly);
+    at.blk_pos = c->ws.t_bpos;
+    at.tile_stats = c->ws.t_stats;
+    at.stats_tiles = tier_stats_tiles(Ly);
+    at.stats_base = kTierSinks;
+    rc = timed_launch(c, kProfAttn, s, "attention",
+                      [&] { return launch_attention(at, Ly.head_dim, G, c->attn_grid, s); });
+    if (rc != KVEV_OK) return rc;
+    CombineArgs cb{};
+    cb.sp.part_o = c->ws.part_o;
+    cb.sp.part_ml = c->ws.part_ml;
+    cb.sp.n_tiles = at.n_tiles_total;
+    cb.sp.row0 = 0;
+    cb.sp.total_warps = c->attn_warps;
+    cb.sp.tiles_per_row = n_bf;
+    if (c->t_nq > 0) {
+        Int2Args ia{};
+        ia.ledger = (const unsigned char*)tc->ledger;
+        ia.max_windows = tc->max_windows;
+        ia.q_list = c->ws.t_qlist;
+        ia.q_ld = tc->max_windows;
+        ia.n_qwin = c->ws.t_nq;
+        ia.q = (const uint16_t*)q;
+        ia.part_o = c->ws.part_o2;
+        ia.part_ml = c->ws.part_ml2;
+        ia.tile_stats = c->ws.t_stats;
+        ia.stats_tiles = tier_stats_tiles(Ly);
+        ia.status = c->ws.status;
+        ia.slots = c->t_nq;
+        ia.n_units = rows * c->t_nq;
+        ia.total_warps = c->int2_warps;
+        ia.n_layers = Ly.n_layers;
+        ia.batch = Ly.batch;
+        ia.n_kv = Ly.n_kv_heads;
+        ia.n_q = Ly.n_q_heads;
+        ia.q_scale = at.q_scale;
+        rc = timed_launch(c, kProfAttn, s, "int2 attention",
+                          [&] { return launch_attn_int2(ia, Ly.head_dim, G, c->int2_grid, s); });
+        if (rc != KVEV_OK) return rc;
+        cb.has2 = 1;
+        cb.sp2.part_o = c->ws.part_o2;
+        cb.sp2.part_ml = c->ws.part_ml2;
+        cb.sp2.n_tiles = ia.n_units;
+        cb.sp2.row0 = 0;
+        cb.sp2.total_warps = c->int2_warps;
+        cb.sp2.tiles_per_row = c->t_nq;
+    }
+    cb.n_rows = (int32_t)rows;
+    cb.out = out;
+    cb.lse2 = c->ws.lse2;
+    cb.n_layers = Ly.n_layers;
+    cb.batch = Ly.batch;
+    cb.n_kv = Ly.n_kv_heads;
+    cb.n_q = Ly.n_q_heads;
+    rc = timed_launch(c, kProfCombine, s, "combine",
+                      [&] { return launch_combine(cb, Ly.head_dim, G, s); });
+    if (rc != KVEV_OK) return rc;
+    rc = timed_launch(c, kProfScore, s, "window score",
+                      [&] { return launch_tier_score(ta, nw, G, s); });
+    if (rc != KVEV_OK) return rc;
+    if (routing) {
+        const int n_quant_max = std::min(c->k_quant, n_cand);
+        const int n_prom_max = std::min(c->t_nq, nf2);
+        rc = timed_launch(c, kProfSelect, s, "route", [&] { return launch_tier_route(ta, s); });
+        if (rc == KVEV_OK)
+            rc = timed_launch(c, kProfCompact, s, "quantize", [&] {
+                return launch_tier_quantize(ta, n_quant_max, c->num_sms, s);
+            });
+        if (rc == KVEV_OK)
+            rc = timed_launch(c, kProfCompact, s, "promote", [&] {
+                return launch_tier_promote(ta, n_prom_max, c->num_sms, s);
+            });
+        if (rc == KVEV_OK)
+            rc = timed_launch(c, kProfCompact, s, "finish",
+                              [&] { return launch_tier_finish(ta, s); });
+        if (rc != KVEV_OK) return rc;
+        c->t_first_u += n_aged;
+        c->t_nf = nf2;
+        c->t_nq = nq2;
+    }
+    c->t_nw = nw;
+    c->t_tl = tl;
+    c->len = L;
+    c->step = step;
     return KVEV_OK;
 }
 

@@ -34,15 +34,13 @@
 #include <math.h>
 
 #include "kvev_internal.h"
+#include "mma_ops.h"
 
 namespace kvev {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
                  : "memory");
@@ -79,11 +77,6 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 
 // ---------------------------------------------------------------------------
@@ -108,7 +101,7 @@ struct MmaCfg {
     static constexpr int NB = D / 8;                // 8-dim output blocks
     static constexpr int KS = D / 16;               // k-steps of the QK contraction
     static constexpr size_t SMEM = 1024 + (size_t)WARPS * STAGES * STAGE_BYTES +
-                                   (size_t)WARPS * STAGES * (sizeof(uint64_t) + sizeof(int));
+                                   (size_t)WARPS * STAGES * (sizeof(uint64_t) + 2 * sizeof(int));
     static_assert(G <= 8 && (D == 64 || D == 128), "mma tile shape");
 };
 
@@ -130,27 +123,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
 }
-// D = A B + C for one 16x8x16 block; A rows 8..15 are zero (a1 = a3 = 0),
-// so only d0, d1 (rows 0..7) are used; d2, d3 are discarded.
-__device__ __forceinline__ void mma_rows8(float& c0, float& c1, uint32_t a0, uint32_t a2,
-                                          uint32_t b0, uint32_t b1) {
-    float d2, d3;   // rows 8..15: discarded
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3},"
-        " {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
-        : "=f"(c0), "=f"(c1), "=f"(d2), "=f"(d3)
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(0.f),
-          "f"(0.f));
-    (void)d2;
-    (void)d3;
-}
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // shared-memory byte address of 16-byte chunk c (0 .. D/8-1) of tile row r
 template <int D>
@@ -182,6 +154,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     int* stage_nv = reinterpret_cast<int*>(reinterpret_cast<uint64_t*>(
                         smem + (size_t)WARPS * STAGES * C::STAGE_BYTES) + WARPS * STAGES) +
                     warp * STAGES;
+    int* stage_pos = stage_nv + WARPS * STAGES;   // first token position of the tile (block mode)
 
     const int w = blockIdx.x * WARPS + warp;
     const int64_t N = a.n_tiles_total;
@@ -206,11 +179,14 @@ __global__ void __launch_bounds__(WARPS * 32)
             const int64_t lb = arow / a.n_kv;
             const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
             nv = 0;
+            int pos = tile * T;
             if (tile < a.n_blocks[b]) {
                 const int page = a.block_table[(size_t)b * a.pps + tile];
                 nv = a.blk_len[(size_t)b * a.pps + tile];
                 y = (int)((((int64_t)page * a.n_layers + l) * a.n_kv + gk) * T);
+                if (a.blk_pos) pos = a.blk_pos[(size_t)b * a.pps + tile];
             }
+            stage_pos[stage] = pos;
         } else {
             y = (int)((a.row0 + row) * a.max_ctx + tile * T);
             nv = min(T, a.L - tile * T);
@@ -299,6 +275,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         const uint32_t ktile = smem_addr(wbuf + (size_t)stage * C::STAGE_BYTES);
         const uint32_t vtile = ktile + C::TILE_BYTES;
         const int nvalid = PAGED ? stage_nv[stage] : min(T, a.L - tok0);
+        const int pos0 = PAGED ? stage_pos[stage] : tok0;   // position of the tile's first token
         if (PAGED && nvalid == 0) {   // past the sequence's live blocks: nothing to do
             __syncwarp();
             if (x + STAGES < x1) {
@@ -337,7 +314,7 @@ __global__ void __launch_bounds__(WARPS * 32)
             for (int e = 0; e < 2; ++e)
                 if (!real || 8 * i + 2 * t + e >= nvalid) sc[i][e] = -INFINITY;
         if (a.write_logits && real) {
-            float* lg = a.logits + ((size_t)(a.row0 + row) * a.logit_ld + tok0) * G + g;
+            float* lg = a.logits + ((size_t)(a.row0 + row) * a.logit_ld + pos0) * G + g;
 #pragma unroll
             for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -368,6 +345,14 @@ __global__ void __launch_bounds__(WARPS * 32)
                 p[i][e] = real ? fast_exp2(sc[i][e] - m_run) : 0.f;
                 l_run += p[i][e];
             }
+        if (PAGED && a.tile_stats && pos0 >= a.stats_base) {   // (running max, tile sum) per head
+            float ts = (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+            ts += __shfl_xor_sync(kFull, ts, 1);
+            ts += __shfl_xor_sync(kFull, ts, 2);
+            if (real && t == 0)
+                a.tile_stats[((size_t)(a.row0 + row) * a.stats_tiles +
+                              (pos0 - a.stats_base) / T) * G + g] = make_float2(m_run, ts);
+        }
         const uint32_t ph0 = pack_bf16x2(p[0][0], p[0][1]);   // tokens 2t, 2t+1
         const uint32_t ph2 = pack_bf16x2(p[1][0], p[1][1]);   // tokens 8+2t, 8+2t+1
         const uint32_t pl0 = pack_bf16x2(p[0][0] - bf16_lo(ph0), p[0][1] - bf16_hi(ph0));
@@ -424,39 +409,42 @@ __global__ void __launch_bounds__(D) combine_kernel(const CombineArgs a) {
     constexpr int kSeg = 8;
     griddep_wait();
     griddep_release();
-    const SplitPartials& sp = a.sp;
     const int64_t r = blockIdx.x;                 // row of the launch
     const int d = threadIdx.x;
-    int64_t lo, hi;
-    split_warps_of_row(sp, r, &lo, &hi);
     float M[G], Ls[G], acc[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) { M[h] = -INFINITY; Ls[h] = 0.f; acc[h] = 0.f; }
-    for (int64_t w0 = lo; w0 <= hi; w0 += kSeg) {
-        float m[kSeg][G], l[kSeg][G], o[kSeg][G];
+    for (int set = 0; set < 1 + a.has2; ++set) {
+        const SplitPartials& sp = set ? a.sp2 : a.sp;
+        int64_t lo, hi;
+        split_warps_of_row(sp, r, &lo, &hi);
+        for (int64_t w0 = lo; w0 <= hi; w0 += kSeg) {
+            float m[kSeg][G], l[kSeg][G], o[kSeg][G];
 #pragma unroll
-        for (int j = 0; j < kSeg; ++j) {
-            const int64_t w = w0 + j;
-            const bool ok = w <= hi && split_warp_has_tiles(w, sp.n_tiles, sp.total_warps);
+            for (int j = 0; j < kSeg; ++j) {
+                const int64_t w = w0 + j;
+                const bool ok = w <= hi && split_warp_has_tiles(w, sp.n_tiles, sp.total_warps);
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                m[j][h] = ok ? __ldcg(sp.part_ml + ((w + r) * G + h) * 2) : -INFINITY;
-                l[j][h] = ok ? __ldcg(sp.part_ml + ((w + r) * G + h) * 2 + 1) : 0.f;
-                o[j][h] = ok ? __ldcg(sp.part_o + ((w + r) * G + h) * D + d) : 0.f;
+                for (int h = 0; h < G; ++h) {
+                    m[j][h] = ok ? __ldcg(sp.part_ml + ((w + r) * G + h) * 2) : -INFINITY;
+                    l[j][h] = ok ? __ldcg(sp.part_ml + ((w + r) * G + h) * 2 + 1) : 0.f;
+                    o[j][h] = ok ? __ldcg(sp.part_o + ((w + r) * G + h) * D + d) : 0.f;
+                }
             }
+#pragma unroll
+            for (int j = 0; j < kSeg; ++j)
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    if (m[j][h] == -INFINITY) continue;
+                    const float mn = fmaxf(M[h], m[j][h]);
+                    const float fo = fast_exp2(M[h] - mn), fj = fast_exp2(m[j][h] - mn);
+                    Ls[h] = Ls[h] * fo + l[j][h] * fj;
+                    acc[h] = acc[h] * fo + o[j][h] * fj;
+                    M[h] = mn;
+                }
         }
-#pragma unroll
-        for (int j = 0; j < kSeg; ++j)
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                if (m[j][h] == -INFINITY) continue;
-                const float mn = fmaxf(M[h], m[j][h]);
-                const float fo = fast_exp2(M[h] - mn), fj = fast_exp2(m[j][h] - mn);
-                Ls[h] = Ls[h] * fo + l[j][h] * fj;
-                acc[h] = acc[h] * fo + o[j][h] * fj;
-                M[h] = mn;
-            }
     }
+    const SplitPartials& sp = a.sp;
     const int64_t arow = sp.row0 + r;
     const int g = (int)(arow % a.n_kv);
     const int64_t lb = arow / a.n_kv;

@@ -1,0 +1,307 @@
+// Attention over the INT2 windows of the two-tier cache ("QEvict: ...",
+// Sec. 4.1: the accessible keys and values include the dequantized INT2
+// windows), with the dequantization folded into the tensor-core products.
+//
+// A key is k_c = code_c * s_c + z_c with (s, z) per channel over a 32-token
+// group, so within a group
+//     q . k = sum_c (q_c s_c) code_c + sum_c q_c z_c :
+// the A operand is q * s (bf16 hi + lo, the product is exact in fp32), the
+// B operand the codes themselves (small integers, exact in bf16), plus a
+// per-head bias.  A value is v_c = code_c * s_g + z_g with (s, z) per token
+// over a 32-channel group g, so
+//     sum_i p_i v_ic = sum_i (p_i s_ig) code_ic + sum_i p_i z_ig :
+// per channel group the A operand is p * s (hi + lo), B the codes, plus a
+// per-head, per-group bias carried through the online softmax like the
+// output.  Codes become bf16 with an OR into the exponent of 128 and a
+// subtraction of 128.
+//
+// Work: every (layer, sequence, KV head) row has `slots` units, one INT2
+// window each (past the sequence's INT2 list a unit is empty); warps take
+// equal contiguous ranges of units (split-K over windows), double-buffer a
+// unit's 12 KiB ledger entry in shared memory with cp.async, and leave a
+// softmax partial per (warp, row) piece for the split combine, plus the
+// per-16-token-tile statistics the window scores are formed from.
+#include <cuda_fp16.h>
+
+#include "kvev_internal.h"
+#include "mma_ops.h"
+
+namespace kvev {
+namespace {
+
+constexpr int kI2Warps = 4;
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_prior() {   // all but the newest group
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+// Two 2-bit codes at bits 0-1 and 16-17 of x (other bits clear) -> bf16x2.
+__device__ __forceinline__ uint32_t codes_bf16x2(uint32_t x) {
+    uint32_t r;
+    const uint32_t biased = x | 0x43004300u;   // 128 + code, exact in bf16
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(0x43004300u));
+    return r;
+}
+__device__ __forceinline__ float half_at(const unsigned char* base, int idx) {
+    return __half2float(reinterpret_cast<const __half*>(base)[idx]);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args a) {
+    using Lay = LedgerLayout<D>;
+    constexpr int KS = D / 16, NB = D / 8, NG = D / kQGroup;
+    extern __shared__ __align__(128) unsigned char smem[];
+    griddep_wait();
+    griddep_release();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned char* wbuf = smem + (size_t)warp * 2 * Lay::BYTES;
+    const int w = blockIdx.x * kI2Warps + warp;
+    const int64_t N = a.n_units;
+    const int64_t x0 = (int64_t)w * N / a.total_warps, x1 = (int64_t)(w + 1) * N / a.total_warps;
+    if (x0 >= x1) return;
+
+    const int g = lane >> 2, t = lane & 3;   // fragment row (query head), column pair
+    const bool real = g < G;
+    // window id of unit x (-1: empty), and its ledger entry
+    auto unit_window = [&](int64_t x, const unsigned char** src) -> int {
+        const int64_t row = x / a.slots;
+        const int j = (int)(x - row * a.slots);
+        const int gk = (int)(row % a.n_kv);
+        const int64_t lb = row / a.n_kv;
+        const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
+        if (j >= a.n_qwin[b]) return -1;
+        const int wi = a.q_list[(size_t)b * a.q_ld + j];
+        *src = a.ledger +
+               ((((size_t)b * a.max_windows + wi) * a.n_layers + l) * a.n_kv + gk) * Lay::BYTES;
+        return wi;
+    };
+    auto issue = [&](int64_t x, int bi) {
+        const unsigned char* src = nullptr;
+        if (unit_window(x, &src) >= 0) {
+            const uint32_t dst = smem_addr(wbuf + (size_t)bi * Lay::BYTES);
+            for (int i = lane; i < Lay::BYTES / 16; i += 32) cp_async16(dst + 16 * i, src + 16 * i);
+        }
+        cp_async_commit();
+    };
+
+    uint32_t qa0[KS], qa2[KS];               // Q fragments (bf16x2) of head g
+    float o[NB][2];
+    float vbias[NG];                         // sum_i p_i z_ig of head g, per channel group
+    float m_run = -INFINITY, l_run = 0.f;
+    int64_t cur_row = -1;
+
+    auto flush = [&](int64_t row) {
+        float l = l_run;
+        l += __shfl_xor_sync(kFull, l, 1);
+        l += __shfl_xor_sync(kFull, l, 2);
+        const int64_t slot = (int64_t)w + row;
+        if (real) {
+            float* po = a.part_o + ((size_t)slot * G + g) * D;
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+                *reinterpret_cast<float2*>(po + 8 * j + 2 * t) =
+                    make_float2(o[j][0] + vbias[j / 4], o[j][1] + vbias[j / 4]);
+            if (t == 0) {
+                float* pml = a.part_ml + ((size_t)slot * G + g) * 2;
+                pml[0] = m_run;
+                pml[1] = l;
+            }
+        }
+    };
+
+    issue(x0, 0);
+    int bi = 0;
+    for (int64_t x = x0; x < x1; ++x, bi ^= 1) {
+        if (x + 1 < x1) issue(x + 1, bi ^ 1);
+        else cp_async_commit();              // keep one group per iteration
+        cp_async_wait_prior();
+        __syncwarp();
+        const int64_t row = x / a.slots;
+        if (row != cur_row) {
+            if (cur_row >= 0) flush(cur_row);
+            cur_row = row;
+            const int gk = (int)(row % a.n_kv);
+            const int64_t lb = row / a.n_kv;
+            const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                a.q + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)gk * G + (real ? g : 0)) * D);
+#pragma unroll
+            for (int s = 0; s < KS; ++s) {
+                qa0[s] = real ? qrow[8 * s + t] : 0u;       // dims 16s + 2t, +1
+                qa2[s] = real ? qrow[8 * s + 4 + t] : 0u;   // dims 16s + 8 + 2t, +1
+            }
+#pragma unroll
+            for (int j = 0; j < NB; ++j) o[j][0] = o[j][1] = 0.f;
+#pragma unroll
+            for (int c = 0; c < NG; ++c) vbias[c] = 0.f;
+            m_run = -INFINITY;
+            l_run = 0.f;
+        }
+        const unsigned char* src = nullptr;
+        const int wid = unit_window(x, &src);
+        if (wid >= 0) {
+            const unsigned char* buf = wbuf + (size_t)bi * Lay::BYTES;
+            const uint32_t* kc = reinterpret_cast<const uint32_t*>(buf + Lay::KC);
+            const uint32_t* vc = reinterpret_cast<const uint32_t*>(buf + Lay::VC);
+            for (int grp = 0; grp < kTierW / kQGroup; ++grp) {
+                // A' = q * s (hi + lo) for this group's key scales, and the key bias
+                uint32_t ahi[KS][2], alo[KS][2];
+                float kb = 0.f;
+#pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    const int c0 = 16 * s + 2 * t, c2 = c0 + 8;
+                    const float q0 = bf16_lo(qa0[s]), q1 = bf16_hi(qa0[s]);
+                    const float q2 = bf16_lo(qa2[s]), q3 = bf16_hi(qa2[s]);
+                    const unsigned char* ks = buf + Lay::KS;
+                    const unsigned char* kz = buf + Lay::KZ;
+                    const float p0 = q0 * half_at(ks, grp * D + c0);
+                    const float p1 = q1 * half_at(ks, grp * D + c0 + 1);
+                    const float p2 = q2 * half_at(ks, grp * D + c2);
+                    const float p3 = q3 * half_at(ks, grp * D + c2 + 1);
+                    kb = fmaf(q0, half_at(kz, grp * D + c0), kb);
+                    kb = fmaf(q1, half_at(kz, grp * D + c0 + 1), kb);
+                    kb = fmaf(q2, half_at(kz, grp * D + c2), kb);
+                    kb = fmaf(q3, half_at(kz, grp * D + c2 + 1), kb);
+                    ahi[s][0] = pack_bf16x2(p0, p1);
+                    ahi[s][1] = pack_bf16x2(p2, p3);
+                    alo[s][0] = pack_bf16x2(p0 - bf16_lo(ahi[s][0]), p1 - bf16_hi(ahi[s][0]));
+                    alo[s][1] = pack_bf16x2(p2 - bf16_lo(ahi[s][1]), p3 - bf16_hi(ahi[s][1]));
+                }
+                kb += __shfl_xor_sync(kFull, kb, 1);
+                kb += __shfl_xor_sync(kFull, kb, 2);
+#pragma unroll 1
+                for (int tt = 0; tt < kQGroup / kTile; ++tt) {
+                    const int ti = grp * (kQGroup / kTile) + tt;   // 16-token tile of the window
+                    const int tok0 = ti * kTile;
+                    // ---- S = A' codes + bias for the two 8-token blocks
+                    float hi_acc[2][2] = {}, lo_acc[2][2] = {};
+#pragma unroll
+                    for (int s = 0; s < KS; ++s)
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const uint32_t y = kc[(tok0 + 8 * i + g) * KS + s] >> (2 * t);
+                            const uint32_t b0 = codes_bf16x2(y & 0x00030003u);
+                            const uint32_t b1 = codes_bf16x2((y >> 8) & 0x00030003u);
+                            mma_rows8(hi_acc[i][0], hi_acc[i][1], ahi[s][0], ahi[s][1], b0, b1);
+                            mma_rows8(lo_acc[i][0], lo_acc[i][1], alo[s][0], alo[s][1], b0, b1);
+                        }
+                    float sc[2][2];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            sc[i][e] = real ? (hi_acc[i][e] + lo_acc[i][e] + kb) * a.q_scale
+                                            : -INFINITY;
+                    // ---- online softmax of head g
+                    float mt = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+                    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+                    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+                    if (real && mt > m_run) {
+                        const float f = fast_exp2(m_run - mt);
+                        m_run = mt;
+                        l_run *= f;
+#pragma unroll
+                        for (int j = 0; j < NB; ++j) {
+                            o[j][0] *= f;
+                            o[j][1] *= f;
+                        }
+#pragma unroll
+                        for (int c = 0; c < NG; ++c) vbias[c] *= f;
+                    }
+                    float p[2][2];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            p[i][e] = real ? fast_exp2(sc[i][e] - m_run) : 0.f;
+                            l_run += p[i][e];
+                        }
+                    if (a.tile_stats) {   // (running max, tile sum) of head g for the window score
+                        float ts = (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+                        ts += __shfl_xor_sync(kFull, ts, 1);
+                        ts += __shfl_xor_sync(kFull, ts, 2);
+                        if (real && t == 0)
+                            a.tile_stats[((size_t)row * a.stats_tiles + (size_t)wid * (kTierW / kTile) +
+                                          ti) * G + g] = make_float2(m_run, ts);
+                    }
+                    // ---- O += (p * s_v) codes + p * z_v, per 32-channel group
+                    const int tk[4] = {tok0 + 2 * t, tok0 + 2 * t + 1, tok0 + 8 + 2 * t,
+                                       tok0 + 9 + 2 * t};
+                    const float pv[4] = {p[0][0], p[0][1], p[1][0], p[1][1]};
+#pragma unroll
+                    for (int cg = 0; cg < NG; ++cg) {
+                        float pp[4], vb = 0.f;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            pp[k] = pv[k] * half_at(buf + Lay::VS, tk[k] * NG + cg);
+                            vb = fmaf(pv[k], half_at(buf + Lay::VZ, tk[k] * NG + cg), vb);
+                        }
+                        vb += __shfl_xor_sync(kFull, vb, 1);
+                        vb += __shfl_xor_sync(kFull, vb, 2);
+                        vbias[cg] += vb;
+                        const uint32_t ph0 = pack_bf16x2(pp[0], pp[1]);
+                        const uint32_t ph2 = pack_bf16x2(pp[2], pp[3]);
+                        const uint32_t pl0 = pack_bf16x2(pp[0] - bf16_lo(ph0), pp[1] - bf16_hi(ph0));
+                        const uint32_t pl2 = pack_bf16x2(pp[2] - bf16_lo(ph2), pp[3] - bf16_hi(ph2));
+#pragma unroll
+                        for (int jj = 0; jj < kQGroup / 8; ++jj) {
+                            const int j = cg * (kQGroup / 8) + jj;      // 8-channel block
+                            const uint32_t y = vc[ti * D + 8 * j + g] >> (2 * t);
+                            const uint32_t b0 = codes_bf16x2(y & 0x00030003u);
+                            const uint32_t b1 = codes_bf16x2((y >> 8) & 0x00030003u);
+                            mma_rows8(o[j][0], o[j][1], ph0, ph2, b0, b1);
+                            mma_rows8(o[j][0], o[j][1], pl0, pl2, b0, b1);
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();   // every lane is done with this buffer before it is refilled
+    }
+    cp_async_wait_all();
+    flush(cur_row);
+}
+
+template <int D, int G>
+int ctas_per_sm_int2() {
+    auto kern = attn_int2_kernel<D, G>;
+    const int smem = kI2Warps * 2 * LedgerLayout<D>::BYTES;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kI2Warps * 32, smem) !=
+        cudaSuccess)
+        return 0;
+    return n;
+}
+
+}  // namespace
+
+int int2_warps_per_cta() { return kI2Warps; }
+
+int int2_ctas_per_sm(int head_dim, int group) {
+    if (head_dim == 128 && group == 4) return ctas_per_sm_int2<128, 4>();
+    return 0;
+}
+
+cudaError_t launch_attn_int2(const Int2Args& a, int head_dim, int group, int grid,
+                             cudaStream_t s) {
+    if (head_dim != 128 || group != 4) return cudaErrorInvalidValue;
+    auto kern = attn_int2_kernel<128, 4>;
+    const int smem = kI2Warps * 2 * LedgerLayout<128>::BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(grid), dim3(kI2Warps * 32), (size_t)smem, s, a);
+}
+
+}  // namespace kvev

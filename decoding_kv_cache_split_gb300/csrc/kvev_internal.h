@@ -47,6 +47,15 @@ struct AttnArgs {
     const int32_t* n_blocks;      // [batch]
     const int32_t* blk_len;       // [batch][pps]
     int32_t pps;
+    // Optional (block mode): position of each block's first token; the
+    // logits of a block go to that position (else to tile index * kTile).
+    const int32_t* blk_pos;       // [batch][pps] or null
+    // Optional per-tile softmax statistics instead of logits: for every
+    // tile at position p >= stats_base (p - stats_base a multiple of kTile),
+    // (running max, sum of exp2(logit - running max)) per head at
+    // tile_stats[((row * stats_tiles) + (p - stats_base) / kTile) * G + h].
+    float2* tile_stats;
+    int32_t stats_tiles, stats_base;
 };
 
 // Where one attention launch left its split partials: warp w's piece of the
@@ -75,6 +84,8 @@ __device__ __forceinline__ void split_warps_of_row(const SplitPartials& p, int64
 
 struct CombineArgs {
     SplitPartials sp;      // the attention launch to merge (its rows from sp.row0)
+    SplitPartials sp2;     // a second launch over the same rows (has2), e.g. the INT2 tier
+    int32_t has2;
     int32_t n_rows;        // rows of that launch
     float* out;            // [b][Ly][Hq][D]
     float* lse2;           // [rows][G] = [Ly][b][Hq]
@@ -176,6 +187,76 @@ struct PagedArgs {
     RegionParams rp;
 };
 
+// Two-tier (bf16 + INT2 windows) mode.
+constexpr int kTierW = KVEV_TIER_WINDOW;    // tokens per window
+constexpr int kTierSinks = KVEV_TIER_SINKS;
+constexpr int kTierRecent = KVEV_TIER_RECENT;
+constexpr int kQGroup = 32;                 // quantization group
+constexpr int kTierRouteCap = 2048;         // windows per sequence the routing sort holds
+
+// Byte layout of one (window, layer, KV head) ledger entry at head_dim D:
+//   kc [128 tokens][D/16] u32: token's channels 16s..16s+15, channel e at bit
+//      (e & 1) * 16 + 2 * (e >> 1) (so a lane's mma pairs sit 16 bits apart);
+//   ks, kz [4 groups][D] fp16 (keys per channel over 32-token groups);
+//   vc [8 chunks][D] u32: channel's tokens 16j..16j+15, token e at the same bits;
+//   vs, vz [128 tokens][D/32] fp16 (values per token over 32-channel groups).
+template <int D>
+struct LedgerLayout {
+    static constexpr int KC = 0;
+    static constexpr int KS = KC + kTierW * D / 4;
+    static constexpr int KZ = KS + (kTierW / kQGroup) * D * 2;
+    static constexpr int VC = KZ + (kTierW / kQGroup) * D * 2;
+    static constexpr int VS = VC + kTierW * D / 4;
+    static constexpr int VZ = VS + kTierW * (D / kQGroup) * 2;
+    static constexpr int BYTES = VZ + kTierW * (D / kQGroup) * 2;
+};
+
+struct Int2Args {
+    const unsigned char* ledger;
+    int32_t max_windows;
+    const int32_t* q_list;   // [b][q_ld] INT2 windows, ascending
+    int32_t q_ld;
+    const int32_t* n_qwin;   // [b]
+    const uint16_t* q;       // [b][Ly][Hq][D]
+    float* part_o;           // [slots][G][D]
+    float* part_ml;          // [slots][G][2]
+    float2* tile_stats;      // as AttnArgs
+    int32_t stats_tiles;
+    uint32_t* status;
+    int64_t n_units;         // rows * slots
+    int32_t slots;           // units per row (INT2 windows per sequence, at most)
+    int32_t total_warps;
+    int32_t n_layers, batch, n_kv, n_q;
+    float q_scale;
+};
+
+struct TierArgs {
+    kvev_tier_cache c;
+    kvev_tier_state st;
+    int32_t* bt;             // [b][bt_ld] attention block list (pages), rebuilt every step
+    int32_t* bpos;
+    int32_t* blen;
+    int32_t* nblk;           // [b]
+    int32_t bt_ld;
+    int32_t* qlist;          // [b][max_windows] INT2 windows, ascending
+    int32_t* nq;             // [b]
+    int32_t* seq_len;        // [b] positions so far
+    int32_t* quant_list;     // [b][max_windows] routing event lists
+    int32_t* n_quant;
+    int32_t* prom_list;
+    int32_t* n_prom;
+    int32_t* free_list;
+    int32_t* n_freeing;
+    const float2* tile_stats;
+    int32_t stats_tiles;
+    const float* lse2;
+    uint32_t* status;
+    int32_t batch, n_layers, n_kv, n_q, head_dim;
+    int32_t k_full, k_quant;
+    int32_t t;
+    float alpha;
+};
+
 // ---- programmatic dependent launch ----------------------------------------
 // Every kernel of the pass is launched with programmatic stream serialisation:
 // it may be scheduled while its predecessor drains, and waits in
@@ -227,8 +308,20 @@ cudaError_t launch_readmit(const PagedArgs& a, int seq, int lid, int persist, cu
 cudaError_t launch_memdecay_score(const ScoreArgs& sc, const PagedArgs& a, int group,
                                   int ub_blocks, cudaStream_t s);
 cudaError_t launch_block_budget(const PagedArgs& a, cudaStream_t s);
+int int2_ctas_per_sm(int head_dim, int group);
+int int2_warps_per_cta();
+cudaError_t launch_attn_int2(const Int2Args& a, int head_dim, int group, int grid, cudaStream_t s);
+cudaError_t launch_tier_begin(const TierArgs& a, int prefill_tokens, cudaStream_t s);
+cudaError_t launch_tier_append(const TierArgs& a, const uint16_t* k_new, const uint16_t* v_new,
+                               cudaStream_t s);
+cudaError_t launch_tier_score(const TierArgs& a, int max_nw, int group, cudaStream_t s);
+cudaError_t launch_tier_route(const TierArgs& a, cudaStream_t s);
+cudaError_t launch_tier_quantize(const TierArgs& a, int max_items, int num_sms, cudaStream_t s);
+cudaError_t launch_tier_promote(const TierArgs& a, int max_items, int num_sms, cudaStream_t s);
+cudaError_t launch_tier_finish(const TierArgs& a, cudaStream_t s);
 
 enum : uint32_t { kStatusNoPage = 2u };   // a sequence ran out of free pages
+enum : uint32_t { kStatusRouteCap = 4u };  // more windows than the routing sort holds
 
 constexpr int kScoreThreads = 256;
 

@@ -1,0 +1,544 @@
+// Two-tier window routing with an INT2 tier ("QEvict: Recoverable Quantized
+// KV Eviction for Attention-Drift-Robust Long-Context Decoding", review
+// page Sec. 4): bookkeeping, window scores, routing, quantization.
+//
+// Positions [0, 5) are sinks, [5 + 128 j, 5 + 128 (j + 1)) window j; the
+// bf16 pool holds 16-token pages aligned to that grid (page b*pps holds the
+// sinks), so a window is 8 pages and its tiles are the 16-token tiles
+// 8 j .. 8 j + 7 of the grid.  A sequence's bookkeeping runs in one CTA;
+// the routing sorts the candidates in shared memory (bitonic), then
+// quantization (first demotion only) and promotion (from the ledger) run as
+// grid-stride kernels over (window, layer, KV head) items, and the pages the
+// demoted and evicted windows held return to the free stack last, after the
+// quantization has read them.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kvev_internal.h"
+
+namespace kvev {
+namespace {
+
+constexpr int kBook = 1024;
+
+__device__ __forceinline__ uint32_t order_bits(float f) {
+    const uint32_t u = __float_as_uint(f + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// Exclusive block scan of one int per thread (blockDim.x = kBook); *total.
+__device__ __forceinline__ int scan_excl(int v, int* red, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, m);
+        if (lane >= m) x += y;
+    }
+    if (lane == 31) red[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nw ? red[lane] : 0;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, m);
+            if (lane >= m) w += y;
+        }
+        red[lane] = w;
+    }
+    __syncthreads();
+    const int before = (warp > 0 ? red[warp - 1] : 0) + x - v;
+    *total = red[nw - 1];
+    __syncthreads();
+    return before;
+}
+__device__ __forceinline__ bool is_bf16_tier(uint8_t t) {
+    return t == KVEV_TIER_UNROUTED || t == KVEV_TIER_FULL;
+}
+
+// ---------------------------------------------------------------- begin
+__global__ void __launch_bounds__(kBook) tier_begin_kernel(const TierArgs a, int n0) {
+    griddep_wait();
+    griddep_release();
+    const int b = blockIdx.x, pps = a.c.pages_per_seq, MW = a.c.max_windows;
+    const int base = b * pps;
+    const int hist = n0 - kTierSinks;
+    const int nw = hist / kTierW, tl = hist - nw * kTierW;
+    const int n_tail_pages = (tl + kTile - 1) / kTile;
+    const int used = 1 + nw * (kTierW / kTile) + n_tail_pages;
+    for (int w = threadIdx.x; w < MW; w += blockDim.x) {
+        const size_t wi = (size_t)b * MW + w;
+        a.st.tier[wi] = w < nw ? KVEV_TIER_UNROUTED : KVEV_TIER_NONE;
+        a.st.score[wi] = 0.f;
+        a.st.has_codes[wi] = 0;
+        for (int i = 0; i < kTierW / kTile; ++i)
+            a.st.win_pages[wi * (kTierW / kTile) + i] = w < nw ? base + 1 + w * (kTierW / kTile) + i : -1;
+    }
+    for (int i = threadIdx.x; i < kTierW / kTile; i += blockDim.x)
+        a.st.tail_pages[(size_t)b * (kTierW / kTile) + i] =
+            i < n_tail_pages ? base + 1 + nw * (kTierW / kTile) + i : -1;
+    for (int k = threadIdx.x; k < pps - used; k += blockDim.x)   // lowest free page on top
+        a.c.free_pages[(size_t)base + k] = base + pps - 1 - k;
+    if (threadIdx.x == 0) {
+        a.c.n_free[b] = pps - used;
+        a.st.n_windows[b] = nw;
+        a.st.tail_len[b] = tl;
+        a.seq_len[b] = n0;
+    }
+}
+
+// --------------------------------------------------------------- append
+// The new token joins the tail (a page popped when the tail needs one); a
+// tail of 128 tokens becomes a new unrouted window.  Then the attention
+// lists are rebuilt: bf16 blocks (sink page, the pages of unrouted and Full
+// windows in window order, the tail pages) with their positions and
+// lengths, and the INT2 windows in window order.
+__global__ void __launch_bounds__(kBook) tier_append_kernel(const TierArgs a,
+                                                            const uint16_t* k_new,
+                                                            const uint16_t* v_new) {
+    __shared__ int red[32];
+    __shared__ int s_page, s_row, s_nw, s_tl;
+    griddep_wait();
+    griddep_release();
+    const int b = blockIdx.x, pps = a.c.pages_per_seq, MW = a.c.max_windows;
+    constexpr int PW = kTierW / kTile;   // pages per window
+    int32_t* tail = a.st.tail_pages + (size_t)b * PW;
+    if (threadIdx.x == 0) {
+        int tl = a.st.tail_len[b];
+        int page = -1;
+        if (tl >= kTierW) {      // no window slot was left for a complete tail
+            atomicOr(a.status, kStatusNoPage);
+        } else if (tl % kTile == 0) {   // the tail needs a fresh page
+            const int nf = a.c.n_free[b];
+            if (nf > 0) {
+                page = a.c.free_pages[(size_t)b * pps + nf - 1];
+                a.c.n_free[b] = nf - 1;
+                tail[tl / kTile] = page;
+            } else {
+                atomicOr(a.status, kStatusNoPage);
+            }
+        } else {
+            page = tail[tl / kTile];
+        }
+        s_page = page;
+        s_row = tl % kTile;
+        int nw = a.st.n_windows[b];
+        if (page >= 0) {
+            ++tl;
+            a.seq_len[b] += 1;
+            if (tl == kTierW && nw < MW) {   // the tail completes window nw
+                const size_t wi = (size_t)b * MW + nw;
+                for (int i = 0; i < PW; ++i) {
+                    a.st.win_pages[wi * PW + i] = tail[i];
+                    tail[i] = -1;
+                }
+                a.st.tier[wi] = KVEV_TIER_UNROUTED;
+                a.st.score[wi] = 0.f;
+                a.st.has_codes[wi] = 0;
+                ++nw;
+                tl = 0;
+            }
+        }
+        a.st.tail_len[b] = tl;
+        a.st.n_windows[b] = nw;
+        s_nw = nw;
+        s_tl = tl;
+    }
+    __syncthreads();
+    const int page = s_page;
+    if (page >= 0) {   // K/V rows of the new token, every layer and KV head
+        const int lpr = a.head_dim / 8;
+        const int rows = a.n_layers * a.n_kv;
+        for (int u = threadIdx.x; u < 2 * rows * lpr; u += blockDim.x) {
+            const int kv = u / (rows * lpr), rest = u - kv * rows * lpr;
+            const int r = rest / lpr, c = rest - r * lpr;
+            const size_t src = ((size_t)b * rows + r) * lpr + c;
+            const size_t dst = (((size_t)page * rows + r) * kTile + s_row) * lpr + c;
+            const uint4 v = reinterpret_cast<const uint4*>(kv ? v_new : k_new)[src];
+            reinterpret_cast<uint4*>(kv ? a.c.v_pool : a.c.k_pool)[dst] = v;
+        }
+    }
+    // ---- attention lists
+    const int nw = s_nw, tl = s_tl;
+    int32_t* bt = a.bt + (size_t)b * a.bt_ld;
+    int32_t* bpos = a.bpos + (size_t)b * a.bt_ld;
+    int32_t* blen = a.blen + (size_t)b * a.bt_ld;
+    if (threadIdx.x == 0) {
+        bt[0] = b * pps;
+        bpos[0] = 0;
+        blen[0] = kTierSinks;
+    }
+    int n_bf = 0, n_q = 0;
+    for (int w0 = 0; w0 < nw; w0 += blockDim.x) {
+        const int w = w0 + threadIdx.x;
+        const uint8_t tr = w < nw ? a.st.tier[(size_t)b * MW + w] : KVEV_TIER_NONE;
+        int tot_bf, tot_q;
+        const int off_bf = scan_excl(is_bf16_tier(tr) ? 1 : 0, red, &tot_bf);
+        const int off_q = scan_excl(tr == KVEV_TIER_QUANT ? 1 : 0, red, &tot_q);
+        if (is_bf16_tier(tr)) {
+            const int j0 = 1 + (n_bf + off_bf) * PW;
+            for (int i = 0; i < PW; ++i) {
+                bt[j0 + i] = a.st.win_pages[((size_t)b * MW + w) * PW + i];
+                bpos[j0 + i] = kTierSinks + w * kTierW + i * kTile;
+                blen[j0 + i] = kTile;
+            }
+        }
+        if (tr == KVEV_TIER_QUANT) a.qlist[(size_t)b * MW + n_q + off_q] = w;
+        n_bf += tot_bf;
+        n_q += tot_q;
+    }
+    const int j0 = 1 + n_bf * PW;
+    const int n_tail = (tl + kTile - 1) / kTile;
+    for (int i = threadIdx.x; i < n_tail; i += blockDim.x) {
+        bt[j0 + i] = tail[i];
+        bpos[j0 + i] = kTierSinks + nw * kTierW + i * kTile;
+        blen[j0 + i] = min(kTile, tl - i * kTile);
+    }
+    if (threadIdx.x == 0) {
+        a.nblk[b] = j0 + n_tail;
+        a.nq[b] = n_q;
+    }
+}
+
+// ---------------------------------------------------------- window score
+// One warp per window: per layer, the head-averaged attention the window's
+// 128 tokens received, from the tile statistics of the attention kernels
+// (running max m, sum of exp2(x - m) per head and 16-token tile) and the
+// combine's log2-sum-exp: sum exp2(m - lse) * sum; folded into the EMA
+// layer after layer.
+template <int G>
+__global__ void __launch_bounds__(256) tier_score_kernel(const TierArgs a) {
+    griddep_wait();
+    griddep_release();
+    const int b = blockIdx.y, MW = a.c.max_windows;
+    const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (w >= a.st.n_windows[b]) return;
+    const size_t wi = (size_t)b * MW + w;
+    const uint8_t tr = a.st.tier[wi];
+    if (!is_bf16_tier(tr) && tr != KVEV_TIER_QUANT) return;
+    constexpr int PW = kTierW / kTile;
+    float m = a.st.score[wi];
+    const float inv_hq = 1.0f / (float)a.n_q, oma = 1.0f - a.alpha;
+    for (int l = 0; l < a.n_layers; ++l) {
+        float s = 0.f;
+        for (int k = lane; k < PW * a.n_kv; k += 32) {   // (tile, KV head) pairs
+            const int i = k % PW, g = k / PW;
+            const size_t row = ((size_t)l * a.batch + b) * a.n_kv + g;
+            const float2* st = a.tile_stats + (row * a.stats_tiles + (size_t)w * PW + i) * G;
+            const float* lse = a.lse2 + ((size_t)l * a.batch + b) * a.n_q + g * G;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float2 v = st[h];
+                s = fmaf(exp2_approx(v.x - lse[h]), v.y, s);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        m = fmaf(a.alpha, s * inv_hq, oma * m);
+    }
+    if (lane == 0) a.st.score[wi] = m;
+}
+
+// --------------------------------------------------------------- routing
+// Candidates: Full and INT2 windows, and unrouted windows whose last token
+// is older than the recent region.  Ranked by score (ties: lower index)
+// with a bitonic sort of (order bits of -score, window) keys; the top K_f
+// are Full, the next K_q INT2, the rest evicted.
+__global__ void __launch_bounds__(kBook) tier_route_kernel(const TierArgs a) {
+    __shared__ unsigned long long keys[kTierRouteCap];
+    __shared__ uint8_t nt[kTierRouteCap];
+    __shared__ int red[32];
+    griddep_wait();
+    griddep_release();
+    const int b = blockIdx.x, pps = a.c.pages_per_seq, MW = a.c.max_windows;
+    constexpr int PW = kTierW / kTile;
+    const int nw = a.st.n_windows[b];
+    if (nw > kTierRouteCap) {
+        if (threadIdx.x == 0) {
+            atomicOr(a.status, kStatusRouteCap);
+            a.n_quant[b] = a.n_prom[b] = a.n_freeing[b] = 0;
+        }
+        return;
+    }
+    int n = 1;
+    while (n < nw) n <<= 1;
+    const int horizon = a.seq_len[b] - kTierRecent;
+    for (int w = threadIdx.x; w < n; w += blockDim.x) {
+        unsigned long long key = ~0ull;
+        if (w < nw) {
+            const size_t wi = (size_t)b * MW + w;
+            const uint8_t tr = a.st.tier[wi];
+            nt[w] = tr;
+            const bool cand = tr == KVEV_TIER_FULL || tr == KVEV_TIER_QUANT ||
+                              (tr == KVEV_TIER_UNROUTED && kTierSinks + (w + 1) * kTierW <= horizon);
+            if (cand) key = ((unsigned long long)order_bits(-a.st.score[wi]) << 32) | (unsigned)w;
+        }
+        keys[w] = key;
+    }
+    __syncthreads();
+    for (int k = 2; k <= n; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int p = i ^ j;
+                if (p > i) {
+                    const unsigned long long x = keys[i], y = keys[p];
+                    if ((x > y) == ((i & k) == 0)) {
+                        keys[i] = y;
+                        keys[p] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    for (int r = threadIdx.x; r < n; r += blockDim.x) {
+        const unsigned long long key = keys[r];
+        if (key != ~0ull) {
+            const int w = (int)(key & 0xffffffffu);
+            nt[w] = r < a.k_full ? KVEV_TIER_FULL
+                    : r < a.k_full + a.k_quant ? KVEV_TIER_QUANT : KVEV_TIER_EVICTED;
+        }
+    }
+    __syncthreads();
+    // transitions: lists for quantization, promotion and freeing
+    int nq = 0, np = 0, nf = 0;
+    const int free0 = a.c.n_free[b];
+    for (int w0 = 0; w0 < nw; w0 += blockDim.x) {
+        const int w = w0 + threadIdx.x;
+        uint8_t o = KVEV_TIER_NONE, t = KVEV_TIER_NONE;
+        bool codes = false;
+        if (w < nw) {
+            o = a.st.tier[(size_t)b * MW + w];
+            t = nt[w];
+            codes = a.st.has_codes[(size_t)b * MW + w] != 0;
+        }
+        const bool quant = is_bf16_tier(o) && t == KVEV_TIER_QUANT && !codes;
+        const bool prom = o == KVEV_TIER_QUANT && t == KVEV_TIER_FULL;
+        const bool frees = is_bf16_tier(o) && (t == KVEV_TIER_QUANT || t == KVEV_TIER_EVICTED);
+        int tq, tp, tf;
+        const int oq = scan_excl(quant ? 1 : 0, red, &tq);
+        const int op = scan_excl(prom ? 1 : 0, red, &tp);
+        const int of = scan_excl(frees ? 1 : 0, red, &tf);
+        if (w < nw) {
+            const size_t wi = (size_t)b * MW + w;
+            if (quant) a.quant_list[(size_t)b * MW + nq + oq] = w;
+            if (frees) a.free_list[(size_t)b * MW + nf + of] = w;
+            if (prom) {   // 8 pages from the top of the free stack (pages freed before this event)
+                const int k = np + op;
+                for (int i = 0; i < PW; ++i) {
+                    const int top = free0 - 1 - k * PW - i;
+                    a.st.win_pages[wi * PW + i] =
+                        top >= 0 ? a.c.free_pages[(size_t)b * pps + top] : -1;
+                }
+                a.prom_list[(size_t)b * MW + k] = w;
+            }
+            if (quant) a.st.has_codes[wi] = 1;
+            if (t == KVEV_TIER_EVICTED) a.st.has_codes[wi] = 0;
+            a.st.tier[wi] = t;
+        }
+        nq += tq;
+        np += tp;
+        nf += tf;
+    }
+    if (threadIdx.x == 0) {
+        a.n_quant[b] = nq;
+        a.n_prom[b] = np;
+        a.n_freeing[b] = nf;
+        if (np * PW > free0) {
+            atomicOr(a.status, kStatusNoPage);
+            a.n_prom[b] = free0 / PW;
+        }
+        a.c.n_free[b] = free0 - min(np * PW, free0 / PW * PW);
+    }
+}
+
+// Items of the quantize / promote kernels: (sequence, list entry, layer,
+// KV head), grid-stride; a CTA of 128 threads per item.
+template <int D>
+__global__ void __launch_bounds__(128) tier_quantize_kernel(const TierArgs a, int max_items) {
+    using Lay = LedgerLayout<D>;
+    constexpr int PW = kTierW / kTile;
+    __shared__ uint8_t codes[kTierW][D];
+    griddep_wait();
+    griddep_release();
+    const int LG = a.n_layers * a.n_kv, MW = a.c.max_windows;
+    const int64_t total = (int64_t)a.batch * max_items * LG;
+    for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
+        const int lg = (int)(it % LG);
+        const int e = (int)((it / LG) % max_items), b = (int)(it / ((int64_t)LG * max_items));
+        if (e >= a.n_quant[b]) continue;   // the same for the whole CTA
+        const int w = a.quant_list[(size_t)b * MW + e];
+        const int l = lg / a.n_kv, g = lg % a.n_kv;
+        const int32_t* pages = a.st.win_pages + ((size_t)b * MW + w) * PW;
+        unsigned char* led = reinterpret_cast<unsigned char*>(a.c.ledger) +
+                             ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES;
+        auto row_of = [&](const void* pool, int tok) {
+            const size_t r = (((size_t)pages[tok / kTile] * a.n_layers + l) * a.n_kv + g) * kTile +
+                             tok % kTile;
+            return reinterpret_cast<const __nv_bfloat16*>(pool) + r * D;
+        };
+        // keys: per channel over 32-token groups (thread = channel)
+        for (int c = threadIdx.x; c < D; c += blockDim.x)
+            for (int grp = 0; grp < kTierW / kQGroup; ++grp) {
+                float mn = INFINITY, mx = -INFINITY;
+                for (int i = 0; i < kQGroup; ++i) {
+                    const float x = __bfloat162float(row_of(a.c.k_pool, grp * kQGroup + i)[c]);
+                    mn = fminf(mn, x);
+                    mx = fmaxf(mx, x);
+                }
+                const __half z16 = __float2half_rn(mn);
+                const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+                const float z = __half2float(z16), s = __half2float(s16);
+                reinterpret_cast<__half*>(led + Lay::KS)[grp * D + c] = s16;
+                reinterpret_cast<__half*>(led + Lay::KZ)[grp * D + c] = z16;
+                for (int i = 0; i < kQGroup; ++i) {
+                    const float x = __bfloat162float(row_of(a.c.k_pool, grp * kQGroup + i)[c]);
+                    const float r = s == 0.f ? 0.f : rintf(__fdiv_rn(__fsub_rn(x, z), s));
+                    codes[grp * kQGroup + i][c] = (uint8_t)fminf(fmaxf(r, 0.f), 3.f);
+                }
+            }
+        __syncthreads();
+        for (int u = threadIdx.x; u < kTierW * (D / 16); u += blockDim.x) {   // pack kc
+            const int tok = u / (D / 16), sblk = u % (D / 16);
+            uint32_t word = 0;
+            for (int e2 = 0; e2 < 16; ++e2)
+                word |= (uint32_t)codes[tok][16 * sblk + e2] << ((e2 & 1) * 16 + 2 * (e2 >> 1));
+            reinterpret_cast<uint32_t*>(led + Lay::KC)[u] = word;
+        }
+        __syncthreads();
+        // values: per token over 32-channel groups (thread = token)
+        for (int tok = threadIdx.x; tok < kTierW; tok += blockDim.x) {
+            const __nv_bfloat16* row = row_of(a.c.v_pool, tok);
+            for (int cg = 0; cg < D / kQGroup; ++cg) {
+                float mn = INFINITY, mx = -INFINITY;
+                for (int i = 0; i < kQGroup; ++i) {
+                    const float x = __bfloat162float(row[cg * kQGroup + i]);
+                    mn = fminf(mn, x);
+                    mx = fmaxf(mx, x);
+                }
+                const __half z16 = __float2half_rn(mn);
+                const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+                const float z = __half2float(z16), s = __half2float(s16);
+                reinterpret_cast<__half*>(led + Lay::VS)[tok * (D / kQGroup) + cg] = s16;
+                reinterpret_cast<__half*>(led + Lay::VZ)[tok * (D / kQGroup) + cg] = z16;
+                for (int i = 0; i < kQGroup; ++i) {
+                    const float x = __bfloat162float(row[cg * kQGroup + i]);
+                    const float r = s == 0.f ? 0.f : rintf(__fdiv_rn(__fsub_rn(x, z), s));
+                    codes[tok][cg * kQGroup + i] = (uint8_t)fminf(fmaxf(r, 0.f), 3.f);
+                }
+            }
+        }
+        __syncthreads();
+        for (int u = threadIdx.x; u < (kTierW / 16) * D; u += blockDim.x) {   // pack vc
+            const int chunk = u / D, c = u % D;
+            uint32_t word = 0;
+            for (int e2 = 0; e2 < 16; ++e2)
+                word |= (uint32_t)codes[16 * chunk + e2][c] << ((e2 & 1) * 16 + 2 * (e2 >> 1));
+            reinterpret_cast<uint32_t*>(led + Lay::VC)[u] = word;
+        }
+        __syncthreads();
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) tier_promote_kernel(const TierArgs a, int max_items) {
+    using Lay = LedgerLayout<D>;
+    constexpr int PW = kTierW / kTile;
+    griddep_wait();
+    griddep_release();
+    const int LG = a.n_layers * a.n_kv, MW = a.c.max_windows;
+    const int64_t total = (int64_t)a.batch * max_items * LG;
+    for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
+        const int lg = (int)(it % LG);
+        const int e = (int)((it / LG) % max_items), b = (int)(it / ((int64_t)LG * max_items));
+        if (e >= a.n_prom[b]) continue;
+        const int w = a.prom_list[(size_t)b * MW + e];
+        const int l = lg / a.n_kv, g = lg % a.n_kv;
+        const int32_t* pages = a.st.win_pages + ((size_t)b * MW + w) * PW;
+        const unsigned char* led = reinterpret_cast<const unsigned char*>(a.c.ledger) +
+                                   ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES;
+        const uint32_t* kc = reinterpret_cast<const uint32_t*>(led + Lay::KC);
+        const uint32_t* vc = reinterpret_cast<const uint32_t*>(led + Lay::VC);
+        const __half* ks = reinterpret_cast<const __half*>(led + Lay::KS);
+        const __half* kz = reinterpret_cast<const __half*>(led + Lay::KZ);
+        const __half* vs = reinterpret_cast<const __half*>(led + Lay::VS);
+        const __half* vz = reinterpret_cast<const __half*>(led + Lay::VZ);
+        for (int u = threadIdx.x; u < kTierW * D; u += blockDim.x) {
+            const int tok = u / D, c = u % D;
+            const int page = pages[tok / kTile];
+            if (page < 0) continue;   // no page could be taken for this promotion
+            const size_t r = (((size_t)page * a.n_layers + l) * a.n_kv + g) * kTile + tok % kTile;
+            const int ek = c % 16, et = tok % 16;
+            const uint32_t qk = (kc[tok * (D / 16) + c / 16] >> ((ek & 1) * 16 + 2 * (ek >> 1))) & 3u;
+            const uint32_t qv = (vc[(tok / 16) * D + c] >> ((et & 1) * 16 + 2 * (et >> 1))) & 3u;
+            const int grp = tok / kQGroup, cg = c / kQGroup;
+            const float kval = fmaf((float)qk, __half2float(ks[grp * D + c]), __half2float(kz[grp * D + c]));
+            const float vval = fmaf((float)qv, __half2float(vs[tok * (D / kQGroup) + cg]),
+                                    __half2float(vz[tok * (D / kQGroup) + cg]));
+            reinterpret_cast<__nv_bfloat16*>(a.c.k_pool)[r * D + c] = __float2bfloat16_rn(kval);
+            reinterpret_cast<__nv_bfloat16*>(a.c.v_pool)[r * D + c] = __float2bfloat16_rn(vval);
+        }
+    }
+}
+
+// The pages of windows that left the bf16 tier return to the free stack.
+__global__ void __launch_bounds__(256) tier_finish_kernel(const TierArgs a) {
+    griddep_wait();
+    griddep_release();
+    const int b = blockIdx.x, pps = a.c.pages_per_seq, MW = a.c.max_windows;
+    constexpr int PW = kTierW / kTile;
+    const int n = a.n_freeing[b], nf = a.c.n_free[b];
+    for (int u = threadIdx.x; u < n * PW; u += blockDim.x) {
+        const int k = u / PW, i = u % PW;
+        const int w = a.free_list[(size_t)b * MW + k];
+        int32_t* wp = a.st.win_pages + ((size_t)b * MW + w) * PW;
+        a.c.free_pages[(size_t)b * pps + nf + u] = wp[i];
+        wp[i] = -1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) a.c.n_free[b] = nf + n * PW;
+}
+
+}  // namespace
+
+cudaError_t launch_tier_begin(const TierArgs& a, int prefill_tokens, cudaStream_t s) {
+    return launch_pdl(tier_begin_kernel, dim3(a.batch), dim3(kBook), 0, s, a, prefill_tokens);
+}
+
+cudaError_t launch_tier_append(const TierArgs& a, const uint16_t* k_new, const uint16_t* v_new,
+                               cudaStream_t s) {
+    return launch_pdl(tier_append_kernel, dim3(a.batch), dim3(kBook), 0, s, a, k_new, v_new);
+}
+
+cudaError_t launch_tier_score(const TierArgs& a, int max_nw, int group, cudaStream_t s) {
+    if (max_nw <= 0) return cudaSuccess;
+    const dim3 grid((max_nw + 7) / 8, a.batch);
+    if (group == 4) return launch_pdl(tier_score_kernel<4>, grid, dim3(256), 0, s, a);
+    if (group == 8) return launch_pdl(tier_score_kernel<8>, grid, dim3(256), 0, s, a);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_tier_route(const TierArgs& a, cudaStream_t s) {
+    return launch_pdl(tier_route_kernel, dim3(a.batch), dim3(kBook), 0, s, a);
+}
+
+cudaError_t launch_tier_quantize(const TierArgs& a, int max_items, int num_sms, cudaStream_t s) {
+    if (max_items <= 0) return cudaSuccess;
+    if (a.head_dim != 128) return cudaErrorInvalidValue;
+    return launch_pdl(tier_quantize_kernel<128>, dim3(4 * num_sms), dim3(128), 0, s, a, max_items);
+}
+
+cudaError_t launch_tier_promote(const TierArgs& a, int max_items, int num_sms, cudaStream_t s) {
+    if (max_items <= 0) return cudaSuccess;
+    if (a.head_dim != 128) return cudaErrorInvalidValue;
+    return launch_pdl(tier_promote_kernel<128>, dim3(4 * num_sms), dim3(128), 0, s, a, max_items);
+}
+
+cudaError_t launch_tier_finish(const TierArgs& a, cudaStream_t s) {
+    return launch_pdl(tier_finish_kernel, dim3(a.batch), dim3(256), 0, s, a);
+}
+
+}  // namespace kvev

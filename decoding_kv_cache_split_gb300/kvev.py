@@ -27,6 +27,9 @@ KVEV_POOL_SUM, KVEV_POOL_MEAN = 0, 1
 KVEV_BF16 = 0
 KVEV_MAX_REGIONS = 16
 KVEV_SCORE_LRFU, KVEV_SCORE_MEMDECAY = 0, 1
+KVEV_TIER_NONE, KVEV_TIER_UNROUTED, KVEV_TIER_FULL, KVEV_TIER_QUANT, KVEV_TIER_EVICTED = range(5)
+KVEV_TIER_SINKS, KVEV_TIER_RECENT, KVEV_TIER_WINDOW = 5, 32, 128
+TIER_LEDGER_BYTES = 12288   # one (window, layer, KV head) entry at head_dim 128
 KVEV_PROFILE_SLOTS = 8
 PROFILE_NAMES = ["append", "attention", "combine", "score", "select", "compact", "init_state",
                  "readmit"]
@@ -36,7 +39,8 @@ EXPORTS = ["kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_siz
            "kvev_refresh_mode", "kvev_configure", "kvev_begin", "kvev_length",
            "kvev_init_state", "kvev_step", "kvev_step_host", "kvev_set_debug",
            "kvev_profile", "kvev_profile_read", "kvev_launch_count", "kvev_sync",
-           "kvev_paged_begin", "kvev_paged_step", "kvev_readmit", "kvev_attend_noalloc"]
+           "kvev_paged_begin", "kvev_paged_step", "kvev_readmit", "kvev_set_tiers",
+           "kvev_tier_begin", "kvev_tier_step", "kvev_attend_noalloc"]
 
 
 class KvevError(RuntimeError):
@@ -104,6 +108,20 @@ def region_table(base, lam, pinned, *, score_kind=KVEV_SCORE_MEMDECAY, rho=0.9,
     return t
 
 
+class kvev_tier_cache(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("pages_per_seq", ctypes.c_int32), ("free_pages", ctypes.c_void_p),
+                ("n_free", ctypes.c_void_p), ("ledger", ctypes.c_void_p),
+                ("max_windows", ctypes.c_int32)]
+
+
+class kvev_tier_state(ctypes.Structure):
+    _fields_ = [("score", ctypes.c_void_p), ("tier", ctypes.c_void_p),
+                ("has_codes", ctypes.c_void_p), ("win_pages", ctypes.c_void_p),
+                ("n_windows", ctypes.c_void_p), ("tail_pages", ctypes.c_void_p),
+                ("tail_len", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -136,6 +154,9 @@ def lib():
             "kvev_paged_begin": ([P, P, P, I32, P], I32),
             "kvev_paged_step": ([P, P, P, P, P, P, I64, P, P, P, P], I32),
             "kvev_readmit": ([P, P, P, I32, I32, I32, P], I32),
+            "kvev_set_tiers": ([P, I64, I64, I32], I32),
+            "kvev_tier_begin": ([P, P, P, I32, P], I32),
+            "kvev_tier_step": ([P, P, P, P, P, P, I64, P, P], I32),
             "kvev_attend_noalloc": ([P, P, P, P, I32, P, P, P], I32),
         }
         for name, (args, res) in sig.items():
@@ -274,6 +295,22 @@ def kvev_readmit(ctx, cache: kvev_paged_cache, state: kvev_block_state, seq: int
                  persist: bool = True, stream=None) -> None:
     _check(lib().kvev_readmit(ctx, ctypes.byref(cache), ctypes.byref(state), int(seq), int(lid),
                               int(bool(persist)), _stream(stream)), ctx)
+
+
+def kvev_set_tiers(ctx, k_full: int, k_quant: int, omega: int) -> None:
+    _check(lib().kvev_set_tiers(ctx, int(k_full), int(k_quant), int(omega)), ctx)
+
+
+def kvev_tier_begin(ctx, cache: kvev_tier_cache, state: kvev_tier_state, prefill_tokens: int,
+                    stream=None) -> None:
+    _check(lib().kvev_tier_begin(ctx, ctypes.byref(cache), ctypes.byref(state),
+                                 int(prefill_tokens), _stream(stream)), ctx)
+
+
+def kvev_tier_step(ctx, q, k_new, v_new, cache: kvev_tier_cache, state: kvev_tier_state,
+                   step: int, out, stream=None) -> None:
+    _check(lib().kvev_tier_step(ctx, _ptr(q), _ptr(k_new), _ptr(v_new), ctypes.byref(cache),
+                                ctypes.byref(state), int(step), _ptr(out), _stream(stream)), ctx)
 
 
 def kvev_attend_noalloc(layout: kvev_layout, q, k, v, length: int, out, lse2, stream=None) -> None:
@@ -432,6 +469,74 @@ class PagedEvictionPass:
 
     def readmit(self, seq: int, lid: int, persist: bool = True, stream=None):
         kvev_readmit(self.ctx, self.cache, self.state, seq, lid, persist, stream)
+
+    def close(self):
+        if self.ctx is not None:
+            kvev_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class TierEvictionPass:
+    """Device buffers plus a context for one two-tier (bf16 + INT2) run.
+
+    bf16 page pools [batch * pps][Ly][Hkv][16][d] (page b*pps holds the 5
+    sinks, page b*pps + 1 + i tokens 5 + 16 i ..); the INT2 ledger
+    [batch][max_windows][Ly][Hkv][12288] bytes; per-window score, tier,
+    ledger flag and pages; outputs out [b][Ly][Hq][d] fp32.  All torch
+    tensors on the current CUDA device."""
+
+    def __init__(self, n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, pages_per_seq,
+                 k_full, k_quant, omega, alpha, device="cuda"):
+        import torch
+        self.torch = torch
+        self.pps, self.max_ctx = int(pages_per_seq), int(max_ctx)
+        self.max_windows = (self.max_ctx - KVEV_TIER_SINKS) // KVEV_TIER_WINDOW
+        self.layout = kvev_layout(n_layers, n_q_heads, n_kv_heads, head_dim, batch, self.max_ctx,
+                                  KVEV_TIER_WINDOW, KVEV_BF16)
+        self.ctx = kvev_create(self.layout, k_full, KVEV_TIER_WINDOW, alpha, 0.0)
+        kvev_set_tiers(self.ctx, k_full, k_quant, omega)
+        i32 = dict(dtype=torch.int32, device=device)
+        pshape = (batch * self.pps, n_layers, n_kv_heads, 16, head_dim)
+        self.k_pool = torch.zeros(pshape, dtype=torch.bfloat16, device=device)
+        self.v_pool = torch.zeros(pshape, dtype=torch.bfloat16, device=device)
+        self.free_pages = torch.zeros((batch, self.pps), **i32)
+        self.n_free = torch.zeros((batch,), **i32)
+        MW = self.max_windows
+        self.ledger = torch.zeros((batch, MW, n_layers, n_kv_heads, TIER_LEDGER_BYTES),
+                                  dtype=torch.uint8, device=device)
+        self.score = torch.zeros((batch, MW), dtype=torch.float32, device=device)
+        self.tier = torch.zeros((batch, MW), dtype=torch.uint8, device=device)
+        self.has_codes = torch.zeros((batch, MW), dtype=torch.uint8, device=device)
+        self.win_pages = torch.zeros((batch, MW, 8), **i32)
+        self.n_windows = torch.zeros((batch,), **i32)
+        self.tail_pages = torch.zeros((batch, 8), **i32)
+        self.tail_len = torch.zeros((batch,), **i32)
+        self.out = torch.zeros((batch, n_layers, n_q_heads, head_dim), dtype=torch.float32,
+                               device=device)
+        self.cache = kvev_tier_cache(self.k_pool.data_ptr(), self.v_pool.data_ptr(), self.pps,
+                                     self.free_pages.data_ptr(), self.n_free.data_ptr(),
+                                     self.ledger.data_ptr(), MW)
+        self.state = kvev_tier_state(self.score.data_ptr(), self.tier.data_ptr(),
+                                     self.has_codes.data_ptr(), self.win_pages.data_ptr(),
+                                     self.n_windows.data_ptr(), self.tail_pages.data_ptr(),
+                                     self.tail_len.data_ptr())
+        self.step_no = 0
+
+    def begin(self, prefill_tokens: int, stream=None):
+        kvev_tier_begin(self.ctx, self.cache, self.state, prefill_tokens, stream)
+        self.step_no = 0
+
+    def step(self, q, k_new, v_new, stream=None):
+        self.step_no += 1
+        kvev_tier_step(self.ctx, q, k_new, v_new, self.cache, self.state, self.step_no, self.out,
+                       stream)
+        return self.out
 
     def close(self):
         if self.ctx is not None:

@@ -327,6 +327,69 @@ kvev_status kvev_readmit(kvev_ctx* ctx, const kvev_paged_cache* cache,
                          const kvev_block_state* state, int32_t seq, int32_t lid,
                          int32_t persist, void* stream);
 
+/* ---- Two-tier window routing with an INT2 tier ---------------------------
+ * "QEvict: Recoverable Quantized KV Eviction for Attention-Drift-Robust
+ * Long-Context Decoding" (review page, Sec. 4): layout->page_tokens = 128
+ * (the window W), budget = K_f.  Tokens [0, 5) are sinks; windows are
+ * [5 + 128 j, 5 + 128 (j + 1)); the tokens after the last complete window
+ * (the tail) and the sinks stay in bf16 and are always attended.  Every step
+ * each live window's score folds the attention its tokens receive, averaged
+ * over query heads, into an EMA (weight alpha on the new value) layer after
+ * layer; every `omega` steps (at the end of steps t with t mod omega = 0)
+ * the candidates (Full and INT2 windows, and new windows whose last token is
+ * older than the 32 most recent) are ranked by score, ties to the lower
+ * index: the top K_f are Full (bf16), the next K_q INT2, the rest evicted for
+ * good (Eqs. (4)-(5)).  A window is quantized on its first demotion and its
+ * codes are kept in a ledger and reused on every later demotion; a promoted
+ * window is dequantized from the ledger into bf16 pages.  Attention runs over
+ * the bf16 pages and, dequantizing in the kernel, the INT2 windows.
+ * INT2 codec: keys per channel over 32-token groups, values per token over
+ * 32-channel groups; zero = fp16(min), scale = fp16((max - min) / 3) in fp32,
+ * code = clamp(rint((x - zero) / scale), 0, 3) in fp32 (0 when scale = 0);
+ * value = code * scale + zero in fp32; a promoted copy rounds it to bf16.
+ * Supported: head_dim 128, 4 query heads per KV head. */
+enum { KVEV_TIER_NONE = 0, KVEV_TIER_UNROUTED = 1, KVEV_TIER_FULL = 2, KVEV_TIER_QUANT = 3,
+       KVEV_TIER_EVICTED = 4 };
+enum { KVEV_TIER_SINKS = 5, KVEV_TIER_RECENT = 32, KVEV_TIER_WINDOW = 128 };
+typedef struct {
+    void* k_pool;            /* [batch * pps][n_layers][n_kv_heads][16][head_dim] bf16 pages */
+    void* v_pool;
+    int32_t pages_per_seq;   /* pps: sequence b owns pages [b*pps, (b+1)*pps) */
+    int32_t* free_pages;     /* [batch][pps] free-page stacks */
+    int32_t* n_free;         /* [batch] */
+    void* ledger;            /* [batch][max_windows][n_layers][n_kv_heads][12288 B] INT2
+                                codes + fp16 scale/zero of each quantized window */
+    int32_t max_windows;     /* (layout->max_ctx - 5) / 128 */
+} kvev_tier_cache;
+
+typedef struct {
+    float* score;            /* [batch][max_windows] window EMA */
+    uint8_t* tier;           /* [batch][max_windows] KVEV_TIER_* */
+    uint8_t* has_codes;      /* [batch][max_windows] ledger entry valid */
+    int32_t* win_pages;      /* [batch][max_windows][8] bf16 pages of a Full or unrouted window */
+    int32_t* n_windows;      /* [batch] complete windows so far */
+    int32_t* tail_pages;     /* [batch][8] bf16 pages of the tail */
+    int32_t* tail_len;       /* [batch] tokens after the last complete window */
+} kvev_tier_state;
+
+/* Tier capacities K_f (Full windows), K_q (INT2 windows) and the routing
+ * interval omega >= 1 (Eq. (3) gives K_f, K_q from a byte budget). */
+kvev_status kvev_set_tiers(kvev_ctx* ctx, int64_t k_full, int64_t k_quant, int32_t omega);
+
+/* Start a tiered run over a prefill of `prefill_tokens` (>= 5) tokens that
+ * the caller wrote into the pool: tokens 0..4 in rows 0..4 of page b*pps,
+ * token 5 + 16 i + r in row r of page b*pps + 1 + i.  All complete windows
+ * start unrouted (bf16) with score 0; the next step is 1. */
+kvev_status kvev_tier_begin(kvev_ctx* ctx, const kvev_tier_cache* cache,
+                            const kvev_tier_state* state, int32_t prefill_tokens, void* stream);
+
+/* One tiered decode step `step` (previous + 1): q, k_new, v_new, out as in
+ * kvev_step; afterwards state->tier holds every window's tier (a routing
+ * event at the end of this step included). */
+kvev_status kvev_tier_step(kvev_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                           const kvev_tier_cache* cache, const kvev_tier_state* state,
+                           int64_t step, float* out, void* stream);
+
 /* Attention of the pass without allocating: no counterpart on the pages;
  * it exists for callers that cannot call cudaMalloc (engines whose allocator
  * owns all device memory, latency-critical paths that cannot take the

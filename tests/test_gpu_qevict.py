@@ -1,0 +1,177 @@
+"""GPU parity of two-tier window routing with an INT2 tier (QEvict).
+
+The CUDA path runs through the C ABI (kvev_set_tiers, kvev_tier_begin,
+kvev_tier_step); the fp64 oracle (oracle/qevict.py) runs free from the same
+seeded prefill and inputs.  Per step and sequence: attention outputs
+(2e-3 relative per vector), window scores (1e-5 absolute), tiers (exact
+away from near ties), the INT2 ledger of every quantized window (codes and
+fp16 scale/zero bit-exact) and the bf16 pages of every full-precision window
+(bit-exact, promoted copies included).  Where two windows' scores sit within
+the tolerance across a tier boundary the device's ranking is checked
+admissible and the oracle continues along it.
+"""
+import copy
+
+import numpy as np
+import pytest
+
+from oracle import qevict as QE
+from workloads import Geometry, Workload
+
+from parity import OUT_RTOL, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from decoding_kv_cache_split_gb300 import kvev  # noqa: E402
+
+M_ATOL = 1e-5
+TIER_NAME = {kvev.KVEV_TIER_UNROUTED: "U", kvev.KVEV_TIER_FULL: "F", kvev.KVEV_TIER_QUANT: "Q",
+             kvev.KVEV_TIER_EVICTED: "E"}
+
+
+def _bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def load(tp, K, V, L0):
+    """Prefill into the windowed page layout: sinks in page b*pps, token
+    5 + 16 i + r in row r of page b*pps + 1 + i."""
+    Ly, batch, Hkv, _, d = K.shape
+    hist = L0 - 5
+    n_pages = -(-hist // 16)
+    for b in range(batch):
+        for src, pool in ((K, tp.k_pool), (V, tp.v_pool)):
+            sink = np.zeros((Ly, Hkv, 16, d), np.uint16)
+            sink[:, :, :5] = src[:, b, :, :5]
+            rest = np.zeros((Ly, Hkv, n_pages * 16, d), np.uint16)
+            rest[:, :, :hist] = src[:, b, :, 5:]
+            pages = rest.reshape(Ly, Hkv, n_pages, 16, d).transpose(2, 0, 1, 3, 4)
+            allp = np.concatenate([sink[None], pages], axis=0)
+            pool[b * tp.pps:b * tp.pps + 1 + n_pages].copy_(
+                torch.from_numpy(np.ascontiguousarray(allp).view(np.int16)).view(torch.bfloat16))
+
+
+def decode_ledger(entry: np.ndarray, d: int = 128):
+    """Codes and fp16 scale/zero of one device ledger entry (12288 bytes)."""
+    W = 128
+    kc = entry[:4096].view(np.uint32).reshape(W, d // 16)
+    ks = entry[4096:5120].view(np.float16).reshape(W // 32, d)
+    kz = entry[5120:6144].view(np.float16).reshape(W // 32, d)
+    vc = entry[6144:10240].view(np.uint32).reshape(W // 16, d)
+    vs = entry[10240:11264].view(np.float16).reshape(W, d // 32)
+    vz = entry[11264:12288].view(np.float16).reshape(W, d // 32)
+    e = np.arange(16)
+    shift = (e & 1) * 16 + 2 * (e >> 1)
+    kq = ((kc[:, :, None] >> shift[None, None, :]) & 3).reshape(W, d).astype(np.uint8)
+    vq = ((vc[:, None, :] >> shift[None, :, None]) & 3).reshape(W, d).astype(np.uint8)
+    return kq, ks, kz, vq, vs, vz
+
+
+def admissible(m: dict, dev_tiers: dict, tol: float):
+    """Every window the device placed higher scores at least as much as
+    every window it placed lower, up to tol."""
+    rank = {"F": 0, "Q": 1, "E": 2}
+    for a, ta in dev_tiers.items():
+        for b, tb in dev_tiers.items():
+            if rank[ta] < rank[tb]:
+                assert m[a] >= m[b] - tol, f"window {a} ({ta}) below {b} ({tb})"
+
+
+def compare(tp, P, seqs, b, t, q, kn, vn, stats):
+    pre = copy.deepcopy(seqs[b])
+    res = QE.step(P, seqs[b], t, q, kn, vn)
+    seq = seqs[b]
+    dev_tier = [TIER_NAME.get(int(x), "-") for x in tp.tier[b, :len(seq.windows)].cpu().numpy()]
+    if res["routed"] and dev_tier != seq.tiers():
+        # a near tie at a tier boundary: check the device's choice, then follow it
+        cand = {w.wid: res["m"][w.wid] for w in pre.windows if w.wid in res["m"]}
+        new_t = {wid: dev_tier[wid] for wid in cand if dev_tier[wid] in ("F", "Q", "E")}
+        admissible(cand, new_t, M_ATOL)
+        order = sorted(new_t, key=lambda wid: ({"F": 0, "Q": 1, "E": 2}[new_t[wid]], -cand[wid], wid))
+        seqs[b] = pre
+        res = QE.step(P, seqs[b], t, q, kn, vn, ranking=order)
+        seq = seqs[b]
+        stats["swaps"] += 1
+    assert dev_tier == seq.tiers(), f"step {t} seq {b}: tiers {dev_tier} vs {seq.tiers()}"
+    for w0, w in zip(pre.windows, seq.windows):
+        stats["promoted"] += w0.tier == "Q" and w.tier == "F"
+        stats["redemoted"] += w0.tier == "F" and w.tier == "Q" and w0.ledger is not None
+    out = tp.out[b].cpu().numpy().astype(np.float64)
+    err = np.abs(out - res["out"]).max(-1) / np.abs(res["out"]).max(-1)
+    assert err.max() <= OUT_RTOL, f"step {t} seq {b}: output rel err {err.max():.2e}"
+    stats["out_rel"] = max(stats["out_rel"], float(err.max()))
+    sc = tp.score[b].cpu().numpy().astype(np.float64)
+    for wid, m in res["m"].items():
+        assert abs(sc[wid] - m) <= M_ATOL, f"step {t} seq {b}: score of window {wid}"
+        stats["m_abs"] = max(stats["m_abs"], abs(sc[wid] - m))
+    assert int(tp.n_windows[b]) == len(seq.windows)
+    assert int(tp.tail_len[b]) == seq.K_tail.shape[2]
+    wp = tp.win_pages[b].cpu().numpy()
+    led = tp.ledger[b].cpu().numpy()
+    for w in seq.windows:
+        if w.tier in ("U", "F"):
+            for i in range(8):
+                page = wp[w.wid, i]
+                assert np.array_equal(_bits(tp.k_pool[page]), w.K[:, :, 16 * i:16 * i + 16]), \
+                    f"K pages of window {w.wid} ({w.tier})"
+                assert np.array_equal(_bits(tp.v_pool[page]), w.V[:, :, 16 * i:16 * i + 16])
+        if w.tier == "Q":
+            for l in range(P.n_layers):
+                for g in range(P.n_kv_heads):
+                    kq, ks, kz, vq, vs, vz = decode_ledger(led[w.wid, l, g])
+                    L = w.ledger
+                    assert np.array_equal(kq, L["kq"][l, g]), f"key codes of window {w.wid}"
+                    assert np.array_equal(ks.view(np.uint16), L["ks"][l, g].view(np.uint16))
+                    assert np.array_equal(kz.view(np.uint16), L["kz"][l, g].view(np.uint16))
+                    assert np.array_equal(vq, L["vq"][l, g]), f"value codes of window {w.wid}"
+                    assert np.array_equal(vs.view(np.uint16), L["vs"][l, g].view(np.uint16))
+                    assert np.array_equal(vz.view(np.uint16), L["vz"][l, g].view(np.uint16))
+            stats["ledgers"] += 1
+
+
+def run_tiers(wl, k_full, k_quant, omega, steps, alpha=0.05, pps_slack=24):
+    g = wl.geom
+    L0 = wl.L0
+    max_ctx = L0 + steps + 8
+    pps = 1 + -(-(L0 - 5) // 16) + pps_slack
+    tp = kvev.TierEvictionPass(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, g.batch,
+                               max_ctx, pps, k_full, k_quant, omega, alpha)
+    K, V = wl.prefill()
+    load(tp, K, V, L0)
+    tp.begin(L0)
+    P = QE.QParams(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, k_full, k_quant,
+                   alpha=alpha, omega=omega)
+    seqs = [QE.QSequence.from_prefill(P, K[:, b], V[:, b]) for b in range(g.batch)]
+    stats = {"swaps": 0, "out_rel": 0.0, "m_abs": 0.0, "ledgers": 0, "promoted": 0,
+             "redemoted": 0}
+    for t in range(1, steps + 1):
+        q, kn, vn = wl.step_inputs(t)
+        tp.step(to_dev_bf16(q), to_dev_bf16(kn), to_dev_bf16(vn))
+        kvev.kvev_sync(tp.ctx)
+        for b in range(g.batch):
+            compare(tp, P, seqs, b, t, q[b], kn[b], vn[b], stats)
+    tp.close()
+    return stats
+
+
+def test_tiers_small_routing_promotion_and_new_window():
+    """2 layers of the Llama-8B geometry, 2 sequences of 1325 tokens (10
+    windows + a 40-token tail), K_f 2, K_q 3, routing every 4 steps, 100
+    steps: windows get quantized, promoted back, re-demoted (ledger reuse),
+    evicted, and one new window forms from decoded tokens."""
+    wl = Workload(Geometry(2, 32, 8, 128, 2), 5 + 128 * 10 + 40, seed=7, outliers=4, needle=16,
+                  needle_period=16)
+    st = run_tiers(wl, 2, 3, 4, 100)
+    print("tiers:", st)
+    assert st["ledgers"] > 0 and st["promoted"] > 0 and st["redemoted"] > 0
+
+
+def test_tiers_no_quantized_tier_and_large_capacity():
+    """K_q = 0 (two tiers: Full or evicted) and K_f covering every window."""
+    wl = Workload(Geometry(2, 32, 8, 128, 1), 5 + 128 * 6 + 3, seed=8, needle=16, needle_period=8)
+    run_tiers(wl, 2, 0, 2, 20)
+    run_tiers(wl, 6, 0, 3, 12)
