@@ -55,6 +55,11 @@ MEMDECAY = dict(workload="region-aware (MemDecay) page eviction, 32 x 16384 toke
                 page=16, budget_tokens=4915, regions="system 5% (pinned), plan 5%, user 10%, "
                 "tool 30%, retrieved 30%, scratchpad 20%; half-lives 160/80/60/30/40/15 steps",
                 rho=0.9, attn_weight=0.5, tau="2/|K_t|", refresh="full (observation every step)")
+TIERS = dict(workload="two-tier (QEvict) windows, 4 x 131072 tokens, 5% bf16 + 20% INT2",
+             n_layers=32, n_q_heads=32, n_kv_heads=8, head_dim=128, batch=4, prefill=131072,
+             window=128, sinks=5, recent=32, k_full=51, k_quant=204, omega=8, alpha=0.05,
+             int2="keys per channel / values per token, groups of 32, fp16 scale and zero",
+             needle="16 positions re-drawn every 64 steps")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -228,7 +233,7 @@ def main():
                     help="smaller cases for profiling; the headline uses 32")
     ap.add_argument("--prefill", type=int, default=WORKLOAD["prefill"])
     ap.add_argument("--workload", default="llama8b-32k",
-                    choices=["llama8b-32k", "paged", "memdecay"],
+                    choices=["llama8b-32k", "paged", "memdecay", "tiers"],
                     help="the headline token-granular step, or the block-granular run")
     ap.add_argument("--batch", type=int, default=PAGED["batch"],
                     help="paged workload: sequences (profiling cases only)")
@@ -245,6 +250,9 @@ def main():
 
     if args.workload in ("paged", "memdecay"):
         bench_paged(args, rank, world, local_rank)
+        return
+    if args.workload == "tiers":
+        bench_tiers(args, rank, world, local_rank)
         return
 
     import torch
@@ -640,6 +648,171 @@ def bench_paged(args, rank, world, local_rank):
         }
         print(json.dumps(line), flush=True)
     pp.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def bench_tiers(args, rank, world, local_rank):
+    """Two-tier run: 4 sequences of 131072 tokens in 128-token windows, K_f
+    51 bf16 windows, K_q 204 INT2 windows, routing every 8 steps.  Timed: K
+    consecutive decode steps from step 1 of a fresh run (steps 1-7 attend the
+    whole prefill, the first routing event quantizes 204 windows per
+    sequence, later steps attend ~6.6k bf16 and ~26k INT2 tokens per
+    sequence); the steady state (steps after the first event) is reported
+    beside it."""
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from decoding_kv_cache_split_gb300 import build as kbuild
+    if not os.path.exists(kbuild.LIB):
+        kbuild.build()
+    from decoding_kv_cache_split_gb300 import kvev
+    from workloads.device import TierDeviceWorkload
+
+    W = dict(TIERS)
+    if args.layers != WORKLOAD["n_layers"] or args.prefill != WORKLOAD["prefill"]:
+        pre = args.prefill if args.prefill != WORKLOAD["prefill"] else W["prefill"]
+        W.update(workload=f"profiling case: {args.layers} layers, {W['batch']} x {pre} tokens",
+                 n_layers=args.layers, prefill=pre)
+    Ly, b, L0 = W["n_layers"], W["batch"], W["prefill"]
+    n_steps = args.steps
+    max_ctx = L0 + max(n_steps, args.warmup) + 16
+    wl = TierDeviceWorkload(0, n_layers=Ly, batch=b, prefill=L0)
+    pps = wl.n_pages + 16 + 8 * W["k_full"]
+    tp = kvev.TierEvictionPass(Ly, W["n_q_heads"], W["n_kv_heads"], W["head_dim"], b, max_ctx,
+                               pps, W["k_full"], W["k_quant"], W["omega"], W["alpha"])
+    wl.fill(torch, tp.k_pool, tp.v_pool, pps)
+    last = max(n_steps, args.warmup)
+    inputs = [wl.step_inputs(torch, t, tp.k_pool, pps) for t in range(1, last + 1)]
+    # the prefill pages are reused once windows are routed: keep a copy to restart from
+    k0, v0 = tp.k_pool.clone(), tp.v_pool.clone()
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def restart():
+        tp.k_pool.copy_(k0)
+        tp.v_pool.copy_(v0)
+        tp.begin(L0, stream)
+
+    restart()
+    for t in range(1, args.warmup + 1):
+        tp.step(*inputs[t - 1], stream)
+    kvev.kvev_sync(tp.ctx)
+
+    # timed: steps 1..K of a fresh run, with an event after the first routing event
+    restart()
+    torch.cuda.synchronize()
+    n0 = kvev.kvev_launch_count(tp.ctx)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps + 1)]
+    evs[0].record(stream)
+    for t in range(1, n_steps + 1):
+        tp.step(*inputs[t - 1], stream)
+        evs[t].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    kvev.kvev_sync(tp.ctx)
+    launches = kvev.kvev_launch_count(tp.ctx) - n0
+    step_ms = [evs[t - 1].elapsed_time(evs[t]) for t in range(1, n_steps + 1)]
+    ms = sum(step_ms) / n_steps
+    if dist:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # replay with per-kernel events, counting what each step attends
+    row_bf16 = 2 * W["head_dim"] * 2 * W["n_kv_heads"] * Ly       # bytes per token, all layers
+    row_int2 = 768 * W["n_kv_heads"] // 8 * Ly
+    kvev.kvev_profile(tp.ctx, True)
+    restart()
+    kvev.kvev_profile_read(tp.ctx)
+    per_step = []
+    for t in range(1, n_steps + 1):
+        tiers = tp.tier.cpu().numpy()
+        tl = tp.tail_len.cpu().numpy()
+        bf = sum(int(((tiers[s_] == kvev.KVEV_TIER_UNROUTED) | (tiers[s_] == kvev.KVEV_TIER_FULL)).sum())
+                 * 128 for s_ in range(b))
+        qn = int((tiers == kvev.KVEV_TIER_QUANT).sum()) * 128
+        tok_bf = bf + b * (5 + int(tl.max()) + 1)      # + sinks and tail (with the new token)
+        per_step.append((tok_bf, qn))
+        tp.step(*inputs[t - 1], stream)
+        kvev.kvev_sync(tp.ctx)
+    prof = kvev.kvev_profile_read(tp.ctx)
+    kvev.kvev_profile(tp.ctx, False)
+    bytes_step = [tb * row_bf16 + tq * row_int2 for tb, tq in per_step]
+    total_bytes = sum(bytes_step)
+    value = world * total_bytes / (sum(step_ms) * 1e-3) / 1e9
+    first = W["omega"]                     # steps after the first routing event
+    steady_ms = sum(step_ms[first:]) / max(1, n_steps - first)
+    steady_bytes = sum(bytes_step[first:]) / max(1, n_steps - first)
+    att_ms = prof.get("attention", (0.0, 0))[0]
+    attn_achieved = total_bytes / (att_ms * 1e-3) / 1e9 if att_ms > 0 else None
+    kernels_us = {k: round(v[0] / n_steps * 1e3, 2) for k, v in prof.items()}
+    kernels_us["launches_per_step"] = {k: round(v[1] / n_steps, 2) for k, v in prof.items()}
+
+    # end to end: pinned host q/k/v in, the output back, every step
+    n_e2e = min(n_steps, 64)
+    host_in = [tuple(x.view(torch.int16).cpu().pin_memory() for x in inputs[t - 1])
+               for t in range(1, n_e2e + 1)]
+    dev_in = [torch.empty_like(x) for x in inputs[0]]
+    out_h = torch.empty(tp.out.shape, dtype=torch.float32).pin_memory()
+    tier_h = torch.empty(tp.tier.shape, dtype=torch.uint8).pin_memory()
+    h2d = sum(x.numel() * 2 for x in host_in[0])
+    d2h = out_h.numel() * 4 + tier_h.numel()
+    restart()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        for d_, h_ in zip(dev_in, host_in[i]):
+            d_.view(torch.int16).copy_(h_, non_blocking=True)
+        tp.step(*dev_in, stream)
+        out_h.copy_(tp.out, non_blocking=True)
+        tier_h.copy_(tp.tier, non_blocking=True)
+        stream.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+    kvev.kvev_sync(tp.ctx)
+    e2e_val = world * (sum(bytes_step[:n_e2e]) / n_e2e) / (e2e_ms * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peak()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": n_steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "us_per_step": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 + int2", "data": "synthetic (device Philox)",
+            "config": dict(W, parallelism=f"replicas{world}", timed="decode steps 1..K",
+                           l2="inputs larger than L2 (>= 5 GB of K/V per step)"),
+            "frac_of_peak": {"measured": round(value / world / peak, 4),
+                             "nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+                             "peak_kind": peak_kind},
+            "steady": {"us": round(steady_ms * 1e3, 2), "bytes": int(steady_bytes),
+                       "GB/s": round(steady_bytes / (steady_ms * 1e-3) / 1e9, 2)},
+            "first_steps_us": [round(x * 1e3, 1) for x in step_ms[:first + 1]],
+            "roofline": {"bound": "hbm", "kernel": "attention (bf16 pages + INT2 windows)",
+                         "achieved": round(attn_achieved, 2) if attn_achieved else None,
+                         "peak": peak, "unit": "GB/s",
+                         "frac": round(attn_achieved / peak, 4) if attn_achieved else None,
+                         "traffic": None, "algorithmic_bytes": int(total_bytes / n_steps),
+                         "peak_kind": f"{peak_kind} (copy bandwidth)"},
+            "kernels_us": kernels_us,
+            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "cpu_baseline": None,
+        }
+        print(json.dumps(line), flush=True)
+    tp.close()
     if dist:
         dist.destroy_process_group()
 

@@ -115,7 +115,8 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
     const size_t G = (size_t)(L.n_q_heads / L.n_kv_heads);
     const size_t ctx = (size_t)L.batch * L.max_ctx;
     const size_t nblk = (size_t)((L.max_ctx + kScoreThreads - 1) / kScoreThreads);
-    w.logits = (float*)take(rows * (size_t)logit_ld(L.max_ctx) * G * 4);
+    // two-tier mode scores windows from per-tile statistics: no logits
+    if (L.page_tokens != kTierW) w.logits = (float*)take(rows * (size_t)logit_ld(L.max_ctx) * G * 4);
     w.part_o = (float*)take((size_t)slots * G * L.head_dim * 4);
     w.part_ml = (float*)take((size_t)slots * G * 2 * 4);
     w.lse2 = (float*)take(rows * G * 4);

@@ -129,13 +129,17 @@ def quantize_window(K_bits, V_bits, group: int = 32):
                 vq=vq.reshape(Ly, Hkv, W, d), vs=vs, vz=vz, group=group)
 
 
-def dequantize_window(led):
-    """fp32 (K, V) [Ly][Hkv][W][d] of a ledger entry."""
+def dequantize_window(led, layer=None):
+    """fp32 (K, V) [Ly][Hkv][W][d] of a ledger entry ([Hkv][W][d] of one
+    layer when `layer` is given)."""
     g = led["group"]
-    Ly, Hkv, W, d = led["kq"].shape
-    k = dequantize(led["kq"].reshape(Ly, Hkv, W // g, g, d), led["ks"], led["kz"], axis=3)
-    v = dequantize(led["vq"].reshape(Ly, Hkv, W, d // g, g), led["vs"], led["vz"], axis=4)
-    return k.reshape(Ly, Hkv, W, d), v.reshape(Ly, Hkv, W, d)
+    sel = slice(None) if layer is None else slice(layer, layer + 1)
+    kq, vq = led["kq"][sel], led["vq"][sel]
+    Ly, Hkv, W, d = kq.shape
+    k = dequantize(kq.reshape(Ly, Hkv, W // g, g, d), led["ks"][sel], led["kz"][sel], axis=3)
+    v = dequantize(vq.reshape(Ly, Hkv, W, d // g, g), led["vs"][sel], led["vz"][sel], axis=4)
+    k, v = k.reshape(Ly, Hkv, W, d), v.reshape(Ly, Hkv, W, d)
+    return (k, v) if layer is None else (k[0], v[0])
 
 
 # ------------------------------------------------------------------ state
@@ -177,26 +181,26 @@ class QSequence:
         return [w.tier for w in self.windows]
 
 
-def accessible(P: QParams, seq: QSequence):
-    """fp32 (K, V) [Ly][Hkv][n][d] of every accessible token in position
-    order, and the window index of each (-1: sink or tail)."""
-    ks, vs, owner = [_bits_to_f32(seq.K_sink)], [_bits_to_f32(seq.V_sink)], [
+def accessible(P: QParams, seq: QSequence, layer: int):
+    """fp32 (K, V) [Hkv][n][d] of every accessible token of one layer in
+    position order, and the window index of each (-1: sink or tail)."""
+    ks, vs, owner = [_bits_to_f32(seq.K_sink[layer])], [_bits_to_f32(seq.V_sink[layer])], [
         np.full(P.n_sink, -1)]
     for j, w in enumerate(seq.windows):
         if w.tier in (UNROUTED, FULL):
-            ks.append(_bits_to_f32(w.K))
-            vs.append(_bits_to_f32(w.V))
+            ks.append(_bits_to_f32(w.K[layer]))
+            vs.append(_bits_to_f32(w.V[layer]))
         elif w.tier == QUANT:
-            k, v = dequantize_window(w.ledger)
+            k, v = dequantize_window(w.ledger, layer)
             ks.append(k)
             vs.append(v)
         else:
             continue
         owner.append(np.full(P.window, j))
-    ks.append(_bits_to_f32(seq.K_tail))
-    vs.append(_bits_to_f32(seq.V_tail))
+    ks.append(_bits_to_f32(seq.K_tail[layer]))
+    vs.append(_bits_to_f32(seq.V_tail[layer]))
     owner.append(np.full(seq.K_tail.shape[2], -1))
-    return np.concatenate(ks, axis=2), np.concatenate(vs, axis=2), np.concatenate(owner)
+    return np.concatenate(ks, axis=1), np.concatenate(vs, axis=1), np.concatenate(owner)
 
 
 def attention_f64(q, K, V):
@@ -204,14 +208,16 @@ def attention_f64(q, K, V):
     q [Hq][d] fp32, K/V [Hkv][n][d] -> (p [Hq][n], out [Hq][d])."""
     Hq, d = q.shape
     Hkv = K.shape[0]
+    G = Hq // Hkv                                # query heads h of KV head h // G
     p = np.zeros((Hq, K.shape[1]))
     out = np.zeros((Hq, d))
-    for h in range(Hq):
-        g = h * Hkv // Hq
-        lg = K[g].astype(np.float64) @ q[h].astype(np.float64) / np.sqrt(d)
-        e = np.exp(lg - lg.max())
-        p[h] = e / e.sum()
-        out[h] = p[h] @ V[g].astype(np.float64)
+    for g in range(Hkv):
+        k64, v64 = K[g].astype(np.float64), V[g].astype(np.float64)
+        heads = slice(g * G, (g + 1) * G)
+        lg = (k64 @ q[heads].astype(np.float64).T).T / np.sqrt(d)     # [G][n]
+        e = np.exp(lg - lg.max(axis=1, keepdims=True))
+        p[heads] = e / e.sum(axis=1, keepdims=True)
+        out[heads] = p[heads] @ v64
     return p, out
 
 
@@ -253,20 +259,23 @@ def step(P: QParams, seq: QSequence, t: int, q_bits, knew_bits, vnew_bits,
         seq.windows.append(QWindow(len(seq.windows), UNROUTED, 0.0, seq.K_tail, seq.V_tail))
         seq.K_tail = seq.K_tail[:, :, :0].copy()
         seq.V_tail = seq.V_tail[:, :, :0].copy()
-    K, V, owner = accessible(P, seq)
     q = _bits_to_f32(q_bits)
     out = np.zeros((Ly, Hq, d))
-    probs = np.zeros((Ly, Hq, K.shape[2])) if want_probs else None
+    probs = None
     live = [j for j, w in enumerate(seq.windows) if w.tier != EVICTED]
     m = np.array([seq.windows[j].m for j in live])
     s_layers = np.zeros((Ly, len(live)))
     for layer in range(Ly):
-        p, o = attention_f64(q[layer], K[layer], V[layer])
+        K, V, owner = accessible(P, seq, layer)
+        p, o = attention_f64(q[layer], K, V)
         out[layer] = o
         if want_probs:
+            probs = np.zeros((Ly, Hq, K.shape[1])) if probs is None else probs
             probs[layer] = p
         tok = p.sum(axis=0) / Hq                 # head-averaged attention per token
-        s = np.array([tok[owner == j].sum() for j in live])
+        inw = owner >= 0                         # window sums: a library bin-count
+        per_window = np.bincount(owner[inw], weights=tok[inw], minlength=len(seq.windows))
+        s = per_window[live]
         s_layers[layer] = s
         m = P.alpha * s + (1.0 - P.alpha) * m
     for k, j in enumerate(live):

@@ -81,7 +81,9 @@ def admissible(m: dict, dev_tiers: dict, tol: float):
                 assert m[a] >= m[b] - tol, f"window {a} ({ta}) below {b} ({tb})"
 
 
-def compare(tp, P, seqs, b, t, q, kn, vn, stats):
+def compare(tp, P, seqs, b, t, q, kn, vn, stats, check_windows=None):
+    """check_windows: ids whose pages / ledger entries are compared (all when
+    None)."""
     pre = copy.deepcopy(seqs[b])
     res = QE.step(P, seqs[b], t, q, kn, vn)
     seq = seqs[b]
@@ -111,8 +113,9 @@ def compare(tp, P, seqs, b, t, q, kn, vn, stats):
     assert int(tp.n_windows[b]) == len(seq.windows)
     assert int(tp.tail_len[b]) == seq.K_tail.shape[2]
     wp = tp.win_pages[b].cpu().numpy()
-    led = tp.ledger[b].cpu().numpy()
     for w in seq.windows:
+        if check_windows is not None and w.wid not in check_windows:
+            continue
         if w.tier in ("U", "F"):
             for i in range(8):
                 page = wp[w.wid, i]
@@ -122,7 +125,7 @@ def compare(tp, P, seqs, b, t, q, kn, vn, stats):
         if w.tier == "Q":
             for l in range(P.n_layers):
                 for g in range(P.n_kv_heads):
-                    kq, ks, kz, vq, vs, vz = decode_ledger(led[w.wid, l, g])
+                    kq, ks, kz, vq, vs, vz = decode_ledger(tp.ledger[b, w.wid, l, g].cpu().numpy())
                     L = w.ledger
                     assert np.array_equal(kq, L["kq"][l, g]), f"key codes of window {w.wid}"
                     assert np.array_equal(ks.view(np.uint16), L["ks"][l, g].view(np.uint16))
@@ -175,3 +178,39 @@ def test_tiers_no_quantized_tier_and_large_capacity():
     wl = Workload(Geometry(2, 32, 8, 128, 1), 5 + 128 * 6 + 3, seed=8, needle=16, needle_period=8)
     run_tiers(wl, 2, 0, 2, 20)
     run_tiers(wl, 6, 0, 3, 12)
+
+
+@pytest.mark.slow
+def test_tiers_full_size_first_routing_event():
+    """The full two-tier workload on the device: 32 layers, 4 sequences of
+    131072 tokens (1023 windows), K_f 51, K_q 204, routing every 8 steps;
+    steps 1-9 of sequence 0 against the oracle (the first routing event
+    quantizes 204 windows; step 9 attends the mixed cache)."""
+    from workloads.device import TierDeviceWorkload
+    L0, batch, Ly = 131072, 4, 32
+    wl = TierDeviceWorkload(0, n_layers=Ly, batch=batch, prefill=L0)
+    pps = wl.n_pages + 16 + 8 * 51
+    tp = kvev.TierEvictionPass(Ly, 32, 8, 128, batch, L0 + 32, pps, 51, 204, 8, 0.05)
+    wl.fill(torch, tp.k_pool, tp.v_pool, pps)
+    inputs = [wl.step_inputs(torch, t, tp.k_pool, pps) for t in range(1, 10)]
+    # sequence 0's prefill in token order, from the windowed pages
+    hist = L0 - 5
+    pages = slice(0, wl.n_pages)
+    kp, vp = _bits(tp.k_pool[pages]), _bits(tp.v_pool[pages])
+    def tokens(p):
+        rest = p[1:].transpose(1, 2, 0, 3, 4).reshape(Ly, 8, -1, 128)[:, :, :hist]
+        return np.concatenate([p[0, :, :, :5], rest], axis=2)
+    P = QE.QParams(Ly, 32, 8, 128, 51, 204, alpha=0.05, omega=8)
+    seqs = [QE.QSequence.from_prefill(P, tokens(kp), tokens(vp))]
+    del kp, vp
+    tp.begin(L0)
+    stats = {"swaps": 0, "out_rel": 0.0, "m_abs": 0.0, "ledgers": 0, "promoted": 0,
+             "redemoted": 0}
+    for t in range(1, 10):
+        q, kn, vn = inputs[t - 1]
+        tp.step(q, kn, vn)
+        kvev.kvev_sync(tp.ctx)
+        compare(tp, P, seqs, 0, t, _bits(q[0]), _bits(kn[0]), _bits(vn[0]), stats,
+                check_windows=set(range(0, 1023, 61)))
+    print("tiers full size:", stats)
+    tp.close()
