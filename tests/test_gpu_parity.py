@@ -1,8 +1,10 @@
 """GPU parity of the eviction pass against the fp64 oracle.
 
-Every test runs the CUDA path through the C ABI (Python binding) and, at
-each step, the oracle from the device's own pre-step state (teacher
-forcing), and compares element by element (tolerances in tests/parity.py).
+Every test runs the CUDA path through the C ABI (Python binding) and the
+oracle from the same seeded prefill and inputs, free-running (it never
+reads the device's state), and compares every step element by element
+(tolerances in tests/parity.py); at a validated near tie the oracle follows
+the device's admissible choice.
 """
 import math
 
@@ -12,7 +14,7 @@ import pytest
 import oracle as O
 from workloads import Geometry, Workload, llama8b_workload, tiny_workload
 
-from parity import (access_alternative, compare_step, load_prefill, oracle_step, snapshot,
+from parity import (access_alternative, compare_step, follow, load_prefill, oracle_step,
                     to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
@@ -48,26 +50,47 @@ def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int,
     kvev.kvev_set_debug(ep.ctx, probs, prio)
     P = O.OracleParams(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, budget, alpha, beta,
                        age_mode, pool_mean)
-    totals = {"swaps": 0, "out_rel": 0.0, "m_abs": 0.0, "p_rel": 0.0, "steps": 0}
+    K, V = wl.prefill()
+    states = [O.SequenceState.from_prefill(K[:, b], V[:, b], wl.L0, max_ctx)
+              for b in range(g.batch)]
+    del K, V
+    totals = {"swaps": 0, "followed": 0, "out_rel": 0.0, "m_abs": 0.0, "p_rel": 0.0,
+              "steps": 0}
     for t in range(1, steps + 1):
         L_prev = ep.length()
         check = (t - 1) % check_every == 0 or t == steps
-        pres = [snapshot(ep, b, L_prev) for b in range(g.batch)] if check else None
         q, kn, vn = wl.step_inputs(t)
         ep.step(to_dev_bf16(q), to_dev_bf16(kn), to_dev_bf16(vn))
         kvev.kvev_sync(ep.ctx)
-        if not check:
-            continue
         refresh_now = O.is_refresh(mode_o, period, t)
         for b in range(g.batch):
-            res, _ = oracle_step(P, pres[b], t, refresh_now, q[b], kn[b], vn[b], wl.L0 + t - 1)
-            alt, amb = access_alternative(res, pres[b], P) if refresh_now else (None, None)
-            st = compare_step(res, ep, b, pres[b], budget, probs, prio, refresh_now, alt,
-                              access_amb=amb)
-            totals["swaps"] += st["swaps"]
-            for k in ("out_rel", "m_abs", "p_rel"):
-                totals[k] = max(totals[k], st.get(k, 0.0))
-            totals["steps"] += 1
+            pre = states[b]
+            assert pre.L == L_prev, "oracle and device cache lengths"
+            res, new = oracle_step(P, pre, t, refresh_now, q[b], kn[b], vn[b], wl.L0 + t - 1,
+                                   want_probs=check)
+            alt, amb = access_alternative(res, pre, P) if refresh_now else (None, None)
+            if check:
+                st = compare_step(res, ep, b, pre, budget, probs, prio, refresh_now, alt,
+                                  access_amb=amb)
+                totals["swaps"] += st["swaps"]
+                for k in ("out_rel", "m_abs", "p_rel"):
+                    totals[k] = max(totals[k], st.get(k, 0.0))
+                totals["steps"] += 1
+            # continue the oracle along the device's choice where it was admissible
+            n = int(ep.n_retained[b].item())
+            kept = ep.retained[b, :n].cpu().numpy().astype(np.int64)
+            t_ref_kept = res["t_ref_upd"][kept]
+            if amb is not None and amb[kept].any():
+                dev = ep.t_ref[b, :n].cpu().numpy().astype(np.int64)
+                t_ref_kept = np.where(amb[kept], dev, t_ref_kept)
+            if not np.array_equal(kept, res["retained"]) or \
+                    not np.array_equal(t_ref_kept, res["t_ref_upd"][kept]):
+                if not check:   # the choice is still checked for admissibility
+                    compare_step(res, ep, b, pre, budget, None, prio, refresh_now, alt,
+                                 access_amb=amb)
+                new = follow(res, pre, kept, t_ref_kept)
+                totals["followed"] += 1
+            states[b] = new
         assert ep.length() == min(L_prev + 1, budget)
     ep.close()
     return totals
