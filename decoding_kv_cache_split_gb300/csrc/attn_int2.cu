@@ -51,12 +51,16 @@ __device__ __forceinline__ uint32_t codes_bf16x2(uint32_t x) {
     asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(0x43004300u));
     return r;
 }
-__device__ __forceinline__ float half_at(const unsigned char* base, int idx) {
-    return __half2float(reinterpret_cast<const __half*>(base)[idx]);
-}
 
+// The 16 x 8 x 16 tensor-core tile has 8 A rows and a group has 4 query
+// heads, so rows 0-3 carry the bf16 "hi" part of each head's operand and
+// rows 4-7 the "lo" part (operand - hi): one MMA per operand pair instead of
+// two, the halves summed with one shuffle (lane g and lane g + 4, i.e. xor
+// 16) where the full value is needed.  Lanes g and g + 4 therefore hold the
+// same head (g & 3) and run identical softmax bookkeeping.
 template <int D, int G>
 __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args a) {
+    static_assert(G == 4, "hi / lo rows need 4 query heads per KV head");
     using Lay = LedgerLayout<D>;
     constexpr int KS = D / 16, NB = D / 8, NG = D / kQGroup;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -69,8 +73,9 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
     const int64_t x0 = (int64_t)w * N / a.total_warps, x1 = (int64_t)(w + 1) * N / a.total_warps;
     if (x0 >= x1) return;
 
-    const int g = lane >> 2, t = lane & 3;   // fragment row (query head), column pair
-    const bool real = g < G;
+    const int g = lane >> 2, t = lane & 3;   // fragment row, column pair
+    const int head = g & 3;                  // query head of the group
+    const bool lo_row = g >= 4;              // this row carries the "lo" parts
     // window id of unit x (-1: empty), and its ledger entry
     auto unit_window = [&](int64_t x, const unsigned char** src) -> int {
         const int64_t row = x / a.slots;
@@ -92,10 +97,15 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
         }
         cp_async_commit();
     };
+    // the lane's half (hi or lo) of a product pair
+    auto half_pair = [&](float x0v, float x1v) -> uint32_t {
+        const uint32_t hi = pack_bf16x2(x0v, x1v);
+        return lo_row ? pack_bf16x2(x0v - bf16_lo(hi), x1v - bf16_hi(hi)) : hi;
+    };
 
-    uint32_t qa0[KS], qa2[KS];               // Q fragments (bf16x2) of head g
-    float o[NB][2];
-    float vbias[NG];                         // sum_i p_i z_ig of head g, per channel group
+    uint32_t qa0[KS], qa2[KS];               // Q (bf16x2) of the lane's head
+    float o[NB][2];                          // hi or lo part of O[head][8j + 2t, +1]
+    float vbias[NG];                         // sum_i p_i z_ig of the head, per channel group
     float m_run = -INFINITY, l_run = 0.f;
     int64_t cur_row = -1;
 
@@ -104,17 +114,19 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
         l += __shfl_xor_sync(kFull, l, 1);
         l += __shfl_xor_sync(kFull, l, 2);
         const int64_t slot = (int64_t)w + row;
-        if (real) {
-            float* po = a.part_o + ((size_t)slot * G + g) * D;
+        float* po = a.part_o + ((size_t)slot * G + head) * D;
 #pragma unroll
-            for (int j = 0; j < NB; ++j)
+        for (int j = 0; j < NB; ++j) {
+            const float v0 = o[j][0] + __shfl_xor_sync(kFull, o[j][0], 16);
+            const float v1 = o[j][1] + __shfl_xor_sync(kFull, o[j][1], 16);
+            if (!lo_row)
                 *reinterpret_cast<float2*>(po + 8 * j + 2 * t) =
-                    make_float2(o[j][0] + vbias[j / 4], o[j][1] + vbias[j / 4]);
-            if (t == 0) {
-                float* pml = a.part_ml + ((size_t)slot * G + g) * 2;
-                pml[0] = m_run;
-                pml[1] = l;
-            }
+                    make_float2(v0 + vbias[j / 4], v1 + vbias[j / 4]);
+        }
+        if (!lo_row && t == 0) {
+            float* pml = a.part_ml + ((size_t)slot * G + head) * 2;
+            pml[0] = m_run;
+            pml[1] = l;
         }
     };
 
@@ -133,11 +145,11 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
             const int64_t lb = row / a.n_kv;
             const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
             const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-                a.q + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)gk * G + (real ? g : 0)) * D);
+                a.q + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)gk * G + head) * D);
 #pragma unroll
             for (int s = 0; s < KS; ++s) {
-                qa0[s] = real ? qrow[8 * s + t] : 0u;       // dims 16s + 2t, +1
-                qa2[s] = real ? qrow[8 * s + 4 + t] : 0u;   // dims 16s + 8 + 2t, +1
+                qa0[s] = qrow[8 * s + t];       // dims 16s + 2t, +1
+                qa2[s] = qrow[8 * s + 4 + t];   // dims 16s + 8 + 2t, +1
             }
 #pragma unroll
             for (int j = 0; j < NB; ++j) o[j][0] = o[j][1] = 0.f;
@@ -152,29 +164,30 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
             const unsigned char* buf = wbuf + (size_t)bi * Lay::BYTES;
             const uint32_t* kc = reinterpret_cast<const uint32_t*>(buf + Lay::KC);
             const uint32_t* vc = reinterpret_cast<const uint32_t*>(buf + Lay::VC);
+            const __half2* ks2 = reinterpret_cast<const __half2*>(buf + Lay::KS);
+            const __half2* kz2 = reinterpret_cast<const __half2*>(buf + Lay::KZ);
+            const uint2* vs4 = reinterpret_cast<const uint2*>(buf + Lay::VS);   // 4 fp16 per token
+            const uint2* vz4 = reinterpret_cast<const uint2*>(buf + Lay::VZ);
             for (int grp = 0; grp < kTierW / kQGroup; ++grp) {
-                // A' = q * s (hi + lo) for this group's key scales, and the key bias
-                uint32_t ahi[KS][2], alo[KS][2];
+                // A' = q * s of this group's key scales (the lane's hi or lo part),
+                // and the key bias sum_c q_c z_c
+                uint32_t af[KS][2];
                 float kb = 0.f;
 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
                     const int c0 = 16 * s + 2 * t, c2 = c0 + 8;
+                    const float2 s01 = __half22float2(ks2[(grp * D + c0) / 2]);
+                    const float2 s23 = __half22float2(ks2[(grp * D + c2) / 2]);
+                    const float2 z01 = __half22float2(kz2[(grp * D + c0) / 2]);
+                    const float2 z23 = __half22float2(kz2[(grp * D + c2) / 2]);
                     const float q0 = bf16_lo(qa0[s]), q1 = bf16_hi(qa0[s]);
                     const float q2 = bf16_lo(qa2[s]), q3 = bf16_hi(qa2[s]);
-                    const unsigned char* ks = buf + Lay::KS;
-                    const unsigned char* kz = buf + Lay::KZ;
-                    const float p0 = q0 * half_at(ks, grp * D + c0);
-                    const float p1 = q1 * half_at(ks, grp * D + c0 + 1);
-                    const float p2 = q2 * half_at(ks, grp * D + c2);
-                    const float p3 = q3 * half_at(ks, grp * D + c2 + 1);
-                    kb = fmaf(q0, half_at(kz, grp * D + c0), kb);
-                    kb = fmaf(q1, half_at(kz, grp * D + c0 + 1), kb);
-                    kb = fmaf(q2, half_at(kz, grp * D + c2), kb);
-                    kb = fmaf(q3, half_at(kz, grp * D + c2 + 1), kb);
-                    ahi[s][0] = pack_bf16x2(p0, p1);
-                    ahi[s][1] = pack_bf16x2(p2, p3);
-                    alo[s][0] = pack_bf16x2(p0 - bf16_lo(ahi[s][0]), p1 - bf16_hi(ahi[s][0]));
-                    alo[s][1] = pack_bf16x2(p2 - bf16_lo(ahi[s][1]), p3 - bf16_hi(ahi[s][1]));
+                    af[s][0] = half_pair(q0 * s01.x, q1 * s01.y);
+                    af[s][1] = half_pair(q2 * s23.x, q3 * s23.y);
+                    kb = fmaf(q0, z01.x, kb);
+                    kb = fmaf(q1, z01.y, kb);
+                    kb = fmaf(q2, z23.x, kb);
+                    kb = fmaf(q3, z23.y, kb);
                 }
                 kb += __shfl_xor_sync(kFull, kb, 1);
                 kb += __shfl_xor_sync(kFull, kb, 2);
@@ -182,8 +195,9 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                 for (int tt = 0; tt < kQGroup / kTile; ++tt) {
                     const int ti = grp * (kQGroup / kTile) + tt;   // 16-token tile of the window
                     const int tok0 = ti * kTile;
-                    // ---- S = A' codes + bias for the two 8-token blocks
-                    float hi_acc[2][2] = {}, lo_acc[2][2] = {};
+                    // ---- S = A' codes (two 8-token blocks; even and odd k-steps in
+                    //      separate accumulators) + bias
+                    float acc[2][2][2] = {};
 #pragma unroll
                     for (int s = 0; s < KS; ++s)
 #pragma unroll
@@ -191,21 +205,21 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                             const uint32_t y = kc[(tok0 + 8 * i + g) * KS + s] >> (2 * t);
                             const uint32_t b0 = codes_bf16x2(y & 0x00030003u);
                             const uint32_t b1 = codes_bf16x2((y >> 8) & 0x00030003u);
-                            mma_rows8(hi_acc[i][0], hi_acc[i][1], ahi[s][0], ahi[s][1], b0, b1);
-                            mma_rows8(lo_acc[i][0], lo_acc[i][1], alo[s][0], alo[s][1], b0, b1);
+                            mma_rows8(acc[s & 1][i][0], acc[s & 1][i][1], af[s][0], af[s][1], b0, b1);
                         }
                     float sc[2][2];
 #pragma unroll
                     for (int i = 0; i < 2; ++i)
 #pragma unroll
-                        for (int e = 0; e < 2; ++e)
-                            sc[i][e] = real ? (hi_acc[i][e] + lo_acc[i][e] + kb) * a.q_scale
-                                            : -INFINITY;
-                    // ---- online softmax of head g
+                        for (int e = 0; e < 2; ++e) {
+                            const float part = acc[0][i][e] + acc[1][i][e];
+                            sc[i][e] = (part + __shfl_xor_sync(kFull, part, 16) + kb) * a.q_scale;
+                        }
+                    // ---- online softmax of the head
                     float mt = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
                     mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
                     mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
-                    if (real && mt > m_run) {
+                    if (mt > m_run) {
                         const float f = fast_exp2(m_run - mt);
                         m_run = mt;
                         l_run *= f;
@@ -217,49 +231,52 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
 #pragma unroll
                         for (int c = 0; c < NG; ++c) vbias[c] *= f;
                     }
-                    float p[2][2];
+                    float pv[4];
 #pragma unroll
                     for (int i = 0; i < 2; ++i)
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            p[i][e] = real ? fast_exp2(sc[i][e] - m_run) : 0.f;
-                            l_run += p[i][e];
+                            pv[2 * i + e] = fast_exp2(sc[i][e] - m_run);
+                            l_run += pv[2 * i + e];
                         }
-                    if (a.tile_stats) {   // (running max, tile sum) of head g for the window score
-                        float ts = (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+                    if (a.tile_stats) {   // (running max, tile sum) of the head for the window score
+                        float ts = (pv[0] + pv[1]) + (pv[2] + pv[3]);
                         ts += __shfl_xor_sync(kFull, ts, 1);
                         ts += __shfl_xor_sync(kFull, ts, 2);
-                        if (real && t == 0)
+                        if (!lo_row && t == 0)
                             a.tile_stats[((size_t)row * a.stats_tiles + (size_t)wid * (kTierW / kTile) +
-                                          ti) * G + g] = make_float2(m_run, ts);
+                                          ti) * G + head] = make_float2(m_run, ts);
                     }
                     // ---- O += (p * s_v) codes + p * z_v, per 32-channel group
-                    const int tk[4] = {tok0 + 2 * t, tok0 + 2 * t + 1, tok0 + 8 + 2 * t,
-                                       tok0 + 9 + 2 * t};
-                    const float pv[4] = {p[0][0], p[0][1], p[1][0], p[1][1]};
+                    uint2 vsr[4], vzr[4];   // the 4 fp16 scales / zeros of the lane's tokens
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int tk = tok0 + (k >> 1) * 8 + 2 * t + (k & 1);
+                        vsr[k] = vs4[tk];
+                        vzr[k] = vz4[tk];
+                    }
 #pragma unroll
                     for (int cg = 0; cg < NG; ++cg) {
-                        float pp[4], vb = 0.f;
+                        float sv[4], vb = 0.f;
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            pp[k] = pv[k] * half_at(buf + Lay::VS, tk[k] * NG + cg);
-                            vb = fmaf(pv[k], half_at(buf + Lay::VZ, tk[k] * NG + cg), vb);
+                            const uint32_t ws = (cg < 2 ? vsr[k].x : vsr[k].y) >> (16 * (cg & 1));
+                            const uint32_t wz = (cg < 2 ? vzr[k].x : vzr[k].y) >> (16 * (cg & 1));
+                            sv[k] = __half2float(__ushort_as_half((unsigned short)(ws & 0xffffu)));
+                            vb = fmaf(pv[k], __half2float(__ushort_as_half((unsigned short)(wz & 0xffffu))), vb);
                         }
                         vb += __shfl_xor_sync(kFull, vb, 1);
                         vb += __shfl_xor_sync(kFull, vb, 2);
                         vbias[cg] += vb;
-                        const uint32_t ph0 = pack_bf16x2(pp[0], pp[1]);
-                        const uint32_t ph2 = pack_bf16x2(pp[2], pp[3]);
-                        const uint32_t pl0 = pack_bf16x2(pp[0] - bf16_lo(ph0), pp[1] - bf16_hi(ph0));
-                        const uint32_t pl2 = pack_bf16x2(pp[2] - bf16_lo(ph2), pp[3] - bf16_hi(ph2));
+                        const uint32_t pa0 = half_pair(pv[0] * sv[0], pv[1] * sv[1]);
+                        const uint32_t pa2 = half_pair(pv[2] * sv[2], pv[3] * sv[3]);
 #pragma unroll
                         for (int jj = 0; jj < kQGroup / 8; ++jj) {
                             const int j = cg * (kQGroup / 8) + jj;      // 8-channel block
                             const uint32_t y = vc[ti * D + 8 * j + g] >> (2 * t);
                             const uint32_t b0 = codes_bf16x2(y & 0x00030003u);
                             const uint32_t b1 = codes_bf16x2((y >> 8) & 0x00030003u);
-                            mma_rows8(o[j][0], o[j][1], ph0, ph2, b0, b1);
-                            mma_rows8(o[j][0], o[j][1], pl0, pl2, b0, b1);
+                            mma_rows8(o[j][0], o[j][1], pa0, pa2, b0, b1);
                         }
                     }
                 }

@@ -356,131 +356,189 @@ __global__ void __launch_bounds__(kBook) tier_route_kernel(const TierArgs a) {
 }
 
 // Items of the quantize / promote kernels: (sequence, list entry, layer,
-// KV head), grid-stride; a CTA of 128 threads per item.
+// KV head) over the lists' actual lengths, grid-stride.
+__device__ __forceinline__ int64_t item_count(const int32_t* n, int batch, int LG) {
+    int64_t c = 0;
+    for (int b = 0; b < batch; ++b) c += (int64_t)n[b] * LG;
+    return c;
+}
+__device__ __forceinline__ void item_at(const int32_t* n, int batch, int LG, int64_t it, int* b,
+                                        int* e, int* lg) {
+    int bb = 0;
+    while (bb < batch - 1 && it >= (int64_t)n[bb] * LG) it -= (int64_t)n[bb++] * LG;
+    *b = bb;
+    *e = (int)(it / LG);
+    *lg = (int)(it % LG);
+}
+
+// Quantization stages the window's 128 key and value
+// rows of the (layer, KV head) in shared memory with 16-byte loads, then
+// quantizes keys per channel (a thread per channel and group) and values per
+// token (a warp per token and channel group, min / max by shuffles).
+constexpr int kQuantThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(128) tier_quantize_kernel(const TierArgs a, int max_items) {
+__global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const TierArgs a,
+                                                                      int max_items) {
     using Lay = LedgerLayout<D>;
     constexpr int PW = kTierW / kTile;
-    __shared__ uint8_t codes[kTierW][D];
+    extern __shared__ __align__(16) unsigned char qsm[];
+    __nv_bfloat16* kt = reinterpret_cast<__nv_bfloat16*>(qsm);            // [128][D]
+    __nv_bfloat16* vt = kt + kTierW * D;                                   // [128][D]
+    uint8_t* codes = reinterpret_cast<uint8_t*>(vt + kTierW * D);          // [128][D]
     griddep_wait();
     griddep_release();
     const int LG = a.n_layers * a.n_kv, MW = a.c.max_windows;
-    const int64_t total = (int64_t)a.batch * max_items * LG;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t total = item_count(a.n_quant, a.batch, LG);
     for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
-        const int lg = (int)(it % LG);
-        const int e = (int)((it / LG) % max_items), b = (int)(it / ((int64_t)LG * max_items));
-        if (e >= a.n_quant[b]) continue;   // the same for the whole CTA
+        int b, e, lg;
+        item_at(a.n_quant, a.batch, LG, it, &b, &e, &lg);
         const int w = a.quant_list[(size_t)b * MW + e];
         const int l = lg / a.n_kv, g = lg % a.n_kv;
         const int32_t* pages = a.st.win_pages + ((size_t)b * MW + w) * PW;
         unsigned char* led = reinterpret_cast<unsigned char*>(a.c.ledger) +
                              ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES;
-        auto row_of = [&](const void* pool, int tok) {
-            const size_t r = (((size_t)pages[tok / kTile] * a.n_layers + l) * a.n_kv + g) * kTile +
-                             tok % kTile;
-            return reinterpret_cast<const __nv_bfloat16*>(pool) + r * D;
-        };
-        // keys: per channel over 32-token groups (thread = channel)
-        for (int c = threadIdx.x; c < D; c += blockDim.x)
-            for (int grp = 0; grp < kTierW / kQGroup; ++grp) {
-                float mn = INFINITY, mx = -INFINITY;
-                for (int i = 0; i < kQGroup; ++i) {
-                    const float x = __bfloat162float(row_of(a.c.k_pool, grp * kQGroup + i)[c]);
-                    mn = fminf(mn, x);
-                    mx = fmaxf(mx, x);
-                }
-                const __half z16 = __float2half_rn(mn);
-                const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-                const float z = __half2float(z16), s = __half2float(s16);
-                reinterpret_cast<__half*>(led + Lay::KS)[grp * D + c] = s16;
-                reinterpret_cast<__half*>(led + Lay::KZ)[grp * D + c] = z16;
-                for (int i = 0; i < kQGroup; ++i) {
-                    const float x = __bfloat162float(row_of(a.c.k_pool, grp * kQGroup + i)[c]);
-                    const float r = s == 0.f ? 0.f : rintf(__fdiv_rn(__fsub_rn(x, z), s));
-                    codes[grp * kQGroup + i][c] = (uint8_t)fminf(fmaxf(r, 0.f), 3.f);
-                }
-            }
+        // stage: page i holds tokens 16 i .. 16 i + 15 of the window, rows contiguous
+        constexpr int kChunks = kTile * D / 8;   // 16-byte chunks per page row block
+        for (int u = tid; u < 2 * PW * kChunks; u += blockDim.x) {
+            const int kv = u / (PW * kChunks), rest = u % (PW * kChunks);
+            const int pi = rest / kChunks, c = rest % kChunks;
+            const size_t off = ((((size_t)pages[pi] * a.n_layers + l) * a.n_kv + g) * kTile) * D / 8 + c;
+            const uint4 v = reinterpret_cast<const uint4*>(kv ? a.c.v_pool : a.c.k_pool)[off];
+            reinterpret_cast<uint4*>(kv ? vt : kt)[(size_t)pi * kChunks + c] = v;
+        }
         __syncthreads();
-        for (int u = threadIdx.x; u < kTierW * (D / 16); u += blockDim.x) {   // pack kc
+        // keys: per channel over 32-token groups
+        for (int u = tid; u < D * (kTierW / kQGroup); u += blockDim.x) {
+            const int c = u % D, grp = u / D;
+            float mn = INFINITY, mx = -INFINITY;
+            for (int i = 0; i < kQGroup; ++i) {
+                const float x = __bfloat162float(kt[(grp * kQGroup + i) * D + c]);
+                mn = fminf(mn, x);
+                mx = fmaxf(mx, x);
+            }
+            const __half z16 = __float2half_rn(mn);
+            const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+            const float z = __half2float(z16), sc = __half2float(s16);
+            reinterpret_cast<__half*>(led + Lay::KS)[grp * D + c] = s16;
+            reinterpret_cast<__half*>(led + Lay::KZ)[grp * D + c] = z16;
+            for (int i = 0; i < kQGroup; ++i) {
+                const float x = __bfloat162float(kt[(grp * kQGroup + i) * D + c]);
+                const float r = sc == 0.f ? 0.f : rintf(__fdiv_rn(__fsub_rn(x, z), sc));
+                codes[(grp * kQGroup + i) * D + c] = (uint8_t)fminf(fmaxf(r, 0.f), 3.f);
+            }
+        }
+        __syncthreads();
+        for (int u = tid; u < kTierW * (D / 16); u += blockDim.x) {   // pack kc
             const int tok = u / (D / 16), sblk = u % (D / 16);
             uint32_t word = 0;
+#pragma unroll
             for (int e2 = 0; e2 < 16; ++e2)
-                word |= (uint32_t)codes[tok][16 * sblk + e2] << ((e2 & 1) * 16 + 2 * (e2 >> 1));
+                word |= (uint32_t)codes[tok * D + 16 * sblk + e2] << ((e2 & 1) * 16 + 2 * (e2 >> 1));
             reinterpret_cast<uint32_t*>(led + Lay::KC)[u] = word;
         }
         __syncthreads();
-        // values: per token over 32-channel groups (thread = token)
-        for (int tok = threadIdx.x; tok < kTierW; tok += blockDim.x) {
-            const __nv_bfloat16* row = row_of(a.c.v_pool, tok);
-            for (int cg = 0; cg < D / kQGroup; ++cg) {
-                float mn = INFINITY, mx = -INFINITY;
-                for (int i = 0; i < kQGroup; ++i) {
-                    const float x = __bfloat162float(row[cg * kQGroup + i]);
-                    mn = fminf(mn, x);
-                    mx = fmaxf(mx, x);
-                }
-                const __half z16 = __float2half_rn(mn);
-                const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-                const float z = __half2float(z16), s = __half2float(s16);
+        // values: per token over 32-channel groups, a warp per (token, group)
+        for (int pr = warp; pr < kTierW * (D / kQGroup); pr += blockDim.x / 32) {
+            const int tok = pr / (D / kQGroup), cg = pr % (D / kQGroup);
+            const float x = __bfloat162float(vt[tok * D + cg * kQGroup + lane]);
+            float mn = x, mx = x;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
+            const __half z16 = __float2half_rn(mn);
+            const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+            const float z = __half2float(z16), sc = __half2float(s16);
+            if (lane == 0) {
                 reinterpret_cast<__half*>(led + Lay::VS)[tok * (D / kQGroup) + cg] = s16;
                 reinterpret_cast<__half*>(led + Lay::VZ)[tok * (D / kQGroup) + cg] = z16;
-                for (int i = 0; i < kQGroup; ++i) {
-                    const float x = __bfloat162float(row[cg * kQGroup + i]);
-                    const float r = s == 0.f ? 0.f : rintf(__fdiv_rn(__fsub_rn(x, z), s));
-                    codes[tok][cg * kQGroup + i] = (uint8_t)fminf(fmaxf(r, 0.f), 3.f);
-                }
             }
+            const float r = sc == 0.f ? 0.f : rintf(__fdiv_rn(__fsub_rn(x, z), sc));
+            codes[tok * D + cg * kQGroup + lane] = (uint8_t)fminf(fmaxf(r, 0.f), 3.f);
         }
         __syncthreads();
-        for (int u = threadIdx.x; u < (kTierW / 16) * D; u += blockDim.x) {   // pack vc
+        for (int u = tid; u < (kTierW / 16) * D; u += blockDim.x) {   // pack vc
             const int chunk = u / D, c = u % D;
             uint32_t word = 0;
+#pragma unroll
             for (int e2 = 0; e2 < 16; ++e2)
-                word |= (uint32_t)codes[16 * chunk + e2][c] << ((e2 & 1) * 16 + 2 * (e2 >> 1));
+                word |= (uint32_t)codes[(16 * chunk + e2) * D + c] << ((e2 & 1) * 16 + 2 * (e2 >> 1));
             reinterpret_cast<uint32_t*>(led + Lay::VC)[u] = word;
         }
         __syncthreads();
     }
 }
 
+// Promotion: the window's ledger entry of the (layer, KV head) is staged in
+// shared memory; each thread then writes 8 dequantized channels of one
+// token (one 16-byte store) to the window's pages.
 template <int D>
-__global__ void __launch_bounds__(128) tier_promote_kernel(const TierArgs a, int max_items) {
+__global__ void __launch_bounds__(kQuantThreads) tier_promote_kernel(const TierArgs a,
+                                                                     int max_items) {
     using Lay = LedgerLayout<D>;
     constexpr int PW = kTierW / kTile;
+    __shared__ __align__(16) unsigned char led_s[Lay::BYTES];
     griddep_wait();
     griddep_release();
+    (void)max_items;
     const int LG = a.n_layers * a.n_kv, MW = a.c.max_windows;
-    const int64_t total = (int64_t)a.batch * max_items * LG;
+    const int64_t total = item_count(a.n_prom, a.batch, LG);
     for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
-        const int lg = (int)(it % LG);
-        const int e = (int)((it / LG) % max_items), b = (int)(it / ((int64_t)LG * max_items));
-        if (e >= a.n_prom[b]) continue;
+        int b, e, lg;
+        item_at(a.n_prom, a.batch, LG, it, &b, &e, &lg);
         const int w = a.prom_list[(size_t)b * MW + e];
         const int l = lg / a.n_kv, g = lg % a.n_kv;
         const int32_t* pages = a.st.win_pages + ((size_t)b * MW + w) * PW;
-        const unsigned char* led = reinterpret_cast<const unsigned char*>(a.c.ledger) +
-                                   ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES;
-        const uint32_t* kc = reinterpret_cast<const uint32_t*>(led + Lay::KC);
-        const uint32_t* vc = reinterpret_cast<const uint32_t*>(led + Lay::VC);
-        const __half* ks = reinterpret_cast<const __half*>(led + Lay::KS);
-        const __half* kz = reinterpret_cast<const __half*>(led + Lay::KZ);
-        const __half* vs = reinterpret_cast<const __half*>(led + Lay::VS);
-        const __half* vz = reinterpret_cast<const __half*>(led + Lay::VZ);
-        for (int u = threadIdx.x; u < kTierW * D; u += blockDim.x) {
-            const int tok = u / D, c = u % D;
+        const uint4* led = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const unsigned char*>(a.c.ledger) +
+            ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES);
+        for (int u = threadIdx.x; u < Lay::BYTES / 16; u += blockDim.x)
+            reinterpret_cast<uint4*>(led_s)[u] = led[u];
+        __syncthreads();
+        const uint32_t* kc = reinterpret_cast<const uint32_t*>(led_s + Lay::KC);
+        const uint32_t* vc = reinterpret_cast<const uint32_t*>(led_s + Lay::VC);
+        const __half* ks = reinterpret_cast<const __half*>(led_s + Lay::KS);
+        const __half* kz = reinterpret_cast<const __half*>(led_s + Lay::KZ);
+        const __half* vs = reinterpret_cast<const __half*>(led_s + Lay::VS);
+        const __half* vz = reinterpret_cast<const __half*>(led_s + Lay::VZ);
+        for (int u = threadIdx.x; u < 2 * kTierW * (D / 8); u += blockDim.x) {
+            const int kv = u / (kTierW * (D / 8)), rest = u % (kTierW * (D / 8));
+            const int tok = rest / (D / 8), c0 = (rest % (D / 8)) * 8;
             const int page = pages[tok / kTile];
             if (page < 0) continue;   // no page could be taken for this promotion
+            uint32_t packed[4];
+#pragma unroll
+            for (int k = 0; k < 8; k += 2) {
+                float v2[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = c0 + k + h;
+                    uint32_t q;
+                    float sc, z;
+                    if (kv == 0) {
+                        const int ek = c % 16;
+                        q = (kc[tok * (D / 16) + c / 16] >> ((ek & 1) * 16 + 2 * (ek >> 1))) & 3u;
+                        sc = __half2float(ks[(tok / kQGroup) * D + c]);
+                        z = __half2float(kz[(tok / kQGroup) * D + c]);
+                    } else {
+                        const int et = tok % 16;
+                        q = (vc[(tok / 16) * D + c] >> ((et & 1) * 16 + 2 * (et >> 1))) & 3u;
+                        sc = __half2float(vs[tok * (D / kQGroup) + c / kQGroup]);
+                        z = __half2float(vz[tok * (D / kQGroup) + c / kQGroup]);
+                    }
+                    v2[h] = fmaf((float)q, sc, z);
+                }
+                const __nv_bfloat162 bb = __floats2bfloat162_rn(v2[0], v2[1]);
+                packed[k / 2] = *reinterpret_cast<const uint32_t*>(&bb);
+            }
             const size_t r = (((size_t)page * a.n_layers + l) * a.n_kv + g) * kTile + tok % kTile;
-            const int ek = c % 16, et = tok % 16;
-            const uint32_t qk = (kc[tok * (D / 16) + c / 16] >> ((ek & 1) * 16 + 2 * (ek >> 1))) & 3u;
-            const uint32_t qv = (vc[(tok / 16) * D + c] >> ((et & 1) * 16 + 2 * (et >> 1))) & 3u;
-            const int grp = tok / kQGroup, cg = c / kQGroup;
-            const float kval = fmaf((float)qk, __half2float(ks[grp * D + c]), __half2float(kz[grp * D + c]));
-            const float vval = fmaf((float)qv, __half2float(vs[tok * (D / kQGroup) + cg]),
-                                    __half2float(vz[tok * (D / kQGroup) + cg]));
-            reinterpret_cast<__nv_bfloat16*>(a.c.k_pool)[r * D + c] = __float2bfloat16_rn(kval);
-            reinterpret_cast<__nv_bfloat16*>(a.c.v_pool)[r * D + c] = __float2bfloat16_rn(vval);
+            reinterpret_cast<uint4*>(kv ? a.c.v_pool : a.c.k_pool)[(r * D + c0) / 8] =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
+        __syncthreads();
     }
 }
 
@@ -528,13 +586,18 @@ cudaError_t launch_tier_route(const TierArgs& a, cudaStream_t s) {
 cudaError_t launch_tier_quantize(const TierArgs& a, int max_items, int num_sms, cudaStream_t s) {
     if (max_items <= 0) return cudaSuccess;
     if (a.head_dim != 128) return cudaErrorInvalidValue;
-    return launch_pdl(tier_quantize_kernel<128>, dim3(4 * num_sms), dim3(128), 0, s, a, max_items);
+    auto kern = tier_quantize_kernel<128>;
+    const int smem = kTierW * 128 * (2 + 2 + 1);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(2 * num_sms), dim3(kQuantThreads), (size_t)smem, s, a, max_items);
 }
 
 cudaError_t launch_tier_promote(const TierArgs& a, int max_items, int num_sms, cudaStream_t s) {
     if (max_items <= 0) return cudaSuccess;
     if (a.head_dim != 128) return cudaErrorInvalidValue;
-    return launch_pdl(tier_promote_kernel<128>, dim3(4 * num_sms), dim3(128), 0, s, a, max_items);
+    return launch_pdl(tier_promote_kernel<128>, dim3(2 * num_sms), dim3(kQuantThreads), 0, s, a,
+                      max_items);
 }
 
 cudaError_t launch_tier_finish(const TierArgs& a, cudaStream_t s) {
