@@ -56,6 +56,16 @@ __device__ __forceinline__ int scan_excl(int v, int* red, int* total) {
     __syncthreads();
     return before;
 }
+// 16-byte asynchronous global -> shared copies: every copy of a stage is in
+// flight at once (no register round trip), then one wait.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ bool is_bf16_tier(uint8_t t) {
     return t == KVEV_TIER_UNROUTED || t == KVEV_TIER_FULL;
 }
@@ -405,9 +415,10 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
             const int kv = u / (PW * kChunks), rest = u % (PW * kChunks);
             const int pi = rest / kChunks, c = rest % kChunks;
             const size_t off = ((((size_t)pages[pi] * a.n_layers + l) * a.n_kv + g) * kTile) * D / 8 + c;
-            const uint4 v = reinterpret_cast<const uint4*>(kv ? a.c.v_pool : a.c.k_pool)[off];
-            reinterpret_cast<uint4*>(kv ? vt : kt)[(size_t)pi * kChunks + c] = v;
+            cp_async16(reinterpret_cast<uint4*>(kv ? vt : kt) + (size_t)pi * kChunks + c,
+                       reinterpret_cast<const uint4*>(kv ? a.c.v_pool : a.c.k_pool) + off);
         }
+        cp_async_wait_all();
         __syncthreads();
         // keys: per channel over 32-token groups
         for (int u = tid; u < D * (kTierW / kQGroup); u += blockDim.x) {
@@ -496,7 +507,8 @@ __global__ void __launch_bounds__(kQuantThreads) tier_promote_kernel(const TierA
             reinterpret_cast<const unsigned char*>(a.c.ledger) +
             ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES);
         for (int u = threadIdx.x; u < Lay::BYTES / 16; u += blockDim.x)
-            reinterpret_cast<uint4*>(led_s)[u] = led[u];
+            cp_async16(reinterpret_cast<uint4*>(led_s) + u, led + u);
+        cp_async_wait_all();
         __syncthreads();
         const uint32_t* kc = reinterpret_cast<const uint32_t*>(led_s + Lay::KC);
         const uint32_t* vc = reinterpret_cast<const uint32_t*>(led_s + Lay::VC);
