@@ -2,18 +2,19 @@
 // Sec. 4.1: the accessible keys and values include the dequantized INT2
 // windows), with the dequantization folded into the tensor-core products.
 //
-// A key is k_c = code_c * s_c + z_c with (s, z) per channel over a 32-token
-// group, so within a group
-//     q . k = sum_c (q_c s_c) code_c + sum_c q_c z_c :
+// A key is k_c = code_c * s_c + z_c = s_c (code_c - 1.5) + (z_c + 1.5 s_c)
+// with (s, z) per channel over a 32-token group, so within a group
+//     q . k = sum_c (q_c s_c)(code_c - 1.5) + sum_c q_c (z_c + 1.5 s_c) :
 // the A operand is q * s (bf16 hi + lo, the product is exact in fp32), the
-// B operand the codes themselves (small integers, exact in bf16), plus a
-// per-head bias.  A value is v_c = code_c * s_g + z_g with (s, z) per token
+// B operand the centred codes (exact in bf16), plus a per-head bias.  A
+// value is v_c = s_g (code_c - 1.5) + (z_g + 1.5 s_g) with (s, z) per token
 // over a 32-channel group g, so
-//     sum_i p_i v_ic = sum_i (p_i s_ig) code_ic + sum_i p_i z_ig :
-// per channel group the A operand is p * s (hi + lo), B the codes, plus a
-// per-head, per-group bias carried through the online softmax like the
-// output.  Codes become bf16 with an OR into the exponent of 128 and a
-// subtraction of 128.
+//     sum_i p_i v_ic = sum_i (p_i s_ig)(code_ic - 1.5) + sum_i p_i (z_ig + 1.5 s_ig) :
+// per channel group the A operand is p * s (hi + lo), B the centred codes,
+// plus a per-head, per-group bias carried through the online softmax like
+// the output.  Centring keeps both sums near the size of the result, so the
+// hi + lo rounding of the products is not magnified by cancellation between
+// a large code sum and a large zero-point sum.
 //
 // Work: every (layer, sequence, KV head) row has `slots` units, one INT2
 // window each (past the sequence's INT2 list a unit is empty); warps take
@@ -44,12 +45,19 @@ __device__ __forceinline__ void cp_async_wait_prior() {   // all but the newest 
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
-// Two 2-bit codes at bits 0-1 and 16-17 of x (other bits clear) -> bf16x2.
-__device__ __forceinline__ uint32_t codes_bf16x2(uint32_t x) {
+// Two 2-bit codes at bits 1-2 and 17-18 of x (other bits clear) -> bf16x2 of
+// the centred codes c - 1.5 (exact): ORed into the mantissa of 64 (unit 0.5)
+// the field 2c reads 64 + c, and 64 + c - 65.5 = c - 1.5.
+__device__ __forceinline__ uint32_t centred_bf16x2(uint32_t x) {
     uint32_t r;
-    const uint32_t biased = x | 0x43004300u;   // 128 + code, exact in bf16
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(0x43004300u));
+    const uint32_t biased = x | 0x42804280u;   // 64 + c
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(0x42834283u));   // - 65.5
     return r;
+}
+// The lane's code word: rotated so that its two code pairs sit at bits 1-2 / 17-18
+// (b0) and 9-10 / 25-26 (b1) for a lane with column pair t.
+__device__ __forceinline__ uint32_t lane_codes(uint32_t u, int t) {
+    return __funnelshift_r(u, u, (2 * t + 31) & 31);
 }
 
 // The 16 x 8 x 16 tensor-core tile has 8 A rows and a group has 4 query
@@ -184,10 +192,10 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                     const float q2 = bf16_lo(qa2[s]), q3 = bf16_hi(qa2[s]);
                     af[s][0] = half_pair(q0 * s01.x, q1 * s01.y);
                     af[s][1] = half_pair(q2 * s23.x, q3 * s23.y);
-                    kb = fmaf(q0, z01.x, kb);
-                    kb = fmaf(q1, z01.y, kb);
-                    kb = fmaf(q2, z23.x, kb);
-                    kb = fmaf(q3, z23.y, kb);
+                    kb = fmaf(q0, fmaf(1.5f, s01.x, z01.x), kb);
+                    kb = fmaf(q1, fmaf(1.5f, s01.y, z01.y), kb);
+                    kb = fmaf(q2, fmaf(1.5f, s23.x, z23.x), kb);
+                    kb = fmaf(q3, fmaf(1.5f, s23.y, z23.y), kb);
                 }
                 kb += __shfl_xor_sync(kFull, kb, 1);
                 kb += __shfl_xor_sync(kFull, kb, 2);
@@ -202,9 +210,9 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                     for (int s = 0; s < KS; ++s)
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
-                            const uint32_t y = kc[(tok0 + 8 * i + g) * KS + s] >> (2 * t);
-                            const uint32_t b0 = codes_bf16x2(y & 0x00030003u);
-                            const uint32_t b1 = codes_bf16x2((y >> 8) & 0x00030003u);
+                            const uint32_t y = lane_codes(kc[(tok0 + 8 * i + g) * KS + s], t);
+                            const uint32_t b0 = centred_bf16x2(y & 0x00060006u);
+                            const uint32_t b1 = centred_bf16x2((y >> 8) & 0x00060006u);
                             mma_rows8(acc[s & 1][i][0], acc[s & 1][i][1], af[s][0], af[s][1], b0, b1);
                         }
                     float sc[2][2];
@@ -263,7 +271,8 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                             const uint32_t ws = (cg < 2 ? vsr[k].x : vsr[k].y) >> (16 * (cg & 1));
                             const uint32_t wz = (cg < 2 ? vzr[k].x : vzr[k].y) >> (16 * (cg & 1));
                             sv[k] = __half2float(__ushort_as_half((unsigned short)(ws & 0xffffu)));
-                            vb = fmaf(pv[k], __half2float(__ushort_as_half((unsigned short)(wz & 0xffffu))), vb);
+                            const float zc = __half2float(__ushort_as_half((unsigned short)(wz & 0xffffu)));
+                            vb = fmaf(pv[k], fmaf(1.5f, sv[k], zc), vb);
                         }
                         vb += __shfl_xor_sync(kFull, vb, 1);
                         vb += __shfl_xor_sync(kFull, vb, 2);
@@ -273,9 +282,9 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
 #pragma unroll
                         for (int jj = 0; jj < kQGroup / 8; ++jj) {
                             const int j = cg * (kQGroup / 8) + jj;      // 8-channel block
-                            const uint32_t y = vc[ti * D + 8 * j + g] >> (2 * t);
-                            const uint32_t b0 = codes_bf16x2(y & 0x00030003u);
-                            const uint32_t b1 = codes_bf16x2((y >> 8) & 0x00030003u);
+                            const uint32_t y = lane_codes(vc[ti * D + 8 * j + g], t);
+                            const uint32_t b0 = centred_bf16x2(y & 0x00060006u);
+                            const uint32_t b1 = centred_bf16x2((y >> 8) & 0x00060006u);
                             mma_rows8(o[j][0], o[j][1], pa0, pa2, b0, b1);
                         }
                     }
