@@ -72,6 +72,23 @@ def kv_bytes(n_layers, n_kv, d, L, budget, batch=1):
     return attn + comp, attn
 
 
+def slowest_ms(ms: float, dist, device: str = "cuda") -> float:
+    """The largest per-rank time (the job ends when its slowest rank does);
+    `ms` itself without a process group."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every replica processes `units_per_rank` per
+    step (weak scaling), the step lasting the slowest rank's `ms`."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -229,6 +246,9 @@ def main():
     ap.add_argument("--impl", default="kvev", choices=["kvev", "reference"])
     ap.add_argument("--cpu-layers", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode-steps", type=int, default=256,
+                    help="decode steps of each (alpha, refresh mode) run reported under 'modes' "
+                         "(0: skip)")
     ap.add_argument("--layers", type=int, default=WORKLOAD["n_layers"],
                     help="smaller cases for profiling; the headline uses 32")
     ap.add_argument("--prefill", type=int, default=WORKLOAD["prefill"])
@@ -319,10 +339,7 @@ def main():
     kvev.kvev_sync(ep.ctx)
     launches = kvev.kvev_launch_count(ep.ctx) - n0
     ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_ms(ms, dist)
 
     # Per-kernel region: CUDA events around every launch, on the launching stream.
     kvev.kvev_profile(ep.ctx, True)
@@ -334,7 +351,7 @@ def main():
     prof = kvev.kvev_profile_read(ep.ctx)
     kvev.kvev_profile(ep.ctx, False)
     nbytes, attn_bytes = kv_bytes(W["n_layers"], W["n_kv_heads"], W["head_dim"], L0 + 1, B)
-    value = world * nbytes / (ms * 1e-3) / 1e9
+    value = job_rate(nbytes, world, ms) / 1e9
 
     # -------------------------------------------------- end to end (host API)
     qh = torch.from_numpy(q.view(np.int16)).pin_memory()
@@ -363,12 +380,48 @@ def main():
         one_e2e()
     torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
-    if dist:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = world * nbytes / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = slowest_ms(e2e_ms, dist)
+    e2e_val = job_rate(nbytes, world, e2e_ms) / 1e9
     assert int(nreth[0]) == B
+
+    # ------------------------------------- refresh modes x alphas (steady state)
+    # Every (alpha, mode) run starts from the prefill at step 1 and decodes
+    # --mode-steps steps; steady = steps 2.. (about B + 1 live tokens each).
+    modes = []
+    if args.mode_steps > 0 and args.layers == WORKLOAD["n_layers"]:
+        k0, v0 = ep.k[0].clone(), ep.v[0].clone()
+        n_ms = args.mode_steps
+        step_in = [tuple(to_dev(x, torch) for x in wl.step_inputs(t)) for t in range(1, n_ms + 1)]
+        row = 2 * W["head_dim"] * 2 * W["n_kv_heads"] * W["n_layers"]
+        for alpha in (0.01, 0.05, 0.15):
+            ctx = kvev.kvev_create(ep.layout, B, 1, alpha, W["beta"])
+            kvev.kvev_configure(ctx, kvev.KVEV_AGE_SINCE_ACCESS, kvev.KVEV_POOL_SUM)
+            for name, mode, period in (("full", kvev.KVEV_REFRESH_FULL, 1),
+                                       ("lazy8", kvev.KVEV_REFRESH_LAZY, 8),
+                                       ("frozen", kvev.KVEV_REFRESH_FROZEN, 1)):
+                kvev.kvev_refresh_mode(ctx, mode, period)
+                ep.k[0].copy_(k0)
+                ep.v[0].copy_(v0)
+                ep.cache.cur = 0
+                kvev.kvev_begin(ctx, L0)
+                kvev.kvev_init_state(ctx, ep.state, stream)
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ms + 1)]
+                torch.cuda.synchronize()
+                evs[0].record(stream)
+                for t in range(1, n_ms + 1):
+                    kvev.kvev_step(ctx, *step_in[t - 1], ep.cache, ep.state, t, ep.out,
+                                   ep.retained, ep.n_retained, stream)
+                    evs[t].record(stream)
+                torch.cuda.synchronize()
+                kvev.kvev_sync(ctx)
+                st = [evs[t - 1].elapsed_time(evs[t]) for t in range(1, n_ms + 1)]
+                steady = sum(st[1:]) / max(1, n_ms - 1)
+                steady_bytes = (B + 1) * row + 2 * B * row   # attention + compaction
+                modes.append({"alpha": alpha, "mode": name, "step1_us": round(st[0] * 1e3, 1),
+                              "steady_us": round(steady * 1e3, 1),
+                              "steady_GBps": round(steady_bytes / (steady * 1e-3) / 1e9, 1)})
+            kvev.kvev_destroy(ctx)
+        del k0, v0, step_in
 
     # --------------------------------------------------------------- roofline
     peak, peak_kind = measured_peak()
@@ -413,6 +466,7 @@ def main():
             "gpu_launches": launches,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "modes": modes,
         }
         print(json.dumps(line), flush=True)
     ep.close()
@@ -528,10 +582,7 @@ def bench_paged(args, rank, world, local_rank):
     kvev.kvev_sync(pp.ctx)
     launches = kvev.kvev_launch_count(pp.ctx) - n0
     ms = e0.elapsed_time(e1) / n_steps
-    if dist:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = slowest_ms(ms, dist)
 
     # replay with per-kernel events; count the live tokens each step attends
     row = 2 * W["head_dim"] * 2 * W["n_kv_heads"] * Ly        # bytes of one token, all layers
@@ -725,10 +776,7 @@ def bench_tiers(args, rank, world, local_rank):
     launches = kvev.kvev_launch_count(tp.ctx) - n0
     step_ms = [evs[t - 1].elapsed_time(evs[t]) for t in range(1, n_steps + 1)]
     ms = sum(step_ms) / n_steps
-    if dist:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = slowest_ms(ms, dist)
 
     # replay with per-kernel events, counting what each step attends
     row_bf16 = 2 * W["head_dim"] * 2 * W["n_kv_heads"] * Ly       # bytes per token, all layers
