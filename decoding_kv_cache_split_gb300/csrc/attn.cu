@@ -33,6 +33,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "kvev_internal.h"
 #include "mma_ops.h"
 
@@ -401,60 +403,112 @@ __global__ void __launch_bounds__(WARPS * 32)
     flush(cur_row);
 }
 
-// Split combine: one CTA per row of the launch, thread d owns output dim d
-// of every head of the row.  All of a row's segments are loaded in batches
-// of kSeg before any is used, and merged with a running max (one pass).
-template <int D, int G>
-__global__ void __launch_bounds__(D) combine_kernel(const CombineArgs a) {
-    constexpr int kSeg = 8;
+// Split combine: one warp per row of the launch (up to 8 rows per CTA); lane l
+// owns output dims [V l, V l + V) of every head (V = D / 32, one vector
+// load per head and segment).  The row's segments are merged with a running
+// max, one at a time with the next one prefetched (KB = 1, rows split over
+// few warps) or in batches of KB loaded before any merge (rows split over
+// many warps).
+constexpr int kCombineWarps = 8;
+
+template <int D, int G, int KB>
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs a) {
+    constexpr int V = D / 32;   // dims per lane
+    static_assert(V == 2 || V == 4, "head_dim 64 or 128");
+    using VecT = typename std::conditional<V == 4, float4, float2>::type;
     griddep_wait();
     griddep_release();
-    const int64_t r = blockIdx.x;                 // row of the launch
-    const int d = threadIdx.x;
-    float M[G], Ls[G], acc[G];
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);   // row of the launch
+    if (r >= a.n_rows) return;
+    float M[G], Ls[G], acc[G][V];
 #pragma unroll
-    for (int h = 0; h < G; ++h) { M[h] = -INFINITY; Ls[h] = 0.f; acc[h] = 0.f; }
+    for (int h = 0; h < G; ++h) {
+        M[h] = -INFINITY;
+        Ls[h] = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[h][v] = 0.f;
+    }
+    auto as_array = [](const VecT& x, float (&o)[V]) {
+        const float* p = reinterpret_cast<const float*>(&x);
+#pragma unroll
+        for (int v = 0; v < V; ++v) o[v] = p[v];
+    };
     for (int set = 0; set < 1 + a.has2; ++set) {
         const SplitPartials& sp = set ? a.sp2 : a.sp;
         int64_t lo, hi;
         split_warps_of_row(sp, r, &lo, &hi);
-        for (int64_t w0 = lo; w0 <= hi; w0 += kSeg) {
-            float m[kSeg][G], l[kSeg][G], o[kSeg][G];
+        // segment w of the row: (m, l) of every head and this lane's dims of o
+        auto load = [&](int64_t w, float (&m)[G], float (&l)[G], VecT (&o)[G]) {
+            const bool ok = w <= hi && split_warp_has_tiles(w, sp.n_tiles, sp.total_warps);
 #pragma unroll
-            for (int j = 0; j < kSeg; ++j) {
-                const int64_t w = w0 + j;
-                const bool ok = w <= hi && split_warp_has_tiles(w, sp.n_tiles, sp.total_warps);
+            for (int h = 0; h < G; ++h) {
+                const float* ml = sp.part_ml + ((w + r) * G + h) * 2;
+                m[h] = ok ? __ldcg(ml) : -INFINITY;
+                l[h] = ok ? __ldcg(ml + 1) : 0.f;
+                o[h] = ok ? __ldcg(reinterpret_cast<const VecT*>(sp.part_o + ((w + r) * G + h) * D) + lane)
+                          : VecT{};
+            }
+        };
+        auto merge = [&](const float (&m)[G], const float (&l)[G], const VecT (&o)[G]) {
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    m[j][h] = ok ? __ldcg(sp.part_ml + ((w + r) * G + h) * 2) : -INFINITY;
-                    l[j][h] = ok ? __ldcg(sp.part_ml + ((w + r) * G + h) * 2 + 1) : 0.f;
-                    o[j][h] = ok ? __ldcg(sp.part_o + ((w + r) * G + h) * D + d) : 0.f;
+            for (int h = 0; h < G; ++h) {
+                if (m[h] == -INFINITY) continue;
+                const float mx = fmaxf(M[h], m[h]);
+                const float fo = fast_exp2(M[h] - mx), fj = fast_exp2(m[h] - mx);
+                float ov[V];
+                as_array(o[h], ov);
+                Ls[h] = Ls[h] * fo + l[h] * fj;
+#pragma unroll
+                for (int v = 0; v < V; ++v) acc[h][v] = acc[h][v] * fo + ov[v] * fj;
+                M[h] = mx;
+            }
+        };
+        if (KB == 1) {   // few segments per row: one at a time, the next one prefetched
+            float mc[G], lc[G];
+            VecT oc[G];
+            load(lo, mc, lc, oc);
+            for (int64_t w = lo; w <= hi; ++w) {
+                float mn[G], ln[G];
+                VecT on[G];
+                if (w + 1 <= hi) load(w + 1, mn, ln, on);
+                merge(mc, lc, oc);
+                if (w + 1 <= hi) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        mc[h] = mn[h];
+                        lc[h] = ln[h];
+                        oc[h] = on[h];
+                    }
                 }
             }
+        } else {         // many segments per row: batches of KB, all loads first
+            for (int64_t w0 = lo; w0 <= hi; w0 += KB) {
+                float m[KB][G], l[KB][G];
+                VecT o[KB][G];
 #pragma unroll
-            for (int j = 0; j < kSeg; ++j)
+                for (int j = 0; j < KB; ++j) load(w0 + j, m[j], l[j], o[j]);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    if (m[j][h] == -INFINITY) continue;
-                    const float mn = fmaxf(M[h], m[j][h]);
-                    const float fo = fast_exp2(M[h] - mn), fj = fast_exp2(m[j][h] - mn);
-                    Ls[h] = Ls[h] * fo + l[j][h] * fj;
-                    acc[h] = acc[h] * fo + o[j][h] * fj;
-                    M[h] = mn;
-                }
+                for (int j = 0; j < KB; ++j) merge(m[j], l[j], o[j]);
+            }
         }
     }
-    const SplitPartials& sp = a.sp;
-    const int64_t arow = sp.row0 + r;
+    const int64_t arow = a.sp.row0 + r;
     const int g = (int)(arow % a.n_kv);
     const int64_t lb = arow / a.n_kv;
     const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        a.out[(((size_t)b * a.n_layers + l) * a.n_q + (size_t)g * G + h) * D + d] = acc[h] / Ls[h];
-        if (d == 0) a.lse2[arow * G + h] = M[h] + log2f(Ls[h]);
+        const float inv = 1.0f / Ls[h];
+        VecT res;
+        float* rp = reinterpret_cast<float*>(&res);
+#pragma unroll
+        for (int v = 0; v < V; ++v) rp[v] = acc[h][v] * inv;
+        reinterpret_cast<VecT*>(a.out + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)g * G + h) * D)[lane] = res;
+        if (lane == 0) a.lse2[arow * G + h] = M[h] + log2f(Ls[h]);
     }
 }
+
 
 #ifndef KVEV_ATTN_STAGES
 #define KVEV_ATTN_STAGES 2
@@ -549,12 +603,23 @@ cudaError_t launch_attention(const AttnArgs& a, int head_dim, int group, int gri
     return cudaErrorInvalidValue;
 }
 
+template <int D, int G>
+cudaError_t launch_combine_t(const CombineArgs& a, cudaStream_t s) {
+    // warps a row's tiles are split over, on average
+    const double per_row = 1.0 + (double)a.sp.total_warps / (a.n_rows > 0 ? a.n_rows : 1);
+    if (per_row < 3.0) {
+        const dim3 grid((a.n_rows + kCombineWarps - 1) / kCombineWarps), block(kCombineWarps * 32);
+        return launch_pdl(combine_kernel<D, G, 1>, grid, block, 0, s, a);
+    }
+    // few rows, many segments each: one warp per CTA to spread the rows over the SMs
+    return launch_pdl(combine_kernel<D, G, (G <= 4 ? 4 : 2)>, dim3(a.n_rows), dim3(32), 0, s, a);
+}
+
 cudaError_t launch_combine(const CombineArgs& a, int head_dim, int group, cudaStream_t s) {
-    const dim3 grid(a.n_rows);
-    if (group == 4 && head_dim == 128) return launch_pdl(combine_kernel<128, 4>, grid, dim3(128), 0, s, a);
-    if (group == 4 && head_dim == 64) return launch_pdl(combine_kernel<64, 4>, grid, dim3(64), 0, s, a);
-    if (group == 8 && head_dim == 128) return launch_pdl(combine_kernel<128, 8>, grid, dim3(128), 0, s, a);
-    if (group == 8 && head_dim == 64) return launch_pdl(combine_kernel<64, 8>, grid, dim3(64), 0, s, a);
+    if (group == 4 && head_dim == 128) return launch_combine_t<128, 4>(a, s);
+    if (group == 4 && head_dim == 64) return launch_combine_t<64, 4>(a, s);
+    if (group == 8 && head_dim == 128) return launch_combine_t<128, 8>(a, s);
+    if (group == 8 && head_dim == 64) return launch_combine_t<64, 8>(a, s);
     return cudaErrorInvalidValue;
 }
 
