@@ -178,13 +178,26 @@ __global__ void __launch_bounds__(256) paged_append_kernel(const PagedArgs a,
     if (page >= 0) {   // copy the new K/V rows into the page, every layer and KV head
         const int lpr = a.head_dim / 8;
         const int rows = a.n_layers * a.n_kv;
-        for (int u = threadIdx.x; u < 2 * rows * lpr; u += blockDim.x) {
-            const int kv = u / (rows * lpr), rest = u - kv * rows * lpr;
-            const int r = rest / lpr, c = rest - r * lpr;   // r = l * n_kv + g
-            const size_t src = (((size_t)b * a.n_layers * a.n_kv) + r) * lpr + c;
-            const size_t dst = ((((size_t)page * rows) + r) * a.page + s_tok) * lpr + c;
-            const uint4 w = reinterpret_cast<const uint4*>(kv ? v_new : k_new)[src];
-            reinterpret_cast<uint4*>(kv ? a.c.v_pool : a.c.k_pool)[dst] = w;
+        constexpr int kBatch = 8;   // loads in flight per thread before their stores
+        for (int u0 = threadIdx.x; u0 < 2 * rows * lpr; u0 += kBatch * blockDim.x) {
+            uint4 w[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int u = u0 + k * blockDim.x;
+                if (u >= 2 * rows * lpr) break;
+                const int kv = u / (rows * lpr), rest = u - kv * rows * lpr;
+                w[k] = __ldg(reinterpret_cast<const uint4*>(kv ? v_new : k_new) +
+                             ((size_t)b * rows * lpr + rest));
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int u = u0 + k * blockDim.x;
+                if (u >= 2 * rows * lpr) break;
+                const int kv = u / (rows * lpr), rest = u - kv * rows * lpr;
+                const int r = rest / lpr, c = rest - r * lpr;   // r = l * n_kv + g
+                const size_t dst = ((((size_t)page * rows) + r) * a.page + s_tok) * lpr + c;
+                reinterpret_cast<uint4*>(kv ? a.c.v_pool : a.c.k_pool)[dst] = w[k];
+            }
         }
     }
     int ntok = 0;

@@ -163,13 +163,26 @@ __global__ void __launch_bounds__(kBook) tier_append_kernel(const TierArgs a,
     if (page >= 0) {   // K/V rows of the new token, every layer and KV head
         const int lpr = a.head_dim / 8;
         const int rows = a.n_layers * a.n_kv;
-        for (int u = threadIdx.x; u < 2 * rows * lpr; u += blockDim.x) {
-            const int kv = u / (rows * lpr), rest = u - kv * rows * lpr;
-            const int r = rest / lpr, c = rest - r * lpr;
-            const size_t src = ((size_t)b * rows + r) * lpr + c;
-            const size_t dst = (((size_t)page * rows + r) * kTile + s_row) * lpr + c;
-            const uint4 v = reinterpret_cast<const uint4*>(kv ? v_new : k_new)[src];
-            reinterpret_cast<uint4*>(kv ? a.c.v_pool : a.c.k_pool)[dst] = v;
+        constexpr int kBatch = 8;   // loads in flight per thread before their stores
+        for (int u0 = threadIdx.x; u0 < 2 * rows * lpr; u0 += kBatch * blockDim.x) {
+            uint4 v[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int u = u0 + k * blockDim.x;
+                if (u >= 2 * rows * lpr) break;
+                const int kv = u / (rows * lpr), rest = u - kv * rows * lpr;
+                v[k] = __ldg(reinterpret_cast<const uint4*>(kv ? v_new : k_new) +
+                             ((size_t)b * rows * lpr + rest));
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int u = u0 + k * blockDim.x;
+                if (u >= 2 * rows * lpr) break;
+                const int kv = u / (rows * lpr), rest = u - kv * rows * lpr;
+                const int r = rest / lpr, c = rest - r * lpr;
+                const size_t dst = (((size_t)page * rows + r) * kTile + s_row) * lpr + c;
+                reinterpret_cast<uint4*>(kv ? a.c.v_pool : a.c.k_pool)[dst] = v[k];
+            }
         }
     }
     // ---- attention lists
