@@ -173,26 +173,48 @@ __global__ void __launch_bounds__(WARPS * 32)
 
     // tiles are walked with (row, tile-in-row) counters: no divisions in the loop
     const int tpr = a.tiles_per_row;
-    auto issue = [&](int64_t row, int tile, int stage) {  // lane 0 only
-        int y = 0, nv;
+    // Block mode: the warp keeps 32 consecutive block-table entries of the row
+    // it is issuing for (lane k holds tile tb_base + k), refreshed together when
+    // the issue moves past them, so issuing a tile needs no dependent loads.
+    int64_t tb_row = -1;
+    int tb_base = 0, tb_y = 0, tb_nv = 0, tb_pos = 0;
+    auto table_for = [&](int64_t row, int tile) {   // every lane of the warp
         if constexpr (PAGED) {
+            if (row == tb_row && tile >= tb_base && tile < tb_base + 32) return;
             const int64_t arow = a.row0 + row;
             const int gk = (int)(arow % a.n_kv);
             const int64_t lb = arow / a.n_kv;
             const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
-            nv = 0;
-            int pos = tile * T;
-            if (tile < a.n_blocks[b]) {
-                const int page = a.block_table[(size_t)b * a.pps + tile];
-                nv = a.blk_len[(size_t)b * a.pps + tile];
-                y = (int)((((int64_t)page * a.n_layers + l) * a.n_kv + gk) * T);
-                if (a.blk_pos) pos = a.blk_pos[(size_t)b * a.pps + tile];
+            const int tk = tile + lane;
+            tb_y = 0;
+            tb_nv = 0;
+            tb_pos = tk * T;
+            if (tk < a.n_blocks[b] && tk < a.tiles_per_row) {
+                const int page = a.block_table[(size_t)b * a.pps + tk];
+                tb_nv = a.blk_len[(size_t)b * a.pps + tk];
+                tb_y = (int)((((int64_t)page * a.n_layers + l) * a.n_kv + gk) * T);
+                if (a.blk_pos) tb_pos = a.blk_pos[(size_t)b * a.pps + tk];
             }
-            stage_pos[stage] = pos;
+            tb_row = row;
+            tb_base = tile;
+        }
+    };
+    auto issue = [&](int64_t row, int tile, int stage) {   // every lane; lane 0 issues
+        if constexpr (!PAGED) {
+            if (lane != 0) return;
+        }
+        int y = 0, nv;
+        if constexpr (PAGED) {
+            table_for(row, tile);
+            y = __shfl_sync(kFull, tb_y, tile - tb_base);
+            nv = __shfl_sync(kFull, tb_nv, tile - tb_base);
+            const int pos = __shfl_sync(kFull, tb_pos, tile - tb_base);
+            if (lane == 0) stage_pos[stage] = pos;
         } else {
             y = (int)((a.row0 + row) * a.max_ctx + tile * T);
             nv = min(T, a.L - tile * T);
         }
+        if (lane != 0) return;
         stage_nv[stage] = nv;
         if (nv == 0) {   // empty tile: complete the phase with no data
             mbar_arrive(&bars[stage]);
@@ -211,7 +233,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     int ptile = (int)(x0 - prow * tpr);
     const int64_t n_issue0 = x1 - x0 < STAGES ? x1 - x0 : STAGES;
     for (int s = 0; s < n_issue0; ++s) {
-        if (lane == 0) issue(prow, ptile, s);
+        issue(prow, ptile, s);
         if (++ptile == tpr) { ptile = 0; ++prow; }
     }
     int64_t crow = x0 / tpr;          // tile being consumed
@@ -281,7 +303,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         if (PAGED && nvalid == 0) {   // past the sequence's live blocks: nothing to do
             __syncwarp();
             if (x + STAGES < x1) {
-                if (lane == 0) issue(prow, ptile, stage);
+                issue(prow, ptile, stage);
                 if (++ptile == tpr) { ptile = 0; ++prow; }
             }
             if (++stage == STAGES) { stage = 0; parity ^= 1u; }
@@ -386,7 +408,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         // a partial tile needed a proxy fence (done there).
         __syncwarp();
         if (x + STAGES < x1) {
-            if (lane == 0) issue(prow, ptile, stage);
+            issue(prow, ptile, stage);
             if (++ptile == tpr) { ptile = 0; ++prow; }
         }
         if (++stage == STAGES) { stage = 0; parity ^= 1u; }
