@@ -1330,6 +1330,122 @@ kvev_status kvev_launch_count(const kvev_ctx* c, int64_t* launches) {
     return KVEV_OK;
 }
 
+// ---- checkpoint / resume ---------------------------------------------------
+
+}  // extern "C"
+
+namespace {
+
+constexpr uint32_t kBlobMagic = 0x5645564bu;   // "KVEV"
+constexpr uint32_t kBlobVersion = 1;
+
+struct BlobHead {
+    uint32_t magic, version;
+    kvev_layout lay;
+    int64_t budget;
+    float alpha, beta;
+    RegionParams rp;
+    int32_t refresh_mode, refresh_period, age_mode, pool;
+    int32_t k_full, k_quant, omega;
+    int32_t begun, len, prefill_len;
+    int64_t step;
+    int32_t t_nw, t_tl, t_first_u, t_nf, t_nq;
+    int32_t n_ub, n_pin;          // then n_ub + n_pin int32 values
+};
+
+}  // namespace
+
+extern "C" {
+
+kvev_status kvev_export_state(const kvev_ctx* c, void* host, size_t* bytes) {
+    if (!c || !bytes) return fail(KVEV_EINVAL, "NULL argument");
+    const size_t need = sizeof(BlobHead) + 4 * (c->ub_blocks.size() + c->pin_blocks.size());
+    if (!host) {
+        *bytes = need;
+        return KVEV_OK;
+    }
+    if (*bytes < need) return fail(KVEV_EINVAL, "buffer of %zu bytes, %zu needed", *bytes, need);
+    BlobHead h;
+    memset(&h, 0, sizeof h);   // no indeterminate padding in the blob
+    h.magic = kBlobMagic;
+    h.version = kBlobVersion;
+    h.lay = c->lay;
+    h.budget = c->budget;
+    h.alpha = c->alpha;
+    h.beta = c->beta;
+    h.rp = c->rp;
+    h.refresh_mode = c->refresh_mode;
+    h.refresh_period = c->refresh_period;
+    h.age_mode = c->age_mode;
+    h.pool = c->pool;
+    h.k_full = c->k_full;
+    h.k_quant = c->k_quant;
+    h.omega = c->omega;
+    h.begun = c->begun ? 1 : 0;
+    h.len = c->len;
+    h.prefill_len = c->prefill_len;
+    h.step = c->step;
+    h.t_nw = c->t_nw;
+    h.t_tl = c->t_tl;
+    h.t_first_u = c->t_first_u;
+    h.t_nf = c->t_nf;
+    h.t_nq = c->t_nq;
+    h.n_ub = (int32_t)c->ub_blocks.size();
+    h.n_pin = (int32_t)c->pin_blocks.size();
+    char* out = static_cast<char*>(host);
+    memcpy(out, &h, sizeof h);
+    memcpy(out + sizeof h, c->ub_blocks.data(), 4 * c->ub_blocks.size());
+    memcpy(out + sizeof h + 4 * c->ub_blocks.size(), c->pin_blocks.data(),
+           4 * c->pin_blocks.size());
+    *bytes = need;
+    return KVEV_OK;
+}
+
+kvev_status kvev_import_state(kvev_ctx* c, const void* host, size_t bytes, void* stream) {
+    if (!c || !host) return fail(KVEV_EINVAL, "NULL argument");
+    BlobHead h;
+    if (bytes < sizeof h) return fail(KVEV_EINVAL, "blob of %zu bytes is too short", bytes);
+    memcpy(&h, host, sizeof h);
+    if (h.magic != kBlobMagic || h.version != kBlobVersion)
+        return fail(KVEV_EINVAL, "not a kvev state blob (or another version)");
+    if (memcmp(&h.lay, &c->lay, sizeof h.lay) != 0 || h.budget != c->budget ||
+        h.alpha != c->alpha || !(h.beta == c->beta) || memcmp(&h.rp, &c->rp, sizeof h.rp) != 0)
+        return fail(KVEV_EINVAL, "blob from a context with another layout, budget, alpha, beta "
+                    "or region table");
+    if (h.n_ub < 0 || h.n_pin < 0 || bytes < sizeof h + 4 * ((size_t)h.n_ub + h.n_pin))
+        return fail(KVEV_EINVAL, "truncated blob");
+    const char* in = static_cast<const char*>(host);
+    c->refresh_mode = h.refresh_mode;
+    c->refresh_period = h.refresh_period;
+    c->age_mode = h.age_mode;
+    c->pool = h.pool;
+    c->k_full = h.k_full;
+    c->k_quant = h.k_quant;
+    c->omega = h.omega;
+    c->begun = h.begun != 0;
+    c->len = h.len;
+    c->prefill_len = h.prefill_len;
+    c->step = h.step;
+    c->t_nw = h.t_nw;
+    c->t_tl = h.t_tl;
+    c->t_first_u = h.t_first_u;
+    c->t_nf = h.t_nf;
+    c->t_nq = h.t_nq;
+    c->ub_blocks.assign(h.n_ub, 0);
+    c->pin_blocks.assign(h.n_pin, 0);
+    memcpy(c->ub_blocks.data(), in + sizeof h, 4 * (size_t)h.n_ub);
+    memcpy(c->pin_blocks.data(), in + sizeof h + 4 * (size_t)h.n_ub, 4 * (size_t)h.n_pin);
+    if (c->lay.page_tokens == kTierW && c->begun) {   // positions so far, per sequence
+        std::vector<int32_t> sl(c->lay.batch, c->len);
+        cudaStream_t s = (cudaStream_t)stream;
+        cudaError_t e = cudaMemcpyAsync(c->ws.t_seq_len, sl.data(), 4 * sl.size(),
+                                        cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "restoring the sequence positions");
+    }
+    return KVEV_OK;
+}
+
 kvev_status kvev_sync(kvev_ctx* c, void* stream) {
     if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
     cudaStream_t s = (cudaStream_t)stream;

@@ -40,7 +40,8 @@ EXPORTS = ["kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_siz
            "kvev_init_state", "kvev_step", "kvev_step_host", "kvev_set_debug",
            "kvev_profile", "kvev_profile_read", "kvev_launch_count", "kvev_sync",
            "kvev_paged_begin", "kvev_paged_step", "kvev_readmit", "kvev_set_tiers",
-           "kvev_tier_begin", "kvev_tier_step", "kvev_attend_noalloc"]
+           "kvev_tier_begin", "kvev_tier_step", "kvev_export_state", "kvev_import_state",
+           "kvev_attend_noalloc"]
 
 
 class KvevError(RuntimeError):
@@ -157,6 +158,8 @@ def lib():
             "kvev_set_tiers": ([P, I64, I64, I32], I32),
             "kvev_tier_begin": ([P, P, P, I32, P], I32),
             "kvev_tier_step": ([P, P, P, P, P, P, I64, P, P], I32),
+            "kvev_export_state": ([P, P, P], I32),
+            "kvev_import_state": ([P, P, ctypes.c_size_t, P], I32),
             "kvev_attend_noalloc": ([P, P, P, P, I32, P, P, P], I32),
         }
         for name, (args, res) in sig.items():
@@ -311,6 +314,20 @@ def kvev_tier_step(ctx, q, k_new, v_new, cache: kvev_tier_cache, state: kvev_tie
                    step: int, out, stream=None) -> None:
     _check(lib().kvev_tier_step(ctx, _ptr(q), _ptr(k_new), _ptr(v_new), ctypes.byref(cache),
                                 ctypes.byref(state), int(step), _ptr(out), _stream(stream)), ctx)
+
+
+def kvev_export_state(ctx) -> bytes:
+    """The context's own state as a byte string (see include/kvev.h)."""
+    n = ctypes.c_size_t()
+    _check(lib().kvev_export_state(ctx, None, ctypes.byref(n)), ctx)
+    buf = ctypes.create_string_buffer(n.value)
+    _check(lib().kvev_export_state(ctx, buf, ctypes.byref(n)), ctx)
+    return buf.raw[:n.value]
+
+
+def kvev_import_state(ctx, blob: bytes, stream=None) -> None:
+    buf = ctypes.create_string_buffer(blob, len(blob))
+    _check(lib().kvev_import_state(ctx, buf, len(blob), _stream(stream)), ctx)
 
 
 def kvev_attend_noalloc(layout: kvev_layout, q, k, v, length: int, out, lse2, stream=None) -> None:

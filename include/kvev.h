@@ -390,6 +390,23 @@ kvev_status kvev_tier_step(kvev_ctx* ctx, const void* q, const void* k_new, cons
                            const kvev_tier_cache* cache, const kvev_tier_state* state,
                            int64_t step, float* out, void* stream);
 
+/* ---- Checkpoint / resume -------------------------------------------------
+ * A context's own state: the run's position (step, live length, the host's
+ * per-sequence block bounds and tier counts) and its configuration (refresh
+ * schedule, age and pooling modes, tier capacities).  Everything else a
+ * checkpoint needs is in the caller's device buffers (cache, per-token or
+ * per-block state, block tables, score table, ledger), which the caller
+ * saves and restores itself; no counterpart on the pages beyond the
+ * persistence of scores across eviction.
+ * kvev_export_state: host memory; with host == NULL only *bytes is set to the
+ * size; otherwise *bytes must be at least that size and is set to it.
+ * kvev_import_state: a blob exported by a context created with the same
+ * layout, budget, alpha, beta and region table (else KVEV_EINVAL); the next
+ * step is the exported step + 1.  Enqueued on `stream` (two-tier contexts
+ * restore a small device counter). */
+kvev_status kvev_export_state(const kvev_ctx* ctx, void* host, size_t* bytes);
+kvev_status kvev_import_state(kvev_ctx* ctx, const void* host, size_t bytes, void* stream);
+
 /* Attention of the pass without allocating: no counterpart on the pages;
  * it exists for callers that cannot call cudaMalloc (engines whose allocator
  * owns all device memory, latency-critical paths that cannot take the
