@@ -260,6 +260,8 @@ struct kvev_ctx {
     float prof_ms[KVEV_PROFILE_SLOTS] = {};
     int64_t prof_n[KVEV_PROFILE_SLOTS] = {};
     int64_t launches = 0;
+    int64_t test_fault_tile = -1;   // test-only timeout injection for the next step
+    uint32_t test_wait_limit = 0;
 };
 
 namespace {
@@ -579,6 +581,10 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     at.write_logits = refresh ? 1 : 0;
     at.q_scale = (float)(1.4426950408889634 / sqrt((double)Ly.head_dim));
     at.view_tokens = (int64_t)Ly.n_layers * Ly.batch * Ly.n_kv_heads * Ly.max_ctx;
+    at.fault_tile_p1 = c->test_fault_tile + 1;
+    at.wait_limit = c->test_wait_limit;
+    c->test_fault_tile = -1;
+    c->test_wait_limit = 0;
 
     ScoreArgs sc{};
     sc.logits = c->ws.logits;
@@ -1443,6 +1449,14 @@ kvev_status kvev_import_state(kvev_ctx* c, const void* host, size_t bytes, void*
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) return cuda_fail(e, "restoring the sequence positions");
     }
+    return KVEV_OK;
+}
+
+kvev_status kvev_test_wait_timeout(kvev_ctx* c, int64_t tile, uint32_t wait_limit) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (tile < 0 || wait_limit == 0) return fail(KVEV_EINVAL, "tile >= 0 and wait_limit >= 1");
+    c->test_fault_tile = tile;
+    c->test_wait_limit = wait_limit;
     return KVEV_OK;
 }
 

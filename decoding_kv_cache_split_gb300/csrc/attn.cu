@@ -69,8 +69,8 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 // Bounded wait on a phase of an mbarrier; false if the phase never completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_test(bar, parity)) return true;
     return false;
 }
@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     __syncwarp();
     const uint64_t pol = evict_first_policy();
+    const uint32_t wait_limit = a.wait_limit ? a.wait_limit : kWaitLimit;
 
     // tiles are walked with (row, tile-in-row) counters: no divisions in the loop
     const int tpr = a.tiles_per_row;
@@ -222,6 +223,8 @@ __global__ void __launch_bounds__(WARPS * 32)
         }
         unsigned char* dst = wbuf + (size_t)stage * C::STAGE_BYTES;
         mbar_expect_tx(&bars[stage], C::STAGE_BYTES);
+        // test-only: the tile's copies are never issued, so its wait runs out
+        if (row * tpr + tile + 1 == a.fault_tile_p1) return;
 #pragma unroll
         for (int bx = 0; bx < C::BOXES; ++bx) {
             tma_load_2d(dst + bx * C::BOX_BYTES, &tmap_k, bx * 64, y, &bars[stage], pol);
@@ -292,7 +295,7 @@ __global__ void __launch_bounds__(WARPS * 32)
             l_run = 0.f;
         }
 
-        if (!mbar_wait(&bars[stage], parity)) {
+        if (!mbar_wait(&bars[stage], parity, wait_limit)) {
             ok = false;
             break;
         }
@@ -415,10 +418,13 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     if (!ok) {
         if (lane == 0) atomicOr(a.status, kStatusTimeout);
-        // let the copies already issued land before the block exits
+        // let the copies already issued land before the block exits (always
+        // the full cap: a shortened test limit must not cut this wait; the
+        // injected tile issued none)
         for (int s = 0; s < STAGES; ++s) {
             const int64_t it2 = it + s;
-            if (x0 + it2 < x1) mbar_wait(&bars[it2 % STAGES], (uint32_t)((it2 / STAGES) & 1));
+            if (x0 + it2 < x1 && x0 + it2 + 1 != a.fault_tile_p1)
+                mbar_wait(&bars[it2 % STAGES], (uint32_t)((it2 / STAGES) & 1), kWaitLimit);
         }
         return;
     }

@@ -56,6 +56,11 @@ struct AttnArgs {
     // tile_stats[((row * stats_tiles) + (p - stats_base) / kTile) * G + h].
     float2* tile_stats;
     int32_t stats_tiles, stats_base;
+    // Test-only: bounded-wait iterations (0: kWaitLimit) and 1 + the tile of
+    // the launch whose copies are not issued (0: none), to exercise the
+    // timeout path without a fault.  Zero-initialised arguments inject nothing.
+    uint32_t wait_limit;
+    int64_t fault_tile_p1;
 };
 
 // Where one attention launch left its split partials: warp w's piece of the

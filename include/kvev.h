@@ -238,7 +238,16 @@ kvev_status kvev_profile_read(kvev_ctx* ctx, float* ms, int64_t* launches);
 /* Total kernel launches this context has made (all entry points). */
 kvev_status kvev_launch_count(const kvev_ctx* ctx, int64_t* launches);
 
-/* Block until `stream`'s work is done; returns KVEV_ECUDA on a device fault. */
+/* Test-only failure injection: in the next kvev_step the attention kernel
+ * arms tile `tile` of its launch but issues none of its copies, and every
+ * bounded device wait gives up after `wait_limit` iterations; the warp that
+ * waits on that tile gives up, records the timeout in the device status word
+ * and returns after its other copies have landed, so kvev_sync (or
+ * kvev_step_host) returns KVEV_ETIMEOUT and the context stays usable (the
+ * step's outputs are undefined).  No counterpart on the pages. */
+kvev_status kvev_test_wait_timeout(kvev_ctx* ctx, int64_t tile, uint32_t wait_limit);
+
+/* Block until `stream`'s work is done; returns KVEV_ECUDA on a device fault. *//* Block until `stream`'s work is done; returns KVEV_ECUDA on a device fault. */
 kvev_status kvev_sync(kvev_ctx* ctx, void* stream);
 
 /* ---- Block-granular eviction with score persistence ----------------------
