@@ -5,16 +5,19 @@
 // A key is k_c = code_c * s_c + z_c = s_c (code_c - 1.5) + (z_c + 1.5 s_c)
 // with (s, z) per channel over a 32-token group, so within a group
 //     q . k = sum_c (q_c s_c)(code_c - 1.5) + sum_c q_c (z_c + 1.5 s_c) :
-// the A operand is q * s (bf16 hi + lo, the product is exact in fp32), the
-// B operand the centred codes (exact in bf16), plus a per-head bias.  A
-// value is v_c = s_g (code_c - 1.5) + (z_g + 1.5 s_g) with (s, z) per token
-// over a 32-channel group g, so
+// the A operand is q * s (bf16 hi + lo), the B operand the centred codes,
+// plus a per-head bias.  A value is v_c = s_g (code_c - 1.5) + (z_g + 1.5 s_g)
+// with (s, z) per token over a 32-channel group g, so
 //     sum_i p_i v_ic = sum_i (p_i s_ig)(code_ic - 1.5) + sum_i p_i (z_ig + 1.5 s_ig) :
 // per channel group the A operand is p * s (hi + lo), B the centred codes,
 // plus a per-head, per-group bias carried through the online softmax like
-// the output.  Centring keeps both sums near the size of the result, so the
-// hi + lo rounding of the products is not magnified by cancellation between
-// a large code sum and a large zero-point sum.
+// the output.  Centring keeps both sums near the size of the result.
+//
+// The ledger stores each code as a sign and a magnitude bit at the bit
+// positions of its tensor-core register (see LedgerLayout): one rotate and
+// one mask-and-OR turn a word into a bf16 pair of exact subnormals
+// (2 code - 3) * 2^-128, and the A operands carry a factor 2^96, so the
+// products are the centred terms times 2^-31, rescaled once per row.
 //
 // Work: every (layer, sequence, KV head) row has `slots` units, one INT2
 // window each (past the sequence's INT2 list a unit is empty); warps take
@@ -32,6 +35,8 @@ namespace {
 
 constexpr int kI2Warps = 4;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr float kAScale = 0x1p96f;    // A operands carry 2^96
+constexpr float kProdScale = 0x1p31f; // undoes 2^96 * 2^-127 (code - 1.5 in the B operand)
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -45,19 +50,13 @@ __device__ __forceinline__ void cp_async_wait_prior() {   // all but the newest 
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
-// Two 2-bit codes at bits 1-2 and 17-18 of x (other bits clear) -> bf16x2 of
-// the centred codes c - 1.5 (exact): ORed into the mantissa of 64 (unit 0.5)
-// the field 2c reads 64 + c, and 64 + c - 65.5 = c - 1.5.
-__device__ __forceinline__ uint32_t centred_bf16x2(uint32_t x) {
-    uint32_t r;
-    const uint32_t biased = x | 0x42804280u;   // 64 + c
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(0x42834283u));   // - 65.5
-    return r;
+// Register `slot` of a ledger code word: the bf16 pair (2 c - 3) * 2^-128.
+__device__ __forceinline__ uint32_t code_reg(uint32_t w, int slot) {
+    const uint32_t x = slot == 0 ? w : __funnelshift_r(w, w, 2 * slot);
+    return (x & 0x80408040u) | 0x00200020u;
 }
-// The lane's code word: rotated so that its two code pairs sit at bits 1-2 / 17-18
-// (b0) and 9-10 / 25-26 (b1) for a lane with column pair t.
-__device__ __forceinline__ uint32_t lane_codes(uint32_t u, int t) {
-    return __funnelshift_r(u, u, (2 * t + 31) & 31);
+__device__ __forceinline__ float2 h2f(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 // The 16 x 8 x 16 tensor-core tile has 8 A rows and a group has 4 query
@@ -69,8 +68,9 @@ __device__ __forceinline__ uint32_t lane_codes(uint32_t u, int t) {
 template <int D, int G>
 __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args a) {
     static_assert(G == 4, "hi / lo rows need 4 query heads per KV head");
+    static_assert(D == 128, "ledger registers are laid out for head_dim 128");
     using Lay = LedgerLayout<D>;
-    constexpr int KS = D / 16, NB = D / 8, NG = D / kQGroup;
+    constexpr int KS = D / 16, NB = D / 8, NG = Lay::NG;
     extern __shared__ __align__(128) unsigned char smem[];
     griddep_wait();
     griddep_release();
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
     const int g = lane >> 2, t = lane & 3;   // fragment row, column pair
     const int head = g & 3;                  // query head of the group
     const bool lo_row = g >= 4;              // this row carries the "lo" parts
+    const float lom = lo_row ? 1.f : 0.f;
     // window id of unit x (-1: empty), and its ledger entry
     auto unit_window = [&](int64_t x, const unsigned char** src) -> int {
         const int64_t row = x / a.slots;
@@ -105,15 +106,16 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
         }
         cp_async_commit();
     };
-    // the lane's half (hi or lo) of a product pair
+    // the lane's half (hi or lo) of a product pair: hi rows round the pair to
+    // bf16, lo rows round what the hi part leaves
     auto half_pair = [&](float x0v, float x1v) -> uint32_t {
         const uint32_t hi = pack_bf16x2(x0v, x1v);
-        return lo_row ? pack_bf16x2(x0v - bf16_lo(hi), x1v - bf16_hi(hi)) : hi;
+        return pack_bf16x2(fmaf(-lom, bf16_lo(hi), x0v), fmaf(-lom, bf16_hi(hi), x1v));
     };
 
-    uint32_t qa0[KS], qa2[KS];               // Q (bf16x2) of the lane's head
-    float o[NB][2];                          // hi or lo part of O[head][8j + 2t, +1]
-    float vbias[NG];                         // sum_i p_i z_ig of the head, per channel group
+    uint32_t qa[KS][2];                      // Q * 2^96 (bf16x2) of the lane's head
+    float o[NB][2];                          // hi or lo part of O[head][8j + 2t, +1] * 2^-31
+    float vbias[NG];                         // the lane's share of sum_i p_i z'_ig
     float m_run = -INFINITY, l_run = 0.f;
     int64_t cur_row = -1;
 
@@ -121,6 +123,12 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
         float l = l_run;
         l += __shfl_xor_sync(kFull, l, 1);
         l += __shfl_xor_sync(kFull, l, 2);
+        float vb[NG];
+#pragma unroll
+        for (int c = 0; c < NG; ++c) {
+            vb[c] = vbias[c] + __shfl_xor_sync(kFull, vbias[c], 1);
+            vb[c] += __shfl_xor_sync(kFull, vb[c], 2);
+        }
         const int64_t slot = (int64_t)w + row;
         float* po = a.part_o + ((size_t)slot * G + head) * D;
 #pragma unroll
@@ -129,7 +137,7 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
             const float v1 = o[j][1] + __shfl_xor_sync(kFull, o[j][1], 16);
             if (!lo_row)
                 *reinterpret_cast<float2*>(po + 8 * j + 2 * t) =
-                    make_float2(v0 + vbias[j / 4], v1 + vbias[j / 4]);
+                    make_float2(fmaf(v0, kProdScale, vb[j / 4]), fmaf(v1, kProdScale, vb[j / 4]));
         }
         if (!lo_row && t == 0) {
             float* pml = a.part_ml + ((size_t)slot * G + head) * 2;
@@ -137,6 +145,8 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
             pml[1] = l;
         }
     };
+    const float acc_scale = a.q_scale * kProdScale;   // logits from the code products
+    const float kb_scale = a.q_scale * (1.f / kAScale);
 
     issue(x0, 0);
     int bi = 0;
@@ -155,10 +165,12 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
             const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
                 a.q + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)gk * G + head) * D);
 #pragma unroll
-            for (int s = 0; s < KS; ++s) {
-                qa0[s] = qrow[8 * s + t];       // dims 16s + 2t, +1
-                qa2[s] = qrow[8 * s + 4 + t];   // dims 16s + 8 + 2t, +1
-            }
+            for (int s = 0; s < KS; ++s)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {   // dims 16s + 8h + 2t, +1 (exact scaling)
+                    const uint32_t qw = qrow[8 * s + 4 * h + t];
+                    qa[s][h] = pack_bf16x2(bf16_lo(qw) * kAScale, bf16_hi(qw) * kAScale);
+                }
 #pragma unroll
             for (int j = 0; j < NB; ++j) o[j][0] = o[j][1] = 0.f;
 #pragma unroll
@@ -170,49 +182,50 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
         const int wid = unit_window(x, &src);
         if (wid >= 0) {
             const unsigned char* buf = wbuf + (size_t)bi * Lay::BYTES;
-            const uint32_t* kc = reinterpret_cast<const uint32_t*>(buf + Lay::KC);
-            const uint32_t* vc = reinterpret_cast<const uint32_t*>(buf + Lay::VC);
-            const __half2* ks2 = reinterpret_cast<const __half2*>(buf + Lay::KS);
-            const __half2* kz2 = reinterpret_cast<const __half2*>(buf + Lay::KZ);
-            const uint2* vs4 = reinterpret_cast<const uint2*>(buf + Lay::VS);   // 4 fp16 per token
-            const uint2* vz4 = reinterpret_cast<const uint2*>(buf + Lay::VZ);
+            const uint4* kc4 = reinterpret_cast<const uint4*>(buf + Lay::KC) + lane;
+            const uint4* vc4 = reinterpret_cast<const uint4*>(buf + Lay::VC) + lane;
+            const uint4* ks4 = reinterpret_cast<const uint4*>(buf + Lay::KS) + 4 * t;
+            const uint4* kz4 = reinterpret_cast<const uint4*>(buf + Lay::KZ) + 4 * t;
+            const uint4* vs4 = reinterpret_cast<const uint4*>(buf + Lay::VS) + 2 * t;
+            const uint4* vz4 = reinterpret_cast<const uint4*>(buf + Lay::VZ) + 2 * t;
             for (int grp = 0; grp < kTierW / kQGroup; ++grp) {
-                // A' = q * s of this group's key scales (the lane's hi or lo part),
-                // and the key bias sum_c q_c z_c
+                // A' = q * s * 2^96 of this group's key scales (the lane's hi or
+                // lo part), and the key bias sum_c q_c (z_c + 1.5 s_c) * 2^96
                 uint32_t af[KS][2];
                 float kb = 0.f;
 #pragma unroll
-                for (int s = 0; s < KS; ++s) {
-                    const int c0 = 16 * s + 2 * t, c2 = c0 + 8;
-                    const float2 s01 = __half22float2(ks2[(grp * D + c0) / 2]);
-                    const float2 s23 = __half22float2(ks2[(grp * D + c2) / 2]);
-                    const float2 z01 = __half22float2(kz2[(grp * D + c0) / 2]);
-                    const float2 z23 = __half22float2(kz2[(grp * D + c2) / 2]);
-                    const float q0 = bf16_lo(qa0[s]), q1 = bf16_hi(qa0[s]);
-                    const float q2 = bf16_lo(qa2[s]), q3 = bf16_hi(qa2[s]);
-                    af[s][0] = half_pair(q0 * s01.x, q1 * s01.y);
-                    af[s][1] = half_pair(q2 * s23.x, q3 * s23.y);
-                    kb = fmaf(q0, fmaf(1.5f, s01.x, z01.x), kb);
-                    kb = fmaf(q1, fmaf(1.5f, s01.y, z01.y), kb);
-                    kb = fmaf(q2, fmaf(1.5f, s23.x, z23.x), kb);
-                    kb = fmaf(q3, fmaf(1.5f, s23.y, z23.y), kb);
+                for (int s2 = 0; s2 < KS / 2; ++s2) {
+                    const uint4 sw = ks4[grp * (D / 8) + s2], zw = kz4[grp * (D / 8) + s2];
+                    const uint32_t sws[4] = {sw.x, sw.y, sw.z, sw.w};
+                    const uint32_t zws[4] = {zw.x, zw.y, zw.z, zw.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {   // (s, h) = (2 s2 + k / 2, k % 2)
+                        const int s = 2 * s2 + k / 2, h = k % 2;
+                        const float2 sc = h2f(sws[k]), zc = h2f(zws[k]);
+                        const float q0 = bf16_lo(qa[s][h]), q1 = bf16_hi(qa[s][h]);
+                        af[s][h] = half_pair(q0 * sc.x, q1 * sc.y);
+                        kb = fmaf(q0, fmaf(1.5f, sc.x, zc.x), kb);
+                        kb = fmaf(q1, fmaf(1.5f, sc.y, zc.y), kb);
+                    }
                 }
                 kb += __shfl_xor_sync(kFull, kb, 1);
                 kb += __shfl_xor_sync(kFull, kb, 2);
+                kb *= kb_scale;
 #pragma unroll 1
                 for (int tt = 0; tt < kQGroup / kTile; ++tt) {
                     const int ti = grp * (kQGroup / kTile) + tt;   // 16-token tile of the window
-                    const int tok0 = ti * kTile;
                     // ---- S = A' codes (two 8-token blocks; even and odd k-steps in
                     //      separate accumulators) + bias
+                    const uint4 kq = kc4[ti * 32];
+                    const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
                     float acc[2][2][2] = {};
 #pragma unroll
                     for (int s = 0; s < KS; ++s)
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
-                            const uint32_t y = lane_codes(kc[(tok0 + 8 * i + g) * KS + s], t);
-                            const uint32_t b0 = centred_bf16x2(y & 0x00060006u);
-                            const uint32_t b1 = centred_bf16x2((y >> 8) & 0x00060006u);
+                            const int slot = 4 * (s & 1) + 2 * i;
+                            const uint32_t b0 = code_reg(kw[s >> 1], slot);
+                            const uint32_t b1 = code_reg(kw[s >> 1], slot + 1);
                             mma_rows8(acc[s & 1][i][0], acc[s & 1][i][1], af[s][0], af[s][1], b0, b1);
                         }
                     float sc[2][2];
@@ -221,7 +234,7 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const float part = acc[0][i][e] + acc[1][i][e];
-                            sc[i][e] = (part + __shfl_xor_sync(kFull, part, 16) + kb) * a.q_scale;
+                            sc[i][e] = fmaf(part + __shfl_xor_sync(kFull, part, 16), acc_scale, kb);
                         }
                     // ---- online softmax of the head
                     float mt = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
@@ -255,36 +268,33 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                             a.tile_stats[((size_t)row * a.stats_tiles + (size_t)wid * (kTierW / kTile) +
                                           ti) * G + head] = make_float2(m_run, ts);
                     }
-                    // ---- O += (p * s_v) codes + p * z_v, per 32-channel group
-                    uint2 vsr[4], vzr[4];   // the 4 fp16 scales / zeros of the lane's tokens
+                    // ---- O += (p * s_v) codes + p * z'_v, per 32-channel group
+                    const uint4 vq = vc4[ti * 32];
+                    const uint32_t vw[4] = {vq.x, vq.y, vq.z, vq.w};
+                    const uint4 s0 = vs4[ti * 8], s1 = vs4[ti * 8 + 1];   // tokens 2t(+1), 2t+8(+1)
+                    const uint4 z0 = vz4[ti * 8], z1 = vz4[ti * 8 + 1];
+                    const uint32_t s0w[4] = {s0.x, s0.y, s0.z, s0.w}, s1w[4] = {s1.x, s1.y, s1.z, s1.w};
+                    const uint32_t z0w[4] = {z0.x, z0.y, z0.z, z0.w}, z1w[4] = {z1.x, z1.y, z1.z, z1.w};
+                    float ps[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int tk = tok0 + (k >> 1) * 8 + 2 * t + (k & 1);
-                        vsr[k] = vs4[tk];
-                        vzr[k] = vz4[tk];
-                    }
+                    for (int k = 0; k < 4; ++k) ps[k] = pv[k] * kAScale;
 #pragma unroll
                     for (int cg = 0; cg < NG; ++cg) {
-                        float sv[4], vb = 0.f;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t ws = (cg < 2 ? vsr[k].x : vsr[k].y) >> (16 * (cg & 1));
-                            const uint32_t wz = (cg < 2 ? vzr[k].x : vzr[k].y) >> (16 * (cg & 1));
-                            sv[k] = __half2float(__ushort_as_half((unsigned short)(ws & 0xffffu)));
-                            const float zc = __half2float(__ushort_as_half((unsigned short)(wz & 0xffffu)));
-                            vb = fmaf(pv[k], fmaf(1.5f, sv[k], zc), vb);
-                        }
-                        vb += __shfl_xor_sync(kFull, vb, 1);
-                        vb += __shfl_xor_sync(kFull, vb, 2);
-                        vbias[cg] += vb;
-                        const uint32_t pa0 = half_pair(pv[0] * sv[0], pv[1] * sv[1]);
-                        const uint32_t pa2 = half_pair(pv[2] * sv[2], pv[3] * sv[3]);
+                        const float2 sa = h2f(s0w[cg]), sb = h2f(s1w[cg]);
+                        const float2 za = h2f(z0w[cg]), zb = h2f(z1w[cg]);
+                        float vb = vbias[cg];
+                        vb = fmaf(pv[0], fmaf(1.5f, sa.x, za.x), vb);
+                        vb = fmaf(pv[1], fmaf(1.5f, sa.y, za.y), vb);
+                        vb = fmaf(pv[2], fmaf(1.5f, sb.x, zb.x), vb);
+                        vb = fmaf(pv[3], fmaf(1.5f, sb.y, zb.y), vb);
+                        vbias[cg] = vb;
+                        const uint32_t pa0 = half_pair(ps[0] * sa.x, ps[1] * sa.y);
+                        const uint32_t pa2 = half_pair(ps[2] * sb.x, ps[3] * sb.y);
 #pragma unroll
                         for (int jj = 0; jj < kQGroup / 8; ++jj) {
                             const int j = cg * (kQGroup / 8) + jj;      // 8-channel block
-                            const uint32_t y = lane_codes(vc[ti * D + 8 * j + g], t);
-                            const uint32_t b0 = centred_bf16x2(y & 0x00060006u);
-                            const uint32_t b1 = centred_bf16x2((y >> 8) & 0x00060006u);
+                            const uint32_t b0 = code_reg(vw[cg], 2 * jj);
+                            const uint32_t b1 = code_reg(vw[cg], 2 * jj + 1);
                             mma_rows8(o[j][0], o[j][1], pa0, pa2, b0, b1);
                         }
                     }

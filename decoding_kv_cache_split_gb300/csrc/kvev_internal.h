@@ -199,22 +199,73 @@ constexpr int kTierRecent = KVEV_TIER_RECENT;
 constexpr int kQGroup = 32;                 // quantization group
 constexpr int kTierRouteCap = 2048;         // windows per sequence the routing sort holds
 
-// Byte layout of one (window, layer, KV head) ledger entry at head_dim D:
-//   kc [128 tokens][D/16] u32: token's channels 16s..16s+15, channel e at bit
-//      (e & 1) * 16 + 2 * (e >> 1) (so a lane's mma pairs sit 16 bits apart);
-//   ks, kz [4 groups][D] fp16 (keys per channel over 32-token groups);
-//   vc [8 chunks][D] u32: channel's tokens 16j..16j+15, token e at the same bits;
-//   vs, vz [128 tokens][D/32] fp16 (values per token over 32-channel groups).
+// Byte layout of one (window, layer, KV head) ledger entry at head_dim D,
+// arranged for the INT2 attention kernel's tensor-core fragments (m16n8k16,
+// lane = 4 g + t): per 16-token tile ti, lane L's D/32 code words sit at
+// words ti * D + L * (D / 32) .. + D / 32 - 1 of kc / vc, one 16-byte load.
+// A word carries 8 operand registers (slot 0..7) of two codes each (half e);
+// a register is the word rotated right by 2 slot, masked to its sign bits 15,
+// 31 and magnitude bits 6, 22, with bits 5, 21 set: the bf16 pair
+// (2 c - 3) * 2^-128 (exact subnormals; sign = c <= 1, magnitude 3 for c = 0
+// or 3, else 1).
+//   kc: key code (token 16 ti + 8 i + g, channel 16 s + 8 h + 2 t + e) in
+//       register 4 s + 2 i + h of lane 4 g + t (the B operand of S = Q K^T);
+//   vc: value code (token 16 ti + 8 h + 2 t + e, channel 8 j + g) in register
+//       2 j + h of lane 4 g + t (the B operand of O += P V);
+//   ks, kz: fp16 key scale / zero of (group, channel 16 s + 8 h + 2 t + e) at
+//       group * D + t * D / 4 + 4 s + 2 h + e (a lane's 32 channels together);
+//   vs, vz: fp16 value scale / zero of (token 16 ti + 8 h + 2 t + e, channel
+//       group cg) at ti * 16 G + t * 4 G + h * 2 G + 2 cg + e, G = D / 32.
 template <int D>
 struct LedgerLayout {
+    static constexpr int NG = D / kQGroup;   // channel groups of a value row
     static constexpr int KC = 0;
     static constexpr int KS = KC + kTierW * D / 4;
     static constexpr int KZ = KS + (kTierW / kQGroup) * D * 2;
     static constexpr int VC = KZ + (kTierW / kQGroup) * D * 2;
     static constexpr int VS = VC + kTierW * D / 4;
-    static constexpr int VZ = VS + kTierW * (D / kQGroup) * 2;
-    static constexpr int BYTES = VZ + kTierW * (D / kQGroup) * 2;
+    static constexpr int VZ = VS + kTierW * NG * 2;
+    static constexpr int BYTES = VZ + kTierW * NG * 2;
+    static constexpr int WORDS_PER_LANE = D / 32;
+    // word of kc / vc and the bit of the sign (the magnitude bit is 9 below)
+    __host__ __device__ static int code_word(int ti, int lane, int reg) {
+        return ti * D + lane * WORDS_PER_LANE + (reg >> 3);
+    }
+    __host__ __device__ static int sign_bit(int reg, int e) {
+        return (15 + 16 * e + 2 * (reg & 7)) & 31;
+    }
+    __host__ __device__ static int mag_bit(int reg, int e) {
+        return (6 + 16 * e + 2 * (reg & 7)) & 31;
+    }
+    // key code (token in window, channel) -> word, register half
+    __host__ __device__ static void key_place(int tok, int c, int* word, int* reg, int* e) {
+        const int ti = tok >> 4, i = (tok >> 3) & 1, g = tok & 7;
+        const int s = c >> 4, h = (c >> 3) & 1, t = (c & 7) >> 1;
+        *reg = 4 * s + 2 * i + h;
+        *e = c & 1;
+        *word = code_word(ti, 4 * g + t, *reg);
+    }
+    __host__ __device__ static void value_place(int tok, int c, int* word, int* reg, int* e) {
+        const int ti = tok >> 4, h = (tok >> 3) & 1, t = (tok & 7) >> 1;
+        const int j = c >> 3, g = c & 7;
+        *reg = 2 * j + h;
+        *e = tok & 1;
+        *word = code_word(ti, 4 * g + t, *reg);
+    }
+    __host__ __device__ static int key_scale_index(int grp, int c) {
+        return grp * D + ((c & 7) >> 1) * (D / 4) + 4 * (c >> 4) + 2 * ((c >> 3) & 1) + (c & 1);
+    }
+    __host__ __device__ static int value_scale_index(int tok, int cg) {
+        return (tok >> 4) * 16 * NG + ((tok & 7) >> 1) * 4 * NG + ((tok >> 3) & 1) * 2 * NG +
+               2 * cg + (tok & 1);
+    }
 };
+// (sign, magnitude) bits of a code and back
+__host__ __device__ inline uint32_t code_sign(uint32_t c) { return c <= 1u; }
+__host__ __device__ inline uint32_t code_mag(uint32_t c) { return c == 0u || c == 3u; }
+__host__ __device__ inline uint32_t code_from_bits(uint32_t sign, uint32_t mag) {
+    return sign ? (mag ? 0u : 1u) : (mag ? 3u : 2u);
+}
 
 struct Int2Args {
     const unsigned char* ledger;

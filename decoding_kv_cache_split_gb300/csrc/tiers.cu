@@ -11,6 +11,8 @@
 // grid-stride kernels over (window, layer, KV head) items, and the pages the
 // demoted and evicted windows held return to the free stack last, after the
 // quantization has read them.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -394,29 +396,61 @@ __device__ __forceinline__ void item_at(const int32_t* n, int batch, int LG, int
     *lg = (int)(it % LG);
 }
 
-// Quantization stages the window's 128 key and value
-// rows of the (layer, KV head) in shared memory with 16-byte loads, then
-// quantizes keys per channel (a thread per channel and group) and values per
-// token (a warp per token and channel group, min / max by shuffles).
+// Sign / magnitude bits (bit 0: code <= 1, bit 1: code 0 or 3) of the code
+// of x in a group with fp16 zero z and scale sc > 0, where the code is rint
+// of the correctly rounded fp32 quotient y = (x - z) / sc, clamped to
+// [0, 3]: code <= 1 iff y < 1.5, code 0 iff y <= 0.5, code 3 iff y > 2.5
+// (rint rounds ties to even).  The quotient is first taken as (x - z) * r
+// with r = 1 / sc correctly rounded: the two roundings put it within
+// 3 * 2^-24 relative of the exact quotient, so within 2^-19 of y while it is
+// below 8 in magnitude; only within 2^-16 of a threshold can it fall on the
+// other side of one than y does, and there the quotient is divided out
+// exactly.
+__device__ __forceinline__ uint32_t int2_bits(float x, float z, float sc, float r) {
+    const float d = __fsub_rn(x, z);
+    float y = __fmul_rn(d, r);
+    const float dc = fabsf(y - 1.5f);
+    if (dc <= 0x1p-16f || fabsf(dc - 1.f) <= 0x1p-16f) y = __fdiv_rn(d, sc);
+    return (uint32_t)(y < 1.5f) | ((uint32_t)(y <= 0.5f || y > 2.5f) << 1);
+}
+// A pair of codes as bytes (bits 0, 1: first code; 8, 9: second) -> the
+// pair's sign bits at 15, 31 and magnitude bits at 6, 22 (a multiply places
+// both halves; the cross terms land on bits the masks drop).
+__device__ __forceinline__ uint32_t pair_reg_bits(uint32_t x) {
+    return (((x & 0x0101u) * 0x00808000u) & 0x80008000u) |
+           (((x & 0x0202u) * 0x00002020u) & 0x00400040u);
+}
+
+// Quantization of one half (keys or values) of a (window, layer, KV head)
+// item: the window's 128 rows are staged in shared memory (rows padded by 16
+// bytes so row-strided reads spread over the banks); keys are quantized per
+// channel (a thread per channel and 32-token group), values per token (a
+// thread per token and 32-channel group), a byte of sign / magnitude bits
+// per code; then each thread packs ledger words from code pairs.
 constexpr int kQuantThreads = 256;
+constexpr int kRowPad = 8;     // bf16 elements of padding per staged row
+constexpr int kCodePad = 4;    // bytes of padding per code row
 
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const TierArgs a,
                                                                       int max_items) {
     using Lay = LedgerLayout<D>;
-    constexpr int PW = kTierW / kTile;
+    static_assert(D == 128, "ledger registers are laid out for head_dim 128");
+    constexpr int PW = kTierW / kTile, NG = Lay::NG, WPL = Lay::WORDS_PER_LANE;
+    constexpr int XS = D + kRowPad;                 // staged row stride (elements)
     extern __shared__ __align__(16) unsigned char qsm[];
-    __nv_bfloat16* kt = reinterpret_cast<__nv_bfloat16*>(qsm);            // [128][D]
-    __nv_bfloat16* vt = kt + kTierW * D;                                   // [128][D]
-    uint8_t* codes = reinterpret_cast<uint8_t*>(vt + kTierW * D);          // [128][D]
+    __nv_bfloat16* xt = reinterpret_cast<__nv_bfloat16*>(qsm);            // [128][XS]
+    uint8_t* codes = reinterpret_cast<uint8_t*>(xt + kTierW * XS);         // [128 or D][+pad]
+    (void)max_items;
     griddep_wait();
     griddep_release();
     const int LG = a.n_layers * a.n_kv, MW = a.c.max_windows;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t total = item_count(a.n_quant, a.batch, LG);
+    const int tid = threadIdx.x;
+    const int64_t total = 2 * item_count(a.n_quant, a.batch, LG);
     for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
+        const int kv = (int)(it & 1);
         int b, e, lg;
-        item_at(a.n_quant, a.batch, LG, it, &b, &e, &lg);
+        item_at(a.n_quant, a.batch, LG, it >> 1, &b, &e, &lg);
         const int w = a.quant_list[(size_t)b * MW + e];
         const int l = lg / a.n_kv, g = lg % a.n_kv;
         const int32_t* pages = a.st.win_pages + ((size_t)b * MW + w) * PW;
@@ -424,144 +458,200 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
                              ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES;
         // stage: page i holds tokens 16 i .. 16 i + 15 of the window, rows contiguous
         constexpr int kChunks = kTile * D / 8;   // 16-byte chunks per page row block
-        for (int u = tid; u < 2 * PW * kChunks; u += blockDim.x) {
-            const int kv = u / (PW * kChunks), rest = u % (PW * kChunks);
-            const int pi = rest / kChunks, c = rest % kChunks;
+        const uint4* pool = reinterpret_cast<const uint4*>(kv ? a.c.v_pool : a.c.k_pool);
+        for (int u = tid; u < PW * kChunks; u += blockDim.x) {
+            const int pi = u / kChunks, c = u % kChunks;
+            const int row = pi * kTile + c / (D / 8), col = c % (D / 8);
             const size_t off = ((((size_t)pages[pi] * a.n_layers + l) * a.n_kv + g) * kTile) * D / 8 + c;
-            cp_async16(reinterpret_cast<uint4*>(kv ? vt : kt) + (size_t)pi * kChunks + c,
-                       reinterpret_cast<const uint4*>(kv ? a.c.v_pool : a.c.k_pool) + off);
+            cp_async16(reinterpret_cast<uint4*>(xt + row * XS) + col, pool + off);
         }
         cp_async_wait_all();
         __syncthreads();
-        // keys: per channel over 32-token groups
-        for (int u = tid; u < D * (kTierW / kQGroup); u += blockDim.x) {
-            const int c = u % D, grp = u / D;
-            float mn = INFINITY, mx = -INFINITY;
-            for (int i = 0; i < kQGroup; ++i) {
-                const float x = __bfloat162float(kt[(grp * kQGroup + i) * D + c]);
-                mn = fminf(mn, x);
-                mx = fmaxf(mx, x);
+        uint32_t* words = reinterpret_cast<uint32_t*>(led + (kv ? Lay::VC : Lay::KC));
+        if (kv == 0) {
+            // keys: per channel over 32-token groups; codes[token][channel]
+            constexpr int CS = D + kCodePad;
+            __half* ks = reinterpret_cast<__half*>(led + Lay::KS);
+            __half* kz = reinterpret_cast<__half*>(led + Lay::KZ);
+            for (int u = tid; u < D * (kTierW / kQGroup); u += blockDim.x) {
+                const int c = u % D, grp = u / D;
+                float mn = INFINITY, mx = -INFINITY;
+#pragma unroll 8
+                for (int i = 0; i < kQGroup; ++i) {
+                    const float x = __bfloat162float(xt[(grp * kQGroup + i) * XS + c]);
+                    mn = fminf(mn, x);
+                    mx = fmaxf(mx, x);
+                }
+                const __half z16 = __float2half_rn(mn);
+                const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+                const float z = __half2float(z16), sc = __half2float(s16);
+                ks[Lay::key_scale_index(grp, c)] = s16;
+                kz[Lay::key_scale_index(grp, c)] = z16;
+                const float r = sc == 0.f ? 0.f : __frcp_rn(sc);
+#pragma unroll 8
+                for (int i = 0; i < kQGroup; ++i) {
+                    const float x = __bfloat162float(xt[(grp * kQGroup + i) * XS + c]);
+                    codes[(grp * kQGroup + i) * CS + c] = sc == 0.f ? 3 : (uint8_t)int2_bits(x, z, sc, r);
+                }
             }
-            const __half z16 = __float2half_rn(mn);
-            const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-            const float z = __half2float(z16), sc = __half2float(s16);
-            reinterpret_cast<__half*>(led + Lay::KS)[grp * D + c] = s16;
-            reinterpret_cast<__half*>(led + Lay::KZ)[grp * D + c] = z16;
-            for (int i = 0; i < kQGroup; ++i) {
-                const float x = __bfloat162float(kt[(grp * kQGroup + i) * D + c]);
-                const float r = sc == 0.f ? 0.f : rintf(__fdiv_rn(__fsub_rn(x, z), sc));
-                codes[(grp * kQGroup + i) * D + c] = (uint8_t)fminf(fmaxf(r, 0.f), 3.f);
-            }
-        }
-        __syncthreads();
-        for (int u = tid; u < kTierW * (D / 16); u += blockDim.x) {   // pack kc
-            const int tok = u / (D / 16), sblk = u % (D / 16);
-            uint32_t word = 0;
+            __syncthreads();
+            // word (tile ti, lane 4 gg + t, wq): register 8 wq + slot holds the key
+            // codes of token 16 ti + 8 i + gg, channels 16 s + 8 h + 2 t (+1)
+            for (int u = tid; u < (kTierW / kTile) * 32 * WPL; u += blockDim.x) {
+                const int ti = u / (32 * WPL), lane = (u / WPL) % 32, wq = u % WPL;
+                const int gg = lane >> 2, t = lane & 3;
+                uint32_t word = 0;
 #pragma unroll
-            for (int e2 = 0; e2 < 16; ++e2)
-                word |= (uint32_t)codes[tok * D + 16 * sblk + e2] << ((e2 & 1) * 16 + 2 * (e2 >> 1));
-            reinterpret_cast<uint32_t*>(led + Lay::KC)[u] = word;
-        }
-        __syncthreads();
-        // values: per token over 32-channel groups, a warp per (token, group)
-        for (int pr = warp; pr < kTierW * (D / kQGroup); pr += blockDim.x / 32) {
-            const int tok = pr / (D / kQGroup), cg = pr % (D / kQGroup);
-            const float x = __bfloat162float(vt[tok * D + cg * kQGroup + lane]);
-            float mn = x, mx = x;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                for (int slot = 0; slot < 8; ++slot) {
+                    const int s4 = 2 * wq + (slot >> 2), i = (slot >> 1) & 1, h = slot & 1;
+                    const uint32_t x = *reinterpret_cast<const uint16_t*>(
+                        codes + (16 * ti + 8 * i + gg) * CS + 16 * s4 + 8 * h + 2 * t);
+                    word |= __funnelshift_l(pair_reg_bits(x), pair_reg_bits(x), 2 * slot);
+                }
+                words[u] = word;
             }
-            const __half z16 = __float2half_rn(mn);
-            const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-            const float z = __half2float(z16), sc = __half2float(s16);
-            if (lane == 0) {
-                reinterpret_cast<__half*>(led + Lay::VS)[tok * (D / kQGroup) + cg] = s16;
-                reinterpret_cast<__half*>(led + Lay::VZ)[tok * (D / kQGroup) + cg] = z16;
-            }
-            const float r = sc == 0.f ? 0.f : rintf(__fdiv_rn(__fsub_rn(x, z), sc));
-            codes[tok * D + cg * kQGroup + lane] = (uint8_t)fminf(fmaxf(r, 0.f), 3.f);
-        }
-        __syncthreads();
-        for (int u = tid; u < (kTierW / 16) * D; u += blockDim.x) {   // pack vc
-            const int chunk = u / D, c = u % D;
-            uint32_t word = 0;
+        } else {
+            // values: per token over 32-channel groups; codes[channel][token]
+            constexpr int CS = kTierW + kCodePad;
+            __half* vs = reinterpret_cast<__half*>(led + Lay::VS);
+            __half* vz = reinterpret_cast<__half*>(led + Lay::VZ);
+            for (int u = tid; u < kTierW * NG; u += blockDim.x) {
+                const int tok = u % kTierW, cg = u / kTierW;
+                const uint4* row = reinterpret_cast<const uint4*>(xt + tok * XS + cg * kQGroup);
+                float xs[kQGroup];
 #pragma unroll
-            for (int e2 = 0; e2 < 16; ++e2)
-                word |= (uint32_t)codes[(16 * chunk + e2) * D + c] << ((e2 & 1) * 16 + 2 * (e2 >> 1));
-            reinterpret_cast<uint32_t*>(led + Lay::VC)[u] = word;
+                for (int k = 0; k < kQGroup / 8; ++k) {
+                    const uint4 q4 = row[k];
+                    const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        xs[8 * k + 2 * m] = __uint_as_float(wv[m] << 16);
+                        xs[8 * k + 2 * m + 1] = __uint_as_float(wv[m] & 0xffff0000u);
+                    }
+                }
+                float mn = xs[0], mx = xs[0];
+#pragma unroll
+                for (int i = 1; i < kQGroup; ++i) {
+                    mn = fminf(mn, xs[i]);
+                    mx = fmaxf(mx, xs[i]);
+                }
+                const __half z16 = __float2half_rn(mn);
+                const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+                const float z = __half2float(z16), sc = __half2float(s16);
+                vs[Lay::value_scale_index(tok, cg)] = s16;
+                vz[Lay::value_scale_index(tok, cg)] = z16;
+                const float r = sc == 0.f ? 0.f : __frcp_rn(sc);
+#pragma unroll
+                for (int i = 0; i < kQGroup; ++i)
+                    codes[(cg * kQGroup + i) * CS + tok] =
+                        sc == 0.f ? 3 : (uint8_t)int2_bits(xs[i], z, sc, r);
+            }
+            __syncthreads();
+            // word (tile ti, lane 4 gg + t, wq): register 8 wq + slot holds the value
+            // codes of tokens 16 ti + 8 h + 2 t (+1), channel 8 j + gg
+            for (int u = tid; u < (kTierW / kTile) * 32 * WPL; u += blockDim.x) {
+                const int ti = u / (32 * WPL), lane = (u / WPL) % 32, wq = u % WPL;
+                const int gg = lane >> 2, t = lane & 3;
+                uint32_t word = 0;
+#pragma unroll
+                for (int slot = 0; slot < 8; ++slot) {
+                    const int j = 4 * wq + (slot >> 1), h = slot & 1;
+                    const uint32_t x = *reinterpret_cast<const uint16_t*>(
+                        codes + (8 * j + gg) * CS + 16 * ti + 8 * h + 2 * t);
+                    word |= __funnelshift_l(pair_reg_bits(x), pair_reg_bits(x), 2 * slot);
+                }
+                words[u] = word;
+            }
         }
         __syncthreads();
     }
 }
 
-// Promotion: the window's ledger entry of the (layer, KV head) is staged in
-// shared memory; each thread then writes 8 dequantized channels of one
-// token (one 16-byte store) to the window's pages.
+// Promotion of one half (keys or values) of a (window, layer, KV head) item:
+// the half's ledger codes and scales are staged in shared memory; each
+// thread then writes 8 dequantized channels of one token (one 16-byte store)
+// to the window's pages, decoding the 8 codes from the 4 (keys) or 8
+// (values) ledger words that hold them.
+constexpr int kPromThreads = 256;
+
+__device__ __forceinline__ uint32_t code_of_bits(uint32_t x, int sign_bit, int mag_bit) {
+    const uint32_t idx = (((x >> sign_bit) & 1u) << 1) | ((x >> mag_bit) & 1u);
+    return (0x0132u >> (4 * idx)) & 3u;   // (sign, mag) = (0,0) 2, (0,1) 3, (1,0) 1, (1,1) 0
+}
+
 template <int D>
-__global__ void __launch_bounds__(kQuantThreads) tier_promote_kernel(const TierArgs a,
-                                                                     int max_items) {
+__global__ void __launch_bounds__(kPromThreads) tier_promote_kernel(const TierArgs a,
+                                                                    int max_items) {
     using Lay = LedgerLayout<D>;
-    constexpr int PW = kTierW / kTile;
-    __shared__ __align__(16) unsigned char led_s[Lay::BYTES];
+    static_assert(D == 128, "ledger registers are laid out for head_dim 128");
+    constexpr int PW = kTierW / kTile, WPL = Lay::WORDS_PER_LANE;
+    constexpr int HALF = Lay::VC;   // bytes of one half: codes, then scales, then zeros
+    __shared__ __align__(16) unsigned char led_s[HALF];
     griddep_wait();
     griddep_release();
     (void)max_items;
     const int LG = a.n_layers * a.n_kv, MW = a.c.max_windows;
-    const int64_t total = item_count(a.n_prom, a.batch, LG);
+    const int64_t total = 2 * item_count(a.n_prom, a.batch, LG);
     for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
+        const int kv = (int)(it & 1);
         int b, e, lg;
-        item_at(a.n_prom, a.batch, LG, it, &b, &e, &lg);
+        item_at(a.n_prom, a.batch, LG, it >> 1, &b, &e, &lg);
         const int w = a.prom_list[(size_t)b * MW + e];
         const int l = lg / a.n_kv, g = lg % a.n_kv;
         const int32_t* pages = a.st.win_pages + ((size_t)b * MW + w) * PW;
         const uint4* led = reinterpret_cast<const uint4*>(
             reinterpret_cast<const unsigned char*>(a.c.ledger) +
-            ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES);
-        for (int u = threadIdx.x; u < Lay::BYTES / 16; u += blockDim.x)
+            ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES +
+            (kv ? Lay::VC : Lay::KC));
+        for (int u = threadIdx.x; u < HALF / 16; u += blockDim.x)
             cp_async16(reinterpret_cast<uint4*>(led_s) + u, led + u);
         cp_async_wait_all();
         __syncthreads();
-        const uint32_t* kc = reinterpret_cast<const uint32_t*>(led_s + Lay::KC);
-        const uint32_t* vc = reinterpret_cast<const uint32_t*>(led_s + Lay::VC);
-        const __half* ks = reinterpret_cast<const __half*>(led_s + Lay::KS);
-        const __half* kz = reinterpret_cast<const __half*>(led_s + Lay::KZ);
-        const __half* vs = reinterpret_cast<const __half*>(led_s + Lay::VS);
-        const __half* vz = reinterpret_cast<const __half*>(led_s + Lay::VZ);
-        for (int u = threadIdx.x; u < 2 * kTierW * (D / 8); u += blockDim.x) {
-            const int kv = u / (kTierW * (D / 8)), rest = u % (kTierW * (D / 8));
-            const int tok = rest / (D / 8), c0 = (rest % (D / 8)) * 8;
+        const uint32_t* cw = reinterpret_cast<const uint32_t*>(led_s);
+        const __half* sc16 = reinterpret_cast<const __half*>(led_s + (Lay::KS - Lay::KC));
+        const __half* zc16 = reinterpret_cast<const __half*>(led_s + (Lay::KZ - Lay::KC));
+        uint4* pool = reinterpret_cast<uint4*>(kv ? a.c.v_pool : a.c.k_pool);
+        for (int u = threadIdx.x; u < kTierW * (D / 8); u += blockDim.x) {
+            const int tok = u / (D / 8), c0 = (u % (D / 8)) * 8;
             const int page = pages[tok / kTile];
             if (page < 0) continue;   // no page could be taken for this promotion
+            const int ti = tok >> 4;
             uint32_t packed[4];
+            if (kv == 0) {
+                // channels c0 + 2 t + e: lane 4 gg + t, register 4 s + 2 i + h, half e
+                const int gg = tok & 7, i = (tok >> 3) & 1, s4 = c0 >> 4, h = (c0 >> 3) & 1;
+                const int reg = 4 * s4 + 2 * i + h;
+                const int grp = tok / kQGroup;
 #pragma unroll
-            for (int k = 0; k < 8; k += 2) {
-                float v2[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c = c0 + k + h;
-                    uint32_t q;
-                    float sc, z;
-                    if (kv == 0) {
-                        const int ek = c % 16;
-                        q = (kc[tok * (D / 16) + c / 16] >> ((ek & 1) * 16 + 2 * (ek >> 1))) & 3u;
-                        sc = __half2float(ks[(tok / kQGroup) * D + c]);
-                        z = __half2float(kz[(tok / kQGroup) * D + c]);
-                    } else {
-                        const int et = tok % 16;
-                        q = (vc[(tok / 16) * D + c] >> ((et & 1) * 16 + 2 * (et >> 1))) & 3u;
-                        sc = __half2float(vs[tok * (D / kQGroup) + c / kQGroup]);
-                        z = __half2float(vz[tok * (D / kQGroup) + c / kQGroup]);
-                    }
-                    v2[h] = fmaf((float)q, sc, z);
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t x = cw[ti * D + (4 * gg + t) * WPL + (reg >> 3)];
+                    const int k = Lay::key_scale_index(grp, c0 + 2 * t);
+                    const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(sc16 + k));
+                    const float2 zf = __half22float2(*reinterpret_cast<const __half2*>(zc16 + k));
+                    const float v0 = fmaf((float)code_of_bits(x, Lay::sign_bit(reg, 0), Lay::mag_bit(reg, 0)), sf.x, zf.x);
+                    const float v1 = fmaf((float)code_of_bits(x, Lay::sign_bit(reg, 1), Lay::mag_bit(reg, 1)), sf.y, zf.y);
+                    const __nv_bfloat162 bb = __floats2bfloat162_rn(v0, v1);
+                    packed[t] = *reinterpret_cast<const uint32_t*>(&bb);
                 }
-                const __nv_bfloat162 bb = __floats2bfloat162_rn(v2[0], v2[1]);
-                packed[k / 2] = *reinterpret_cast<const uint32_t*>(&bb);
+            } else {
+                // channels c0 + gg: lane 4 gg + t, register 2 j + h, half e (token parity)
+                const int h = (tok >> 3) & 1, t = (tok & 7) >> 1, e2 = tok & 1;
+                const int reg = 2 * (c0 >> 3) + h;
+                const int k = Lay::value_scale_index(tok, c0 / kQGroup);
+                const float sf = __half2float(sc16[k]), zf = __half2float(zc16[k]);
+                const int sb = Lay::sign_bit(reg, e2), mb = Lay::mag_bit(reg, e2);
+#pragma unroll
+                for (int gp = 0; gp < 4; ++gp) {
+                    const uint32_t x0 = cw[ti * D + (4 * (2 * gp) + t) * WPL + (reg >> 3)];
+                    const uint32_t x1 = cw[ti * D + (4 * (2 * gp + 1) + t) * WPL + (reg >> 3)];
+                    const float v0 = fmaf((float)code_of_bits(x0, sb, mb), sf, zf);
+                    const float v1 = fmaf((float)code_of_bits(x1, sb, mb), sf, zf);
+                    const __nv_bfloat162 bb = __floats2bfloat162_rn(v0, v1);
+                    packed[gp] = *reinterpret_cast<const uint32_t*>(&bb);
+                }
             }
             const size_t r = (((size_t)page * a.n_layers + l) * a.n_kv + g) * kTile + tok % kTile;
-            reinterpret_cast<uint4*>(kv ? a.c.v_pool : a.c.k_pool)[(r * D + c0) / 8] =
-                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            pool[(r * D + c0) / 8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
         __syncthreads();
     }
@@ -612,16 +702,20 @@ cudaError_t launch_tier_quantize(const TierArgs& a, int max_items, int num_sms, 
     if (max_items <= 0) return cudaSuccess;
     if (a.head_dim != 128) return cudaErrorInvalidValue;
     auto kern = tier_quantize_kernel<128>;
-    const int smem = kTierW * 128 * (2 + 2 + 1);
+    const int smem = kTierW * (128 + kRowPad) * 2 + 128 * (kTierW + kCodePad);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3(2 * num_sms), dim3(kQuantThreads), (size_t)smem, s, a, max_items);
+    const int64_t items = 2LL * a.batch * max_items * a.n_layers * a.n_kv;
+    const int grid = (int)std::min<int64_t>(items, 4LL * num_sms);
+    return launch_pdl(kern, dim3(grid), dim3(kQuantThreads), (size_t)smem, s, a, max_items);
 }
 
 cudaError_t launch_tier_promote(const TierArgs& a, int max_items, int num_sms, cudaStream_t s) {
     if (max_items <= 0) return cudaSuccess;
     if (a.head_dim != 128) return cudaErrorInvalidValue;
-    return launch_pdl(tier_promote_kernel<128>, dim3(2 * num_sms), dim3(kQuantThreads), 0, s, a,
+    const int64_t items = 2LL * a.batch * max_items * a.n_layers * a.n_kv;
+    const int grid = (int)std::min<int64_t>(items, 8LL * num_sms);
+    return launch_pdl(tier_promote_kernel<128>, dim3(grid), dim3(kPromThreads), 0, s, a,
                       max_items);
 }
 
