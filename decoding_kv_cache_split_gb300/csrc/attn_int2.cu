@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                 kb += __shfl_xor_sync(kFull, kb, 1);
                 kb += __shfl_xor_sync(kFull, kb, 2);
                 kb *= kb_scale;
-#pragma unroll 1
+#pragma unroll
                 for (int tt = 0; tt < kQGroup / kTile; ++tt) {
                     const int ti = grp * (kQGroup / kTile) + tt;   // 16-token tile of the window
                     // ---- S = A' codes (two 8-token blocks; even and odd k-steps in
