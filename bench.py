@@ -808,8 +808,9 @@ def bench_tiers(args, rank, world, local_rank):
     kernels_us = {k: round(v[0] / n_steps * 1e3, 2) for k, v in prof.items()}
     kernels_us["launches_per_step"] = {k: round(v[1] / n_steps, 2) for k, v in prof.items()}
 
-    # end to end: pinned host q/k/v in, the output back, every step
-    n_e2e = min(n_steps, 64)
+    # end to end over the same steps 1..K: pinned host q/k/v in, the output
+    # and the tiers back, every step
+    n_e2e = n_steps
     host_in = [tuple(x.view(torch.int16).cpu().pin_memory() for x in inputs[t - 1])
                for t in range(1, n_e2e + 1)]
     dev_in = [torch.empty_like(x) for x in inputs[0]]
