@@ -568,15 +568,19 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
 }
 
 // Promotion of one half (keys or values) of a (window, layer, KV head) item:
-// the half's ledger codes and scales are staged in shared memory; each
-// thread then writes 8 dequantized channels of one token (one 16-byte store)
-// to the window's pages, decoding the 8 codes from the 4 (keys) or 8
-// (values) ledger words that hold them.
+// the half's ledger codes and scales are staged in shared memory, then each
+// thread walks the two pages of one channel pair and a quarter of the window
+// (for keys a 32-token group, so one scale pair), turning each ledger
+// register into its two codes and writing
+// code * scale + zero rounded to bf16 (warps store 128 contiguous bytes of
+// a page row).  A register's bf16 pair is (2 c - 3) * 2^-128 (exact
+// subnormals), so c = v * 2^127 + 1.5 exactly in fp32.
 constexpr int kPromThreads = 256;
 
-__device__ __forceinline__ uint32_t code_of_bits(uint32_t x, int sign_bit, int mag_bit) {
-    const uint32_t idx = (((x >> sign_bit) & 1u) << 1) | ((x >> mag_bit) & 1u);
-    return (0x0132u >> (4 * idx)) & 3u;   // (sign, mag) = (0,0) 2, (0,1) 3, (1,0) 1, (1,1) 0
+__device__ __forceinline__ float2 reg_codes(uint32_t x) {   // x rotated to slot 0
+    const uint32_t r = (x & 0x80408040u) | 0x00200020u;
+    return make_float2(fmaf(__uint_as_float(r << 16), 0x1p127f, 1.5f),
+                       fmaf(__uint_as_float(r & 0xffff0000u), 0x1p127f, 1.5f));
 }
 
 template <int D>
@@ -592,6 +596,7 @@ __global__ void __launch_bounds__(kPromThreads) tier_promote_kernel(const TierAr
     (void)max_items;
     const int LG = a.n_layers * a.n_kv, MW = a.c.max_windows;
     const int64_t total = 2 * item_count(a.n_prom, a.batch, LG);
+    const int tid = threadIdx.x;
     for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
         const int kv = (int)(it & 1);
         int b, e, lg;
@@ -603,55 +608,62 @@ __global__ void __launch_bounds__(kPromThreads) tier_promote_kernel(const TierAr
             reinterpret_cast<const unsigned char*>(a.c.ledger) +
             ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES +
             (kv ? Lay::VC : Lay::KC));
-        for (int u = threadIdx.x; u < HALF / 16; u += blockDim.x)
+        for (int u = tid; u < HALF / 16; u += blockDim.x)
             cp_async16(reinterpret_cast<uint4*>(led_s) + u, led + u);
         cp_async_wait_all();
         __syncthreads();
         const uint32_t* cw = reinterpret_cast<const uint32_t*>(led_s);
-        const __half* sc16 = reinterpret_cast<const __half*>(led_s + (Lay::KS - Lay::KC));
-        const __half* zc16 = reinterpret_cast<const __half*>(led_s + (Lay::KZ - Lay::KC));
-        uint4* pool = reinterpret_cast<uint4*>(kv ? a.c.v_pool : a.c.k_pool);
-        for (int u = threadIdx.x; u < kTierW * (D / 8); u += blockDim.x) {
-            const int tok = u / (D / 8), c0 = (u % (D / 8)) * 8;
-            const int page = pages[tok / kTile];
-            if (page < 0) continue;   // no page could be taken for this promotion
-            const int ti = tok >> 4;
-            uint32_t packed[4];
-            if (kv == 0) {
-                // channels c0 + 2 t + e: lane 4 gg + t, register 4 s + 2 i + h, half e
-                const int gg = tok & 7, i = (tok >> 3) & 1, s4 = c0 >> 4, h = (c0 >> 3) & 1;
-                const int reg = 4 * s4 + 2 * i + h;
-                const int grp = tok / kQGroup;
+        const __half2* sc2 = reinterpret_cast<const __half2*>(led_s + (Lay::KS - Lay::KC));
+        const __half2* zc2 = reinterpret_cast<const __half2*>(led_s + (Lay::KZ - Lay::KC));
+        uint32_t* pool = reinterpret_cast<uint32_t*>(kv ? a.c.v_pool : a.c.k_pool);
+        const int p = tid & 63;   // channel pair 2p, 2p + 1
+        const int q4 = tid >> 6;  // key group / quarter of the window: pages 2 q4, 2 q4 + 1
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint32_t x = cw[ti * D + (4 * gg + t) * WPL + (reg >> 3)];
-                    const int k = Lay::key_scale_index(grp, c0 + 2 * t);
-                    const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(sc16 + k));
-                    const float2 zf = __half22float2(*reinterpret_cast<const __half2*>(zc16 + k));
-                    const float v0 = fmaf((float)code_of_bits(x, Lay::sign_bit(reg, 0), Lay::mag_bit(reg, 0)), sf.x, zf.x);
-                    const float v1 = fmaf((float)code_of_bits(x, Lay::sign_bit(reg, 1), Lay::mag_bit(reg, 1)), sf.y, zf.y);
-                    const __nv_bfloat162 bb = __floats2bfloat162_rn(v0, v1);
-                    packed[t] = *reinterpret_cast<const uint32_t*>(&bb);
+        for (int pg = 0; pg < 2; ++pg) {
+            const int page = pages[2 * q4 + pg];
+            if (page < 0) continue;   // no page could be taken for this promotion
+            uint32_t* dst = pool + ((((int64_t)page * a.n_layers + l) * a.n_kv + g) * kTile) * D / 2 + p;
+            const uint32_t* cwt = cw + (2 * q4 + pg) * D;   // code words of this 16-token tile
+            if (kv == 0) {
+                // keys: channels 2p, 2p + 1 of token 16 (2 q4 + pg) + r: register
+                // 4 s + 2 i + h of lane 4 (r & 7) + t
+                const int t = p & 3, s4 = p >> 3, h = (p >> 2) & 1;
+                const int k = Lay::key_scale_index(q4, 2 * p);
+                const float2 sf = __half22float2(sc2[k / 2]), zf = __half22float2(zc2[k / 2]);
+                const uint32_t* cwl = cwt + t * WPL + (s4 >> 1);
+                const int rot0 = 2 * (4 * (s4 & 1) + h);
+#pragma unroll
+                for (int r = 0; r < kTile; ++r) {
+                    const int i = r >> 3;
+                    const uint32_t wd = cwl[4 * (r & 7) * WPL];
+                    const float2 c = reg_codes(__funnelshift_r(wd, wd, rot0 + 4 * i));
+                    const __nv_bfloat162 bb = __floats2bfloat162_rn(fmaf(c.x, sf.x, zf.x),
+                                                                    fmaf(c.y, sf.y, zf.y));
+                    dst[r * (D / 2)] = *reinterpret_cast<const uint32_t*>(&bb);
                 }
             } else {
-                // channels c0 + gg: lane 4 gg + t, register 2 j + h, half e (token parity)
-                const int h = (tok >> 3) & 1, t = (tok & 7) >> 1, e2 = tok & 1;
-                const int reg = 2 * (c0 >> 3) + h;
-                const int k = Lay::value_scale_index(tok, c0 / kQGroup);
-                const float sf = __half2float(sc16[k]), zf = __half2float(zc16[k]);
-                const int sb = Lay::sign_bit(reg, e2), mb = Lay::mag_bit(reg, e2);
+                // values: channels c0 = 2p, 2p + 1 (lanes 4 gg + t, 4 (gg + 1) + t) of the
+                // token pair 16 (2 q4 + pg) + 2 kk (+1): register 2 j + h, h = kk / 4, t = kk % 4
+                const int c0 = 2 * p, j = c0 >> 3, gg = c0 & 7, cg = c0 / kQGroup;
+                const uint32_t* cwl = cwt + 4 * gg * WPL + (j >> 2);
+                const int rot0 = 2 * (2 * (j & 3));
 #pragma unroll
-                for (int gp = 0; gp < 4; ++gp) {
-                    const uint32_t x0 = cw[ti * D + (4 * (2 * gp) + t) * WPL + (reg >> 3)];
-                    const uint32_t x1 = cw[ti * D + (4 * (2 * gp + 1) + t) * WPL + (reg >> 3)];
-                    const float v0 = fmaf((float)code_of_bits(x0, sb, mb), sf, zf);
-                    const float v1 = fmaf((float)code_of_bits(x1, sb, mb), sf, zf);
-                    const __nv_bfloat162 bb = __floats2bfloat162_rn(v0, v1);
-                    packed[gp] = *reinterpret_cast<const uint32_t*>(&bb);
+                for (int kk = 0; kk < kTile / 2; ++kk) {
+                    const int h = kk >> 2, t = kk & 3;
+                    const uint32_t w0 = cwl[t * WPL];
+                    const uint32_t w1 = cwl[(4 + t) * WPL];
+                    const float2 ca = reg_codes(__funnelshift_r(w0, w0, rot0 + 2 * h));   // channel c0
+                    const float2 cb = reg_codes(__funnelshift_r(w1, w1, rot0 + 2 * h));   // channel c0 + 1
+                    const int kq = Lay::value_scale_index(16 * (2 * q4 + pg) + 2 * kk, cg);
+                    const float2 sf = __half22float2(sc2[kq / 2]), zf = __half22float2(zc2[kq / 2]);
+                    const __nv_bfloat162 r0 = __floats2bfloat162_rn(fmaf(ca.x, sf.x, zf.x),
+                                                                    fmaf(cb.x, sf.x, zf.x));
+                    const __nv_bfloat162 r1 = __floats2bfloat162_rn(fmaf(ca.y, sf.y, zf.y),
+                                                                    fmaf(cb.y, sf.y, zf.y));
+                    dst[(2 * kk) * (D / 2)] = *reinterpret_cast<const uint32_t*>(&r0);
+                    dst[(2 * kk + 1) * (D / 2)] = *reinterpret_cast<const uint32_t*>(&r1);
                 }
             }
-            const size_t r = (((size_t)page * a.n_layers + l) * a.n_kv + g) * kTile + tok % kTile;
-            pool[(r * D + c0) / 8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
         __syncthreads();
     }
