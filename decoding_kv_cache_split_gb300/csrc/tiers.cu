@@ -405,12 +405,13 @@ __device__ __forceinline__ void item_at(const int32_t* n, int batch, int LG, int
 // 3 * 2^-24 relative of the exact quotient, so within 2^-19 of y while it is
 // below 8 in magnitude; only within 2^-16 of a threshold can it fall on the
 // other side of one than y does, and there the quotient is divided out
-// exactly.
+// exactly (out of line: the rare path stays out of the unrolled loops).
+__device__ __noinline__ float exact_quotient(float d, float sc) { return __fdiv_rn(d, sc); }
 __device__ __forceinline__ uint32_t int2_bits(float x, float z, float sc, float r) {
     const float d = __fsub_rn(x, z);
     float y = __fmul_rn(d, r);
     const float dc = fabsf(y - 1.5f);
-    if (dc <= 0x1p-16f || fabsf(dc - 1.f) <= 0x1p-16f) y = __fdiv_rn(d, sc);
+    if (dc <= 0x1p-16f || fabsf(dc - 1.f) <= 0x1p-16f) y = exact_quotient(d, sc);
     return (uint32_t)(y < 1.5f) | ((uint32_t)(y <= 0.5f || y > 2.5f) << 1);
 }
 // A pair of codes as bytes (bits 0, 1: first code; 8, 9: second) -> the
@@ -423,13 +424,14 @@ __device__ __forceinline__ uint32_t pair_reg_bits(uint32_t x) {
 
 // Quantization of one half (keys or values) of a (window, layer, KV head)
 // item: the window's 128 rows are staged in shared memory (rows padded by 16
-// bytes so row-strided reads spread over the banks); keys are quantized per
-// channel (a thread per channel and 32-token group), values per token (a
-// thread per token and 32-channel group), a byte of sign / magnitude bits
-// per code; then each thread packs ledger words from code pairs.
+// bytes so row-strided reads spread over the banks).  Keys: a thread per
+// channel pair and 32-token group (min / max on bf16 pairs); values: a
+// thread per token and 32-channel group.  Each thread turns its codes into
+// the sign / magnitude bits of their ledger registers, and the threads
+// whose bits share a ledger word OR them together with two shuffles; one of
+// them stores the word.
 constexpr int kQuantThreads = 256;
 constexpr int kRowPad = 8;     // bf16 elements of padding per staged row
-constexpr int kCodePad = 4;    // bytes of padding per code row
 
 template <int D>
 __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const TierArgs a,
@@ -440,12 +442,11 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
     constexpr int XS = D + kRowPad;                 // staged row stride (elements)
     extern __shared__ __align__(16) unsigned char qsm[];
     __nv_bfloat16* xt = reinterpret_cast<__nv_bfloat16*>(qsm);            // [128][XS]
-    uint8_t* codes = reinterpret_cast<uint8_t*>(xt + kTierW * XS);         // [128 or D][+pad]
     (void)max_items;
     griddep_wait();
     griddep_release();
     const int LG = a.n_layers * a.n_kv, MW = a.c.max_windows;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t total = 2 * item_count(a.n_quant, a.batch, LG);
     for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
         const int kv = (int)(it & 1);
@@ -459,108 +460,115 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
         // stage: page i holds tokens 16 i .. 16 i + 15 of the window, rows contiguous
         constexpr int kChunks = kTile * D / 8;   // 16-byte chunks per page row block
         const uint4* pool = reinterpret_cast<const uint4*>(kv ? a.c.v_pool : a.c.k_pool);
-        for (int u = tid; u < PW * kChunks; u += blockDim.x) {
-            const int pi = u / kChunks, c = u % kChunks;
-            const int row = pi * kTile + c / (D / 8), col = c % (D / 8);
-            const size_t off = ((((size_t)pages[pi] * a.n_layers + l) * a.n_kv + g) * kTile) * D / 8 + c;
-            cp_async16(reinterpret_cast<uint4*>(xt + row * XS) + col, pool + off);
+#pragma unroll
+        for (int pi = 0; pi < PW; ++pi) {
+            const uint4* src = pool + ((((size_t)pages[pi] * a.n_layers + l) * a.n_kv + g) * kTile) * D / 8;
+#pragma unroll
+            for (int k = 0; k < kChunks / kQuantThreads; ++k) {
+                const int c = tid + k * kQuantThreads;
+                cp_async16(reinterpret_cast<uint4*>(xt + (pi * kTile + c / (D / 8)) * XS) + c % (D / 8),
+                           src + c);
+            }
         }
         cp_async_wait_all();
         __syncthreads();
         uint32_t* words = reinterpret_cast<uint32_t*>(led + (kv ? Lay::VC : Lay::KC));
         if (kv == 0) {
-            // keys: per channel over 32-token groups; codes[token][channel]
-            constexpr int CS = D + kCodePad;
-            __half* ks = reinterpret_cast<__half*>(led + Lay::KS);
-            __half* kz = reinterpret_cast<__half*>(led + Lay::KZ);
-            for (int u = tid; u < D * (kTierW / kQGroup); u += blockDim.x) {
-                const int c = u % D, grp = u / D;
-                float mn = INFINITY, mx = -INFINITY;
-#pragma unroll 8
-                for (int i = 0; i < kQGroup; ++i) {
-                    const float x = __bfloat162float(xt[(grp * kQGroup + i) * XS + c]);
-                    mn = fminf(mn, x);
-                    mx = fmaxf(mx, x);
-                }
-                const __half z16 = __float2half_rn(mn);
-                const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-                const float z = __half2float(z16), sc = __half2float(s16);
-                ks[Lay::key_scale_index(grp, c)] = s16;
-                kz[Lay::key_scale_index(grp, c)] = z16;
-                const float r = sc == 0.f ? 0.f : __frcp_rn(sc);
-#pragma unroll 8
-                for (int i = 0; i < kQGroup; ++i) {
-                    const float x = __bfloat162float(xt[(grp * kQGroup + i) * XS + c]);
-                    codes[(grp * kQGroup + i) * CS + c] = sc == 0.f ? 3 : (uint8_t)int2_bits(x, z, sc, r);
-                }
-            }
-            __syncthreads();
-            // word (tile ti, lane 4 gg + t, wq): register 8 wq + slot holds the key
-            // codes of token 16 ti + 8 i + gg, channels 16 s + 8 h + 2 t (+1)
-            for (int u = tid; u < (kTierW / kTile) * 32 * WPL; u += blockDim.x) {
-                const int ti = u / (32 * WPL), lane = (u / WPL) % 32, wq = u % WPL;
-                const int gg = lane >> 2, t = lane & 3;
-                uint32_t word = 0;
+            // keys: channels 2p, 2p + 1 over group grp (tokens 32 grp .. + 31)
+            const int p = 32 * (warp & 1) + lane, grp = warp >> 1;
+            const __nv_bfloat162* col =
+                reinterpret_cast<const __nv_bfloat162*>(xt + grp * kQGroup * XS) + p;
+            __nv_bfloat162 mn2 = col[0], mx2 = col[0];
 #pragma unroll
-                for (int slot = 0; slot < 8; ++slot) {
-                    const int s4 = 2 * wq + (slot >> 2), i = (slot >> 1) & 1, h = slot & 1;
-                    const uint32_t x = *reinterpret_cast<const uint16_t*>(
-                        codes + (16 * ti + 8 * i + gg) * CS + 16 * s4 + 8 * h + 2 * t);
-                    word |= __funnelshift_l(pair_reg_bits(x), pair_reg_bits(x), 2 * slot);
-                }
-                words[u] = word;
+            for (int r = 1; r < kQGroup; ++r) {
+                mn2 = __hmin2(mn2, col[r * (XS / 2)]);
+                mx2 = __hmax2(mx2, col[r * (XS / 2)]);
             }
+            const float2 mn = __bfloat1622float2(mn2), mx = __bfloat1622float2(mx2);
+            const __half2 z16 = __floats2half2_rn(mn.x, mn.y);
+            const __half2 s16 = __floats2half2_rn(__fdiv_rn(__fsub_rn(mx.x, mn.x), 3.0f),
+                                                  __fdiv_rn(__fsub_rn(mx.y, mn.y), 3.0f));
+            const float2 z = __half22float2(z16), sc = __half22float2(s16);
+            const int k = Lay::key_scale_index(grp, 2 * p);
+            reinterpret_cast<__half2*>(led + Lay::KS)[k / 2] = s16;
+            reinterpret_cast<__half2*>(led + Lay::KZ)[k / 2] = z16;
+            const float r0 = sc.x == 0.f ? 0.f : __frcp_rn(sc.x);
+            const float r1 = sc.y == 0.f ? 0.f : __frcp_rn(sc.y);
+            // register 4 s + 2 i + h of lane 4 gg + t (token 8 i + gg of its tile):
+            // word wq = s / 2, slot 4 (s & 1) + 2 i + h; the 4 threads p with the
+            // same t and s / 2 (lanes xor 4, xor 8) fill one word's 8 slots
+            const int t = p & 3, s4 = p >> 3, h = (p >> 2) & 1;
+            const int rot0 = 2 * (4 * (s4 & 1) + h);
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+                for (int gg = 0; gg < 8; ++gg) {
+                    uint32_t word = 0;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const float2 x = __bfloat1622float2(col[(16 * tt + 8 * i + gg) * (XS / 2)]);
+                        const uint32_t b0 = sc.x == 0.f ? 3u : int2_bits(x.x, z.x, sc.x, r0);
+                        const uint32_t b1 = sc.y == 0.f ? 3u : int2_bits(x.y, z.y, sc.y, r1);
+                        const uint32_t bits = pair_reg_bits(b0 | (b1 << 8));
+                        word |= __funnelshift_l(bits, bits, rot0 + 4 * i);
+                    }
+                    word |= __shfl_xor_sync(0xffffffffu, word, 4);
+                    word |= __shfl_xor_sync(0xffffffffu, word, 8);
+                    if ((lane & 12) == 0)
+                        words[(2 * grp + tt) * D + (4 * gg + t) * WPL + (s4 >> 1)] = word;
+                }
         } else {
-            // values: per token over 32-channel groups; codes[channel][token]
-            constexpr int CS = kTierW + kCodePad;
-            __half* vs = reinterpret_cast<__half*>(led + Lay::VS);
-            __half* vz = reinterpret_cast<__half*>(led + Lay::VZ);
-            for (int u = tid; u < kTierW * NG; u += blockDim.x) {
-                const int tok = u % kTierW, cg = u / kTierW;
-                const uint4* row = reinterpret_cast<const uint4*>(xt + tok * XS + cg * kQGroup);
-                float xs[kQGroup];
+            // values: token tok over channel groups cg and cg + 2; the codes of
+            // channel 8 j + gg sit in register 2 j + h of lane 4 gg + t, half e,
+            // for token 2 t + 8 h + e of the tile: the lanes xor 1 and xor 8
+            // (tokens e and h) fill one word's 8 slots with the 4 j of a group
+            const int tok = tid & 127;
+            const int e2 = tok & 1, t = (tok & 7) >> 1, hh = (tok >> 3) & 1, ti = tok >> 4;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int cg = (tid >> 7) + 2 * half;
+                const __nv_bfloat162* row =
+                    reinterpret_cast<const __nv_bfloat162*>(xt + tok * XS + cg * kQGroup);
+                __nv_bfloat162 v2[kQGroup / 2];
 #pragma unroll
                 for (int k = 0; k < kQGroup / 8; ++k) {
-                    const uint4 q4 = row[k];
-                    const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        xs[8 * k + 2 * m] = __uint_as_float(wv[m] << 16);
-                        xs[8 * k + 2 * m + 1] = __uint_as_float(wv[m] & 0xffff0000u);
-                    }
+                    const uint4 q4 = reinterpret_cast<const uint4*>(row)[k];
+                    v2[4 * k] = *reinterpret_cast<const __nv_bfloat162*>(&q4.x);
+                    v2[4 * k + 1] = *reinterpret_cast<const __nv_bfloat162*>(&q4.y);
+                    v2[4 * k + 2] = *reinterpret_cast<const __nv_bfloat162*>(&q4.z);
+                    v2[4 * k + 3] = *reinterpret_cast<const __nv_bfloat162*>(&q4.w);
                 }
-                float mn = xs[0], mx = xs[0];
+                __nv_bfloat162 mn2 = v2[0], mx2 = v2[0];
 #pragma unroll
-                for (int i = 1; i < kQGroup; ++i) {
-                    mn = fminf(mn, xs[i]);
-                    mx = fmaxf(mx, xs[i]);
+                for (int i = 1; i < kQGroup / 2; ++i) {
+                    mn2 = __hmin2(mn2, v2[i]);
+                    mx2 = __hmax2(mx2, v2[i]);
                 }
-                const __half z16 = __float2half_rn(mn);
-                const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+                const float mnf = fminf(__low2float(mn2), __high2float(mn2));
+                const float mxf = fmaxf(__low2float(mx2), __high2float(mx2));
+                const __half z16 = __float2half_rn(mnf);
+                const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mxf, mnf), 3.0f));
                 const float z = __half2float(z16), sc = __half2float(s16);
-                vs[Lay::value_scale_index(tok, cg)] = s16;
-                vz[Lay::value_scale_index(tok, cg)] = z16;
+                reinterpret_cast<__half*>(led + Lay::VS)[Lay::value_scale_index(tok, cg)] = s16;
+                reinterpret_cast<__half*>(led + Lay::VZ)[Lay::value_scale_index(tok, cg)] = z16;
                 const float r = sc == 0.f ? 0.f : __frcp_rn(sc);
+                // channel 32 cg + 8 jj + gg -> register 2 (4 cg + jj) + hh: word cg,
+                // slot 2 jj + hh, half e2
 #pragma unroll
-                for (int i = 0; i < kQGroup; ++i)
-                    codes[(cg * kQGroup + i) * CS + tok] =
-                        sc == 0.f ? 3 : (uint8_t)int2_bits(xs[i], z, sc, r);
-            }
-            __syncthreads();
-            // word (tile ti, lane 4 gg + t, wq): register 8 wq + slot holds the value
-            // codes of tokens 16 ti + 8 h + 2 t (+1), channel 8 j + gg
-            for (int u = tid; u < (kTierW / kTile) * 32 * WPL; u += blockDim.x) {
-                const int ti = u / (32 * WPL), lane = (u / WPL) % 32, wq = u % WPL;
-                const int gg = lane >> 2, t = lane & 3;
-                uint32_t word = 0;
+                for (int gg = 0; gg < 8; ++gg) {
+                    uint32_t word = 0;
 #pragma unroll
-                for (int slot = 0; slot < 8; ++slot) {
-                    const int j = 4 * wq + (slot >> 1), h = slot & 1;
-                    const uint32_t x = *reinterpret_cast<const uint16_t*>(
-                        codes + (8 * j + gg) * CS + 16 * ti + 8 * h + 2 * t);
-                    word |= __funnelshift_l(pair_reg_bits(x), pair_reg_bits(x), 2 * slot);
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int c = 8 * jj + gg;
+                        const float x = (c & 1) ? __high2float(v2[c >> 1]) : __low2float(v2[c >> 1]);
+                        const uint32_t bits = pair_reg_bits((sc == 0.f ? 3u : int2_bits(x, z, sc, r)) << (8 * e2));
+                        word |= __funnelshift_l(bits, bits, 2 * (2 * jj + hh));
+                    }
+                    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+                    word |= __shfl_xor_sync(0xffffffffu, word, 8);
+                    if ((lane & 9) == 0)
+                        words[ti * D + (4 * gg + t) * WPL + cg] = word;
                 }
-                words[u] = word;
             }
         }
         __syncthreads();
@@ -714,7 +722,7 @@ cudaError_t launch_tier_quantize(const TierArgs& a, int max_items, int num_sms, 
     if (max_items <= 0) return cudaSuccess;
     if (a.head_dim != 128) return cudaErrorInvalidValue;
     auto kern = tier_quantize_kernel<128>;
-    const int smem = kTierW * (128 + kRowPad) * 2 + 128 * (kTierW + kCodePad);
+    const int smem = kTierW * (128 + kRowPad) * 2;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t items = 2LL * a.batch * max_items * a.n_layers * a.n_kv;
