@@ -58,6 +58,33 @@ __device__ __forceinline__ uint32_t code_reg(uint32_t w, int slot) {
 __device__ __forceinline__ float2 h2f(uint32_t w) {
     return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
+// Two independent fp32 operations in one instruction (each correctly
+// rounded, as the scalar ones).
+__device__ __forceinline__ uint64_t pk2(float2 a) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+    return r;
+}
+__device__ __forceinline__ float2 up2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)), "l"(pk2(c)));
+    return up2(r);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)));
+    return up2(r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)));
+    return up2(r);
+}
 
 // The 16 x 8 x 16 tensor-core tile has 8 A rows and a group has 4 query
 // heads, so rows 0-3 carry the bf16 "hi" part of each head's operand and
@@ -108,14 +135,16 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
     };
     // the lane's half (hi or lo) of a product pair: hi rows round the pair to
     // bf16, lo rows round what the hi part leaves
-    auto half_pair = [&](float x0v, float x1v) -> uint32_t {
-        const uint32_t hi = pack_bf16x2(x0v, x1v);
-        return pack_bf16x2(fmaf(-lom, bf16_lo(hi), x0v), fmaf(-lom, bf16_hi(hi), x1v));
+    const float2 nlom = make_float2(-lom, -lom);
+    auto half_pair = [&](float2 xv) -> uint32_t {
+        const uint32_t hi = pack_bf16x2(xv.x, xv.y);
+        const float2 r = fma2(nlom, make_float2(bf16_lo(hi), bf16_hi(hi)), xv);
+        return pack_bf16x2(r.x, r.y);
     };
 
     uint32_t qa[KS][2];                      // Q * 2^96 (bf16x2) of the lane's head
-    float o[NB][2];                          // hi or lo part of O[head][8j + 2t, +1] * 2^-31
-    float vbias[NG];                         // the lane's share of sum_i p_i z'_ig
+    float2 o[NB];                            // hi or lo part of O[head][8j + 2t, +1] * 2^-31
+    float2 vbias[NG];                        // the lane's share of sum_i p_i z'_ig (2 parts)
     float m_run = -INFINITY, l_run = 0.f;
     int64_t cur_row = -1;
 
@@ -126,18 +155,19 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
         float vb[NG];
 #pragma unroll
         for (int c = 0; c < NG; ++c) {
-            vb[c] = vbias[c] + __shfl_xor_sync(kFull, vbias[c], 1);
+            vb[c] = vbias[c].x + vbias[c].y;
+            vb[c] += __shfl_xor_sync(kFull, vb[c], 1);
             vb[c] += __shfl_xor_sync(kFull, vb[c], 2);
         }
         const int64_t slot = (int64_t)w + row;
         float* po = a.part_o + ((size_t)slot * G + head) * D;
 #pragma unroll
         for (int j = 0; j < NB; ++j) {
-            const float v0 = o[j][0] + __shfl_xor_sync(kFull, o[j][0], 16);
-            const float v1 = o[j][1] + __shfl_xor_sync(kFull, o[j][1], 16);
+            const float2 v = make_float2(o[j].x + __shfl_xor_sync(kFull, o[j].x, 16),
+                                         o[j].y + __shfl_xor_sync(kFull, o[j].y, 16));
             if (!lo_row)
                 *reinterpret_cast<float2*>(po + 8 * j + 2 * t) =
-                    make_float2(fmaf(v0, kProdScale, vb[j / 4]), fmaf(v1, kProdScale, vb[j / 4]));
+                    fma2(v, make_float2(kProdScale, kProdScale), make_float2(vb[j / 4], vb[j / 4]));
         }
         if (!lo_row && t == 0) {
             float* pml = a.part_ml + ((size_t)slot * G + head) * 2;
@@ -172,9 +202,9 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                     qa[s][h] = pack_bf16x2(bf16_lo(qw) * kAScale, bf16_hi(qw) * kAScale);
                 }
 #pragma unroll
-            for (int j = 0; j < NB; ++j) o[j][0] = o[j][1] = 0.f;
+            for (int j = 0; j < NB; ++j) o[j] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < NG; ++c) vbias[c] = 0.f;
+            for (int c = 0; c < NG; ++c) vbias[c] = make_float2(0.f, 0.f);
             m_run = -INFINITY;
             l_run = 0.f;
         }
@@ -192,7 +222,7 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                 // A' = q * s * 2^96 of this group's key scales (the lane's hi or
                 // lo part), and the key bias sum_c q_c (z_c + 1.5 s_c) * 2^96
                 uint32_t af[KS][2];
-                float kb = 0.f;
+                float2 kb2 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int s2 = 0; s2 < KS / 2; ++s2) {
                     const uint4 sw = ks4[grp * (D / 8) + s2], zw = kz4[grp * (D / 8) + s2];
@@ -202,12 +232,12 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                     for (int k = 0; k < 4; ++k) {   // (s, h) = (2 s2 + k / 2, k % 2)
                         const int s = 2 * s2 + k / 2, h = k % 2;
                         const float2 sc = h2f(sws[k]), zc = h2f(zws[k]);
-                        const float q0 = bf16_lo(qa[s][h]), q1 = bf16_hi(qa[s][h]);
-                        af[s][h] = half_pair(q0 * sc.x, q1 * sc.y);
-                        kb = fmaf(q0, fmaf(1.5f, sc.x, zc.x), kb);
-                        kb = fmaf(q1, fmaf(1.5f, sc.y, zc.y), kb);
+                        const float2 q01 = make_float2(bf16_lo(qa[s][h]), bf16_hi(qa[s][h]));
+                        af[s][h] = half_pair(mul2(q01, sc));
+                        kb2 = fma2(q01, fma2(make_float2(1.5f, 1.5f), sc, zc), kb2);
                     }
                 }
+                float kb = kb2.x + kb2.y;
                 kb += __shfl_xor_sync(kFull, kb, 1);
                 kb += __shfl_xor_sync(kFull, kb, 2);
                 kb *= kb_scale;
@@ -230,12 +260,16 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                         }
                     float sc[2][2];
 #pragma unroll
-                    for (int i = 0; i < 2; ++i)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const float part = acc[0][i][e] + acc[1][i][e];
-                            sc[i][e] = fmaf(part + __shfl_xor_sync(kFull, part, 16), acc_scale, kb);
-                        }
+                    for (int i = 0; i < 2; ++i) {
+                        float2 part = add2(make_float2(acc[0][i][0], acc[0][i][1]),
+                                           make_float2(acc[1][i][0], acc[1][i][1]));
+                        part = add2(part, make_float2(__shfl_xor_sync(kFull, part.x, 16),
+                                                      __shfl_xor_sync(kFull, part.y, 16)));
+                        const float2 v = fma2(part, make_float2(acc_scale, acc_scale),
+                                              make_float2(kb, kb));
+                        sc[i][0] = v.x;
+                        sc[i][1] = v.y;
+                    }
                     // ---- online softmax of the head
                     float mt = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
                     mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
@@ -245,12 +279,9 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                         m_run = mt;
                         l_run *= f;
 #pragma unroll
-                        for (int j = 0; j < NB; ++j) {
-                            o[j][0] *= f;
-                            o[j][1] *= f;
-                        }
+                        for (int j = 0; j < NB; ++j) o[j] = mul2(o[j], make_float2(f, f));
 #pragma unroll
-                        for (int c = 0; c < NG; ++c) vbias[c] *= f;
+                        for (int c = 0; c < NG; ++c) vbias[c] = mul2(vbias[c], make_float2(f, f));
                     }
                     float pv[4];
 #pragma unroll
@@ -275,27 +306,24 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                     const uint4 z0 = vz4[ti * 8], z1 = vz4[ti * 8 + 1];
                     const uint32_t s0w[4] = {s0.x, s0.y, s0.z, s0.w}, s1w[4] = {s1.x, s1.y, s1.z, s1.w};
                     const uint32_t z0w[4] = {z0.x, z0.y, z0.z, z0.w}, z1w[4] = {z1.x, z1.y, z1.z, z1.w};
-                    float ps[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) ps[k] = pv[k] * kAScale;
+                    const float2 p01 = make_float2(pv[0], pv[1]), p23 = make_float2(pv[2], pv[3]);
+                    const float2 ps01 = mul2(p01, make_float2(kAScale, kAScale));
+                    const float2 ps23 = mul2(p23, make_float2(kAScale, kAScale));
 #pragma unroll
                     for (int cg = 0; cg < NG; ++cg) {
                         const float2 sa = h2f(s0w[cg]), sb = h2f(s1w[cg]);
                         const float2 za = h2f(z0w[cg]), zb = h2f(z1w[cg]);
-                        float vb = vbias[cg];
-                        vb = fmaf(pv[0], fmaf(1.5f, sa.x, za.x), vb);
-                        vb = fmaf(pv[1], fmaf(1.5f, sa.y, za.y), vb);
-                        vb = fmaf(pv[2], fmaf(1.5f, sb.x, zb.x), vb);
-                        vb = fmaf(pv[3], fmaf(1.5f, sb.y, zb.y), vb);
-                        vbias[cg] = vb;
-                        const uint32_t pa0 = half_pair(ps[0] * sa.x, ps[1] * sa.y);
-                        const uint32_t pa2 = half_pair(ps[2] * sb.x, ps[3] * sb.y);
+                        const float2 k15 = make_float2(1.5f, 1.5f);
+                        vbias[cg] = fma2(p01, fma2(k15, sa, za), vbias[cg]);
+                        vbias[cg] = fma2(p23, fma2(k15, sb, zb), vbias[cg]);
+                        const uint32_t pa0 = half_pair(mul2(ps01, sa));
+                        const uint32_t pa2 = half_pair(mul2(ps23, sb));
 #pragma unroll
                         for (int jj = 0; jj < kQGroup / 8; ++jj) {
                             const int j = cg * (kQGroup / 8) + jj;      // 8-channel block
                             const uint32_t b0 = code_reg(vw[cg], 2 * jj);
                             const uint32_t b1 = code_reg(vw[cg], 2 * jj + 1);
-                            mma_rows8(o[j][0], o[j][1], pa0, pa2, b0, b1);
+                            mma_rows8(o[j].x, o[j].y, pa0, pa2, b0, b1);
                         }
                     }
                 }
