@@ -246,6 +246,8 @@ def main():
     ap.add_argument("--impl", default="kvev", choices=["kvev", "reference"])
     ap.add_argument("--cpu-layers", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay timing of the headline pass")
     ap.add_argument("--mode-steps", type=int, default=256,
                     help="decode steps of each (alpha, refresh mode) run reported under 'modes' "
                          "(0: skip)")
@@ -340,6 +342,30 @@ def main():
     launches = kvev.kvev_launch_count(ep.ctx) - n0
     ms = e0.elapsed_time(e1) / args.steps
     ms = slowest_ms(ms, dist)
+
+    # The same pass captured once in a CUDA graph (re-setting the context's host
+    # state, the state reset and step 1 against the untouched prefill) and
+    # replayed: launch overhead off the host, same outputs bit for bit.
+    graph_us = None
+    if not args.no_graph:
+        ref_out = ep.out.clone()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            ep.begin(L0, torch.cuda.current_stream())
+            ep.step(qd, knd, vnd, torch.cuda.current_stream())
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        kvev.kvev_sync(ep.ctx)
+        graph_us = g0.elapsed_time(g1) / args.steps * 1e3
+        assert torch.equal(ep.out, ref_out), "graph replay differs from the eager step"
+        del g
 
     # Per-kernel region: CUDA events around every launch, on the launching stream.
     kvev.kvev_profile(ep.ctx, True)
@@ -463,6 +489,7 @@ def main():
             "kernels_us": kernels_us,
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "graph": ({"us_per_step": round(graph_us, 2), "replays": args.steps} if graph_us else None),
             "gpu_launches": launches,
             "clocks": clk,
             "cpu_baseline": cpu,
