@@ -18,6 +18,7 @@ import pytest
 from oracle import qevict as QE
 from workloads import Geometry, Workload
 
+from ledger_codec import decode_ledger
 from parity import OUT_RTOL, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
@@ -53,51 +54,6 @@ def load(tp, K, V, L0):
             allp = np.concatenate([sink[None], pages], axis=0)
             pool[b * tp.pps:b * tp.pps + 1 + n_pages].copy_(
                 torch.from_numpy(np.ascontiguousarray(allp).view(np.int16)).view(torch.bfloat16))
-
-
-def decode_ledger(entry: np.ndarray, d: int = 128):
-    """Codes and fp16 scale/zero of one device ledger entry (12288 bytes).
-
-    The entry is laid out for the attention kernel's tensor-core fragments:
-    per 16-token tile, lane 4 g + t owns 4 consecutive code words; a word
-    holds 8 registers (slot = register % 8) of two codes (half e), each code
-    as a sign bit at (15 + 16 e + 2 slot) % 32 and a magnitude bit at
-    (6 + 16 e + 2 slot) % 32 (sign: code <= 1; magnitude: code 0 or 3)."""
-    W = 128
-    kc = entry[:4096].view(np.uint32)
-    ks_raw = entry[4096:5120].view(np.float16)
-    kz_raw = entry[5120:6144].view(np.float16)
-    vc = entry[6144:10240].view(np.uint32)
-    vs_raw = entry[10240:11264].view(np.float16)
-    vz_raw = entry[11264:12288].view(np.float16)
-    tok = np.arange(W)[:, None]
-    c = np.arange(d)[None, :]
-
-    def codes(words, lane, reg, e, ti):
-        word = ti * d + lane * (d // 32) + (reg >> 3)
-        slot = reg & 7
-        x = words[word]
-        sign = (x >> ((15 + 16 * e + 2 * slot) % 32)) & 1
-        mag = (x >> ((6 + 16 * e + 2 * slot) % 32)) & 1
-        return np.where(sign == 1, np.where(mag == 1, 0, 1), np.where(mag == 1, 3, 2)).astype(np.uint8)
-
-    # keys: token 16 ti + 8 i + g, channel 16 s + 8 h + 2 t + e, register 4 s + 2 i + h
-    ti, i, g = tok >> 4, (tok >> 3) & 1, tok & 7
-    s_, h, t, e = c >> 4, (c >> 3) & 1, (c & 7) >> 1, c & 1
-    kq = codes(kc, 4 * g + t, 4 * s_ + 2 * i + h, e, ti)
-    # values: token 16 ti + 8 h + 2 t + e, channel 8 j + g, register 2 j + h
-    ti, h, t, e = tok >> 4, (tok >> 3) & 1, (tok & 7) >> 1, tok & 1
-    j, g = c >> 3, c & 7
-    vq = codes(vc, 4 * g + t, 2 * j + h, e, ti)
-    # key scale / zero of (group, channel): group * d + t * d / 4 + 4 s + 2 h + e
-    grp = np.arange(W // 32)[:, None]
-    kidx = grp * d + ((c & 7) >> 1) * (d // 4) + 4 * (c >> 4) + 2 * ((c >> 3) & 1) + (c & 1)
-    ks, kz = ks_raw[kidx], kz_raw[kidx]
-    # value scale / zero of (token, channel group): ti * 64 + t * 16 + h * 8 + 2 cg + e
-    cg = np.arange(d // 32)[None, :]
-    vidx = (tok >> 4) * 64 + ((tok & 7) >> 1) * 16 + ((tok >> 3) & 1) * 8 + 2 * cg + (tok & 1)
-    vs, vz = vs_raw[vidx], vz_raw[vidx]
-    return kq, ks, kz, vq, vs, vz
 
 
 def admissible(m: dict, dev_tiers: dict, tol: float):
