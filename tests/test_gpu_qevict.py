@@ -165,6 +165,39 @@ def test_tiers_no_quantized_tier_and_large_capacity():
     run_tiers(wl, 6, 0, 3, 12)
 
 
+def test_tiers_route_every_step():
+    """Omega 1: routing, first demotions, promotions and evictions at the end
+    of every step, with a needle that moves every 3 steps."""
+    wl = Workload(Geometry(2, 32, 8, 128, 2), 5 + 128 * 8 + 7, seed=21, needle=16,
+                  needle_period=3)
+    st = run_tiers(wl, 2, 3, 1, 16)
+    assert st["ledgers"] > 0 and st["promoted"] > 0
+
+
+def test_tiers_quantizer_exact_ties():
+    """Groups whose quotients (x - zero) / scale land exactly on 0.5, 1.5 and
+    2.5 (scale 1 and 2: min 0, max 3 or 6) in the keys of channels 0-15 and
+    the values of channel group 0, in every window: rint's ties to even
+    decide codes 0, 2, 2 on both sides (the quantizer's exact-division path)."""
+    wl = Workload(Geometry(2, 32, 8, 128, 1), 5 + 128 * 4 + 20, seed=12, needle=16,
+                  needle_period=8)
+    K, V = wl.prefill()      # cached arrays: edited in place for both sides
+    bf = {0: 0x0000, 0.5: 0x3F00, 1: 0x3F80, 1.5: 0x3FC0, 2: 0x4000, 2.5: 0x4020,
+          3: 0x4040, 5: 0x40A0, 6: 0x40C0}
+    pat1 = [0, 3, 0.5, 1.5, 2.5, 1, 2, 0.5] * 4             # scale 1
+    pat2 = [0, 6, 1, 3, 5, 2, 0, 6] * 4                     # scale 2: ties at 1, 3, 5
+    for w in range(4):
+        t0 = 5 + 128 * w
+        for i in range(32):
+            K[:, :, :, t0 + i, 0:8] = bf[pat1[i]]
+            K[:, :, :, t0 + i, 8:16] = bf[pat2[i]]
+        for i in range(16):
+            V[:, :, :, t0 + i, 0:32] = np.array([bf[x] for x in (pat1 if i % 2 else pat2)],
+                                                np.uint16)
+    st = run_tiers(wl, 1, 3, 4, 12)
+    assert st["ledgers"] > 0
+
+
 @pytest.mark.slow
 def test_tiers_full_size_first_routing_event():
     """The full two-tier workload on the device: 32 layers, 4 sequences of
