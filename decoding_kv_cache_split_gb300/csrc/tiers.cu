@@ -248,22 +248,37 @@ __global__ void __launch_bounds__(256) tier_score_kernel(const TierArgs a) {
     constexpr int PW = kTierW / kTile;
     float m = a.st.score[wi];
     const float inv_hq = 1.0f / (float)a.n_q, oma = 1.0f - a.alpha;
-    for (int l = 0; l < a.n_layers; ++l) {
-        float s = 0.f;
-        for (int k = lane; k < PW * a.n_kv; k += 32) {   // (tile, KV head) pairs
-            const int i = k % PW, g = k / PW;
-            const size_t row = ((size_t)l * a.batch + b) * a.n_kv + g;
-            const float2* st = a.tile_stats + (row * a.stats_tiles + (size_t)w * PW + i) * G;
-            const float* lse = a.lse2 + ((size_t)l * a.batch + b) * a.n_q + g * G;
+    // the layers' masses in batches of 8 (their loads are independent), then
+    // the EMA folded over them in layer order
+    constexpr int kLB = 8;
+    for (int l0 = 0; l0 < a.n_layers; l0 += kLB) {
+        float sl[kLB];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float2 v = st[h];
-                s = fmaf(exp2_approx(v.x - lse[h]), v.y, s);
+        for (int u = 0; u < kLB; ++u) {
+            const int l = l0 + u;
+            float s = 0.f;
+            if (l < a.n_layers) {
+#pragma unroll 2
+                for (int k = lane; k < PW * a.n_kv; k += 32) {   // (tile, KV head) pairs
+                    const int i = k % PW, g = k / PW;
+                    const size_t row = ((size_t)l * a.batch + b) * a.n_kv + g;
+                    const float2* st = a.tile_stats + (row * a.stats_tiles + (size_t)w * PW + i) * G;
+                    const float* lse = a.lse2 + ((size_t)l * a.batch + b) * a.n_q + g * G;
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float2 v = st[h];
+                        s = fmaf(exp2_approx(v.x - lse[h]), v.y, s);
+                    }
+                }
             }
+            sl[u] = s;
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        m = fmaf(a.alpha, s * inv_hq, oma * m);
+        for (int u = 0; u < kLB; ++u) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sl[u] += __shfl_xor_sync(0xffffffffu, sl[u], o);
+            if (l0 + u < a.n_layers) m = fmaf(a.alpha, sl[u] * inv_hq, oma * m);
+        }
     }
     if (lane == 0) a.st.score[wi] = m;
 }
