@@ -10,6 +10,8 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kvev_internal.h"
 
 namespace kvev {
@@ -48,6 +50,14 @@ enum {
 
 // Target size of the logits of one group of layers (see kvev_step).
 constexpr int64_t kLogitGroupBytes = int64_t(1) << 40;
+
+// An NVTX range around each step-level call (free when no tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 struct Workspace {
     float* logits = nullptr;
@@ -94,7 +104,15 @@ struct Workspace {
     float* part_o2 = nullptr;         // INT2 attention partials
     float* part_ml2 = nullptr;
     size_t bytes = 0;
+    // a guard band of kGuardBytes follows every region: its offset and the
+    // region's name (checked by kvev_check_scratch)
+    static constexpr int kMaxRegions = 64;
+    size_t guard_off[kMaxRegions] = {};
+    const char* guard_name[kMaxRegions] = {};
+    int n_guard = 0;
 };
+constexpr size_t kGuardBytes = 256;
+constexpr unsigned char kGuardByte = 0xA5;
 
 // Lays out (or, with base == nullptr, only sizes) the context's scratch.
 int tier_max_windows(const kvev_layout& L) { return (L.max_ctx - kTierSinks) / kTierW; }
@@ -106,9 +124,14 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
                 int64_t slots2 = 0) {
     Workspace w;
     size_t off = 0;
-    auto take = [&](size_t bytes) -> char* {
+    auto take = [&](size_t bytes, const char* name) -> char* {
         char* p = base ? base + off : nullptr;
         off += align_up(bytes, 256);
+        if (w.n_guard < Workspace::kMaxRegions) {
+            w.guard_off[w.n_guard] = off;
+            w.guard_name[w.n_guard++] = name;
+        }
+        off += kGuardBytes;
         return p;
     };
     const size_t rows = (size_t)L.n_layers * L.batch * L.n_kv_heads;
@@ -116,53 +139,54 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
     const size_t ctx = (size_t)L.batch * L.max_ctx;
     const size_t nblk = (size_t)((L.max_ctx + kScoreThreads - 1) / kScoreThreads);
     // two-tier mode scores windows from per-tile statistics: no logits
-    if (L.page_tokens != kTierW) w.logits = (float*)take(rows * (size_t)logit_ld(L.max_ctx) * G * 4);
-    w.part_o = (float*)take((size_t)slots * G * L.head_dim * 4);
-    w.part_ml = (float*)take((size_t)slots * G * 2 * 4);
-    w.lse2 = (float*)take(rows * G * 4);
-    w.keys = (uint32_t*)take(ctx * 4);
-    w.m_s = (float*)take(ctx * 4);
-    w.tref_s = (int32_t*)take(ctx * 4);
-    w.tins_s = (int32_t*)take(ctx * 4);
-    w.pos_s = (int32_t*)take(ctx * 4);
-    w.msum_part = (float*)take((size_t)L.batch * nblk * 4);
-    w.tot_s = (float*)take(ctx * 4);
-    w.status = (uint32_t*)take(4);
+    if (L.page_tokens != kTierW)
+        w.logits = (float*)take(rows * (size_t)logit_ld(L.max_ctx) * G * 4, "logits");
+    w.part_o = (float*)take((size_t)slots * G * L.head_dim * 4, "part_o");
+    w.part_ml = (float*)take((size_t)slots * G * 2 * 4, "part_ml");
+    w.lse2 = (float*)take(rows * G * 4, "lse2");
+    w.keys = (uint32_t*)take(ctx * 4, "keys");
+    w.m_s = (float*)take(ctx * 4, "m_s");
+    w.tref_s = (int32_t*)take(ctx * 4, "tref_s");
+    w.tins_s = (int32_t*)take(ctx * 4, "tins_s");
+    w.pos_s = (int32_t*)take(ctx * 4, "pos_s");
+    w.msum_part = (float*)take((size_t)L.batch * nblk * 4, "msum_part");
+    w.tot_s = (float*)take(ctx * 4, "tot_s");
+    w.status = (uint32_t*)take(4, "status");
     const size_t qn = (size_t)L.batch * L.n_layers * L.n_q_heads * L.head_dim;
     const size_t kn = (size_t)L.batch * L.n_layers * L.n_kv_heads * L.head_dim;
-    w.stg_q = (uint16_t*)take(qn * 2);
-    w.stg_k = (uint16_t*)take(kn * 2);
-    w.stg_v = (uint16_t*)take(kn * 2);
-    w.stg_out = (float*)take(qn * 4);
-    w.stg_ret = (int32_t*)take((size_t)L.batch * budget * 4);
-    w.stg_nret = (int32_t*)take((size_t)L.batch * 4);
+    w.stg_q = (uint16_t*)take(qn * 2, "stg_q");
+    w.stg_k = (uint16_t*)take(kn * 2, "stg_k");
+    w.stg_v = (uint16_t*)take(kn * 2, "stg_v");
+    w.stg_out = (float*)take(qn * 4, "stg_out");
+    w.stg_ret = (int32_t*)take((size_t)L.batch * budget * 4, "stg_ret");
+    w.stg_nret = (int32_t*)take((size_t)L.batch * 4, "stg_nret");
     const size_t units = (size_t)L.batch * (L.max_ctx / L.page_tokens);
-    w.lid_s = (int32_t*)take(units * 4);
-    w.len_s = (int32_t*)take(units * 4);
-    w.page_s = (int32_t*)take(units * 4);
-    w.tokens = (int32_t*)take((size_t)L.batch * 4);
-    w.sel = (int32_t*)take(units * 4);
-    w.budgets = (int32_t*)take((size_t)L.batch * 4);
-    w.readmit_page = (int32_t*)take(4);
+    w.lid_s = (int32_t*)take(units * 4, "lid_s");
+    w.len_s = (int32_t*)take(units * 4, "len_s");
+    w.page_s = (int32_t*)take(units * 4, "page_s");
+    w.tokens = (int32_t*)take((size_t)L.batch * 4, "tokens");
+    w.sel = (int32_t*)take(units * 4, "sel");
+    w.budgets = (int32_t*)take((size_t)L.batch * 4, "budgets");
+    w.readmit_page = (int32_t*)take(4, "readmit_page");
     if (L.page_tokens == kTierW) {
         const size_t B = (size_t)L.batch, MW = (size_t)tier_max_windows(L);
         const size_t bt = B * tier_bt_ld(L);
-        w.t_bt = (int32_t*)take(bt * 4);
-        w.t_bpos = (int32_t*)take(bt * 4);
-        w.t_blen = (int32_t*)take(bt * 4);
-        w.t_nblk = (int32_t*)take(B * 4);
-        w.t_qlist = (int32_t*)take(B * MW * 4);
-        w.t_nq = (int32_t*)take(B * 4);
-        w.t_seq_len = (int32_t*)take(B * 4);
-        w.t_quant = (int32_t*)take(B * MW * 4);
-        w.t_nquant = (int32_t*)take(B * 4);
-        w.t_prom = (int32_t*)take(B * MW * 4);
-        w.t_nprom = (int32_t*)take(B * 4);
-        w.t_free = (int32_t*)take(B * MW * 4);
-        w.t_nfree = (int32_t*)take(B * 4);
-        w.t_stats = (float2*)take(rows * (size_t)tier_stats_tiles(L) * G * sizeof(float2));
-        w.part_o2 = (float*)take((size_t)slots2 * G * L.head_dim * 4);
-        w.part_ml2 = (float*)take((size_t)slots2 * G * 2 * 4);
+        w.t_bt = (int32_t*)take(bt * 4, "t_bt");
+        w.t_bpos = (int32_t*)take(bt * 4, "t_bpos");
+        w.t_blen = (int32_t*)take(bt * 4, "t_blen");
+        w.t_nblk = (int32_t*)take(B * 4, "t_nblk");
+        w.t_qlist = (int32_t*)take(B * MW * 4, "t_qlist");
+        w.t_nq = (int32_t*)take(B * 4, "t_nq");
+        w.t_seq_len = (int32_t*)take(B * 4, "t_seq_len");
+        w.t_quant = (int32_t*)take(B * MW * 4, "t_quant");
+        w.t_nquant = (int32_t*)take(B * 4, "t_nquant");
+        w.t_prom = (int32_t*)take(B * MW * 4, "t_prom");
+        w.t_nprom = (int32_t*)take(B * 4, "t_nprom");
+        w.t_free = (int32_t*)take(B * MW * 4, "t_free");
+        w.t_nfree = (int32_t*)take(B * 4, "t_nfree");
+        w.t_stats = (float2*)take(rows * (size_t)tier_stats_tiles(L) * G * sizeof(float2), "t_stats");
+        w.part_o2 = (float*)take((size_t)slots2 * G * L.head_dim * 4, "part_o2");
+        w.part_ml2 = (float*)take((size_t)slots2 * G * 2 * 4, "part_ml2");
     }
     w.bytes = off;
     return w;
@@ -429,6 +453,9 @@ kvev_status kvev_create(const kvev_layout* layout, int64_t budget, int32_t granu
     c->ws = carve(*layout, budget, c->attn_warps + rows, c->ws_base, slots2);
     c->k_full = (int)budget;
     e = cudaMemset(c->ws_base, 0, bytes);   // row counters and status start at zero
+    for (int i = 0; i < c->ws.n_guard && e == cudaSuccess; ++i)
+        e = cudaMemset(c->ws_base + c->ws.guard_off[i], kGuardByte, kGuardBytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaFree(c->ws_base);
         delete c;
@@ -508,6 +535,7 @@ kvev_status kvev_set_debug(kvev_ctx* c, float* probs, float* priority) {
 kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void* v_new,
                       kvev_cache* cache, const kvev_state* st, int64_t step, float* out,
                       int32_t* retained_idx, int32_t* n_retained, void* stream) {
+    const NvtxRange trace("kvev_step");
     if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
     if (!q || !k_new || !v_new || !cache || !st || !out || !retained_idx || !n_retained)
         return fail(KVEV_EINVAL, "NULL argument");
@@ -718,6 +746,7 @@ kvev_status kvev_step_host(kvev_ctx* c, const void* q_host, const void* k_new_ho
                            const void* v_new_host, kvev_cache* cache, const kvev_state* st,
                            int64_t step, float* out_host, int32_t* retained_idx_host,
                            int32_t* n_retained_host, void* stream) {
+    const NvtxRange trace("kvev_step_host");
     if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
     if (!q_host || !k_new_host || !v_new_host || !out_host || !retained_idx_host ||
         !n_retained_host)
@@ -867,6 +896,7 @@ kvev_status kvev_paged_step(kvev_ctx* c, const void* q, const void* k_new, const
                             const kvev_paged_cache* pc, const kvev_block_state* bs, int64_t step,
                             float* out, int32_t* retained_lid, int32_t* n_retained,
                             void* stream) {
+    const NvtxRange trace("kvev_paged_step");
     kvev_status rc = check_paged(c, pc, bs);
     if (rc != KVEV_OK) return rc;
     if (!q || !k_new || !v_new || !out || !retained_lid || !n_retained)
@@ -1013,6 +1043,7 @@ kvev_status kvev_paged_step(kvev_ctx* c, const void* q, const void* k_new, const
 
 kvev_status kvev_readmit(kvev_ctx* c, const kvev_paged_cache* pc, const kvev_block_state* bs,
                          int32_t seq, int32_t lid, int32_t persist, void* stream) {
+    const NvtxRange trace("kvev_readmit");
     kvev_status rc = check_paged(c, pc, bs);
     if (rc != KVEV_OK) return rc;
     if (!c->begun) return fail(KVEV_ESTATE, "kvev_paged_begin must come first");
@@ -1148,6 +1179,7 @@ kvev_status kvev_tier_begin(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_t
 kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const void* v_new,
                            const kvev_tier_cache* tc, const kvev_tier_state* ts, int64_t step,
                            float* out, void* stream) {
+    const NvtxRange trace("kvev_tier_step");
     kvev_status rc = check_tier(c, tc, ts);
     if (rc != KVEV_OK) return rc;
     if (!q || !k_new || !v_new || !out) return fail(KVEV_EINVAL, "NULL argument");
@@ -1457,6 +1489,24 @@ kvev_status kvev_test_wait_timeout(kvev_ctx* c, int64_t tile, uint32_t wait_limi
     if (tile < 0 || wait_limit == 0) return fail(KVEV_EINVAL, "tile >= 0 and wait_limit >= 1");
     c->test_fault_tile = tile;
     c->test_wait_limit = wait_limit;
+    return KVEV_OK;
+}
+
+kvev_status kvev_check_scratch(kvev_ctx* c, void* stream) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    cudaStream_t s = (cudaStream_t)stream;
+    std::vector<unsigned char> band((size_t)c->ws.n_guard * kGuardBytes);
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < c->ws.n_guard && e == cudaSuccess; ++i)
+        e = cudaMemcpyAsync(band.data() + (size_t)i * kGuardBytes, c->ws_base + c->ws.guard_off[i],
+                            kGuardBytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the scratch guard bands");
+    for (int i = 0; i < c->ws.n_guard; ++i)
+        for (size_t k = 0; k < kGuardBytes; ++k)
+            if (band[(size_t)i * kGuardBytes + k] != kGuardByte)
+                return fail(KVEV_ESTATE, "scratch guard band after region %s overwritten at byte %zu",
+                            c->ws.guard_name[i], k);
     return KVEV_OK;
 }
 

@@ -39,7 +39,7 @@ EXPORTS = ["kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_siz
            "kvev_refresh_mode", "kvev_configure", "kvev_begin", "kvev_length",
            "kvev_init_state", "kvev_step", "kvev_step_host", "kvev_set_debug",
            "kvev_profile", "kvev_profile_read", "kvev_launch_count", "kvev_test_wait_timeout",
-           "kvev_sync",
+           "kvev_check_scratch", "kvev_sync",
            "kvev_paged_begin", "kvev_paged_step", "kvev_readmit", "kvev_set_tiers",
            "kvev_tier_begin", "kvev_tier_step", "kvev_export_state", "kvev_import_state",
            "kvev_attend_noalloc"]
@@ -153,6 +153,7 @@ def lib():
             "kvev_profile_read": ([P, P, P], I32),
             "kvev_launch_count": ([P, P], I32),
             "kvev_test_wait_timeout": ([P, I64, ctypes.c_uint32], I32),
+            "kvev_check_scratch": ([P, P], I32),
             "kvev_sync": ([P, P], I32),
             "kvev_paged_begin": ([P, P, P, I32, P], I32),
             "kvev_paged_step": ([P, P, P, P, P, P, I64, P, P, P, P], I32),
@@ -282,6 +283,11 @@ def kvev_launch_count(ctx) -> int:
 def kvev_test_wait_timeout(ctx, tile: int, wait_limit: int) -> None:
     """Test-only timeout injection for the next step (see include/kvev.h)."""
     _check(lib().kvev_test_wait_timeout(ctx, int(tile), int(wait_limit)), ctx)
+
+
+def kvev_check_scratch(ctx, stream=None) -> None:
+    """Raise KvevError if a guard band of the context's scratch was overwritten."""
+    _check(lib().kvev_check_scratch(ctx, _stream(stream)), ctx)
 
 
 def kvev_sync(ctx, stream=None) -> None:

@@ -247,7 +247,13 @@ kvev_status kvev_launch_count(const kvev_ctx* ctx, int64_t* launches);
  * step's outputs are undefined).  No counterpart on the pages. */
 kvev_status kvev_test_wait_timeout(kvev_ctx* ctx, int64_t tile, uint32_t wait_limit);
 
-/* Block until `stream`'s work is done; returns KVEV_ECUDA on a device fault. *//* Block until `stream`'s work is done; returns KVEV_ECUDA on a device fault. */
+/* Debugging aid: every region of the context's scratch is followed by a
+ * 256-byte guard band filled at create; this call reads the bands back
+ * (synchronising `stream`) and returns KVEV_ESTATE naming the first region
+ * whose band was overwritten, KVEV_OK when all are intact. */
+kvev_status kvev_check_scratch(kvev_ctx* ctx, void* stream);
+
+/* Block until `stream`'s work is done; returns KVEV_ECUDA on a device fault. */
 kvev_status kvev_sync(kvev_ctx* ctx, void* stream);
 
 /* ---- Block-granular eviction with score persistence ----------------------

@@ -47,4 +47,5 @@ def test_step_replays_from_a_cuda_graph():
     for k in STATE:
         assert torch.equal(getattr(ep, k), want[k]), f"graph replay differs in {k}"
     assert torch.equal(ep.k[1], want["k"]), "graph replay differs in the compacted keys"
+    kvev.kvev_check_scratch(ep.ctx)   # no scratch region overran its guard band
     ep.close()

@@ -193,6 +193,7 @@ def run_memdecay(wl, budget, steps, *, pps_slack=4, refresh=kvev.KVEV_REFRESH_FU
         ref_now = refresh == kvev.KVEV_REFRESH_FULL or (t - 1) % period == 0
         for b in range(g.batch):
             compare(pp, P, seqs, b, t, ref_now, q[b], kn[b], vn[b], probs, prio, stats)
+    kvev.kvev_check_scratch(pp.ctx)   # no scratch region overran its guard band
     pp.close()
     return stats
 
@@ -264,4 +265,5 @@ def test_memdecay_full_size_steps_1_2():
             compare(pp, P, seqs, s, t, True, _bits(q[s]), _bits(kn[s]), _bits(vn[s]), probs,
                     prio, stats)
     print("memdecay full size:", stats)
+    kvev.kvev_check_scratch(pp.ctx)   # no scratch region overran its guard band
     pp.close()

@@ -188,6 +188,7 @@ def run_paged(wl, budget, alpha, beta, steps, *, pps, age_mode=O.AGE_SINCE_ACCES
         ref_now = O.is_refresh(refresh_o, period, t)
         for b in range(g.batch):
             step_and_compare(pp, P, seqs, b, t, ref_now, q[b], kn[b], vn[b], probs, prio, stats)
+    kvev.kvev_check_scratch(pp.ctx)   # no scratch region overran its guard band
     pp.close()
     return stats
 
@@ -263,4 +264,5 @@ def test_paged_full_size_steps_1_2():
             step_and_compare(pp, P, seqs, s, t, True, _bits(q[s]), _bits(kn[s]), _bits(vn[s]),
                              probs, prio, stats)
     print("paged full size:", stats)
+    kvev.kvev_check_scratch(pp.ctx)   # no scratch region overran its guard band
     pp.close()

@@ -92,6 +92,7 @@ def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int,
                 totals["followed"] += 1
             states[b] = new
         assert ep.length() == min(L_prev + 1, budget)
+    kvev.kvev_check_scratch(ep.ctx)   # no scratch region overran its guard band
     ep.close()
     return totals
 
@@ -152,6 +153,7 @@ def test_probabilities_sum_to_one():
     kvev.kvev_sync(ep.ctx)
     s = probs[0, :, :, :778].sum(-1).cpu().numpy()
     assert np.allclose(s, 1.0, atol=1e-5)
+    kvev.kvev_check_scratch(ep.ctx)   # no scratch region overran its guard band
     ep.close()
 
 

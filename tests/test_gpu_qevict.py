@@ -142,6 +142,7 @@ def run_tiers(wl, k_full, k_quant, omega, steps, alpha=0.05, pps_slack=24):
         kvev.kvev_sync(tp.ctx)
         for b in range(g.batch):
             compare(tp, P, seqs, b, t, q[b], kn[b], vn[b], stats)
+    kvev.kvev_check_scratch(tp.ctx)   # no scratch region overran its guard band
     tp.close()
     return stats
 
@@ -231,4 +232,5 @@ def test_tiers_full_size_first_routing_event():
         compare(tp, P, seqs, 0, t, _bits(q[0]), _bits(kn[0]), _bits(vn[0]), stats,
                 check_windows=set(range(0, 1023, 61)))
     print("tiers full size:", stats)
+    kvev.kvev_check_scratch(tp.ctx)   # no scratch region overran its guard band
     tp.close()

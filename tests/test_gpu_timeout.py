@@ -64,6 +64,7 @@ def test_injected_wait_timeout_is_reported_and_context_recovers(tile):
     for w, g in zip(want, got):
         for k in w:
             assert torch.equal(w[k], g[k]), f"after the timeout the run differs in {k}"
+    kvev.kvev_check_scratch(a.ctx)
     a.close()
     b.close()
 
