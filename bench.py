@@ -98,20 +98,34 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(kernel_file: str, units: float):
-    """Per-launch DRAM bytes of the attention kernel from the committed ncu
-    summary, if it was taken on the current source; else None."""
+def _traffic_record(key: str, kernel_file: str):
+    """The committed ncu DRAM record `key`, if it was taken on the current
+    source of `kernel_file`; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as fh:
-            rec = json.load(fh)["attention"]
+            rec = json.load(fh)[key]
         src = open(os.path.join(ROOT, "decoding_kv_cache_split_gb300", "csrc", kernel_file),
                    "rb").read()
         if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
             return None
-        return float(rec["bytes_per_token_layer"]) * units
+        return rec
     except Exception:
         return None
+
+
+def ncu_traffic(kernel_file: str, units: float):
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    summary, if it was taken on the current source; else None."""
+    rec = _traffic_record("attention", kernel_file)
+    return None if rec is None else float(rec["bytes_per_token_layer"]) * units
+
+
+def traffic_ratio(key: str, kernel_file: str):
+    """DRAM bytes over algorithmic bytes of a smaller ncu capture of the same
+    kernel (applied to the bench's launches by the units they process)."""
+    rec = _traffic_record(key, kernel_file)
+    return None if rec is None else float(rec["ratio_to_algorithmic"])
 
 
 class ClockSampler:
@@ -693,6 +707,11 @@ def bench_paged(args, rank, world, local_rank):
     e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
     kvev.kvev_sync(pp.ctx)
     e2e_val = world * (attn_bytes_total / n_steps) / (e2e_ms * 1e-3) / 1e9
+    # DRAM bytes per launch: the algorithmic bytes times the ratio of an ncu
+    # capture of the same kernel on a smaller block workload (the region-aware
+    # workload runs another instantiation: none)
+    ratio = traffic_ratio("attention_paged", "attn.cu")
+    paged_traffic = round(attn_bytes_total / n_steps * ratio) if ratio and not md else None
 
     peak, peak_kind = measured_peak()
     if rank == 0:
@@ -715,7 +734,7 @@ def bench_paged(args, rank, world, local_rank):
                          "achieved": round(attn_achieved, 2) if attn_achieved else None,
                          "peak": peak, "unit": "GB/s",
                          "frac": round(attn_achieved / peak, 4) if attn_achieved else None,
-                         "traffic": None, "algorithmic_bytes": attn_bytes_total // n_steps,
+                         "traffic": paged_traffic, "algorithmic_bytes": attn_bytes_total // n_steps,
                          "peak_kind": f"{peak_kind} (copy bandwidth)"},
             "kernels_us": kernels_us,
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
@@ -826,6 +845,13 @@ def bench_tiers(args, rank, world, local_rank):
     kvev.kvev_profile(tp.ctx, False)
     bytes_step = [tb * row_bf16 + tq * row_int2 for tb, tq in per_step]
     total_bytes = sum(bytes_step)
+    # DRAM bytes per step of the two attention kernels: their algorithmic bytes
+    # times the ratios of ncu captures of the same kernels on smaller cases
+    r_bf, r_q = traffic_ratio("attention_paged", "attn.cu"), traffic_ratio("attention_int2",
+                                                                          "attn_int2.cu")
+    tier_traffic = (round(sum(tb * row_bf16 * r_bf + tq * row_int2 * r_q
+                              for tb, tq in per_step) / n_steps)
+                    if r_bf and r_q else None)
     value = world * total_bytes / (sum(step_ms) * 1e-3) / 1e9
     first = W["omega"]                     # steps after the first routing event
     steady_ms = sum(step_ms[first:]) / max(1, n_steps - first)
@@ -878,7 +904,7 @@ def bench_tiers(args, rank, world, local_rank):
                          "achieved": round(attn_achieved, 2) if attn_achieved else None,
                          "peak": peak, "unit": "GB/s",
                          "frac": round(attn_achieved / peak, 4) if attn_achieved else None,
-                         "traffic": None, "algorithmic_bytes": int(total_bytes / n_steps),
+                         "traffic": tier_traffic, "algorithmic_bytes": int(total_bytes / n_steps),
                          "peak_kind": f"{peak_kind} (copy bandwidth)"},
             "kernels_us": kernels_us,
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
