@@ -252,6 +252,39 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def log_mode_steps(fh, ctx, ep, step_in, step_ms, alpha, name, period, L0, B, row, k0, v0,
+                   stream):
+    """Per-step JSONL records of one refresh-mode run: the timed step's
+    duration, bytes and GB/s, whether the step refreshed the scores, and the
+    retained-set churn (the share of the previous step's retained tokens,
+    by original position, that this step evicted), from a replay of the run
+    that reads the state back after every step (outside the timed region)."""
+    from decoding_kv_cache_split_gb300 import kvev
+    ep.k[0].copy_(k0)
+    ep.v[0].copy_(v0)
+    ep.cache.cur = 0
+    kvev.kvev_begin(ctx, L0)
+    kvev.kvev_init_state(ctx, ep.state, stream)
+    prev = None
+    for t, ins in enumerate(step_in, start=1):
+        L = kvev.kvev_length(ctx) + 1                 # live tokens after the append
+        kvev.kvev_step(ctx, *ins, ep.cache, ep.state, t, ep.out, ep.retained, ep.n_retained,
+                       stream)
+        kvev.kvev_sync(ctx)
+        n = int(ep.n_retained[0].item())
+        kept = set(ep.pos[0, :n].cpu().tolist())
+        churn = None if prev is None else len(prev - kept) / max(1, len(prev))
+        refresh = (name == "full" or (name == "lazy8" and (t - 1) % period == 0)
+                   or (name == "frozen" and t == 1))
+        nbytes = L * row + 2 * n * row
+        fh.write(json.dumps({"alpha": alpha, "mode": name, "step": t,
+                             "us": round(step_ms[t - 1] * 1e3, 2), "bytes": nbytes,
+                             "GBps": round(nbytes / (step_ms[t - 1] * 1e-3) / 1e9, 1),
+                             "refresh": refresh, "live": L, "kept": n,
+                             "churn": None if churn is None else round(churn, 6)}) + "\n")
+        prev = kept
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -260,6 +293,8 @@ def main():
     ap.add_argument("--impl", default="kvev", choices=["kvev", "reference"])
     ap.add_argument("--cpu-layers", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--log-steps", default=None,
+                    help="write a JSONL record per step of the refresh-mode runs to this file")
     ap.add_argument("--no-graph", action="store_true",
                     help="skip the CUDA-graph replay timing of the headline pass")
     ap.add_argument("--mode-steps", type=int, default=256,
@@ -428,6 +463,7 @@ def main():
     # Every (alpha, mode) run starts from the prefill at step 1 and decodes
     # --mode-steps steps; steady = steps 2.. (about B + 1 live tokens each).
     modes = []
+    step_log = open(args.log_steps, "w") if args.log_steps and rank == 0 else None
     if args.mode_steps > 0 and args.layers == WORKLOAD["n_layers"]:
         k0, v0 = ep.k[0].clone(), ep.v[0].clone()
         n_ms = args.mode_steps
@@ -457,11 +493,16 @@ def main():
                 st = [evs[t - 1].elapsed_time(evs[t]) for t in range(1, n_ms + 1)]
                 steady = sum(st[1:]) / max(1, n_ms - 1)
                 steady_bytes = (B + 1) * row + 2 * B * row   # attention + compaction
+                if step_log is not None:
+                    log_mode_steps(step_log, ctx, ep, step_in, st, alpha, name, period, L0, B,
+                                   row, k0, v0, stream)
                 modes.append({"alpha": alpha, "mode": name, "step1_us": round(st[0] * 1e3, 1),
                               "steady_us": round(steady * 1e3, 1),
                               "steady_GBps": round(steady_bytes / (steady * 1e-3) / 1e9, 1)})
             kvev.kvev_destroy(ctx)
         del k0, v0, step_in
+    if step_log is not None:
+        step_log.close()
 
     # --------------------------------------------------------------- roofline
     peak, peak_kind = measured_peak()
