@@ -252,37 +252,48 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def log_mode_steps(fh, ctx, ep, step_in, step_ms, alpha, name, period, L0, B, row, k0, v0,
-                   stream):
-    """Per-step JSONL records of one refresh-mode run: the timed step's
-    duration, bytes and GB/s, whether the step refreshed the scores, and the
-    retained-set churn (the share of the previous step's retained tokens,
-    by original position, that this step evicted), from a replay of the run
-    that reads the state back after every step (outside the timed region)."""
+def replay_mode(fh, ctx, ep, step_in, step_ms, alpha, name, period, L0, B, row, k0, v0,
+                stream):
+    """Replays one refresh-mode run (outside the timed region; the run is
+    deterministic) reading the state back after every step, and returns each
+    step's algorithmic bytes: the attention over the live tokens plus the
+    read and write of the rows the compaction shifts (those at and after the
+    first slot the step evicted).  With `fh`, also writes a JSONL record per
+    step: the timed step's duration, bytes and GB/s, whether it refreshed
+    the scores, and the retained-set churn (the share of the previous step's
+    retained tokens, by original position, that this step evicted)."""
+    import torch
     from decoding_kv_cache_split_gb300 import kvev
     ep.k[0].copy_(k0)
     ep.v[0].copy_(v0)
     ep.cache.cur = 0
     kvev.kvev_begin(ctx, L0)
     kvev.kvev_init_state(ctx, ep.state, stream)
-    prev = None
+    prev, step_bytes = None, []
     for t, ins in enumerate(step_in, start=1):
         L = kvev.kvev_length(ctx) + 1                 # live tokens after the append
         kvev.kvev_step(ctx, *ins, ep.cache, ep.state, t, ep.out, ep.retained, ep.n_retained,
                        stream)
         kvev.kvev_sync(ctx)
         n = int(ep.n_retained[0].item())
-        kept = set(ep.pos[0, :n].cpu().tolist())
-        churn = None if prev is None else len(prev - kept) / max(1, len(prev))
-        refresh = (name == "full" or (name == "lazy8" and (t - 1) % period == 0)
-                   or (name == "frozen" and t == 1))
-        nbytes = L * row + 2 * n * row
-        fh.write(json.dumps({"alpha": alpha, "mode": name, "step": t,
-                             "us": round(step_ms[t - 1] * 1e3, 2), "bytes": nbytes,
-                             "GBps": round(nbytes / (step_ms[t - 1] * 1e-3) / 1e9, 1),
-                             "refresh": refresh, "live": L, "kept": n,
-                             "churn": None if churn is None else round(churn, 6)}) + "\n")
-        prev = kept
+        ret = ep.retained[0, :n].cpu()
+        moved = (ret != torch.arange(n, dtype=ret.dtype)).nonzero()
+        first_gap = int(moved[0]) if len(moved) else n       # rows below it did not move
+        nbytes = L * row + 2 * (n - first_gap) * row
+        step_bytes.append(nbytes)
+        if fh is not None:
+            kept = set(ep.pos[0, :n].cpu().tolist())
+            churn = None if prev is None else len(prev - kept) / max(1, len(prev))
+            refresh = (name == "full" or (name == "lazy8" and (t - 1) % period == 0)
+                       or (name == "frozen" and t == 1))
+            fh.write(json.dumps({"alpha": alpha, "mode": name, "step": t,
+                                 "us": round(step_ms[t - 1] * 1e3, 2), "bytes": nbytes,
+                                 "GBps": round(nbytes / (step_ms[t - 1] * 1e-3) / 1e9, 1),
+                                 "refresh": refresh, "live": L, "kept": n,
+                                 "churn": None if churn is None else round(churn, 6),
+                                 "first_moved_row": first_gap}) + "\n")
+            prev = kept
+    return step_bytes
 
 
 def main():
@@ -492,13 +503,13 @@ def main():
                 kvev.kvev_sync(ctx)
                 st = [evs[t - 1].elapsed_time(evs[t]) for t in range(1, n_ms + 1)]
                 steady = sum(st[1:]) / max(1, n_ms - 1)
-                steady_bytes = (B + 1) * row + 2 * B * row   # attention + compaction
-                if step_log is not None:
-                    log_mode_steps(step_log, ctx, ep, step_in, st, alpha, name, period, L0, B,
-                                   row, k0, v0, stream)
+                sb = replay_mode(step_log, ctx, ep, step_in, st, alpha, name, period, L0, B,
+                                 row, k0, v0, stream)
+                steady_bytes = sum(sb[1:]) / max(1, n_ms - 1)   # attention + shifted rows
                 modes.append({"alpha": alpha, "mode": name, "step1_us": round(st[0] * 1e3, 1),
                               "steady_us": round(steady * 1e3, 1),
-                              "steady_GBps": round(steady_bytes / (steady * 1e-3) / 1e9, 1)})
+                              "steady_GBps": round(steady_bytes / (steady * 1e-3) / 1e9, 1),
+                              "steady_bytes": int(steady_bytes)})
             kvev.kvev_destroy(ctx)
         del k0, v0, step_in
     if step_log is not None:

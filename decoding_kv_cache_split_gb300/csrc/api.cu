@@ -86,6 +86,8 @@ struct Workspace {
     int32_t* sel = nullptr;           // [batch][units] kept block slots
     int32_t* budgets = nullptr;       // [batch] blocks kept (region-aware selection)
     int32_t* readmit_page = nullptr;  // [1]
+    int32_t* first_moved = nullptr;   // [batch] first slot not kept this step
+    int32_t* vp = nullptr;            // [2][batch] reused-prefix rows, by step parity
     // two-tier mode (page_tokens = window)
     int32_t* t_bt = nullptr;          // [batch][bt_ld] attention block list
     int32_t* t_bpos = nullptr;
@@ -168,6 +170,8 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
     w.sel = (int32_t*)take(units * 4, "sel");
     w.budgets = (int32_t*)take((size_t)L.batch * 4, "budgets");
     w.readmit_page = (int32_t*)take(4, "readmit_page");
+    w.first_moved = (int32_t*)take((size_t)L.batch * 4, "first_moved");
+    w.vp = (int32_t*)take((size_t)L.batch * 8, "vp");
     if (L.page_tokens == kTierW) {
         const size_t B = (size_t)L.batch, MW = (size_t)tier_max_windows(L);
         const size_t bt = B * tier_bt_ld(L);
@@ -521,7 +525,7 @@ kvev_status kvev_init_state(kvev_ctx* c, const kvev_state* st, void* stream) {
     cudaStream_t s = (cudaStream_t)stream;
     const int len = c->len;
     return timed_launch(c, kProfInit, s, "init_state", [&] {
-        return launch_init_state(*st, c->lay.batch, c->lay.max_ctx, len, s);
+        return launch_init_state(*st, c->lay.batch, c->lay.max_ctx, len, c->ws.vp, s);
     });
 }
 
@@ -709,11 +713,15 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     se.max_ctx = Ly.max_ctx;
     se.budget = (int)c->budget;
     se.refresh = refresh ? 1 : 0;
+    se.first_moved = c->ws.first_moved;
     rc = timed_launch(c, kProfSelect, s, "select",
                       [&] { return launch_select(se, Ly.batch, s); });
     if (rc != KVEV_OK) return rc;
 
     CompactArgs cp{};
+    cp.first_moved = c->ws.first_moved;
+    cp.vp_in = c->ws.vp + (step & 1) * Ly.batch;
+    cp.vp_out = c->ws.vp + ((step + 1) & 1) * Ly.batch;
     cp.k_src = (const uint16_t*)cache->k[cur];
     cp.v_src = (const uint16_t*)cache->v[cur];
     cp.k_dst = (uint16_t*)cache->k[cur ^ 1];
@@ -1473,6 +1481,12 @@ kvev_status kvev_import_state(kvev_ctx* c, const void* host, size_t bytes, void*
     c->pin_blocks.assign(h.n_pin, 0);
     memcpy(c->ub_blocks.data(), in + sizeof h, 4 * (size_t)h.n_ub);
     memcpy(c->pin_blocks.data(), in + sizeof h + 4 * (size_t)h.n_ub, 4 * (size_t)h.n_pin);
+    {   // the caller's other cache buffer holds nothing the next step may reuse
+        cudaStream_t s = (cudaStream_t)stream;
+        cudaError_t e = cudaMemsetAsync(c->ws.vp, 0, (size_t)c->lay.batch * 8, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "resetting the reused-prefix counts");
+    }
     if (c->lay.page_tokens == kTierW && c->begun) {   // positions so far, per sequence
         std::vector<int32_t> sl(c->lay.batch, c->len);
         cudaStream_t s = (cudaStream_t)stream;

@@ -28,6 +28,9 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const CompactArgs
     const int32_t* idx = a.retained + (size_t)b * a.budget;
 
     if (r == 0 && blockIdx.z == 0) {
+        if (blockIdx.x == 0 && a.vp_out)   // next step's reused prefix
+            for (int bb = threadIdx.x; bb < a.batch; bb += kCopyThreads)
+                a.vp_out[bb] = a.identity ? a.vp_in[bb] : a.first_moved[bb];
         for (int e = threadIdx.x; e < chunk * a.batch; e += kCopyThreads) {
             const int j = j0 + e % chunk, bb = e / chunk;
             if (j >= a.n_keep) continue;
@@ -40,6 +43,9 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const CompactArgs
         }
     }
     if (a.identity) return;
+    // rows the destination already holds (identity below first_moved)
+    const int skip = a.vp_in ? min(a.vp_in[b], a.first_moved[b]) : 0;
+    if (j0 + chunk <= skip) return;
 
     const uint4* src = reinterpret_cast<const uint4*>(blockIdx.z == 0 ? a.k_src : a.v_src) +
                        (size_t)r * a.max_ctx * lpr;
@@ -56,10 +62,10 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const CompactArgs
     }
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u)
-        if (jj[u] < a.n_keep) buf[u] = __ldcs(src + (size_t)from[u] * lpr + c);
+        if (jj[u] < a.n_keep && jj[u] >= skip) buf[u] = __ldcs(src + (size_t)from[u] * lpr + c);
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u)
-        if (jj[u] < a.n_keep) __stcs(dst + (size_t)jj[u] * lpr + c, buf[u]);
+        if (jj[u] < a.n_keep && jj[u] >= skip) __stcs(dst + (size_t)jj[u] * lpr + c, buf[u]);
 }
 
 __global__ void append_kernel(const AppendArgs a) {
@@ -87,9 +93,11 @@ __global__ void append_kernel(const AppendArgs a) {
     }
 }
 
-__global__ void init_state_kernel(kvev_state st, int batch, int max_ctx, int len) {
+__global__ void init_state_kernel(kvev_state st, int batch, int max_ctx, int len, int32_t* vp) {
     griddep_wait();
     griddep_release();
+    if (vp && blockIdx.x == 0)   // no reused rows yet
+        for (int i = threadIdx.x; i < 2 * batch; i += blockDim.x) vp[i] = 0;
     const int64_t n = (int64_t)batch * len;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
          e += (int64_t)gridDim.x * blockDim.x) {
@@ -117,11 +125,14 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
     return launch_pdl(append_kernel, dim3(rows), dim3(32), 0, s, a);
 }
 
-cudaError_t launch_init_state(kvev_state st, int batch, int max_ctx, int len, cudaStream_t s) {
-    if (len == 0 || batch == 0) return cudaSuccess;
+cudaError_t launch_init_state(kvev_state st, int batch, int max_ctx, int len, int32_t* vp,
+                              cudaStream_t s) {
+    if (batch == 0 || (len == 0 && !vp)) return cudaSuccess;
     const int64_t n = (int64_t)batch * len;
-    const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    return launch_pdl(init_state_kernel, dim3(blocks), dim3(256), 0, s, st, batch, max_ctx, len);
+    int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(init_state_kernel, dim3(blocks), dim3(256), 0, s, st, batch, max_ctx, len,
+                      vp);
 }
 
 }  // namespace kvev

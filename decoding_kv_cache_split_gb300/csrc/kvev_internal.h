@@ -133,6 +133,7 @@ struct SelectArgs {
     int32_t L, max_ctx, budget, refresh;   // L: upper bound of n_units when n_units is set
     const int32_t* budgets;   // [b] per-sequence kept count (null: budget)
     int32_t ret_ld;           // row stride of retained (0: budget)
+    int32_t* first_moved;     // [b] first slot not kept (L when none), or null
 };
 
 struct CompactArgs {
@@ -144,6 +145,13 @@ struct CompactArgs {
     int32_t n_keep;            // retained per sequence (min(L, budget))
     int32_t identity;          // 1: no eviction, state only
     int32_t rows, batch, n_kv, max_ctx, budget, head_dim;
+    // Reused prefix: vp_in[b] leading rows of the destination buffer already
+    // equal the source's (it was the source of an earlier step), so rows below
+    // min(vp_in[b], first_moved[b]) are not copied; vp_out[b] is that count for
+    // the next step's destination (this step's source).  Null: copy all.
+    const int32_t* first_moved;
+    const int32_t* vp_in;
+    int32_t* vp_out;
 };
 
 struct AppendArgs {
@@ -353,7 +361,8 @@ cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStrea
 cudaError_t launch_select(const SelectArgs& a, int batch, cudaStream_t s);
 cudaError_t launch_compact(const CompactArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
-cudaError_t launch_init_state(kvev_state st, int batch, int max_ctx, int len, cudaStream_t s);
+cudaError_t launch_init_state(kvev_state st, int batch, int max_ctx, int len, int32_t* vp,
+                              cudaStream_t s);
 cudaError_t launch_paged_begin(const PagedArgs& a, int prefill_tokens, cudaStream_t s);
 cudaError_t launch_paged_append(const PagedArgs& a, const uint16_t* k_new, const uint16_t* v_new,
                                 cudaStream_t s);

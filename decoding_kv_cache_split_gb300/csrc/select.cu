@@ -102,7 +102,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     if (L <= B) {   // nothing to evict: identity (the same for every CTA: no exchange)
         if (rank == 0) {
             for (int i = tid; i < L; i += kSelThreads) ret[i] = i;
-            if (tid == 0) a.n_retained[b] = L;
+            if (tid == 0) {
+                a.n_retained[b] = L;
+                if (a.first_moved) a.first_moved[b] = L;
+            }
         }
         return;
     }
@@ -202,6 +205,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     int cta_kept;
     const int out0 = out_before_c + block_exclusive_scan(my_keep, red, &cta_kept);
     int o = out0, eqr = eq_before;
+    // the thread whose slots hold the first one not kept, with every slot
+    // before them kept, records it (exactly one such thread: L > B)
+    bool all_before = out0 == c0 + i0;
     for (int i = i0; i < i1; ++i) {
         const uint32_t u = keys[i];
         bool keep = u < T;
@@ -209,7 +215,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
             keep = eqr < keep_eq;
             ++eqr;
         }
-        if (keep) ret[o++] = c0 + i;
+        if (keep) {
+            ret[o++] = c0 + i;
+        } else if (all_before) {
+            if (a.first_moved) a.first_moved[b] = c0 + i;
+            all_before = false;
+        }
     }
     if (rank == kCl - 1 && tid == 0) a.n_retained[b] = out_before_c + cta_kept;
     cluster_sync();   // no CTA leaves while another may still read its shared memory

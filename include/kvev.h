@@ -93,7 +93,11 @@ typedef struct {
  * [n_layers][batch][n_kv_heads][max_ctx][head_dim] bf16, 16-byte aligned.
  * Slots [0, len) of buffer `cur` are live.  kvev_step reads buffer `cur`,
  * appends into it, and when it evicts writes the compacted cache into the
- * other buffer and flips `cur`. */
+ * other buffer and flips `cur`.  The other buffer is the library's between
+ * steps: its leading rows still equal the live buffer's up to the slot the
+ * previous compaction first moved, and the next compaction does not copy
+ * them again, so the caller must not write into it during a run (from
+ * kvev_init_state or kvev_import_state on). */
 typedef struct {
     void* k[2];
     void* v[2];
