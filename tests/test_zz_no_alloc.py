@@ -37,9 +37,10 @@ def _rel_err(a, b):
 
 
 def test_noalloc_attention_matches_kvev_step_on_two_calls():
-    """Two decode steps through kvev_step; after each, the allocation-free
-    call attends over the same appended cache (the buffer the step read,
-    which its compaction left untouched) and must give the step's output."""
+    """Two decode steps through kvev_step; for each, the allocation-free
+    call attends over the same appended cache (a copy of the buffer the step
+    read, with the step's new K/V written at its slot: the step's compaction
+    may rewrite that buffer in place) and must give the step's output."""
     wl = llama8b_workload(0, prefill_len=3000, n_layers=4)
     g = wl.geom
     max_ctx, budget = 3100, 300
@@ -52,13 +53,15 @@ def test_noalloc_attention_matches_kvev_step_on_two_calls():
     out = torch.empty_like(ep.out)
     lse2 = torch.empty((g.n_layers, g.batch, g.n_q_heads), dtype=torch.float32, device="cuda")
     for t in (1, 2):
-        read_buf = ep.cur
         L = ep.length() + 1
         q, kn, vn = wl.step_inputs(t)
-        qd = _dev(q)
-        ep.step(qd, _dev(kn), _dev(vn))
+        qd, knd, vnd = _dev(q), _dev(kn), _dev(vn)
+        kc, vc = ep.live_k().clone(), ep.live_v().clone()   # [Ly][b][Hkv][slot][d]
+        kc[:, :, :, L - 1] = knd.transpose(0, 1)             # new rows are [b][Ly][Hkv][d]
+        vc[:, :, :, L - 1] = vnd.transpose(0, 1)
+        ep.step(qd, knd, vnd)
         out.fill_(float("nan"))
-        kvev.kvev_attend_noalloc(ep.layout, qd, ep.k[read_buf], ep.v[read_buf], L, out, lse2)
+        kvev.kvev_attend_noalloc(ep.layout, qd, kc, vc, L, out, lse2)
         torch.cuda.synchronize()
         err = _rel_err(out, ep.out)
         assert err <= OUT_RTOL, f"call {t}: rel err {err:.3e}"
