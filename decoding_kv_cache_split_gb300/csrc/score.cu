@@ -38,12 +38,18 @@ __device__ __forceinline__ uint32_t order_bits(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Refresh steps: one thread per token, lanes on consecutive tokens (every
-// load instruction of a warp reads 512 contiguous bytes).  The number of KV
-// heads is a template parameter so a layer's heads are an unrolled loop with
-// no index arithmetic; the loads of kLB layers are all issued before any is
-// used, and each layer is folded into the EMA as soon as it is summed.
+// Refresh steps: a CTA takes 32 consecutive tokens (a warp's lanes, so
+// every load instruction of a warp reads 512 contiguous bytes) and its 4
+// warps split the layers into 4 consecutive segments.  The EMA over a
+// segment is affine in the score it starts from, m_out = (1 - alpha)^n m_in
+// + c, so each warp folds its layers in order starting from 0 (the first
+// segment from the token's score itself) and the first warp chains the 4
+// segments: the layer order of the recurrence is kept and 4x more threads
+// share the loads.  The number of KV heads is a template parameter so a
+// layer's heads are an unrolled loop with no index arithmetic; the loads of
+// kLB layers are all issued before any is used.
 constexpr int kRefreshThreads = 128;
+constexpr int kRefreshSegs = kRefreshThreads / 32;
 
 template <int G, int NKV>
 __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const ScoreArgs a) {
@@ -51,6 +57,7 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
     constexpr int kLB = NKV * V4 >= 16 ? 1 : (16 / (NKV * V4) > 4 ? 4 : 16 / (NKV * V4));  // layers in flight
     constexpr int kPerLine = 128 / (G * 4);                 // tokens per 128-byte line
     extern __shared__ float s_lse[];                        // [l1 - l0][NKV * G]
+    __shared__ float s_c[kRefreshSegs][32], s_tot[kRefreshSegs][32];
     griddep_wait();
     griddep_release();
     const int b = blockIdx.y;
@@ -61,12 +68,18 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
         s_lse[k] = a.lse2[((size_t)(a.l0 + l) * a.batch + b) * a.n_q + h];
     }
     __syncthreads();
-    const int i = blockIdx.x * kRefreshThreads + threadIdx.x;
-    if (i >= a.L) return;
+    const int seg = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = blockIdx.x * 32 + lane;
+    const bool live = i < a.L;
+    const int la = seg * n_lay / kRefreshSegs, lb = (seg + 1) * n_lay / kRefreshSegs;
 
     const size_t si = (size_t)b * a.max_ctx + i;
-    float m = a.first_group ? a.st.score[si] : a.m_s[si];
-    float tot = a.first_group ? 0.f : a.tot_s[si];
+    float m0 = 0.f, tot0 = 0.f;
+    if (live && seg == 0) {
+        m0 = a.first_group ? a.st.score[si] : a.m_s[si];
+        tot0 = a.first_group ? 0.f : a.tot_s[si];
+    }
+    float c = m0, tot = tot0;   // the first segment starts from the score itself
     const float oma = 1.0f - a.alpha;
     const float inv_hq = 1.0f / (float)a.n_q;
     const size_t head_stride = (size_t)a.logit_ld * G;                  // one (layer, KV head) row
@@ -74,59 +87,75 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
     const float* base = a.logits + ((size_t)a.l0 * a.batch + b) * NKV * head_stride + (size_t)i * G;
     const bool drop = i % kPerLine == 0 && i + kPerLine <= a.L;         // this thread drops lines
 
-    for (int l0 = 0; l0 < n_lay; l0 += kLB) {
-        float4 xb[kLB][NKV][V4];
+    if (live) {
+        for (int l0 = la; l0 < lb; l0 += kLB) {
+            float4 xb[kLB][NKV][V4];
 #pragma unroll
-        for (int u = 0; u < kLB; ++u)                 // all loads of the batch first ...
-#pragma unroll
-            for (int g = 0; g < NKV; ++g)
-#pragma unroll
-                for (int c = 0; c < V4; ++c)
-                    xb[u][g][c] = l0 + u < n_lay
-                        ? __ldcs(reinterpret_cast<const float4*>(
-                              base + (size_t)(l0 + u) * layer_stride + g * head_stride) + c)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < kLB; ++u) {               // ... then the layers in order
-            const int lr = l0 + u;
-            if (lr >= n_lay) break;
-            const float4* lg = reinterpret_cast<const float4*>(s_lse + lr * NKV * G);
-            float s = 0.f;
-#pragma unroll
-            for (int g = 0; g < NKV; ++g)
-#pragma unroll
-                for (int c = 0; c < V4; ++c) {
-                    const float4 x = xb[u][g][c], e = lg[g * V4 + c];
-                    const float p0 = fast_exp2(x.x - e.x), p1 = fast_exp2(x.y - e.y);
-                    const float p2 = fast_exp2(x.z - e.z), p3 = fast_exp2(x.w - e.w);
-                    if (a.dbg_probs) {
-                        float* dp = a.dbg_probs +
-                                    (((size_t)b * a.n_layers + a.l0 + lr) * a.n_q + g * G + 4 * c) *
-                                        a.max_ctx + i;
-                        dp[0] = p0;
-                        dp[(size_t)a.max_ctx] = p1;
-                        dp[2 * (size_t)a.max_ctx] = p2;
-                        dp[3 * (size_t)a.max_ctx] = p3;
-                    }
-                    s += (p0 + p1) + (p2 + p3);
-                }
-            // The logits are dead once read: drop their L2 lines without
-            // writing them back.  A 128-byte line holds kPerLine tokens of
-            // one (layer, KV head) row (rows start on a line), all loaded by
-            // this warp's load, which has completed since its values were
-            // just used (the discard takes `s` as an operand, so it cannot
-            // move above that use).  The line's first token's thread drops it.
-            if (drop) {
+            for (int u = 0; u < kLB; ++u)                 // all loads of the batch first ...
 #pragma unroll
                 for (int g = 0; g < NKV; ++g)
-                    asm volatile("discard.global.L2 [%0], 128;" ::"l"(
-                                     base + (size_t)lr * layer_stride + g * head_stride),
-                                 "f"(s)
-                                 : "memory");
+#pragma unroll
+                    for (int cc = 0; cc < V4; ++cc)
+                        xb[u][g][cc] = l0 + u < lb
+                            ? __ldcs(reinterpret_cast<const float4*>(
+                                  base + (size_t)(l0 + u) * layer_stride + g * head_stride) + cc)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < kLB; ++u) {               // ... then the layers in order
+                const int lr = l0 + u;
+                if (lr >= lb) break;
+                const float4* lg = reinterpret_cast<const float4*>(s_lse + lr * NKV * G);
+                float s = 0.f;
+#pragma unroll
+                for (int g = 0; g < NKV; ++g)
+#pragma unroll
+                    for (int cc = 0; cc < V4; ++cc) {
+                        const float4 x = xb[u][g][cc], e = lg[g * V4 + cc];
+                        const float p0 = fast_exp2(x.x - e.x), p1 = fast_exp2(x.y - e.y);
+                        const float p2 = fast_exp2(x.z - e.z), p3 = fast_exp2(x.w - e.w);
+                        if (a.dbg_probs) {
+                            float* dp = a.dbg_probs +
+                                        (((size_t)b * a.n_layers + a.l0 + lr) * a.n_q + g * G + 4 * cc) *
+                                            a.max_ctx + i;
+                            dp[0] = p0;
+                            dp[(size_t)a.max_ctx] = p1;
+                            dp[2 * (size_t)a.max_ctx] = p2;
+                            dp[3 * (size_t)a.max_ctx] = p3;
+                        }
+                        s += (p0 + p1) + (p2 + p3);
+                    }
+                // The logits are dead once read: drop their L2 lines without
+                // writing them back.  A 128-byte line holds kPerLine tokens of
+                // one (layer, KV head) row (rows start on a line), all loaded by
+                // this warp's load, which has completed since its values were
+                // just used (the discard takes `s` as an operand, so it cannot
+                // move above that use).  The line's first token's thread drops it.
+                if (drop) {
+#pragma unroll
+                    for (int g = 0; g < NKV; ++g)
+                        asm volatile("discard.global.L2 [%0], 128;" ::"l"(
+                                         base + (size_t)lr * layer_stride + g * head_stride),
+                                     "f"(s)
+                                     : "memory");
+                }
+                tot += s;
+                c = fmaf(a.alpha, a.pool_mean ? s * inv_hq : s, oma * c);
             }
-            tot += s;
-            m = fmaf(a.alpha, a.pool_mean ? s * inv_hq : s, oma * m);
         }
+    }
+    s_c[seg][lane] = c;
+    s_tot[seg][lane] = tot;
+    __syncthreads();
+    if (seg != 0 || !live) return;
+    // chain the segments in layer order: m <- (1 - alpha)^(layers of k) m + c_k
+    float m = c;
+    tot = s_tot[0][lane];
+    for (int k = 1; k < kRefreshSegs; ++k) {
+        const int ka = k * n_lay / kRefreshSegs, kb = (k + 1) * n_lay / kRefreshSegs;
+        float decay = 1.f;
+        for (int l = ka; l < kb; ++l) decay *= oma;
+        m = fmaf(decay, m, s_c[k][lane]);
+        tot += s_tot[k][lane];
     }
     if (!a.last_group) {   // carry the state to the next group of layers
         a.m_s[si] = m;
@@ -200,7 +229,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_stale_kernel(const ScoreA
 
 cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStream_t s) {
     if (a.refresh) {
-        const int nb = (a.L + kRefreshThreads - 1) / kRefreshThreads;
+        const int nb = (a.L + 31) / 32;   // 32 tokens per CTA
         *n_blocks = nb;
         const dim3 grid(nb, a.batch);
         const size_t smem = sizeof(float) * (size_t)(a.l1 - a.l0) * a.n_q;
