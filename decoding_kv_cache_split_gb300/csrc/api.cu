@@ -715,7 +715,7 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     se.refresh = refresh ? 1 : 0;
     se.first_moved = c->ws.first_moved;
     rc = timed_launch(c, kProfSelect, s, "select",
-                      [&] { return launch_select(se, Ly.batch, s); });
+                      [&] { return launch_select(se, Ly.batch, c->num_sms, s); });
     if (rc != KVEV_OK) return rc;
 
     CompactArgs cp{};
@@ -1027,7 +1027,7 @@ kvev_status kvev_paged_step(kvev_ctx* c, const void* q, const void* k_new, const
     se.ret_ld = pa.sel_ld;
     se.refresh = 1;   // a new block's score was set by the append
     rc = timed_launch(c, kProfSelect, s, "select",
-                      [&] { return launch_select(se, Ly.batch, s); });
+                      [&] { return launch_select(se, Ly.batch, c->num_sms, s); });
     if (rc != KVEV_OK) return rc;
     rc = timed_launch(c, kProfCompact, s, "paged compact",
                       [&] { return launch_paged_compact(pa, s); });

@@ -358,7 +358,7 @@ cudaError_t launch_attention(const AttnArgs& a, int head_dim, int group, int gri
                              cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int head_dim, int group, cudaStream_t s);
 cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStream_t s);
-cudaError_t launch_select(const SelectArgs& a, int batch, cudaStream_t s);
+cudaError_t launch_select(const SelectArgs& a, int batch, int num_sms, cudaStream_t s);
 cudaError_t launch_compact(const CompactArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_init_state(kvev_state st, int batch, int max_ctx, int len, int32_t* vp,

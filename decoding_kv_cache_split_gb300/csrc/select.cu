@@ -6,7 +6,8 @@
 // priority of the kv-cache-docs "ema-eviction" figure a higher priority is
 // evicted, so the B lowest priorities are retained.
 //
-// One thread-block cluster of kCl CTAs per sequence.  The keys are the
+// One thread-block cluster of kCl CTAs per sequence (one CTA when the
+// sequence's keys fit its shared memory).  The keys are the
 // order-preserving bits of the fp32 priorities; CTA r of the cluster stages
 // the r-th contiguous chunk of a sequence's keys in shared memory.  A 4-pass
 // radix select (8-bit digits) finds the B-th smallest key T: in every pass
@@ -71,6 +72,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* red, int* total)
     return before;
 }
 
+template <int CL>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a) {
     extern __shared__ uint32_t s_keys[];             // this CTA's chunk (if it fits)
     __shared__ uint32_t hist[kSelWarps][256];
@@ -82,9 +84,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
     griddep_wait();
     griddep_release();
     const uint32_t rank = cta_rank();
-    const int b = blockIdx.x / kCl;
+    const int b = blockIdx.x / CL;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int L = a.n_units ? min(a.n_units[blockIdx.x / kCl], a.L) : a.L;
+    const int L = a.n_units ? min(a.n_units[blockIdx.x / CL], a.L) : a.L;
     const int B = a.budgets ? a.budgets[b] : a.budget;
     const uint32_t* gkeys = a.keys + (size_t)b * a.max_ctx;
     int32_t* ret = a.retained + (size_t)b * (a.ret_ld ? a.ret_ld : a.budget);
@@ -109,7 +111,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
         }
         return;
     }
-    const int chunk = (L + kCl - 1) / kCl;
+    const int chunk = (L + CL - 1) / CL;
     const int c0 = min(L, (int)rank * chunk), c1 = min(L, c0 + chunk);
     const int n = c1 - c0;
     const bool staged = chunk <= kChunkCap;
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
         if (warp < 8) {   // sum over the cluster, then scan the 256 bins
             uint32_t t = 0;
 #pragma unroll
-            for (uint32_t r = 0; r < kCl; ++r) t += ld_remote(&mine[tid], r);
+            for (uint32_t r = 0; r < CL; ++r) t += ld_remote(&mine[tid], r);
             uint32_t x = t;
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
@@ -222,33 +224,39 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
             all_before = false;
         }
     }
-    if (rank == kCl - 1 && tid == 0) a.n_retained[b] = out_before_c + cta_kept;
+    if (rank == CL - 1 && tid == 0) a.n_retained[b] = out_before_c + cta_kept;
     cluster_sync();   // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace
 
-cudaError_t launch_select(const SelectArgs& a, int batch, cudaStream_t s) {
-    const int chunk = (a.L + kCl - 1) / kCl;
+cudaError_t launch_select(const SelectArgs& a, int batch, int num_sms, cudaStream_t s) {
+    // Many sequences whose keys fit one CTA's shared memory: one CTA each (no
+    // cluster barriers or remote reads; the sequences fill the GPU).  Few
+    // sequences, or long ones: a cluster of kCl CTAs each.
+    const bool one = a.L <= kChunkCap && batch * kCl > num_sms;
+    const int cl = one ? 1 : kCl;
+    const int chunk = (a.L + cl - 1) / cl;
     const size_t smem = chunk <= kChunkCap ? sizeof(uint32_t) * (size_t)chunk : 0;
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = one ? select_kernel<1> : select_kernel<kCl>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(sizeof(uint32_t) * kChunkCap));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kCl * batch);
+    cfg.gridDim = dim3(cl * batch);
     cfg.blockDim = dim3(kSelThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCl;
+    attr[0].val.clusterDim.x = cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, select_kernel, a);
+    e = cudaLaunchKernelEx(&cfg, kern, a);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -207,6 +207,13 @@ def test_memdecay_small_partial_prefill_page():
     print("memdecay small:", st)
 
 
+def test_memdecay_many_sequences():
+    """24 sequences (one selection CTA per sequence), 2 layers, 96-token
+    prefills, a 28-token budget, 8 steps."""
+    wl = memdecay_workload(0, prefill_len=96, n_layers=2, batch=24)
+    run_memdecay(wl, 28, 8)
+
+
 def test_memdecay_1700_full_depth():
     """36 layers, 1700-token contexts (the short tier's length), budget 510,
     6 steps, one sequence."""

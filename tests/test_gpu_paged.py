@@ -225,6 +225,13 @@ def test_paged_edge_sizes(L0, budget):
     run_paged(wl, budget, 0.05, 0.001, 20, pps=budget + 8)
 
 
+def test_paged_many_sequences():
+    """24 sequences (the selection then runs one CTA per sequence instead of
+    a cluster per sequence), small geometry, 6 steps."""
+    wl = Workload(Geometry(2, 8, 2, 64, 24), 96, seed=24, heavy=2)
+    run_paged(wl, 3, 0.05, 0.001, 6, pps=12)
+
+
 def test_paged_beta_infinite():
     wl = paged_workload(3, prefill_len=256, n_layers=2, batch=1, needle_period=50)
     run_paged(wl, 4, 0.2, math.inf, 6, pps=20)
