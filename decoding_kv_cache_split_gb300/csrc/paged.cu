@@ -245,15 +245,26 @@ __global__ void __launch_bounds__(kPagedThreads) score_paged_kernel(const ScoreA
         const float* lbase = sc.logits + ((size_t)b * NKV) * head_stride + (size_t)slot * G;
         const float oma = 1.0f - a.alpha, inv_hq = 1.0f / (float)sc.n_q;
         float tot = 0.f;
+        // the next layer's loads are issued before this layer is used
+        float4 nx[NKV][V4];
+#pragma unroll
+        for (int g = 0; g < NKV; ++g)
+#pragma unroll
+            for (int c = 0; c < V4; ++c)
+                nx[g][c] = live ? __ldcs(reinterpret_cast<const float4*>(lbase + g * head_stride) + c)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int l = 0; l < sc.n_layers; ++l) {
             float4 xb[NKV][V4];
 #pragma unroll
             for (int g = 0; g < NKV; ++g)
 #pragma unroll
-                for (int c = 0; c < V4; ++c)
-                    xb[g][c] = live ? __ldcs(reinterpret_cast<const float4*>(
-                                          lbase + (size_t)l * layer_stride + g * head_stride) + c)
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int c = 0; c < V4; ++c) {
+                    xb[g][c] = nx[g][c];
+                    nx[g][c] = live && l + 1 < sc.n_layers
+                                   ? __ldcs(reinterpret_cast<const float4*>(
+                                         lbase + (size_t)(l + 1) * layer_stride + g * head_stride) + c)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             float s = 0.f;
             if (live) {
                 const float4* lg = reinterpret_cast<const float4*>(s_lse + l * NKV * G);
