@@ -502,15 +502,25 @@ __global__ void __launch_bounds__(kPagedThreads) score_memdecay_kernel(const Sco
             const size_t layer_stride = (size_t)sc.batch * NKV * head_stride;
             const float* lbase = sc.logits + ((size_t)b * NKV) * head_stride + (size_t)slot * G;
             float tot = 0.f;
+            // the next layer's loads are issued before this layer is used
+            float4 nx[NKV][V4];
+#pragma unroll
+            for (int g = 0; g < NKV; ++g)
+#pragma unroll
+                for (int c = 0; c < V4; ++c)
+                    nx[g][c] = __ldcs(reinterpret_cast<const float4*>(lbase + g * head_stride) + c);
             for (int l = 0; l < sc.n_layers; ++l) {
                 float4 xb[NKV][V4];
 #pragma unroll
                 for (int g = 0; g < NKV; ++g)
 #pragma unroll
-                    for (int c = 0; c < V4; ++c)
-                        xb[g][c] = __ldcs(reinterpret_cast<const float4*>(
-                                              lbase + (size_t)l * layer_stride + g * head_stride) +
-                                          c);
+                    for (int c = 0; c < V4; ++c) {
+                        xb[g][c] = nx[g][c];
+                        if (l + 1 < sc.n_layers)
+                            nx[g][c] = __ldcs(reinterpret_cast<const float4*>(
+                                                  lbase + (size_t)(l + 1) * layer_stride +
+                                                  g * head_stride) + c);
+                    }
                 const float4* lg = reinterpret_cast<const float4*>(s_lse + l * NKV * G);
                 float sl = 0.f;
 #pragma unroll
