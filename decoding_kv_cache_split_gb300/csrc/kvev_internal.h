@@ -75,16 +75,27 @@ struct SplitPartials {
 };
 
 // Warps of the split whose tile range is empty write no partial.
+// floor(a / n) for 0 <= a < 2^62, 0 < n, when the quotient is below 2^22:
+// a single-precision estimate (off by at most one there) fixed with exact
+// 64-bit products, instead of a 64-bit integer division.
+__device__ __forceinline__ int64_t small_quotient(int64_t a, int64_t n) {
+    if (n <= 0) return 0;
+    int64_t q = (int64_t)__fdividef((float)a, (float)n);
+    if (q < 0) q = 0;
+    while (q * n > a) --q;
+    while ((q + 1) * n <= a) ++q;
+    return q;
+}
 __device__ __forceinline__ bool split_warp_has_tiles(int64_t w, int64_t N, int64_t W) {
-    return w * N / W != (w + 1) * N / W;
+    return N >= W || w * N / W != (w + 1) * N / W;   // every warp has a tile when N >= W
 }
 // The warps whose tile ranges meet launch row r: [*lo, *hi] (some may be empty).
 __device__ __forceinline__ void split_warps_of_row(const SplitPartials& p, int64_t r,
                                                    int64_t* lo, int64_t* hi) {
     const int64_t first = r * p.tiles_per_row, last = first + p.tiles_per_row - 1;
     const int64_t W = p.total_warps, N = p.n_tiles;
-    *lo = ((first + 1) * W - 1) / N;   // the largest w with floor(w N / W) <= tile
-    *hi = ((last + 1) * W - 1) / N;
+    *lo = small_quotient((first + 1) * W - 1, N);   // the largest w with floor(w N / W) <= tile
+    *hi = small_quotient((last + 1) * W - 1, N);
 }
 
 struct CombineArgs {
