@@ -3,9 +3,12 @@
 //
 // Compaction: retained slot retained[b][j] (ascending) moves to slot j, in
 // every layer and KV head, out of place into the other ping-pong buffer, so
-// no row is overwritten before it is read.  One CTA moves a chunk of retained
-// rows of one (K or V, layer, sequence, KV head) row of the cache with
-// 16-byte loads and stores; a warp covers 32/(D/8) rows per instruction.
+// no row is overwritten before it is read.  That buffer still holds the
+// live rows below the first slot the previous compaction moved; rows below
+// the smaller of that and this step's first moved slot are not copied again.
+// One CTA moves a chunk of retained rows of one (K or V, layer, sequence,
+// KV head) row of the cache with 16-byte loads and stores; a warp covers
+// 32/(D/8) rows per instruction.
 // The per-token state (score, clocks, position) is gathered from the
 // scoring kernel's scratch copy by the CTAs of the first cache row.
 #include "kvev_internal.h"
