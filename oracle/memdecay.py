@@ -20,6 +20,11 @@ Cache Eviction for Efficient LLM Agent Inference":
     (a min-heap); a page holding any pinned token is pinned (Sec. IV-A:
     pinning protects whole pages).
 
+Parity unpinned: the per-region base priorities b_r.  The page prints the
+caption of its Table I without the values; this build reads b_r = 1 for every
+region (any b_r enters the same Eq. (4), whose structure the pins check), so
+no test can tie the values themselves to the page.
+
 Readings where the paper is silent: decoded tokens take the label
 ``decode_region`` (scratchpad); a new token joins the last page while it has
 room, else opens a page; among equal page scores the higher page index is

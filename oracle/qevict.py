@@ -24,6 +24,13 @@ Attention-Drift-Robust Long-Context Decoding" (the review page), Sec. 4:
     demotion only; its codes and scale/zero stay in a ledger and are reused on
     every later demotion; a promoted window is dequantized from the ledger.
 
+Parity unpinned: the window geometry and routing interval (sinks 5, recent
+32, windows of 128 tokens on the grid after the sinks, routing every Omega = 8
+steps at the end of the step).  The page gives the sink and recent counts and
+Omega but not where windows start or when in a step routing happens; these
+are this build's readings, and no pin ties them to the page beyond the
+capacity example of Eq. (3).
+
 INT2 codec (asymmetric, as the page's KIVI-style scheme: per-channel keys,
 per-token values, groups of 32): for each group zero = fp16(min), scale =
 fp16((max - min) / 3) with the difference and division in fp32, code =
