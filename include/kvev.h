@@ -187,7 +187,8 @@ kvev_status kvev_length(const kvev_ctx* ctx, int32_t* len);
 
 /* Write the prefill state on `stream`: for every sequence and slot i below
  * the prefill length, score = 0, t_ins = t_ref = 0, pos = i (Appendix E
- * "Momentum initialization": m0 = 0). */
+ * "Momentum initialization": m0 = 0).  The next compaction copies every
+ * retained row (nothing in the other cache buffer is reused). */
 kvev_status kvev_init_state(kvev_ctx* ctx, const kvev_state* state, void* stream);
 
 /* One decode step `step` (must be the previous step + 1; the first step
