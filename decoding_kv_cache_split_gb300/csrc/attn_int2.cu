@@ -133,12 +133,15 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
         }
         cp_async_commit();
     };
-    // the lane's half (hi or lo) of a product pair: hi rows round the pair to
-    // bf16, lo rows round what the hi part leaves
-    const float2 nlom = make_float2(-lom, -lom);
+    // the lane's half (hi or lo) of a product pair: the hi part is the pair
+    // truncated to bf16 (exact), the lo part what it leaves (exact in fp32)
+    // rounded to bf16; hi rows form 0 * x + hi, lo rows 1 * x + (-hi)
+    const uint32_t hi_sign = lo_row ? 0x80000000u : 0u;
+    const float2 lo_sel = make_float2(lom, lom);
     auto half_pair = [&](float2 xv) -> uint32_t {
-        const uint32_t hi = pack_bf16x2(xv.x, xv.y);
-        const float2 r = fma2(nlom, make_float2(bf16_lo(hi), bf16_hi(hi)), xv);
+        const float2 hb = make_float2(__uint_as_float((__float_as_uint(xv.x) & 0xffff0000u) ^ hi_sign),
+                                      __uint_as_float((__float_as_uint(xv.y) & 0xffff0000u) ^ hi_sign));
+        const float2 r = fma2(lo_sel, xv, hb);
         return pack_bf16x2(r.x, r.y);
     };
 
