@@ -88,6 +88,11 @@ typedef struct {
     int32_t page_tokens;  /* 1 = token-granular eviction; 16 = paged blocks */
     int32_t kv_dtype;     /* KVEV_BF16 */
 } kvev_layout;
+/* Size limit: the kernels address a cache buffer (or a page pool) as rows of
+ * head_dim elements with 32-bit TMA coordinates, so
+ * n_layers * batch * n_kv_heads * max_ctx must stay below 2^31.  The library
+ * does not check this, because such a cache needs at least 2 x 256 GiB of K/V,
+ * more than one GPU holds. */
 
 /* The KV cache: two ping-pong buffers.  Each of k[0], k[1], v[0], v[1] is
  * [n_layers][batch][n_kv_heads][max_ctx][head_dim] bf16, 16-byte aligned.
