@@ -206,12 +206,15 @@ def test_budget_met_exactly_stops_the_eviction():
     assert res["evicted"] == [4, 3] and seq.n_tokens == 12
 
 
-def test_decoded_token_enters_at_full_structural_priority():
+@pytest.mark.parametrize("L0", [4, 6])
+def test_decoded_token_enters_at_full_structural_priority(L0):
     """A new token is inserted at t (t_ref = t_ins = t), so its prior term is
-    b of the decode region, plus alpha (1 - rho) A_bar from this step."""
+    b of the decode region, plus alpha (1 - rho) A_bar from this step; the
+    same whether it opens a page (L0 = 4, pages of 4) or joins the partial
+    last page (L0 = 6).  Uniform attention over L0 + 1 tokens."""
     P = _params(base=(1.0, 2.5))
-    seq = _seq(np.zeros((1, 1, 4, 4)), [0] * 4)
+    seq = _seq(np.zeros((1, 1, L0, 4)), [0] * L0)
     kn, vn = _zeros(P)
     res = MD.step(P, seq, 7, True, _q(P), kn, vn)
-    assert res["t_ref"][4] == 7
-    assert res["s"][4] == pytest.approx(2.5 + 0.5 * 0.1 * (1 / 5), rel=1e-12)
+    assert res["t_ref"][L0] == 7
+    assert res["s"][L0] == pytest.approx(2.5 + 0.5 * 0.1 * (1 / (L0 + 1)), rel=1e-12)

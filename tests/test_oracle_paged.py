@@ -129,6 +129,22 @@ def test_budget_counts_blocks_and_open_block_fills_first():
     assert seq.next_lid >= 7
 
 
+def test_appending_into_the_open_block_is_an_access():
+    """Insertion counts as an access: the decode block opened at step 1 takes
+    the token of step 2 (a non-refresh step, so no attention decides any
+    access) and its clock moves to 2 (age 0, priority 0), while the prefill
+    blocks keep the clock of their insertion (step 0)."""
+    rng = np.random.default_rng(3)
+    P = _params(n_layers=1, n_q_heads=2, n_kv_heads=1, head_dim=4, budget=10)
+    seq = _random_seq(rng, P, 8, 4)                # 2 prefill blocks
+    PG.step(P, seq, 1, True, *_inputs(rng, P))     # opens block 2
+    res = PG.step(P, seq, 2, False, *_inputs(rng, P))
+    assert [b.n for b in seq.blocks] == [4, 4, 2]
+    assert not res["accessed"].any()
+    assert [b.t_ref for b in seq.blocks] == [0, 0, 2]
+    assert res["priority"][2] == 0.0 and (res["priority"][:2] != 0.0).all()
+
+
 def test_block_access_when_any_member_token_is_accessed():
     """A block whose one token takes almost all the attention is accessed
     (its clock resets, priority 0); blocks of uniform tokens are not."""

@@ -76,6 +76,35 @@ def test_window_partition():
     seq = QE.QSequence.from_prefill(P, z, z)
     assert len(seq.windows) == 3 and seq.K_tail.shape[2] == 10 and seq.K_sink.shape[2] == 5
     assert (131072 - 5) // 128 == 1023 and (131072 - 5) % 128 == 123
+    # a window needs all of its 128 positions after the sinks: one short of
+    # two windows leaves one window and a 127-token tail
+    for L0, nw, tail in ((5 + 128 * 2 - 1, 1, 127), (5 + 128, 1, 0), (5 + 127, 0, 127)):
+        z = np.zeros((1, 1, L0, 32), np.uint16)
+        seq = QE.QSequence.from_prefill(P, z, z)
+        assert (len(seq.windows), seq.K_tail.shape[2]) == (nw, tail)
+        assert [seq.window_end(P, w) for w in seq.windows] == [5 + 128 * (j + 1) for j in range(nw)]
+
+
+def test_attention_is_the_scaled_softmax_over_gqa_groups():
+    """The tier oracle's own attention: two keys give the logistic of the
+    logit difference q.(k1 - k2) / sqrt(d); query heads 2h, 2h + 1 read KV
+    head h (Hq = 4, Hkv = 2); the output is the probability-weighted sum of
+    the values."""
+    d = 16
+    q = np.zeros((4, d), np.float32)
+    q[:, 0] = [1.0, 2.0, 3.0, -1.0]
+    K = np.zeros((2, 2, d), np.float32)
+    K[0, 0, 0], K[0, 1, 0] = 2.0, -2.0             # KV head 0: logit gap 4 q0 / 4
+    K[1, 0, 0], K[1, 1, 0] = -1.0, 3.0             # KV head 1: logit gap -4 q0 / 4
+    V = np.zeros((2, 2, d), np.float32)
+    V[:, 0, 1], V[:, 1, 1] = 10.0, -6.0
+    p, out = QE.attention_f64(q, K, V)
+    gap = np.array([1.0, 2.0, -3.0, 1.0])          # (l0 - l1) per query head
+    p0 = 1.0 / (1.0 + np.exp(-gap))
+    assert np.allclose(p[:, 0], p0, rtol=1e-14, atol=0)
+    assert np.allclose(p.sum(axis=1), 1.0, rtol=1e-15, atol=0)
+    assert np.allclose(out[:, 1], 10.0 * p0 - 6.0 * (1.0 - p0), rtol=1e-13, atol=0)
+    assert not out[:, 0].any() and not out[:, 2:].any()
 
 
 def test_window_score_is_a_layer_sequential_ema_of_head_mean_mass():
@@ -117,6 +146,27 @@ def test_routing_top_k_full_next_k_quantized_rest_evicted():
     QE.route(P, seq)                                # evicted windows never come back
     assert seq.tiers()[0] == "E" and seq.tiers()[3] == "E" and seq.tiers()[5] == "E"
     assert seq.windows[2].ledger is not None and seq.windows[2].K is None
+
+
+def test_routing_runs_at_the_end_of_every_omega_th_step():
+    """This build's reading of the routing time (the page gives Omega, not
+    where in a step routing falls): an event at the end of each step t with
+    t mod Omega = 0, taking effect from the next step.  Omega = 3, one
+    candidate window, no capacity for it: it is evicted after step 3 and
+    attended until then."""
+    P = _params(k_full=0, k_quant=0, n_recent=1, omega=3)
+    rng = np.random.default_rng(5)
+    K = _bits(rng.standard_normal((1, 1, P.n_sink + P.window + 2, P.head_dim)))
+    seq = QE.QSequence.from_prefill(P, K, K.copy())
+    routed = []
+    for t in range(1, 7):
+        q, kn = (_bits(rng.standard_normal(shape)) for shape in ((1, 1, 32), (1, 1, 32)))
+        res = QE.step(P, seq, t, q, kn, kn)
+        routed.append(res["routed"])
+        attended = (res["owner"] == 0).any()
+        assert attended == (t <= 3)
+    assert routed == [False, False, True, False, False, True]
+    assert seq.tiers() == ["E"]
 
 
 def test_ledger_is_reused_across_migrations():
