@@ -222,6 +222,10 @@ def test_selection_pinned_units_are_forced_in():
     pr = np.array([0.9, 0.1, 0.8, 0.2, 0.95])
     kept = O.select(pr, 2, pinned=np.array([1, 0, 0, 0, 1]))
     assert list(kept) == [0, 4]
+    # forced in even past the budget: three pinned units under B = 2 are all
+    # kept, and nothing else
+    kept = O.select(pr, 2, pinned=np.array([1, 0, 1, 0, 1]))
+    assert list(kept) == [0, 2, 4]
 
 
 def test_beta_infinite_reduces_to_lowest_score_eviction():
@@ -341,6 +345,23 @@ def test_access_clock_threshold():
     assert list(np.nonzero(res["accessed"])[0]) == [2]
     assert res["t_ref_upd"][2] == 3 and res["t_ref_upd"][0] == 0
     assert res["priority"][2] == 0.0                # age 0 after the reset
+
+
+def test_access_threshold_is_inclusive():
+    """Attention of exactly 2/L resets the clock (>=): one prefill token and
+    the new one (L = 2, threshold 1), logits 100 and 0, so the prefill token
+    takes probability exactly 1.0 in fp64 (1 + e^-100 rounds to 1)."""
+    d = 16
+    P = _small_params(n_q_heads=1, n_kv_heads=1, head_dim=d, budget=100,
+                      age_mode=O.AGE_SINCE_ACCESS)
+    K = np.zeros((1, 1, 1, d), np.float32)
+    K[0, 0, 0, 0] = 40.0
+    st = O.SequenceState.from_prefill(_bits(K), _bits(K), 1, 4)
+    q = np.zeros((1, 1, d), np.float32); q[0, 0, 0] = 10.0      # logit 10 * 40 / 4
+    z = np.zeros((1, 1, d), np.uint16)
+    res, _ = O.step(P, st, 5, True, _bits(q), z, z, 1)
+    assert res["score_sum"][0] == 1.0
+    assert bool(res["accessed"][0]) and res["t_ref_upd"][0] == 5
 
 
 def test_step_age_since_insertion_and_budget():
