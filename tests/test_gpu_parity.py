@@ -131,6 +131,14 @@ def test_edge_lengths(L0, budget):
     run_parity(wl, budget, 0.05, 0.001, 4)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_eight_query_heads_per_kv_head(d):
+    """Token mode with 8 query heads per KV head (16 q / 2 KV), both head
+    sizes, two sequences, ragged prefill 260, access-clock ages."""
+    wl = Workload(Geometry(2, 16, 2, d, 2), 260, seed=40 + d, outliers=2, heavy=3)
+    run_parity(wl, 64, 0.05, 0.001, 5, age_mode=O.AGE_SINCE_ACCESS)
+
+
 def test_beta_infinite_and_head_mean():
     """beta = +inf (rank by score, newest token protected) with head-mean
     pooling (Sec. 3.1 Eq. (1))."""
