@@ -82,6 +82,60 @@ def test_null_context_is_rejected(lib):
     lib.kvev_destroy(None)   # no-op
 
 
+def _out():
+    return ctypes.byref(ctypes.c_int64())
+
+
+# every entry point that takes a context, called with a NULL one (and NULL
+# for its other pointers): KVEV_EINVAL with a message, before any CUDA call
+NULL_CTX_CALLS = {
+    "kvev_length": lambda L: L.kvev_length(None, _out()),
+    "kvev_init_state": lambda L: L.kvev_init_state(None, None, None),
+    "kvev_step_host": lambda L: L.kvev_step_host(None, None, None, None, None, None, 1, None,
+                                                 None, None, None),
+    "kvev_set_debug": lambda L: L.kvev_set_debug(None, None, None),
+    "kvev_profile": lambda L: L.kvev_profile(None, 1),
+    "kvev_profile_read": lambda L: L.kvev_profile_read(None, None, None),
+    "kvev_launch_count": lambda L: L.kvev_launch_count(None, _out()),
+    "kvev_test_wait_timeout": lambda L: L.kvev_test_wait_timeout(None, 0, 1),
+    "kvev_check_scratch": lambda L: L.kvev_check_scratch(None, None),
+    "kvev_paged_begin": lambda L: L.kvev_paged_begin(None, None, None, 0, None),
+    "kvev_paged_step": lambda L: L.kvev_paged_step(None, None, None, None, None, None, 1, None,
+                                                   None, None, None),
+    "kvev_readmit": lambda L: L.kvev_readmit(None, None, None, 0, 0, 1, None),
+    "kvev_set_tiers": lambda L: L.kvev_set_tiers(None, 1, 1, 8),
+    "kvev_tier_begin": lambda L: L.kvev_tier_begin(None, None, None, 0, None),
+    "kvev_tier_step": lambda L: L.kvev_tier_step(None, None, None, None, None, None, 1, None, None),
+    "kvev_export_state": lambda L: L.kvev_export_state(None, None, _out()),
+    "kvev_import_state": lambda L: L.kvev_import_state(None, None, 0, None),
+}
+
+
+def test_every_context_call_is_covered():
+    with_ctx = {"kvev_refresh_mode", "kvev_configure", "kvev_begin", "kvev_step", "kvev_sync"}
+    no_ctx = {"kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_size",
+              "kvev_attend_noalloc"}
+    assert set(NULL_CTX_CALLS) | with_ctx | no_ctx == set(kvev.EXPORTS)
+
+
+@pytest.mark.parametrize("name", sorted(NULL_CTX_CALLS))
+def test_every_entry_point_rejects_a_null_context(lib, name):
+    assert NULL_CTX_CALLS[name](lib) == kvev.KVEV_EINVAL
+    assert kvev.kvev_last_error()
+
+
+def test_noalloc_rejects_null_buffers_and_bad_layouts(lib):
+    lay = layout(max_ctx=64)
+    one = ctypes.c_void_p(16)          # never dereferenced: refused before any access
+    assert lib.kvev_attend_noalloc(None, one, one, one, 8, one, one, None) == kvev.KVEV_EINVAL
+    assert lib.kvev_attend_noalloc(ctypes.byref(lay), None, one, one, 8, one, one, None) == kvev.KVEV_EINVAL
+    assert lib.kvev_attend_noalloc(ctypes.byref(lay), one, one, one, 0, one, one, None) == kvev.KVEV_EINVAL
+    assert lib.kvev_attend_noalloc(ctypes.byref(lay), one, one, one, 65, one, one, None) == kvev.KVEV_EINVAL
+    bad = layout(head_dim=96)
+    assert lib.kvev_attend_noalloc(ctypes.byref(bad), one, one, one, 8, one, one, None) == \
+        kvev.KVEV_EUNSUPPORTED
+
+
 def test_binding_raises_with_message(lib):
     with pytest.raises(kvev.KvevError) as ei:
         kvev.kvev_create(layout(head_dim=80), 8, 1, 0.05, 0.001)
