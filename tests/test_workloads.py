@@ -69,8 +69,12 @@ def test_needle_is_redrawn_every_period_and_pulls_the_query():
     k = bf16_bits_to_f32(wl.prefill()[0]).astype(np.float64)          # [Ly][b][g][L0][d]
     mean = k[:, 0][:, :, pos, :].mean(axis=2)                         # [Ly][g][d]
     want = q0[0] + 0.5 * np.repeat(mean, 4, axis=1)
-    # both q and the plain draw q0 are bf16 roundings (half an ulp, 2^-9 relative, each)
-    assert np.all(np.abs(q[0] - want) <= 2.0 ** -9 * (np.abs(q[0]) + np.abs(q0[0])) + 1e-6)
+    # q and the plain draw q0 are each a bf16 rounding (unit roundoff 2^-8)
+    assert np.all(np.abs(q[0] - want) <= 2.0 ** -8 * (np.abs(q[0]) + np.abs(q0[0])) + 1e-6)
+    # a query without the pull, or with the full mean, misses by far more
+    for w in (0.0, 1.0):
+        other = q0[0] + w * np.repeat(mean, 4, axis=1)
+        assert np.abs(q[0] - other).max() > 0.05
 
 
 def test_named_workloads_have_the_stated_shapes():
