@@ -1055,7 +1055,9 @@ kvev_status kvev_readmit(kvev_ctx* c, const kvev_paged_cache* pc, const kvev_blo
     kvev_status rc = check_paged(c, pc, bs);
     if (rc != KVEV_OK) return rc;
     if (!c->begun) return fail(KVEV_ESTATE, "kvev_paged_begin must come first");
-    if (c->rp.memdecay) return fail(KVEV_EUNSUPPORTED, "re-admission needs LRFU scoring");
+    if (c->rp.on)
+        return fail(KVEV_EUNSUPPORTED, "re-admission needs LRFU scoring without a region table "
+                    "(the backing tier keeps no region labels)");
     if (seq < 0 || seq >= c->lay.batch)
         return fail(KVEV_EINVAL, "seq %d out of [0, %d)", seq, c->lay.batch);
     if (lid < 0 || lid >= pc->n_backing)

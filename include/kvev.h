@@ -340,7 +340,8 @@ kvev_status kvev_paged_step(kvev_ctx* ctx, const void* q, const void* k_new, con
                             int32_t* n_retained, void* stream);
 
 /* Re-admit prefill block `lid` (0 <= lid < n_backing, a full block) of
- * sequence `seq` (LRFU scoring only)
+ * sequence `seq` (LRFU scoring without a region table, else
+ * KVEV_EUNSUPPORTED: the backing tier keeps no region labels)
  * before the next step (a no-op when it is resident): a free page receives
  * the block's K/V from the backing tier, the block returns to its slot
  * (ascending logical id), its score is the persisted one (persist != 0 and

@@ -18,7 +18,13 @@ keeps one sequence's block list and applies, in the pages' order:
     with the scaled threshold); a re-admitted or newly opened block counts as
     accessed when it enters;
   * whenever the cache holds more than B blocks, the B of lowest priority are
-    kept, ties to the lower slot (Sec. 3.1 of the first paper).
+    kept, ties to the lower slot (Sec. 3.1 of the first paper);
+  * with pinned regions (optional): every token carries a region label and
+    a block holding a token of a pinned region is never evicted (MemDecay
+    Sec. III-A and IV-A: pinning protects whole pages); pinned blocks are
+    forced into the kept set, past the budget when they outnumber it.
+    Decoded tokens take ``decode_region``.  Re-admission is not combined with
+    regions (the backing tier keeps no labels).
 
 Block order is slot order: ascending logical id (prefill blocks first, then
 blocks opened by decoding); a re-admitted block returns to its sorted place.
@@ -40,6 +46,7 @@ class Block:
     m: float = 0.0
     t_ins: int = 0
     t_ref: int = 0
+    region: np.ndarray = None   # [n] labels, with pinned regions only
 
     @property
     def n(self) -> int:
@@ -56,21 +63,37 @@ class PagedSequence:
     backing_K: np.ndarray            # [n_prefill_blocks][Ly][Hkv][page][d]
     backing_V: np.ndarray
     table: dict = field(default_factory=dict)   # lid -> persisted score
+    pinned_regions: tuple = None     # per region label: pinned or not
+    decode_region: int = 0
 
     @staticmethod
-    def from_prefill(K, V, page: int) -> "PagedSequence":
-        """K, V: [Ly][Hkv][L0][d] bits, L0 a multiple of `page`."""
+    def from_prefill(K, V, page: int, region=None, pinned_regions=None,
+                     decode_region: int = 0) -> "PagedSequence":
+        """K, V: [Ly][Hkv][L0][d] bits, L0 a multiple of `page`; `region`:
+        [L0] labels, given together with `pinned_regions`."""
         Ly, Hkv, L0, d = K.shape
         nb = L0 // page
         bk = K.reshape(Ly, Hkv, nb, page, d).transpose(2, 0, 1, 3, 4).copy()
         bv = V.reshape(Ly, Hkv, nb, page, d).transpose(2, 0, 1, 3, 4).copy()
-        blocks = [Block(j, bk[j].copy(), bv[j].copy()) for j in range(nb)]
-        return PagedSequence(blocks, page, nb, bk, bv)
+        lab = (None if pinned_regions is None
+               else np.asarray(region, dtype=np.int64).reshape(nb, page))
+        blocks = [Block(j, bk[j].copy(), bv[j].copy(),
+                        region=None if lab is None else lab[j].copy()) for j in range(nb)]
+        return PagedSequence(blocks, page, nb, bk, bv, {},
+                             None if pinned_regions is None else tuple(pinned_regions),
+                             int(decode_region))
 
     def copy(self) -> "PagedSequence":
-        return PagedSequence([Block(b.lid, b.K.copy(), b.V.copy(), b.m, b.t_ins, b.t_ref)
+        return PagedSequence([Block(b.lid, b.K.copy(), b.V.copy(), b.m, b.t_ins, b.t_ref,
+                                    None if b.region is None else b.region.copy())
                               for b in self.blocks], self.page, self.next_lid, self.backing_K,
-                             self.backing_V, dict(self.table))
+                             self.backing_V, dict(self.table), self.pinned_regions,
+                             self.decode_region)
+
+    def pinned_blocks(self) -> np.ndarray:
+        """Per live block: whether it holds a token of a pinned region."""
+        return np.array([any(self.pinned_regions[r] for r in b.region) for b in self.blocks],
+                        dtype=np.uint8)
 
     @property
     def n_tokens(self) -> int:
@@ -84,6 +107,8 @@ def readmit(seq: PagedSequence, lid: int, t: int, persist: bool = True) -> bool:
     """Bring prefill block `lid` back from the backing tier (no-op when it is
     resident).  Its score is the persisted one (0 when persistence is off or
     it was never evicted); its access time is t."""
+    if seq.pinned_regions is not None:
+        raise ValueError("re-admission is not combined with pinned regions")
     if lid in seq.lids():
         return False
     m = seq.table.get(lid, 0.0) if persist else 0.0
@@ -114,13 +139,16 @@ def step(P: O.OracleParams, seq: PagedSequence, t: int, refresh: bool, q_bits, k
             m0 = 0.0
         else:
             m0 = float(np.mean([b.m for b in seq.blocks]))
-        seq.blocks.append(Block(seq.next_lid, kn.copy(), vn.copy(), m0, t, t))
+        lab = None if seq.pinned_regions is None else np.array([seq.decode_region])
+        seq.blocks.append(Block(seq.next_lid, kn.copy(), vn.copy(), m0, t, t, lab))
         seq.next_lid += 1
     else:
         ob = seq.blocks[-1]
         ob.K = np.concatenate([ob.K, kn], axis=2)
         ob.V = np.concatenate([ob.V, vn], axis=2)
         ob.t_ref = t
+        if seq.pinned_regions is not None:
+            ob.region = np.append(ob.region, seq.decode_region)
     # 2. attention over every live token, slot order
     Kall = np.concatenate([b.K for b in seq.blocks], axis=2)   # [Ly][Hkv][L][d]
     Vall = np.concatenate([b.V for b in seq.blocks], axis=2)
@@ -158,8 +186,9 @@ def step(P: O.OracleParams, seq: PagedSequence, t: int, refresh: bool, q_bits, k
             b.t_ref = t
     pr = np.array([O.priority(b.m, t - (b.t_ref if P.age_mode == O.AGE_SINCE_ACCESS else b.t_ins),
                               P.beta) for b in seq.blocks])
+    pinned = None if seq.pinned_regions is None else seq.pinned_blocks()
     if kept is None:
-        kept = O.select(pr, P.budget)
+        kept = O.select(pr, P.budget, pinned=pinned)
     kept = np.asarray(kept, dtype=np.int64)
     evicted = [j for j in range(nb) if j not in set(kept.tolist())]
     for j in evicted:
@@ -167,5 +196,6 @@ def step(P: O.OracleParams, seq: PagedSequence, t: int, refresh: bool, q_bits, k
     lids_before = [b.lid for b in seq.blocks]
     seq.blocks = [seq.blocks[j] for j in kept]
     return dict(out=out, probs=probs, priority=pr, m_upd=m, accessed=accessed, kept=kept,
+                pinned=pinned,
                 lids_before=lids_before, evicted_lids=[lids_before[j] for j in evicted],
                 L=L, owner=owner, token_sum=tok_sum)

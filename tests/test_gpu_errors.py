@@ -87,6 +87,19 @@ def test_block_and_tier_contexts_refuse_the_other_modes():
     tp.close()
 
 
+def test_readmission_is_refused_with_a_region_table():
+    """The backing tier keeps no region labels, so a context with a region
+    table refuses kvev_readmit (before launching anything)."""
+    table = kvev.region_table([1.0, 1.0], [0.0, 0.0], [False, True],
+                              score_kind=kvev.KVEV_SCORE_LRFU)
+    pp = kvev.PagedEvictionPass(2, 8, 2, 64, 1, 8, 16, 2, 0.05, 0.001, n_backing=4,
+                                regions=table)
+    pp.begin(64)
+    assert _status(pp.readmit, 0, 1) == kvev.KVEV_EUNSUPPORTED
+    kvev.kvev_sync(pp.ctx)
+    pp.close()
+
+
 def test_scratch_that_cannot_be_allocated_is_reported():
     """A layout whose scratch exceeds the device (hundreds of TB): the
     allocation fails, KVEV_ENOMEM comes back, and the device stays usable."""

@@ -152,9 +152,17 @@ def step_and_compare(pp, P, seqs, b, t, ref_now, q, kn, vn, probs, prio, stats):
 
 def run_paged(wl, budget, alpha, beta, steps, *, pps, age_mode=O.AGE_SINCE_ACCESS,
               refresh=kvev.KVEV_REFRESH_FULL, refresh_o=O.REFRESH_FULL, period=1,
-              pool_mean=False, readmit=None, persist=True):
+              pool_mean=False, readmit=None, persist=True, pinned_regions=None, labels=None,
+              decode_region=0):
+    """`pinned_regions` (per label) with `labels` [batch][L0]: LRFU scoring
+    with a region table; blocks holding a pinned token are never evicted."""
     g = wl.geom
     nb0 = wl.L0 // PAGE
+    regions = None
+    if pinned_regions is not None:
+        n = len(pinned_regions)
+        regions = kvev.region_table([1.0] * n, [0.0] * n, pinned_regions,
+                                    score_kind=kvev.KVEV_SCORE_LRFU, decode_region=decode_region)
     pp = kvev.PagedEvictionPass(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, g.batch, pps,
                                 PAGE, budget, alpha, beta, n_backing=nb0,
                                 table_len=nb0 + steps // PAGE + 4,
@@ -162,14 +170,22 @@ def run_paged(wl, budget, alpha, beta, steps, *, pps, age_mode=O.AGE_SINCE_ACCES
                                           if age_mode == O.AGE_SINCE_ACCESS
                                           else kvev.KVEV_AGE_SINCE_INSERT),
                                 pool=kvev.KVEV_POOL_MEAN if pool_mean else kvev.KVEV_POOL_SUM,
-                                refresh=refresh, period=period)
+                                refresh=refresh, period=period, regions=regions)
     load_pool(pp, wl, nb0)
+    if regions is not None:   # prefill block j of sequence b sits in page b * pps + j
+        lab = torch.zeros((g.batch, pps * PAGE), dtype=torch.uint8)
+        lab[:, :wl.L0] = torch.from_numpy(np.asarray(labels, dtype=np.uint8))
+        pp.region.copy_(lab.reshape(-1))
     pp.begin(wl.L0)
     probs = torch.zeros((g.batch, g.n_layers, g.n_q_heads, pps * PAGE), device="cuda")
     prio = torch.zeros((g.batch, pps), device="cuda")
     kvev.kvev_set_debug(pp.ctx, probs, prio)
     K, V = wl.prefill()
-    seqs = [PG.PagedSequence.from_prefill(K[:, b], V[:, b], PAGE) for b in range(g.batch)]
+    seqs = [PG.PagedSequence.from_prefill(K[:, b], V[:, b], PAGE,
+                                          region=None if labels is None else labels[b],
+                                          pinned_regions=pinned_regions,
+                                          decode_region=decode_region)
+            for b in range(g.batch)]
     P = O.OracleParams(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, budget, alpha, beta,
                        age_mode, pool_mean)
     stats = {"swaps": 0, "amb": 0, "readmitted": 0, "out_rel": 0.0, "m_abs": 0.0}
@@ -235,6 +251,37 @@ def test_paged_many_sequences():
 def test_paged_beta_infinite():
     wl = paged_workload(3, prefill_len=256, n_layers=2, batch=1, needle_period=50)
     run_paged(wl, 4, 0.2, math.inf, 6, pps=20)
+
+
+def _labels(batch, L0, pinned_tokens):
+    lab = np.zeros((batch, L0), dtype=np.uint8)
+    for b, toks in enumerate(pinned_tokens):
+        lab[b, list(toks)] = 1
+    return lab
+
+
+def test_paged_lrfu_with_pinned_regions():
+    """LRFU block scoring with a region table: blocks holding a token of the
+    pinned region 1 stay whatever their priority (one token of block 2 in
+    sequence 0; blocks 12, 18 and 19 in sequence 1), the budget's other
+    slots go by priority, and decoded tokens (region 0) are not pinned."""
+    wl = paged_workload(4, prefill_len=320, n_layers=2, batch=2, needle_period=50)
+    lab = _labels(2, 320, [[35], [200, *range(300, 311)]])
+    st = run_paged(wl, 6, 0.05, 0.001, 12, pps=40, pinned_regions=(False, True), labels=lab)
+    print("paged pinned:", st)
+
+
+def test_paged_pinned_blocks_past_the_budget_and_a_pinned_decode_region():
+    """More pinned blocks than the budget (5 under B = 2 in sequence 0): all
+    stay and nothing else; with the decode region pinned too, every block
+    opened by decoding stays as well (sequence 1 holds no pinned prefill)."""
+    wl = paged_workload(5, prefill_len=160, n_layers=2, batch=2, needle_period=50)
+    lab = _labels(2, 160, [[0, 20, 40, 60, 150], []])
+    # a pinned decode region makes the host's page bound grow by one block per
+    # step, so the pool holds the 10 prefill blocks plus one page per step
+    st = run_paged(wl, 2, 0.05, 0.001, 20, pps=32, pinned_regions=(False, True), labels=lab,
+                   decode_region=1)
+    print("paged pinned past budget:", st)
 
 
 @pytest.mark.slow

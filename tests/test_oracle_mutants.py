@@ -93,6 +93,13 @@ MUTANTS += [
     ("paged.py", "m = np.array([O.ema(m[j], s_blk[j], P.alpha)", "m = np.array([O.ema(s_blk[j], m[j], P.alpha)",
      "EMA operands swapped"),
     ("paged.py", "        ob.t_ref = t\n", "        pass\n", "append into the open block is no access"),
+    ("paged.py", "kept = O.select(pr, P.budget, pinned=pinned)", "kept = O.select(pr, P.budget)",
+     "block pinning ignored"),
+    ("paged.py", "return np.array([any(self.pinned_regions[r] for r in b.region)",
+     "return np.array([all(self.pinned_regions[r] for r in b.region)",
+     "block pinned only if all its tokens are"),
+    ("paged.py", "ob.region = np.append(ob.region, seq.decode_region)",
+     "ob.region = np.append(ob.region, 0)", "decoded token joining a block loses its label"),
     # MemDecay oracle
     ("memdecay.py", "a = P.rho * a + (1.0 - P.rho) * A_bar", "a = (1.0 - P.rho) * a + P.rho * A_bar",
      "importance EWMA weights swapped"),

@@ -158,3 +158,58 @@ def test_block_access_when_any_member_token_is_accessed():
     assert list(res["accessed"]) == [False, True, False]  # block 1 holds token 5
     assert res["priority"][1] == 0.0 and res["priority"][0] > 0.0
     assert res["priority"][2] == 0.0                       # opened this step: age 0
+
+
+def _pinned_seq(rng, P, L0, page, region, pinned_regions, decode_region=0, zero_blocks=()):
+    K = rng.standard_normal((P.n_layers, P.n_kv_heads, L0, P.head_dim))
+    for j in zero_blocks:                          # keys of 0: logits 0, the smallest block max
+        K[:, :, j * page:(j + 1) * page] = 0.0
+    V = rng.standard_normal((P.n_layers, P.n_kv_heads, L0, P.head_dim))
+    return PG.PagedSequence.from_prefill(_bits(K), _bits(V), page, region=region,
+                                         pinned_regions=pinned_regions,
+                                         decode_region=decode_region)
+
+
+def test_a_block_with_a_pinned_token_is_never_evicted():
+    """MemDecay Sec. III-A / IV-A under LRFU: one token of block 0 is in a
+    pinned region, so block 0 survives although its priority is the highest
+    (its keys are 0, its block max the smallest); the other slot goes to
+    the lowest priority (the new block, age 0; ages since insertion, so every
+    prefill block is one step old)."""
+    rng = np.random.default_rng(11)
+    P = _params(n_layers=1, n_q_heads=2, n_kv_heads=1, head_dim=8, budget=2,
+                age_mode=O.AGE_SINCE_INSERT)
+    region = np.zeros(16, dtype=np.int64)
+    region[2] = 1
+    seq = _pinned_seq(rng, P, 16, 4, region, (False, True), zero_blocks=(0,))
+    res = PG.step(P, seq, 1, True, *_inputs(rng, P))
+    assert list(res["pinned"]) == [1, 0, 0, 0, 0]
+    assert int(np.argmax(res["priority"])) == 0      # unpinned, block 0 would go first
+    assert 0 not in O.select(res["priority"], 2)
+    assert seq.lids() == [0, 4]
+
+
+def test_pinned_blocks_past_the_budget_are_all_kept():
+    """Forced in even past the budget: three pinned blocks under B = 2 stay,
+    and nothing else does (not even the new block of priority 0)."""
+    rng = np.random.default_rng(12)
+    P = _params(n_layers=1, n_q_heads=2, n_kv_heads=1, head_dim=8, budget=2)
+    region = np.repeat([1, 0, 1, 1], 4)
+    seq = _pinned_seq(rng, P, 16, 4, region, (False, True))
+    res = PG.step(P, seq, 1, True, *_inputs(rng, P))
+    assert res["priority"][4] == 0.0
+    assert seq.lids() == [0, 2, 3]
+
+
+def test_decoded_tokens_take_the_decode_region():
+    """With a pinned decode region every block opened by decoding is pinned:
+    under B = 1 they accumulate while the prefill blocks go."""
+    rng = np.random.default_rng(13)
+    P = _params(n_layers=1, n_q_heads=2, n_kv_heads=1, head_dim=8, budget=1)
+    seq = _pinned_seq(rng, P, 8, 2, np.zeros(8, dtype=np.int64), (False, True), decode_region=1)
+    for t in range(1, 6):
+        PG.step(P, seq, t, True, *_inputs(rng, P))
+    assert seq.lids() == [4, 5, 6]                   # tokens 1-2, 3-4 and 5 of decoding
+    assert [b.region.tolist() for b in seq.blocks] == [[1, 1], [1, 1], [1]]
+    with pytest.raises(ValueError):
+        PG.readmit(seq, 0, 6)
