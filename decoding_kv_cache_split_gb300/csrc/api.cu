@@ -1462,7 +1462,29 @@ kvev_status kvev_import_state(kvev_ctx* c, const void* host, size_t bytes, void*
                     "or region table");
     if (h.n_ub < 0 || h.n_pin < 0 || bytes < sizeof h + 4 * ((size_t)h.n_ub + h.n_pin))
         return fail(KVEV_EINVAL, "truncated blob");
+    // Every blob this library exports satisfies these; a damaged one would
+    // otherwise reach a division (the lazy period, the routing interval) or
+    // size a launch.  Nothing of the context changes before they pass.
+    const auto in_range = [](int64_t x, int64_t lo, int64_t hi) { return x >= lo && x <= hi; };
+    const int32_t nb = c->lay.batch;
+    bool sane = in_range(h.refresh_mode, KVEV_REFRESH_FULL, KVEV_REFRESH_FROZEN) &&
+                h.refresh_period >= 1 && in_range(h.age_mode, 0, 1) && in_range(h.pool, 0, 1) &&
+                h.omega >= 1 && h.step >= 0 && h.len >= 0 && h.prefill_len >= 0 &&
+                (h.n_ub == 0 || h.n_ub == nb) && (h.n_pin == 0 || h.n_pin == nb);
+    if (c->lay.page_tokens == kTierW) {
+        const int mw = tier_max_windows(c->lay);
+        sane = sane && in_range(h.k_full, 0, mw) && in_range(h.k_quant, 0, mw) &&
+               in_range(h.t_nw, 0, mw) && in_range(h.t_first_u, 0, h.t_nw) &&
+               in_range(h.t_tl, 0, kTierW - 1) && in_range(h.t_nf, 0, mw) &&
+               in_range(h.t_nq, 0, mw);
+    }
     const char* in = static_cast<const char*>(host);
+    for (int32_t i = 0; sane && i < h.n_ub + h.n_pin; ++i) {
+        int32_t x;
+        memcpy(&x, in + sizeof h + 4 * (size_t)i, 4);
+        sane = x >= 0;
+    }
+    if (!sane) return fail(KVEV_EINVAL, "state blob with fields out of range (damaged?)");
     c->refresh_mode = h.refresh_mode;
     c->refresh_period = h.refresh_period;
     c->age_mode = h.age_mode;
