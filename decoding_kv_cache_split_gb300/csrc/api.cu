@@ -48,7 +48,10 @@ enum {
     kProfReadmit
 };
 
-// Target size of the logits of one group of layers (see kvev_step).
+// Target size of the logits of one group of layers (see kvev_step).  Far
+// above any real cache, so every layer forms one group: groups small enough
+// for their logits to stay in L2 were measured slower (the extra attention
+// launches cost more than the HBM traffic they saved).
 constexpr int64_t kLogitGroupBytes = int64_t(1) << 40;
 
 // An NVTX range around each step-level call (free when no tool is attached).
@@ -646,9 +649,10 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     sc.beta = c->beta;
     sc.access_thr = (float)(2.0 * Ly.n_q_heads * Ly.n_layers / (double)L);
 
-    // On refresh steps the layers go in groups whose logits fit comfortably
-    // in L2 (the scoring kernel reads them right after the group's attention
-    // and drops the lines, so they need not reach HBM).
+    // On refresh steps the layers go in groups of about kLogitGroupBytes of
+    // logits, each group's attention followed by its scoring (which reads
+    // the logits once and drops the lines from L2); with the target above,
+    // one group holds every layer.
     const int64_t rows_per_layer = (int64_t)Ly.batch * Ly.n_kv_heads;
     const int64_t logit_bytes_per_layer = rows_per_layer * L * G * 4;
     int group_layers = Ly.n_layers;
