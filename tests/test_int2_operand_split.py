@@ -1,0 +1,87 @@
+"""Numerics of the INT2 attention's operands, restated in numpy.
+
+A key is k_c = s_c (code_c - 1.5) + (z_c + 1.5 s_c).  The tensor cores
+multiply, channel by channel:
+- the A operand, q_c s_c 2^96 in fp32, split into a bf16 hi part (the value
+  truncated) and a bf16 lo part (the exact remainder, rounded);
+- the B operand, the centred code as the exact subnormal bf16 (2 code - 3)
+  2^-128.
+Products are exact and sums fp32.  Times 2^31 plus the bias
+sum_c q_c (z_c + 1.5 s_c), that gives q.k.  Checked here:
+- the split loses at most 2^-16 of each operand;
+- the logit is within 1e-5 of sum_c |q_c k_c| (2e-6 seen) of the fp64 dot
+  product of q with the dequantized key (code * scale + zero in fp32), far
+  inside the 2e-3 probability tolerance;
+- the hi part alone is not enough, missing by ~1.3e-3 of the same sum."""
+import numpy as np
+
+F = np.float32
+
+
+def bf16_trunc(x):
+    return (np.asarray(x, F).view(np.uint32) & np.uint32(0xFFFF0000)).view(F)
+
+
+def bf16_rn(x):
+    u = np.asarray(x, F).view(np.uint32).astype(np.uint64)
+    return (((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16).astype(np.uint32).view(F)
+
+
+def split(a):
+    hi = bf16_trunc(a)
+    lo = bf16_rn((a - hi).astype(F))              # a - hi is exact in fp32
+    return hi, lo
+
+
+def test_split_loses_at_most_two_to_the_minus_16():
+    rng = np.random.default_rng(0)
+    a = (rng.standard_normal(200000) * np.exp2(rng.uniform(-20, 20, 200000))).astype(F)
+    hi, lo = split(a)
+    err = np.abs(hi.astype(np.float64) + lo.astype(np.float64) - a.astype(np.float64))
+    assert np.all(err <= 2.0 ** -16 * np.abs(a.astype(np.float64)))
+
+
+def _case(rng, n=128, key_scale=1.0):
+    q = bf16_rn(rng.standard_normal(n).astype(F))
+    x = (rng.standard_normal((32, n)) * key_scale).astype(F)          # a 32-token key group
+    zero = x.min(axis=0).astype(np.float16)
+    scale = ((x.max(axis=0) - x.min(axis=0)) / F(3)).astype(np.float16)
+    s32, z32 = scale.astype(F), zero.astype(F)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        codes = np.clip(np.rint((x[0] - z32) / s32), 0, 3)
+    codes = np.where(s32 == 0, 0, codes)
+    return q, codes, s32, z32
+
+
+def _device_logit(q, codes, s, z, use_lo=True):
+    a = (q * s * F(2.0 ** 96)).astype(F)                 # q s 2^96
+    hi, lo = split(a)
+    b = ((2 * codes - 3) * 2.0 ** -128)                   # exact subnormal bf16 values
+    acc = F(0)
+    for c in range(len(q)):                               # exact products, fp32 sums
+        acc = F(acc + F(hi[c] * b[c]))
+        if use_lo:
+            acc = F(acc + F(lo[c] * b[c]))
+    bias = F(0)
+    for c in range(len(q)):
+        bias = F(bias + F(q[c] * F(z[c] + F(1.5) * s[c])))
+    return float(F(acc * F(2.0 ** 31)) + bias)
+
+
+def _reference_logit(q, codes, s, z):
+    k = (codes.astype(F) * s + z).astype(F)               # the oracle's dequantized key
+    return float(np.dot(q.astype(np.float64), k.astype(np.float64)))
+
+
+def test_logits_from_the_split_operands_match_the_dequantized_keys():
+    rng = np.random.default_rng(1)
+    worst = worst_hi_only = 0.0
+    for trial in range(300):
+        q, codes, s, z = _case(rng, key_scale=(0.05, 1.0, 20.0)[trial % 3])
+        ref = _reference_logit(q, codes, s, z)
+        norm = float(np.sum(np.abs(q.astype(np.float64) * (codes * s + z))))
+        worst = max(worst, abs(_device_logit(q, codes, s, z) - ref) / norm)
+        worst_hi_only = max(worst_hi_only,
+                            abs(_device_logit(q, codes, s, z, use_lo=False) - ref) / norm)
+    assert worst <= 1e-5, worst                  # fp32 roundings of the 256 summed products
+    assert worst_hi_only >= 1e-4, worst_hi_only  # the lo part carries ~8 more bits
