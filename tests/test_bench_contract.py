@@ -83,3 +83,15 @@ def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
     s = bench.ClockSampler(0)
     s.start()
     assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_cpu_baseline_repeats_the_oracle_step_to_a_bounded_sample():
+    from workloads import llama8b_workload
+    wl = llama8b_workload(0, prefill_len=400, n_layers=2)
+    val, secs, sample = bench.cpu_baseline(wl, 2, min_seconds=0.2, max_reps=3)
+    reps = int(sample.split("timed ")[1].split()[0])
+    assert 1 <= reps <= 3 and secs > 0
+    assert "first 2 of 32 layers (all 401 tokens)" in sample
+    nbytes, _ = bench.kv_bytes(2, bench.WORKLOAD["n_kv_heads"], bench.WORKLOAD["head_dim"], 401,
+                               bench.WORKLOAD["budget"])
+    assert val == pytest.approx(nbytes * reps / secs / 1e9)
