@@ -60,6 +60,9 @@ TIERS = dict(workload="two-tier (QEvict) windows, 4 x 131072 tokens, 5% bf16 + 2
              window=128, sinks=5, recent=32, k_full=51, k_quant=204, omega=8, alpha=0.05,
              int2="keys per channel / values per token, groups of 32, fp16 scale and zero",
              needle="16 positions re-drawn every 64 steps")
+# decode steps of the workloads the headline line carries (the block run
+# reaches the re-admission at t = 201; the two-tier run 32 routing events)
+WORKLOAD_STEPS = {"paged": 256, "memdecay": 128, "tiers": 256}
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -98,16 +101,43 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_sha256(text: str) -> str:
+    """Hash of a CUDA source's code: comments dropped and whitespace runs
+    collapsed, so a comment edit keeps a DRAM record while any change of the
+    code voids it."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':                                   # string literal: kept as is
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    code = " ".join("".join(out).split())
+    return hashlib.sha256(code.encode()).hexdigest()
+
+
 def _traffic_record(key: str, kernel_file: str):
     """The committed ncu DRAM record `key`, if it was taken on the current
-    source of `kernel_file`; else None."""
+    code of `kernel_file`; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as fh:
             rec = json.load(fh)[key]
         src = open(os.path.join(ROOT, "decoding_kv_cache_split_gb300", "csrc", kernel_file),
-                   "rb").read()
-        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+                   encoding="utf-8").read()
+        if rec.get("code_sha256") != code_sha256(src):
             return None
         return rec
     except Exception:
@@ -233,6 +263,9 @@ def reference_arm(args, rank, world):
     P = O.OracleParams(1, W["n_q_heads"], W["n_kv_heads"], W["head_dim"], budget, W["alpha"],
                        W["beta"], O.AGE_SINCE_ACCESS)
 
+    n_cores, model = host_cpu()
+    used = O.set_threads(n_cores)
+
     def one():
         O.step(P, st, 1, True, q[0], kn[0], vn[0], tokens, want_probs=False)
 
@@ -245,14 +278,15 @@ def reference_arm(args, rank, world):
     nbytes, _ = kv_bytes(1, W["n_kv_heads"], W["head_dim"], tokens + 1, budget)
     val = nbytes / dt / 1e9
     sample = (f"1 of 32 layers, {tokens}-token prefill + 1, budget {budget} "
-              f"(same geometry, alpha, beta, access clock)")
+              f"(same geometry, alpha, beta, access clock); the attention's query heads on "
+              f"{used} threads")
     line = {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": dict(W, sample=sample),
-            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1,
-                             "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": used,
+                             "kind": "oracle", "cpu": model, "sample": sample},
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -276,7 +310,10 @@ def replay_mode(fh, ctx, ep, step_in, step_ms, alpha, name, period, L0, B, row, 
     kvev.kvev_begin(ctx, L0)
     kvev.kvev_init_state(ctx, ep.state, stream)
     prev, step_bytes = None, []
+    kvev.kvev_profile(ctx, True)          # per-kernel events of steps 2.. (synchronised steps)
     for t, ins in enumerate(step_in, start=1):
+        if t == 2:
+            kvev.kvev_profile_read(ctx)    # drop step 1
         L = kvev.kvev_length(ctx) + 1                 # live tokens after the append
         kvev.kvev_step(ctx, *ins, ep.cache, ep.state, t, ep.out, ep.retained, ep.n_retained,
                        stream)
@@ -299,7 +336,54 @@ def replay_mode(fh, ctx, ep, step_in, step_ms, alpha, name, period, L0, B, row, 
                                  "churn": None if churn is None else round(churn, 6),
                                  "first_moved_row": first_gap}) + "\n")
             prev = kept
-    return step_bytes
+    prof = kvev.kvev_profile_read(ctx)
+    kvev.kvev_profile(ctx, False)
+    n = max(1, len(step_in) - 1)
+    kernels = {k: round(v[0] / n * 1e3, 2) for k, v in prof.items()}
+    return step_bytes, kernels
+
+
+def steady_graph_us(ctx, ep, step_in, L0, k0, v0, stream, warmup, n_capture=8, reps=25):
+    """Steady steps replayed from a CUDA graph: decode steps 2..9 of a run
+    are captured once (their kernels, with the sizes and buffers of those
+    steps) and the graph is replayed; returns the time per step in us.  The
+    replays redo the same eight steps' work on the evolving state (same
+    sizes: the cache stays at the budget), which is what the timing needs."""
+    import torch
+    from decoding_kv_cache_split_gb300 import kvev
+    ep.k[0].copy_(k0)
+    ep.v[0].copy_(v0)
+    ep.cache.cur = 0
+    kvev.kvev_begin(ctx, L0)
+    kvev.kvev_init_state(ctx, ep.state, stream)
+    kvev.kvev_step(ctx, *step_in[0], ep.cache, ep.state, 1, ep.out, ep.retained, ep.n_retained,
+                   stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        for t in range(2, 2 + n_capture):
+            kvev.kvev_step(ctx, *step_in[t - 1], ep.cache, ep.state, t, ep.out, ep.retained,
+                           ep.n_retained, cs)
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    kvev.kvev_sync(ctx)
+    del g
+    return round(e0.elapsed_time(e1) / (reps * n_capture) * 1e3, 2)
+
+
+def finish_dist(world):
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
 
 
 def main():
@@ -325,6 +409,11 @@ def main():
                     help="the headline token-granular step, or the block-granular run")
     ap.add_argument("--batch", type=int, default=PAGED["batch"],
                     help="paged workload: sequences (profiling cases only)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="the headline line only: skip the block, region-aware and two-tier "
+                         "workloads it carries under 'workloads'")
+    ap.add_argument("--omega", type=int, default=TIERS["omega"],
+                    help="two-tier workload: routing interval")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -337,25 +426,17 @@ def main():
         return
 
     if args.workload in ("paged", "memdecay"):
-        bench_paged(args, rank, world, local_rank)
+        bench_paged(args, rank, world, local_rank, md=args.workload == "memdecay")
+        finish_dist(world)
         return
     if args.workload == "tiers":
-        bench_tiers(args, rank, world, local_rank)
+        bench_tiers(args, rank, world, local_rank, omega=args.omega)
+        finish_dist(world)
         return
 
     import torch
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-
-    from decoding_kv_cache_split_gb300 import build as kbuild
-    if not os.path.exists(kbuild.LIB):
-        kbuild.build()
-    from decoding_kv_cache_split_gb300 import kvev
+    dist = init_dist(world, local_rank)
+    kvev = load_kvev()
     from workloads import llama8b_workload
 
     W = dict(WORKLOAD)
@@ -446,15 +527,18 @@ def main():
     value = job_rate(nbytes, world, ms) / 1e9
 
     # -------------------------------------------------- end to end (host API)
+    # the user's call: host buffers in, the bf16 attention output (the type a
+    # caller feeds to the next bf16 projection) and the retained list back
+    kvev.kvev_set_output(ep.ctx, kvev.KVEV_OUT_BF16)
     qh = torch.from_numpy(q.view(np.int16)).pin_memory()
     knh = torch.from_numpy(kn.view(np.int16)).pin_memory()
     vnh = torch.from_numpy(vn.view(np.int16)).pin_memory()
     outh = torch.empty((1, W["n_layers"], W["n_q_heads"], W["head_dim"]),
-                       dtype=torch.float32).pin_memory()
+                       dtype=torch.bfloat16).pin_memory()
     reth = torch.empty((1, B), dtype=torch.int32).pin_memory()
     nreth = torch.empty((1,), dtype=torch.int32).pin_memory()
     h2d = qh.numel() * 2 + knh.numel() * 2 + vnh.numel() * 2
-    d2h = outh.numel() * 4 + reth.numel() * 4 + nreth.numel() * 4
+    d2h = outh.numel() * 2 + reth.numel() * 4 + nreth.numel() * 4
 
     def one_e2e(step_no=1):
         ep.begin(L0, stream)
@@ -475,6 +559,7 @@ def main():
     e2e_ms = slowest_ms(e2e_ms, dist)
     e2e_val = job_rate(nbytes, world, e2e_ms) / 1e9
     assert int(nreth[0]) == B
+    kvev.kvev_set_output(ep.ctx, kvev.KVEV_OUT_F32)
 
     # ------------------------------------- refresh modes x alphas (steady state)
     # Every (alpha, mode) run starts from the prefill at step 1 and decodes
@@ -509,13 +594,20 @@ def main():
                 kvev.kvev_sync(ctx)
                 st = [evs[t - 1].elapsed_time(evs[t]) for t in range(1, n_ms + 1)]
                 steady = sum(st[1:]) / max(1, n_ms - 1)
-                sb = replay_mode(step_log, ctx, ep, step_in, st, alpha, name, period, L0, B,
-                                 row, k0, v0, stream)
+                sb, kern = replay_mode(step_log, ctx, ep, step_in, st, alpha, name, period, L0,
+                                       B, row, k0, v0, stream)
                 steady_bytes = sum(sb[1:]) / max(1, n_ms - 1)   # attention + shifted rows
-                modes.append({"alpha": alpha, "mode": name, "step1_us": round(st[0] * 1e3, 1),
-                              "steady_us": round(steady * 1e3, 1),
-                              "steady_GBps": round(steady_bytes / (steady * 1e-3) / 1e9, 1),
-                              "steady_bytes": int(steady_bytes)})
+                rec = {"alpha": alpha, "mode": name, "step1_us": round(st[0] * 1e3, 1),
+                       "steady_us": round(steady * 1e3, 1),
+                       "steady_GBps": round(steady_bytes / (steady * 1e-3) / 1e9, 1),
+                       "steady_frac_measured": round(steady_bytes / (steady * 1e-3) / 1e9
+                                                     / measured_peak()[0], 4),
+                       "steady_bytes": int(steady_bytes),
+                       "steady_kernels_us": kern}
+                if alpha == 0.05 and not args.no_graph:
+                    rec["steady_graph_us"] = steady_graph_us(ctx, ep, step_in, L0, k0, v0,
+                                                             stream, args.warmup)
+                modes.append(rec)
             kvev.kvev_destroy(ctx)
         del k0, v0, step_in
     if step_log is not None:
@@ -538,9 +630,17 @@ def main():
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            val, secs, sample = cpu_baseline(wl, min(args.cpu_layers, W["n_layers"]))
-            cpu = {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                   "sample": sample, "seconds": round(secs, 2)}
+            import oracle as O
+            n_cores, model = host_cpu()
+            O.set_threads(1)
+            val1, secs1, sample = cpu_baseline(wl, min(args.cpu_layers, W["n_layers"]))
+            used = O.set_threads(n_cores)
+            valn, secsn, _ = cpu_baseline(wl, min(args.cpu_layers, W["n_layers"]))
+            cpu = {"value": round(valn, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+                   "cpu": model, "sample": sample + f"; the attention's query heads on {used} "
+                   "threads (OpenMP)", "seconds": round(secsn, 2),
+                   "single_thread": {"value": round(val1, 4), "cores": 1,
+                                     "seconds": round(secs1, 2)}}
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -560,43 +660,147 @@ def main():
                          "peak_kind": f"{peak_kind} (copy bandwidth)"},
             "kernels_us": kernels_us,
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "output": "bf16",
+                    "call": "kvev_step_host"},
             "graph": ({"us_per_step": round(graph_us, 2), "replays": args.steps} if graph_us else None),
             "gpu_launches": launches,
             "clocks": clk,
             "cpu_baseline": cpu,
             "modes": modes,
         }
-        print(json.dumps(line), flush=True)
     ep.close()
-    if dist:
-        dist.destroy_process_group()
+    del ep
+    torch.cuda.empty_cache()
+
+    # ------------------------------ the other workloads, each at its own size
+    # (block-granular with re-admission, region-aware, two-tier INT2); their
+    # step counts are fixed so that the run stays within a few minutes
+    if not args.no_workloads and args.layers == WORKLOAD["n_layers"] and \
+            args.prefill == WORKLOAD["prefill"]:
+        subs = []
+        for name, fn in (("paged", lambda: bench_paged(args, rank, world, local_rank,
+                                                        steps=WORKLOAD_STEPS["paged"],
+                                                        quiet=True)),
+                         ("memdecay", lambda: bench_paged(args, rank, world, local_rank, md=True,
+                                                           steps=WORKLOAD_STEPS["memdecay"],
+                                                           quiet=True)),
+                         ("tiers", lambda: bench_tiers(args, rank, world, local_rank,
+                                                       steps=WORKLOAD_STEPS["tiers"],
+                                                       quiet=True))):
+            rec = fn()
+            if rec is not None:
+                rec = {k: v for k, v in rec.items() if k not in ("metric", "n_gpus", "warmup")}
+                rec["name"] = name
+                subs.append(rec)
+        if line is not None:
+            line["workloads"] = subs
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    finish_dist(world)
 
 
-def bench_paged(args, rank, world, local_rank):
-    """Block-granular runs.  "paged": 64 sequences of 8192 tokens in 16-token
-    blocks, budget 128 blocks; step 1 evicts from 513 to 128 blocks per
-    sequence, later steps attend over ~2049 tokens per sequence; the needle
-    blocks are re-admitted (scores restored) when the needle is re-drawn.
-    "memdecay": Qwen2.5-3B geometry, 32 sequences of 16384 region-labelled
-    tokens, MemDecay page scores, budget 4915 tokens.  Timed: K consecutive
-    decode steps after step 1 (readmissions included); step 1 alone is timed
-    separately (re-run on the untouched prefill pages)."""
+def init_dist(world, local_rank):
+    """The process group under torchrun (None for one process) and the device."""
     import torch
-    dist = None
     if world > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
+        if not dist.is_initialized():
+            dist.init_process_group("nccl")
+        return dist
+    torch.cuda.set_device(0)
+    return None
+
+
+def load_kvev():
     from decoding_kv_cache_split_gb300 import build as kbuild
     if not os.path.exists(kbuild.LIB):
         kbuild.build()
     from decoding_kv_cache_split_gb300 import kvev
+    return kvev
+
+
+def host_cpu():
+    """(logical CPUs, CPU model) of this host, for the CPU-baseline legs."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        import platform
+        model = platform.processor() or platform.machine()
+    return os.cpu_count() or 1, model
+
+
+def timed_reps(fn, min_seconds: float, max_reps: int):
+    """Run fn until about min_seconds of wall time (at least once); returns
+    (repetitions, seconds)."""
+    total, reps = 0.0, 0
+    while reps < 1 or (total < min_seconds and reps < max_reps):
+        t0 = time.perf_counter()
+        fn()
+        total += time.perf_counter() - t0
+        reps += 1
+    return reps, total
+
+
+def cpu_baseline_block(kind, W, seq_K, seq_V, inputs1, labels=None, min_seconds=8.0):
+    """The oracle of a block workload (oracle/paged.py or oracle/memdecay.py)
+    on one sequence of the batch, decode step 1 over its whole prefill,
+    repeated to about `min_seconds`; the sequences are independent, so one
+    sequence's time is the per-sequence cost of the batch.  Threads: the
+    oracle's attention runs its query heads on all host cores."""
+    import oracle as O
+    q, kn, vn = inputs1
+    Ly, d = W["n_layers"], W["head_dim"]
+    if kind == "memdecay":
+        import math
+        from oracle import memdecay as MD
+        from workloads import DECODE_REGION, REGION_HALF_LIVES, REGION_PINNED
+        lam = tuple(math.log(2.0) / h for h in REGION_HALF_LIVES)
+        P = MD.MDParams(Ly, W["n_q_heads"], W["n_kv_heads"], d, W["budget_tokens"],
+                        base=(1.0,) * len(lam), lam=lam, pinned=REGION_PINNED,
+                        decode_region=DECODE_REGION)
+        seq0 = MD.MDSequence.from_prefill(seq_K, seq_V, labels, W["page"])
+        fn = lambda: MD.step(P, seq0.copy(), 1, True, q, kn, vn)
+    else:
+        from oracle import paged as PG
+        P = O.OracleParams(Ly, W["n_q_heads"], W["n_kv_heads"], d, W["budget_blocks"],
+                           W["alpha"], W["beta"], O.AGE_SINCE_ACCESS, False)
+        seq0 = PG.PagedSequence.from_prefill(seq_K, seq_V, W["page"])
+        fn = lambda: PG.step(P, seq0.copy(), 1, True, q, kn, vn)
+    threads = O.set_threads(os.cpu_count() or 1)
+    reps, secs = timed_reps(fn, min_seconds, 4)
+    row = 2 * d * 2 * W["n_kv_heads"] * Ly
+    nbytes = (W["prefill"] + 1) * row
+    cores, model = host_cpu()
+    return {"value": round(nbytes * reps / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "cpu": model, "seconds": round(secs, 2),
+            "sample": f"decode step 1 of sequence 0 of {W['batch']} ({W['prefill']} + 1 tokens, "
+                      f"all {Ly} layers), timed {reps} times; sequences are independent"}
+
+
+def bench_paged(args, rank, world, local_rank, md=False, steps=None, quiet=False):
+    """Block-granular runs.  Block workload: 64 sequences of 8192 tokens in
+    16-token blocks, budget 128 blocks; step 1 evicts from 513 to 128 blocks
+    per sequence, later steps attend over ~2049 tokens per sequence; the
+    needle blocks are re-admitted (scores restored) when the needle is
+    re-drawn.  Region-aware (md): Qwen2.5-3B geometry, 32 sequences of 16384
+    region-labelled tokens, MemDecay page scores, budget 4915 tokens.  Timed:
+    K consecutive decode steps after step 1 (readmissions included); step 1
+    alone is timed separately (re-run on the untouched prefill pages).
+    Returns the JSON record (rank 0) or None."""
+    import torch
+    dist = init_dist(world, local_rank)
+    kvev = load_kvev()
     from workloads.device import PagedDeviceWorkload
 
-    md = args.workload == "memdecay"
     W = dict(MEMDECAY if md else PAGED)
     if args.layers != WORKLOAD["n_layers"] or args.batch != PAGED["batch"] or \
             args.prefill != WORKLOAD["prefill"]:
@@ -610,6 +814,7 @@ def bench_paged(args, rank, world, local_rank):
     Ly, b, P = W["n_layers"], W["batch"], W["page"]
     nb0 = -(-W["prefill"] // P)
     pps = nb0 + 8
+    labels = None
     if md:
         import math
         from workloads import (DECODE_REGION, REGION_HALF_LIVES, REGION_PINNED,
@@ -625,8 +830,9 @@ def bench_paged(args, rank, world, local_rank):
         pp = kvev.PagedEvictionPass(Ly, W["n_q_heads"], W["n_kv_heads"], W["head_dim"], b, pps,
                                     P, W["budget_tokens"], 0.05, 0.001, regions=table)
         wl.fill(torch, pp.k_pool, pp.v_pool, pps)
+        labels = region_labels(W["prefill"])
         lab = np.zeros(nb0 * P, np.uint8)
-        lab[:W["prefill"]] = region_labels(W["prefill"])
+        lab[:W["prefill"]] = labels
         lab_t = torch.from_numpy(lab).cuda()
         for s_ in range(b):
             pp.region[s_ * pps * P:s_ * pps * P + nb0 * P].copy_(lab_t)
@@ -638,7 +844,7 @@ def bench_paged(args, rank, world, local_rank):
                                     P, W["budget_blocks"], W["alpha"], W["beta"], n_backing=nb0,
                                     table_len=nb0, age_mode=kvev.KVEV_AGE_SINCE_ACCESS)
         wl.fill(torch, pp.k_pool, pp.v_pool, pps, pp.backing_k, pp.backing_v)
-    n_steps = args.steps
+    n_steps = steps if steps is not None else args.steps
     last = max(n_steps + 1, args.warmup)
     inputs = [wl.step_inputs(torch, t, pp.backing_k) for t in range(1, last + 1)]
     readmits = {}
@@ -690,6 +896,7 @@ def bench_paged(args, rank, world, local_rank):
     run_step(1)
     kvev.kvev_sync(pp.ctx)
     kvev.kvev_profile_read(pp.ctx)
+
     def live_tokens():
         nb, lens = pp.n_blocks.cpu().numpy(), pp.len.cpu().numpy()
         return int(sum(lens[s, :nb[s]].sum() for s in range(b)))
@@ -721,7 +928,7 @@ def bench_paged(args, rank, world, local_rank):
     kernels_us = {k: round(v[0] / n_steps * 1e3, 2) for k, v in prof.items()}
     kernels_us["launches_per_step"] = {k: round(v[1] / n_steps, 2) for k, v in prof.items()}
 
-    # step 1 alone: 64 x 8193 tokens, eviction to 128 blocks
+    # step 1 alone: every sequence's whole prefill, eviction to the budget
     n1 = 10
     pp.begin(W["prefill"], stream)
     run_step(1)
@@ -738,16 +945,19 @@ def bench_paged(args, rank, world, local_rank):
     kvev.kvev_sync(pp.ctx)
     step1_bytes = b * (W["prefill"] + 1) * row
 
-    # end to end: host inputs (pinned) in, outputs out, every step
+    # end to end: host inputs (pinned) in, the bf16 output and the kept ids
+    # back, every step
+    kvev.kvev_set_output(pp.ctx, kvev.KVEV_OUT_BF16)
+    out_dev = torch.empty(pp.out.shape, dtype=torch.bfloat16, device="cuda")
     n_e2e = min(n_steps, 64)
     host_in = [tuple(x.view(torch.int16).cpu().pin_memory() for x in inputs[t - 1])
                for t in range(2, n_e2e + 2)]
     dev_in = [torch.empty_like(x) for x in inputs[0]]
-    out_h = torch.empty(pp.out.shape, dtype=torch.float32).pin_memory()
+    out_h = torch.empty(pp.out.shape, dtype=torch.bfloat16).pin_memory()
     ret_h = torch.empty(pp.retained_lid.shape, dtype=torch.int32).pin_memory()
     nret_h = torch.empty(pp.n_retained.shape, dtype=torch.int32).pin_memory()
     h2d = sum(x.numel() * 2 for x in host_in[0])
-    d2h = out_h.numel() * 4 + ret_h.numel() * 4 + nret_h.numel() * 4
+    d2h = out_h.numel() * 2 + ret_h.numel() * 4 + nret_h.numel() * 4
     pp.begin(W["prefill"], stream)
     run_step(1)
     torch.cuda.synchronize()
@@ -757,13 +967,16 @@ def bench_paged(args, rank, world, local_rank):
             d.view(torch.int16).copy_(h, non_blocking=True)
         for (s, lid) in readmits.get(t, ()):
             pp.readmit(s, lid, True, stream)
-        pp.step(*dev_in, stream)
-        out_h.copy_(pp.out, non_blocking=True)
+        pp.step_no += 1
+        kvev.kvev_paged_step(pp.ctx, *dev_in, pp.cache, pp.state, pp.step_no, out_dev,
+                             pp.retained_lid, pp.n_retained, stream)
+        out_h.copy_(out_dev, non_blocking=True)
         ret_h.copy_(pp.retained_lid, non_blocking=True)
         nret_h.copy_(pp.n_retained, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
     kvev.kvev_sync(pp.ctx)
+    kvev.kvev_set_output(pp.ctx, kvev.KVEV_OUT_F32)
     e2e_val = world * (attn_bytes_total / n_steps) / (e2e_ms * 1e-3) / 1e9
     # DRAM bytes per launch: the algorithmic bytes times the ratio of an ncu
     # capture of the same kernel on a smaller block workload (the region-aware
@@ -771,7 +984,23 @@ def bench_paged(args, rank, world, local_rank):
     ratio = traffic_ratio("attention_paged", "attn.cu")
     paged_traffic = round(attn_bytes_total / n_steps * ratio) if ratio and not md else None
 
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        seq_pages = slice(0, nb0)
+        src_k = pp.k_pool[seq_pages] if md else pp.backing_k[0, :nb0]
+        src_v = pp.v_pool[seq_pages] if md else pp.backing_v[0, :nb0]
+        bits = lambda x: x.view(torch.int16).cpu().numpy().view(np.uint16)
+        Kh = bits(src_k).transpose(1, 2, 0, 3, 4).reshape(Ly, W["n_kv_heads"], -1, W["head_dim"])
+        Vh = bits(src_v).transpose(1, 2, 0, 3, 4).reshape(Ly, W["n_kv_heads"], -1, W["head_dim"])
+        Kh = np.ascontiguousarray(Kh[:, :, :W["prefill"]])
+        Vh = np.ascontiguousarray(Vh[:, :, :W["prefill"]])
+        q1, kn1, vn1 = inputs[0]
+        cpu = cpu_baseline_block("memdecay" if md else "paged", W, Kh, Vh,
+                                 (bits(q1[0]), bits(kn1[0]), bits(vn1[0])), labels)
+        del Kh, Vh
+
     peak, peak_kind = measured_peak()
+    line = None
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -796,62 +1025,62 @@ def bench_paged(args, rank, world, local_rank):
                          "peak_kind": f"{peak_kind} (copy bandwidth)"},
             "kernels_us": kernels_us,
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "output": "bf16", "steps": n_e2e},
             "gpu_launches": launches,
             "clocks": clk,
-            "cpu_baseline": None,
+            "cpu_baseline": cpu,
         }
-        print(json.dumps(line), flush=True)
+        if not quiet:
+            print(json.dumps(line), flush=True)
     pp.close()
-    if dist:
-        dist.destroy_process_group()
+    del pp, inputs
+    torch.cuda.empty_cache()
+    return line
 
 
-def bench_tiers(args, rank, world, local_rank):
+def bench_tiers(args, rank, world, local_rank, steps=None, omega=None, quiet=False,
+                omega_sweep=(1, 32), sweep_steps=96):
     """Two-tier run: 4 sequences of 131072 tokens in 128-token windows, K_f
-    51 bf16 windows, K_q 204 INT2 windows, routing every 8 steps.  Timed: K
-    consecutive decode steps from step 1 of a fresh run (steps 1-7 attend the
-    whole prefill, the first routing event quantizes 204 windows per
-    sequence, later steps attend ~6.6k bf16 and ~26k INT2 tokens per
+    51 bf16 windows, K_q 204 INT2 windows, routing every omega = 8 steps.
+    Timed: K consecutive decode steps from step 1 of a fresh run (steps 1-7
+    attend the whole prefill, the first routing event quantizes 204 windows
+    per sequence, later steps attend ~6.6k bf16 and ~26k INT2 tokens per
     sequence); the steady state (steps after the first event) is reported
-    beside it."""
+    beside it, with the memory the tiers hold (bf16 pages, INT2 ledger) per
+    step, and short runs at other routing intervals (omega_sweep).  Returns
+    the JSON record (rank 0) or None."""
     import torch
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    from decoding_kv_cache_split_gb300 import build as kbuild
-    if not os.path.exists(kbuild.LIB):
-        kbuild.build()
-    from decoding_kv_cache_split_gb300 import kvev
+    dist = init_dist(world, local_rank)
+    kvev = load_kvev()
     from workloads.device import TierDeviceWorkload
 
     W = dict(TIERS)
+    if omega is not None:
+        W["omega"] = int(omega)
     if args.layers != WORKLOAD["n_layers"] or args.prefill != WORKLOAD["prefill"]:
         pre = args.prefill if args.prefill != WORKLOAD["prefill"] else W["prefill"]
         W.update(workload=f"profiling case: {args.layers} layers, {W['batch']} x {pre} tokens",
                  n_layers=args.layers, prefill=pre)
     Ly, b, L0 = W["n_layers"], W["batch"], W["prefill"]
-    n_steps = args.steps
-    max_ctx = L0 + max(n_steps, args.warmup) + 16
+    n_steps = steps if steps is not None else args.steps
+    max_ctx = L0 + max(n_steps, args.warmup, sweep_steps) + 16
     wl = TierDeviceWorkload(0, n_layers=Ly, batch=b, prefill=L0)
     pps = wl.n_pages + 16 + 8 * W["k_full"]
     tp = kvev.TierEvictionPass(Ly, W["n_q_heads"], W["n_kv_heads"], W["head_dim"], b, max_ctx,
                                pps, W["k_full"], W["k_quant"], W["omega"], W["alpha"])
     wl.fill(torch, tp.k_pool, tp.v_pool, pps)
-    last = max(n_steps, args.warmup)
+    last = max(n_steps, args.warmup, sweep_steps if omega_sweep else 0)
     inputs = [wl.step_inputs(torch, t, tp.k_pool, pps) for t in range(1, last + 1)]
     # the prefill pages are reused once windows are routed: keep a copy to restart from
     k0, v0 = tp.k_pool.clone(), tp.v_pool.clone()
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
 
-    def restart():
+    def restart(om=None):
         tp.k_pool.copy_(k0)
         tp.v_pool.copy_(v0)
+        kvev.kvev_set_tiers(tp.ctx, W["k_full"], W["k_quant"], om or W["omega"])
         tp.begin(L0, stream)
 
     restart()
@@ -859,7 +1088,7 @@ def bench_tiers(args, rank, world, local_rank):
         tp.step(*inputs[t - 1], stream)
     kvev.kvev_sync(tp.ctx)
 
-    # timed: steps 1..K of a fresh run, with an event after the first routing event
+    # timed: steps 1..K of a fresh run, with an event after every step
     restart()
     torch.cuda.synchronize()
     n0 = kvev.kvev_launch_count(tp.ctx)
@@ -882,13 +1111,15 @@ def bench_tiers(args, rank, world, local_rank):
     ms = sum(step_ms) / n_steps
     ms = slowest_ms(ms, dist)
 
-    # replay with per-kernel events, counting what each step attends
+    # replay with per-kernel events, counting what each step attends and the
+    # memory the tiers hold after it
     row_bf16 = 2 * W["head_dim"] * 2 * W["n_kv_heads"] * Ly       # bytes per token, all layers
     row_int2 = 768 * W["n_kv_heads"] // 8 * Ly
+    ledger_entry = kvev.TIER_LEDGER_BYTES * Ly * W["n_kv_heads"]  # one window, all layers
     kvev.kvev_profile(tp.ctx, True)
     restart()
     kvev.kvev_profile_read(tp.ctx)
-    per_step = []
+    per_step, mem = [], []
     for t in range(1, n_steps + 1):
         tiers = tp.tier.cpu().numpy()
         tl = tp.tail_len.cpu().numpy()
@@ -899,6 +1130,11 @@ def bench_tiers(args, rank, world, local_rank):
         per_step.append((tok_bf, qn))
         tp.step(*inputs[t - 1], stream)
         kvev.kvev_sync(tp.ctx)
+        tiers = tp.tier.cpu().numpy()
+        n_bf_win = int(((tiers == kvev.KVEV_TIER_UNROUTED) | (tiers == kvev.KVEV_TIER_FULL)).sum())
+        n_led = int(tp.has_codes.cpu().numpy().astype(bool).sum())
+        mem.append((n_bf_win * 128 * row_bf16, n_led * ledger_entry,
+                    int((tiers == kvev.KVEV_TIER_QUANT).sum())))
     prof = kvev.kvev_profile_read(tp.ctx)
     kvev.kvev_profile(tp.ctx, False)
     bytes_step = [tb * row_bf16 + tq * row_int2 for tb, tq in per_step]
@@ -918,32 +1154,75 @@ def bench_tiers(args, rank, world, local_rank):
     attn_achieved = total_bytes / (att_ms * 1e-3) / 1e9 if att_ms > 0 else None
     kernels_us = {k: round(v[0] / n_steps * 1e3, 2) for k, v in prof.items()}
     kernels_us["launches_per_step"] = {k: round(v[1] / n_steps, 2) for k, v in prof.items()}
+    full_bf16 = b * (L0 + n_steps) * row_bf16
+    memory = {"bf16_window_bytes_end": mem[-1][0], "ledger_bytes_end": mem[-1][1],
+              "ledger_bytes_max": max(m[1] for m in mem),
+              "quant_windows_end": mem[-1][2],
+              "ledger_bytes_per_step": [m[1] for m in mem[::max(1, len(mem) // 32)]],
+              "full_bf16_cache_bytes": full_bf16,
+              "note": "bf16 bytes of unrouted and Full windows (sinks and tail aside) and the "
+                      "INT2 ledger (codes kept for every window ever quantized), summed over "
+                      "sequences, after each step"}
 
-    # end to end over the same steps 1..K: pinned host q/k/v in, the output
-    # and the tiers back, every step
+    # end to end over the same steps 1..K: pinned host q/k/v in, the bf16
+    # output and the tiers back, every step
     n_e2e = n_steps
     host_in = [tuple(x.view(torch.int16).cpu().pin_memory() for x in inputs[t - 1])
                for t in range(1, n_e2e + 1)]
     dev_in = [torch.empty_like(x) for x in inputs[0]]
-    out_h = torch.empty(tp.out.shape, dtype=torch.float32).pin_memory()
+    kvev.kvev_set_output(tp.ctx, kvev.KVEV_OUT_BF16)
+    out_dev = torch.empty(tp.out.shape, dtype=torch.bfloat16, device="cuda")
+    out_h = torch.empty(tp.out.shape, dtype=torch.bfloat16).pin_memory()
     tier_h = torch.empty(tp.tier.shape, dtype=torch.uint8).pin_memory()
     h2d = sum(x.numel() * 2 for x in host_in[0])
-    d2h = out_h.numel() * 4 + tier_h.numel()
+    d2h = out_h.numel() * 2 + tier_h.numel()
     restart()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(n_e2e):
         for d_, h_ in zip(dev_in, host_in[i]):
             d_.view(torch.int16).copy_(h_, non_blocking=True)
-        tp.step(*dev_in, stream)
-        out_h.copy_(tp.out, non_blocking=True)
+        tp.step_no += 1
+        kvev.kvev_tier_step(tp.ctx, *dev_in, tp.cache, tp.state, tp.step_no, out_dev, stream)
+        out_h.copy_(out_dev, non_blocking=True)
         tier_h.copy_(tp.tier, non_blocking=True)
         stream.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
     kvev.kvev_sync(tp.ctx)
+    kvev.kvev_set_output(tp.ctx, kvev.KVEV_OUT_F32)
+    del host_in
     e2e_val = world * (sum(bytes_step[:n_e2e]) / n_e2e) / (e2e_ms * 1e-3) / 1e9
 
+    # routing interval sweep: the same run with routing every omega' steps,
+    # timed over steps 1..sweep_steps (mean step and the steps after the
+    # first routing event)
+    sweep = []
+    for om in (omega_sweep or ()):
+        if om == W["omega"]:
+            continue
+        restart(om)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(sweep_steps + 1)]
+        ev[0].record(stream)
+        for t in range(1, sweep_steps + 1):
+            tp.step(*inputs[t - 1], stream)
+            ev[t].record(stream)
+        torch.cuda.synchronize()
+        kvev.kvev_sync(tp.ctx)
+        sm = [ev[t - 1].elapsed_time(ev[t]) for t in range(1, sweep_steps + 1)]
+        sweep.append({"omega": om, "steps": sweep_steps,
+                      "mean_us": round(sum(sm) / len(sm) * 1e3, 1),
+                      "after_first_route_us": round(sum(sm[om:]) / max(1, len(sm) - om) * 1e3, 1),
+                      "quant_windows_end": int((tp.tier.cpu().numpy() == kvev.KVEV_TIER_QUANT).sum()),
+                      "ledger_bytes_end": int(tp.has_codes.cpu().numpy().astype(bool).sum()) * ledger_entry})
+    restart()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_tiers(tp, wl, W, inputs[0])
+
     peak, peak_kind = measured_peak()
+    line = None
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -956,8 +1235,11 @@ def bench_tiers(args, rank, world, local_rank):
                              "nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
                              "peak_kind": peak_kind},
             "steady": {"us": round(steady_ms * 1e3, 2), "bytes": int(steady_bytes),
-                       "GB/s": round(steady_bytes / (steady_ms * 1e-3) / 1e9, 2)},
+                       "GB/s": round(steady_bytes / (steady_ms * 1e-3) / 1e9, 2),
+                       "frac_measured": round(steady_bytes / (steady_ms * 1e-3) / 1e9 / peak, 4)},
             "first_steps_us": [round(x * 1e3, 1) for x in step_ms[:first + 1]],
+            "memory": memory,
+            "omega_sweep": sweep,
             "roofline": {"bound": "hbm", "kernel": "attention (bf16 pages + INT2 windows)",
                          "achieved": round(attn_achieved, 2) if attn_achieved else None,
                          "peak": peak, "unit": "GB/s",
@@ -966,15 +1248,54 @@ def bench_tiers(args, rank, world, local_rank):
                          "peak_kind": f"{peak_kind} (copy bandwidth)"},
             "kernels_us": kernels_us,
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "output": "bf16"},
             "gpu_launches": launches,
             "clocks": clk,
-            "cpu_baseline": None,
+            "cpu_baseline": cpu,
         }
-        print(json.dumps(line), flush=True)
+        if not quiet:
+            print(json.dumps(line), flush=True)
     tp.close()
-    if dist:
-        dist.destroy_process_group()
+    del tp, inputs, k0, v0
+    torch.cuda.empty_cache()
+    return line
+
+
+def cpu_baseline_tiers(tp, wl, W, inputs1, n_layers_sample=2, min_seconds=8.0):
+    """The two-tier oracle (oracle/qevict.py) on sequence 0 of the batch,
+    its first `n_layers_sample` layers, decode step 1 over the whole bf16
+    prefill, repeated to about `min_seconds`."""
+    import torch
+
+    import oracle as O
+    from oracle import qevict as QE
+    Ly, d, Hkv = n_layers_sample, W["head_dim"], W["n_kv_heads"]
+    L0 = W["prefill"]
+    bits = lambda x: x.view(torch.int16).cpu().numpy().view(np.uint16)
+    kp = bits(tp.k_pool[0:wl.n_pages, :Ly])
+    vp = bits(tp.v_pool[0:wl.n_pages, :Ly])
+
+    def tokens(p):
+        rest = p[1:].transpose(1, 2, 0, 3, 4).reshape(Ly, Hkv, -1, d)[:, :, :L0 - 5]
+        return np.ascontiguousarray(np.concatenate([p[0, :, :, :5], rest], axis=2))
+
+    K, V = tokens(kp), tokens(vp)
+    del kp, vp
+    P = QE.QParams(Ly, W["n_q_heads"], Hkv, d, W["k_full"], W["k_quant"], alpha=W["alpha"],
+                   omega=W["omega"])
+    seq0 = QE.QSequence.from_prefill(P, K, V)
+    q, kn, vn = (bits(x[0, :Ly]) for x in inputs1)
+    import copy
+    threads = O.set_threads(os.cpu_count() or 1)
+    reps, secs = timed_reps(lambda: QE.step(P, copy.deepcopy(seq0), 1, q, kn, vn),
+                            min_seconds, 4)
+    nbytes = (L0 + 1) * 2 * d * 2 * Hkv * Ly
+    cores, model = host_cpu()
+    return {"value": round(nbytes * reps / secs / 1e9, 4), "unit": "GB/s",
+            "cores": cores, "kind": "oracle", "cpu": model, "seconds": round(secs, 2),
+            "sample": f"decode step 1 of sequence 0 of {W['batch']}, its first {Ly} of "
+                      f"{W['n_layers']} layers ({L0} + 1 tokens), timed {reps} times; numpy "
+                      f"fp64 on the host's BLAS threads"}
 
 
 if __name__ == "__main__":

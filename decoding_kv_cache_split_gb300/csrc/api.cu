@@ -48,12 +48,6 @@ enum {
     kProfReadmit
 };
 
-// Target size of the logits of one group of layers (see kvev_step).  Far
-// above any real cache, so every layer forms one group: groups small enough
-// for their logits to stay in L2 were measured slower (the extra attention
-// launches cost more than the HBM traffic they saved).
-constexpr int64_t kLogitGroupBytes = int64_t(1) << 40;
-
 // An NVTX range around each step-level call (free when no tool is attached).
 struct NvtxRange {
     explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
@@ -73,7 +67,6 @@ struct Workspace {
     int32_t* tins_s = nullptr;
     int32_t* pos_s = nullptr;
     float* msum_part = nullptr;
-    float* tot_s = nullptr;
     uint32_t* status = nullptr;
     uint16_t* stg_q = nullptr;
     uint16_t* stg_k = nullptr;
@@ -155,7 +148,6 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
     w.tins_s = (int32_t*)take(ctx * 4, "tins_s");
     w.pos_s = (int32_t*)take(ctx * 4, "pos_s");
     w.msum_part = (float*)take((size_t)L.batch * nblk * 4, "msum_part");
-    w.tot_s = (float*)take(ctx * 4, "tot_s");
     w.status = (uint32_t*)take(4, "status");
     const size_t qn = (size_t)L.batch * L.n_layers * L.n_q_heads * L.head_dim;
     const size_t kn = (size_t)L.batch * L.n_layers * L.n_kv_heads * L.head_dim;
@@ -245,6 +237,17 @@ int64_t attn_grid_for_device(int num_sms, const kvev_layout& L) {
     return (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
 }
 
+// Warps of one attention launch over n_tiles tiles: at most one per tile, so
+// a short cache is not spread over warps that hold nothing (their empty
+// split slots would only lengthen the combine's walk over a row's warps).
+// Sets *grid to the CTAs that hold them.
+int attn_launch_warps(int max_warps, int64_t n_tiles, int* grid) {
+    const int w = n_tiles < (int64_t)max_warps ? (int)(n_tiles > 0 ? n_tiles : 1) : max_warps;
+    const int wpc = attn_warps_per_cta();
+    *grid = (w + wpc - 1) / wpc;
+    return w;
+}
+
 int64_t int2_grid_for_device(int num_sms, const kvev_layout& L) {
     if (L.page_tokens != kTierW) return 0;
     const int per_sm = int2_ctas_per_sm(L.head_dim, L.n_q_heads / L.n_kv_heads);
@@ -265,6 +268,7 @@ struct kvev_ctx {
     float alpha = 0.f, beta = 0.f;
     int32_t refresh_mode = KVEV_REFRESH_FULL, refresh_period = 1;
     int32_t age_mode = KVEV_AGE_SINCE_INSERT, pool = KVEV_POOL_SUM;
+    int32_t out_type = KVEV_OUT_F32;
     int32_t group = 4;
     RegionParams rp{};
     std::vector<int32_t> pin_blocks;  // per sequence: prefill blocks holding a pinned token
@@ -539,8 +543,16 @@ kvev_status kvev_set_debug(kvev_ctx* c, float* probs, float* priority) {
     return KVEV_OK;
 }
 
+kvev_status kvev_set_output(kvev_ctx* c, int32_t out_type) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (out_type != KVEV_OUT_F32 && out_type != KVEV_OUT_BF16)
+        return fail(KVEV_EINVAL, "unknown output type %d", out_type);
+    c->out_type = out_type;
+    return KVEV_OK;
+}
+
 kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void* v_new,
-                      kvev_cache* cache, const kvev_state* st, int64_t step, float* out,
+                      kvev_cache* cache, const kvev_state* st, int64_t step, void* out,
                       int32_t* retained_idx, int32_t* n_retained, void* stream) {
     const NvtxRange trace("kvev_step");
     if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
@@ -612,7 +624,6 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     at.batch = Ly.batch;
     at.n_kv = Ly.n_kv_heads;
     at.n_q = Ly.n_q_heads;
-    at.total_warps = c->attn_warps;
     at.write_logits = refresh ? 1 : 0;
     at.q_scale = (float)(1.4426950408889634 / sqrt((double)Ly.head_dim));
     at.view_tokens = (int64_t)Ly.n_layers * Ly.batch * Ly.n_kv_heads * Ly.max_ctx;
@@ -632,7 +643,6 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     sc.pos_s = c->ws.pos_s;
     sc.keys = c->ws.keys;
     sc.msum_part = c->ws.msum_part;
-    sc.tot_s = c->ws.tot_s;
     sc.dbg_probs = refresh ? c->dbg_probs : nullptr;
     sc.dbg_prio = c->dbg_prio;
     sc.L = L;
@@ -649,62 +659,37 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     sc.beta = c->beta;
     sc.access_thr = (float)(2.0 * Ly.n_q_heads * Ly.n_layers / (double)L);
 
-    // On refresh steps the layers go in groups of about kLogitGroupBytes of
-    // logits, each group's attention followed by its scoring (which reads
-    // the logits once and drops the lines from L2); with the target above,
-    // one group holds every layer.
     const int64_t rows_per_layer = (int64_t)Ly.batch * Ly.n_kv_heads;
-    const int64_t logit_bytes_per_layer = rows_per_layer * L * G * 4;
-    int group_layers = Ly.n_layers;
-    if (refresh) {
-        group_layers = (int)(kLogitGroupBytes / logit_bytes_per_layer);
-        group_layers = group_layers < 1 ? 1 : group_layers > Ly.n_layers ? Ly.n_layers : group_layers;
-        const int n_groups = (Ly.n_layers + group_layers - 1) / group_layers;
-        group_layers = (Ly.n_layers + n_groups - 1) / n_groups;   // balanced groups
-    }
+    at.row0 = 0;
+    at.n_tiles_total = (int64_t)Ly.n_layers * rows_per_layer * tiles_per_row;
+    int attn_grid = 0;
+    at.total_warps = attn_launch_warps(c->attn_warps, at.n_tiles_total, &attn_grid);
+    rc = timed_launch(c, kProfAttn, s, "attention", [&] {
+        return launch_attention(at, Ly.head_dim, G, attn_grid, s);
+    });
+    if (rc != KVEV_OK) return rc;
+    CombineArgs cb{};   // merge the split: outputs and per-head log2-sum-exp
+    cb.sp.part_o = c->ws.part_o;
+    cb.sp.part_ml = c->ws.part_ml;
+    cb.sp.n_tiles = at.n_tiles_total;
+    cb.sp.row0 = 0;
+    cb.sp.total_warps = at.total_warps;
+    cb.sp.tiles_per_row = tiles_per_row;
+    cb.n_rows = (int32_t)(Ly.n_layers * rows_per_layer);
+    cb.out = out;
+    cb.out_bf16 = c->out_type == KVEV_OUT_BF16 ? 1 : 0;
+    cb.lse2 = c->ws.lse2;
+    cb.n_layers = Ly.n_layers;
+    cb.batch = Ly.batch;
+    cb.n_kv = Ly.n_kv_heads;
+    cb.n_q = Ly.n_q_heads;
+    rc = timed_launch(c, kProfCombine, s, "combine",
+                      [&] { return launch_combine(cb, Ly.head_dim, G, s); });
+    if (rc != KVEV_OK) return rc;
     int n_part = 0;
-    for (int l0 = 0; l0 < Ly.n_layers; l0 += group_layers) {
-        const int l1 = l0 + group_layers < Ly.n_layers ? l0 + group_layers : Ly.n_layers;
-        at.row0 = (int64_t)l0 * rows_per_layer;
-        at.n_tiles_total = (int64_t)(l1 - l0) * rows_per_layer * tiles_per_row;
-        rc = timed_launch(c, kProfAttn, s, "attention", [&] {
-            return launch_attention(at, Ly.head_dim, G, c->attn_grid, s);
-        });
-        if (rc != KVEV_OK) return rc;
-        CombineArgs cb{};   // merge the split: outputs and per-head log2-sum-exp
-        cb.sp.part_o = c->ws.part_o;
-        cb.sp.part_ml = c->ws.part_ml;
-        cb.sp.n_tiles = at.n_tiles_total;
-        cb.sp.row0 = at.row0;
-        cb.sp.total_warps = c->attn_warps;
-        cb.sp.tiles_per_row = tiles_per_row;
-        cb.n_rows = (int32_t)((l1 - l0) * rows_per_layer);
-        cb.out = out;
-        cb.lse2 = c->ws.lse2;
-        cb.n_layers = Ly.n_layers;
-        cb.batch = Ly.batch;
-        cb.n_kv = Ly.n_kv_heads;
-        cb.n_q = Ly.n_q_heads;
-        rc = timed_launch(c, kProfCombine, s, "combine",
-                          [&] { return launch_combine(cb, Ly.head_dim, G, s); });
-        if (rc != KVEV_OK) return rc;
-        if (!refresh) continue;
-        sc.l0 = l0;
-        sc.l1 = l1;
-        sc.first_group = l0 == 0;
-        sc.last_group = l1 == Ly.n_layers;
-        rc = timed_launch(c, kProfScore, s, "score",
-                          [&] { return launch_score(sc, G, &n_part, s); });
-        if (rc != KVEV_OK) return rc;
-    }
-    if (!refresh) {
-        sc.l0 = 0;
-        sc.l1 = Ly.n_layers;
-        sc.first_group = sc.last_group = 1;
-        rc = timed_launch(c, kProfScore, s, "score",
-                          [&] { return launch_score(sc, G, &n_part, s); });
-        if (rc != KVEV_OK) return rc;
-    }
+    rc = timed_launch(c, kProfScore, s, "score",
+                      [&] { return launch_score(sc, G, &n_part, s); });
+    if (rc != KVEV_OK) return rc;
 
     SelectArgs se{};
     se.keys = c->ws.keys;
@@ -756,7 +741,7 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
 
 kvev_status kvev_step_host(kvev_ctx* c, const void* q_host, const void* k_new_host,
                            const void* v_new_host, kvev_cache* cache, const kvev_state* st,
-                           int64_t step, float* out_host, int32_t* retained_idx_host,
+                           int64_t step, void* out_host, int32_t* retained_idx_host,
                            int32_t* n_retained_host, void* stream) {
     const NvtxRange trace("kvev_step_host");
     if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
@@ -774,7 +759,9 @@ kvev_status kvev_step_host(kvev_ctx* c, const void* q_host, const void* k_new_ho
     kvev_status rc = kvev_step(c, c->ws.stg_q, c->ws.stg_k, c->ws.stg_v, cache, st, step,
                                c->ws.stg_out, c->ws.stg_ret, c->ws.stg_nret, stream);
     if (rc != KVEV_OK) return rc;
-    e = cudaMemcpyAsync(out_host, c->ws.stg_out, qb * 2, cudaMemcpyDeviceToHost, s);
+    // qb is the bf16 size of q, which has the output's shape
+    e = cudaMemcpyAsync(out_host, c->ws.stg_out, c->out_type == KVEV_OUT_BF16 ? qb : qb * 2,
+                        cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(retained_idx_host, c->ws.stg_ret, (size_t)Ly.batch * c->budget * 4,
                             cudaMemcpyDeviceToHost, s);
@@ -906,7 +893,7 @@ kvev_status kvev_paged_begin(kvev_ctx* c, const kvev_paged_cache* pc, const kvev
 
 kvev_status kvev_paged_step(kvev_ctx* c, const void* q, const void* k_new, const void* v_new,
                             const kvev_paged_cache* pc, const kvev_block_state* bs, int64_t step,
-                            float* out, int32_t* retained_lid, int32_t* n_retained,
+                            void* out, int32_t* retained_lid, int32_t* n_retained,
                             void* stream) {
     const NvtxRange trace("kvev_paged_step");
     kvev_status rc = check_paged(c, pc, bs);
@@ -964,7 +951,8 @@ kvev_status kvev_paged_step(kvev_ctx* c, const void* q, const void* k_new, const
     at.batch = Ly.batch;
     at.n_kv = Ly.n_kv_heads;
     at.n_q = Ly.n_q_heads;
-    at.total_warps = c->attn_warps;
+    int attn_grid = 0;
+    at.total_warps = attn_launch_warps(c->attn_warps, at.n_tiles_total, &attn_grid);
     at.write_logits = refresh ? 1 : 0;
     at.q_scale = (float)(1.4426950408889634 / sqrt((double)Ly.head_dim));
     at.view_tokens = (int64_t)Ly.batch * pps * Ly.n_layers * Ly.n_kv_heads * Ly.page_tokens;
@@ -973,17 +961,18 @@ kvev_status kvev_paged_step(kvev_ctx* c, const void* q, const void* k_new, const
     at.blk_len = bs->len;
     at.pps = pps;
     rc = timed_launch(c, kProfAttn, s, "attention",
-                      [&] { return launch_attention(at, Ly.head_dim, G, c->attn_grid, s); });
+                      [&] { return launch_attention(at, Ly.head_dim, G, attn_grid, s); });
     if (rc != KVEV_OK) return rc;
     CombineArgs cb{};
     cb.sp.part_o = c->ws.part_o;
     cb.sp.part_ml = c->ws.part_ml;
     cb.sp.n_tiles = at.n_tiles_total;
     cb.sp.row0 = 0;
-    cb.sp.total_warps = c->attn_warps;
+    cb.sp.total_warps = at.total_warps;
     cb.sp.tiles_per_row = ub;
     cb.n_rows = (int32_t)rows;
     cb.out = out;
+    cb.out_bf16 = c->out_type == KVEV_OUT_BF16 ? 1 : 0;
     cb.lse2 = c->ws.lse2;
     cb.n_layers = Ly.n_layers;
     cb.batch = Ly.batch;
@@ -1192,7 +1181,7 @@ kvev_status kvev_tier_begin(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_t
 
 kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const void* v_new,
                            const kvev_tier_cache* tc, const kvev_tier_state* ts, int64_t step,
-                           float* out, void* stream) {
+                           void* out, void* stream) {
     const NvtxRange trace("kvev_tier_step");
     kvev_status rc = check_tier(c, tc, ts);
     if (rc != KVEV_OK) return rc;
@@ -1263,7 +1252,8 @@ kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const 
     at.batch = Ly.batch;
     at.n_kv = Ly.n_kv_heads;
     at.n_q = Ly.n_q_heads;
-    at.total_warps = c->attn_warps;
+    int attn_grid = 0;
+    at.total_warps = attn_launch_warps(c->attn_warps, at.n_tiles_total, &attn_grid);
     at.write_logits = 0;
     at.q_scale = (float)(1.4426950408889634 / sqrt((double)Ly.head_dim));
     at.view_tokens = (int64_t)Ly.batch * pps * Ly.n_layers * Ly.n_kv_heads * kTile;
@@ -1276,14 +1266,14 @@ kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const 
     at.stats_tiles = tier_stats_tiles(Ly);
     at.stats_base = kTierSinks;
     rc = timed_launch(c, kProfAttn, s, "attention",
-                      [&] { return launch_attention(at, Ly.head_dim, G, c->attn_grid, s); });
+                      [&] { return launch_attention(at, Ly.head_dim, G, attn_grid, s); });
     if (rc != KVEV_OK) return rc;
     CombineArgs cb{};
     cb.sp.part_o = c->ws.part_o;
     cb.sp.part_ml = c->ws.part_ml;
     cb.sp.n_tiles = at.n_tiles_total;
     cb.sp.row0 = 0;
-    cb.sp.total_warps = c->attn_warps;
+    cb.sp.total_warps = at.total_warps;
     cb.sp.tiles_per_row = n_bf;
     if (c->t_nq > 0) {
         Int2Args ia{};
@@ -1319,6 +1309,7 @@ kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const 
     }
     cb.n_rows = (int32_t)rows;
     cb.out = out;
+    cb.out_bf16 = c->out_type == KVEV_OUT_BF16 ? 1 : 0;
     cb.lse2 = c->ws.lse2;
     cb.n_layers = Ly.n_layers;
     cb.batch = Ly.batch;
@@ -1389,7 +1380,7 @@ kvev_status kvev_launch_count(const kvev_ctx* c, int64_t* launches) {
 namespace {
 
 constexpr uint32_t kBlobMagic = 0x5645564bu;   // "KVEV"
-constexpr uint32_t kBlobVersion = 1;
+constexpr uint32_t kBlobVersion = 2;
 
 struct BlobHead {
     uint32_t magic, version;
@@ -1397,7 +1388,7 @@ struct BlobHead {
     int64_t budget;
     float alpha, beta;
     RegionParams rp;
-    int32_t refresh_mode, refresh_period, age_mode, pool;
+    int32_t refresh_mode, refresh_period, age_mode, pool, out_type;
     int32_t k_full, k_quant, omega;
     int32_t begun, len, prefill_len;
     int64_t step;
@@ -1430,6 +1421,7 @@ kvev_status kvev_export_state(const kvev_ctx* c, void* host, size_t* bytes) {
     h.refresh_period = c->refresh_period;
     h.age_mode = c->age_mode;
     h.pool = c->pool;
+    h.out_type = c->out_type;
     h.k_full = c->k_full;
     h.k_quant = c->k_quant;
     h.omega = c->omega;
@@ -1473,6 +1465,7 @@ kvev_status kvev_import_state(kvev_ctx* c, const void* host, size_t bytes, void*
     const int32_t nb = c->lay.batch;
     bool sane = in_range(h.refresh_mode, KVEV_REFRESH_FULL, KVEV_REFRESH_FROZEN) &&
                 h.refresh_period >= 1 && in_range(h.age_mode, 0, 1) && in_range(h.pool, 0, 1) &&
+                in_range(h.out_type, KVEV_OUT_F32, KVEV_OUT_BF16) &&
                 h.omega >= 1 && h.step >= 0 && h.len >= 0 && h.prefill_len >= 0 &&
                 (h.n_ub == 0 || h.n_ub == nb) && (h.n_pin == 0 || h.n_pin == nb);
     if (c->lay.page_tokens == kTierW) {
@@ -1493,6 +1486,7 @@ kvev_status kvev_import_state(kvev_ctx* c, const void* host, size_t bytes, void*
     c->refresh_period = h.refresh_period;
     c->age_mode = h.age_mode;
     c->pool = h.pool;
+    c->out_type = h.out_type;
     c->k_full = h.k_full;
     c->k_quant = h.k_quant;
     c->omega = h.omega;

@@ -25,10 +25,13 @@
 //    two contractions of a tile run on mma.sync m16n8k16 (bf16 in, fp32
 //    accumulate), which removes most of the per-token instructions.
 //  * Softmax partials (running max, sum, output) of each warp's piece of a
-//    row go to a slot.  On refresh steps the scoring kernel merges them (it
-//    needs the per-head log2-sum-exp anyway); otherwise the combine kernel
-//    below does.  Merging inside this kernel (last warp of a row) stalled
+//    row go to a slot, and the combine kernel below merges a row's slots on
+//    every step into the output and the per-head log2-sum-exp the scoring
+//    kernel needs.  Merging inside this kernel (last warp of a row) stalled
 //    that warp's TMA pipeline and cost ~3% of the kernel.
+//  * A warp whose bounded wait gives up flags the status word and writes
+//    NaN as the running max of every slot it owns, so the combine turns the
+//    rows it touched into NaN instead of merging stale partials.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -159,6 +162,7 @@ __global__ void __launch_bounds__(WARPS * 32)
     int* stage_pos = stage_nv + WARPS * STAGES;   // first token position of the tile (block mode)
 
     const int w = blockIdx.x * WARPS + warp;
+    if (w >= a.total_warps) return;   // the launch's last CTA may hold spare warps
     const int64_t N = a.n_tiles_total;
     const int64_t x0 = (int64_t)w * N / a.total_warps;
     const int64_t x1 = (int64_t)(w + 1) * N / a.total_warps;
@@ -418,6 +422,17 @@ __global__ void __launch_bounds__(WARPS * 32)
     }
     if (!ok) {
         if (lane == 0) atomicOr(a.status, kStatusTimeout);
+        // poison every slot this warp owns: a NaN running max makes the
+        // combine's merge of the row NaN (the slots may hold an earlier
+        // launch's partials)
+        for (int64_t r = x0 / tpr + (lane >> 2); r <= (x1 - 1) / tpr; r += 8)
+            if ((lane & 3) < G)
+                a.part_ml[((size_t)((int64_t)w + r) * G + (lane & 3)) * 2] = __int_as_float(0x7fc00000);
+        if (G > 4)
+            for (int64_t r = x0 / tpr + (lane >> 2); r <= (x1 - 1) / tpr; r += 8)
+                if (4 + (lane & 3) < G)
+                    a.part_ml[((size_t)((int64_t)w + r) * G + 4 + (lane & 3)) * 2] =
+                        __int_as_float(0x7fc00000);
         // let the copies already issued land before the block exits (always
         // the full cap: a shortened test limit must not cut this wait; the
         // injected tile issued none)
@@ -532,7 +547,19 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
         float* rp = reinterpret_cast<float*>(&res);
 #pragma unroll
         for (int v = 0; v < V; ++v) rp[v] = acc[h][v] * inv;
-        reinterpret_cast<VecT*>(a.out + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)g * G + h) * D)[lane] = res;
+        const size_t o0 = (((size_t)b * a.n_layers + l) * a.n_q + (size_t)g * G + h) * D;
+        if (a.out_bf16) {   // the same fp32 values rounded to bf16
+            uint32_t pk[V / 2];
+#pragma unroll
+            for (int v = 0; v < V / 2; ++v) pk[v] = pack_bf16x2(rp[2 * v], rp[2 * v + 1]);
+            uint16_t* ob = static_cast<uint16_t*>(a.out) + o0 + (size_t)lane * V;
+            if constexpr (V == 4)
+                *reinterpret_cast<uint2*>(ob) = make_uint2(pk[0], pk[1]);
+            else
+                *reinterpret_cast<uint32_t*>(ob) = pk[0];
+        } else {
+            reinterpret_cast<VecT*>(static_cast<float*>(a.out) + o0)[lane] = res;
+        }
         if (lane == 0) a.lse2[arow * G + h] = M[h] + log2f(Ls[h]);
     }
 }

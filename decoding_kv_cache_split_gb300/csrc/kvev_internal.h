@@ -103,7 +103,8 @@ struct CombineArgs {
     SplitPartials sp2;     // a second launch over the same rows (has2), e.g. the INT2 tier
     int32_t has2;
     int32_t n_rows;        // rows of that launch
-    float* out;            // [b][Ly][Hq][D]
+    void* out;             // [b][Ly][Hq][D], fp32 or (out_bf16) bf16
+    int32_t out_bf16;      // 1: round the fp32 result to bf16 (nearest even)
     float* lse2;           // [rows][G] = [Ly][b][Hq]
     int32_t n_layers, batch, n_kv, n_q;
 };
@@ -126,11 +127,6 @@ struct ScoreArgs {
     int32_t refresh, age_mode, pool_mean;
     int32_t t;
     float alpha, beta, access_thr;   // access: sum over layers of head-summed p >= access_thr
-    // Refresh steps may score the layers in groups [l0, l1) (each right after
-    // the attention of its layers, while their logits are still in L2); the
-    // EMA state and the access sum are carried between groups in m_s / tot_s.
-    int32_t l0, l1, first_group, last_group;
-    float* tot_s;          // scratch [b][max_ctx]
 };
 
 struct SelectArgs {
@@ -143,6 +139,8 @@ struct SelectArgs {
     int32_t* n_retained;   // [b]
     int32_t L, max_ctx, budget, refresh;   // L: upper bound of n_units when n_units is set
     const int32_t* budgets;   // [b] per-sequence kept count (null: budget)
+    int32_t staged;           // 1: the launch reserved shared memory for the keys of
+                              //    its longest chunk (select_stages_keys on the host)
     int32_t ret_ld;           // row stride of retained (0: budget)
     int32_t* first_moved;     // [b] first slot not kept (L when none), or null
 };
@@ -400,5 +398,21 @@ enum : uint32_t { kStatusNoPage = 2u };   // a sequence ran out of free pages
 enum : uint32_t { kStatusRouteCap = 4u };  // more windows than the routing sort holds
 
 constexpr int kScoreThreads = 256;
+
+// Selection: the keys of a sequence are cut into `cl` chunks (one per CTA of
+// its cluster); a CTA stages its chunk in shared memory when the launch's
+// longest chunk fits kSelChunkCap keys (the host then reserves that much
+// dynamic shared memory).  A sequence shorter than the launch's longest
+// (block mode: fewer live blocks) stages exactly when the launch did, so a
+// kernel never stages into memory the launch did not reserve.
+constexpr int kSelChunkCap = 10240;
+__host__ __device__ inline int select_chunk(int n_keys, int cl) { return (n_keys + cl - 1) / cl; }
+__host__ __device__ inline bool select_stages_keys(int launch_keys, int cl) {
+    return select_chunk(launch_keys, cl) <= kSelChunkCap;
+}
+// dynamic shared memory a selection launch reserves per CTA
+__host__ __device__ inline size_t select_smem_bytes(int launch_keys, int cl) {
+    return select_stages_keys(launch_keys, cl) ? 4 * (size_t)select_chunk(launch_keys, cl) : 0;
+}
 
 }  // namespace kvev

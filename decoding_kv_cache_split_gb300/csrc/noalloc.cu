@@ -19,6 +19,17 @@
 // call's contents.  Calls whose work overlaps on the GPU (different streams,
 // or different host threads) race on it and give undefined results; order
 // them on one stream.  The status word is cleared at the start of every call.
+//
+// A bounded device wait that gives up is not returned as a status (nothing
+// reads the status word back, which would synchronise the stream): the warp
+// that gave up writes NaN as the running max of its split slots, so the
+// rows it touched come out NaN in `out` and `lse2` rather than merged from
+// stale partials.
+//
+// The address looked up at set-up belongs to the device's current CUDA
+// context: after cudaDeviceReset (or any teardown of the primary context)
+// the library image is loaded again and the cached address is stale, so do
+// not call this entry point after a reset in the same process.
 #include <math.h>
 #include <stdio.h>
 
@@ -70,10 +81,10 @@ extern "C" kvev_status kvev_attend_noalloc(const kvev_layout* L, const void* q, 
         L->n_q_heads % L->n_kv_heads != 0)
         return report_error(KVEV_EINVAL, "kvev_attend_noalloc: bad head/layer/batch counts");
     const int G = L->n_q_heads / L->n_kv_heads;
-    if ((L->head_dim != 64 && L->head_dim != 128) || G != 4)
+    if ((L->head_dim != 64 && L->head_dim != 128) || (G != 4 && G != 8))
         return report_error(KVEV_EUNSUPPORTED,
-                            "kvev_attend_noalloc: supports head_dim 64/128 with 4 query heads per "
-                            "KV head");
+                            "kvev_attend_noalloc: supports head_dim 64/128 with 4 or 8 query heads "
+                            "per KV head");
     if (len < 1 || len > L->max_ctx)
         return report_error(KVEV_EINVAL, "kvev_attend_noalloc: len must be in [1, max_ctx]");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
@@ -105,16 +116,21 @@ extern "C" kvev_status kvev_attend_noalloc(const kvev_layout* L, const void* q, 
     int64_t grid = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
     const int64_t grid_fit = (slot_cap - rows) / wpc;   // CTAs whose partials fit
     if (grid > grid_fit) grid = grid_fit;
+    // at most one warp per tile, as kvev_step launches it (the same split,
+    // so the same output bit for bit)
+    const int tiles_per_row = (len + kTile - 1) / kTile;
+    const int64_t n_tiles = rows * tiles_per_row;
+    const int64_t warps = n_tiles < grid * wpc ? n_tiles : grid * wpc;
+    grid = (warps + wpc - 1) / wpc;
 
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t* status = reinterpret_cast<uint32_t*>(base);
     float* part_ml = reinterpret_cast<float*>(base + 256);
-    const int64_t slots = grid * wpc + rows;
+    const int64_t slots = warps + rows;
     float* part_o = part_ml + slots * G * 2;
     e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
     if (e != cudaSuccess) return report_error(KVEV_ECUDA, cudaGetErrorString(e));
 
-    const int tiles_per_row = (len + kTile - 1) / kTile;
     AttnArgs at{};
     at.k = (const uint16_t*)k;
     at.v = (const uint16_t*)v;
@@ -123,7 +139,7 @@ extern "C" kvev_status kvev_attend_noalloc(const kvev_layout* L, const void* q, 
     at.part_o = part_o;
     at.part_ml = part_ml;
     at.status = status;
-    at.n_tiles_total = rows * tiles_per_row;
+    at.n_tiles_total = n_tiles;
     at.tiles_per_row = tiles_per_row;
     at.L = len;
     at.max_ctx = L->max_ctx;
@@ -131,7 +147,7 @@ extern "C" kvev_status kvev_attend_noalloc(const kvev_layout* L, const void* q, 
     at.batch = L->batch;
     at.n_kv = L->n_kv_heads;
     at.n_q = L->n_q_heads;
-    at.total_warps = (int32_t)(grid * wpc);
+    at.total_warps = (int32_t)warps;
     at.write_logits = 0;
     at.q_scale = (float)(1.4426950408889634 / sqrt((double)L->head_dim));
     at.view_tokens = rows * L->max_ctx;

@@ -56,16 +56,16 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
     constexpr int V4 = G / 4;                               // float4 per (layer, KV head)
     constexpr int kLB = NKV * V4 >= 16 ? 1 : (16 / (NKV * V4) > 4 ? 4 : 16 / (NKV * V4));  // layers in flight
     constexpr int kPerLine = 128 / (G * 4);                 // tokens per 128-byte line
-    extern __shared__ float s_lse[];                        // [l1 - l0][NKV * G]
+    extern __shared__ float s_lse[];                        // [n_layers][NKV * G]
     __shared__ float s_c[kRefreshSegs][32], s_tot[kRefreshSegs][32];
     griddep_wait();
     griddep_release();
     const int b = blockIdx.y;
-    const int n_lay = a.l1 - a.l0;
+    const int n_lay = a.n_layers;
     const int nlse = n_lay * NKV * G;
     for (int k = threadIdx.x; k < nlse; k += blockDim.x) {
         const int l = k / (NKV * G), h = k % (NKV * G);
-        s_lse[k] = a.lse2[((size_t)(a.l0 + l) * a.batch + b) * a.n_q + h];
+        s_lse[k] = a.lse2[((size_t)l * a.batch + b) * a.n_q + h];
     }
     __syncthreads();
     const int seg = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -74,17 +74,13 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
     const int la = seg * n_lay / kRefreshSegs, lb = (seg + 1) * n_lay / kRefreshSegs;
 
     const size_t si = (size_t)b * a.max_ctx + i;
-    float m0 = 0.f, tot0 = 0.f;
-    if (live && seg == 0) {
-        m0 = a.first_group ? a.st.score[si] : a.m_s[si];
-        tot0 = a.first_group ? 0.f : a.tot_s[si];
-    }
-    float c = m0, tot = tot0;   // the first segment starts from the score itself
+    float c = live && seg == 0 ? a.st.score[si] : 0.f;   // the first segment starts
+    float tot = 0.f;                                        // from the score itself
     const float oma = 1.0f - a.alpha;
     const float inv_hq = 1.0f / (float)a.n_q;
     const size_t head_stride = (size_t)a.logit_ld * G;                  // one (layer, KV head) row
     const size_t layer_stride = (size_t)a.batch * NKV * head_stride;
-    const float* base = a.logits + ((size_t)a.l0 * a.batch + b) * NKV * head_stride + (size_t)i * G;
+    const float* base = a.logits + (size_t)b * NKV * head_stride + (size_t)i * G;
     const bool drop = i % kPerLine == 0 && i + kPerLine <= a.L;         // this thread drops lines
 
     if (live) {
@@ -115,7 +111,7 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
                         const float p2 = fast_exp2(x.z - e.z), p3 = fast_exp2(x.w - e.w);
                         if (a.dbg_probs) {
                             float* dp = a.dbg_probs +
-                                        (((size_t)b * a.n_layers + a.l0 + lr) * a.n_q + g * G + 4 * cc) *
+                                        (((size_t)b * a.n_layers + lr) * a.n_q + g * G + 4 * cc) *
                                             a.max_ctx + i;
                             dp[0] = p0;
                             dp[(size_t)a.max_ctx] = p1;
@@ -156,11 +152,6 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
         for (int l = ka; l < kb; ++l) decay *= oma;
         m = fmaf(decay, m, s_c[k][lane]);
         tot += s_tot[k][lane];
-    }
-    if (!a.last_group) {   // carry the state to the next group of layers
-        a.m_s[si] = m;
-        a.tot_s[si] = tot;
-        return;
     }
     int t_ref = a.st.t_ref[si];
     const int t_ins = a.st.t_ins[si];
@@ -232,7 +223,7 @@ cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStrea
         const int nb = (a.L + 31) / 32;   // 32 tokens per CTA
         *n_blocks = nb;
         const dim3 grid(nb, a.batch);
-        const size_t smem = sizeof(float) * (size_t)(a.l1 - a.l0) * a.n_q;
+        const size_t smem = sizeof(float) * (size_t)a.n_layers * a.n_q;
         void* kern = group == 4 ? refresh_kernel_for<4>(a.n_kv)
                    : group == 8 ? refresh_kernel_for<8>(a.n_kv) : nullptr;
         if (!kern) return cudaErrorInvalidValue;

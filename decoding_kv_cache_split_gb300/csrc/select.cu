@@ -26,7 +26,6 @@ namespace {
 constexpr int kCl = 8;                      // CTAs per sequence (portable cluster size)
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kChunkCap = 10240;            // keys per CTA staged in shared memory
 
 __device__ __forceinline__ uint32_t cta_rank() {
     uint32_t r;
@@ -111,10 +110,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
         }
         return;
     }
-    const int chunk = (L + CL - 1) / CL;
+    const int chunk = select_chunk(L, CL);
     const int c0 = min(L, (int)rank * chunk), c1 = min(L, c0 + chunk);
     const int n = c1 - c0;
-    const bool staged = chunk <= kChunkCap;
+    const bool staged = a.staged != 0;   // chunk <= the launch's chunk: it fits
     if (staged) {
         for (int i = tid; i < n; i += kSelThreads) s_keys[i] = __ldcg(gkeys + c0 + i);
     }
@@ -234,13 +233,14 @@ cudaError_t launch_select(const SelectArgs& a, int batch, int num_sms, cudaStrea
     // Many sequences whose keys fit one CTA's shared memory: one CTA each (no
     // cluster barriers or remote reads; the sequences fill the GPU).  Few
     // sequences, or long ones: a cluster of kCl CTAs each.
-    const bool one = a.L <= kChunkCap && batch * kCl > num_sms;
+    const bool one = a.L <= kSelChunkCap && batch * kCl > num_sms;
     const int cl = one ? 1 : kCl;
-    const int chunk = (a.L + cl - 1) / cl;
-    const size_t smem = chunk <= kChunkCap ? sizeof(uint32_t) * (size_t)chunk : 0;
+    SelectArgs args = a;
+    args.staged = select_stages_keys(a.L, cl) ? 1 : 0;
+    const size_t smem = select_smem_bytes(a.L, cl);
     auto kern = one ? select_kernel<1> : select_kernel<kCl>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(uint32_t) * kChunkCap));
+                                         (int)(sizeof(uint32_t) * kSelChunkCap));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cl * batch);
@@ -256,7 +256,7 @@ cudaError_t launch_select(const SelectArgs& a, int batch, int num_sms, cudaStrea
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, kern, a);
+    e = cudaLaunchKernelEx(&cfg, kern, args);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -24,6 +24,7 @@ STATUS_NAMES = ["OK", "EINVAL", "ENOMEM", "ECUDA", "ESTATE", "ETIMEOUT", "EUNSUP
 KVEV_REFRESH_FULL, KVEV_REFRESH_LAZY, KVEV_REFRESH_FROZEN = 0, 1, 2
 KVEV_AGE_SINCE_INSERT, KVEV_AGE_SINCE_ACCESS = 0, 1
 KVEV_POOL_SUM, KVEV_POOL_MEAN = 0, 1
+KVEV_OUT_F32, KVEV_OUT_BF16 = 0, 1
 KVEV_BF16 = 0
 KVEV_MAX_REGIONS = 16
 KVEV_SCORE_LRFU, KVEV_SCORE_MEMDECAY = 0, 1
@@ -36,7 +37,8 @@ PROFILE_NAMES = ["append", "attention", "combine", "score", "select", "compact",
 
 # every entry point declared in include/kvev.h
 EXPORTS = ["kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_size",
-           "kvev_refresh_mode", "kvev_configure", "kvev_begin", "kvev_length",
+           "kvev_refresh_mode", "kvev_configure", "kvev_set_output", "kvev_begin",
+           "kvev_length",
            "kvev_init_state", "kvev_step", "kvev_step_host", "kvev_set_debug",
            "kvev_profile", "kvev_profile_read", "kvev_launch_count", "kvev_test_wait_timeout",
            "kvev_check_scratch", "kvev_sync",
@@ -143,6 +145,7 @@ def lib():
             "kvev_workspace_size": ([P, I64, P], I32),
             "kvev_refresh_mode": ([P, I32, I32], I32),
             "kvev_configure": ([P, I32, I32], I32),
+            "kvev_set_output": ([P, I32], I32),
             "kvev_begin": ([P, I32], I32),
             "kvev_length": ([P, P], I32),
             "kvev_init_state": ([P, P, P], I32),
@@ -229,6 +232,10 @@ def kvev_refresh_mode(ctx, mode: int, period: int = 1) -> None:
 
 def kvev_configure(ctx, age_mode: int, pool: int) -> None:
     _check(lib().kvev_configure(ctx, int(age_mode), int(pool)), ctx)
+
+
+def kvev_set_output(ctx, out_type: int) -> None:
+    _check(lib().kvev_set_output(ctx, int(out_type)), ctx)
 
 
 def kvev_begin(ctx, prefill_len: int) -> None:
@@ -354,12 +361,13 @@ class EvictionPass:
     """Device buffers plus a context for one decode run (token granularity).
 
     Cache buffers: k[2], v[2] each [Ly][b][Hkv][max_ctx][d] bf16; state arrays
-    [b][max_ctx]; outputs out [b][Ly][Hq][d] fp32, retained [b][budget] int32,
-    n_retained [b] int32.  All torch tensors on the current CUDA device."""
+    [b][max_ctx]; outputs out [b][Ly][Hq][d] fp32 (bf16 with out_type
+    KVEV_OUT_BF16), retained [b][budget] int32, n_retained [b] int32.  All
+    torch tensors on the current CUDA device."""
 
     def __init__(self, n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, budget,
                  alpha, beta, *, age_mode=KVEV_AGE_SINCE_INSERT, pool=KVEV_POOL_SUM,
-                 refresh=KVEV_REFRESH_FULL, period=1, device="cuda"):
+                 refresh=KVEV_REFRESH_FULL, period=1, out_type=KVEV_OUT_F32, device="cuda"):
         import torch
         self.torch = torch
         self.layout = kvev_layout(n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, 1,
@@ -368,6 +376,7 @@ class EvictionPass:
         self.ctx = kvev_create(self.layout, budget, 1, alpha, beta)
         kvev_configure(self.ctx, age_mode, pool)
         kvev_refresh_mode(self.ctx, refresh, period)
+        kvev_set_output(self.ctx, out_type)
         shape = (n_layers, batch, n_kv_heads, max_ctx, head_dim)
         self.k = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]
         self.v = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]
@@ -375,7 +384,8 @@ class EvictionPass:
         self.t_ins = torch.zeros((batch, max_ctx), dtype=torch.int32, device=device)
         self.t_ref = torch.zeros((batch, max_ctx), dtype=torch.int32, device=device)
         self.pos = torch.zeros((batch, max_ctx), dtype=torch.int32, device=device)
-        self.out = torch.zeros((batch, n_layers, n_q_heads, head_dim), dtype=torch.float32,
+        self.out = torch.zeros((batch, n_layers, n_q_heads, head_dim),
+                               dtype=torch.bfloat16 if out_type == KVEV_OUT_BF16 else torch.float32,
                                device=device)
         self.retained = torch.zeros((batch, self.budget), dtype=torch.int32, device=device)
         self.n_retained = torch.zeros((batch,), dtype=torch.int32, device=device)

@@ -183,6 +183,20 @@ kvev_status kvev_refresh_mode(kvev_ctx* ctx, int32_t mode, int32_t period);
 /* Age definition (kvev_age_mode) and head pooling (kvev_pool). */
 kvev_status kvev_configure(kvev_ctx* ctx, int32_t age_mode, int32_t pool);
 
+/* Element type of the attention output `out` of kvev_step, kvev_step_host,
+ * kvev_paged_step and kvev_tier_step (from the next step on):
+ *   KVEV_OUT_F32   fp32, the combine's result as computed (default: it keeps
+ *                  the accumulation's precision, which the parity checks at
+ *                  2e-3 relative need, since bf16 rounding alone costs up to
+ *                  2^-9 = 1.95e-3 of a vector's largest element);
+ *   KVEV_OUT_BF16  the same fp32 values rounded to bf16 (nearest even), half
+ *                  the bytes, for a caller that feeds the output to a bf16
+ *                  projection.
+ * The pages state no output type: the attention output is the input of the
+ * next layer, which the eviction pass does not compute. */
+typedef enum { KVEV_OUT_F32 = 0, KVEV_OUT_BF16 = 1 } kvev_out_type;
+kvev_status kvev_set_output(kvev_ctx* ctx, int32_t out_type);
+
 /* Start a decode run: every sequence holds `prefill_len` live tokens
  * (0 <= prefill_len < max_ctx) and the next step is step 1. */
 kvev_status kvev_begin(kvev_ctx* ctx, int32_t prefill_len);
@@ -202,8 +216,9 @@ kvev_status kvev_init_state(kvev_ctx* ctx, const kvev_state* state, void* stream
  *   k_new  [batch][n_layers][n_kv_heads][head_dim] bf16
  *   v_new  [batch][n_layers][n_kv_heads][head_dim] bf16
  * Device outputs:
- *   out           [batch][n_layers][n_q_heads][head_dim] fp32 attention
- *                 output of this step (over the cache including the new token)
+ *   out           [batch][n_layers][n_q_heads][head_dim] attention output of
+ *                 this step (over the cache including the new token), fp32
+ *                 or bf16 as kvev_set_output chose
  *   retained_idx  [batch][budget] int32: the retained slots of the cache as it
  *                 was after the append, ascending; after the call retained
  *                 slot retained_idx[b][j] lives at slot j.  When the cache
@@ -212,7 +227,7 @@ kvev_status kvev_init_state(kvev_ctx* ctx, const kvev_state* state, void* stream
  *   n_retained    [batch] int32: entries written to retained_idx.
  * `cache` and `state` are read and updated (cache->cur may flip). */
 kvev_status kvev_step(kvev_ctx* ctx, const void* q, const void* k_new, const void* v_new,
-                      kvev_cache* cache, const kvev_state* state, int64_t step, float* out,
+                      kvev_cache* cache, const kvev_state* state, int64_t step, void* out,
                       int32_t* retained_idx, int32_t* n_retained, void* stream);
 
 /* kvev_step with the per-step inputs and outputs in HOST memory (pinned
@@ -223,7 +238,7 @@ kvev_status kvev_step(kvev_ctx* ctx, const void* q, const void* k_new, const voi
  * device. */
 kvev_status kvev_step_host(kvev_ctx* ctx, const void* q_host, const void* k_new_host,
                            const void* v_new_host, kvev_cache* cache, const kvev_state* state,
-                           int64_t step, float* out_host, int32_t* retained_idx_host,
+                           int64_t step, void* out_host, int32_t* retained_idx_host,
                            int32_t* n_retained_host, void* stream);
 
 /* Optional diagnostic outputs written by later steps (NULL disables):
@@ -336,7 +351,7 @@ kvev_status kvev_paged_begin(kvev_ctx* ctx, const kvev_paged_cache* cache,
  * KVEV_SCORE_MEMDECAY). */
 kvev_status kvev_paged_step(kvev_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                             const kvev_paged_cache* cache, const kvev_block_state* state,
-                            int64_t step, float* out, int32_t* retained_lid,
+                            int64_t step, void* out, int32_t* retained_lid,
                             int32_t* n_retained, void* stream);
 
 /* Re-admit prefill block `lid` (0 <= lid < n_backing, a full block) of
@@ -414,7 +429,7 @@ kvev_status kvev_tier_begin(kvev_ctx* ctx, const kvev_tier_cache* cache,
  * event at the end of this step included). */
 kvev_status kvev_tier_step(kvev_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                            const kvev_tier_cache* cache, const kvev_tier_state* state,
-                           int64_t step, float* out, void* stream);
+                           int64_t step, void* out, void* stream);
 
 /* ---- Checkpoint / resume -------------------------------------------------
  * A context's own state: the run's position (step, live length, the host's
@@ -440,21 +455,27 @@ kvev_status kvev_import_state(kvev_ctx* ctx, const void* host, size_t bytes, voi
  * attention and split combine of kvev_step, with no context, keeping the
  * split partials in a 16 MiB array in device memory that belongs to the
  * library image (every GPU that loads the library holds it until exit).
+ * With the same layout and cache it splits the work as kvev_step does, so
+ * `out` equals kvev_step's fp32 output bit for bit.
  *   q      [batch][n_layers][n_q_heads][head_dim] bf16 (device)
  *   k, v   ONE cache buffer, [n_layers][batch][n_kv_heads][max_ctx][head_dim]
  *          bf16 (device); slots [0, len) are attended, 1 <= len <= max_ctx
  *   out    [batch][n_layers][n_q_heads][head_dim] fp32 (device)
  *   lse2   [n_layers][batch][n_q_heads] fp32 (device): log2 of the softmax
  *          normaliser, i.e. ln(sum_i exp(q.k_i/sqrt(d))) / ln 2
- * Limits: head_dim 64 or 128, 4 query heads per KV head, and
- * n_layers*batch*n_kv_heads at most floor((16 MiB - 256) / (16 (head_dim +
- * 2))) - 4, i.e. 8061 at head_dim 128 and 15883 at 64; larger layouts return
- * KVEV_EINVAL before anything is launched.  layout->page_tokens,
- * kv_dtype are ignored (bf16 tokens).  The first call on a device looks up
- * the array's address (make it before any stream capture).  All calls share
- * the array: calls that overlap on the GPU race; order them on one stream.
- * Asynchronous on `stream`; a device wait that gives up leaves `out`
- * undefined and is not reported by this call. */
+ * Limits: head_dim 64 or 128, 4 or 8 query heads per KV head, and
+ * n_layers*batch*n_kv_heads at most floor((16 MiB - 256) / (4 G (head_dim +
+ * 2))) minus the attention warps per CTA (4 in the default build), G the
+ * query heads per KV head: 8061 at head_dim 128 and 15883 at 64 with G = 4;
+ * larger layouts return KVEV_EINVAL, with the limit in the message, before
+ * anything is launched.  layout->page_tokens and kv_dtype are ignored (bf16
+ * tokens).  The first call on a device looks up the array's address (make
+ * it before any stream capture); the address is kept for the life of the
+ * process, so the entry point must not be called after cudaDeviceReset.
+ * All calls share the array: calls that overlap on the GPU race; order them
+ * on one stream.  Asynchronous on `stream`.  A device wait that gives up is
+ * not reported by this call: the rows it touched come out NaN in `out` and
+ * `lse2`. */
 kvev_status kvev_attend_noalloc(const kvev_layout* layout, const void* q, const void* k,
                                 const void* v, int32_t len, float* out, float* lse2,
                                 void* stream);

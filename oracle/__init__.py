@@ -18,5 +18,6 @@ from .oracle import (  # noqa: F401
     is_refresh,
     priority,
     select,
+    set_threads,
     step,
 )

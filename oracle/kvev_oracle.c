@@ -37,11 +37,32 @@
  *               0..B-1.
  *
  * Parity pins for each function live in tests/test_oracle_pins.py.
+ *
+ * Threads: the query heads of one layer's attention are independent and may
+ * run on several host threads (OpenMP, kvo_set_threads); each head's
+ * arithmetic and its order are the same on any number of threads, so the
+ * results are identical bit for bit.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Host threads for the attention's query heads (1 = single thread).
+ * Returns the count in effect (1 when built without OpenMP). */
+int kvo_set_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
 
 /* Exact widening of a bf16 bit pattern. */
 static double bf16_to_double(uint16_t bits) {
@@ -78,6 +99,9 @@ void kvo_attention(int Hq, int Hkv, int d, int64_t L, const uint16_t* q,
                    const uint16_t* k, const uint16_t* v, int64_t ld,
                    double* probs, double* out) {
     double scale = 1.0 / sqrt((double)d);
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int h = 0; h < Hq; ++h) {
         int g = h * Hkv / Hq;
         double* p = probs + (int64_t)h * L;

@@ -31,7 +31,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".{os.getpid()}.tmp"
         subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
-                               "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
+                               "-fno-fast-math", "-fopenmp", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -50,6 +50,8 @@ def _load():
                                       P, P, P, ctypes.c_int64, P, P]
         lib.kvo_select.restype = ctypes.c_int64
         lib.kvo_select.argtypes = [ctypes.c_int64, P, P, ctypes.c_int64, P]
+        lib.kvo_set_threads.restype = ctypes.c_int
+        lib.kvo_set_threads.argtypes = [ctypes.c_int]
         lib.kvo_step.restype = ctypes.c_int64
         lib.kvo_step.argtypes = ([P, ctypes.c_int64, ctypes.c_int, ctypes.c_int64]
                                  + [P] * 6 + [ctypes.c_int64] + [P] * 17)
@@ -68,6 +70,12 @@ class _Params(ctypes.Structure):
                 ("budget", ctypes.c_int64), ("alpha", ctypes.c_double),
                 ("beta", ctypes.c_double), ("age_mode", ctypes.c_int32),
                 ("pool_mean", ctypes.c_int32)]
+
+
+def set_threads(n: int = 0) -> int:
+    """Host threads of the attention (n >= 1; 0 keeps the current count).
+    Returns the count in effect.  Results do not depend on it."""
+    return int(_load().kvo_set_threads(int(n)))
 
 
 # ------------------------------------------------------------- scalar rules

@@ -88,7 +88,7 @@ def compare_step(res, ep, b: int, pre: O.SequenceState, budget: int, dbg_probs=N
     import torch
     L = res["L"]
     stats = {}
-    out = ep.out[b].cpu().numpy().astype(np.float64)
+    out = ep.out[b].float().cpu().numpy().astype(np.float64)   # fp32 or bf16 output
     ref = res["out"]
     err = np.abs(out - ref).max(axis=-1) / np.abs(ref).max(axis=-1)
     stats["out_rel"] = float(err.max())

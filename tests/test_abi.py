@@ -94,6 +94,7 @@ NULL_CTX_CALLS = {
     "kvev_step_host": lambda L: L.kvev_step_host(None, None, None, None, None, None, 1, None,
                                                  None, None, None),
     "kvev_set_debug": lambda L: L.kvev_set_debug(None, None, None),
+    "kvev_set_output": lambda L: L.kvev_set_output(None, 1),
     "kvev_profile": lambda L: L.kvev_profile(None, 1),
     "kvev_profile_read": lambda L: L.kvev_profile_read(None, None, None),
     "kvev_launch_count": lambda L: L.kvev_launch_count(None, _out()),

@@ -1,7 +1,7 @@
 """bench.py's roofline traffic comes from the committed ncu records only
-while they match the kernel sources they were taken on: a record whose
-source hash differs (the kernel changed since the capture) gives null."""
-import hashlib
+while they match the kernel code they were taken on: a record whose code
+hash differs (the kernel changed since the capture) gives null; an edit of
+comments or whitespace alone keeps it."""
 import json
 import os
 
@@ -21,9 +21,9 @@ def _records():
                                      ("attention_int2", "attn_int2.cu")])
 def test_records_name_their_source_and_ratios_are_close_to_one(key, src):
     rec = _records()[key]
-    assert len(rec["source_sha256"]) == 64
+    assert rec["code_sha256"] is None or len(rec["code_sha256"]) == 64
     path = os.path.join(ROOT, "decoding_kv_cache_split_gb300", "csrc", src)
-    current = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    current = bench.code_sha256(open(path, encoding="utf-8").read())
     if key == "attention":
         got = bench.ncu_traffic(src, 1000.0)
         expect = rec["bytes_per_token_layer"] * 1000.0
@@ -31,7 +31,7 @@ def test_records_name_their_source_and_ratios_are_close_to_one(key, src):
         got = bench.traffic_ratio(key, src)
         expect = rec["ratio_to_algorithmic"]
         assert 1.0 <= expect < 1.05     # DRAM bytes at most a few % above the algorithmic ones
-    if rec["source_sha256"] == current:
+    if rec["code_sha256"] == current:
         assert got == pytest.approx(expect)
     else:
         assert got is None
@@ -40,7 +40,7 @@ def test_records_name_their_source_and_ratios_are_close_to_one(key, src):
 def test_a_changed_source_gives_no_traffic(tmp_path, monkeypatch):
     recs = _records()
     for rec in recs.values():
-        rec["source_sha256"] = "0" * 64
+        rec["code_sha256"] = "0" * 64
     prof = tmp_path / "profiles"
     prof.mkdir()
     (prof / "ncu_traffic.json").write_text(json.dumps(recs))
@@ -52,3 +52,13 @@ def test_a_changed_source_gives_no_traffic(tmp_path, monkeypatch):
     assert bench.ncu_traffic("attn.cu", 10.0) is None
     assert bench.traffic_ratio("attention_paged", "attn.cu") is None
     assert bench.traffic_ratio("attention_int2", "attn_int2.cu") is None
+
+
+def test_code_hash_ignores_comments_and_whitespace_only():
+    a = 'int a; // note\n/* block */ int  b; const char* s = "//kept";\n'
+    b = 'int a;\nint b; const char* s = "//kept";'
+    c = 'int a;\nint b; const char* s = "//kept!";'
+    d = 'int a;\nint c; const char* s = "//kept";'
+    assert bench.code_sha256(a) == bench.code_sha256(b)
+    assert bench.code_sha256(b) != bench.code_sha256(c)
+    assert bench.code_sha256(b) != bench.code_sha256(d)

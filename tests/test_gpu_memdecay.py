@@ -231,11 +231,12 @@ def test_memdecay_lazy_observation_and_small_budget():
 
 
 @pytest.mark.slow
-def test_memdecay_full_size_steps_1_2():
+def test_memdecay_full_size_through_step_16():
     """The full region-aware workload on the device: Qwen2.5-3B geometry (36
     layers, 16 q / 2 KV heads), 32 sequences of 16384 labelled tokens,
-    budget 4915 tokens; steps 1 and 2 of sequences 0 and 31 against the
-    oracle, element by element."""
+    budget 4915 tokens; steps 1 to 16 of sequences 0 and 31 against the
+    oracle, element by element (decoded tokens fill the last page, open new
+    ones and get evicted with it)."""
     from workloads import Geometry
     from workloads.device import PagedDeviceWorkload
     L0, batch, Ly, budget = 16384, 32, 36, 4915
@@ -264,7 +265,7 @@ def test_memdecay_full_size_steps_1_2():
         seqs[s] = MD.MDSequence.from_prefill(np.ascontiguousarray(K), np.ascontiguousarray(V),
                                              labels, PAGE)
     stats = {"swaps": 0, "amb": 0, "out_rel": 0.0, "S_abs": 0.0, "a_abs": 0.0}
-    for t in (1, 2):
+    for t in range(1, 17):
         q, kn, vn = wl.step_inputs(torch, t, None)
         pp.step(q, kn, vn)
         kvev.kvev_sync(pp.ctx)

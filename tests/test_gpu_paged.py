@@ -51,9 +51,9 @@ def load_pool(pp, wl, nb0):
             back[b, :nb0].copy_(xt)
 
 
-def check_pages(pp, b, seq):
-    """Block table, free stack and page contents of sequence b against the
-    oracle's block list."""
+def check_pages(pp, b, seq, contents=True):
+    """Block table, free stack and (`contents`) page contents of sequence b
+    against the oracle's block list."""
     nb = int(pp.n_blocks[b])
     assert nb == len(seq.blocks), "live block count"
     table = pp.block_table[b, :nb].cpu().numpy()
@@ -65,6 +65,8 @@ def check_pages(pp, b, seq):
     lens = pp.len[b, :nb].cpu().numpy()
     assert list(lens) == [blk.n for blk in seq.blocks], "block lengths"
     assert list(pp.lid[b, :nb].cpu().numpy()) == seq.lids(), "logical ids"
+    if not contents:
+        return
     for j, blk in enumerate(seq.blocks):
         kd = _bits(pp.k_pool[table[j], :, :, :blk.n])
         vd = _bits(pp.v_pool[table[j], :, :, :blk.n])
@@ -109,8 +111,10 @@ def ambiguous_blocks(res, P):
     return amb
 
 
-def step_and_compare(pp, P, seqs, b, t, ref_now, q, kn, vn, probs, prio, stats):
-    """Run the oracle's step t on sequence b and compare the device's."""
+def step_and_compare(pp, P, seqs, b, t, ref_now, q, kn, vn, probs, prio, stats, full=True):
+    """Run the oracle's step t on sequence b and compare the device's
+    (`full`: the probabilities and every live page's K/V too; otherwise
+    outputs, priorities, the kept set, block tables and per-block state)."""
     budget, beta, age_mode = P.budget, P.beta, P.age_mode
     pre = seqs[b].copy()
     res = PG.step(P, seqs[b], t, ref_now, q, kn, vn, want_probs=True)
@@ -122,7 +126,7 @@ def step_and_compare(pp, P, seqs, b, t, ref_now, q, kn, vn, probs, prio, stats):
     owner = res["owner"]
     first = np.searchsorted(owner, np.arange(len(res["lids_before"])))
     slot = owner * PAGE + (np.arange(res["L"]) - first[owner])
-    if ref_now:
+    if ref_now and full:
         p = probs[b].cpu().numpy().astype(np.float64)[:, :, slot]
         bad = np.abs(p - res["probs"]) > P_RTOL * res["probs"] + P_ATOL
         assert not bad.any(), f"step {t} seq {b}: {bad.sum()} probabilities"
@@ -146,7 +150,7 @@ def step_and_compare(pp, P, seqs, b, t, ref_now, q, kn, vn, probs, prio, stats):
         res = PG.step(P, seqs[b], t, ref_now, q, kn, vn, kept=dev_slots)
     stats["amb"] += int(amb.sum())
     amb_lids = {res["lids_before"][j] for j in np.nonzero(amb)[0]}
-    check_pages(pp, b, seqs[b])
+    check_pages(pp, b, seqs[b], contents=full)
     stats["m_abs"] = max(stats["m_abs"], check_state(pp, b, seqs[b], amb_lids))
 
 
@@ -285,14 +289,20 @@ def test_paged_pinned_blocks_past_the_budget_and_a_pinned_decode_region():
 
 
 @pytest.mark.slow
-def test_paged_full_size_steps_1_2():
+def test_paged_full_size_through_readmission():
     """The full block-granular workload on the device: 32 layers, 64
-    sequences of 8192 tokens (512 blocks), budget 128 blocks; steps 1 and 2
-    of sequences 0 and 63 against the oracle, element by element."""
+    sequences of 8192 tokens (512 blocks), budget 128 blocks, through step
+    202: at t = 201 the needle is re-drawn and every sequence's new needle
+    blocks are re-admitted from the backing tier with their persisted
+    scores.  Sequences 0 and 63 run in the oracle beside the device on every
+    step; outputs, block priorities, kept sets, block tables, per-block state
+    and the persisted score table are compared on every step, the
+    probabilities and every live page's K/V on steps 1, 2, every 25th, and
+    199 to 202."""
     from workloads.device import PagedDeviceWorkload
     wl = PagedDeviceWorkload(0)
     Ly, b, nb0 = wl.n_layers, wl.batch, wl.n_blocks
-    pps, budget = nb0 + 8, 128
+    pps, budget, T = nb0 + 8, 128, 202
     pp = kvev.PagedEvictionPass(Ly, 32, 8, 128, b, pps, PAGE, budget, 0.05, 0.001,
                                 n_backing=nb0, table_len=nb0,
                                 age_mode=kvev.KVEV_AGE_SINCE_ACCESS)
@@ -309,14 +319,27 @@ def test_paged_full_size_steps_1_2():
         seqs[s] = PG.PagedSequence.from_prefill(np.ascontiguousarray(K),
                                                 np.ascontiguousarray(V), PAGE)
     P = O.OracleParams(Ly, 32, 8, 128, budget, 0.05, 0.001, O.AGE_SINCE_ACCESS, False)
-    stats = {"swaps": 0, "amb": 0, "out_rel": 0.0, "m_abs": 0.0}
-    for t in (1, 2):
+    stats = {"swaps": 0, "amb": 0, "out_rel": 0.0, "m_abs": 0.0, "readmitted": 0}
+    for t in range(1, T + 1):
+        if t > 1 and (t - 1) % wl.needle_period == 0:
+            nd = wl.needle(t)
+            for s in range(b):
+                for lid in nd[s]:
+                    pp.readmit(s, int(lid), True)
+                    if s in seqs:
+                        stats["readmitted"] += int(PG.readmit(seqs[s], int(lid), t, True))
+            kvev.kvev_sync(pp.ctx)
+            for s in sample:
+                check_pages(pp, s, seqs[s])
+                check_state(pp, s, seqs[s])
         q, kn, vn = wl.step_inputs(torch, t, pp.backing_k)
         pp.step(q, kn, vn)
         kvev.kvev_sync(pp.ctx)
+        full = t <= 2 or t % 25 == 0 or t >= 199
         for s in sample:
             step_and_compare(pp, P, seqs, s, t, True, _bits(q[s]), _bits(kn[s]), _bits(vn[s]),
-                             probs, prio, stats)
-    print("paged full size:", stats)
+                             probs, prio, stats, full=full)
+    print("paged full size through re-admission:", stats)
+    assert stats["readmitted"] > 0
     kvev.kvev_check_scratch(pp.ctx)   # no scratch region overran its guard band
     pp.close()

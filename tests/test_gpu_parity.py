@@ -173,3 +173,20 @@ def test_llama8b_32k_step1_full_size():
     wl = llama8b_workload(0, prefill_len=32768)
     tot = run_parity(wl, 3277, 0.05, 0.001, 2, age_mode=O.AGE_SINCE_ACCESS, max_ctx=32768 + 64)
     print("llama8b 32k:", tot)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("refresh", ["lazy", "frozen"])
+def test_llama8b_32k_lazy_and_frozen_through_step_64(refresh):
+    """The full Llama-3.1-8B-shaped pass over the horizon the refresh-mode
+    measurements cover: 32768-token prefill, budget 3277, alpha 0.05, beta
+    0.001, access clock, 64 steps with lazy refresh every 8 steps (refresh
+    at t = 1, 9, ..., 57) or Score-Free (t = 1 only), through the needle
+    re-draw at t = 51.  The oracle runs free beside the device on every
+    step (and checks every admissible choice it follows); every 4th step
+    and the last are compared element by element."""
+    wl = llama8b_workload(0, prefill_len=32768)
+    tot = run_parity(wl, 3277, 0.05, 0.001, 64, age_mode=O.AGE_SINCE_ACCESS, refresh=refresh,
+                     period=8, max_ctx=32768 + 96, check_every=4)
+    print(f"llama8b 32k {refresh} x 64:", tot)
+    assert tot["steps"] == 17

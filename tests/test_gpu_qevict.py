@@ -200,18 +200,21 @@ def test_tiers_quantizer_exact_ties():
 
 
 @pytest.mark.slow
-def test_tiers_full_size_first_routing_event():
+def test_tiers_full_size_three_routing_events():
     """The full two-tier workload on the device: 32 layers, 4 sequences of
     131072 tokens (1023 windows), K_f 51, K_q 204, routing every 8 steps;
-    steps 1-9 of sequence 0 against the oracle (the first routing event
-    quantizes 204 windows; step 9 attends the mixed cache)."""
+    steps 1-24 of sequence 0 against the oracle: the first routing event
+    (t = 8) quantizes 204 windows, the next ones (t = 16, 24) move windows
+    between the tiers (promotions from the ledger included), and the steps
+    in between attend the mixed bf16 / INT2 cache."""
     from workloads.device import TierDeviceWorkload
     L0, batch, Ly = 131072, 4, 32
     wl = TierDeviceWorkload(0, n_layers=Ly, batch=batch, prefill=L0)
     pps = wl.n_pages + 16 + 8 * 51
     tp = kvev.TierEvictionPass(Ly, 32, 8, 128, batch, L0 + 32, pps, 51, 204, 8, 0.05)
     wl.fill(torch, tp.k_pool, tp.v_pool, pps)
-    inputs = [wl.step_inputs(torch, t, tp.k_pool, pps) for t in range(1, 10)]
+    T = 24
+    inputs = [wl.step_inputs(torch, t, tp.k_pool, pps) for t in range(1, T + 1)]
     # sequence 0's prefill in token order, from the windowed pages
     hist = L0 - 5
     pages = slice(0, wl.n_pages)
@@ -225,12 +228,13 @@ def test_tiers_full_size_first_routing_event():
     tp.begin(L0)
     stats = {"swaps": 0, "out_rel": 0.0, "m_abs": 0.0, "ledgers": 0, "promoted": 0,
              "redemoted": 0}
-    for t in range(1, 10):
+    for t in range(1, T + 1):
         q, kn, vn = inputs[t - 1]
         tp.step(q, kn, vn)
         kvev.kvev_sync(tp.ctx)
         compare(tp, P, seqs, 0, t, _bits(q[0]), _bits(kn[0]), _bits(vn[0]), stats,
                 check_windows=set(range(0, 1023, 61)))
     print("tiers full size:", stats)
+    assert stats["ledgers"] > 0
     kvev.kvev_check_scratch(tp.ctx)   # no scratch region overran its guard band
     tp.close()

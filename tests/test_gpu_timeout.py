@@ -55,6 +55,15 @@ def test_injected_wait_timeout_is_reported_and_context_recovers(tile):
     with pytest.raises(kvev.KvevError) as err:
         kvev.kvev_sync(a.ctx)
     assert err.value.status == kvev.KVEV_ETIMEOUT
+    # the warp that gave up poisoned its split slots: the row of the withheld
+    # tile (layer, sequence, KV head) comes out NaN instead of a partial merge
+    g = wl.geom
+    tiles_per_row = -(-(wl.L0 + 1) // 16)
+    row = tile // tiles_per_row
+    kvh, lb = row % g.n_kv_heads, row // g.n_kv_heads
+    b, layer = lb % g.batch, lb // g.batch
+    G = g.n_q_heads // g.n_kv_heads
+    assert torch.isnan(a.out[b, layer, kvh * G:(kvh + 1) * G]).all()
     # the injection covers one step only, and the status word was cleared
     _restart(a, wl)
     got = _run(a, wl, 6)

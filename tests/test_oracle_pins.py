@@ -408,3 +408,24 @@ def test_no_eviction_below_budget():
     z = _bits(rng.standard_normal((1, 1, 8)))
     res, new = O.step(P, st, 1, True, _bits(rng.standard_normal((1, 2, 8))), z, z, 10)
     assert list(res["retained"]) == list(range(11)) and new.L == 11
+
+
+def test_threads_leave_every_result_bit_identical():
+    """The oracle's attention may run its query heads on several host
+    threads; each head's arithmetic is unchanged, so a step's outputs,
+    probabilities, scores, priorities and kept set are identical bit for
+    bit on one thread and on four."""
+    from workloads import Geometry, Workload
+    wl = Workload(Geometry(2, 8, 2, 64, 1), 300, seed=77, heavy=3)
+    K, V = wl.prefill()
+    q, kn, vn = wl.step_inputs(1)
+    P = O.OracleParams(2, 8, 2, 64, 50, 0.05, 0.001, O.AGE_SINCE_ACCESS)
+    runs = []
+    for n in (1, 4):
+        O.set_threads(n)
+        st = O.SequenceState.from_prefill(K[:, 0], V[:, 0], 300, 310)
+        res, _ = O.step(P, st, 1, True, q[0], kn[0], vn[0], 300)
+        runs.append(res)
+    O.set_threads(0)
+    for key in ("out", "probs", "m_upd", "priority", "retained"):
+        assert np.array_equal(runs[0][key], runs[1][key]), key

@@ -64,3 +64,50 @@ def test_host_buffer_step_matches_the_device_step():
     kvev.kvev_check_scratch(host.ctx)   # no scratch region overran its guard band
     dev.close()
     host.close()
+
+
+def test_bf16_output_is_the_rounded_fp32_output():
+    """With KVEV_OUT_BF16 the step writes its fp32 result rounded to bf16
+    (nearest even), bit for bit, through kvev_step and kvev_step_host alike
+    (the host copy then moves half the bytes); everything else is unchanged.
+    The rounded output still meets the attention tolerance against the
+    oracle (checked through compare_step in the parity helpers)."""
+    import oracle as O
+    from parity import compare_step, oracle_step
+    wl = Workload(Geometry(2, 8, 2, 128, 2), 300, seed=23, heavy=3)
+    g = wl.geom
+    budget = 64
+
+    def make(out_type):
+        ep = kvev.EvictionPass(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, g.batch,
+                               wl.L0 + 8, budget, 0.05, 0.001, out_type=out_type)
+        load_prefill(ep, wl)
+        ep.begin(wl.L0)
+        return ep
+
+    f32, b16, host = make(kvev.KVEV_OUT_F32), make(kvev.KVEV_OUT_BF16), make(kvev.KVEV_OUT_BF16)
+    assert b16.out.dtype == torch.bfloat16
+    out_h = torch.empty((g.batch, g.n_layers, g.n_q_heads, g.head_dim),
+                        dtype=torch.bfloat16).pin_memory()
+    ret_h = torch.empty((g.batch, budget), dtype=torch.int32).pin_memory()
+    nret_h = torch.empty((g.batch,), dtype=torch.int32).pin_memory()
+    K, V = wl.prefill()
+    P = O.OracleParams(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, budget, 0.05, 0.001)
+    pre = [O.SequenceState.from_prefill(K[:, b], V[:, b], wl.L0, wl.L0 + 8)
+           for b in range(g.batch)]
+    q, kn, vn = wl.step_inputs(1)
+    f32.step(to_dev_bf16(q), to_dev_bf16(kn), to_dev_bf16(vn))
+    b16.step(to_dev_bf16(q), to_dev_bf16(kn), to_dev_bf16(vn))
+    kvev.kvev_step_host(host.ctx, _host_bf16(q), _host_bf16(kn), _host_bf16(vn), host.cache,
+                        host.state, 1, out_h, ret_h, nret_h)
+    kvev.kvev_sync(f32.ctx)
+    want = f32.out.to(torch.bfloat16)                    # round to nearest even
+    assert torch.equal(b16.out.view(torch.int16), want.view(torch.int16))
+    assert torch.equal(out_h.view(torch.int16), want.cpu().view(torch.int16))
+    assert torch.equal(b16.retained, f32.retained) and torch.equal(b16.score, f32.score)
+    for b in range(g.batch):
+        res, _ = oracle_step(P, pre[b], 1, True, q[b], kn[b], vn[b], wl.L0)
+        st = compare_step(res, b16, b, pre[b], budget)
+        assert st["out_rel"] <= 2e-3
+    for ep in (f32, b16, host):
+        ep.close()
