@@ -101,6 +101,12 @@ struct Workspace {
     float2* t_stats = nullptr;        // [rows][stats_tiles][G]
     float* part_o2 = nullptr;         // INT2 attention partials
     float* part_ml2 = nullptr;
+    // token mode, scorer weightings (VNorm, entropy)
+    float* part_e = nullptr;          // [slots][G]
+    float* part_vn = nullptr;         // [slots]
+    float* vnorm = nullptr;           // [rows][logit_ld]
+    float* ent = nullptr;             // [rows][G]
+    float* vmean = nullptr;           // [rows]
     size_t bytes = 0;
     // a guard band of kGuardBytes follows every region: its offset and the
     // region's name (checked by kvev_check_scratch)
@@ -167,6 +173,13 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
     w.readmit_page = (int32_t*)take(4, "readmit_page");
     w.first_moved = (int32_t*)take((size_t)L.batch * 4, "first_moved");
     w.vp = (int32_t*)take((size_t)L.batch * 8, "vp");
+    if (L.page_tokens == 1) {
+        w.part_e = (float*)take((size_t)slots * G * 4, "part_e");
+        w.part_vn = (float*)take((size_t)slots * 4, "part_vn");
+        w.vnorm = (float*)take(rows * (size_t)logit_ld(L.max_ctx) * 4, "vnorm");
+        w.ent = (float*)take(rows * G * 4, "ent");
+        w.vmean = (float*)take(rows * 4, "vmean");
+    }
     if (L.page_tokens == kTierW) {
         const size_t B = (size_t)L.batch, MW = (size_t)tier_max_windows(L);
         const size_t bt = B * tier_bt_ld(L);
@@ -269,6 +282,7 @@ struct kvev_ctx {
     int32_t refresh_mode = KVEV_REFRESH_FULL, refresh_period = 1;
     int32_t age_mode = KVEV_AGE_SINCE_INSERT, pool = KVEV_POOL_SUM;
     int32_t out_type = KVEV_OUT_F32;
+    int32_t aggregation = KVEV_AGG_EMA, weighting = 0;
     int32_t group = 4;
     RegionParams rp{};
     std::vector<int32_t> pin_blocks;  // per sequence: prefill blocks holding a pinned token
@@ -543,6 +557,20 @@ kvev_status kvev_set_debug(kvev_ctx* c, float* probs, float* priority) {
     return KVEV_OK;
 }
 
+kvev_status kvev_set_scorer(kvev_ctx* c, int32_t aggregation, int32_t weighting) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (aggregation != KVEV_AGG_EMA && aggregation != KVEV_AGG_CUMULATIVE)
+        return fail(KVEV_EINVAL, "unknown aggregation %d", aggregation);
+    if (weighting & ~(KVEV_W_VNORM | KVEV_W_ENTROPY))
+        return fail(KVEV_EINVAL, "unknown weighting bits 0x%x", weighting);
+    if (c->lay.page_tokens != 1 && (aggregation != KVEV_AGG_EMA || weighting != 0))
+        return fail(KVEV_EUNSUPPORTED, "cumulative aggregation and the weightings are built for "
+                    "token granularity");
+    c->aggregation = aggregation;
+    c->weighting = weighting;
+    return KVEV_OK;
+}
+
 kvev_status kvev_set_output(kvev_ctx* c, int32_t out_type) {
     if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
     if (out_type != KVEV_OUT_F32 && out_type != KVEV_OUT_BF16)
@@ -631,6 +659,13 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     at.wait_limit = c->test_wait_limit;
     c->test_fault_tile = -1;
     c->test_wait_limit = 0;
+    // the weightings' statistics, gathered by the attention on refresh steps
+    const int stats = !refresh ? 0
+                      : ((c->weighting & KVEV_W_ENTROPY) ? kStatEntropy : 0) |
+                            ((c->weighting & KVEV_W_VNORM) ? kStatVNorm : 0);
+    at.part_e = (stats & kStatEntropy) ? c->ws.part_e : nullptr;
+    at.vnorm = (stats & kStatVNorm) ? c->ws.vnorm : nullptr;
+    at.part_vn = (stats & kStatVNorm) ? c->ws.part_vn : nullptr;
 
     ScoreArgs sc{};
     sc.logits = c->ws.logits;
@@ -655,7 +690,12 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     sc.age_mode = c->age_mode;
     sc.pool_mean = c->pool == KVEV_POOL_MEAN ? 1 : 0;
     sc.t = t;
-    sc.alpha = c->alpha;
+    const bool cumulative = c->aggregation == KVEV_AGG_CUMULATIVE;
+    sc.alpha = cumulative ? 1.0f : c->alpha;
+    sc.oma = cumulative ? 1.0f : 1.0f - c->alpha;
+    sc.ent = (stats & kStatEntropy) ? c->ws.ent : nullptr;
+    sc.vnorm = (stats & kStatVNorm) ? c->ws.vnorm : nullptr;
+    sc.vmean = (stats & kStatVNorm) ? c->ws.vmean : nullptr;
     sc.beta = c->beta;
     sc.access_thr = (float)(2.0 * Ly.n_q_heads * Ly.n_layers / (double)L);
 
@@ -665,10 +705,15 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     int attn_grid = 0;
     at.total_warps = attn_launch_warps(c->attn_warps, at.n_tiles_total, &attn_grid);
     rc = timed_launch(c, kProfAttn, s, "attention", [&] {
-        return launch_attention(at, Ly.head_dim, G, attn_grid, s);
+        return launch_attention(at, Ly.head_dim, G, attn_grid, s, stats);
     });
     if (rc != KVEV_OK) return rc;
     CombineArgs cb{};   // merge the split: outputs and per-head log2-sum-exp
+    cb.part_e = at.part_e;
+    cb.ent = at.part_e ? c->ws.ent : nullptr;
+    cb.part_vn = at.part_vn;
+    cb.vmean = at.part_vn ? c->ws.vmean : nullptr;
+    cb.n_tokens = L;
     cb.sp.part_o = c->ws.part_o;
     cb.sp.part_ml = c->ws.part_ml;
     cb.sp.n_tiles = at.n_tiles_total;
@@ -1388,7 +1433,7 @@ struct BlobHead {
     int64_t budget;
     float alpha, beta;
     RegionParams rp;
-    int32_t refresh_mode, refresh_period, age_mode, pool, out_type;
+    int32_t refresh_mode, refresh_period, age_mode, pool, out_type, aggregation, weighting;
     int32_t k_full, k_quant, omega;
     int32_t begun, len, prefill_len;
     int64_t step;
@@ -1422,6 +1467,8 @@ kvev_status kvev_export_state(const kvev_ctx* c, void* host, size_t* bytes) {
     h.age_mode = c->age_mode;
     h.pool = c->pool;
     h.out_type = c->out_type;
+    h.aggregation = c->aggregation;
+    h.weighting = c->weighting;
     h.k_full = c->k_full;
     h.k_quant = c->k_quant;
     h.omega = c->omega;
@@ -1466,6 +1513,8 @@ kvev_status kvev_import_state(kvev_ctx* c, const void* host, size_t bytes, void*
     bool sane = in_range(h.refresh_mode, KVEV_REFRESH_FULL, KVEV_REFRESH_FROZEN) &&
                 h.refresh_period >= 1 && in_range(h.age_mode, 0, 1) && in_range(h.pool, 0, 1) &&
                 in_range(h.out_type, KVEV_OUT_F32, KVEV_OUT_BF16) &&
+                in_range(h.aggregation, KVEV_AGG_EMA, KVEV_AGG_CUMULATIVE) &&
+                in_range(h.weighting, 0, KVEV_W_VNORM | KVEV_W_ENTROPY) &&
                 h.omega >= 1 && h.step >= 0 && h.len >= 0 && h.prefill_len >= 0 &&
                 (h.n_ub == 0 || h.n_ub == nb) && (h.n_pin == 0 || h.n_pin == nb);
     if (c->lay.page_tokens == kTierW) {
@@ -1487,6 +1536,8 @@ kvev_status kvev_import_state(kvev_ctx* c, const void* host, size_t bytes, void*
     c->age_mode = h.age_mode;
     c->pool = h.pool;
     c->out_type = h.out_type;
+    c->aggregation = h.aggregation;
+    c->weighting = h.weighting;
     c->k_full = h.k_full;
     c->k_quant = h.k_quant;
     c->omega = h.omega;

@@ -139,7 +139,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-template <int D, int G, int STAGES, int WARPS, bool PAGED>
+template <int D, int G, int STAGES, int WARPS, bool PAGED, int ST>
 __global__ void __launch_bounds__(WARPS * 32)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a) {
@@ -251,6 +251,8 @@ __global__ void __launch_bounds__(WARPS * 32)
     uint32_t qa0[KS], qa2[KS];               // Q as the A operand, per k-step
     float o[NB][2];                          // O[g][8j + 2t .. 2t+1]
     float m_run = -INFINITY, l_run = 0.f;
+    float e_run = 0.f;    // ST & kStatEntropy: sum of exp2(x - m_run) * x, this thread's tokens
+    float vn_run = 0.f;   // ST & kStatVNorm: sum of the value norms of this lane's tokens
     int64_t cur_row = -1;
 
     auto flush = [&](int64_t row) {
@@ -258,6 +260,18 @@ __global__ void __launch_bounds__(WARPS * 32)
         l += __shfl_xor_sync(kFull, l, 1);
         l += __shfl_xor_sync(kFull, l, 2);
         const int64_t slot = (int64_t)w + row;
+        if constexpr ((ST & kStatEntropy) != 0) {
+            float e = e_run;
+            e += __shfl_xor_sync(kFull, e, 1);
+            e += __shfl_xor_sync(kFull, e, 2);
+            if (real && t == 0) a.part_e[(size_t)slot * G + g] = e;
+        }
+        if constexpr ((ST & kStatVNorm) != 0) {
+            float v = vn_run;
+#pragma unroll
+            for (int k = 16; k > 0; k >>= 1) v += __shfl_xor_sync(kFull, v, k);
+            if (lane == 0) a.part_vn[slot] = v;
+        }
         if (real) {
             float* po = a.part_o + ((size_t)slot * G + g) * D;
 #pragma unroll
@@ -297,6 +311,8 @@ __global__ void __launch_bounds__(WARPS * 32)
             for (int j = 0; j < NB; ++j) o[j][0] = o[j][1] = 0.f;
             m_run = -INFINITY;
             l_run = 0.f;
+            e_run = 0.f;
+            vn_run = 0.f;
         }
 
         if (!mbar_wait(&bars[stage], parity, wait_limit)) {
@@ -362,6 +378,7 @@ __global__ void __launch_bounds__(WARPS * 32)
             const float f = fast_exp2(m_run - mt);
             m_run = mt;
             l_run *= f;
+            if constexpr ((ST & kStatEntropy) != 0) e_run *= f;
 #pragma unroll
             for (int j = 0; j < NB; ++j) {
                 o[j][0] *= f;
@@ -375,6 +392,8 @@ __global__ void __launch_bounds__(WARPS * 32)
             for (int e = 0; e < 2; ++e) {
                 p[i][e] = real ? fast_exp2(sc[i][e] - m_run) : 0.f;
                 l_run += p[i][e];
+                if constexpr ((ST & kStatEntropy) != 0)   // -inf logits (no token) add 0
+                    e_run = fmaf(p[i][e], p[i][e] > 0.f ? sc[i][e] : 0.f, e_run);
             }
         if (PAGED && a.tile_stats && pos0 >= a.stats_base) {   // (running max, tile sum) per head
             float ts = (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
@@ -398,6 +417,31 @@ __global__ void __launch_bounds__(WARPS * 32)
             }
             fence_proxy_async();   // ordered before the next TMA write to this stage
             __syncwarp();
+        }
+        if constexpr ((ST & kStatVNorm) != 0) {   // l2 norm of each token's value row
+            constexpr int CPL = D / 16;            // 16-byte chunks per lane: two lanes a row
+            const int r = lane & 15, hf = lane >> 4;
+            float ss = 0.f;
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) {
+                uint32_t u0, u1, u2, u3;
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(u0), "=r"(u1), "=r"(u2), "=r"(u3)
+                             : "r"(tile_chunk<D>(vtile, r, hf * CPL + k)));
+                const uint32_t uu[4] = {u0, u1, u2, u3};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float x0 = bf16_lo(uu[j]), x1 = bf16_hi(uu[j]);
+                    ss = fmaf(x0, x0, ss);
+                    ss = fmaf(x1, x1, ss);
+                }
+            }
+            ss += __shfl_xor_sync(kFull, ss, 16);
+            if (lane < 16 && r < nvalid) {
+                const float nrm = sqrtf(ss);
+                a.vnorm[(size_t)(a.row0 + row) * a.logit_ld + pos0 + r] = nrm;
+                vn_run += nrm;
+            }
         }
         // ---- O += P V, two 8-dim blocks per ldmatrix.x4.trans
 #pragma unroll
@@ -540,6 +584,37 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     const int g = (int)(arow % a.n_kv);
     const int64_t lb = arow / a.n_kv;
     const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
+    if ((a.part_e || a.part_vn) && lane == 0) {
+        // weighting statistics: each head's sum of p * x over the row (its
+        // segments rescaled to the merged max, like the softmax sums) and the
+        // row's sum of value norms, in segment order
+        int64_t lo, hi;
+        split_warps_of_row(a.sp, r, &lo, &hi);
+        float E[G], VS = 0.f;
+#pragma unroll
+        for (int h = 0; h < G; ++h) E[h] = 0.f;
+        for (int64_t w = lo; w <= hi; ++w) {
+            if (!split_warp_has_tiles(w, a.sp.n_tiles, a.sp.total_warps)) continue;
+            if (a.part_e) {
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float m = __ldcg(a.sp.part_ml + ((w + r) * G + h) * 2);
+                    if (m != -INFINITY)
+                        E[h] += __ldcg(a.part_e + (w + r) * G + h) * fast_exp2(m - M[h]);
+                }
+            }
+            if (a.part_vn) VS += __ldcg(a.part_vn + w + r);
+        }
+        const float n_tok = (float)a.n_tokens;
+        if (a.ent) {   // entropy in bits = log2-sum-exp - E[p x]; over log2(tokens)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float hb = M[h] + log2f(Ls[h]) - E[h] / Ls[h];
+                a.ent[arow * G + h] = a.n_tokens > 1 ? hb / log2f(n_tok) : 1.0f;
+            }
+        }
+        if (a.vmean) a.vmean[arow] = VS / n_tok;
+    }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         const float inv = 1.0f / Ls[h];
@@ -597,10 +672,10 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int64_t n_tokens, int 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int G, bool PAGED>
+template <int D, int G, bool PAGED, int ST = 0>
 cudaError_t launch_attn_t(const AttnArgs& a, int grid, cudaStream_t s) {
     using C = MmaCfg<D, G, kStages, kWarps>;
-    auto kern = attn_mma_kernel<D, G, kStages, kWarps, PAGED>;
+    auto kern = attn_mma_kernel<D, G, kStages, kWarps, PAGED, ST>;
     CUtensorMap mk, mv;
     if (!encode_cache_map(&mk, a.k, a.view_tokens, D) || !encode_cache_map(&mv, a.v, a.view_tokens, D))
         return cudaErrorInvalidValue;
@@ -613,7 +688,7 @@ cudaError_t launch_attn_t(const AttnArgs& a, int grid, cudaStream_t s) {
 template <int D, int G>
 int ctas_per_sm_t() {
     using C = MmaCfg<D, G, kStages, kWarps>;
-    auto kern = attn_mma_kernel<D, G, kStages, kWarps, false>;
+    auto kern = attn_mma_kernel<D, G, kStages, kWarps, false, 0>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) !=
         cudaSuccess)
         return 0;
@@ -644,9 +719,29 @@ size_t attn_smem_bytes(int head_dim, int group) {
     return 0;
 }
 
+// The token-mode kernel with the weighting statistics `stats` (kStat* bits).
+template <int D, int G>
+cudaError_t launch_attn_stats(const AttnArgs& a, int grid, int stats, cudaStream_t s) {
+    switch (stats) {
+        case kStatEntropy: return launch_attn_t<D, G, false, kStatEntropy>(a, grid, s);
+        case kStatVNorm: return launch_attn_t<D, G, false, kStatVNorm>(a, grid, s);
+        case kStatEntropy | kStatVNorm:
+            return launch_attn_t<D, G, false, kStatEntropy | kStatVNorm>(a, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_attention(const AttnArgs& a, int head_dim, int group, int grid,
-                             cudaStream_t s) {
+                             cudaStream_t s, int stats) {
     const bool paged = a.block_table != nullptr;
+    if (stats != 0) {
+        if (paged) return cudaErrorInvalidValue;
+        if (group == 4 && head_dim == 128) return launch_attn_stats<128, 4>(a, grid, stats, s);
+        if (group == 4 && head_dim == 64) return launch_attn_stats<64, 4>(a, grid, stats, s);
+        if (group == 8 && head_dim == 128) return launch_attn_stats<128, 8>(a, grid, stats, s);
+        if (group == 8 && head_dim == 64) return launch_attn_stats<64, 8>(a, grid, stats, s);
+        return cudaErrorInvalidValue;
+    }
     if (group == 4 && head_dim == 128)
         return paged ? launch_attn_t<128, 4, true>(a, grid, s) : launch_attn_t<128, 4, false>(a, grid, s);
     if (group == 4 && head_dim == 64)

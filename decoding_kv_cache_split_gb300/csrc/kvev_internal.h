@@ -61,7 +61,19 @@ struct AttnArgs {
     // timeout path without a fault.  Zero-initialised arguments inject nothing.
     uint32_t wait_limit;
     int64_t fault_tile_p1;
+    // Optional statistics of the scorer's weightings (token mode, refresh
+    // steps): part_e [slots][G] the split's sum of exp2(x - running max) * x
+    // per head (x the log2-domain logit), merged like the softmax sum into
+    // each head's entropy; vnorm [rows][logit_ld] the l2 norm of each
+    // token's value row, and part_vn [slots] the split's sum of those norms.
+    float* part_e;
+    float* vnorm;
+    float* part_vn;
 };
+
+// Attention statistics the scorer's weightings need (template flags of the
+// attention kernel; 0 = the plain kernel).
+enum : int { kStatEntropy = 1, kStatVNorm = 2 };
 
 // Where one attention launch left its split partials: warp w's piece of the
 // launch's row r (rows counted from row0) is slot w + r.
@@ -100,6 +112,12 @@ __device__ __forceinline__ void split_warps_of_row(const SplitPartials& p, int64
 
 struct CombineArgs {
     SplitPartials sp;      // the attention launch to merge (its rows from sp.row0)
+    // Optional weighting statistics of sp (null: not gathered):
+    const float* part_e;   // [slots][G] -> ent [rows][G]: each head's attention
+    float* ent;            //   entropy over log2 of the row's tokens (1 if <= 1 token)
+    const float* part_vn;  // [slots]    -> vmean [rows]: mean l2 norm of the
+    float* vmean;          //   row's value rows
+    int32_t n_tokens;      // live tokens of every row (token mode)
     SplitPartials sp2;     // a second launch over the same rows (has2), e.g. the INT2 tier
     int32_t has2;
     int32_t n_rows;        // rows of that launch
@@ -113,6 +131,15 @@ struct CombineArgs {
 struct ScoreArgs {
     const float* logits;   // [rows][logit_ld][G]
     int32_t logit_ld;
+    // Aggregation and weightings ("What Matters..." Sec. 3.1 Eqs. (3)-(4),
+    // Appendix E "Per-step scoring"): per layer m <- alpha s + oma m (EMA:
+    // oma = 1 - alpha; cumulative: alpha = oma = 1); ent [rows][G] per-head
+    // normalized entropies whose head mean weighs a layer (null: 1); vnorm /
+    // vmean the VNorm factors of each (row, token) (null: 1).
+    float oma;
+    const float* ent;
+    const float* vnorm;
+    const float* vmean;
     const float* lse2;     // [Ly][b][Hq] log2-sum-exp from the split combine
     kvev_state st;         // caller's state (read)
     float* m_s;            // scratch [b][max_ctx] updated score
@@ -364,7 +391,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 int attn_ctas_per_sm(int head_dim, int group);
 size_t attn_smem_bytes(int head_dim, int group);
 cudaError_t launch_attention(const AttnArgs& a, int head_dim, int group, int grid,
-                             cudaStream_t s);
+                             cudaStream_t s, int stats = 0);
 cudaError_t launch_combine(const CombineArgs& a, int head_dim, int group, cudaStream_t s);
 cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, int batch, int num_sms, cudaStream_t s);

@@ -5,11 +5,15 @@
 //             kernel, from the logits it kept and the log2-sum-exp of the
 //             split combine; "What Matters for Aggressive Decoding-Time KV
 //             Eviction?" Sec. 3.1 Eq. (1))
-//  s_l(i)   = sum_h p_h(i)   (or the head mean, Eq. (1))
+//  s_l(i)   = sum_h p_h(i)   (or the head mean, Eq. (1)); optionally each
+//             head's p_h(i) times ||v_i|| / mean_j ||v_j|| of its KV head
+//             (VNorm), and the layer's s_l times the mean over heads of the
+//             normalized entropy of p_h (Appendix E "Per-step scoring")
 //  m(i)    <- alpha * s_l(i) + (1 - alpha) * m(i) for l = 0 .. Ly-1 in order
 //             (kv-cache-docs "ema-eviction" EMA table; Appendix E "Layer
 //             scoring" of the same paper: every layer updates the shared
-//             state immediately)
+//             state immediately); cumulative aggregation (Sec. 3.1 Eq. (3))
+//             takes m(i) <- s_l(i) + m(i): both weights 1
 //  access   sum_l s_l(i) >= 2 Hq Ly / L  (attention averaged over heads and
 //             layers at least twice uniform: MemDecay Sec. III-C Eq. (3))
 //  pr(i)    = (1 - m(i)) * (1 - exp(-beta * age))  ("ema-eviction" priority)
@@ -51,12 +55,14 @@ __device__ __forceinline__ uint32_t order_bits(float f) {
 constexpr int kRefreshThreads = 128;
 constexpr int kRefreshSegs = kRefreshThreads / 32;
 
-template <int G, int NKV>
+template <int G, int NKV, bool VN>
 __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const ScoreArgs a) {
     constexpr int V4 = G / 4;                               // float4 per (layer, KV head)
     constexpr int kLB = NKV * V4 >= 16 ? 1 : (16 / (NKV * V4) > 4 ? 4 : 16 / (NKV * V4));  // layers in flight
     constexpr int kPerLine = 128 / (G * 4);                 // tokens per 128-byte line
-    extern __shared__ float s_lse[];                        // [n_layers][NKV * G]
+    extern __shared__ float s_lse[];                        // [n_layers][NKV * G], then
+    float* s_lw = s_lse + a.n_layers * NKV * G;             // [n_layers] layer weights,
+    float* s_ivm = s_lw + a.n_layers;                       // [n_layers][NKV] 1 / mean norm
     __shared__ float s_c[kRefreshSegs][32], s_tot[kRefreshSegs][32];
     griddep_wait();
     griddep_release();
@@ -67,6 +73,21 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
         const int l = k / (NKV * G), h = k % (NKV * G);
         s_lse[k] = a.lse2[((size_t)l * a.batch + b) * a.n_q + h];
     }
+    for (int l = threadIdx.x; l < n_lay; l += blockDim.x) {   // entropy weight: head mean
+        float w = 1.f;
+        if (a.ent) {
+            w = 0.f;
+            for (int h = 0; h < NKV * G; ++h) w += a.ent[((size_t)l * a.batch + b) * a.n_q + h];
+            w /= (float)(NKV * G);
+        }
+        s_lw[l] = w;
+    }
+    if constexpr (VN) {
+        for (int k = threadIdx.x; k < n_lay * NKV; k += blockDim.x) {
+            const float vm = a.vmean[((size_t)(k / NKV) * a.batch + b) * NKV + k % NKV];
+            s_ivm[k] = vm > 0.f ? 1.0f / vm : -1.0f;   // -1: every norm 0, factor 1
+        }
+    }
     __syncthreads();
     const int seg = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i = blockIdx.x * 32 + lane;
@@ -76,7 +97,7 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
     const size_t si = (size_t)b * a.max_ctx + i;
     float c = live && seg == 0 ? a.st.score[si] : 0.f;   // the first segment starts
     float tot = 0.f;                                        // from the score itself
-    const float oma = 1.0f - a.alpha;
+    const float oma = a.oma;
     const float inv_hq = 1.0f / (float)a.n_q;
     const size_t head_stride = (size_t)a.logit_ld * G;                  // one (layer, KV head) row
     const size_t layer_stride = (size_t)a.batch * NKV * head_stride;
@@ -86,24 +107,32 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
     if (live) {
         for (int l0 = la; l0 < lb; l0 += kLB) {
             float4 xb[kLB][NKV][V4];
+            float vb[kLB][NKV];
 #pragma unroll
             for (int u = 0; u < kLB; ++u)                 // all loads of the batch first ...
 #pragma unroll
-                for (int g = 0; g < NKV; ++g)
+                for (int g = 0; g < NKV; ++g) {
 #pragma unroll
                     for (int cc = 0; cc < V4; ++cc)
                         xb[u][g][cc] = l0 + u < lb
                             ? __ldcs(reinterpret_cast<const float4*>(
                                   base + (size_t)(l0 + u) * layer_stride + g * head_stride) + cc)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if constexpr (VN)
+                        vb[u][g] = l0 + u < lb
+                            ? __ldcs(a.vnorm + (((size_t)(l0 + u) * a.batch + b) * NKV + g) *
+                                                   a.logit_ld + i)
+                            : 0.f;
+                }
 #pragma unroll
             for (int u = 0; u < kLB; ++u) {               // ... then the layers in order
                 const int lr = l0 + u;
                 if (lr >= lb) break;
                 const float4* lg = reinterpret_cast<const float4*>(s_lse + lr * NKV * G);
-                float s = 0.f;
+                float s = 0.f, sw = 0.f;   // head sum; with VNorm, weighted by the value norms
 #pragma unroll
-                for (int g = 0; g < NKV; ++g)
+                for (int g = 0; g < NKV; ++g) {
+                    float sg = 0.f;
 #pragma unroll
                     for (int cc = 0; cc < V4; ++cc) {
                         const float4 x = xb[u][g][cc], e = lg[g * V4 + cc];
@@ -118,8 +147,14 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
                             dp[2 * (size_t)a.max_ctx] = p2;
                             dp[3 * (size_t)a.max_ctx] = p3;
                         }
-                        s += (p0 + p1) + (p2 + p3);
+                        sg += (p0 + p1) + (p2 + p3);
                     }
+                    s += sg;
+                    if constexpr (VN) {
+                        const float iv = s_ivm[lr * NKV + g];
+                        sw = fmaf(iv >= 0.f ? vb[u][g] * iv : 1.0f, sg, sw);
+                    }
+                }
                 // The logits are dead once read: drop their L2 lines without
                 // writing them back.  A 128-byte line holds kPerLine tokens of
                 // one (layer, KV head) row (rows start on a line), all loaded by
@@ -134,8 +169,10 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
                                      "f"(s)
                                      : "memory");
                 }
-                tot += s;
-                c = fmaf(a.alpha, a.pool_mean ? s * inv_hq : s, oma * c);
+                tot += s;                  // the access test reads the plain attention
+                float sl = VN ? sw : s;
+                if (a.pool_mean) sl *= inv_hq;
+                c = fmaf(a.alpha, sl * s_lw[lr], oma * c);
             }
         }
     }
@@ -166,13 +203,13 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
     if (a.dbg_prio) a.dbg_prio[si] = pr + 0.0f;
 }
 
-template <int G>
+template <int G, bool VN>
 void* refresh_kernel_for(int nkv) {
     switch (nkv) {
-        case 1: return (void*)score_refresh_kernel<G, 1>;
-        case 2: return (void*)score_refresh_kernel<G, 2>;
-        case 4: return (void*)score_refresh_kernel<G, 4>;
-        case 8: return (void*)score_refresh_kernel<G, 8>;
+        case 1: return (void*)score_refresh_kernel<G, 1, VN>;
+        case 2: return (void*)score_refresh_kernel<G, 2, VN>;
+        case 4: return (void*)score_refresh_kernel<G, 4, VN>;
+        case 8: return (void*)score_refresh_kernel<G, 8, VN>;
         default: return nullptr;
     }
 }
@@ -223,9 +260,13 @@ cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStrea
         const int nb = (a.L + 31) / 32;   // 32 tokens per CTA
         *n_blocks = nb;
         const dim3 grid(nb, a.batch);
-        const size_t smem = sizeof(float) * (size_t)a.n_layers * a.n_q;
-        void* kern = group == 4 ? refresh_kernel_for<4>(a.n_kv)
-                   : group == 8 ? refresh_kernel_for<8>(a.n_kv) : nullptr;
+        const size_t smem = sizeof(float) * (size_t)a.n_layers * (a.n_q + 1 + a.n_kv);
+        const bool vn = a.vnorm != nullptr;
+        void* kern = group == 4 ? (vn ? refresh_kernel_for<4, true>(a.n_kv)
+                                      : refresh_kernel_for<4, false>(a.n_kv))
+                   : group == 8 ? (vn ? refresh_kernel_for<8, true>(a.n_kv)
+                                      : refresh_kernel_for<8, false>(a.n_kv))
+                   : nullptr;
         if (!kern) return cudaErrorInvalidValue;
         return launch_pdl(reinterpret_cast<void (*)(ScoreArgs)>(kern), grid,
                           dim3(kRefreshThreads), smem, s, a);

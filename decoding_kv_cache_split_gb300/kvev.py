@@ -25,6 +25,8 @@ KVEV_REFRESH_FULL, KVEV_REFRESH_LAZY, KVEV_REFRESH_FROZEN = 0, 1, 2
 KVEV_AGE_SINCE_INSERT, KVEV_AGE_SINCE_ACCESS = 0, 1
 KVEV_POOL_SUM, KVEV_POOL_MEAN = 0, 1
 KVEV_OUT_F32, KVEV_OUT_BF16 = 0, 1
+KVEV_AGG_EMA, KVEV_AGG_CUMULATIVE = 0, 1
+KVEV_W_VNORM, KVEV_W_ENTROPY = 1, 2
 KVEV_BF16 = 0
 KVEV_MAX_REGIONS = 16
 KVEV_SCORE_LRFU, KVEV_SCORE_MEMDECAY = 0, 1
@@ -37,7 +39,8 @@ PROFILE_NAMES = ["append", "attention", "combine", "score", "select", "compact",
 
 # every entry point declared in include/kvev.h
 EXPORTS = ["kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_size",
-           "kvev_refresh_mode", "kvev_configure", "kvev_set_output", "kvev_begin",
+           "kvev_refresh_mode", "kvev_configure", "kvev_set_output", "kvev_set_scorer",
+           "kvev_begin",
            "kvev_length",
            "kvev_init_state", "kvev_step", "kvev_step_host", "kvev_set_debug",
            "kvev_profile", "kvev_profile_read", "kvev_launch_count", "kvev_test_wait_timeout",
@@ -146,6 +149,7 @@ def lib():
             "kvev_refresh_mode": ([P, I32, I32], I32),
             "kvev_configure": ([P, I32, I32], I32),
             "kvev_set_output": ([P, I32], I32),
+            "kvev_set_scorer": ([P, I32, I32], I32),
             "kvev_begin": ([P, I32], I32),
             "kvev_length": ([P, P], I32),
             "kvev_init_state": ([P, P, P], I32),
@@ -236,6 +240,10 @@ def kvev_configure(ctx, age_mode: int, pool: int) -> None:
 
 def kvev_set_output(ctx, out_type: int) -> None:
     _check(lib().kvev_set_output(ctx, int(out_type)), ctx)
+
+
+def kvev_set_scorer(ctx, aggregation: int, weighting: int = 0) -> None:
+    _check(lib().kvev_set_scorer(ctx, int(aggregation), int(weighting)), ctx)
 
 
 def kvev_begin(ctx, prefill_len: int) -> None:
@@ -367,7 +375,8 @@ class EvictionPass:
 
     def __init__(self, n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, budget,
                  alpha, beta, *, age_mode=KVEV_AGE_SINCE_INSERT, pool=KVEV_POOL_SUM,
-                 refresh=KVEV_REFRESH_FULL, period=1, out_type=KVEV_OUT_F32, device="cuda"):
+                 refresh=KVEV_REFRESH_FULL, period=1, out_type=KVEV_OUT_F32,
+                 aggregation=KVEV_AGG_EMA, weighting=0, device="cuda"):
         import torch
         self.torch = torch
         self.layout = kvev_layout(n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, 1,
@@ -377,6 +386,7 @@ class EvictionPass:
         kvev_configure(self.ctx, age_mode, pool)
         kvev_refresh_mode(self.ctx, refresh, period)
         kvev_set_output(self.ctx, out_type)
+        kvev_set_scorer(self.ctx, aggregation, weighting)
         shape = (n_layers, batch, n_kv_heads, max_ctx, head_dim)
         self.k = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]
         self.v = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]

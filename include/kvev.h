@@ -197,6 +197,29 @@ kvev_status kvev_configure(kvev_ctx* ctx, int32_t age_mode, int32_t pool);
 typedef enum { KVEV_OUT_F32 = 0, KVEV_OUT_BF16 = 1 } kvev_out_type;
 kvev_status kvev_set_output(kvev_ctx* ctx, int32_t out_type);
 
+/* Score aggregation and weighting of token-granular contexts ("What Matters
+ * for Aggressive Decoding-Time KV Eviction?", Sec. 3.1 Eqs. (2)-(4) and
+ * Appendix E "Per-step scoring"); from the next step on.
+ *   aggregation  KVEV_AGG_EMA (default): m <- alpha s_l + (1 - alpha) m per
+ *                layer (alpha = 1 is the single-step rule, Eq. (2));
+ *                KVEV_AGG_CUMULATIVE: m <- m + s_l per layer (Eq. (3), the
+ *                H2O-style sum that never forgets; alpha is unused).
+ *   weighting    bit mask, applied on refresh steps before the fold:
+ *                KVEV_W_VNORM: each query head's probability of token i times
+ *                ||v_i|| / (mean over the cached tokens of ||v_j||), the value
+ *                rows of its KV head in that layer (factor 1 when every norm
+ *                is 0); KVEV_W_ENTROPY: the layer's pooled score times the
+ *                mean over query heads of H(p_h) / ln L (H the entropy of the
+ *                head's attention over the L cached tokens; 1 when L = 1).
+ *                The access clock keeps reading the plain attention.
+ * The attention gathers the weightings' statistics (value norms from the
+ * tiles it already holds, the entropy from its softmax sums), so neither
+ * reads the cache again.  Block-granular and two-tier contexts take only
+ * the defaults (KVEV_EUNSUPPORTED otherwise). */
+typedef enum { KVEV_AGG_EMA = 0, KVEV_AGG_CUMULATIVE = 1 } kvev_aggregation;
+enum { KVEV_W_VNORM = 1, KVEV_W_ENTROPY = 2 };
+kvev_status kvev_set_scorer(kvev_ctx* ctx, int32_t aggregation, int32_t weighting);
+
 /* Start a decode run: every sequence holds `prefill_len` live tokens
  * (0 <= prefill_len < max_ctx) and the next step is step 1. */
 kvev_status kvev_begin(kvev_ctx* ctx, int32_t prefill_len);

@@ -6,10 +6,14 @@ no code with the CUDA library.
 """
 from .oracle import (  # noqa: F401
     AGE_SINCE_ACCESS,
+    AGG_CUMULATIVE,
+    AGG_EMA,
     AGE_SINCE_INSERT,
     REFRESH_FROZEN,
     REFRESH_FULL,
     REFRESH_LAZY,
+    W_ENTROPY,
+    W_VNORM,
     OracleParams,
     SequenceState,
     attention,

@@ -15,10 +15,20 @@
  *               with GQA each KV head serves its query-head group.
  *   pooling     p1 Eq. (1) (head mean) / the head sum used by the eviction
  *               configurations; selected by `pool_mean`.
+ *   weighting   p1 Appendix E "Per-step scoring", optional: VNorm multiplies
+ *               each head's attention to token i by the l2 norm of token i's
+ *               value state (its KV head) over the mean of those norms across
+ *               the cached tokens, before pooling; entropy weighting
+ *               multiplies the layer's pooled score by the normalized entropy
+ *               of its attention distributions (their entropy over ln L,
+ *               averaged over the query heads).
  *   EMA         "ema-eviction" figure (kv-cache-docs, ch07), worked EMA
  *               table: score = alpha*new + (1-alpha)*score.  Applied once per
  *               layer in ascending layer order, the state carried across
  *               steps: p1 Appendix E "Layer scoring".
+ *   cumulative  p1 Sec. 3.1 Eq. (3), the aggregation that never forgets:
+ *               score = score + new, per layer in the same order.  (Eq. (2),
+ *               single-step, is the EMA with alpha = 1.)
  *   refresh     p1 Sec. 3.2 Eq. (6) (lazy refresh) and "Score-Free
  *               decoding"; new tokens on non-refresh steps take the mean
  *               momentum of the existing tokens (p1 Appendix E "New token
@@ -182,7 +192,49 @@ typedef struct {
     double beta;           /* recency coefficient (may be +inf) */
     int32_t age_mode;      /* 0: steps since insertion, 1: since last access */
     int32_t pool_mean;     /* 0: sum over query heads, 1: mean */
+    int32_t aggregation;   /* 0: EMA, 1: cumulative */
+    int32_t weighting;     /* bit 0: VNorm, bit 1: entropy */
 } kvo_params;
+
+enum { KVO_AGG_EMA = 0, KVO_AGG_CUMULATIVE = 1 };
+enum { KVO_W_VNORM = 1, KVO_W_ENTROPY = 2 };
+
+/* VNorm factors of one layer: for KV head g and token i, the l2 norm of
+ * v_{g,i} over the mean of the norms of the L cached tokens of head g (1
+ * where every norm is 0).  v rows as in kvo_attention; w [Hkv][L] out. */
+void kvo_vnorm(int Hkv, int d, int64_t L, const uint16_t* v, int64_t ld, double* w) {
+    for (int g = 0; g < Hkv; ++g) {
+        double* wg = w + (int64_t)g * L;
+        double mean = 0.0;
+        for (int64_t i = 0; i < L; ++i) {
+            const uint16_t* vr = v + ((int64_t)g * ld + i) * d;
+            double ss = 0.0;
+            for (int c = 0; c < d; ++c) ss += bf16_to_double(vr[c]) * bf16_to_double(vr[c]);
+            wg[i] = sqrt(ss);
+            mean += wg[i];
+        }
+        mean /= (double)L;
+        for (int64_t i = 0; i < L; ++i) wg[i] = mean > 0.0 ? wg[i] / mean : 1.0;
+    }
+}
+
+/* Entropy weight of one layer: the entropy -sum_i p_i ln p_i of each query
+ * head's attention distribution over ln L (1 for a uniform distribution, 0
+ * for a one-hot one), averaged over the Hq heads; 1 when L = 1.
+ * probs [Hq][L]. */
+double kvo_layer_entropy(int Hq, int64_t L, const double* probs) {
+    if (L <= 1) return 1.0;
+    double acc = 0.0;
+    for (int h = 0; h < Hq; ++h) {
+        double hh = 0.0;
+        for (int64_t i = 0; i < L; ++i) {
+            double pi = probs[(int64_t)h * L + i];
+            if (pi > 0.0) hh -= pi * log(pi);
+        }
+        acc += hh / log((double)L);
+    }
+    return acc / (double)Hq;
+}
 
 /* One decode step of one sequence, token granularity.
  *
@@ -230,18 +282,28 @@ int64_t kvo_step(const kvo_params* P, int64_t t, int refresh, int64_t L_prev,
     /* 2. attention per layer; 3. head pooling and EMA, layers in order */
     double* p = (double*)malloc(sizeof(double) * (size_t)Hq * (size_t)L);
     double* ssum = (double*)calloc((size_t)L, sizeof(double));
+    double* vw = (double*)malloc(sizeof(double) * (size_t)Hkv * (size_t)L);
     for (int64_t i = 0; i < L; ++i) m_upd[i] = m[i];
     for (int l = 0; l < Ly; ++l) {
         kvo_attention(Hq, Hkv, d, L, q + (int64_t)l * Hq * d, K + l * P->layer_stride,
                       V + l * P->layer_stride, P->cap, p, out + (int64_t)l * Hq * d);
         if (probs) memcpy(probs + (int64_t)l * Hq * L, p, sizeof(double) * (size_t)Hq * L);
         if (!refresh) continue;
+        const int vnorm = (P->weighting & KVO_W_VNORM) != 0;
+        if (vnorm) kvo_vnorm(Hkv, d, L, V + l * P->layer_stride, P->cap, vw);
+        const double lw = (P->weighting & KVO_W_ENTROPY) ? kvo_layer_entropy(Hq, L, p) : 1.0;
         for (int64_t i = 0; i < L; ++i) {
-            double s = 0.0;
-            for (int h = 0; h < Hq; ++h) s += p[(int64_t)h * L + i];
-            ssum[i] += s;
+            double s = 0.0, sw = 0.0;
+            for (int h = 0; h < Hq; ++h) {
+                s += p[(int64_t)h * L + i];
+                if (vnorm) sw += p[(int64_t)h * L + i] * vw[(int64_t)(h * Hkv / Hq) * L + i];
+            }
+            ssum[i] += s;          /* the access test reads the plain attention */
+            if (vnorm) s = sw;
             if (P->pool_mean) s /= (double)Hq;
-            m_upd[i] = kvo_ema(m_upd[i], s, P->alpha);
+            s *= lw;
+            m_upd[i] = P->aggregation == KVO_AGG_CUMULATIVE ? m_upd[i] + s
+                                                            : kvo_ema(m_upd[i], s, P->alpha);
         }
     }
 
@@ -282,5 +344,6 @@ int64_t kvo_step(const kvo_params* P, int64_t t, int refresh, int64_t L_prev,
     }
     free(p);
     free(ssum);
+    free(vw);
     return n;
 }

@@ -22,6 +22,8 @@ _LIB = os.path.join(_HERE, "libkvev_oracle.so")
 _lib = None
 
 REFRESH_FULL, REFRESH_LAZY, REFRESH_FROZEN = 0, 1, 2
+AGG_EMA, AGG_CUMULATIVE = 0, 1
+W_VNORM, W_ENTROPY = 1, 2
 AGE_SINCE_INSERT, AGE_SINCE_ACCESS = 0, 1
 
 
@@ -69,7 +71,8 @@ class _Params(ctypes.Structure):
                 ("cap", ctypes.c_int64), ("layer_stride", ctypes.c_int64),
                 ("budget", ctypes.c_int64), ("alpha", ctypes.c_double),
                 ("beta", ctypes.c_double), ("age_mode", ctypes.c_int32),
-                ("pool_mean", ctypes.c_int32)]
+                ("pool_mean", ctypes.c_int32), ("aggregation", ctypes.c_int32),
+                ("weighting", ctypes.c_int32)]
 
 
 def set_threads(n: int = 0) -> int:
@@ -131,6 +134,8 @@ class OracleParams:
     beta: float
     age_mode: int = AGE_SINCE_INSERT
     pool_mean: bool = False
+    aggregation: int = 0      # AGG_EMA or AGG_CUMULATIVE (p1 Sec. 3.1 Eqs. (3), (4))
+    weighting: int = 0        # W_VNORM | W_ENTROPY (p1 Appendix E "Per-step scoring")
 
 
 @dataclass
@@ -177,7 +182,8 @@ def step(P: OracleParams, st: SequenceState, t: int, refresh: bool, q_bits, knew
     work = st.copy()
     L = st.L + 1
     prm = _Params(P.n_layers, P.n_q_heads, P.n_kv_heads, P.head_dim, cap, Hkv * cap * d,
-                  P.budget, P.alpha, P.beta, P.age_mode, int(P.pool_mean))
+                  P.budget, P.alpha, P.beta, P.age_mode, int(P.pool_mean),
+                  int(P.aggregation), int(P.weighting))
     q = np.ascontiguousarray(q_bits, dtype=np.uint16)
     kn = np.ascontiguousarray(knew_bits, dtype=np.uint16)
     vn = np.ascontiguousarray(vnew_bits, dtype=np.uint16)

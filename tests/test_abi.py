@@ -95,6 +95,7 @@ NULL_CTX_CALLS = {
                                                  None, None, None),
     "kvev_set_debug": lambda L: L.kvev_set_debug(None, None, None),
     "kvev_set_output": lambda L: L.kvev_set_output(None, 1),
+    "kvev_set_scorer": lambda L: L.kvev_set_scorer(None, 1, 0),
     "kvev_profile": lambda L: L.kvev_profile(None, 1),
     "kvev_profile_read": lambda L: L.kvev_profile_read(None, None, None),
     "kvev_launch_count": lambda L: L.kvev_launch_count(None, _out()),

@@ -34,14 +34,19 @@ REFRESH = {"full": (O.REFRESH_FULL, kvev.KVEV_REFRESH_FULL),
 
 def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int, *,
                age_mode=O.AGE_SINCE_INSERT, refresh="full", period=8, pool_mean=False,
-               max_ctx=None, check_every=1):
+               max_ctx=None, check_every=1, aggregation=O.AGG_EMA, weighting=0,
+               m_atol=None):
     g = wl.geom
     max_ctx = max_ctx or max(wl.L0 + steps + 1, budget + 1)
     mode_o, mode_d = REFRESH[refresh]
     ep = kvev.EvictionPass(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, g.batch, max_ctx,
                            budget, alpha, beta, age_mode=AGE_NAMES[age_mode],
                            pool=kvev.KVEV_POOL_MEAN if pool_mean else kvev.KVEV_POOL_SUM,
-                           refresh=mode_d, period=period)
+                           refresh=mode_d, period=period,
+                           aggregation={O.AGG_EMA: kvev.KVEV_AGG_EMA,
+                                        O.AGG_CUMULATIVE: kvev.KVEV_AGG_CUMULATIVE}[aggregation],
+                           weighting=((kvev.KVEV_W_VNORM if weighting & O.W_VNORM else 0) |
+                                      (kvev.KVEV_W_ENTROPY if weighting & O.W_ENTROPY else 0)))
     load_prefill(ep, wl)
     ep.begin(wl.L0)
     probs = torch.zeros((g.batch, g.n_layers, g.n_q_heads, max_ctx), dtype=torch.float32,
@@ -49,7 +54,7 @@ def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int,
     prio = torch.zeros((g.batch, max_ctx), dtype=torch.float32, device="cuda")
     kvev.kvev_set_debug(ep.ctx, probs, prio)
     P = O.OracleParams(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, budget, alpha, beta,
-                       age_mode, pool_mean)
+                       age_mode, pool_mean, aggregation, weighting)
     K, V = wl.prefill()
     states = [O.SequenceState.from_prefill(K[:, b], V[:, b], wl.L0, max_ctx)
               for b in range(g.batch)]
@@ -71,7 +76,7 @@ def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int,
             alt, amb = access_alternative(res, pre, P) if refresh_now else (None, None)
             if check:
                 st = compare_step(res, ep, b, pre, budget, probs, prio, refresh_now, alt,
-                                  access_amb=amb)
+                                  access_amb=amb, **({} if m_atol is None else {"m_atol": m_atol}))
                 totals["swaps"] += st["swaps"]
                 for k in ("out_rel", "m_abs", "p_rel"):
                     totals[k] = max(totals[k], st.get(k, 0.0))
@@ -144,6 +149,34 @@ def test_beta_infinite_and_head_mean():
     pooling (Sec. 3.1 Eq. (1))."""
     wl = Workload(Geometry(2, 8, 2, 64, 1), 300, seed=11, heavy=4)
     run_parity(wl, 64, 0.2, math.inf, 5, pool_mean=True)
+
+
+@pytest.mark.parametrize("aggregation,weighting", [
+    (O.AGG_CUMULATIVE, 0), (O.AGG_EMA, O.W_VNORM), (O.AGG_EMA, O.W_ENTROPY),
+    (O.AGG_EMA, O.W_VNORM | O.W_ENTROPY), (O.AGG_CUMULATIVE, O.W_VNORM | O.W_ENTROPY)])
+def test_scorer_variants(aggregation, weighting):
+    """The aggregation and weighting variants of the scorer (Sec. 3.1 Eqs.
+    (3)-(4), Appendix E "Per-step scoring"): cumulative sums, VNorm value-norm
+    factors, per-layer entropy weights, alone and together, on the
+    Llama-3.1-8B head geometry (3 layers, ragged 1000-token prefill; N(0,1)
+    value rows, whose norms differ by a few per cent), 10 steps with lazy
+    refresh every 3 steps (the statistics are gathered on refresh steps
+    only), access-clock ages."""
+    wl = llama8b_workload(2, prefill_len=1000, n_layers=3, needle_period=4)
+    tot = run_parity(wl, 100, 0.1, 0.001, 10, age_mode=O.AGE_SINCE_ACCESS, refresh="lazy",
+                     period=3, aggregation=aggregation, weighting=weighting)
+    print(aggregation, weighting, tot)
+
+
+@pytest.mark.parametrize("weighting", [O.W_VNORM, O.W_ENTROPY])
+def test_scorer_weightings_on_small_shapes(weighting):
+    """Weightings with head_dim 64, 8 query heads per KV head, a ragged
+    prefill, two sequences and head-mean pooling; and a single cached token
+    (entropy weight 1)."""
+    wl = Workload(Geometry(2, 16, 2, 64, 2), 77, seed=90 + weighting, heavy=2)
+    run_parity(wl, 40, 0.2, 0.001, 5, weighting=weighting, pool_mean=True)
+    wl1 = Workload(Geometry(1, 4, 1, 128, 1), 0, seed=5)
+    run_parity(wl1, 2, 0.3, 0.001, 4, weighting=weighting)
 
 
 def test_probabilities_sum_to_one():

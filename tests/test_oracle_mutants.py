@@ -13,8 +13,8 @@ import sys
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PIN_FILES = ["test_oracle_pins.py", "test_oracle_paged.py", "test_oracle_memdecay.py",
-             "test_oracle_qevict.py"]
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_scorers.py", "test_oracle_paged.py",
+             "test_oracle_memdecay.py", "test_oracle_qevict.py"]
 
 # (oracle file, text, replacement, the mistake it models)
 MUTANTS = [
@@ -70,6 +70,18 @@ MUTANTS = [
     ("kvev_oracle.c", "memcpy(K_out + dst, K + src, sizeof(uint16_t) * d);",
      "memcpy(K_out + dst, V + src, sizeof(uint16_t) * d);", "compaction copies V into K"),
     ("kvev_oracle.c", "ssum[i] += s;", "ssum[i] += s / (double)Hq;", "access mass scaled twice"),
+    # aggregation and weighting variants
+    ("kvev_oracle.c", "? m_upd[i] + s", "? s", "cumulative forgets the state"),
+    ("kvev_oracle.c", "mean /= (double)L;", ";", "VNorm not normalised by the mean norm"),
+    ("kvev_oracle.c", "wg[i] = sqrt(ss);", "wg[i] = ss;", "VNorm on the squared norm"),
+    ("kvev_oracle.c", "vw[(int64_t)(h * Hkv / Hq) * L + i]", "vw[i]",
+     "VNorm factors of KV head 0 for every head"),
+    ("kvev_oracle.c", "if (vnorm) s = sw;", ";", "VNorm factors unused"),
+    ("kvev_oracle.c", "acc += hh / log((double)L);", "acc += hh;", "entropy not normalised"),
+    ("kvev_oracle.c", "return acc / (double)Hq;", "return acc;", "entropy summed over heads"),
+    ("kvev_oracle.c", "    s *= lw;", ";", "entropy weight unused"),
+    ("kvev_oracle.c", "if (L <= 1) return 1.0;", "if (L <= 1) return 0.0;",
+     "a single token's entropy weight 0"),
 ]
 MUTANTS += [
     # block-granular oracle
