@@ -343,6 +343,56 @@ def replay_mode(fh, ctx, ep, step_in, step_ms, alpha, name, period, L0, B, row, 
     return step_bytes, kernels
 
 
+def diagnostics_run(fh, ctx, ep, step_in, L0, k0, v0, stream, alpha, name):
+    """One more replay of a refresh-mode run with the device's ranking
+    diagnostics on (kvev_set_diagnostics): per scoring step the raw top-B set
+    R (the attention summed over heads and layers, before aggregation)
+    against the retained set E.  Returns the means over the scoring steps
+    after the first of: raw/EMA Jaccard |R & E| / |R | E|, raw churn (Jaccard
+    distance of consecutive raw sets), EMA churn (of consecutive retained
+    sets, every step) and the share of R evicted; with `fh`, a JSONL record
+    per step with the counters."""
+    import torch
+    from decoding_kv_cache_split_gb300 import kvev
+    cnt = torch.zeros((1, kvev.KVEV_DIAG_FIELDS), dtype=torch.int32, device="cuda")
+    kvev.kvev_set_diagnostics(ctx, cnt, None)
+    ep.k[0].copy_(k0)
+    ep.v[0].copy_(v0)
+    ep.cache.cur = 0
+    kvev.kvev_begin(ctx, L0)
+    kvev.kvev_init_state(ctx, ep.state, stream)
+    jac, raw_churn, ema_churn, raw_ev = [], [], [], []
+    prev_kept = None
+    for t, ins in enumerate(step_in, start=1):
+        kvev.kvev_step(ctx, *ins, ep.cache, ep.state, t, ep.out, ep.retained, ep.n_retained,
+                       stream)
+        kvev.kvev_sync(ctx)
+        c = dict(zip(kvev.DIAG_NAMES, cnt[0].cpu().tolist()))
+        if prev_kept is not None:
+            ee = c["kept_and_prev_kept"]
+            ema_churn.append(1 - ee / max(1, c["n_kept"] + prev_kept - ee))
+        prev_kept = c["n_kept"]
+        rec = {"alpha": alpha, "mode": name, "step": t, "diag": c}
+        if c["refreshed"] and c["n_raw"]:
+            j = c["raw_and_kept"] / (c["n_raw"] + c["n_kept"] - c["raw_and_kept"])
+            rec["raw_ema_jaccard"] = round(j, 6)
+            if t > 1:
+                jac.append(j)
+                raw_ev.append(1 - c["raw_and_kept"] / c["n_raw"])
+            if c["n_prev_raw"]:
+                rr = c["raw_and_prev_raw"]
+                ch = 1 - rr / (c["n_raw"] + c["n_prev_raw"] - rr)
+                raw_churn.append(ch)
+                rec["raw_churn"] = round(ch, 6)
+        if fh is not None:
+            fh.write(json.dumps(rec) + "\n")
+    kvev.kvev_set_diagnostics(ctx, None, None)
+    mean = lambda x: round(sum(x) / len(x), 6) if x else None
+    return {"raw_ema_jaccard": mean(jac), "raw_churn": mean(raw_churn),
+            "ema_churn": mean(ema_churn), "raw_top_evicted": mean(raw_ev),
+            "scoring_steps": len(jac) + 1}
+
+
 def steady_graph_us(ctx, ep, step_in, L0, k0, v0, stream, warmup, n_capture=8, reps=25):
     """Steady steps replayed from a CUDA graph: decode steps 2..9 of a run
     are captured once (their kernels, with the sizes and buffers of those
@@ -607,6 +657,9 @@ def main():
                 if alpha == 0.05 and not args.no_graph:
                     rec["steady_graph_us"] = steady_graph_us(ctx, ep, step_in, L0, k0, v0,
                                                              stream, args.warmup)
+                if name != "frozen":   # Score-Free scores once: no ranking to trace
+                    rec["diagnostics"] = diagnostics_run(step_log, ctx, ep, step_in, L0, k0,
+                                                         v0, stream, alpha, name)
                 modes.append(rec)
             kvev.kvev_destroy(ctx)
         del k0, v0, step_in

@@ -101,12 +101,20 @@ struct Workspace {
     float2* t_stats = nullptr;        // [rows][stats_tiles][G]
     float* part_o2 = nullptr;         // INT2 attention partials
     float* part_ml2 = nullptr;
+    int32_t* lir_streak = nullptr;    // [batch][max_windows] Global LIR streaks
     // token mode, scorer weightings (VNorm, entropy)
     float* part_e = nullptr;          // [slots][G]
     float* part_vn = nullptr;         // [slots]
     float* vnorm = nullptr;           // [rows][logit_ld]
     float* ent = nullptr;             // [rows][G]
     float* vmean = nullptr;           // [rows]
+    // token mode, ranking diagnostics
+    uint32_t* raw_keys = nullptr;     // [batch][max_ctx]
+    int32_t* raw_list = nullptr;      // [batch][budget]
+    int32_t* raw_n = nullptr;         // [batch]
+    uint8_t* in_raw = nullptr;        // [batch][max_ctx]
+    uint8_t* raw_flags = nullptr;     // [2][batch][max_ctx], by step parity
+    int32_t* raw_prev_n = nullptr;    // [batch]
     size_t bytes = 0;
     // a guard band of kGuardBytes follows every region: its offset and the
     // region's name (checked by kvev_check_scratch)
@@ -179,6 +187,12 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
         w.vnorm = (float*)take(rows * (size_t)logit_ld(L.max_ctx) * 4, "vnorm");
         w.ent = (float*)take(rows * G * 4, "ent");
         w.vmean = (float*)take(rows * 4, "vmean");
+        w.raw_keys = (uint32_t*)take(ctx * 4, "raw_keys");
+        w.raw_list = (int32_t*)take((size_t)L.batch * budget * 4, "raw_list");
+        w.raw_n = (int32_t*)take((size_t)L.batch * 4, "raw_n");
+        w.in_raw = (uint8_t*)take(ctx, "in_raw");
+        w.raw_flags = (uint8_t*)take(2 * ctx, "raw_flags");
+        w.raw_prev_n = (int32_t*)take((size_t)L.batch * 4, "raw_prev_n");
     }
     if (L.page_tokens == kTierW) {
         const size_t B = (size_t)L.batch, MW = (size_t)tier_max_windows(L);
@@ -199,6 +213,7 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
         w.t_stats = (float2*)take(rows * (size_t)tier_stats_tiles(L) * G * sizeof(float2), "t_stats");
         w.part_o2 = (float*)take((size_t)slots2 * G * L.head_dim * 4, "part_o2");
         w.part_ml2 = (float*)take((size_t)slots2 * G * 2 * 4, "part_ml2");
+        w.lir_streak = (int32_t*)take(B * MW * 4, "lir_streak");
     }
     w.bytes = off;
     return w;
@@ -302,6 +317,11 @@ struct kvev_ctx {
     Workspace ws;
     float* dbg_probs = nullptr;
     float* dbg_prio = nullptr;
+    int32_t* lir_counters = nullptr;    // Global LIR counts (two-tier mode)
+    int32_t lir_sustain = 0;
+    int32_t* diag_counters = nullptr;   // ranking diagnostics (token mode)
+    float* diag_raw = nullptr;
+    bool diag_flags_valid = false;      // the raw-set flags of the live cache are set
     bool prof = false;
     std::vector<cudaEvent_t> ev_pool;
     std::vector<int> ev_kind;   // kernel slot of each recorded start/end pair
@@ -529,6 +549,7 @@ kvev_status kvev_begin(kvev_ctx* c, int32_t prefill_len) {
     c->prefill_len = prefill_len;
     c->step = 0;
     c->begun = true;
+    c->diag_flags_valid = false;
     return KVEV_OK;
 }
 
@@ -545,9 +566,41 @@ kvev_status kvev_init_state(kvev_ctx* c, const kvev_state* st, void* stream) {
     if (!c->begun) return fail(KVEV_ESTATE, "kvev_begin must come first");
     cudaStream_t s = (cudaStream_t)stream;
     const int len = c->len;
+    c->diag_flags_valid = false;
     return timed_launch(c, kProfInit, s, "init_state", [&] {
         return launch_init_state(*st, c->lay.batch, c->lay.max_ctx, len, c->ws.vp, s);
     });
+}
+
+kvev_status kvev_set_diagnostics(kvev_ctx* c, int32_t* counters, float* raw_score) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (c->lay.page_tokens != 1 && (counters || raw_score))
+        return fail(KVEV_EUNSUPPORTED, "ranking diagnostics are built for token granularity");
+    c->diag_counters = counters;
+    c->diag_raw = raw_score;
+    c->diag_flags_valid = false;
+    return KVEV_OK;
+}
+
+kvev_status kvev_missed_mass(const float* full_score, int32_t score_ld, int32_t n_pos,
+                             const int32_t* pos, int32_t pos_ld, int32_t n_cached,
+                             int32_t batch, float* out, void* stream) {
+    if (!full_score || !out || (n_cached > 0 && !pos))
+        return fail(KVEV_EINVAL, "kvev_missed_mass: NULL argument");
+    if (batch < 1 || n_pos < 1 || score_ld < n_pos || n_cached < 0 || pos_ld < n_cached)
+        return fail(KVEV_EINVAL, "kvev_missed_mass: batch >= 1, 1 <= n_pos <= score_ld and "
+                    "0 <= n_cached <= pos_ld needed");
+    MissedMassArgs a{};
+    a.full_score = full_score;
+    a.pos = pos;
+    a.out = out;
+    a.score_ld = score_ld;
+    a.n_pos = n_pos;
+    a.pos_ld = pos_ld;
+    a.n_cached = n_cached;
+    cudaError_t e = launch_missed_mass(a, batch, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "missed mass");
+    return KVEV_OK;
 }
 
 kvev_status kvev_set_debug(kvev_ctx* c, float* probs, float* priority) {
@@ -563,9 +616,12 @@ kvev_status kvev_set_scorer(kvev_ctx* c, int32_t aggregation, int32_t weighting)
         return fail(KVEV_EINVAL, "unknown aggregation %d", aggregation);
     if (weighting & ~(KVEV_W_VNORM | KVEV_W_ENTROPY))
         return fail(KVEV_EINVAL, "unknown weighting bits 0x%x", weighting);
-    if (c->lay.page_tokens != 1 && (aggregation != KVEV_AGG_EMA || weighting != 0))
-        return fail(KVEV_EUNSUPPORTED, "cumulative aggregation and the weightings are built for "
-                    "token granularity");
+    if (c->lay.page_tokens != 1 && weighting != 0)
+        return fail(KVEV_EUNSUPPORTED, "the weightings are built for token granularity");
+    if (c->lay.page_tokens != 1 && c->lay.page_tokens != kTierW &&
+        aggregation != KVEV_AGG_EMA)
+        return fail(KVEV_EUNSUPPORTED, "cumulative aggregation is built for token "
+                    "granularity and two-tier windows");
     c->aggregation = aggregation;
     c->weighting = weighting;
     return KVEV_OK;
@@ -698,6 +754,9 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     sc.vmean = (stats & kStatVNorm) ? c->ws.vmean : nullptr;
     sc.beta = c->beta;
     sc.access_thr = (float)(2.0 * Ly.n_q_heads * Ly.n_layers / (double)L);
+    const bool diag = c->diag_counters != nullptr;
+    sc.raw_keys = diag && refresh ? c->ws.raw_keys : nullptr;
+    sc.dbg_raw = refresh ? c->diag_raw : nullptr;
 
     const int64_t rows_per_layer = (int64_t)Ly.batch * Ly.n_kv_heads;
     at.row0 = 0;
@@ -751,6 +810,40 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     rc = timed_launch(c, kProfSelect, s, "select",
                       [&] { return launch_select(se, Ly.batch, c->num_sms, s); });
     if (rc != KVEV_OK) return rc;
+    if (diag) {   // ranking diagnostics: the raw top-B set, then the counts
+        if (refresh) {
+            SelectArgs sr = se;
+            sr.keys = c->ws.raw_keys;
+            sr.retained = c->ws.raw_list;
+            sr.n_retained = c->ws.raw_n;
+            sr.refresh = 1;          // no new-token score to set
+            sr.first_moved = nullptr;
+            rc = timed_launch(c, kProfSelect, s, "raw select",
+                              [&] { return launch_select(sr, Ly.batch, c->num_sms, s); });
+            if (rc != KVEV_OK) return rc;
+        }
+        DiagArgs dg{};
+        dg.retained = retained_idx;
+        dg.n_retained = n_retained;
+        dg.raw_list = c->ws.raw_list;
+        dg.raw_n = c->ws.raw_n;
+        dg.in_raw = c->ws.in_raw;
+        const size_t cb_ctx = (size_t)Ly.batch * Ly.max_ctx;
+        dg.flags_in = c->ws.raw_flags + (step & 1) * cb_ctx;
+        dg.flags_out = c->ws.raw_flags + ((step + 1) & 1) * cb_ctx;
+        dg.prev_n = c->ws.raw_prev_n;
+        dg.counters = c->diag_counters;
+        dg.L = L;
+        dg.max_ctx = Ly.max_ctx;
+        dg.budget = (int)c->budget;
+        dg.t = t;
+        dg.refresh = refresh ? 1 : 0;
+        dg.flags_valid = c->diag_flags_valid ? 1 : 0;
+        rc = timed_launch(c, kProfSelect, s, "diagnostics",
+                          [&] { return launch_diag(dg, Ly.batch, s); });
+        if (rc != KVEV_OK) return rc;
+        c->diag_flags_valid = c->diag_flags_valid || refresh;
+    }
 
     CompactArgs cp{};
     cp.first_moved = c->ws.first_moved;
@@ -1169,7 +1262,12 @@ TierArgs tier_args(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_tier_state
     a.k_full = c->k_full;
     a.k_quant = c->k_quant;
     a.t = t;
-    a.alpha = c->alpha;
+    const bool cumulative = c->aggregation == KVEV_AGG_CUMULATIVE;
+    a.alpha = cumulative ? 1.0f : c->alpha;
+    a.oma = cumulative ? 1.0f : 1.0f - c->alpha;
+    a.lir_streak = c->ws.lir_streak;
+    a.lir_counters = c->lir_counters;
+    a.lir_sustain = c->lir_sustain;
     return a;
 }
 
@@ -1182,6 +1280,23 @@ int tier_used_pages(const kvev_ctx* c) {
 }  // namespace
 
 extern "C" {
+
+kvev_status kvev_tier_diagnostics(kvev_ctx* c, int32_t sustain, int32_t* counters,
+                                  void* stream) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (c->lay.page_tokens != kTierW)
+        return fail(KVEV_ESTATE, "not a two-tier context (layout.page_tokens must be %d)", kTierW);
+    if (counters && sustain < 1) return fail(KVEV_EINVAL, "sustain must be >= 1");
+    c->lir_counters = counters;
+    c->lir_sustain = counters ? sustain : 0;
+    if (!counters) return KVEV_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(c->ws.lir_streak, 0,
+                                    (size_t)c->lay.batch * tier_max_windows(c->lay) * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(counters, 0, (size_t)c->lay.batch * 3 * 4, s);
+    if (e != cudaSuccess) return cuda_fail(e, "resetting the LIR counts");
+    return KVEV_OK;
+}
 
 kvev_status kvev_set_tiers(kvev_ctx* c, int64_t k_full, int64_t k_quant, int32_t omega) {
     if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
@@ -1213,6 +1328,13 @@ kvev_status kvev_tier_begin(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_t
     rc = timed_launch(c, kProfInit, s, "tier begin",
                       [&] { return launch_tier_begin(a, prefill_tokens, s); });
     if (rc != KVEV_OK) return rc;
+    if (c->lir_counters) {   // Global LIR counts start over with the run
+        cudaError_t e = cudaMemsetAsync(c->ws.lir_streak, 0,
+                                        (size_t)c->lay.batch * tier_max_windows(c->lay) * 4, s);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(c->lir_counters, 0, (size_t)c->lay.batch * 3 * 4, s);
+        if (e != cudaSuccess) return cuda_fail(e, "resetting the LIR counts");
+    }
     c->t_nw = hist / kTierW;
     c->t_tl = hist % kTierW;
     c->t_first_u = 0;
@@ -1381,6 +1503,8 @@ kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const 
         if (rc == KVEV_OK)
             rc = timed_launch(c, kProfCompact, s, "finish",
                               [&] { return launch_tier_finish(ta, s); });
+        if (rc == KVEV_OK && c->lir_counters)
+            rc = timed_launch(c, kProfSelect, s, "lir", [&] { return launch_tier_lir(ta, s); });
         if (rc != KVEV_OK) return rc;
         c->t_first_u += n_aged;
         c->t_nf = nf2;
@@ -1552,6 +1676,7 @@ kvev_status kvev_import_state(kvev_ctx* c, const void* host, size_t bytes, void*
     c->t_nq = h.t_nq;
     c->ub_blocks.assign(h.n_ub, 0);
     c->pin_blocks.assign(h.n_pin, 0);
+    c->diag_flags_valid = false;   // the raw-set flags are not part of a checkpoint
     memcpy(c->ub_blocks.data(), in + sizeof h, 4 * (size_t)h.n_ub);
     memcpy(c->pin_blocks.data(), in + sizeof h + 4 * (size_t)h.n_ub, 4 * (size_t)h.n_pin);
     {   // the caller's other cache buffer holds nothing the next step may reuse

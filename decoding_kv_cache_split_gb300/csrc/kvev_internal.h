@@ -154,6 +154,32 @@ struct ScoreArgs {
     int32_t refresh, age_mode, pool_mean;
     int32_t t;
     float alpha, beta, access_thr;   // access: sum over layers of head-summed p >= access_thr
+    // ranking diagnostics (refresh steps): the raw per-step score (the
+    // head-summed probability summed over layers) as a sortable key that
+    // ranks the largest first, and optionally as a value
+    uint32_t* raw_keys;    // [b][max_ctx] or null
+    float* dbg_raw;        // [b][max_ctx] or null
+};
+
+// Ranking diagnostics of one token-mode step (diag.cu).
+struct DiagArgs {
+    const int32_t* retained;    // [b][budget] kept slots (ascending), n_retained [b]
+    const int32_t* n_retained;
+    const int32_t* raw_list;    // [b][budget] top-B slots of the raw score (refresh)
+    const int32_t* raw_n;       // [b]
+    uint8_t* in_raw;            // [b][max_ctx] scratch
+    const uint8_t* flags_in;    // [b][max_ctx] slot in the last raw set (pre-step cache)
+    uint8_t* flags_out;         // [b][max_ctx] the same after this step's compaction
+    int32_t* prev_n;            // [b] size of the last raw set
+    int32_t* counters;          // [b][KVEV_DIAG_FIELDS] user output
+    int32_t L, max_ctx, budget, t, refresh, flags_valid;
+};
+
+struct MissedMassArgs {
+    const float* full_score;    // [b][score_ld] FullKV raw score by position
+    const int32_t* pos;         // [b][pos_ld] positions the policy holds
+    float* out;                 // [b]
+    int32_t score_ld, n_pos, pos_ld, n_cached;
 };
 
 struct SelectArgs {
@@ -354,7 +380,14 @@ struct TierArgs {
     int32_t batch, n_layers, n_kv, n_q, head_dim;
     int32_t k_full, k_quant;
     int32_t t;
-    float alpha;
+    float alpha;           // window score per layer: m <- alpha s + oma m (EMA:
+    float oma;             //   oma = 1 - alpha; cumulative, Eq. (1): both 1)
+    // Global LIR bookkeeping (null: off): routing events each window has
+    // spent outside the Full tier in a row, and per sequence the counts
+    // {routing events, revivals, sustained-inactive spans}
+    int32_t* lir_streak;   // [b][max_windows]
+    int32_t* lir_counters; // [b][3]
+    int32_t lir_sustain;
 };
 
 // ---- programmatic dependent launch ----------------------------------------
@@ -395,6 +428,8 @@ cudaError_t launch_attention(const AttnArgs& a, int head_dim, int group, int gri
 cudaError_t launch_combine(const CombineArgs& a, int head_dim, int group, cudaStream_t s);
 cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, int batch, int num_sms, cudaStream_t s);
+cudaError_t launch_diag(const DiagArgs& a, int batch, cudaStream_t s);
+cudaError_t launch_missed_mass(const MissedMassArgs& a, int batch, cudaStream_t s);
 cudaError_t launch_compact(const CompactArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_init_state(kvev_state st, int batch, int max_ctx, int len, int32_t* vp,
@@ -420,6 +455,7 @@ cudaError_t launch_tier_route(const TierArgs& a, cudaStream_t s);
 cudaError_t launch_tier_quantize(const TierArgs& a, int max_items, int num_sms, cudaStream_t s);
 cudaError_t launch_tier_promote(const TierArgs& a, int max_items, int num_sms, cudaStream_t s);
 cudaError_t launch_tier_finish(const TierArgs& a, cudaStream_t s);
+cudaError_t launch_tier_lir(const TierArgs& a, cudaStream_t s);
 
 enum : uint32_t { kStatusNoPage = 2u };   // a sequence ran out of free pages
 enum : uint32_t { kStatusRouteCap = 4u };  // more windows than the routing sort holds

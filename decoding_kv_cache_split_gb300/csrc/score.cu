@@ -201,6 +201,8 @@ __global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const Sc
     a.tins_s[si] = t_ins;
     a.pos_s[si] = a.st.pos[si];
     if (a.dbg_prio) a.dbg_prio[si] = pr + 0.0f;
+    if (a.raw_keys) a.raw_keys[si] = order_bits(-tot);   // the largest raw score first
+    if (a.dbg_raw) a.dbg_raw[si] = tot;
 }
 
 template <int G, bool VN>

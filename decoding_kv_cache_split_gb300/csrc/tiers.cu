@@ -234,7 +234,8 @@ __global__ void __launch_bounds__(kBook) tier_append_kernel(const TierArgs a,
 // 128 tokens received, from the tile statistics of the attention kernels
 // (running max m, sum of exp2(x - m) per head and 16-token tile) and the
 // combine's log2-sum-exp: sum exp2(m - lse) * sum; folded into the EMA
-// layer after layer.
+// layer after layer, or added to the score (the cumulative score of the
+// review's Sec. 4.2 Eq. (1): alpha = oma = 1).
 template <int G>
 __global__ void __launch_bounds__(256) tier_score_kernel(const TierArgs a) {
     griddep_wait();
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(256) tier_score_kernel(const TierArgs a) {
     if (!is_bf16_tier(tr) && tr != KVEV_TIER_QUANT) return;
     constexpr int PW = kTierW / kTile;
     float m = a.st.score[wi];
-    const float inv_hq = 1.0f / (float)a.n_q, oma = 1.0f - a.alpha;
+    const float inv_hq = 1.0f / (float)a.n_q, oma = a.oma;
     // the layers' masses in batches of 8 (their loads are independent), then
     // the EMA folded over them in layer order
     constexpr int kLB = 8;
@@ -710,7 +711,61 @@ __global__ void __launch_bounds__(256) tier_finish_kernel(const TierArgs a) {
     if (threadIdx.x == 0) a.c.n_free[b] = nf + n * PW;
 }
 
+// Global LIR bookkeeping after a routing event (the QEvict review, Sec. 3:
+// how often a window inactive for a sustained period re-enters the
+// full-precision set).  Per window of the sequence, routed ones only: Full
+// -> a revival when it had been outside Full at `sustain` or more routing
+// events in a row, then its streak restarts; INT2 or evicted -> the streak
+// grows, and reaching `sustain` opens a sustained-inactive span.  One CTA
+// per sequence; the counts are added in a fixed order (block reduction).
+__global__ void __launch_bounds__(256) tier_lir_kernel(const TierArgs a) {
+    __shared__ int red[2][8];
+    griddep_wait();
+    griddep_release();
+    const int b = blockIdx.x, MW = a.c.max_windows;
+    const int nw = a.st.n_windows[b];
+    int rev = 0, span = 0;
+    for (int w = threadIdx.x; w < nw; w += blockDim.x) {
+        const size_t wi = (size_t)b * MW + w;
+        const uint8_t tr = a.st.tier[wi];
+        if (tr == KVEV_TIER_UNROUTED || tr == KVEV_TIER_NONE) continue;
+        const int st = a.lir_streak[wi];
+        if (tr == KVEV_TIER_FULL) {
+            rev += st >= a.lir_sustain;
+            a.lir_streak[wi] = 0;
+        } else {
+            a.lir_streak[wi] = st + 1;
+            span += st + 1 == a.lir_sustain;
+        }
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+        rev += __shfl_xor_sync(0xffffffffu, rev, m);
+        span += __shfl_xor_sync(0xffffffffu, span, m);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        red[0][threadIdx.x >> 5] = rev;
+        red[1][threadIdx.x >> 5] = span;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int r = 0, sp = 0;
+        for (int k = 0; k < 8; ++k) {
+            r += red[0][k];
+            sp += red[1][k];
+        }
+        int32_t* c = a.lir_counters + (size_t)b * 3;
+        c[0] += 1;
+        c[1] += r;
+        c[2] += sp;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_tier_lir(const TierArgs& a, cudaStream_t s) {
+    return launch_pdl(tier_lir_kernel, dim3(a.batch), dim3(256), 0, s, a);
+}
 
 cudaError_t launch_tier_begin(const TierArgs& a, int prefill_tokens, cudaStream_t s) {
     return launch_pdl(tier_begin_kernel, dim3(a.batch), dim3(kBook), 0, s, a, prefill_tokens);

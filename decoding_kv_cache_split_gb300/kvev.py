@@ -27,6 +27,9 @@ KVEV_POOL_SUM, KVEV_POOL_MEAN = 0, 1
 KVEV_OUT_F32, KVEV_OUT_BF16 = 0, 1
 KVEV_AGG_EMA, KVEV_AGG_CUMULATIVE = 0, 1
 KVEV_W_VNORM, KVEV_W_ENTROPY = 1, 2
+KVEV_DIAG_FIELDS = 8
+DIAG_NAMES = ["step", "refreshed", "n_raw", "n_kept", "raw_and_kept", "raw_and_prev_raw",
+              "n_prev_raw", "kept_and_prev_kept"]
 KVEV_BF16 = 0
 KVEV_MAX_REGIONS = 16
 KVEV_SCORE_LRFU, KVEV_SCORE_MEMDECAY = 0, 1
@@ -43,9 +46,11 @@ EXPORTS = ["kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_siz
            "kvev_begin",
            "kvev_length",
            "kvev_init_state", "kvev_step", "kvev_step_host", "kvev_set_debug",
+           "kvev_set_diagnostics", "kvev_missed_mass",
            "kvev_profile", "kvev_profile_read", "kvev_launch_count", "kvev_test_wait_timeout",
            "kvev_check_scratch", "kvev_sync",
            "kvev_paged_begin", "kvev_paged_step", "kvev_readmit", "kvev_set_tiers",
+           "kvev_tier_diagnostics",
            "kvev_tier_begin", "kvev_tier_step", "kvev_export_state", "kvev_import_state",
            "kvev_attend_noalloc"]
 
@@ -156,6 +161,8 @@ def lib():
             "kvev_step": ([P, P, P, P, P, P, I64, P, P, P, P], I32),
             "kvev_step_host": ([P, P, P, P, P, P, I64, P, P, P, P], I32),
             "kvev_set_debug": ([P, P, P], I32),
+            "kvev_set_diagnostics": ([P, P, P], I32),
+            "kvev_missed_mass": ([P, I32, I32, P, I32, I32, I32, P, P], I32),
             "kvev_profile": ([P, I32], I32),
             "kvev_profile_read": ([P, P, P], I32),
             "kvev_launch_count": ([P, P], I32),
@@ -166,6 +173,7 @@ def lib():
             "kvev_paged_step": ([P, P, P, P, P, P, I64, P, P, P, P], I32),
             "kvev_readmit": ([P, P, P, I32, I32, I32, P], I32),
             "kvev_set_tiers": ([P, I64, I64, I32], I32),
+            "kvev_tier_diagnostics": ([P, I32, P, P], I32),
             "kvev_tier_begin": ([P, P, P, I32, P], I32),
             "kvev_tier_step": ([P, P, P, P, P, P, I64, P, P], I32),
             "kvev_export_state": ([P, P, P], I32),
@@ -278,6 +286,18 @@ def kvev_set_debug(ctx, probs=None, priority=None) -> None:
     _check(lib().kvev_set_debug(ctx, _ptr(probs), _ptr(priority)), ctx)
 
 
+def kvev_set_diagnostics(ctx, counters=None, raw_score=None) -> None:
+    _check(lib().kvev_set_diagnostics(ctx, _ptr(counters), _ptr(raw_score)), ctx)
+
+
+def kvev_missed_mass(full_score, score_ld: int, n_pos: int, pos, pos_ld: int, n_cached: int,
+                     batch: int, out, stream=None) -> None:
+    """Future Missed Mass of one step (see include/kvev.h)."""
+    _check(lib().kvev_missed_mass(_ptr(full_score), int(score_ld), int(n_pos), _ptr(pos),
+                                  int(pos_ld), int(n_cached), int(batch), _ptr(out),
+                                  _stream(stream)))
+
+
 def kvev_profile(ctx, enable: bool) -> None:
     _check(lib().kvev_profile(ctx, int(bool(enable))), ctx)
 
@@ -330,6 +350,10 @@ def kvev_readmit(ctx, cache: kvev_paged_cache, state: kvev_block_state, seq: int
 
 def kvev_set_tiers(ctx, k_full: int, k_quant: int, omega: int) -> None:
     _check(lib().kvev_set_tiers(ctx, int(k_full), int(k_quant), int(omega)), ctx)
+
+
+def kvev_tier_diagnostics(ctx, sustain: int, counters=None, stream=None) -> None:
+    _check(lib().kvev_tier_diagnostics(ctx, int(sustain), _ptr(counters), _stream(stream)), ctx)
 
 
 def kvev_tier_begin(ctx, cache: kvev_tier_cache, state: kvev_tier_state, prefill_tokens: int,
@@ -542,7 +566,7 @@ class TierEvictionPass:
     tensors on the current CUDA device."""
 
     def __init__(self, n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, pages_per_seq,
-                 k_full, k_quant, omega, alpha, device="cuda"):
+                 k_full, k_quant, omega, alpha, aggregation=KVEV_AGG_EMA, device="cuda"):
         import torch
         self.torch = torch
         self.pps, self.max_ctx = int(pages_per_seq), int(max_ctx)
@@ -551,6 +575,7 @@ class TierEvictionPass:
                                   KVEV_TIER_WINDOW, KVEV_BF16)
         self.ctx = kvev_create(self.layout, k_full, KVEV_TIER_WINDOW, alpha, 0.0)
         kvev_set_tiers(self.ctx, k_full, k_quant, omega)
+        kvev_set_scorer(self.ctx, aggregation, 0)
         i32 = dict(dtype=torch.int32, device=device)
         pshape = (batch * self.pps, n_layers, n_kv_heads, 16, head_dim)
         self.k_pool = torch.zeros(pshape, dtype=torch.bfloat16, device=device)

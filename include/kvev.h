@@ -186,9 +186,9 @@ kvev_status kvev_configure(kvev_ctx* ctx, int32_t age_mode, int32_t pool);
 /* Element type of the attention output `out` of kvev_step, kvev_step_host,
  * kvev_paged_step and kvev_tier_step (from the next step on):
  *   KVEV_OUT_F32   fp32, the combine's result as computed (default: it keeps
- *                  the accumulation's precision, which the parity checks at
- *                  2e-3 relative need, since bf16 rounding alone costs up to
- *                  2^-9 = 1.95e-3 of a vector's largest element);
+ *                  the accumulation's precision; the attention tolerance of
+ *                  2e-3 relative is below bf16's own unit roundoff 2^-8 =
+ *                  3.9e-3, so a bf16 output could not be held to it);
  *   KVEV_OUT_BF16  the same fp32 values rounded to bf16 (nearest even), half
  *                  the bytes, for a caller that feeds the output to a bf16
  *                  projection.
@@ -263,6 +263,45 @@ kvev_status kvev_step_host(kvev_ctx* ctx, const void* q_host, const void* k_new_
                            const void* v_new_host, kvev_cache* cache, const kvev_state* state,
                            int64_t step, void* out_host, int32_t* retained_idx_host,
                            int32_t* n_retained_host, void* stream);
+
+/* Ranking diagnostics of token-granular steps ("What Matters for
+ * Aggressive Decoding-Time KV Eviction?", Sec. 5.3 and Appendix I, Table 13),
+ * computed on the device by every later step (counters NULL disables them):
+ *   counters   [batch][KVEV_DIAG_FIELDS] int32, per step and sequence:
+ *              step t, refreshed (1 on scoring steps), |R| (the raw top-B
+ *              set: the `budget` tokens of largest raw score, ties to the
+ *              lower slot; 0 on non-scoring steps), |E| (the retained set),
+ *              |R & E|, |R & R_prev| (tokens of the previous scoring step's
+ *              raw set still cached), |R_prev| (0 before the second scoring
+ *              step), |E & E_prev| (retained tokens held before this step);
+ *              raw/EMA Jaccard = |R & E| / (|R| + |E| - |R & E|), raw churn =
+ *              1 - |R & R_prev| / (|R| + |R_prev| - |R & R_prev|), EMA churn
+ *              likewise from |E & E_prev|, raw-top evicted = 1 - |R & E|/|R|;
+ *   raw_score  [batch][max_ctx] fp32 or NULL: each slot's raw score of
+ *              scoring steps (the attention summed over query heads and
+ *              layers, before any aggregation), slots of the cache after the
+ *              append (before compaction).
+ * The raw score is the scorer's own sum (no extra read of the cache); the
+ * raw set costs one more selection launch and the counts one small kernel
+ * per step.  Block-granular and two-tier contexts: KVEV_EUNSUPPORTED. */
+enum { KVEV_DIAG_FIELDS = 8 };
+kvev_status kvev_set_diagnostics(kvev_ctx* ctx, int32_t* counters, float* raw_score);
+
+/* Future Missed Mass (QEvict review, Sec. 3 "Diagnosing the problem") of one
+ * step of a compressed run against a FullKV run of the same inputs: per
+ * sequence b,
+ *   out[b] = 1 - (sum over the positions p the policy holds of F[b][p] +
+ *                 F[b][n_pos - 1]) / (sum over p < n_pos of F[b][p])
+ * with F the FullKV run's raw scores by position (e.g. the raw_score output
+ * of a context whose budget is never reached, where slot = position) after
+ * its step over n_pos positions, and pos[b][0 .. n_cached) the positions
+ * the policy held before its own step over the same new token (its
+ * kvev_state.pos and kvev_length then); the new token (position n_pos - 1)
+ * counts as held and positions outside [0, n_pos - 1) are ignored.  No
+ * context, no allocation; asynchronous on `stream`. */
+kvev_status kvev_missed_mass(const float* full_score, int32_t score_ld, int32_t n_pos,
+                             const int32_t* pos, int32_t pos_ld, int32_t n_cached,
+                             int32_t batch, float* out, void* stream);
 
 /* Optional diagnostic outputs written by later steps (NULL disables):
  *   probs     [batch][n_layers][n_q_heads][max_ctx] fp32, the attention
@@ -437,8 +476,25 @@ typedef struct {
 } kvev_tier_state;
 
 /* Tier capacities K_f (Full windows), K_q (INT2 windows) and the routing
- * interval omega >= 1 (Eq. (3) gives K_f, K_q from a byte budget). */
+ * interval omega >= 1 (Eq. (3) gives K_f, K_q from a byte budget).  The
+ * window score is the EMA above by default; kvev_set_scorer with
+ * KVEV_AGG_CUMULATIVE makes it Sec. 4.2 Eq. (1)'s cumulative score: the
+ * head-averaged window attention added up over steps and layers, never
+ * decaying. */
 kvev_status kvev_set_tiers(kvev_ctx* ctx, int64_t k_full, int64_t k_quant, int32_t omega);
+
+/* Global LIR (Long-term Importance Revival, the QEvict review's Sec. 3
+ * "Diagnosing the problem"): how often a window that stayed out of the Full
+ * tier for a sustained period re-enters it.  With `counters` set
+ * ([batch][3] int32, device), every later routing event adds per sequence
+ * {1 routing event, revivals, sustained-inactive spans}: a routed window
+ * outside Full (INT2 or evicted) at `sustain` routing events in a row opens
+ * a span; such a window routed to Full counts a revival and its count
+ * restarts.  Windows not yet routed do not count.  LIR = revivals / spans.
+ * This call and kvev_tier_begin zero the counts (enqueued on `stream`);
+ * counters = NULL turns the bookkeeping off. */
+kvev_status kvev_tier_diagnostics(kvev_ctx* ctx, int32_t sustain, int32_t* counters,
+                                  void* stream);
 
 /* Start a tiered run over a prefill of `prefill_tokens` (>= 5) tokens that
  * the caller wrote into the pool: tokens 0..4 in rows 0..4 of page b*pps,

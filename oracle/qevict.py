@@ -13,7 +13,10 @@ Attention-Drift-Robust Long-Context Decoding" (the review page), Sec. 4:
     (the inner sums of Eq. (1)), folded per step into an EMA with weight
     alpha on the new value, layer after layer in ascending order, kept
     across steps (the LRFU EMA of the kv-cache-docs figure "ema-eviction",
-    the reading this build takes for "EMA accumulated-attention score");
+    the reading this build takes for "EMA accumulated-attention score"); or,
+    with `cumulative`, Sec. 4.2 Eq. (1) itself: the head-averaged window
+    attention added up over steps and, since one routing decision covers
+    every layer, over layers too (a sum that never forgets);
   * Eq. (3): tier capacities K_f = floor((1-q) B_hist / M_f) and
     K_q = floor(q B_hist / M_q);
   * Eqs. (4)-(5) and the routing algorithm: every Omega steps the candidates
@@ -71,6 +74,7 @@ class QParams:
     n_recent: int = 32
     omega: int = 8
     group: int = 32
+    cumulative: bool = False      # Eq. (1): the window score sums, never decays
 
 
 def capacities(b_hist: float, q: float, m_full: float, m_quant: float):
@@ -284,7 +288,10 @@ def step(P: QParams, seq: QSequence, t: int, q_bits, knew_bits, vnew_bits,
         per_window = np.bincount(owner[inw], weights=tok[inw], minlength=len(seq.windows))
         s = per_window[live]
         s_layers[layer] = s
-        m = P.alpha * s + (1.0 - P.alpha) * m
+        if P.cumulative:                         # Eq. (1): add the layer's mass
+            m = m + s
+        else:
+            m = P.alpha * s + (1.0 - P.alpha) * m
     for k, j in enumerate(live):
         seq.windows[j].m = float(m[k])
     routed = t % P.omega == 0

@@ -96,6 +96,7 @@ NULL_CTX_CALLS = {
     "kvev_set_debug": lambda L: L.kvev_set_debug(None, None, None),
     "kvev_set_output": lambda L: L.kvev_set_output(None, 1),
     "kvev_set_scorer": lambda L: L.kvev_set_scorer(None, 1, 0),
+    "kvev_set_diagnostics": lambda L: L.kvev_set_diagnostics(None, None, None),
     "kvev_profile": lambda L: L.kvev_profile(None, 1),
     "kvev_profile_read": lambda L: L.kvev_profile_read(None, None, None),
     "kvev_launch_count": lambda L: L.kvev_launch_count(None, _out()),
@@ -106,6 +107,7 @@ NULL_CTX_CALLS = {
                                                    None, None, None),
     "kvev_readmit": lambda L: L.kvev_readmit(None, None, None, 0, 0, 1, None),
     "kvev_set_tiers": lambda L: L.kvev_set_tiers(None, 1, 1, 8),
+    "kvev_tier_diagnostics": lambda L: L.kvev_tier_diagnostics(None, 4, None, None),
     "kvev_tier_begin": lambda L: L.kvev_tier_begin(None, None, None, 0, None),
     "kvev_tier_step": lambda L: L.kvev_tier_step(None, None, None, None, None, None, 1, None, None),
     "kvev_export_state": lambda L: L.kvev_export_state(None, None, _out()),
@@ -116,7 +118,7 @@ NULL_CTX_CALLS = {
 def test_every_context_call_is_covered():
     with_ctx = {"kvev_refresh_mode", "kvev_configure", "kvev_begin", "kvev_step", "kvev_sync"}
     no_ctx = {"kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_size",
-              "kvev_attend_noalloc"}
+              "kvev_attend_noalloc", "kvev_missed_mass"}
     assert set(NULL_CTX_CALLS) | with_ctx | no_ctx == set(kvev.EXPORTS)
 
 
@@ -177,3 +179,14 @@ def test_region_table_layout_matches_the_header():
     assert T.base_priority.offset == 4 and T.decay_lambda.offset == 68
     assert T.pinned.offset == 132 and T.score_kind.offset == 148
     assert ctypes.sizeof(T) == 168
+
+
+def test_missed_mass_rejects_bad_arguments(lib):
+    one = ctypes.c_void_p(16)          # never dereferenced: refused before any launch
+    assert lib.kvev_missed_mass(None, 8, 4, one, 4, 2, 1, one, None) == kvev.KVEV_EINVAL
+    assert lib.kvev_missed_mass(one, 8, 4, one, 4, 2, 1, None, None) == kvev.KVEV_EINVAL
+    assert lib.kvev_missed_mass(one, 8, 0, one, 4, 2, 1, one, None) == kvev.KVEV_EINVAL
+    assert lib.kvev_missed_mass(one, 3, 4, one, 4, 2, 1, one, None) == kvev.KVEV_EINVAL
+    assert lib.kvev_missed_mass(one, 8, 4, one, 1, 2, 1, one, None) == kvev.KVEV_EINVAL
+    assert lib.kvev_missed_mass(one, 8, 4, one, 4, 2, 0, one, None) == kvev.KVEV_EINVAL
+    assert lib.kvev_missed_mass(one, 8, 4, None, 4, 2, 1, one, None) == kvev.KVEV_EINVAL

@@ -14,8 +14,8 @@ import pytest
 import oracle as O
 from workloads import Geometry, Workload, llama8b_workload, tiny_workload
 
-from parity import (access_alternative, compare_step, follow, load_prefill, oracle_step,
-                    to_dev_bf16)
+from parity import (access_alternative, boundary_check, compare_step, follow, load_prefill,
+                    oracle_step, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,7 +35,9 @@ REFRESH = {"full": (O.REFRESH_FULL, kvev.KVEV_REFRESH_FULL),
 def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int, *,
                age_mode=O.AGE_SINCE_INSERT, refresh="full", period=8, pool_mean=False,
                max_ctx=None, check_every=1, aggregation=O.AGG_EMA, weighting=0,
-               m_atol=None):
+               m_atol=None, diagnostics=False):
+    """`diagnostics`: the ranking counters and raw scores are gathered on
+    the device every step and checked (check_diagnostics)."""
     g = wl.geom
     max_ctx = max_ctx or max(wl.L0 + steps + 1, budget + 1)
     mode_o, mode_d = REFRESH[refresh]
@@ -53,6 +55,13 @@ def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int,
                         device="cuda")
     prio = torch.zeros((g.batch, max_ctx), dtype=torch.float32, device="cuda")
     kvev.kvev_set_debug(ep.ctx, probs, prio)
+    counters = raw_dev = None
+    if diagnostics:
+        counters = torch.full((g.batch, kvev.KVEV_DIAG_FIELDS), -1, dtype=torch.int32,
+                              device="cuda")
+        raw_dev = torch.zeros((g.batch, max_ctx), dtype=torch.float32, device="cuda")
+        kvev.kvev_set_diagnostics(ep.ctx, counters, raw_dev)
+    prev_raw = [None] * g.batch          # positions of the last raw top-B set, its size
     P = O.OracleParams(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, budget, alpha, beta,
                        age_mode, pool_mean, aggregation, weighting)
     K, V = wl.prefill()
@@ -73,6 +82,9 @@ def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int,
             assert pre.L == L_prev, "oracle and device cache lengths"
             res, new = oracle_step(P, pre, t, refresh_now, q[b], kn[b], vn[b], wl.L0 + t - 1,
                                    want_probs=check)
+            if diagnostics:
+                totals["diag_swaps"] = totals.get("diag_swaps", 0) + check_diagnostics(
+                    res, ep, b, pre, budget, counters, raw_dev, prev_raw, refresh_now, t)
             alt, amb = access_alternative(res, pre, P) if refresh_now else (None, None)
             if check:
                 st = compare_step(res, ep, b, pre, budget, probs, prio, refresh_now, alt,
@@ -100,6 +112,40 @@ def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int,
     kvev.kvev_check_scratch(ep.ctx)   # no scratch region overran its guard band
     ep.close()
     return totals
+
+
+def check_diagnostics(res, ep, b, pre, budget, counters, raw_dev, prev_raw, refresh, t):
+    """The device's ranking diagnostics of step t, sequence b: its raw
+    scores against the oracle's (the head- and layer-summed probabilities,
+    the probability tolerance), its raw top-B set (restated on the host from
+    its own fp32 scores: the B largest, ties to the lower slot) admissible
+    against the oracle's fp64 ranking, and its counters equal to the exact
+    counts of its sets (oracle/diagnostics.py).  Returns the near-tie swaps
+    of the raw set; updates prev_raw[b]."""
+    from oracle import diagnostics as D
+    L = res["L"]
+    c = counters[b].cpu().numpy()
+    n = int(ep.n_retained[b].item())
+    kept = ep.retained[b, :n].cpu().numpy().astype(np.int64)
+    pos = np.append(pre.pos[:L - 1], res["new_pos"])
+    assert c[0] == t and c[1] == int(refresh)
+    swaps = 0
+    if refresh:
+        raw = raw_dev[b, :L].cpu().numpy().astype(np.float64)
+        ref = res["score_sum"]
+        atol = 1e-9 * ep.layout.n_layers * ep.layout.n_q_heads   # the probabilities' own
+        assert (np.abs(raw - ref) <= 2e-3 * ref + atol).all(), "raw scores"
+        R = D.raw_topb(raw.astype(np.float32).astype(np.float64), budget)
+        swaps = boundary_check(-ref, R, budget, 1e-5)
+        prev = prev_raw[b]
+        want = D.step_counts(R, kept, L, None if prev is None else prev[0],
+                             0 if prev is None else prev[1], pos)
+        prev_raw[b] = (pos[R], len(R))
+    else:
+        want = D.step_counts([], kept, L)
+    got = dict(zip(kvev.DIAG_NAMES[2:], (int(x) for x in c[2:])))
+    assert got == want, f"step {t}: counters {got} vs {want}"
+    return swaps
 
 
 def test_tiny_token_eviction_64_steps():
@@ -177,6 +223,27 @@ def test_scorer_weightings_on_small_shapes(weighting):
     run_parity(wl, 40, 0.2, 0.001, 5, weighting=weighting, pool_mean=True)
     wl1 = Workload(Geometry(1, 4, 1, 128, 1), 0, seed=5)
     run_parity(wl1, 2, 0.3, 0.001, 4, weighting=weighting)
+
+
+@pytest.mark.parametrize("refresh", ["full", "lazy"])
+def test_ranking_diagnostics(refresh):
+    """The device's raw top-B / retained-set counters (Sec. 5.3, Appendix I
+    Table 13) over 14 steps of the Llama-3.1-8B head geometry (3 layers,
+    1000-token prefill, budget 100, a needle re-drawn every 5 steps), full
+    refresh or lazy refresh every 3 steps (counts on the scoring steps only,
+    the raw-set flags carried through the compactions in between)."""
+    wl = llama8b_workload(0, prefill_len=1000, n_layers=3, needle_period=5)
+    tot = run_parity(wl, 100, 0.05, 0.001, 14, age_mode=O.AGE_SINCE_ACCESS, refresh=refresh,
+                     period=3, diagnostics=True)
+    print(refresh, tot)
+
+
+def test_ranking_diagnostics_tiny_and_below_budget():
+    """The tiny workload (heavy hitters, 64 steps) and a cache that stays
+    below the budget (the raw set is every token)."""
+    run_parity(tiny_workload(0), 128, 0.05, 0.001, 64, diagnostics=True)
+    wl = Workload(Geometry(2, 8, 2, 64, 2), 20, seed=9, heavy=2)
+    run_parity(wl, 40, 0.05, 0.001, 6, diagnostics=True)
 
 
 def test_probabilities_sum_to_one():

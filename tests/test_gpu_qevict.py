@@ -66,9 +66,16 @@ def admissible(m: dict, dev_tiers: dict, tol: float):
                 assert m[a] >= m[b] - tol, f"window {a} ({ta}) below {b} ({tb})"
 
 
-def compare(tp, P, seqs, b, t, q, kn, vn, stats, check_windows=None):
+def score_tol(P, m):
+    """Window-score tolerance: 1e-5 absolute for the EMA; the cumulative
+    score grows with every step and layer, where fp32 keeps 1e-5 relative."""
+    return M_ATOL * max(1.0, abs(m)) if P.cumulative else M_ATOL
+
+
+def compare(tp, P, seqs, b, t, q, kn, vn, stats, check_windows=None, lir=None):
     """check_windows: ids whose pages / ledger entries are compared (all when
-    None)."""
+    None); lir: (oracle LIRCounter per sequence, device counters) to check
+    after routing events."""
     pre = copy.deepcopy(seqs[b])
     res = QE.step(P, seqs[b], t, q, kn, vn)
     seq = seqs[b]
@@ -77,7 +84,7 @@ def compare(tp, P, seqs, b, t, q, kn, vn, stats, check_windows=None):
         # a near tie at a tier boundary: check the device's choice, then follow it
         cand = {w.wid: res["m"][w.wid] for w in pre.windows if w.wid in res["m"]}
         new_t = {wid: dev_tier[wid] for wid in cand if dev_tier[wid] in ("F", "Q", "E")}
-        admissible(cand, new_t, M_ATOL)
+        admissible(cand, new_t, max(score_tol(P, m) for m in cand.values()))
         order = sorted(new_t, key=lambda wid: ({"F": 0, "Q": 1, "E": 2}[new_t[wid]], -cand[wid], wid))
         seqs[b] = pre
         res = QE.step(P, seqs[b], t, q, kn, vn, ranking=order)
@@ -93,8 +100,15 @@ def compare(tp, P, seqs, b, t, q, kn, vn, stats, check_windows=None):
     stats["out_rel"] = max(stats["out_rel"], float(err.max()))
     sc = tp.score[b].cpu().numpy().astype(np.float64)
     for wid, m in res["m"].items():
-        assert abs(sc[wid] - m) <= M_ATOL, f"step {t} seq {b}: score of window {wid}"
+        assert abs(sc[wid] - m) <= score_tol(P, m), f"step {t} seq {b}: score of window {wid}"
         stats["m_abs"] = max(stats["m_abs"], abs(sc[wid] - m))
+    if lir is not None and res["routed"]:
+        counter, dev = lir
+        counter[b].route({w.wid: w.tier for w in seq.windows})
+        got = dev[b].cpu().numpy().tolist()
+        assert got == [counter[b].events, counter[b].revivals, counter[b].spans], \
+            f"step {t} seq {b}: LIR counts {got}"
+        stats["revivals"] = stats.get("revivals", 0) + 0   # reported at the end
     assert int(tp.n_windows[b]) == len(seq.windows)
     assert int(tp.tail_len[b]) == seq.K_tail.shape[2]
     wp = tp.win_pages[b].cpu().numpy()
@@ -121,18 +135,28 @@ def compare(tp, P, seqs, b, t, q, kn, vn, stats, check_windows=None):
             stats["ledgers"] += 1
 
 
-def run_tiers(wl, k_full, k_quant, omega, steps, alpha=0.05, pps_slack=24):
+def run_tiers(wl, k_full, k_quant, omega, steps, alpha=0.05, pps_slack=24, cumulative=False,
+              sustain=None):
+    """sustain: check the Global LIR counts with that span length."""
     g = wl.geom
     L0 = wl.L0
     max_ctx = L0 + steps + 8
     pps = 1 + -(-(L0 - 5) // 16) + pps_slack
     tp = kvev.TierEvictionPass(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, g.batch,
-                               max_ctx, pps, k_full, k_quant, omega, alpha)
+                               max_ctx, pps, k_full, k_quant, omega, alpha,
+                               aggregation=kvev.KVEV_AGG_CUMULATIVE if cumulative
+                               else kvev.KVEV_AGG_EMA)
+    lir = None
+    if sustain is not None:
+        from oracle import diagnostics as D
+        dev = torch.full((g.batch, 3), -1, dtype=torch.int32, device="cuda")
+        kvev.kvev_tier_diagnostics(tp.ctx, sustain, dev)
+        lir = ([D.LIRCounter(sustain) for _ in range(g.batch)], dev)
     K, V = wl.prefill()
     load(tp, K, V, L0)
     tp.begin(L0)
     P = QE.QParams(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, k_full, k_quant,
-                   alpha=alpha, omega=omega)
+                   alpha=alpha, omega=omega, cumulative=cumulative)
     seqs = [QE.QSequence.from_prefill(P, K[:, b], V[:, b]) for b in range(g.batch)]
     stats = {"swaps": 0, "out_rel": 0.0, "m_abs": 0.0, "ledgers": 0, "promoted": 0,
              "redemoted": 0}
@@ -141,7 +165,9 @@ def run_tiers(wl, k_full, k_quant, omega, steps, alpha=0.05, pps_slack=24):
         tp.step(to_dev_bf16(q), to_dev_bf16(kn), to_dev_bf16(vn))
         kvev.kvev_sync(tp.ctx)
         for b in range(g.batch):
-            compare(tp, P, seqs, b, t, q[b], kn[b], vn[b], stats)
+            compare(tp, P, seqs, b, t, q[b], kn[b], vn[b], stats, lir=lir)
+    if lir is not None:
+        stats["lir"] = [(c.events, c.revivals, c.spans) for c in lir[0]]
     kvev.kvev_check_scratch(tp.ctx)   # no scratch region overran its guard band
     tp.close()
     return stats
@@ -157,6 +183,21 @@ def test_tiers_small_routing_promotion_and_new_window():
     st = run_tiers(wl, 2, 3, 4, 100)
     print("tiers:", st)
     assert st["ledgers"] > 0 and st["promoted"] > 0 and st["redemoted"] > 0
+
+
+def test_tiers_cumulative_window_score_and_global_lir():
+    """The review's Sec. 4.2 Eq. (1) cumulative window score (sums over steps
+    and layers, never decays) driving the routing, with the Global LIR counts
+    (Sec. 3) checked after every routing event against the oracle's
+    restatement; then the EMA score with LIR counts over a drifting needle,
+    where windows leave the Full tier and come back."""
+    wl = Workload(Geometry(2, 32, 8, 128, 2), 5 + 128 * 10 + 40, seed=7, outliers=4, needle=16,
+                  needle_period=16)
+    st = run_tiers(wl, 2, 3, 4, 60, cumulative=True, sustain=2)
+    print("tiers cumulative:", st)
+    st = run_tiers(wl, 2, 3, 4, 100, sustain=2)
+    print("tiers EMA + LIR:", st)
+    assert any(r > 0 for _, r, _ in st["lir"]), "no revival in 100 steps of needle drift"
 
 
 def test_tiers_no_quantized_tier_and_large_capacity():

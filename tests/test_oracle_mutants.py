@@ -13,8 +13,8 @@ import sys
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PIN_FILES = ["test_oracle_pins.py", "test_oracle_scorers.py", "test_oracle_paged.py",
-             "test_oracle_memdecay.py", "test_oracle_qevict.py"]
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_scorers.py", "test_oracle_diagnostics.py",
+             "test_oracle_paged.py", "test_oracle_memdecay.py", "test_oracle_qevict.py"]
 
 # (oracle file, text, replacement, the mistake it models)
 MUTANTS = [
@@ -82,6 +82,19 @@ MUTANTS = [
     ("kvev_oracle.c", "    s *= lw;", ";", "entropy weight unused"),
     ("kvev_oracle.c", "if (L <= 1) return 1.0;", "if (L <= 1) return 0.0;",
      "a single token's entropy weight 0"),
+    # ranking diagnostics
+    ("diagnostics.py", "key=lambda i: (-raw[i], i)", "key=lambda i: (-raw[i], -i)",
+     "raw top-B ties to the higher slot"),
+    ("diagnostics.py", "key=lambda i: (-raw[i], i)", "key=lambda i: (raw[i], i)",
+     "raw top-B keeps the lowest scores"),
+    ("diagnostics.py", "len(a & b) / len(union)", "len(a & b) / max(len(a), 1)",
+     "Jaccard over one set's size"),
+    ("diagnostics.py", "held = set(int(p) for p in held_pos) | {int(new_pos)}",
+     "held = set(int(p) for p in held_pos)", "new token counted as missed"),
+    ("diagnostics.py", "if s >= self.sustain:", "if s > self.sustain:",
+     "revival needs a longer span"),
+    ("diagnostics.py", '"kept_and_prev_kept": len(E - {L - 1})', '"kept_and_prev_kept": len(E)',
+     "new token counted as previously kept"),
 ]
 MUTANTS += [
     # block-granular oracle
@@ -161,6 +174,7 @@ MUTANTS += [
     ("qevict.py", "m = P.alpha * s + (1.0 - P.alpha) * m", "m = (1.0 - P.alpha) * s + P.alpha * m",
      "window EMA weights swapped"),
     ("qevict.py", "tok = p.sum(axis=0) / Hq", "tok = p.sum(axis=0)", "head sum instead of mean"),
+    ("qevict.py", "            m = m + s\n", "            m = s\n", "cumulative score forgets"),
     ("qevict.py", "routed = t % P.omega == 0", "routed = t % P.omega == 1", "routing one step early"),
     ("qevict.py", "lg = (k64 @ q[heads].astype(np.float64).T).T / np.sqrt(d)",
      "lg = (k64 @ q[heads].astype(np.float64).T).T / d", "tier attention scale 1/d"),

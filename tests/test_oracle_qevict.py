@@ -123,6 +123,23 @@ def test_window_score_is_a_layer_sequential_ema_of_head_mean_mass():
     assert res["m"][1] == pytest.approx(want, rel=1e-12)
 
 
+def test_cumulative_window_score_sums_every_layer_and_step():
+    """Eq. (1) as the cumulative mode reads it: with uniform attention a
+    window's per-layer mass at a step over n cached tokens is W/n, so after
+    steps 1..3 (n = 69, 70, 71) over Ly layers its score is
+    Ly W (1/69 + 1/70 + 1/71): nothing decays."""
+    P = _params(n_layers=3, n_q_heads=2, n_kv_heads=1, alpha=0.2, omega=100, cumulative=True)
+    z = np.zeros((3, 1, 1 + 32 * 2 + 3, 32), np.uint16)
+    seq = QE.QSequence.from_prefill(P, z, z)
+    zq = np.zeros((3, 2, 32), np.uint16)
+    zk = np.zeros((3, 1, 32), np.uint16)
+    for t in (1, 2, 3):
+        res = QE.step(P, seq, t, zq, zk, zk)
+    want = 3 * 32 * (1 / 69 + 1 / 70 + 1 / 71)
+    assert res["m"][0] == pytest.approx(want, rel=1e-12)
+    assert res["m"][1] == pytest.approx(want, rel=1e-12)
+
+
 def _seq_with_scores(P, scores, tail=3):
     nw = len(scores)
     rng = np.random.default_rng(1)

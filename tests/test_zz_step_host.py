@@ -70,8 +70,8 @@ def test_bf16_output_is_the_rounded_fp32_output():
     """With KVEV_OUT_BF16 the step writes its fp32 result rounded to bf16
     (nearest even), bit for bit, through kvev_step and kvev_step_host alike
     (the host copy then moves half the bytes); everything else is unchanged.
-    The rounded output still meets the attention tolerance against the
-    oracle (checked through compare_step in the parity helpers)."""
+    Against the oracle the rounded output is within the attention tolerance
+    plus bf16's unit roundoff 2^-8 (rounding to 8 significant bits)."""
     import oracle as O
     from parity import compare_step, oracle_step
     wl = Workload(Geometry(2, 8, 2, 128, 2), 300, seed=23, heavy=3)
@@ -107,7 +107,9 @@ def test_bf16_output_is_the_rounded_fp32_output():
     assert torch.equal(b16.retained, f32.retained) and torch.equal(b16.score, f32.score)
     for b in range(g.batch):
         res, _ = oracle_step(P, pre[b], 1, True, q[b], kn[b], vn[b], wl.L0)
-        st = compare_step(res, b16, b, pre[b], budget)
-        assert st["out_rel"] <= 2e-3
+        compare_step(res, f32, b, pre[b], budget)          # the fp32 output, as every test
+        out = b16.out[b].float().cpu().numpy().astype(np.float64)
+        err = np.abs(out - res["out"]).max(-1) / np.abs(res["out"]).max(-1)
+        assert err.max() <= 2e-3 + 2.0 ** -8, f"bf16 output rel err {err.max():.3e}"
     for ep in (f32, b16, host):
         ep.close()
