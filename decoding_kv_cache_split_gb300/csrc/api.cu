@@ -68,6 +68,7 @@ struct Workspace {
     int32_t* pos_s = nullptr;
     float* msum_part = nullptr;
     uint32_t* status = nullptr;
+    uint32_t* gbar = nullptr;         // [2] grid barrier of the fused step (zero at rest)
     uint16_t* stg_q = nullptr;
     uint16_t* stg_k = nullptr;
     uint16_t* stg_v = nullptr;
@@ -163,6 +164,7 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
     w.pos_s = (int32_t*)take(ctx * 4, "pos_s");
     w.msum_part = (float*)take((size_t)L.batch * nblk * 4, "msum_part");
     w.status = (uint32_t*)take(4, "status");
+    w.gbar = (uint32_t*)take(8, "gbar");
     const size_t qn = (size_t)L.batch * L.n_layers * L.n_q_heads * L.head_dim;
     const size_t kn = (size_t)L.batch * L.n_layers * L.n_kv_heads * L.head_dim;
     w.stg_q = (uint16_t*)take(qn * 2, "stg_q");
@@ -313,6 +315,10 @@ struct kvev_ctx {
     bool begun = false;
     int device = 0, num_sms = 0;
     int attn_grid = 0, attn_warps = 0;
+    int fused_grid = 0;                 // CTAs of the fused refresh step (0: no such shape)
+    bool fused = false;                 // refresh steps run as one fused launch
+    int32_t test_skip_cta = -1;         // test-only barrier timeout injection
+    uint32_t test_bar_limit = 0;
     char* ws_base = nullptr;
     Workspace ws;
     float* dbg_probs = nullptr;
@@ -394,6 +400,8 @@ kvev_status check_status_word(kvev_ctx* c, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_fail(e, "device status");
     if (host != 0) {
         cudaMemsetAsync(c->ws.status, 0, 4, s);
+        // a barrier that gave up may have left arrivals behind
+        if (host & kStatusTimeout) cudaMemsetAsync(c->ws.gbar, 0, 8, s);
         cudaStreamSynchronize(s);
     }
     if (host & kStatusTimeout)
@@ -484,6 +492,9 @@ kvev_status kvev_create(const kvev_layout* layout, int64_t budget, int32_t granu
     }
     c->attn_grid = (int)attn_grid_for_device(c->num_sms, *layout);
     c->attn_warps = c->attn_grid * attn_warps_per_cta();
+    if (layout->page_tokens == 1)
+        c->fused_grid = c->num_sms * attn_fused_ctas_per_sm(layout->head_dim, c->group,
+                                                            layout->n_kv_heads);
     c->int2_grid = (int)int2_grid_for_device(c->num_sms, *layout);
     c->int2_warps = c->int2_grid * int2_warps_per_cta();
     const int64_t rows = (int64_t)layout->n_layers * layout->batch * layout->n_kv_heads;
@@ -627,6 +638,15 @@ kvev_status kvev_set_scorer(kvev_ctx* c, int32_t aggregation, int32_t weighting)
     return KVEV_OK;
 }
 
+kvev_status kvev_set_fused_step(kvev_ctx* c, int32_t on) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (on && c->fused_grid <= 0)
+        return fail(KVEV_EUNSUPPORTED, "no fused step for this layout (token granularity; "
+                    "head_dim 64/128; 4 or 8 query heads per KV head; 1, 2 or 8 KV heads)");
+    c->fused = on != 0;
+    return KVEV_OK;
+}
+
 kvev_status kvev_set_output(kvev_ctx* c, int32_t out_type) {
     if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
     if (out_type != KVEV_OUT_F32 && out_type != KVEV_OUT_BF16)
@@ -761,12 +781,18 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     const int64_t rows_per_layer = (int64_t)Ly.batch * Ly.n_kv_heads;
     at.row0 = 0;
     at.n_tiles_total = (int64_t)Ly.n_layers * rows_per_layer * tiles_per_row;
+    // the fused step: refresh steps without the weightings' statistics
+    const bool fused = c->fused && refresh && stats == 0 && c->fused_grid > 0;
     int attn_grid = 0;
-    at.total_warps = attn_launch_warps(c->attn_warps, at.n_tiles_total, &attn_grid);
-    rc = timed_launch(c, kProfAttn, s, "attention", [&] {
-        return launch_attention(at, Ly.head_dim, G, attn_grid, s, stats);
-    });
-    if (rc != KVEV_OK) return rc;
+    at.total_warps = attn_launch_warps(fused ? c->fused_grid * attn_warps_per_cta()
+                                             : c->attn_warps,
+                                       at.n_tiles_total, &attn_grid);
+    if (!fused) {
+        rc = timed_launch(c, kProfAttn, s, "attention", [&] {
+            return launch_attention(at, Ly.head_dim, G, attn_grid, s, stats);
+        });
+        if (rc != KVEV_OK) return rc;
+    }
     CombineArgs cb{};   // merge the split: outputs and per-head log2-sum-exp
     cb.part_e = at.part_e;
     cb.ent = at.part_e ? c->ws.ent : nullptr;
@@ -787,13 +813,27 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     cb.batch = Ly.batch;
     cb.n_kv = Ly.n_kv_heads;
     cb.n_q = Ly.n_q_heads;
-    rc = timed_launch(c, kProfCombine, s, "combine",
-                      [&] { return launch_combine(cb, Ly.head_dim, G, s); });
-    if (rc != KVEV_OK) return rc;
     int n_part = 0;
-    rc = timed_launch(c, kProfScore, s, "score",
-                      [&] { return launch_score(sc, G, &n_part, s); });
-    if (rc != KVEV_OK) return rc;
+    if (fused) {   // attention, combine and scoring in one cooperative launch
+        FusedArgs fa{};
+        fa.bar = c->ws.gbar;
+        fa.wait_limit = c->test_bar_limit;
+        fa.skip_cta_p1 = c->test_skip_cta + 1;
+        c->test_skip_cta = -1;
+        c->test_bar_limit = 0;
+        n_part = (L + 31) / 32;   // (not read on refresh steps)
+        rc = timed_launch(c, kProfAttn, s, "fused step", [&] {
+            return launch_attn_fused(at, cb, sc, fa, Ly.head_dim, G, c->fused_grid, s);
+        });
+        if (rc != KVEV_OK) return rc;
+    } else {
+        rc = timed_launch(c, kProfCombine, s, "combine",
+                          [&] { return launch_combine(cb, Ly.head_dim, G, s); });
+        if (rc != KVEV_OK) return rc;
+        rc = timed_launch(c, kProfScore, s, "score",
+                          [&] { return launch_score(sc, G, &n_part, s); });
+        if (rc != KVEV_OK) return rc;
+    }
 
     SelectArgs se{};
     se.keys = c->ws.keys;
@@ -1701,6 +1741,14 @@ kvev_status kvev_test_wait_timeout(kvev_ctx* c, int64_t tile, uint32_t wait_limi
     if (tile < 0 || wait_limit == 0) return fail(KVEV_EINVAL, "tile >= 0 and wait_limit >= 1");
     c->test_fault_tile = tile;
     c->test_wait_limit = wait_limit;
+    return KVEV_OK;
+}
+
+kvev_status kvev_test_barrier_timeout(kvev_ctx* c, int32_t cta, uint32_t wait_limit) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (cta < 0 || wait_limit == 0) return fail(KVEV_EINVAL, "cta >= 0 and wait_limit >= 1");
+    c->test_skip_cta = cta;
+    c->test_bar_limit = wait_limit;
     return KVEV_OK;
 }
 

@@ -40,6 +40,7 @@
 
 #include "kvev_internal.h"
 #include "mma_ops.h"
+#include "score_refresh.cuh"
 
 namespace kvev {
 namespace {
@@ -139,18 +140,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// One warp's share of an attention launch (the kernel below, and the first
+// phase of the fused step).  `smem` is the CTA's 1024-byte aligned dynamic
+// shared memory.  Returns false when a bounded wait gave up (the status word
+// is flagged and the warp's split slots poisoned).
 template <int D, int G, int STAGES, int WARPS, bool PAGED, int ST>
-__global__ void __launch_bounds__(WARPS * 32)
-    attn_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                    const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a) {
+__device__ __forceinline__ bool attn_warp(const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                          const AttnArgs& a, unsigned char* smem) {
     using C = MmaCfg<D, G, STAGES, WARPS>;
     constexpr int T = C::T, NB = C::NB, KS = C::KS;
-
-    extern __shared__ unsigned char smem_raw[];
-    griddep_wait();
-    griddep_release();
-    // 128-byte swizzled boxes want 1024-byte aligned destinations
-    unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned char* wbuf = smem + (size_t)warp * STAGES * C::STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)WARPS * STAGES * C::STAGE_BYTES) +
@@ -162,11 +160,11 @@ __global__ void __launch_bounds__(WARPS * 32)
     int* stage_pos = stage_nv + WARPS * STAGES;   // first token position of the tile (block mode)
 
     const int w = blockIdx.x * WARPS + warp;
-    if (w >= a.total_warps) return;   // the launch's last CTA may hold spare warps
+    if (w >= a.total_warps) return true;   // the launch's last CTA may hold spare warps
     const int64_t N = a.n_tiles_total;
     const int64_t x0 = (int64_t)w * N / a.total_warps;
     const int64_t x1 = (int64_t)(w + 1) * N / a.total_warps;
-    if (x0 >= x1) return;
+    if (x0 >= x1) return true;
 
     if (lane == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
@@ -231,8 +229,8 @@ __global__ void __launch_bounds__(WARPS * 32)
         if (row * tpr + tile + 1 == a.fault_tile_p1) return;
 #pragma unroll
         for (int bx = 0; bx < C::BOXES; ++bx) {
-            tma_load_2d(dst + bx * C::BOX_BYTES, &tmap_k, bx * 64, y, &bars[stage], pol);
-            tma_load_2d(dst + C::TILE_BYTES + bx * C::BOX_BYTES, &tmap_v, bx * 64, y,
+            tma_load_2d(dst + bx * C::BOX_BYTES, tmap_k, bx * 64, y, &bars[stage], pol);
+            tma_load_2d(dst + C::TILE_BYTES + bx * C::BOX_BYTES, tmap_v, bx * 64, y,
                         &bars[stage], pol);
         }
     };
@@ -485,9 +483,22 @@ __global__ void __launch_bounds__(WARPS * 32)
             if (x0 + it2 < x1 && x0 + it2 + 1 != a.fault_tile_p1)
                 mbar_wait(&bars[it2 % STAGES], (uint32_t)((it2 / STAGES) & 1), kWaitLimit);
         }
-        return;
+        return false;
     }
     flush(cur_row);
+    return true;
+}
+
+template <int D, int G, int STAGES, int WARPS, bool PAGED, int ST>
+__global__ void __launch_bounds__(WARPS * 32)
+    attn_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    griddep_wait();
+    griddep_release();
+    // 128-byte swizzled boxes want 1024-byte aligned destinations
+    unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+    attn_warp<D, G, STAGES, WARPS, PAGED, ST>(&tmap_k, &tmap_v, a, smem);
 }
 
 // Split combine: one warp per row of the launch (up to 8 rows per CTA); lane l
@@ -498,16 +509,12 @@ __global__ void __launch_bounds__(WARPS * 32)
 // many warps).
 constexpr int kCombineWarps = 8;
 
+// Merge launch row r (one warp, lane = this thread's lane).
 template <int D, int G, int KB>
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs a) {
+__device__ __forceinline__ void combine_row(const CombineArgs& a, int64_t r, int lane) {
     constexpr int V = D / 32;   // dims per lane
     static_assert(V == 2 || V == 4, "head_dim 64 or 128");
     using VecT = typename std::conditional<V == 4, float4, float2>::type;
-    griddep_wait();
-    griddep_release();
-    const int lane = threadIdx.x & 31;
-    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);   // row of the launch
-    if (r >= a.n_rows) return;
     float M[G], Ls[G], acc[G][V];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -639,6 +646,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     }
 }
 
+template <int D, int G, int KB>
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineArgs a) {
+    griddep_wait();
+    griddep_release();
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);   // row of the launch
+    if (r >= a.n_rows) return;
+    combine_row<D, G, KB>(a, r, lane);
+}
+
 
 #ifndef KVEV_ATTN_STAGES
 #define KVEV_ATTN_STAGES 2
@@ -648,6 +665,101 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
 #endif
 constexpr int kStages = KVEV_ATTN_STAGES;   // tiles in flight per warp
 constexpr int kWarps = KVEV_ATTN_WARPS;     // warps per CTA
+
+// ---------------------------------------------------------------------------
+// The fused refresh step: one cooperative launch of the attention grid does
+// the attention (phase A), then, behind a grid barrier, the split combine of
+// every row (phase B: one warp per row), then, behind a second barrier, the
+// scoring of every token block (phase C: the scorer's 128-thread body per
+// 32 tokens, in the CTA's shared memory that the attention stages no longer
+// use).  The work and its arithmetic are those of the three kernels it
+// replaces, in the same order, so the results are the same bit for bit when
+// the attention is split the same way; what goes is two kernel boundaries
+// (their drain and launch) per step.
+//
+// Grid barrier: a count and a generation word in global memory.  Thread 0 of
+// each CTA publishes its CTA's writes (fence), reads the generation and
+// arrives; the last arrival zeroes the count and bumps the generation, the
+// others spin on it with a bounded number of iterations (then they flag the
+// status word and their CTA leaves).  The cooperative launch guarantees every
+// CTA is resident, so the wait ends; the count is back to zero after every
+// barrier, so the next barrier (and the next launch, graph replays included)
+// starts from a clean state.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ bool grid_barrier(const FusedArgs& f, uint32_t* status) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        bool ok = true;
+        const uint32_t gen = ld_acquire_gpu(f.bar + 1);
+        __threadfence();   // this CTA's writes before its arrival
+        if (f.skip_cta_p1 == (int)blockIdx.x + 1) {
+            ok = false;   // test-only: this CTA never arrives
+        } else if (atomicAdd(f.bar, 1u) == gridDim.x - 1) {
+            f.bar[0] = 0;                 // reset for the next barrier
+            __threadfence();
+            atomicAdd(f.bar + 1, 1u);     // release the others
+        } else {
+            const uint32_t limit = f.wait_limit ? f.wait_limit : kWaitLimit;
+            uint32_t i = 0;
+            while (ld_acquire_gpu(f.bar + 1) == gen) {
+                if (++i >= limit) {
+                    ok = false;
+                    atomicOr(status, kStatusTimeout);
+                    break;
+                }
+            }
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+template <int D, int G, int NKV>
+__global__ void __launch_bounds__(kWarps * 32)
+    attn_fused_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a,
+                      const CombineArgs cb, const ScoreArgs sc, const FusedArgs f) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+    __shared__ float s_c[kRefreshSegs][32], s_tot[kRefreshSegs][32];
+    static_assert(kWarps * 32 == kRefreshThreads, "one CTA is one scorer block");
+    // phase A: attention, logits kept, split partials
+    attn_warp<D, G, kStages, kWarps, false, 0>(&tmap_k, &tmap_v, a, smem);
+    if (!grid_barrier(f, a.status)) return;
+    // phase B: merge every row's split (output, per-head log2-sum-exp)
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const bool many = 1.0 + (double)cb.sp.total_warps / (cb.n_rows > 0 ? cb.n_rows : 1) >= 3.0;
+    for (int64_t r = gw; r < cb.n_rows; r += nw) {
+        if (many)
+            combine_row<D, G, (G <= 4 ? 4 : 2)>(cb, r, lane);
+        else
+            combine_row<D, G, 1>(cb, r, lane);
+    }
+    if (!grid_barrier(f, a.status)) return;
+    // phase C: score every token block (the stage buffers hold the tables)
+    float* tab = reinterpret_cast<float*>(smem);
+    const int nblk = (sc.L + 31) / 32;
+    for (int b = 0; b < sc.batch; ++b) {
+        __syncthreads();   // the previous tables and chain are done
+        score_tables<G, NKV, false>(sc, b, tab);
+        for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+            __syncthreads();
+            score_block<G, NKV, false>(sc, b, blk, tab, s_c, s_tot);
+        }
+    }
+    griddep_release();
+}
+
 
 // 2-D view of one cache buffer: rows x max_ctx tokens of D bf16; boxes of
 // 16 tokens x 64 dims with the 128-byte swizzle.
@@ -765,11 +877,77 @@ cudaError_t launch_combine_t(const CombineArgs& a, cudaStream_t s) {
     return launch_pdl(combine_kernel<D, G, (G <= 4 ? 4 : 2)>, dim3(a.n_rows), dim3(32), 0, s, a);
 }
 
+template <int D, int G, int NKV>
+int fused_ctas_per_sm_t() {
+    using C = MmaCfg<D, G, kStages, kWarps>;
+    auto kern = attn_fused_kernel<D, G, NKV>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) !=
+        cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, C::SMEM) !=
+        cudaSuccess)
+        return 0;
+    return n;
+}
+
+template <int D, int G, int NKV>
+cudaError_t launch_fused_t(const AttnArgs& a, const CombineArgs& cb, const ScoreArgs& sc,
+                           const FusedArgs& f, int grid, cudaStream_t s) {
+    using C = MmaCfg<D, G, kStages, kWarps>;
+    auto kern = attn_fused_kernel<D, G, NKV>;
+    // the scorer's tables live in the stage buffers once the attention is done
+    if ((size_t)sc.n_layers * (sc.n_q + 1 + sc.n_kv) * sizeof(float) >
+        (size_t)kWarps * kStages * C::STAGE_BYTES)
+        return cudaErrorInvalidValue;
+    CUtensorMap mk, mv;
+    if (!encode_cache_map(&mk, a.k, a.view_tokens, D) || !encode_cache_map(&mv, a.v, a.view_tokens, D))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: the barriers end
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mk, mv, a, cb, sc, f);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t launch_combine(const CombineArgs& a, int head_dim, int group, cudaStream_t s) {
     if (group == 4 && head_dim == 128) return launch_combine_t<128, 4>(a, s);
     if (group == 4 && head_dim == 64) return launch_combine_t<64, 4>(a, s);
     if (group == 8 && head_dim == 128) return launch_combine_t<128, 8>(a, s);
     if (group == 8 && head_dim == 64) return launch_combine_t<64, 8>(a, s);
+    return cudaErrorInvalidValue;
+}
+
+// Shapes with a fused step: head_dim 128 and 64, 4 or 8 query heads per KV
+// head, and the KV-head counts of the workloads (8, 2, 1).
+#define KVEV_FUSED_SHAPES(X) \
+    X(128, 4, 8) X(128, 4, 2) X(128, 4, 1) X(64, 4, 2) X(128, 8, 2) X(64, 8, 2)
+
+int attn_fused_ctas_per_sm(int head_dim, int group, int n_kv) {
+#define KVEV_FUSED_OCC(D, G, N) \
+    if (head_dim == D && group == G && n_kv == N) return fused_ctas_per_sm_t<D, G, N>();
+    KVEV_FUSED_SHAPES(KVEV_FUSED_OCC)
+#undef KVEV_FUSED_OCC
+    return 0;
+}
+
+cudaError_t launch_attn_fused(const AttnArgs& a, const CombineArgs& cb, const ScoreArgs& sc,
+                              const FusedArgs& f, int head_dim, int group, int grid,
+                              cudaStream_t s) {
+#define KVEV_FUSED_LAUNCH(D, G, N) \
+    if (head_dim == D && group == G && sc.n_kv == N) return launch_fused_t<D, G, N>(a, cb, sc, f, grid, s);
+    KVEV_FUSED_SHAPES(KVEV_FUSED_LAUNCH)
+#undef KVEV_FUSED_LAUNCH
     return cudaErrorInvalidValue;
 }
 

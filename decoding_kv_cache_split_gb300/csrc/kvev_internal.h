@@ -71,6 +71,14 @@ struct AttnArgs {
     float* part_vn;
 };
 
+// The fused refresh step (attention, split combine and scoring in one
+// cooperative launch, phases separated by grid barriers).
+struct FusedArgs {
+    uint32_t* bar;          // [2] grid barrier: arrivals, generation (zero at rest)
+    uint32_t wait_limit;    // bounded barrier wait (0: kWaitLimit)
+    int32_t skip_cta_p1;    // test-only: 1 + a CTA that leaves without arriving (0: none)
+};
+
 // Attention statistics the scorer's weightings need (template flags of the
 // attention kernel; 0 = the plain kernel).
 enum : int { kStatEntropy = 1, kStatVNorm = 2 };
@@ -426,6 +434,11 @@ size_t attn_smem_bytes(int head_dim, int group);
 cudaError_t launch_attention(const AttnArgs& a, int head_dim, int group, int grid,
                              cudaStream_t s, int stats = 0);
 cudaError_t launch_combine(const CombineArgs& a, int head_dim, int group, cudaStream_t s);
+// 0 when the shape has no fused step
+int attn_fused_ctas_per_sm(int head_dim, int group, int n_kv);
+cudaError_t launch_attn_fused(const AttnArgs& a, const CombineArgs& cb, const ScoreArgs& sc,
+                              const FusedArgs& f, int head_dim, int group, int grid,
+                              cudaStream_t s);
 cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, int batch, int num_sms, cudaStream_t s);
 cudaError_t launch_diag(const DiagArgs& a, int batch, cudaStream_t s);

@@ -43,6 +43,7 @@ PROFILE_NAMES = ["append", "attention", "combine", "score", "select", "compact",
 # every entry point declared in include/kvev.h
 EXPORTS = ["kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_size",
            "kvev_refresh_mode", "kvev_configure", "kvev_set_output", "kvev_set_scorer",
+           "kvev_set_fused_step", "kvev_test_barrier_timeout",
            "kvev_begin",
            "kvev_length",
            "kvev_init_state", "kvev_step", "kvev_step_host", "kvev_set_debug",
@@ -155,6 +156,8 @@ def lib():
             "kvev_configure": ([P, I32, I32], I32),
             "kvev_set_output": ([P, I32], I32),
             "kvev_set_scorer": ([P, I32, I32], I32),
+            "kvev_set_fused_step": ([P, I32], I32),
+            "kvev_test_barrier_timeout": ([P, I32, ctypes.c_uint32], I32),
             "kvev_begin": ([P, I32], I32),
             "kvev_length": ([P, P], I32),
             "kvev_init_state": ([P, P, P], I32),
@@ -252,6 +255,15 @@ def kvev_set_output(ctx, out_type: int) -> None:
 
 def kvev_set_scorer(ctx, aggregation: int, weighting: int = 0) -> None:
     _check(lib().kvev_set_scorer(ctx, int(aggregation), int(weighting)), ctx)
+
+
+def kvev_set_fused_step(ctx, on: bool) -> None:
+    _check(lib().kvev_set_fused_step(ctx, int(bool(on))), ctx)
+
+
+def kvev_test_barrier_timeout(ctx, cta: int, wait_limit: int) -> None:
+    """Test-only barrier timeout injection for the next fused step."""
+    _check(lib().kvev_test_barrier_timeout(ctx, int(cta), int(wait_limit)), ctx)
 
 
 def kvev_begin(ctx, prefill_len: int) -> None:
@@ -400,7 +412,7 @@ class EvictionPass:
     def __init__(self, n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, budget,
                  alpha, beta, *, age_mode=KVEV_AGE_SINCE_INSERT, pool=KVEV_POOL_SUM,
                  refresh=KVEV_REFRESH_FULL, period=1, out_type=KVEV_OUT_F32,
-                 aggregation=KVEV_AGG_EMA, weighting=0, device="cuda"):
+                 aggregation=KVEV_AGG_EMA, weighting=0, fused=False, device="cuda"):
         import torch
         self.torch = torch
         self.layout = kvev_layout(n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, 1,
@@ -411,6 +423,8 @@ class EvictionPass:
         kvev_refresh_mode(self.ctx, refresh, period)
         kvev_set_output(self.ctx, out_type)
         kvev_set_scorer(self.ctx, aggregation, weighting)
+        if fused:
+            kvev_set_fused_step(self.ctx, True)
         shape = (n_layers, batch, n_kv_heads, max_ctx, head_dim)
         self.k = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]
         self.v = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]

@@ -216,6 +216,20 @@ kvev_status kvev_set_output(kvev_ctx* ctx, int32_t out_type);
  * tiles it already holds, the entropy from its softmax sums), so neither
  * reads the cache again.  Block-granular and two-tier contexts take only
  * the defaults (KVEV_EUNSUPPORTED otherwise). */
+/* Fused refresh step (token granularity; on != 0 turns it on, from the next
+ * step): on refresh steps without a weighting, the attention, the split
+ * combine and the scoring run as ONE cooperative launch, their phases
+ * separated by grid barriers, instead of three launches.  The arithmetic is
+ * the three kernels' own, in the same order; the outputs are the same bit
+ * for bit whenever the attention splits its tiles over the same number of
+ * warps (the same CTAs per SM).  Every barrier wait is bounded: one that
+ * gives up reports KVEV_ETIMEOUT at the next kvev_sync.  No counterpart on
+ * the pages (their implementation reads the attention weights through a
+ * separate eager pass: "What Matters...", Appendix J).  KVEV_EUNSUPPORTED for
+ * shapes without a fused kernel (head_dim 64 or 128, 4 or 8 query heads per
+ * KV head, 1, 2 or 8 KV heads are built). */
+kvev_status kvev_set_fused_step(kvev_ctx* ctx, int32_t on);
+
 typedef enum { KVEV_AGG_EMA = 0, KVEV_AGG_CUMULATIVE = 1 } kvev_aggregation;
 enum { KVEV_W_VNORM = 1, KVEV_W_ENTROPY = 2 };
 kvev_status kvev_set_scorer(kvev_ctx* ctx, int32_t aggregation, int32_t weighting);
@@ -333,6 +347,14 @@ kvev_status kvev_launch_count(const kvev_ctx* ctx, int64_t* launches);
  * kvev_step_host) returns KVEV_ETIMEOUT and the context stays usable (the
  * step's outputs are undefined).  No counterpart on the pages. */
 kvev_status kvev_test_wait_timeout(kvev_ctx* ctx, int64_t tile, uint32_t wait_limit);
+
+/* Test-only failure injection for the fused step: in the next fused step CTA
+ * `cta` leaves without arriving at the first grid barrier and every barrier
+ * wait gives up after `wait_limit` iterations, so the other CTAs stop waiting,
+ * flag the status word and leave; kvev_sync then returns KVEV_ETIMEOUT, the
+ * barrier state is reset and the context stays usable (the step's outputs are
+ * undefined).  No counterpart on the pages. */
+kvev_status kvev_test_barrier_timeout(kvev_ctx* ctx, int32_t cta, uint32_t wait_limit);
 
 /* Debugging aid: every region of the context's scratch is followed by a
  * 256-byte guard band filled at create; this call reads the bands back

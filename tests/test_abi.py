@@ -97,6 +97,8 @@ NULL_CTX_CALLS = {
     "kvev_set_output": lambda L: L.kvev_set_output(None, 1),
     "kvev_set_scorer": lambda L: L.kvev_set_scorer(None, 1, 0),
     "kvev_set_diagnostics": lambda L: L.kvev_set_diagnostics(None, None, None),
+    "kvev_set_fused_step": lambda L: L.kvev_set_fused_step(None, 1),
+    "kvev_test_barrier_timeout": lambda L: L.kvev_test_barrier_timeout(None, 0, 10),
     "kvev_profile": lambda L: L.kvev_profile(None, 1),
     "kvev_profile_read": lambda L: L.kvev_profile_read(None, None, None),
     "kvev_launch_count": lambda L: L.kvev_launch_count(None, _out()),

@@ -35,7 +35,7 @@ REFRESH = {"full": (O.REFRESH_FULL, kvev.KVEV_REFRESH_FULL),
 def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int, *,
                age_mode=O.AGE_SINCE_INSERT, refresh="full", period=8, pool_mean=False,
                max_ctx=None, check_every=1, aggregation=O.AGG_EMA, weighting=0,
-               m_atol=None, diagnostics=False):
+               m_atol=None, diagnostics=False, fused=False):
     """`diagnostics`: the ranking counters and raw scores are gathered on
     the device every step and checked (check_diagnostics)."""
     g = wl.geom
@@ -48,7 +48,8 @@ def run_parity(wl: Workload, budget: int, alpha: float, beta: float, steps: int,
                            aggregation={O.AGG_EMA: kvev.KVEV_AGG_EMA,
                                         O.AGG_CUMULATIVE: kvev.KVEV_AGG_CUMULATIVE}[aggregation],
                            weighting=((kvev.KVEV_W_VNORM if weighting & O.W_VNORM else 0) |
-                                      (kvev.KVEV_W_ENTROPY if weighting & O.W_ENTROPY else 0)))
+                                      (kvev.KVEV_W_ENTROPY if weighting & O.W_ENTROPY else 0)),
+                           fused=fused)
     load_prefill(ep, wl)
     ep.begin(wl.L0)
     probs = torch.zeros((g.batch, g.n_layers, g.n_q_heads, max_ctx), dtype=torch.float32,
