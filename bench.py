@@ -343,6 +343,37 @@ def replay_mode(fh, ctx, ep, step_in, step_ms, alpha, name, period, L0, B, row, 
     return step_bytes, kernels
 
 
+def fused_mode_run(ctx, ep, step_in, L0, k0, v0, stream, mode=None):
+    """The refresh-mode run again with a fused refresh step (`mode`, default
+    all three phases): step 1 and the mean of steps 2.. in us (CUDA events
+    between steps)."""
+    import torch
+    from decoding_kv_cache_split_gb300 import kvev
+    try:
+        kvev.kvev_set_fused_step(ctx, kvev.KVEV_FUSED_ALL if mode is None else mode)
+    except kvev.KvevError as err:
+        return {"unavailable": str(err)}
+    ep.k[0].copy_(k0)
+    ep.v[0].copy_(v0)
+    ep.cache.cur = 0
+    kvev.kvev_begin(ctx, L0)
+    kvev.kvev_init_state(ctx, ep.state, stream)
+    n = len(step_in)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for t in range(1, n + 1):
+        kvev.kvev_step(ctx, *step_in[t - 1], ep.cache, ep.state, t, ep.out, ep.retained,
+                       ep.n_retained, stream)
+        evs[t].record(stream)
+    torch.cuda.synchronize()
+    kvev.kvev_sync(ctx)
+    kvev.kvev_set_fused_step(ctx, kvev.KVEV_FUSED_OFF)
+    st = [evs[t - 1].elapsed_time(evs[t]) for t in range(1, n + 1)]
+    return {"step1_us": round(st[0] * 1e3, 1),
+            "steady_us": round(sum(st[1:]) / max(1, n - 1) * 1e3, 1)}
+
+
 def diagnostics_run(fh, ctx, ep, step_in, L0, k0, v0, stream, alpha, name):
     """One more replay of a refresh-mode run with the device's ranking
     diagnostics on (kvev_set_diagnostics): per scoring step the raw top-B set
@@ -564,6 +595,36 @@ def main():
         assert torch.equal(ep.out, ref_out), "graph replay differs from the eager step"
         del g
 
+    # The same pass with the fused refresh step (attention, combine and scoring
+    # in one cooperative launch), timed the same way; its output is compared
+    # with the three-launch pass's.
+    fused = {}
+    for fname, fmode in (("all", kvev.KVEV_FUSED_ALL),
+                         ("attn_combine", kvev.KVEV_FUSED_ATTN_COMBINE)):
+        try:
+            kvev.kvev_set_fused_step(ep.ctx, fmode)
+            ref_out = ep.out.clone()
+            for _ in range(args.warmup):
+                one_step()
+            torch.cuda.synchronize()
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            for _ in range(args.steps):
+                one_step()
+            f1.record(stream)
+            torch.cuda.synchronize()
+            kvev.kvev_sync(ep.ctx)
+            fus_ms = f0.elapsed_time(f1) / args.steps
+            fused[fname] = {
+                "us_per_step": round(fus_ms * 1e3, 2),
+                "GBps": round(kv_bytes(W["n_layers"], W["n_kv_heads"], W["head_dim"], L0 + 1,
+                                       B)[0] / (fus_ms * 1e-3) / 1e9, 2),
+                "same_output_bits": bool(torch.equal(ep.out, ref_out))}
+        except kvev.KvevError as err:
+            fused[fname] = {"unavailable": str(err)}
+        finally:
+            kvev.kvev_set_fused_step(ep.ctx, kvev.KVEV_FUSED_OFF)
+
     # Per-kernel region: CUDA events around every launch, on the launching stream.
     kvev.kvev_profile(ep.ctx, True)
     kvev.kvev_profile_read(ep.ctx)          # reset accumulators
@@ -657,6 +718,12 @@ def main():
                 if alpha == 0.05 and not args.no_graph:
                     rec["steady_graph_us"] = steady_graph_us(ctx, ep, step_in, L0, k0, v0,
                                                              stream, args.warmup)
+                if alpha == 0.05:   # the same run with the fused refresh steps
+                    rec["fused"] = {
+                        "all": fused_mode_run(ctx, ep, step_in, L0, k0, v0, stream,
+                                              kvev.KVEV_FUSED_ALL),
+                        "attn_combine": fused_mode_run(ctx, ep, step_in, L0, k0, v0, stream,
+                                                       kvev.KVEV_FUSED_ATTN_COMBINE)}
                 if name != "frozen":   # Score-Free scores once: no ranking to trace
                     rec["diagnostics"] = diagnostics_run(step_log, ctx, ep, step_in, L0, k0,
                                                          v0, stream, alpha, name)
@@ -716,6 +783,7 @@ def main():
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "output": "bf16",
                     "call": "kvev_step_host"},
             "graph": ({"us_per_step": round(graph_us, 2), "replays": args.steps} if graph_us else None),
+            "fused_step": fused,
             "gpu_launches": launches,
             "clocks": clk,
             "cpu_baseline": cpu,

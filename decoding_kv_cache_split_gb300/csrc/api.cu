@@ -316,7 +316,7 @@ struct kvev_ctx {
     int device = 0, num_sms = 0;
     int attn_grid = 0, attn_warps = 0;
     int fused_grid = 0;                 // CTAs of the fused refresh step (0: no such shape)
-    bool fused = false;                 // refresh steps run as one fused launch
+    int32_t fused = 0;                  // KVEV_FUSED_* of refresh steps
     int32_t test_skip_cta = -1;         // test-only barrier timeout injection
     uint32_t test_bar_limit = 0;
     char* ws_base = nullptr;
@@ -405,7 +405,8 @@ kvev_status check_status_word(kvev_ctx* c, cudaStream_t s) {
         cudaStreamSynchronize(s);
     }
     if (host & kStatusTimeout)
-        return fail(KVEV_ETIMEOUT, "a device wait exceeded its iteration limit");
+        return fail(KVEV_ETIMEOUT, "a device wait exceeded its iteration limit%s",
+                    (host & kStatusBarrier) ? " (a grid barrier of the fused step)" : "");
     if (host & kStatusNoPage)
         return fail(KVEV_ESTATE, "a sequence had no free page for a new or re-admitted block");
     return KVEV_OK;
@@ -492,9 +493,14 @@ kvev_status kvev_create(const kvev_layout* layout, int64_t budget, int32_t granu
     }
     c->attn_grid = (int)attn_grid_for_device(c->num_sms, *layout);
     c->attn_warps = c->attn_grid * attn_warps_per_cta();
-    if (layout->page_tokens == 1)
-        c->fused_grid = c->num_sms * attn_fused_ctas_per_sm(layout->head_dim, c->group,
-                                                            layout->n_kv_heads);
+    if (layout->page_tokens == 1) {
+        // at most the attention kernel's grid: the split partial slots are
+        // sized for its warps, and with the same CTAs the two paths split the
+        // tiles alike (the same outputs bit for bit)
+        const int fg = c->num_sms * attn_fused_ctas_per_sm(layout->head_dim, c->group,
+                                                           layout->n_kv_heads);
+        c->fused_grid = fg < c->attn_grid ? fg : c->attn_grid;
+    }
     c->int2_grid = (int)int2_grid_for_device(c->num_sms, *layout);
     c->int2_warps = c->int2_grid * int2_warps_per_cta();
     const int64_t rows = (int64_t)layout->n_layers * layout->batch * layout->n_kv_heads;
@@ -638,12 +644,14 @@ kvev_status kvev_set_scorer(kvev_ctx* c, int32_t aggregation, int32_t weighting)
     return KVEV_OK;
 }
 
-kvev_status kvev_set_fused_step(kvev_ctx* c, int32_t on) {
+kvev_status kvev_set_fused_step(kvev_ctx* c, int32_t mode) {
     if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
-    if (on && c->fused_grid <= 0)
+    if (mode != KVEV_FUSED_OFF && mode != KVEV_FUSED_ALL && mode != KVEV_FUSED_ATTN_COMBINE)
+        return fail(KVEV_EINVAL, "unknown fused-step mode %d", mode);
+    if (mode != KVEV_FUSED_OFF && c->fused_grid <= 0)
         return fail(KVEV_EUNSUPPORTED, "no fused step for this layout (token granularity; "
                     "head_dim 64/128; 4 or 8 query heads per KV head; 1, 2 or 8 KV heads)");
-    c->fused = on != 0;
+    c->fused = mode;
     return KVEV_OK;
 }
 
@@ -819,6 +827,7 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
         fa.bar = c->ws.gbar;
         fa.wait_limit = c->test_bar_limit;
         fa.skip_cta_p1 = c->test_skip_cta + 1;
+        fa.score = c->fused == KVEV_FUSED_ALL ? 1 : 0;
         c->test_skip_cta = -1;
         c->test_bar_limit = 0;
         n_part = (L + 31) / 32;   // (not read on refresh steps)
@@ -826,6 +835,11 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
             return launch_attn_fused(at, cb, sc, fa, Ly.head_dim, G, c->fused_grid, s);
         });
         if (rc != KVEV_OK) return rc;
+        if (!fa.score) {
+            rc = timed_launch(c, kProfScore, s, "score",
+                              [&] { return launch_score(sc, G, &n_part, s); });
+            if (rc != KVEV_OK) return rc;
+        }
     } else {
         rc = timed_launch(c, kProfCombine, s, "combine",
                           [&] { return launch_combine(cb, Ly.head_dim, G, s); });

@@ -489,8 +489,11 @@ __device__ __forceinline__ bool attn_warp(const CUtensorMap* tmap_k, const CUten
     return true;
 }
 
+#ifndef KVEV_ATTN_MIN_CTAS
+#define KVEV_ATTN_MIN_CTAS 1
+#endif
 template <int D, int G, int STAGES, int WARPS, bool PAGED, int ST>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, KVEV_ATTN_MIN_CTAS)
     attn_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const AttnArgs a) {
     extern __shared__ unsigned char smem_raw[];
@@ -710,7 +713,7 @@ __device__ __forceinline__ bool grid_barrier(const FusedArgs& f, uint32_t* statu
             while (ld_acquire_gpu(f.bar + 1) == gen) {
                 if (++i >= limit) {
                     ok = false;
-                    atomicOr(status, kStatusTimeout);
+                    atomicOr(status, kStatusTimeout | kStatusBarrier);
                     break;
                 }
             }
@@ -744,6 +747,10 @@ __global__ void __launch_bounds__(kWarps * 32)
             combine_row<D, G, (G <= 4 ? 4 : 2)>(cb, r, lane);
         else
             combine_row<D, G, 1>(cb, r, lane);
+    }
+    if (!f.score) {   // the scorer runs as its own launch after this one
+        griddep_release();
+        return;
     }
     if (!grid_barrier(f, a.status)) return;
     // phase C: score every token block (the stage buffers hold the tables)

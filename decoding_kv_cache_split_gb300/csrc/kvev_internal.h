@@ -77,6 +77,7 @@ struct FusedArgs {
     uint32_t* bar;          // [2] grid barrier: arrivals, generation (zero at rest)
     uint32_t wait_limit;    // bounded barrier wait (0: kWaitLimit)
     int32_t skip_cta_p1;    // test-only: 1 + a CTA that leaves without arriving (0: none)
+    int32_t score;          // 1: the scoring phase too; 0: it stays a launch of its own
 };
 
 // Attention statistics the scorer's weightings need (template flags of the
@@ -472,6 +473,7 @@ cudaError_t launch_tier_lir(const TierArgs& a, cudaStream_t s);
 
 enum : uint32_t { kStatusNoPage = 2u };   // a sequence ran out of free pages
 enum : uint32_t { kStatusRouteCap = 4u };  // more windows than the routing sort holds
+enum : uint32_t { kStatusBarrier = 8u };   // with kStatusTimeout: a grid-barrier wait gave up
 
 constexpr int kScoreThreads = 256;
 

@@ -28,6 +28,7 @@ KVEV_OUT_F32, KVEV_OUT_BF16 = 0, 1
 KVEV_AGG_EMA, KVEV_AGG_CUMULATIVE = 0, 1
 KVEV_W_VNORM, KVEV_W_ENTROPY = 1, 2
 KVEV_DIAG_FIELDS = 8
+KVEV_FUSED_OFF, KVEV_FUSED_ALL, KVEV_FUSED_ATTN_COMBINE = 0, 1, 2
 DIAG_NAMES = ["step", "refreshed", "n_raw", "n_kept", "raw_and_kept", "raw_and_prev_raw",
               "n_prev_raw", "kept_and_prev_kept"]
 KVEV_BF16 = 0
@@ -257,8 +258,9 @@ def kvev_set_scorer(ctx, aggregation: int, weighting: int = 0) -> None:
     _check(lib().kvev_set_scorer(ctx, int(aggregation), int(weighting)), ctx)
 
 
-def kvev_set_fused_step(ctx, on: bool) -> None:
-    _check(lib().kvev_set_fused_step(ctx, int(bool(on))), ctx)
+def kvev_set_fused_step(ctx, mode: int) -> None:
+    """KVEV_FUSED_OFF, KVEV_FUSED_ALL or KVEV_FUSED_ATTN_COMBINE (True: ALL)."""
+    _check(lib().kvev_set_fused_step(ctx, int(mode)), ctx)
 
 
 def kvev_test_barrier_timeout(ctx, cta: int, wait_limit: int) -> None:
@@ -424,7 +426,7 @@ class EvictionPass:
         kvev_set_output(self.ctx, out_type)
         kvev_set_scorer(self.ctx, aggregation, weighting)
         if fused:
-            kvev_set_fused_step(self.ctx, True)
+            kvev_set_fused_step(self.ctx, KVEV_FUSED_ALL if fused is True else int(fused))
         shape = (n_layers, batch, n_kv_heads, max_ctx, head_dim)
         self.k = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]
         self.v = [torch.zeros(shape, dtype=torch.bfloat16, device=device) for _ in range(2)]

@@ -216,10 +216,12 @@ kvev_status kvev_set_output(kvev_ctx* ctx, int32_t out_type);
  * tiles it already holds, the entropy from its softmax sums), so neither
  * reads the cache again.  Block-granular and two-tier contexts take only
  * the defaults (KVEV_EUNSUPPORTED otherwise). */
-/* Fused refresh step (token granularity; on != 0 turns it on, from the next
- * step): on refresh steps without a weighting, the attention, the split
- * combine and the scoring run as ONE cooperative launch, their phases
- * separated by grid barriers, instead of three launches.  The arithmetic is
+/* Fused refresh step (token granularity; from the next step): on refresh
+ * steps without a weighting, KVEV_FUSED_ALL runs the attention, the split
+ * combine and the scoring as ONE cooperative launch, their phases separated
+ * by grid barriers, instead of three launches; KVEV_FUSED_ATTN_COMBINE fuses
+ * the attention and the combine only (the scorer keeps its own launch);
+ * KVEV_FUSED_OFF (default) launches the three kernels.  The arithmetic is
  * the three kernels' own, in the same order; the outputs are the same bit
  * for bit whenever the attention splits its tiles over the same number of
  * warps (the same CTAs per SM).  Every barrier wait is bounded: one that
@@ -228,7 +230,8 @@ kvev_status kvev_set_output(kvev_ctx* ctx, int32_t out_type);
  * separate eager pass: "What Matters...", Appendix J).  KVEV_EUNSUPPORTED for
  * shapes without a fused kernel (head_dim 64 or 128, 4 or 8 query heads per
  * KV head, 1, 2 or 8 KV heads are built). */
-kvev_status kvev_set_fused_step(kvev_ctx* ctx, int32_t on);
+enum { KVEV_FUSED_OFF = 0, KVEV_FUSED_ALL = 1, KVEV_FUSED_ATTN_COMBINE = 2 };
+kvev_status kvev_set_fused_step(kvev_ctx* ctx, int32_t mode);
 
 typedef enum { KVEV_AGG_EMA = 0, KVEV_AGG_CUMULATIVE = 1 } kvev_aggregation;
 enum { KVEV_W_VNORM = 1, KVEV_W_ENTROPY = 2 };

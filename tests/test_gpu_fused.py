@@ -25,8 +25,10 @@ from decoding_kv_cache_split_gb300 import kvev  # noqa: E402
 OUTPUTS = ("out", "retained", "n_retained", "score", "t_ins", "t_ref", "pos")
 
 
-def test_fused_tiny_64_steps():
-    tot = run_parity(tiny_workload(0), 128, 0.05, 0.001, 64, fused=True)
+@pytest.mark.parametrize("mode", ["all", "attn_combine"])
+def test_fused_tiny_64_steps(mode):
+    m = kvev.KVEV_FUSED_ALL if mode == "all" else kvev.KVEV_FUSED_ATTN_COMBINE
+    tot = run_parity(tiny_workload(0), 128, 0.05, 0.001, 64, fused=m)
     assert tot["steps"] == 64
 
 
@@ -40,6 +42,15 @@ def test_fused_llama_geometry(refresh):
                period=4, diagnostics=True, fused=True)
 
 
+@pytest.mark.slow
+def test_fused_llama8b_32k_steps_1_to_4():
+    """The full 32-layer, 32768-token pass with the fused step (many tiles
+    per warp at step 1), steps 1-4 against the oracle."""
+    wl = llama8b_workload(0, prefill_len=32768)
+    run_parity(wl, 3277, 0.05, 0.001, 4, age_mode=O.AGE_SINCE_ACCESS, max_ctx=32768 + 64,
+               fused=True)
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_fused_eight_query_heads_and_batches(d):
     wl = Workload(Geometry(2, 16, 2, d, 2), 260, seed=40 + d, outliers=2, heavy=3)
@@ -50,7 +61,7 @@ def test_fused_eight_query_heads_and_batches(d):
 
 @pytest.mark.parametrize("L0,budget", [(1, 1), (17, 16), (33, 40)])
 def test_fused_edge_lengths(L0, budget):
-    wl = Workload(Geometry(2, 4, 1, 64, 1), L0, seed=L0, heavy=1)
+    wl = Workload(Geometry(2, 8, 2, 64, 1), L0, seed=L0, heavy=1)
     run_parity(wl, budget, 0.05, math.inf, 4, fused=True)
 
 
@@ -75,12 +86,14 @@ def _run(ep, wl, steps):
     return got
 
 
-def test_fused_equals_the_three_launches_bit_for_bit():
-    """Llama-3.1-8B head geometry (32 q / 8 KV, d 128): the fused kernel has
-    the attention kernel's CTAs per SM, so both split the tiles alike and
-    every output, kept list, state array and compacted K/V row agrees."""
+@pytest.mark.parametrize("mode", [1, 2])
+def test_fused_equals_the_three_launches_bit_for_bit(mode):
+    """Llama-3.1-8B head geometry (32 q / 8 KV, d 128), several tiles per
+    warp: the fused step runs on the attention kernel's grid, so both split
+    the tiles alike and every output, kept list, state array and compacted
+    K/V row agrees; no scratch region overran its guard band."""
     wl = llama8b_workload(1, prefill_len=2000, n_layers=4, needle_period=3)
-    a, b = _make(wl, 200, False), _make(wl, 200, True)
+    a, b = _make(wl, 200, False), _make(wl, 200, mode)
     want, got = _run(a, wl, 6), _run(b, wl, 6)
     for t, (w, g) in enumerate(zip(want, got), start=1):
         for k in w:
