@@ -495,6 +495,8 @@ def main():
                          "workloads it carries under 'workloads'")
     ap.add_argument("--omega", type=int, default=TIERS["omega"],
                     help="two-tier workload: routing interval")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="two-tier workload: skip the routing-interval sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -511,7 +513,8 @@ def main():
         finish_dist(world)
         return
     if args.workload == "tiers":
-        bench_tiers(args, rank, world, local_rank, omega=args.omega)
+        bench_tiers(args, rank, world, local_rank, omega=args.omega,
+                    omega_sweep=() if args.no_sweep else (1, 32))
         finish_dist(world)
         return
 

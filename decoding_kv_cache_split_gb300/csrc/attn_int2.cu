@@ -25,6 +25,15 @@
 // unit's 12 KiB ledger entry in shared memory with cp.async, and leave a
 // softmax partial per (warp, row) piece for the split combine, plus the
 // per-16-token-tile statistics the window scores are formed from.
+//
+// The bias terms run on the tensor cores too, as fp16 products (fp16 scale and
+// zero times q or p split into fp16 hi + lo rows: exact products, fp32 sums):
+// per unit one 8-k-step MMA of q against a B operand whose columns are the
+// four key groups' zeros and scales gives every group's sum_c q_c z_c and
+// sum_c q_c s_c; per tile one MMA of p 2^10 (the scaling keeps its fp16 lo
+// part out of the subnormal range) against the tokens' value zeros and
+// scales (columns = channel groups) adds sum_i p_i z_ig and sum_i p_i s_ig to
+// an accumulator that the online softmax rescales like the output.
 #include <cuda_fp16.h>
 
 #include "kvev_internal.h"
@@ -34,9 +43,11 @@ namespace kvev {
 namespace {
 
 constexpr int kI2Warps = 4;
+constexpr int kQhBytes = 32 * 16 * 4;   // per warp: q as fp16 hi / lo operand pairs
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kAScale = 0x1p96f;    // A operands carry 2^96
 constexpr float kProdScale = 0x1p31f; // undoes 2^96 * 2^-127 (code - 1.5 in the B operand)
+constexpr float kPScale = 0x1p10f;    // p in the value-bias MMA: its fp16 lo part stays normal
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -102,7 +113,10 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
     griddep_wait();
     griddep_release();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    unsigned char* wbuf = smem + (size_t)warp * 2 * Lay::BYTES;
+    unsigned char* wbuf = smem + (size_t)warp * (2 * Lay::BYTES + kQhBytes);
+    // q of the current row as fp16 operand pairs, k-step major: uint4 k of lane l
+    // at qh4[32 k + l] holds (s, h) = (2k, 0), (2k, 1), (2k + 1, 0), (2k + 1, 1)
+    uint4* qh4 = reinterpret_cast<uint4*>(wbuf + 2 * Lay::BYTES);
     const int w = blockIdx.x * kI2Warps + warp;
     const int64_t N = a.n_units;
     const int64_t x0 = (int64_t)w * N / a.total_warps, x1 = (int64_t)(w + 1) * N / a.total_warps;
@@ -147,7 +161,9 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
 
     uint32_t qa[KS][2];                      // Q * 2^96 (bf16x2) of the lane's head
     float2 o[NB];                            // hi or lo part of O[head][8j + 2t, +1] * 2^-31
-    float2 vbias[NG];                        // the lane's share of sum_i p_i z'_ig (2 parts)
+    // value-bias accumulator (fp16 MMA): row g, columns 2t, 2t+1; columns 0-3
+    // sum_i p_i z_ig, columns 4-7 sum_i p_i s_ig of channel group (column & 3)
+    float2 vbc;
     float m_run = -INFINITY, l_run = 0.f;
     int64_t cur_row = -1;
 
@@ -155,12 +171,16 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
         float l = l_run;
         l += __shfl_xor_sync(kFull, l, 1);
         l += __shfl_xor_sync(kFull, l, 2);
+        // the head's value bias of group c: z part + 1.5 s part (hi + lo rows)
+        float2 vt = add2(vbc, make_float2(__shfl_xor_sync(kFull, vbc.x, 16),
+                                          __shfl_xor_sync(kFull, vbc.y, 16)));
+        vt = mul2(vt, make_float2(1.0f / kPScale, 1.0f / kPScale));   // exact
         float vb[NG];
 #pragma unroll
         for (int c = 0; c < NG; ++c) {
-            vb[c] = vbias[c].x + vbias[c].y;
-            vb[c] += __shfl_xor_sync(kFull, vb[c], 1);
-            vb[c] += __shfl_xor_sync(kFull, vb[c], 2);
+            const float zc = __shfl_sync(kFull, (c & 1) ? vt.y : vt.x, (lane & ~3) + (c >> 1));
+            const float sc2 = __shfl_sync(kFull, (c & 1) ? vt.y : vt.x, (lane & ~3) + 2 + (c >> 1));
+            vb[c] = fmaf(1.5f, sc2, zc);
         }
         const int64_t slot = (int64_t)w + row;
         float* po = a.part_o + ((size_t)slot * G + head) * D;
@@ -179,7 +199,6 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
         }
     };
     const float acc_scale = a.q_scale * kProdScale;   // logits from the code products
-    const float kb_scale = a.q_scale * (1.f / kAScale);
 
     issue(x0, 0);
     int bi = 0;
@@ -197,17 +216,28 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
             const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
             const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
                 a.q + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)gk * G + head) * D);
+            uint32_t qhw[KS][2];
 #pragma unroll
             for (int s = 0; s < KS; ++s)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {   // dims 16s + 8h + 2t, +1 (exact scaling)
                     const uint32_t qw = qrow[8 * s + 4 * h + t];
                     qa[s][h] = pack_bf16x2(bf16_lo(qw) * kAScale, bf16_hi(qw) * kAScale);
+                    // fp16 hi (rows 0-3) or what it leaves (rows 4-7) of the same q
+                    const float q0 = bf16_lo(qw), q1 = bf16_hi(qw);
+                    const uint32_t hw = pack_f16x2(q0, q1);
+                    const float2 hf = unpack_f16x2(hw);
+                    qhw[s][h] = lo_row ? pack_f16x2(q0 - hf.x, q1 - hf.y) : hw;
                 }
+            __syncwarp();   // the previous row's q pairs are no longer read
+#pragma unroll
+            for (int k = 0; k < KS / 2; ++k)
+                qh4[32 * k + lane] = make_uint4(qhw[2 * k][0], qhw[2 * k][1], qhw[2 * k + 1][0],
+                                                qhw[2 * k + 1][1]);
+            __syncwarp();
 #pragma unroll
             for (int j = 0; j < NB; ++j) o[j] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int c = 0; c < NG; ++c) vbias[c] = make_float2(0.f, 0.f);
+            vbc = make_float2(0.f, 0.f);
             m_run = -INFINITY;
             l_run = 0.f;
         }
@@ -218,32 +248,44 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
             const uint4* kc4 = reinterpret_cast<const uint4*>(buf + Lay::KC) + lane;
             const uint4* vc4 = reinterpret_cast<const uint4*>(buf + Lay::VC) + lane;
             const uint4* ks4 = reinterpret_cast<const uint4*>(buf + Lay::KS) + 4 * t;
-            const uint4* kz4 = reinterpret_cast<const uint4*>(buf + Lay::KZ) + 4 * t;
             const uint4* vs4 = reinterpret_cast<const uint4*>(buf + Lay::VS) + 2 * t;
-            const uint4* vz4 = reinterpret_cast<const uint4*>(buf + Lay::VZ) + 2 * t;
+            const uint32_t* vzs = reinterpret_cast<const uint32_t*>(
+                buf + (lo_row ? Lay::VS : Lay::VZ)) + t * (4 * NG / 2) + (g & 3);
+            // key biases of the four groups: sum_c q_c z_c (columns 0-3) and
+            // sum_c q_c s_c (columns 4-7), one fp16 MMA chain over the channels
+            float2 kbc = make_float2(0.f, 0.f);
+            {
+                const uint4* zs4 = reinterpret_cast<const uint4*>(buf + (lo_row ? Lay::KS : Lay::KZ)) +
+                                   (g & 3) * (D / 8) + t * (D / 32);
+#pragma unroll
+                for (int k = 0; k < KS / 2; ++k) {
+                    const uint4 qw = qh4[32 * k + lane], zw = zs4[k];
+                    mma_rows8_f16(kbc.x, kbc.y, qw.x, qw.y, zw.x, zw.y);
+                    mma_rows8_f16(kbc.x, kbc.y, qw.z, qw.w, zw.z, zw.w);
+                }
+                kbc = add2(kbc, make_float2(__shfl_xor_sync(kFull, kbc.x, 16),
+                                            __shfl_xor_sync(kFull, kbc.y, 16)));
+            }
             for (int grp = 0; grp < kTierW / kQGroup; ++grp) {
                 // A' = q * s * 2^96 of this group's key scales (the lane's hi or
-                // lo part), and the key bias sum_c q_c (z_c + 1.5 s_c) * 2^96
+                // lo part); the key bias sum_c q_c (z_c + 1.5 s_c) of the head
                 uint32_t af[KS][2];
-                float2 kb2 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int s2 = 0; s2 < KS / 2; ++s2) {
-                    const uint4 sw = ks4[grp * (D / 8) + s2], zw = kz4[grp * (D / 8) + s2];
+                    const uint4 sw = ks4[grp * (D / 8) + s2];
                     const uint32_t sws[4] = {sw.x, sw.y, sw.z, sw.w};
-                    const uint32_t zws[4] = {zw.x, zw.y, zw.z, zw.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {   // (s, h) = (2 s2 + k / 2, k % 2)
                         const int s = 2 * s2 + k / 2, h = k % 2;
-                        const float2 sc = h2f(sws[k]), zc = h2f(zws[k]);
+                        const float2 sc = h2f(sws[k]);
                         const float2 q01 = make_float2(bf16_lo(qa[s][h]), bf16_hi(qa[s][h]));
                         af[s][h] = half_pair(mul2(q01, sc));
-                        kb2 = fma2(q01, fma2(make_float2(1.5f, 1.5f), sc, zc), kb2);
                     }
                 }
-                float kb = kb2.x + kb2.y;
-                kb += __shfl_xor_sync(kFull, kb, 1);
-                kb += __shfl_xor_sync(kFull, kb, 2);
-                kb *= kb_scale;
+                const float kz = __shfl_sync(kFull, (grp & 1) ? kbc.y : kbc.x, (lane & ~3) + (grp >> 1));
+                const float ks_ = __shfl_sync(kFull, (grp & 1) ? kbc.y : kbc.x,
+                                              (lane & ~3) + 2 + (grp >> 1));
+                const float kb = fmaf(1.5f, ks_, kz) * a.q_scale;
 #pragma unroll
                 for (int tt = 0; tt < kQGroup / kTile; ++tt) {
                     const int ti = grp * (kQGroup / kTile) + tt;   // 16-token tile of the window
@@ -283,8 +325,7 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                         l_run *= f;
 #pragma unroll
                         for (int j = 0; j < NB; ++j) o[j] = mul2(o[j], make_float2(f, f));
-#pragma unroll
-                        for (int c = 0; c < NG; ++c) vbias[c] = mul2(vbias[c], make_float2(f, f));
+                        vbc = mul2(vbc, make_float2(f, f));
                     }
                     float pv[4];
 #pragma unroll
@@ -302,23 +343,30 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                             a.tile_stats[((size_t)row * a.stats_tiles + (size_t)wid * (kTierW / kTile) +
                                           ti) * G + head] = make_float2(m_run, ts);
                     }
-                    // ---- O += (p * s_v) codes + p * z'_v, per 32-channel group
+                    // ---- O += (p * s_v) codes, per 32-channel group; the value bias
+                    //      sum_i p_i (z_ig, s_ig) by one fp16 MMA (p as hi / lo rows)
                     const uint4 vq = vc4[ti * 32];
                     const uint32_t vw[4] = {vq.x, vq.y, vq.z, vq.w};
                     const uint4 s0 = vs4[ti * 8], s1 = vs4[ti * 8 + 1];   // tokens 2t(+1), 2t+8(+1)
-                    const uint4 z0 = vz4[ti * 8], z1 = vz4[ti * 8 + 1];
                     const uint32_t s0w[4] = {s0.x, s0.y, s0.z, s0.w}, s1w[4] = {s1.x, s1.y, s1.z, s1.w};
-                    const uint32_t z0w[4] = {z0.x, z0.y, z0.z, z0.w}, z1w[4] = {z1.x, z1.y, z1.z, z1.w};
                     const float2 p01 = make_float2(pv[0], pv[1]), p23 = make_float2(pv[2], pv[3]);
+                    {   // p 2^10 (exact) as fp16 hi or lo
+                        const float2 q01 = mul2(p01, make_float2(kPScale, kPScale));
+                        const float2 q23 = mul2(p23, make_float2(kPScale, kPScale));
+                        const uint32_t h01 = pack_f16x2(q01.x, q01.y), h23 = pack_f16x2(q23.x, q23.y);
+                        uint32_t a0 = h01, a2 = h23;
+                        if (lo_row) {
+                            const float2 f01 = unpack_f16x2(h01), f23 = unpack_f16x2(h23);
+                            a0 = pack_f16x2(q01.x - f01.x, q01.y - f01.y);
+                            a2 = pack_f16x2(q23.x - f23.x, q23.y - f23.y);
+                        }
+                        mma_rows8_f16(vbc.x, vbc.y, a0, a2, vzs[ti * 32], vzs[ti * 32 + 4]);
+                    }
                     const float2 ps01 = mul2(p01, make_float2(kAScale, kAScale));
                     const float2 ps23 = mul2(p23, make_float2(kAScale, kAScale));
 #pragma unroll
                     for (int cg = 0; cg < NG; ++cg) {
                         const float2 sa = h2f(s0w[cg]), sb = h2f(s1w[cg]);
-                        const float2 za = h2f(z0w[cg]), zb = h2f(z1w[cg]);
-                        const float2 k15 = make_float2(1.5f, 1.5f);
-                        vbias[cg] = fma2(p01, fma2(k15, sa, za), vbias[cg]);
-                        vbias[cg] = fma2(p23, fma2(k15, sb, zb), vbias[cg]);
                         const uint32_t pa0 = half_pair(mul2(ps01, sa));
                         const uint32_t pa2 = half_pair(mul2(ps23, sb));
 #pragma unroll
@@ -341,7 +389,7 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
 template <int D, int G>
 int ctas_per_sm_int2() {
     auto kern = attn_int2_kernel<D, G>;
-    const int smem = kI2Warps * 2 * LedgerLayout<D>::BYTES;
+    const int smem = kI2Warps * (2 * LedgerLayout<D>::BYTES + kQhBytes);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return 0;
@@ -365,7 +413,7 @@ cudaError_t launch_attn_int2(const Int2Args& a, int head_dim, int group, int gri
                              cudaStream_t s) {
     if (head_dim != 128 || group != 4) return cudaErrorInvalidValue;
     auto kern = attn_int2_kernel<128, 4>;
-    const int smem = kI2Warps * 2 * LedgerLayout<128>::BYTES;
+    const int smem = kI2Warps * (2 * LedgerLayout<128>::BYTES + kQhBytes);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kI2Warps * 32), (size_t)smem, s, a);

@@ -28,6 +28,30 @@ __device__ __forceinline__ void mma_rows8(float& c0, float& c1, uint32_t a0, uin
     (void)d2;
     (void)d3;
 }
+// The same with fp16 operands (A and B both fp16).
+__device__ __forceinline__ void mma_rows8_f16(float& c0, float& c1, uint32_t a0, uint32_t a2,
+                                              uint32_t b0, uint32_t b1) {
+    float d2, d3;   // rows 8..15: discarded
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3},"
+        " {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(c0), "=f"(c1), "=f"(d2), "=f"(d3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(0.f),
+          "f"(0.f));
+    (void)d2;
+    (void)d3;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
+    float2 r;
+    asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.f32.f16 %0, lo;\n"
+        " cvt.f32.f16 %1, hi;\n}" : "=f"(r.x), "=f"(r.y) : "r"(w));
+    return r;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -53,7 +53,27 @@ def _case(rng, n=128, key_scale=1.0):
     return q, codes, s32, z32
 
 
-def _device_logit(q, codes, s, z, use_lo=True):
+def f16_split(x):
+    """x (fp32) as an fp16 hi part (rounded) and the rounded fp16 remainder:
+    the bias operands of the INT2 attention (rows 0-3 hi, rows 4-7 lo)."""
+    x = np.asarray(x, F)
+    hi = x.astype(np.float16)
+    lo = (x - hi.astype(F)).astype(np.float16)
+    return hi, lo
+
+
+def _bias_mma(x, w16):
+    """sum_c x_c w_c as the fp16 tensor-core products take it: x split into
+    fp16 hi + lo, each product with the fp16 w exact, fp32 sums."""
+    hi, lo = f16_split(x)
+    acc = F(0)
+    for c in range(len(x)):
+        acc = F(acc + F(hi[c].astype(F) * w16[c].astype(F)))
+        acc = F(acc + F(lo[c].astype(F) * w16[c].astype(F)))
+    return acc
+
+
+def _device_logit(q, codes, s, z, use_lo=True, bias_mma=False):
     a = (q * s * F(2.0 ** 96)).astype(F)                 # q s 2^96
     hi, lo = split(a)
     b = ((2 * codes - 3) * 2.0 ** -128)                   # exact subnormal bf16 values
@@ -62,9 +82,13 @@ def _device_logit(q, codes, s, z, use_lo=True):
         acc = F(acc + F(hi[c] * b[c]))
         if use_lo:
             acc = F(acc + F(lo[c] * b[c]))
-    bias = F(0)
-    for c in range(len(q)):
-        bias = F(bias + F(q[c] * F(z[c] + F(1.5) * s[c])))
+    if bias_mma:   # sum q z and sum q s by fp16 products, then z part + 1.5 s part
+        bias = F(_bias_mma(q, z.astype(np.float16)) +
+                 F(1.5) * _bias_mma(q, s.astype(np.float16)))
+    else:
+        bias = F(0)
+        for c in range(len(q)):
+            bias = F(bias + F(q[c] * F(z[c] + F(1.5) * s[c])))
     return float(F(acc * F(2.0 ** 31)) + bias)
 
 
@@ -85,3 +109,25 @@ def test_logits_from_the_split_operands_match_the_dequantized_keys():
                             abs(_device_logit(q, codes, s, z, use_lo=False) - ref) / norm)
     assert worst <= 1e-5, worst                  # fp32 roundings of the 256 summed products
     assert worst_hi_only >= 1e-4, worst_hi_only  # the lo part carries ~8 more bits
+
+
+def test_bias_terms_from_fp16_products_match_the_dequantized_keys():
+    """The key bias sum_c q_c (z_c + 1.5 s_c) taken as two fp16 tensor-core
+    sums (q as fp16 hi + lo against the fp16 zeros and scales) keeps the
+    logit as close to the dequantized keys' as the fp32 chain does; p, scaled
+    by 2^10 so that its fp16 lo part stays normal, as fp16 hi + lo loses at
+    most 2^-21 of each probability above 2^-14 (and 2^-35 absolute below)."""
+    rng = np.random.default_rng(3)
+    worst = 0.0
+    for trial in range(300):
+        q, codes, s, z = _case(rng, key_scale=(0.05, 1.0, 20.0)[trial % 3])
+        ref = _reference_logit(q, codes, s, z)
+        norm = float(np.sum(np.abs(q.astype(np.float64) * (codes * s + z))))
+        worst = max(worst, abs(_device_logit(q, codes, s, z, bias_mma=True) - ref) / norm)
+    assert worst <= 1e-5, worst
+    p = np.exp2(-rng.uniform(0, 30, 200000)).astype(F)
+    hi, lo = f16_split(p * F(1024))
+    err = np.abs((hi.astype(np.float64) + lo.astype(np.float64)) / 1024 - p.astype(np.float64))
+    big = p >= 2.0 ** -14
+    assert np.all(err[big] <= 2.0 ** -21 * p[big].astype(np.float64))
+    assert np.all(err[~big] <= 2.0 ** -35)
