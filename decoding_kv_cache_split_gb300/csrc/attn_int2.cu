@@ -287,10 +287,14 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                                               (lane & ~3) + 2 + (grp >> 1));
                 const float kb = fmaf(1.5f, ks_, kz) * a.q_scale;
 #pragma unroll
-                for (int tt = 0; tt < kQGroup / kTile; ++tt) {
-                    const int ti = grp * (kQGroup / kTile) + tt;   // 16-token tile of the window
-                    // ---- S = A' codes (two 8-token blocks; even and odd k-steps in
-                    //      separate accumulators) + bias
+                // ---- S = A' codes + bias for both tiles of the group (two 8-token
+                //      blocks each; even and odd k-steps in separate accumulators):
+                //      their 32 MMAs are independent of the softmax below
+                constexpr int TT = kQGroup / kTile;            // tiles per key group
+                float sc[TT][2][2];
+#pragma unroll
+                for (int tt = 0; tt < TT; ++tt) {
+                    const int ti = grp * TT + tt;               // 16-token tile of the window
                     const uint4 kq = kc4[ti * 32];
                     const uint32_t kw[4] = {kq.x, kq.y, kq.z, kq.w};
                     float acc[2][2][2] = {};
@@ -303,7 +307,6 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                             const uint32_t b1 = code_reg(kw[s >> 1], slot + 1);
                             mma_rows8(acc[s & 1][i][0], acc[s & 1][i][1], af[s][0], af[s][1], b0, b1);
                         }
-                    float sc[2][2];
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
                         float2 part = add2(make_float2(acc[0][i][0], acc[0][i][1]),
@@ -312,44 +315,58 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                                                       __shfl_xor_sync(kFull, part.y, 16)));
                         const float2 v = fma2(part, make_float2(acc_scale, acc_scale),
                                               make_float2(kb, kb));
-                        sc[i][0] = v.x;
-                        sc[i][1] = v.y;
+                        sc[tt][i][0] = v.x;
+                        sc[tt][i][1] = v.y;
                     }
-                    // ---- online softmax of the head
-                    float mt = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-                    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
-                    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
-                    if (mt > m_run) {
-                        const float f = fast_exp2(m_run - mt);
-                        m_run = mt;
-                        l_run *= f;
+                }
+                // ---- online softmax of the head, one update for the group's 32 tokens
+                float mt = -INFINITY;
 #pragma unroll
-                        for (int j = 0; j < NB; ++j) o[j] = mul2(o[j], make_float2(f, f));
-                        vbc = mul2(vbc, make_float2(f, f));
-                    }
-                    float pv[4];
+                for (int tt = 0; tt < TT; ++tt)
+                    mt = fmaxf(mt, fmaxf(fmaxf(sc[tt][0][0], sc[tt][0][1]),
+                                         fmaxf(sc[tt][1][0], sc[tt][1][1])));
+                mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+                mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+                if (mt > m_run) {
+                    const float f = fast_exp2(m_run - mt);
+                    m_run = mt;
+                    l_run *= f;
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) o[j] = mul2(o[j], make_float2(f, f));
+                    vbc = mul2(vbc, make_float2(f, f));
+                }
+                float pv[TT][4];
+#pragma unroll
+                for (int tt = 0; tt < TT; ++tt)
 #pragma unroll
                     for (int i = 0; i < 2; ++i)
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            pv[2 * i + e] = fast_exp2(sc[i][e] - m_run);
-                            l_run += pv[2 * i + e];
+                            pv[tt][2 * i + e] = fast_exp2(sc[tt][i][e] - m_run);
+                            l_run += pv[tt][2 * i + e];
                         }
-                    if (a.tile_stats) {   // (running max, tile sum) of the head for the window score
-                        float ts = (pv[0] + pv[1]) + (pv[2] + pv[3]);
+                if (a.tile_stats) {   // (running max, tile sum) per head and tile, for the window score
+#pragma unroll
+                    for (int tt = 0; tt < TT; ++tt) {
+                        float ts = (pv[tt][0] + pv[tt][1]) + (pv[tt][2] + pv[tt][3]);
                         ts += __shfl_xor_sync(kFull, ts, 1);
                         ts += __shfl_xor_sync(kFull, ts, 2);
                         if (!lo_row && t == 0)
                             a.tile_stats[((size_t)row * a.stats_tiles + (size_t)wid * (kTierW / kTile) +
-                                          ti) * G + head] = make_float2(m_run, ts);
+                                          grp * TT + tt) * G + head] = make_float2(m_run, ts);
                     }
+                }
+#pragma unroll
+                for (int tt = 0; tt < TT; ++tt) {
+                    const int ti = grp * TT + tt;
                     // ---- O += (p * s_v) codes, per 32-channel group; the value bias
                     //      sum_i p_i (z_ig, s_ig) by one fp16 MMA (p as hi / lo rows)
                     const uint4 vq = vc4[ti * 32];
                     const uint32_t vw[4] = {vq.x, vq.y, vq.z, vq.w};
                     const uint4 s0 = vs4[ti * 8], s1 = vs4[ti * 8 + 1];   // tokens 2t(+1), 2t+8(+1)
                     const uint32_t s0w[4] = {s0.x, s0.y, s0.z, s0.w}, s1w[4] = {s1.x, s1.y, s1.z, s1.w};
-                    const float2 p01 = make_float2(pv[0], pv[1]), p23 = make_float2(pv[2], pv[3]);
+                    const float2 p01 = make_float2(pv[tt][0], pv[tt][1]);
+                    const float2 p23 = make_float2(pv[tt][2], pv[tt][3]);
                     {   // p 2^10 (exact) as fp16 hi or lo
                         const float2 q01 = mul2(p01, make_float2(kPScale, kPScale));
                         const float2 q23 = mul2(p23, make_float2(kPScale, kPScale));
