@@ -267,12 +267,15 @@ int64_t attn_grid_for_device(int num_sms, const kvev_layout& L) {
     return (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
 }
 
-// Warps of one attention launch over n_tiles tiles: at most one per tile, so
-// a short cache is not spread over warps that hold nothing (their empty
-// split slots would only lengthen the combine's walk over a row's warps).
-// Sets *grid to the CTAs that hold them.
+// Warps of one attention launch over n_tiles tiles: all of them when every
+// warp gets kMinTilesPerWarp tiles or more, else one per kMinTilesPerWarp
+// tiles, so a short cache is not cut into many one-tile pieces (the combine
+// walks a row's pieces one after another).  Sets *grid to the CTAs that hold
+// them.
+constexpr int kMinTilesPerWarp = 4;
 int attn_launch_warps(int max_warps, int64_t n_tiles, int* grid) {
-    const int w = n_tiles < (int64_t)max_warps ? (int)(n_tiles > 0 ? n_tiles : 1) : max_warps;
+    const int64_t want = (n_tiles + kMinTilesPerWarp - 1) / kMinTilesPerWarp;
+    const int w = want < (int64_t)max_warps ? (int)(want > 0 ? want : 1) : max_warps;
     const int wpc = attn_warps_per_cta();
     *grid = (w + wpc - 1) / wpc;
     return w;

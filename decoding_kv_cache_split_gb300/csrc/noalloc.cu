@@ -116,11 +116,12 @@ extern "C" kvev_status kvev_attend_noalloc(const kvev_layout* L, const void* q, 
     int64_t grid = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
     const int64_t grid_fit = (slot_cap - rows) / wpc;   // CTAs whose partials fit
     if (grid > grid_fit) grid = grid_fit;
-    // at most one warp per tile, as kvev_step launches it (the same split,
+    // one warp per 4 tiles at most, as kvev_step launches it (the same split,
     // so the same output bit for bit)
     const int tiles_per_row = (len + kTile - 1) / kTile;
     const int64_t n_tiles = rows * tiles_per_row;
-    const int64_t warps = n_tiles < grid * wpc ? n_tiles : grid * wpc;
+    const int64_t want = (n_tiles + 3) / 4;
+    const int64_t warps = want < grid * wpc ? (want > 0 ? want : 1) : grid * wpc;
     grid = (warps + wpc - 1) / wpc;
 
     cudaStream_t s = (cudaStream_t)stream;
