@@ -40,7 +40,8 @@ def _needs(target: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(OBJ, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    headers = sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [
+    headers = sorted(glob.glob(os.path.join(CSRC, "*.h")) +
+                     glob.glob(os.path.join(CSRC, "*.cuh"))) + [
         os.path.join(HERE, "..", "include", "kvev.h")]
     cc = nvcc()
     extra = os.environ.get("KVEV_EXTRA_NVCC_FLAGS", "").split()

@@ -85,6 +85,7 @@ struct Workspace {
     int32_t* readmit_page = nullptr;  // [1]
     int32_t* first_moved = nullptr;   // [batch] first slot not kept this step
     int32_t* vp = nullptr;            // [2][batch] reused-prefix rows, by step parity
+    int32_t* evicted = nullptr;       // [batch][kFewEvict] slots a few-eviction step drops
     // two-tier mode (page_tokens = window)
     int32_t* t_bt = nullptr;          // [batch][bt_ld] attention block list
     int32_t* t_bpos = nullptr;
@@ -183,6 +184,7 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
     w.readmit_page = (int32_t*)take(4, "readmit_page");
     w.first_moved = (int32_t*)take((size_t)L.batch * 4, "first_moved");
     w.vp = (int32_t*)take((size_t)L.batch * 8, "vp");
+    w.evicted = (int32_t*)take((size_t)L.batch * kFewEvict * 4, "evicted");
     if (L.page_tokens == 1) {
         w.part_e = (float*)take((size_t)slots * G * 4, "part_e");
         w.part_vn = (float*)take((size_t)slots * 4, "part_vn");
@@ -780,6 +782,14 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     const bool cumulative = c->aggregation == KVEV_AGG_CUMULATIVE;
     sc.alpha = cumulative ? 1.0f : c->alpha;
     sc.oma = cumulative ? 1.0f : 1.0f - c->alpha;
+    for (int k = 0; k < kScoreSegMax; ++k) {   // oma^(layers of scorer segment k), fp64
+        const int n = k < kScoreSegs
+                          ? (k + 1) * Ly.n_layers / kScoreSegs - k * Ly.n_layers / kScoreSegs
+                          : 0;
+        double d = 1.0;
+        for (int i = 0; i < n; ++i) d *= (double)sc.oma;
+        sc.seg_decay[k] = (float)d;
+    }
     sc.ent = (stats & kStatEntropy) ? c->ws.ent : nullptr;
     sc.vnorm = (stats & kStatVNorm) ? c->ws.vnorm : nullptr;
     sc.vmean = (stats & kStatVNorm) ? c->ws.vmean : nullptr;
@@ -864,6 +874,10 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     se.budget = (int)c->budget;
     se.refresh = refresh ? 1 : 0;
     se.first_moved = c->ws.first_moved;
+    // few evictions: the maxima path lists them and the compaction runs in place
+    const bool in_place = !identity && L - n_keep <= kFewEvict;
+    se.evicted = in_place ? c->ws.evicted : nullptr;
+    se.few = in_place ? 1 : 0;
     rc = timed_launch(c, kProfSelect, s, "select",
                       [&] { return launch_select(se, Ly.batch, c->num_sms, s); });
     if (rc != KVEV_OK) return rc;
@@ -875,6 +889,7 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
             sr.n_retained = c->ws.raw_n;
             sr.refresh = 1;          // no new-token score to set
             sr.first_moved = nullptr;
+            sr.evicted = nullptr;    // (the compaction reads the step's own list)
             rc = timed_launch(c, kProfSelect, s, "raw select",
                               [&] { return launch_select(sr, Ly.batch, c->num_sms, s); });
             if (rc != KVEV_OK) return rc;
@@ -906,10 +921,14 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
     cp.first_moved = c->ws.first_moved;
     cp.vp_in = c->ws.vp + (step & 1) * Ly.batch;
     cp.vp_out = c->ws.vp + ((step + 1) & 1) * Ly.batch;
+    const int dst = identity || in_place ? cur : cur ^ 1;   // the live buffer after the step
     cp.k_src = (const uint16_t*)cache->k[cur];
     cp.v_src = (const uint16_t*)cache->v[cur];
-    cp.k_dst = (uint16_t*)cache->k[cur ^ 1];
-    cp.v_dst = (uint16_t*)cache->v[cur ^ 1];
+    cp.k_dst = (uint16_t*)cache->k[dst];
+    cp.v_dst = (uint16_t*)cache->v[dst];
+    cp.in_place = in_place ? 1 : 0;
+    cp.n_evict = L - n_keep;
+    cp.evicted = c->ws.evicted;
     cp.retained = retained_idx;
     cp.m_s = c->ws.m_s;
     cp.tref_s = c->ws.tref_s;
@@ -928,7 +947,7 @@ kvev_status kvev_step(kvev_ctx* c, const void* q, const void* k_new, const void*
                       [&] { return launch_compact(cp, c->num_sms, s); });
     if (rc != KVEV_OK) return rc;
 
-    if (!identity) cache->cur = cur ^ 1;
+    cache->cur = dst;
     c->len = n_keep;
     c->step = step;
     return KVEV_OK;

@@ -732,8 +732,7 @@ __global__ void __launch_bounds__(kWarps * 32)
                       const CombineArgs cb, const ScoreArgs sc, const FusedArgs f) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
-    __shared__ float s_c[kRefreshSegs][32], s_tot[kRefreshSegs][32];
-    static_assert(kWarps * 32 == kRefreshThreads, "one CTA is one scorer block");
+    __shared__ float s_c[kScoreSegs][32], s_tot[kScoreSegs][32];
     // phase A: attention, logits kept, split partials
     attn_warp<D, G, kStages, kWarps, false, 0>(&tmap_k, &tmap_v, a, smem);
     if (!grid_barrier(f, a.status)) return;
@@ -761,7 +760,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         score_tables<G, NKV, false>(sc, b, tab);
         for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
             __syncthreads();
-            score_block<G, NKV, false>(sc, b, blk, tab, s_c, s_tot);
+            score_block<G, NKV, false, kScoreSegs, kWarps>(sc, b, blk, tab, s_c, s_tot);
         }
     }
     griddep_release();

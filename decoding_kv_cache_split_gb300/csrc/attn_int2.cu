@@ -126,22 +126,44 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
     const int head = g & 3;                  // query head of the group
     const bool lo_row = g >= 4;              // this row carries the "lo" parts
     const float lom = lo_row ? 1.f : 0.f;
-    // window id of unit x (-1: empty), and its ledger entry
-    auto unit_window = [&](int64_t x, const unsigned char** src) -> int {
-        const int64_t row = x / a.slots;
-        const int j = (int)(x - row * a.slots);
-        const int gk = (int)(row % a.n_kv);
-        const int64_t lb = row / a.n_kv;
-        const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
-        if (j >= a.n_qwin[b]) return -1;
-        const int wi = a.q_list[(size_t)b * a.q_ld + j];
+    // Unit x is INT2 slot j of row (layer l, sequence b, KV head gk), rows
+    // ordered ((l batch) + b) n_kv + gk; a warp's units are consecutive, so
+    // the position is divided out once and then stepped.
+    struct UnitPos {
+        int64_t row;
+        int j, b, l, gk;
+    };
+    auto locate = [&](int64_t x) {
+        UnitPos u;
+        u.row = x / a.slots;
+        u.j = (int)(x - u.row * a.slots);
+        u.gk = (int)(u.row % a.n_kv);
+        const int64_t lb = u.row / a.n_kv;
+        u.b = (int)(lb % a.batch);
+        u.l = (int)(lb / a.batch);
+        return u;
+    };
+    auto advance = [&](UnitPos& u) {
+        if (++u.j < a.slots) return;
+        u.j = 0;
+        ++u.row;
+        if (++u.gk < a.n_kv) return;
+        u.gk = 0;
+        if (++u.b < a.batch) return;
+        u.b = 0;
+        ++u.l;
+    };
+    // window id of a unit (-1: past the sequence's INT2 list), and its ledger entry
+    auto unit_window = [&](const UnitPos& u, const unsigned char** src) -> int {
+        if (u.j >= a.n_qwin[u.b]) return -1;
+        const int wi = a.q_list[(size_t)u.b * a.q_ld + u.j];
         *src = a.ledger +
-               ((((size_t)b * a.max_windows + wi) * a.n_layers + l) * a.n_kv + gk) * Lay::BYTES;
+               ((((size_t)u.b * a.max_windows + wi) * a.n_layers + u.l) * a.n_kv + u.gk) *
+                   Lay::BYTES;
         return wi;
     };
-    auto issue = [&](int64_t x, int bi) {
-        const unsigned char* src = nullptr;
-        if (unit_window(x, &src) >= 0) {
+    auto issue = [&](const unsigned char* src, int wid, int bi) {
+        if (wid >= 0) {
             const uint32_t dst = smem_addr(wbuf + (size_t)bi * Lay::BYTES);
             for (int i = lane; i < Lay::BYTES / 16; i += 32) cp_async16(dst + 16 * i, src + 16 * i);
         }
@@ -200,20 +222,28 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
     };
     const float acc_scale = a.q_scale * kProdScale;   // logits from the code products
 
-    issue(x0, 0);
+    UnitPos cur = locate(x0), nxt = cur;
+    const unsigned char* src = nullptr;
+    int wid = unit_window(cur, &src);
+    issue(src, wid, 0);
     int bi = 0;
     for (int64_t x = x0; x < x1; ++x, bi ^= 1) {
-        if (x + 1 < x1) issue(x + 1, bi ^ 1);
-        else cp_async_commit();              // keep one group per iteration
+        advance(nxt);                        // unit x + 1
+        const unsigned char* src_next = nullptr;
+        int wid_next = -1;
+        if (x + 1 < x1) {
+            wid_next = unit_window(nxt, &src_next);
+            issue(src_next, wid_next, bi ^ 1);
+        } else {
+            cp_async_commit();               // keep one group per iteration
+        }
         cp_async_wait_prior();
         __syncwarp();
-        const int64_t row = x / a.slots;
+        const int64_t row = cur.row;
         if (row != cur_row) {
             if (cur_row >= 0) flush(cur_row);
             cur_row = row;
-            const int gk = (int)(row % a.n_kv);
-            const int64_t lb = row / a.n_kv;
-            const int b = (int)(lb % a.batch), l = (int)(lb / a.batch);
+            const int gk = cur.gk, b = cur.b, l = cur.l;
             const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
                 a.q + (((size_t)b * a.n_layers + l) * a.n_q + (size_t)gk * G + head) * D);
             uint32_t qhw[KS][2];
@@ -241,8 +271,6 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
             m_run = -INFINITY;
             l_run = 0.f;
         }
-        const unsigned char* src = nullptr;
-        const int wid = unit_window(x, &src);
         if (wid >= 0) {
             const unsigned char* buf = wbuf + (size_t)bi * Lay::BYTES;
             const uint4* kc4 = reinterpret_cast<const uint4*>(buf + Lay::KC) + lane;
@@ -398,6 +426,8 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
             }
         }
         __syncwarp();   // every lane is done with this buffer before it is refilled
+        cur = nxt;
+        wid = wid_next;
     }
     cp_async_wait_all();
     flush(cur_row);

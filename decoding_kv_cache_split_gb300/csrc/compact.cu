@@ -11,6 +11,19 @@
 // 32/(D/8) rows per instruction.
 // The per-token state (score, clocks, position) is gathered from the
 // scoring kernel's scratch copy by the CTAs of the first cache row.
+//
+// Steps that evict few rows (at most kFewEvict: the steady state, one token
+// in and one out) compact in place instead: only the rows at and after the
+// first evicted slot move, each by the number of evicted slots below it.  One
+// CTA walks one (K or V, layer, sequence, KV head) row of the cache upwards
+// in chunks; slot j's source is never below j, so a chunk's stores land below
+// the next chunk's sources, and the loads of chunk c + 1 are issued before the
+// stores of chunk c.  A barrier after each chunk orders every load of the next
+// chunk before any of its stores (another thread's store may hit a row this
+// thread loaded).  The other ping-pong buffer is left as it is: its rows
+// still equal the live ones below the first moved slot.
+#include <climits>
+
 #include "kvev_internal.h"
 
 namespace kvev {
@@ -71,6 +84,69 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const CompactArgs
         if (jj[u] < a.n_keep && jj[u] >= skip) __stcs(dst + (size_t)jj[u] * lpr + c, buf[u]);
 }
 
+constexpr int kInThreads = 256;
+constexpr int kInUnroll = 4;
+
+__global__ void __launch_bounds__(kInThreads, 4) compact_inplace_kernel(const CompactArgs a) {
+    griddep_wait();
+    griddep_release();
+    const int nthreads = gridDim.x * gridDim.y * kInThreads;
+    const int gtid = (blockIdx.y * gridDim.x + blockIdx.x) * kInThreads + threadIdx.x;
+    // per-token state, gathered by every CTA's threads in turn
+    for (int64_t e = gtid; e < (int64_t)a.batch * a.n_keep; e += nthreads) {
+        const int bb = (int)(e / a.n_keep), j = (int)(e % a.n_keep);
+        const int src = a.retained[(size_t)bb * a.budget + j];
+        const size_t si = (size_t)bb * a.max_ctx + src, di = (size_t)bb * a.max_ctx + j;
+        a.st.score[di] = a.m_s[si];
+        a.st.t_ins[di] = a.tins_s[si];
+        a.st.t_ref[di] = a.tref_s[si];
+        a.st.pos[di] = a.pos_s[si];
+    }
+    if (gtid < a.batch && a.vp_out)   // the other buffer equals this one below both
+        a.vp_out[gtid] = min(a.vp_in[gtid], a.first_moved[gtid]);
+
+    const int r = blockIdx.x;                        // (layer, sequence, KV head)
+    const int b = (r / a.n_kv) % a.batch;
+    int f[kFewEvict];                                // e_i - i, ascending
+#pragma unroll
+    for (int i = 0; i < kFewEvict; ++i)
+        f[i] = i < a.n_evict ? __ldg(a.evicted + (size_t)b * kFewEvict + i) - i : INT_MAX;
+    const int lpr = a.head_dim / 8;
+    const int rows_per_pass = kInThreads / lpr;
+    const int chunk = rows_per_pass * kInUnroll;
+    const int c = threadIdx.x % lpr, jr = threadIdx.x / lpr;
+    uint4* rowp = reinterpret_cast<uint4*>(blockIdx.y == 0 ? a.k_dst : a.v_dst) +
+                  (size_t)r * a.max_ctx * lpr;
+    auto source = [&](int j) {
+        int s = j;
+#pragma unroll
+        for (int i = 0; i < kFewEvict; ++i) s += f[i] <= j;
+        return s;
+    };
+    uint4 cur[kInUnroll], nxt[kInUnroll] = {};
+    auto load = [&](int j0, uint4* buf) {
+#pragma unroll
+        for (int u = 0; u < kInUnroll; ++u) {
+            const int j = j0 + u * rows_per_pass + jr;
+            if (j < a.n_keep) buf[u] = __ldcg(rowp + (size_t)source(j) * lpr + c);
+        }
+    };
+    const int first = a.n_evict > 0 ? f[0] : a.n_keep;   // e_0: rows below stay
+    load(first, cur);
+    __syncthreads();
+    for (int j0 = first; j0 < a.n_keep; j0 += chunk) {
+        if (j0 + chunk < a.n_keep) load(j0 + chunk, nxt);
+#pragma unroll
+        for (int u = 0; u < kInUnroll; ++u) {
+            const int j = j0 + u * rows_per_pass + jr;
+            if (j < a.n_keep) __stcg(rowp + (size_t)j * lpr + c, cur[u]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kInUnroll; ++u) cur[u] = nxt[u];
+    }
+}
+
 __global__ void append_kernel(const AppendArgs a) {
     // one CTA per (layer, sequence, KV head) row; threads copy 16-byte units
     griddep_wait();
@@ -117,6 +193,8 @@ __global__ void init_state_kernel(kvev_state st, int batch, int max_ctx, int len
 
 cudaError_t launch_compact(const CompactArgs& a, int num_sms, cudaStream_t s) {
     (void)num_sms;
+    if (a.in_place && !a.identity)
+        return launch_pdl(compact_inplace_kernel, dim3(a.rows, 2), dim3(kInThreads), 0, s, a);
     const int lpr = a.head_dim / 8;
     const int chunk = (kCopyThreads / lpr) * kCopyUnroll;
     const dim3 grid((a.n_keep + chunk - 1) / chunk, a.identity ? 1 : a.rows, a.identity ? 1 : 2);

@@ -137,6 +137,10 @@ struct CombineArgs {
 };
 
 
+constexpr int kScoreSegs = 4;     // layer segments of the refresh scorer (a warp each)
+constexpr int kScoreSegMax = 8;   // room for the scorer's layer segments
+static_assert(kScoreSegs <= kScoreSegMax, "ScoreArgs holds one decay per segment");
+
 struct ScoreArgs {
     const float* logits;   // [rows][logit_ld][G]
     int32_t logit_ld;
@@ -168,6 +172,9 @@ struct ScoreArgs {
     // ranks the largest first, and optionally as a value
     uint32_t* raw_keys;    // [b][max_ctx] or null
     float* dbg_raw;        // [b][max_ctx] or null
+    // oma^n for the layers n of each scorer segment 1.. (kScoreSegs segments
+    // of the layers in order), formed in fp64 on the host and rounded once
+    float seg_decay[kScoreSegMax];
 };
 
 // Ranking diagnostics of one token-mode step (diag.cu).
@@ -205,6 +212,10 @@ struct SelectArgs {
                               //    its longest chunk (select_stages_keys on the host)
     int32_t ret_ld;           // row stride of retained (0: budget)
     int32_t* first_moved;     // [b] first slot not kept (L when none), or null
+    int32_t* evicted;         // [b][kFewEvict] evicted slots, ascending, when L - B
+                              //    <= kFewEvict (the maxima path), or null
+    int32_t few;              // 1: every sequence evicts at most kFewEvict (host-known):
+                              //    one CTA per sequence, no cluster
 };
 
 struct CompactArgs {
@@ -223,6 +234,12 @@ struct CompactArgs {
     const int32_t* first_moved;
     const int32_t* vp_in;
     int32_t* vp_out;
+    // In place (few evictions): the sources are the destinations' buffer and
+    // slot j's source is j plus the number of evicted slots e_i with
+    // e_i - i <= j (evicted: [b][kFewEvict], ascending, n_evict of them).
+    int32_t in_place;
+    int32_t n_evict;
+    const int32_t* evicted;
 };
 
 struct AppendArgs {
@@ -484,6 +501,9 @@ constexpr int kScoreThreads = 256;
 // (block mode: fewer live blocks) stages exactly when the launch did, so a
 // kernel never stages into memory the launch did not reserve.
 constexpr int kSelChunkCap = 10240;
+// Steps evicting at most this many units select by block maxima and (token
+// mode) compact in place.
+constexpr int kFewEvict = 8;
 __host__ __device__ inline int select_chunk(int n_keys, int cl) { return (n_keys + cl - 1) / cl; }
 __host__ __device__ inline bool select_stages_keys(int launch_keys, int cl) {
     return select_chunk(launch_keys, cl) <= kSelChunkCap;

@@ -33,13 +33,14 @@ namespace kvev {
 namespace {
 
 template <int G, int NKV, bool VN>
-__global__ void __launch_bounds__(kRefreshThreads) score_refresh_kernel(const ScoreArgs a) {
+__global__ void __launch_bounds__(kScoreSegs * 32) score_refresh_kernel(const ScoreArgs a) {
     extern __shared__ float s_tab[];
-    __shared__ float s_c[kRefreshSegs][32], s_tot[kRefreshSegs][32];
+    __shared__ float s_c[kScoreSegs][32], s_tot[kScoreSegs][32];
     griddep_wait();
     griddep_release();
     score_tables<G, NKV, VN>(a, blockIdx.y, s_tab);
-    score_block<G, NKV, VN>(a, blockIdx.y, blockIdx.x, s_tab, s_c, s_tot);
+    score_block<G, NKV, VN, kScoreSegs, kScoreSegs>(a, blockIdx.y, blockIdx.x, s_tab, s_c,
+                                                    s_tot);
 }
 
 template <int G, bool VN>
@@ -108,7 +109,7 @@ cudaError_t launch_score(const ScoreArgs& a, int group, int* n_blocks, cudaStrea
                    : nullptr;
         if (!kern) return cudaErrorInvalidValue;
         return launch_pdl(reinterpret_cast<void (*)(ScoreArgs)>(kern), grid,
-                          dim3(kRefreshThreads), smem, s, a);
+                          dim3(kScoreSegs * 32), smem, s, a);
     }
     const int nb = (a.L + kScoreThreads - 1) / kScoreThreads;
     *n_blocks = nb;

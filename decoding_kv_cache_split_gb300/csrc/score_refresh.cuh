@@ -15,17 +15,16 @@ __device__ __forceinline__ uint32_t order_bits(float f) {
 }
 
 // Refresh steps: a CTA takes 32 consecutive tokens (a warp's lanes, so
-// every load instruction of a warp reads 512 contiguous bytes) and its 4
-// warps split the layers into 4 consecutive segments.  The EMA over a
-// segment is affine in the score it starts from, m_out = (1 - alpha)^n m_in
-// + c, so each warp folds its layers in order starting from 0 (the first
-// segment from the token's score itself) and the first warp chains the 4
-// segments: the layer order of the recurrence is kept and 4x more threads
-// share the loads.  The number of KV heads is a template parameter so a
+// every load instruction of a warp reads 512 contiguous bytes) and splits
+// the layers into 4 consecutive segments, one per warp (the fused step's
+// CTAs have the same 4 warps).  The EMA over a segment is affine in the
+// score it starts from, m_out = (1 - alpha)^n m_in + c, so each segment is
+// folded in order starting from 0 (the first from the token's score itself)
+// and the first warp chains the segments with (1 - alpha)^n from the host:
+// the layer order of the recurrence is kept and 4x more threads share the
+// loads.  The number of KV heads is a template parameter so a
 // layer's heads are an unrolled loop with no index arithmetic; the loads of
 // kLB layers are all issued before any is used.
-constexpr int kRefreshThreads = 128;
-constexpr int kRefreshSegs = kRefreshThreads / 32;
 
 // Shared-memory tables of sequence b (every thread of the CTA takes part;
 // ends with a barrier): [n_layers][NKV * G] log2-sum-exp, then [n_layers]
@@ -58,26 +57,25 @@ __device__ __forceinline__ void score_tables(const ScoreArgs& a, int b, float* s
     __syncthreads();
 }
 
-// The 32 tokens of block `blk` of sequence b (128 threads: 4 warps, one
-// layer segment each), with the tables of score_tables in s_lse.
-template <int G, int NKV, bool VN>
+// The 32 tokens of block `blk` of sequence b, folded in SEGS layer segments
+// by the CTA's WARPS warps (warp w takes segments w, w + WARPS, ...; the
+// arithmetic of a segment does not depend on which warp runs it), with the
+// tables of score_tables in s_lse.
+template <int G, int NKV, bool VN, int SEGS, int WARPS>
 __device__ __forceinline__ void score_block(const ScoreArgs& a, int b, int blk,
                                             const float* s_lse, float (*s_c)[32],
                                             float (*s_tot)[32]) {
+    static_assert(SEGS % WARPS == 0, "every warp takes the same number of segments");
     constexpr int V4 = G / 4;                               // float4 per (layer, KV head)
     constexpr int kLB = NKV * V4 >= 16 ? 1 : (16 / (NKV * V4) > 4 ? 4 : 16 / (NKV * V4));  // layers in flight
     constexpr int kPerLine = 128 / (G * 4);                 // tokens per 128-byte line
     const float* s_lw = s_lse + a.n_layers * NKV * G;
     const float* s_ivm = s_lw + a.n_layers;
     const int n_lay = a.n_layers;
-    const int seg = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i = blk * 32 + lane;
     const bool live = i < a.L;
-    const int la = seg * n_lay / kRefreshSegs, lb = (seg + 1) * n_lay / kRefreshSegs;
-
     const size_t si = (size_t)b * a.max_ctx + i;
-    float c = live && seg == 0 ? a.st.score[si] : 0.f;   // the first segment starts
-    float tot = 0.f;                                        // from the score itself
     const float oma = a.oma;
     const float inv_hq = 1.0f / (float)a.n_q;
     const size_t head_stride = (size_t)a.logit_ld * G;                  // one (layer, KV head) row
@@ -85,90 +83,97 @@ __device__ __forceinline__ void score_block(const ScoreArgs& a, int b, int blk,
     const float* base = a.logits + (size_t)b * NKV * head_stride + (size_t)i * G;
     const bool drop = i % kPerLine == 0 && i + kPerLine <= a.L;         // this thread drops lines
 
-    if (live) {
-        for (int l0 = la; l0 < lb; l0 += kLB) {
-            float4 xb[kLB][NKV][V4];
-            float vb[kLB][NKV];
+    float c = 0.f, tot = 0.f;
 #pragma unroll
-            for (int u = 0; u < kLB; ++u)                 // all loads of the batch first ...
+    for (int k = 0; k < SEGS / WARPS; ++k) {
+        const int seg = warp + k * WARPS;
+        const int la = seg * n_lay / SEGS, lb = (seg + 1) * n_lay / SEGS;
+        c = live && seg == 0 ? a.st.score[si] : 0.f;   // the first segment starts from
+        tot = 0.f;                                      // the score itself, the others at 0
+        if (live) {
+            for (int l0 = la; l0 < lb; l0 += kLB) {
+                float4 xb[kLB][NKV][V4];
+                float vb[kLB][NKV];
 #pragma unroll
-                for (int g = 0; g < NKV; ++g) {
+                for (int u = 0; u < kLB; ++u)                 // all loads of the batch first ...
 #pragma unroll
-                    for (int cc = 0; cc < V4; ++cc)
-                        xb[u][g][cc] = l0 + u < lb
-                            ? __ldcs(reinterpret_cast<const float4*>(
-                                  base + (size_t)(l0 + u) * layer_stride + g * head_stride) + cc)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-                    if constexpr (VN)
-                        vb[u][g] = l0 + u < lb
-                            ? __ldcs(a.vnorm + (((size_t)(l0 + u) * a.batch + b) * NKV + g) *
-                                                   a.logit_ld + i)
-                            : 0.f;
-                }
+                    for (int g = 0; g < NKV; ++g) {
 #pragma unroll
-            for (int u = 0; u < kLB; ++u) {               // ... then the layers in order
-                const int lr = l0 + u;
-                if (lr >= lb) break;
-                const float4* lg = reinterpret_cast<const float4*>(s_lse + lr * NKV * G);
-                float s = 0.f, sw = 0.f;   // head sum; with VNorm, weighted by the value norms
+                        for (int cc = 0; cc < V4; ++cc)
+                            xb[u][g][cc] = l0 + u < lb
+                                ? __ldcs(reinterpret_cast<const float4*>(
+                                      base + (size_t)(l0 + u) * layer_stride + g * head_stride) + cc)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                        if constexpr (VN)
+                            vb[u][g] = l0 + u < lb
+                                ? __ldcs(a.vnorm + (((size_t)(l0 + u) * a.batch + b) * NKV + g) *
+                                                       a.logit_ld + i)
+                                : 0.f;
+                    }
 #pragma unroll
-                for (int g = 0; g < NKV; ++g) {
-                    float sg = 0.f;
+                for (int u = 0; u < kLB; ++u) {               // ... then the layers in order
+                    const int lr = l0 + u;
+                    if (lr >= lb) break;
+                    const float4* lg = reinterpret_cast<const float4*>(s_lse + lr * NKV * G);
+                    float s = 0.f, sw = 0.f;   // head sum; with VNorm, weighted by the value norms
 #pragma unroll
-                    for (int cc = 0; cc < V4; ++cc) {
-                        const float4 x = xb[u][g][cc], e = lg[g * V4 + cc];
-                        const float p0 = fast_exp2(x.x - e.x), p1 = fast_exp2(x.y - e.y);
-                        const float p2 = fast_exp2(x.z - e.z), p3 = fast_exp2(x.w - e.w);
-                        if (a.dbg_probs) {
-                            float* dp = a.dbg_probs +
-                                        (((size_t)b * a.n_layers + lr) * a.n_q + g * G + 4 * cc) *
-                                            a.max_ctx + i;
-                            dp[0] = p0;
-                            dp[(size_t)a.max_ctx] = p1;
-                            dp[2 * (size_t)a.max_ctx] = p2;
-                            dp[3 * (size_t)a.max_ctx] = p3;
+                    for (int g = 0; g < NKV; ++g) {
+                        float sg = 0.f;
+#pragma unroll
+                        for (int cc = 0; cc < V4; ++cc) {
+                            const float4 x = xb[u][g][cc], e = lg[g * V4 + cc];
+                            const float p0 = fast_exp2(x.x - e.x), p1 = fast_exp2(x.y - e.y);
+                            const float p2 = fast_exp2(x.z - e.z), p3 = fast_exp2(x.w - e.w);
+                            if (a.dbg_probs) {
+                                float* dp = a.dbg_probs +
+                                            (((size_t)b * a.n_layers + lr) * a.n_q + g * G + 4 * cc) *
+                                                a.max_ctx + i;
+                                dp[0] = p0;
+                                dp[(size_t)a.max_ctx] = p1;
+                                dp[2 * (size_t)a.max_ctx] = p2;
+                                dp[3 * (size_t)a.max_ctx] = p3;
+                            }
+                            sg += (p0 + p1) + (p2 + p3);
                         }
-                        sg += (p0 + p1) + (p2 + p3);
+                        s += sg;
+                        if constexpr (VN) {
+                            const float iv = s_ivm[lr * NKV + g];
+                            sw = fmaf(iv >= 0.f ? vb[u][g] * iv : 1.0f, sg, sw);
+                        }
                     }
-                    s += sg;
-                    if constexpr (VN) {
-                        const float iv = s_ivm[lr * NKV + g];
-                        sw = fmaf(iv >= 0.f ? vb[u][g] * iv : 1.0f, sg, sw);
-                    }
-                }
-                // The logits are dead once read: drop their L2 lines without
-                // writing them back.  A 128-byte line holds kPerLine tokens of
-                // one (layer, KV head) row (rows start on a line), all loaded by
-                // this warp's load, which has completed since its values were
-                // just used (the discard takes `s` as an operand, so it cannot
-                // move above that use).  The line's first token's thread drops it.
-                if (drop) {
+                    // The logits are dead once read: drop their L2 lines without
+                    // writing them back.  A 128-byte line holds kPerLine tokens of
+                    // one (layer, KV head) row (rows start on a line), all loaded by
+                    // this warp's load, which has completed since its values were
+                    // just used (the discard takes `s` as an operand, so it cannot
+                    // move above that use).  The line's first token's thread drops it.
+                    if (drop) {
 #pragma unroll
-                    for (int g = 0; g < NKV; ++g)
-                        asm volatile("discard.global.L2 [%0], 128;" ::"l"(
-                                         base + (size_t)lr * layer_stride + g * head_stride),
-                                     "f"(s)
-                                     : "memory");
+                        for (int g = 0; g < NKV; ++g)
+                            asm volatile("discard.global.L2 [%0], 128;" ::"l"(
+                                             base + (size_t)lr * layer_stride + g * head_stride),
+                                         "f"(s)
+                                         : "memory");
+                    }
+                    tot += s;                  // the access test reads the plain attention
+                    float sl = VN ? sw : s;
+                    if (a.pool_mean) sl *= inv_hq;
+                    c = fmaf(a.alpha, sl * s_lw[lr], oma * c);
                 }
-                tot += s;                  // the access test reads the plain attention
-                float sl = VN ? sw : s;
-                if (a.pool_mean) sl *= inv_hq;
-                c = fmaf(a.alpha, sl * s_lw[lr], oma * c);
             }
         }
+        s_c[seg][lane] = c;
+        s_tot[seg][lane] = tot;
     }
-    s_c[seg][lane] = c;
-    s_tot[seg][lane] = tot;
     __syncthreads();
-    if (seg != 0 || !live) return;
+    if (warp != 0 || !live) return;
+    c = s_c[0][lane];
     // chain the segments in layer order: m <- (1 - alpha)^(layers of k) m + c_k
     float m = c;
     tot = s_tot[0][lane];
-    for (int k = 1; k < kRefreshSegs; ++k) {
-        const int ka = k * n_lay / kRefreshSegs, kb = (k + 1) * n_lay / kRefreshSegs;
-        float decay = 1.f;
-        for (int l = ka; l < kb; ++l) decay *= oma;
-        m = fmaf(decay, m, s_c[k][lane]);
+#pragma unroll
+    for (int k = 1; k < SEGS; ++k) {
+        m = fmaf(a.seg_decay[k], m, s_c[k][lane]);
         tot += s_tot[k][lane];
     }
     int t_ref = a.st.t_ref[si];

@@ -18,6 +18,12 @@
 // (all keys < T, and the first keys == T in slot order up to B) at its
 // offset, ascending.  The cluster barriers are hardware barriers
 // (barrier.cluster), there is no software spin-wait.
+//
+// Few evictions (L - B <= kFewEvict, the steady state of a decode, where one
+// new token arrives and one leaves): the first CTA alone takes the L - B
+// largest (key, slot) pairs by repeated block-wide maxima and keeps every
+// other slot, which is the same set as the radix path's (the B smallest
+// pairs, ties to the lower slot) at a fraction of its barriers.
 #include "kvev_internal.h"
 
 namespace kvev {
@@ -71,6 +77,79 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* red, int* total)
     return before;
 }
 
+// The L - B (<= kFewEvict) largest (key, slot) pairs leave, every other slot
+// is kept in ascending order.  Pairs are distinct (the slot breaks ties), so
+// each round's maximum below the previous round's is a new pair.
+__device__ void select_few(const uint32_t* gkeys, int L, int B, int32_t* ret,
+                           int32_t* n_retained, int32_t* first_moved, int32_t* evicted) {
+    __shared__ unsigned long long wmax[kSelWarps];
+    __shared__ int ev[kFewEvict];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = L - B;
+    unsigned long long prev = ~0ull;
+    for (int r = 0; r < E; ++r) {
+        // a thread without candidates offers (0, 0), the least pair: B >= 1
+        // leaves at least one candidate in every round, so the maximum is real
+        unsigned long long best = 0;
+        for (int i = tid; i < L; i += kSelThreads) {
+            const unsigned long long c = ((unsigned long long)__ldcg(gkeys + i) << 32) | (uint32_t)i;
+            if (c < prev && c > best) best = c;
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, m);
+            best = o > best ? o : best;
+        }
+        if (lane == 0) wmax[warp] = best;
+        __syncthreads();
+        if (warp == 0) {
+            static_assert(kSelWarps == 32, "one warp reduces the warps' maxima");
+            unsigned long long v = wmax[lane];
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) {
+                const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, m);
+                v = o > v ? o : v;
+            }
+            if (lane == 0) {
+                ev[r] = (int)(uint32_t)v;
+                wmax[0] = v;
+            }
+        }
+        __syncthreads();
+        prev = wmax[0];
+        __syncthreads();   // wmax is rewritten by the next round
+    }
+    // keep every slot but the E evicted ones, ascending
+    int gone_slot[kFewEvict];
+    int lowest = L;
+#pragma unroll
+    for (int k = 0; k < kFewEvict; ++k) {
+        gone_slot[k] = k < E ? ev[k] : L;
+        lowest = min(lowest, gone_slot[k]);
+    }
+    for (int i = tid; i < L; i += kSelThreads) {
+        int below = 0;
+        bool gone = false;
+#pragma unroll
+        for (int k = 0; k < kFewEvict; ++k) {
+            below += gone_slot[k] < i;
+            gone |= gone_slot[k] == i;
+        }
+        if (!gone) ret[i - below] = i;
+    }
+    if (evicted && tid < E) {   // ascending: thread k writes the k-th pick at its rank
+        const int mine = ev[tid];   // (ev is only read after the last barrier)
+        int rank = 0;
+#pragma unroll
+        for (int k = 0; k < kFewEvict; ++k) rank += gone_slot[k] < mine;
+        evicted[rank] = mine;
+    }
+    if (tid == 0) {
+        *n_retained = B;
+        if (first_moved) *first_moved = lowest;
+    }
+}
+
 template <int CL>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a) {
     extern __shared__ uint32_t s_keys[];             // this CTA's chunk (if it fits)
@@ -108,6 +187,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
                 if (a.first_moved) a.first_moved[b] = L;
             }
         }
+        return;
+    }
+    if (L - B <= kFewEvict) {   // the same for every CTA of the cluster: no exchange
+        if (rank == 0)
+            select_few(gkeys, L, B, ret, a.n_retained + b,
+                       a.first_moved ? a.first_moved + b : nullptr,
+                       a.evicted ? a.evicted + (size_t)b * kFewEvict : nullptr);
         return;
     }
     const int chunk = select_chunk(L, CL);
@@ -230,10 +316,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a)
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, int batch, int num_sms, cudaStream_t s) {
-    // Many sequences whose keys fit one CTA's shared memory: one CTA each (no
-    // cluster barriers or remote reads; the sequences fill the GPU).  Few
-    // sequences, or long ones: a cluster of kCl CTAs each.
-    const bool one = a.L <= kSelChunkCap && batch * kCl > num_sms;
+    // Many sequences whose keys fit one CTA's shared memory, or steps that
+    // evict few tokens (the maxima path runs on one CTA): one CTA each (no
+    // cluster barriers or remote reads).  Otherwise a cluster of kCl CTAs each.
+    const bool one = a.few || (a.L <= kSelChunkCap && batch * kCl > num_sms);
     const int cl = one ? 1 : kCl;
     SelectArgs args = a;
     args.staged = select_stages_keys(a.L, cl) ? 1 : 0;

@@ -96,13 +96,16 @@ typedef struct {
 
 /* The KV cache: two ping-pong buffers.  Each of k[0], k[1], v[0], v[1] is
  * [n_layers][batch][n_kv_heads][max_ctx][head_dim] bf16, 16-byte aligned.
- * Slots [0, len) of buffer `cur` are live.  kvev_step reads buffer `cur`,
- * appends into it, and when it evicts writes the compacted cache into the
- * other buffer and flips `cur`.  The other buffer is the library's between
- * steps: its leading rows still equal the live buffer's up to the slot the
- * previous compaction first moved, and the next compaction does not copy
- * them again, so the caller must not write into it during a run (from
- * kvev_init_state or kvev_import_state on). */
+ * Slots [0, len) of buffer `cur` are live.  kvev_step reads buffer `cur` and
+ * appends into it.  When it evicts more than 8 tokens per sequence it writes
+ * the compacted cache into the other buffer and flips `cur`; when it evicts
+ * 1 to 8 (the steady state: one token in, one out) it shifts the rows after
+ * the first evicted slot down within buffer `cur`, which stays live.  The
+ * other buffer is the library's between steps: its leading rows still equal
+ * the live buffer's up to the first slot a compaction since has moved, and
+ * the next out-of-place compaction does not copy them again, so the caller
+ * must not write into it during a run (from kvev_init_state or
+ * kvev_import_state on). */
 typedef struct {
     void* k[2];
     void* v[2];
@@ -265,7 +268,8 @@ kvev_status kvev_init_state(kvev_ctx* ctx, const kvev_state* state, void* stream
  *                 does not exceed the budget nothing is evicted and the list
  *                 is 0..len-1.
  *   n_retained    [batch] int32: entries written to retained_idx.
- * `cache` and `state` are read and updated (cache->cur may flip). */
+ * `cache` and `state` are read and updated (cache->cur flips when the step
+ * evicts more than 8 tokens per sequence). */
 kvev_status kvev_step(kvev_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                       kvev_cache* cache, const kvev_state* state, int64_t step, void* out,
                       int32_t* retained_idx, int32_t* n_retained, void* stream);

@@ -183,6 +183,21 @@ def test_edge_lengths(L0, budget):
     run_parity(wl, budget, 0.05, 0.001, 4)
 
 
+@pytest.mark.parametrize("excess", [1, 2, 5, 8, 9, 12])
+@pytest.mark.parametrize("beta", [0.0, 0.001])
+def test_few_evictions_and_all_ties(excess, beta):
+    """Step 1 evicts `excess` tokens (L0 + 1 - B): up to 8 go through the
+    selection's block-maxima path, more through the radix select, and every
+    later step evicts one.  beta = 0 makes every priority 0, so the tie rule
+    alone decides (the lowest B slots are kept) and the device must take the
+    oracle's set exactly at every step."""
+    L0 = 200
+    wl = Workload(Geometry(2, 8, 2, 64, 2), L0, seed=70 + excess, heavy=3)
+    totals = run_parity(wl, L0 + 1 - excess, 0.05, beta, 3)
+    if beta == 0.0:
+        assert totals["followed"] == 0 and totals["swaps"] == 0
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_eight_query_heads_per_kv_head(d):
     """Token mode with 8 query heads per KV head (16 q / 2 KV), both head
