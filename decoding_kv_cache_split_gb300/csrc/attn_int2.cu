@@ -31,9 +31,12 @@
 // per unit one 8-k-step MMA of q against a B operand whose columns are the
 // four key groups' zeros and scales gives every group's sum_c q_c z_c and
 // sum_c q_c s_c; per tile one MMA of p 2^10 (the scaling keeps its fp16 lo
-// part out of the subnormal range) against the tokens' value zeros and
-// scales (columns = channel groups) adds sum_i p_i z_ig and sum_i p_i s_ig to
-// an accumulator that the online softmax rescales like the output.
+// part out of the subnormal range) against the tokens' group centres
+// z + 1.5 s as fp16 hi and lo columns adds sum_i p_i (z_ig + 1.5 s_ig) to an
+// accumulator that the online softmax rescales like the output.  The centres
+// take both signs, so the tensor cores' accumulation, which drops low bits as
+// it adds, does not build up a one-signed error the way separate sums of p z
+// and p s do over a long row.
 #include <cuda_fp16.h>
 
 #include "kvev_internal.h"
@@ -183,8 +186,10 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
 
     uint32_t qa[KS][2];                      // Q * 2^96 (bf16x2) of the lane's head
     float2 o[NB];                            // hi or lo part of O[head][8j + 2t, +1] * 2^-31
-    // value-bias accumulator (fp16 MMA): row g, columns 2t, 2t+1; columns 0-3
-    // sum_i p_i z_ig, columns 4-7 sum_i p_i s_ig of channel group (column & 3)
+    // value-bias accumulator (fp16 MMA): row g, columns 2t, 2t+1; column c < 4
+    // sum_i p_i mid_ic, c >= 4 the same sum over what the fp16 mid_i(c-4)
+    // leaves, mid = z + 1.5 s the group's centre (centred terms: a tensor-core
+    // sum of one-signed terms, sum p z or sum p s, loses low bits every add)
     float2 vbc;
     float m_run = -INFINITY, l_run = 0.f;
     int64_t cur_row = -1;
@@ -193,16 +198,16 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
         float l = l_run;
         l += __shfl_xor_sync(kFull, l, 1);
         l += __shfl_xor_sync(kFull, l, 2);
-        // the head's value bias of group c: z part + 1.5 s part (hi + lo rows)
+        // the head's value bias of group c: the centre sum's hi + lo columns (and rows)
         float2 vt = add2(vbc, make_float2(__shfl_xor_sync(kFull, vbc.x, 16),
                                           __shfl_xor_sync(kFull, vbc.y, 16)));
         vt = mul2(vt, make_float2(1.0f / kPScale, 1.0f / kPScale));   // exact
         float vb[NG];
 #pragma unroll
         for (int c = 0; c < NG; ++c) {
-            const float zc = __shfl_sync(kFull, (c & 1) ? vt.y : vt.x, (lane & ~3) + (c >> 1));
-            const float sc2 = __shfl_sync(kFull, (c & 1) ? vt.y : vt.x, (lane & ~3) + 2 + (c >> 1));
-            vb[c] = fmaf(1.5f, sc2, zc);
+            const float mh = __shfl_sync(kFull, (c & 1) ? vt.y : vt.x, (lane & ~3) + (c >> 1));
+            const float ml = __shfl_sync(kFull, (c & 1) ? vt.y : vt.x, (lane & ~3) + 2 + (c >> 1));
+            vb[c] = mh + ml;
         }
         const int64_t slot = (int64_t)w + row;
         float* po = a.part_o + ((size_t)slot * G + head) * D;
@@ -277,8 +282,19 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
             const uint4* vc4 = reinterpret_cast<const uint4*>(buf + Lay::VC) + lane;
             const uint4* ks4 = reinterpret_cast<const uint4*>(buf + Lay::KS) + 4 * t;
             const uint4* vs4 = reinterpret_cast<const uint4*>(buf + Lay::VS) + 2 * t;
-            const uint32_t* vzs = reinterpret_cast<const uint32_t*>(
-                buf + (lo_row ? Lay::VS : Lay::VZ)) + t * (4 * NG / 2) + (g & 3);
+            // the value bias's B operand for tokens (2t, 2t+1) + 8 h of a tile:
+            // the fp16 hi (columns 0-3) or lo (columns 4-7) part of the centre
+            // z + 1.5 s (fp32) of channel group g & 3
+            const uint32_t* vz32 = reinterpret_cast<const uint32_t*>(buf + Lay::VZ) +
+                                   t * (4 * NG / 2) + (g & 3);
+            const uint32_t* vs32 = reinterpret_cast<const uint32_t*>(buf + Lay::VS) +
+                                   t * (4 * NG / 2) + (g & 3);
+            auto centre_reg = [&](int idx) -> uint32_t {
+                const float2 m = fma2(make_float2(1.5f, 1.5f), h2f(vs32[idx]), h2f(vz32[idx]));
+                const uint32_t hi = pack_f16x2(m.x, m.y);
+                const float2 hf = unpack_f16x2(hi);
+                return lo_row ? pack_f16x2(m.x - hf.x, m.y - hf.y) : hi;
+            };
             // key biases of the four groups: sum_c q_c z_c (columns 0-3) and
             // sum_c q_c s_c (columns 4-7), one fp16 MMA chain over the channels
             float2 kbc = make_float2(0.f, 0.f);
@@ -405,7 +421,8 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                             a0 = pack_f16x2(q01.x - f01.x, q01.y - f01.y);
                             a2 = pack_f16x2(q23.x - f23.x, q23.y - f23.y);
                         }
-                        mma_rows8_f16(vbc.x, vbc.y, a0, a2, vzs[ti * 32], vzs[ti * 32 + 4]);
+                        mma_rows8_f16(vbc.x, vbc.y, a0, a2, centre_reg(ti * 32),
+                                      centre_reg(ti * 32 + 4));
                     }
                     const float2 ps01 = mul2(p01, make_float2(kAScale, kAScale));
                     const float2 ps23 = mul2(p23, make_float2(kAScale, kAScale));

@@ -97,6 +97,10 @@ def compare(tp, P, seqs, b, t, q, kn, vn, stats, check_windows=None, lir=None):
     out = tp.out[b].cpu().numpy().astype(np.float64)
     err = np.abs(out - res["out"]).max(-1) / np.abs(res["out"]).max(-1)
     assert err.max() <= OUT_RTOL, f"step {t} seq {b}: output rel err {err.max():.2e}"
+    if float(err.max()) > stats["out_rel"]:   # where the largest error sits
+        layer, head = np.unravel_index(int(np.argmax(err)), err.shape)
+        stats["out_rel_at"] = (t, int(layer), int(head),
+                               float(np.abs(res["out"][layer, head]).max()))
     stats["out_rel"] = max(stats["out_rel"], float(err.max()))
     sc = tp.score[b].cpu().numpy().astype(np.float64)
     for wid, m in res["m"].items():

@@ -131,3 +131,23 @@ def test_bias_terms_from_fp16_products_match_the_dequantized_keys():
     big = p >= 2.0 ** -14
     assert np.all(err[big] <= 2.0 ** -21 * p[big].astype(np.float64))
     assert np.all(err[~big] <= 2.0 ** -35)
+
+
+def test_value_bias_centres_as_fp16_hi_and_lo():
+    """The value bias enters the fp16 tensor-core products as each token
+    group's centre z + 1.5 s (fp32) split into an fp16 hi part and the fp16
+    remainder: the pair keeps the centre to 2^-22 relative for centres down
+    to 2^-10, and the centres take both signs around 0 for zero-mean values,
+    unlike z (the group minimum) and s, whose sums only grow."""
+    rng = np.random.default_rng(4)
+    v = rng.standard_normal((20000, 32)).astype(F)
+    zero = v.min(axis=1).astype(np.float16).astype(F)
+    scale = ((v.max(axis=1) - v.min(axis=1)) / F(3)).astype(np.float16).astype(F)
+    mid = (F(1.5) * scale + zero).astype(F)
+    hi, lo = f16_split(mid)
+    err = np.abs(hi.astype(np.float64) + lo.astype(np.float64) - mid.astype(np.float64))
+    big = np.abs(mid) >= 2.0 ** -10
+    assert np.all(err[big] <= 2.0 ** -22 * np.abs(mid[big]).astype(np.float64))
+    assert np.all(err[~big] <= 2.0 ** -33)
+    assert np.all(zero < 0) and np.all(scale > 0)
+    assert 0.3 < np.mean(mid > 0) < 0.7
