@@ -2,22 +2,29 @@
 // Sec. 4.1: the accessible keys and values include the dequantized INT2
 // windows), with the dequantization folded into the tensor-core products.
 //
-// A key is k_c = code_c * s_c + z_c = s_c (code_c - 1.5) + (z_c + 1.5 s_c)
-// with (s, z) per channel over a 32-token group, so within a group
-//     q . k = sum_c (q_c s_c)(code_c - 1.5) + sum_c q_c (z_c + 1.5 s_c) :
-// the A operand is q * s (bf16 hi + lo), the B operand the centred codes,
-// plus a per-head bias.  A value is v_c = s_g (code_c - 1.5) + (z_g + 1.5 s_g)
+// A key is k_c = code_c * s_c + z_c with (s, z) per channel over a 32-token
+// group, so within a group
+//     q . k = sum_c (q_c s_c) code_c + sum_c q_c z_c :
+// the A operand is q * s (bf16 hi + lo), the B operand the codes, plus a
+// per-head bias (q has both signs and a logit sums 128 channels afresh, so
+// the codes need no centring here).  A value is v_c = s_g (code_c - 1.5) + (z_g + 1.5 s_g)
 // with (s, z) per token over a 32-channel group g, so
 //     sum_i p_i v_ic = sum_i (p_i s_ig)(code_ic - 1.5) + sum_i p_i (z_ig + 1.5 s_ig) :
 // per channel group the A operand is p * s (hi + lo), B the centred codes,
 // plus a per-head, per-group bias carried through the online softmax like
-// the output.  Centring keeps both sums near the size of the result.
+// the output.  Centring keeps the value sums, which run over whole rows,
+// near the size of the result.
 //
-// The ledger stores each code as a sign and a magnitude bit at the bit
-// positions of its tensor-core register (see LedgerLayout): one rotate and
-// one mask-and-OR turn a word into a bf16 pair of exact subnormals
-// (2 code - 3) * 2^-128, and the A operands carry a factor 2^96, so the
-// products are the centred terms times 2^-31, rescaled once per row.
+// The ledger stores each key code as a plain 2-bit number at the bit
+// positions of its tensor-core register (see LedgerLayout): a word shifted by
+// 0, 6 or 12 and masked gives a bf16 pair of exact subnormals c 2^(2 k)
+// 2^-133, k the register's scale class, two shifts and eight masks per word;
+// the A operand of k-step s carries 2^(96 - 2 k(s)), so every key product is
+// code * q s * 2^-37.  Each value code is a sign and a magnitude bit at the
+// positions of its register: one rotate and one mask-and-OR turn a word into
+// a bf16 pair of exact subnormals (2 c - 3) * 2^-128; the value A operands
+// carry 2^96, so the output products are the centred terms times 2^-31,
+// rescaled once per row.
 //
 // Work: every (layer, sequence, KV head) row has `slots` units, one INT2
 // window each (past the sequence's INT2 list a unit is empty); warps take
@@ -29,8 +36,8 @@
 // The bias terms run on the tensor cores too, as fp16 products (fp16 scale and
 // zero times q or p split into fp16 hi + lo rows: exact products, fp32 sums):
 // per unit one 8-k-step MMA of q against a B operand whose columns are the
-// four key groups' zeros and scales gives every group's sum_c q_c z_c and
-// sum_c q_c s_c; per tile one MMA of p 2^10 (the scaling keeps its fp16 lo
+// four key groups' zeros (and scales, unused) gives every group's
+// sum_c q_c z_c; per tile one MMA of p 2^10 (the scaling keeps its fp16 lo
 // part out of the subnormal range) against the tokens' group centres
 // z + 1.5 s as fp16 hi and lo columns adds sum_i p_i (z_ig + 1.5 s_ig) to an
 // accumulator that the online softmax rescales like the output.  The centres
@@ -48,8 +55,9 @@ namespace {
 constexpr int kI2Warps = 4;
 constexpr int kQhBytes = 32 * 16 * 4;   // per warp: q as fp16 hi / lo operand pairs
 constexpr unsigned kFull = 0xffffffffu;
-constexpr float kAScale = 0x1p96f;    // A operands carry 2^96
-constexpr float kProdScale = 0x1p31f; // undoes 2^96 * 2^-127 (code - 1.5 in the B operand)
+constexpr float kAScale = 0x1p96f;    // A operands carry 2^96 (keys: divided by the class scale)
+constexpr float kProdScale = 0x1p31f; // undoes 2^96 * 2^-127 (code - 1.5 in a value B operand)
+constexpr float kKeyScale = 0x1p37f;  // undoes 2^96 * 2^-133 (a code in a key B operand)
 constexpr float kPScale = 0x1p10f;    // p in the value-bias MMA: its fp16 lo part stays normal
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -64,7 +72,12 @@ __device__ __forceinline__ void cp_async_wait_prior() {   // all but the newest 
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
-// Register `slot` of a ledger code word: the bf16 pair (2 c - 3) * 2^-128.
+// Register of field f of a key code word: the bf16 pair c 2^(2 (f % 3)) 2^-133.
+// f is a compile-time constant in every use; the shifts of a word are shared.
+__device__ __forceinline__ uint32_t field_reg(uint32_t w, int f) {
+    return (w >> (6 * (f / 3))) & (0x00030003u << (2 * (f % 3)));
+}
+// Register `slot` of a value code word: the bf16 pair (2 c - 3) * 2^-128.
 __device__ __forceinline__ uint32_t code_reg(uint32_t w, int slot) {
     const uint32_t x = slot == 0 ? w : __funnelshift_r(w, w, 2 * slot);
     return (x & 0x80408040u) | 0x00200020u;
@@ -184,13 +197,13 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
         return pack_bf16x2(r.x, r.y);
     };
 
-    uint32_t qa[KS][2];                      // Q * 2^96 (bf16x2) of the lane's head
+    uint32_t qa[KS][2];                      // Q * 2^(96 - 2 class(s)) (bf16x2) of the lane's head
     float2 o[NB];                            // hi or lo part of O[head][8j + 2t, +1] * 2^-31
     // value-bias accumulator (fp16 MMA): row g, columns 2t, 2t+1; column c < 4
     // sum_i p_i mid_ic, c >= 4 the same sum over what the fp16 mid_i(c-4)
     // leaves, mid = z + 1.5 s the group's centre (centred terms: a tensor-core
     // sum of one-signed terms, sum p z or sum p s, loses low bits every add)
-    float2 vbc;
+    float2 vbc = make_float2(0.f, 0.f);
     float m_run = -INFINITY, l_run = 0.f;
     int64_t cur_row = -1;
 
@@ -225,7 +238,7 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
             pml[1] = l;
         }
     };
-    const float acc_scale = a.q_scale * kProdScale;   // logits from the code products
+    const float acc_scale = a.q_scale * kKeyScale;    // logits from the code products
 
     UnitPos cur = locate(x0), nxt = cur;
     const unsigned char* src = nullptr;
@@ -257,9 +270,11 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {   // dims 16s + 8h + 2t, +1 (exact scaling)
                     const uint32_t qw = qrow[8 * s + 4 * h + t];
-                    qa[s][h] = pack_bf16x2(bf16_lo(qw) * kAScale, bf16_hi(qw) * kAScale);
                     // fp16 hi (rows 0-3) or what it leaves (rows 4-7) of the same q
                     const float q0 = bf16_lo(qw), q1 = bf16_hi(qw);
+                    // the key-side A operand of k-step s carries 2^(96 - 2 class(s))
+                    const float ka = s < 3 ? kAScale : s < 6 ? 0x1p94f : 0x1p92f;
+                    qa[s][h] = pack_bf16x2(q0 * ka, q1 * ka);
                     const uint32_t hw = pack_f16x2(q0, q1);
                     const float2 hf = unpack_f16x2(hw);
                     qhw[s][h] = lo_row ? pack_f16x2(q0 - hf.x, q1 - hf.y) : hw;
@@ -295,8 +310,8 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                 const float2 hf = unpack_f16x2(hi);
                 return lo_row ? pack_f16x2(m.x - hf.x, m.y - hf.y) : hi;
             };
-            // key biases of the four groups: sum_c q_c z_c (columns 0-3) and
-            // sum_c q_c s_c (columns 4-7), one fp16 MMA chain over the channels
+            // key biases of the four groups: sum_c q_c z_c (columns 0-3; columns
+            // 4-7 take the scales and are not read), one fp16 MMA chain
             float2 kbc = make_float2(0.f, 0.f);
             {
                 const uint4* zs4 = reinterpret_cast<const uint4*>(buf + (lo_row ? Lay::KS : Lay::KZ)) +
@@ -311,8 +326,8 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                                             __shfl_xor_sync(kFull, kbc.y, 16)));
             }
             for (int grp = 0; grp < kTierW / kQGroup; ++grp) {
-                // A' = q * s * 2^96 of this group's key scales (the lane's hi or
-                // lo part); the key bias sum_c q_c (z_c + 1.5 s_c) of the head
+                // A' = q * s * 2^(96 - 2 class(s)) of this group's key scales (the
+                // lane's hi or lo part); the key bias sum_c q_c z_c of the head
                 uint32_t af[KS][2];
 #pragma unroll
                 for (int s2 = 0; s2 < KS / 2; ++s2) {
@@ -327,10 +342,7 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                     }
                 }
                 const float kz = __shfl_sync(kFull, (grp & 1) ? kbc.y : kbc.x, (lane & ~3) + (grp >> 1));
-                const float ks_ = __shfl_sync(kFull, (grp & 1) ? kbc.y : kbc.x,
-                                              (lane & ~3) + 2 + (grp >> 1));
-                const float kb = fmaf(1.5f, ks_, kz) * a.q_scale;
-#pragma unroll
+                const float kb = kz * a.q_scale;   // the head's key bias sum_c q_c z_c
                 // ---- S = A' codes + bias for both tiles of the group (two 8-token
                 //      blocks each; even and odd k-steps in separate accumulators):
                 //      their 32 MMAs are independent of the softmax below
@@ -346,9 +358,8 @@ __global__ void __launch_bounds__(kI2Warps * 32) attn_int2_kernel(const Int2Args
                     for (int s = 0; s < KS; ++s)
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
-                            const int slot = 4 * (s & 1) + 2 * i;
-                            const uint32_t b0 = code_reg(kw[s >> 1], slot);
-                            const uint32_t b1 = code_reg(kw[s >> 1], slot + 1);
+                            const uint32_t b0 = field_reg(kw[2 * i], Lay::key_field(s));
+                            const uint32_t b1 = field_reg(kw[2 * i + 1], Lay::key_field(s));
                             mma_rows8(acc[s & 1][i][0], acc[s & 1][i][1], af[s][0], af[s][1], b0, b1);
                         }
 #pragma unroll

@@ -299,21 +299,30 @@ constexpr int kTierRouteCap = 2048;         // windows per sequence the routing 
 // arranged for the INT2 attention kernel's tensor-core fragments (m16n8k16,
 // lane = 4 g + t): per 16-token tile ti, lane L's D/32 code words sit at
 // words ti * D + L * (D / 32) .. + D / 32 - 1 of kc / vc, one 16-byte load.
-// A word carries 8 operand registers (slot 0..7) of two codes each (half e);
-// a register is the word rotated right by 2 slot, masked to its sign bits 15,
-// 31 and magnitude bits 6, 22, with bits 5, 21 set: the bf16 pair
-// (2 c - 3) * 2^-128 (exact subnormals; sign = c <= 1, magnitude 3 for c = 0
-// or 3, else 1).
-//   kc: key code (token 16 ti + 8 i + g, channel 16 s + 8 h + 2 t + e) in
-//       register 4 s + 2 i + h of lane 4 g + t (the B operand of S = Q K^T);
-//   vc: value code (token 16 ti + 8 h + 2 t + e, channel 8 j + g) in register
-//       2 j + h of lane 4 g + t (the B operand of O += P V);
+//   kc: a key word has 8 fields f; a field holds two codes (half e) as plain
+//       2-bit numbers at bits 2 f + 16 e, + 1.  Field f is an operand register
+//       after a right shift by 6 (f / 3) and a mask to bits 2 (f % 3), + 1 of
+//       each half: the bf16 pair c 2^(2 (f % 3)) 2^-133 (exact subnormals),
+//       two shifts and eight masks per word.  Key code (token 16 ti + 8 i + g,
+//       channel 16 s + 8 h + 2 t + e) sits in field 3 (s % 3) + s / 3 of word
+//       2 i + h of lane 4 g + t, so the four registers of k-step s share the
+//       scale class s / 3 that the A operand undoes (the B operand of
+//       S = Q K^T);
+//   vc: a value word carries 8 operand registers (slot 0..7) of two codes
+//       each (half e); a register is the word rotated right by 2 slot, masked
+//       to its sign bits 15, 31 and magnitude bits 6, 22, with bits 5, 21 set:
+//       the bf16 pair (2 c - 3) * 2^-128 (exact subnormals; sign = c <= 1,
+//       magnitude 3 for c = 0 or 3, else 1).  Value code (token 16 ti + 8 h +
+//       2 t + e, channel 8 j + g) sits in register 2 j + h of lane 4 g + t (the
+//       B operand of O += P V; centred codes keep the output sums, which run
+//       over whole rows, near the size of the result);
 //   ks, kz: fp16 key scale / zero of (group, channel 16 s + 8 h + 2 t + e) at
 //       group * D + t * D / 4 + 4 s + 2 h + e (a lane's 32 channels together);
 //   vs, vz: fp16 value scale / zero of (token 16 ti + 8 h + 2 t + e, channel
 //       group cg) at ti * 16 G + t * 4 G + h * 2 G + 2 cg + e, G = D / 32.
 template <int D>
 struct LedgerLayout {
+    static_assert(D == 128, "the key fields cover 8 k-steps");
     static constexpr int NG = D / kQGroup;   // channel groups of a value row
     static constexpr int KC = 0;
     static constexpr int KS = KC + kTierW * D / 4;
@@ -323,9 +332,13 @@ struct LedgerLayout {
     static constexpr int VZ = VS + kTierW * NG * 2;
     static constexpr int BYTES = VZ + kTierW * NG * 2;
     static constexpr int WORDS_PER_LANE = D / 32;
-    // word of kc / vc and the bit of the sign (the magnitude bit is 9 below)
-    __host__ __device__ static int code_word(int ti, int lane, int reg) {
-        return ti * D + lane * WORDS_PER_LANE + (reg >> 3);
+    // key fields: k-step s -> field, and the low bit of a field's half e (the
+    // code's high bit is the next)
+    __host__ __device__ static constexpr int key_field(int s) { return 3 * (s % 3) + s / 3; }
+    __host__ __device__ static constexpr int key_bit(int field, int e) { return 2 * field + 16 * e; }
+    // value words: the bit of the sign (the magnitude bit is 9 below)
+    __host__ __device__ static int code_word(int ti, int lane, int w) {
+        return ti * D + lane * WORDS_PER_LANE + w;
     }
     __host__ __device__ static int sign_bit(int reg, int e) {
         return (15 + 16 * e + 2 * (reg & 7)) & 31;
@@ -333,20 +346,21 @@ struct LedgerLayout {
     __host__ __device__ static int mag_bit(int reg, int e) {
         return (6 + 16 * e + 2 * (reg & 7)) & 31;
     }
-    // key code (token in window, channel) -> word, register half
-    __host__ __device__ static void key_place(int tok, int c, int* word, int* reg, int* e) {
+    // key code (token in window, channel) -> word, field, half
+    __host__ __device__ static void key_place(int tok, int c, int* word, int* field, int* e) {
         const int ti = tok >> 4, i = (tok >> 3) & 1, g = tok & 7;
         const int s = c >> 4, h = (c >> 3) & 1, t = (c & 7) >> 1;
-        *reg = 4 * s + 2 * i + h;
+        *field = key_field(s);
         *e = c & 1;
-        *word = code_word(ti, 4 * g + t, *reg);
+        *word = code_word(ti, 4 * g + t, 2 * i + h);
     }
+    // value code (token in window, channel) -> word, register, half
     __host__ __device__ static void value_place(int tok, int c, int* word, int* reg, int* e) {
         const int ti = tok >> 4, h = (tok >> 3) & 1, t = (tok & 7) >> 1;
         const int j = c >> 3, g = c & 7;
         *reg = 2 * j + h;
         *e = tok & 1;
-        *word = code_word(ti, 4 * g + t, *reg);
+        *word = code_word(ti, 4 * g + t, *reg >> 3);
     }
     __host__ __device__ static int key_scale_index(int grp, int c) {
         return grp * D + ((c & 7) >> 1) * (D / 4) + 4 * (c >> 4) + 2 * ((c >> 3) & 1) + (c & 1);

@@ -412,23 +412,26 @@ __device__ __forceinline__ void item_at(const int32_t* n, int batch, int LG, int
     *lg = (int)(it % LG);
 }
 
-// Sign / magnitude bits (bit 0: code <= 1, bit 1: code 0 or 3) of the code
-// of x in a group with fp16 zero z and scale sc > 0, where the code is rint
-// of the correctly rounded fp32 quotient y = (x - z) / sc, clamped to
-// [0, 3]: code <= 1 iff y < 1.5, code 0 iff y <= 0.5, code 3 iff y > 2.5
-// (rint rounds ties to even).  The quotient is first taken as (x - z) * r
-// with r = 1 / sc correctly rounded: the two roundings put it within
-// 3 * 2^-24 relative of the exact quotient, so within 2^-19 of y while it is
-// below 8 in magnitude; only within 2^-16 of a threshold can it fall on the
-// other side of one than y does, and there the quotient is divided out
-// exactly (out of line: the rare path stays out of the unrolled loops).
+// The code of x in a group with fp16 zero z and scale sc > 0: rint of the
+// correctly rounded fp32 quotient y = (x - z) / sc, clamped to [0, 3], i.e.
+// (y > 0.5) + (y >= 1.5) + (y > 2.5) (rint rounds ties to even).  The
+// quotient is first taken as (x - z) * r with r = 1 / sc correctly rounded:
+// the two roundings put it within 3 * 2^-24 relative of the exact quotient,
+// so within 2^-19 of y while it is below 8 in magnitude; only within 2^-16
+// of a threshold can it fall on the other side of one than y does, and there
+// the quotient is divided out exactly (out of line: the rare path stays out
+// of the unrolled loops).
 __device__ __noinline__ float exact_quotient(float d, float sc) { return __fdiv_rn(d, sc); }
-__device__ __forceinline__ uint32_t int2_bits(float x, float z, float sc, float r) {
+__device__ __forceinline__ uint32_t int2_code(float x, float z, float sc, float r) {
     const float d = __fsub_rn(x, z);
     float y = __fmul_rn(d, r);
     const float dc = fabsf(y - 1.5f);
     if (dc <= 0x1p-16f || fabsf(dc - 1.f) <= 0x1p-16f) y = exact_quotient(d, sc);
-    return (uint32_t)(y < 1.5f) | ((uint32_t)(y <= 0.5f || y > 2.5f) << 1);
+    return (uint32_t)(y > 0.5f) + (uint32_t)(y >= 1.5f) + (uint32_t)(y > 2.5f);
+}
+// A value code's sign / magnitude bits: bit 0 code <= 1, bit 1 code 0 or 3.
+__device__ __forceinline__ uint32_t sign_mag(uint32_t c) {
+    return (uint32_t)(c <= 1u) | ((uint32_t)(c == 0u || c == 3u) << 1);
 }
 // A pair of codes as bytes (bits 0, 1: first code; 8, 9: second) -> the
 // pair's sign bits at 15, 31 and magnitude bits at 6, 22 (a multiply places
@@ -441,11 +444,13 @@ __device__ __forceinline__ uint32_t pair_reg_bits(uint32_t x) {
 // Quantization of one half (keys or values) of a (window, layer, KV head)
 // item: the window's 128 rows are staged in shared memory (rows padded by 16
 // bytes so row-strided reads spread over the banks).  Keys: a thread per
-// channel pair and 32-token group (min / max on bf16 pairs); values: a
-// thread per token and 32-channel group.  Each thread turns its codes into
-// the sign / magnitude bits of their ledger registers, and the threads
-// whose bits share a ledger word OR them together with two shuffles; one of
-// them stores the word.
+// channel pair and 32-token group (min / max on bf16 pairs), the 8 threads
+// whose codes share a ledger word in consecutive lanes; each places its
+// codes in their fields and the 8 OR them together with three shuffles.
+// Values: a thread per token and 32-channel group; each turns its codes into
+// the sign / magnitude bits of their ledger registers, and the threads whose
+// bits share a word OR them together with two shuffles.  One thread of a
+// word stores it.
 constexpr int kQuantThreads = 256;
 constexpr int kRowPad = 8;     // bf16 elements of padding per staged row
 
@@ -454,7 +459,7 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
                                                                       int max_items) {
     using Lay = LedgerLayout<D>;
     static_assert(D == 128, "ledger registers are laid out for head_dim 128");
-    constexpr int PW = kTierW / kTile, NG = Lay::NG, WPL = Lay::WORDS_PER_LANE;
+    constexpr int PW = kTierW / kTile, WPL = Lay::WORDS_PER_LANE;
     constexpr int XS = D + kRowPad;                 // staged row stride (elements)
     extern __shared__ __align__(16) unsigned char qsm[];
     __nv_bfloat16* xt = reinterpret_cast<__nv_bfloat16*>(qsm);            // [128][XS]
@@ -490,8 +495,11 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
         __syncthreads();
         uint32_t* words = reinterpret_cast<uint32_t*>(led + (kv ? Lay::VC : Lay::KC));
         if (kv == 0) {
-            // keys: channels 2p, 2p + 1 over group grp (tokens 32 grp .. + 31)
-            const int p = 32 * (warp & 1) + lane, grp = warp >> 1;
+            // keys: channels c = 16 s + 8 h + 2 t, c + 1 over group grp (tokens
+            // 32 grp .. + 31); lane = 8 t + s, h = warp & 1, so the 8 threads of
+            // a word (its 8 k-steps s) are consecutive lanes
+            const int s8 = lane & 7, t = lane >> 3, h = warp & 1, grp = warp >> 1;
+            const int p = 8 * s8 + 4 * h + t;   // channel pair 2p, 2p + 1
             const __nv_bfloat162* col =
                 reinterpret_cast<const __nv_bfloat162*>(xt + grp * kQGroup * XS) + p;
             __nv_bfloat162 mn2 = col[0], mx2 = col[0];
@@ -510,29 +518,24 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
             reinterpret_cast<__half2*>(led + Lay::KZ)[k / 2] = z16;
             const float r0 = sc.x == 0.f ? 0.f : __frcp_rn(sc.x);
             const float r1 = sc.y == 0.f ? 0.f : __frcp_rn(sc.y);
-            // register 4 s + 2 i + h of lane 4 gg + t (token 8 i + gg of its tile):
-            // word wq = s / 2, slot 4 (s & 1) + 2 i + h; the 4 threads p with the
-            // same t and s / 2 (lanes xor 4, xor 8) fill one word's 8 slots
-            const int t = p & 3, s4 = p >> 3, h = (p >> 2) & 1;
-            const int rot0 = 2 * (4 * (s4 & 1) + h);
+            const int b0 = Lay::key_bit(Lay::key_field(s8), 0);   // field of k-step s8
+            // token 8 i + gg of tile 2 grp + tt: word 2 i + h of lane 4 gg + t
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
-                for (int gg = 0; gg < 8; ++gg) {
-                    uint32_t word = 0;
+                for (int gg = 0; gg < 8; ++gg)
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
                         const float2 x = __bfloat1622float2(col[(16 * tt + 8 * i + gg) * (XS / 2)]);
-                        const uint32_t b0 = sc.x == 0.f ? 3u : int2_bits(x.x, z.x, sc.x, r0);
-                        const uint32_t b1 = sc.y == 0.f ? 3u : int2_bits(x.y, z.y, sc.y, r1);
-                        const uint32_t bits = pair_reg_bits(b0 | (b1 << 8));
-                        word |= __funnelshift_l(bits, bits, rot0 + 4 * i);
+                        const uint32_t c0 = sc.x == 0.f ? 0u : int2_code(x.x, z.x, sc.x, r0);
+                        const uint32_t c1 = sc.y == 0.f ? 0u : int2_code(x.y, z.y, sc.y, r1);
+                        uint32_t word = (c0 << b0) | (c1 << (b0 + 16));
+                        word |= __shfl_xor_sync(0xffffffffu, word, 1);
+                        word |= __shfl_xor_sync(0xffffffffu, word, 2);
+                        word |= __shfl_xor_sync(0xffffffffu, word, 4);
+                        if (s8 == 0)
+                            words[(2 * grp + tt) * D + (4 * gg + t) * WPL + 2 * i + h] = word;
                     }
-                    word |= __shfl_xor_sync(0xffffffffu, word, 4);
-                    word |= __shfl_xor_sync(0xffffffffu, word, 8);
-                    if ((lane & 12) == 0)
-                        words[(2 * grp + tt) * D + (4 * gg + t) * WPL + (s4 >> 1)] = word;
-                }
         } else {
             // values: token tok over channel groups cg and cg + 2; the codes of
             // channel 8 j + gg sit in register 2 j + h of lane 4 gg + t, half e,
@@ -577,7 +580,8 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
                     for (int jj = 0; jj < 4; ++jj) {
                         const int c = 8 * jj + gg;
                         const float x = (c & 1) ? __high2float(v2[c >> 1]) : __low2float(v2[c >> 1]);
-                        const uint32_t bits = pair_reg_bits((sc == 0.f ? 3u : int2_bits(x, z, sc, r)) << (8 * e2));
+                        const uint32_t code = sc == 0.f ? 0u : int2_code(x, z, sc, r);
+                        const uint32_t bits = pair_reg_bits(sign_mag(code) << (8 * e2));
                         word |= __funnelshift_l(bits, bits, 2 * (2 * jj + hh));
                     }
                     word |= __shfl_xor_sync(0xffffffffu, word, 1);
@@ -594,11 +598,11 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
 // Promotion of one half (keys or values) of a (window, layer, KV head) item:
 // the half's ledger codes and scales are staged in shared memory, then each
 // thread walks the two pages of one channel pair and a quarter of the window
-// (for keys a 32-token group, so one scale pair), turning each ledger
-// register into its two codes and writing
-// code * scale + zero rounded to bf16 (warps store 128 contiguous bytes of
-// a page row).  A register's bf16 pair is (2 c - 3) * 2^-128 (exact
-// subnormals), so c = v * 2^127 + 1.5 exactly in fp32.
+// (for keys a 32-token group, so one scale pair), reading each code (keys:
+// from its field; values: a register's bf16 pair (2 c - 3) * 2^-128, exact
+// subnormals, so c = v * 2^127 + 1.5 exactly in fp32) and writing
+// code * scale + zero rounded to bf16 (warps store 128 contiguous bytes of a
+// page row).
 constexpr int kPromThreads = 256;
 
 __device__ __forceinline__ float2 reg_codes(uint32_t x) {   // x rotated to slot 0
@@ -649,20 +653,19 @@ __global__ void __launch_bounds__(kPromThreads) tier_promote_kernel(const TierAr
             uint32_t* dst = pool + ((((int64_t)page * a.n_layers + l) * a.n_kv + g) * kTile) * D / 2 + p;
             const uint32_t* cwt = cw + (2 * q4 + pg) * D;   // code words of this 16-token tile
             if (kv == 0) {
-                // keys: channels 2p, 2p + 1 of token 16 (2 q4 + pg) + r: register
-                // 4 s + 2 i + h of lane 4 (r & 7) + t
-                const int t = p & 3, s4 = p >> 3, h = (p >> 2) & 1;
+                // keys: channels 2p, 2p + 1 (one field, halves 0 and 1) of the
+                // tokens 16 (2 q4 + pg) + r, read from their ledger fields
                 const int k = Lay::key_scale_index(q4, 2 * p);
                 const float2 sf = __half22float2(sc2[k / 2]), zf = __half22float2(zc2[k / 2]);
-                const uint32_t* cwl = cwt + t * WPL + (s4 >> 1);
-                const int rot0 = 2 * (4 * (s4 & 1) + h);
 #pragma unroll
                 for (int r = 0; r < kTile; ++r) {
-                    const int i = r >> 3;
-                    const uint32_t wd = cwl[4 * (r & 7) * WPL];
-                    const float2 c = reg_codes(__funnelshift_r(wd, wd, rot0 + 4 * i));
-                    const __nv_bfloat162 bb = __floats2bfloat162_rn(fmaf(c.x, sf.x, zf.x),
-                                                                    fmaf(c.y, sf.y, zf.y));
+                    int word, field, half;
+                    Lay::key_place(16 * (2 * q4 + pg) + r, 2 * p, &word, &field, &half);
+                    const uint32_t wd = cw[word];
+                    const float c0 = (float)((wd >> Lay::key_bit(field, 0)) & 3u);
+                    const float c1 = (float)((wd >> Lay::key_bit(field, 1)) & 3u);
+                    const __nv_bfloat162 bb = __floats2bfloat162_rn(fmaf(c0, sf.x, zf.x),
+                                                                    fmaf(c1, sf.y, zf.y));
                     dst[r * (D / 2)] = *reinterpret_cast<const uint32_t*>(&bb);
                 }
             } else {

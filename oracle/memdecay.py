@@ -111,8 +111,8 @@ def retention(P: MDParams, region, a, t_ref, t: int) -> np.ndarray:
 
 
 def evict_pages(S, n_tok, pinned, budget: int):
-    """Algorithm 1 lines 5-9: pop non-pinned pages of minimum score (ties:
-    higher index first) until the token count is within the budget.
+    """Algorithm 1's eviction loop: pop non-pinned pages of minimum score
+    (ties: higher index first) until the token count is within the budget.
     Returns the evicted page indexes in eviction order."""
     total = int(sum(n_tok))
     heap = [(float(S[j]), -j) for j in range(len(S)) if not pinned[j]]

@@ -11,8 +11,8 @@ int main() {
     for (int tok = 0; tok < 128; ++tok)
         for (int c = 0; c < 128; ++c) {
             int w, reg, e;
-            L::key_place(tok, c, &w, &reg, &e);
-            std::printf("k %d %d %d %d %d\n", tok, c, w, L::sign_bit(reg, e), L::mag_bit(reg, e));
+            L::key_place(tok, c, &w, &reg, &e);   // reg: the key's field
+            std::printf("k %d %d %d %d %d\n", tok, c, w, reg, L::key_bit(reg, e));
             L::value_place(tok, c, &w, &reg, &e);
             std::printf("v %d %d %d %d %d\n", tok, c, w, L::sign_bit(reg, e), L::mag_bit(reg, e));
         }

@@ -1,18 +1,18 @@
 """Numerics of the INT2 attention's operands, restated in numpy.
 
-A key is k_c = s_c (code_c - 1.5) + (z_c + 1.5 s_c).  The tensor cores
-multiply, channel by channel:
-- the A operand, q_c s_c 2^96 in fp32, split into a bf16 hi part (the value
-  truncated) and a bf16 lo part (the exact remainder, rounded);
-- the B operand, the centred code as the exact subnormal bf16 (2 code - 3)
-  2^-128.
-Products are exact and sums fp32.  Times 2^31 plus the bias
-sum_c q_c (z_c + 1.5 s_c), that gives q.k.  Checked here:
+A key is k_c = s_c code_c + z_c.  The tensor cores multiply, channel by
+channel:
+- the A operand, q_c s_c 2^(96 - 2 k) in fp32 (k the scale class of the
+  channel's k-step, s / 3), split into a bf16 hi part (the value truncated)
+  and a bf16 lo part (the exact remainder, rounded);
+- the B operand, the code as the exact subnormal bf16 code 2^(2 k - 133).
+Products are exact and sums fp32.  Times 2^37 plus the bias sum_c q_c z_c,
+that gives q.k.  Checked here:
 - the split loses at most 2^-16 of each operand;
-- the logit is within 1e-5 of sum_c |q_c k_c| (2e-6 seen) of the fp64 dot
-  product of q with the dequantized key (code * scale + zero in fp32), far
-  inside the 2e-3 probability tolerance;
-- the hi part alone is not enough, missing by ~1.3e-3 of the same sum."""
+- the logit is within 1e-5 of sum_c |q_c k_c| of the fp64 dot product of q
+  with the dequantized key (code * scale + zero in fp32), far inside the
+  2e-3 probability tolerance;
+- the hi part alone is not enough, missing by more than 1e-4 of the same sum."""
 import numpy as np
 
 F = np.float32
@@ -74,22 +74,22 @@ def _bias_mma(x, w16):
 
 
 def _device_logit(q, codes, s, z, use_lo=True, bias_mma=False):
-    a = (q * s * F(2.0 ** 96)).astype(F)                 # q s 2^96
+    cls = (np.arange(len(q)) >> 4) // 3                   # scale class of each channel's k-step
+    a = (q * s * np.exp2(96.0 - 2 * cls)).astype(F)      # q s 2^(96 - 2 k)
     hi, lo = split(a)
-    b = ((2 * codes - 3) * 2.0 ** -128)                   # exact subnormal bf16 values
+    b = codes * np.exp2(2.0 * cls - 133)                  # exact subnormal bf16 values
     acc = F(0)
     for c in range(len(q)):                               # exact products, fp32 sums
         acc = F(acc + F(hi[c] * b[c]))
         if use_lo:
             acc = F(acc + F(lo[c] * b[c]))
-    if bias_mma:   # sum q z and sum q s by fp16 products, then z part + 1.5 s part
-        bias = F(_bias_mma(q, z.astype(np.float16)) +
-                 F(1.5) * _bias_mma(q, s.astype(np.float16)))
+    if bias_mma:   # sum q z by fp16 products
+        bias = _bias_mma(q, z.astype(np.float16))
     else:
         bias = F(0)
         for c in range(len(q)):
-            bias = F(bias + F(q[c] * F(z[c] + F(1.5) * s[c])))
-    return float(F(acc * F(2.0 ** 31)) + bias)
+            bias = F(bias + F(q[c] * z[c]))
+    return float(F(acc * F(2.0 ** 37)) + bias)
 
 
 def _reference_logit(q, codes, s, z):
@@ -112,8 +112,8 @@ def test_logits_from_the_split_operands_match_the_dequantized_keys():
 
 
 def test_bias_terms_from_fp16_products_match_the_dequantized_keys():
-    """The key bias sum_c q_c (z_c + 1.5 s_c) taken as two fp16 tensor-core
-    sums (q as fp16 hi + lo against the fp16 zeros and scales) keeps the
+    """The key bias sum_c q_c z_c taken as an fp16 tensor-core sum (q as
+    fp16 hi + lo against the fp16 zeros) keeps the
     logit as close to the dequantized keys' as the fp32 chain does; p, scaled
     by 2^10 so that its fp16 lo part stays normal, as fp16 hi + lo loses at
     most 2^-21 of each probability above 2^-14 (and 2^-35 absolute below)."""
