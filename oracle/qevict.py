@@ -40,8 +40,23 @@ fp16((max - min) / 3) with the difference and division in fp32, code =
 clamp(rint((x - zero) / scale), 0, 3) with the subtraction and division in
 fp32 (round half to even), code 0 when scale is 0; dequantized value =
 code * scale + zero in fp32.  A promoted window's full-precision copy is
-that value rounded to bf16.  Keys are the cached keys as given (no rotary
-embedding is applied anywhere in this pass).
+that value rounded to bf16.
+
+Rotary positions (Sec. 4.4, "Positional handling for promoted keys" and the
+routing algorithm's promotion step), with `rope` set: the cached keys are the
+model's rotated keys; a window is quantized in the pre-rotation domain, each
+key rotated back by its position p before the codec, and every use of an
+INT2 window rotates the dequantized key forward again: a promoted window's
+bf16 key is the rotated value rounded to bf16, and attention runs over the
+INT2 windows reconstructed the same way (keys rotated, keys and values
+rounded to bf16), the review's "reconstruct (dequantize, re-apply RoPE) the
+active low-bit windows" before attention.  Rotation of channel pair
+(j, j + d/2) by the table's (cos, sin) at position p, every product and sum
+rounded to fp32 in this order:
+    forward  y_j = x_j cos - x_{j+d/2} sin,  y_{j+d/2} = x_{j+d/2} cos + x_j sin
+    back     x_j = y_j cos + y_{j+d/2} sin,  x_{j+d/2} = y_{j+d/2} cos - y_j sin.
+The table is the model's own (cos, sin) cache, an input: [positions][d/2][2]
+fp32.
 
 Readings where the page is silent: sinks are tokens [0, n_sink); windows
 are [n_sink + W j, n_sink + W (j + 1)); a window exists (score 0, Full
@@ -75,6 +90,7 @@ class QParams:
     omega: int = 8
     group: int = 32
     cumulative: bool = False      # Eq. (1): the window score sums, never decays
+    rope: np.ndarray = None       # [positions][d/2][2] fp32 (cos, sin), or None
 
 
 def capacities(b_hist: float, q: float, m_full: float, m_quant: float):
@@ -127,12 +143,34 @@ def dequantize(codes, scale, zero, axis: int):
     return (codes.astype(np.float32) * s + z).astype(np.float32)
 
 
-def quantize_window(K_bits, V_bits, group: int = 32):
+def rotate(x, cs, back: bool = False):
+    """Rotate fp32 keys x [..., W, d] by the (cos, sin) rows cs [W][d/2][2]
+    of their positions, pairs (j, j + d/2), each product and sum rounded to
+    fp32 (forward, or back with the sine negated)."""
+    x = np.asarray(x, dtype=np.float32)
+    h = x.shape[-1] // 2
+    c = np.asarray(cs[..., 0], dtype=np.float32)
+    s = np.asarray(cs[..., 1], dtype=np.float32)
+    a, b = x[..., :h], x[..., h:]
+    if back:
+        ya = (a * c).astype(np.float32) + (b * s).astype(np.float32)
+        yb = (b * c).astype(np.float32) - (a * s).astype(np.float32)
+    else:
+        ya = (a * c).astype(np.float32) - (b * s).astype(np.float32)
+        yb = (b * c).astype(np.float32) + (a * s).astype(np.float32)
+    return np.concatenate([ya.astype(np.float32), yb.astype(np.float32)], axis=-1)
+
+
+def quantize_window(K_bits, V_bits, group: int = 32, cs=None):
     """Ledger entry of one window.  K, V: [Ly][Hkv][W][d] bf16 bits.
     Keys per channel over groups of `group` tokens; values per token over
-    groups of `group` channels."""
+    groups of `group` channels.  cs: the (cos, sin) rows of the window's
+    positions [W][d/2][2]: the keys are rotated back first."""
     Ly, Hkv, W, d = K_bits.shape
-    k = _bits_to_f32(K_bits).reshape(Ly, Hkv, W // group, group, d)
+    kf = _bits_to_f32(K_bits)
+    if cs is not None:
+        kf = rotate(kf, cs, back=True)
+    k = kf.reshape(Ly, Hkv, W // group, group, d)
     v = _bits_to_f32(V_bits).reshape(Ly, Hkv, W, d // group, group)
     kq, ks, kz = quantize_groups(k, axis=3)             # scale/zero [Ly][Hkv][W/g][d]
     vq, vs, vz = quantize_groups(v, axis=4)             # scale/zero [Ly][Hkv][W][d/g]
@@ -140,9 +178,10 @@ def quantize_window(K_bits, V_bits, group: int = 32):
                 vq=vq.reshape(Ly, Hkv, W, d), vs=vs, vz=vz, group=group)
 
 
-def dequantize_window(led, layer=None):
+def dequantize_window(led, layer=None, cs=None):
     """fp32 (K, V) [Ly][Hkv][W][d] of a ledger entry ([Hkv][W][d] of one
-    layer when `layer` is given)."""
+    layer when `layer` is given); cs: the window's (cos, sin) rows, the keys
+    rotated forward."""
     g = led["group"]
     sel = slice(None) if layer is None else slice(layer, layer + 1)
     kq, vq = led["kq"][sel], led["vq"][sel]
@@ -150,7 +189,17 @@ def dequantize_window(led, layer=None):
     k = dequantize(kq.reshape(Ly, Hkv, W // g, g, d), led["ks"][sel], led["kz"][sel], axis=3)
     v = dequantize(vq.reshape(Ly, Hkv, W, d // g, g), led["vs"][sel], led["vz"][sel], axis=4)
     k, v = k.reshape(Ly, Hkv, W, d), v.reshape(Ly, Hkv, W, d)
+    if cs is not None:
+        k = rotate(k, cs)
     return (k, v) if layer is None else (k[0], v[0])
+
+
+def window_cs(P: QParams, wid: int):
+    """The (cos, sin) rows of window wid's positions, or None without rope."""
+    if P.rope is None:
+        return None
+    p0 = P.n_sink + P.window * wid
+    return P.rope[p0:p0 + P.window]
 
 
 # ------------------------------------------------------------------ state
@@ -202,7 +251,10 @@ def accessible(P: QParams, seq: QSequence, layer: int):
             ks.append(_bits_to_f32(w.K[layer]))
             vs.append(_bits_to_f32(w.V[layer]))
         elif w.tier == QUANT:
-            k, v = dequantize_window(w.ledger, layer)
+            k, v = dequantize_window(w.ledger, layer, window_cs(P, w.wid))
+            if P.rope is not None:   # reconstructed as bf16 before attention
+                k = _bits_to_f32(_f32_to_bf16_bits(k))
+                v = _bits_to_f32(_f32_to_bf16_bits(v))
             ks.append(k)
             vs.append(v)
         else:
@@ -242,12 +294,12 @@ def route(P: QParams, seq: QSequence):
     for w in new_q:
         if w.tier != QUANT:
             if w.ledger is None:                 # first demotion: quantize once
-                w.ledger = quantize_window(w.K, w.V, P.group)
+                w.ledger = quantize_window(w.K, w.V, P.group, window_cs(P, w.wid))
             w.K = w.V = None
             w.tier = QUANT
     for w in new_f:
         if w.tier == QUANT:                      # promotion: from the ledger
-            k, v = dequantize_window(w.ledger)
+            k, v = dequantize_window(w.ledger, cs=window_cs(P, w.wid))
             w.K, w.V = _f32_to_bf16_bits(k), _f32_to_bf16_bits(v)
         w.tier = FULL
     for w in cand[P.k_full + P.k_quant:]:

@@ -181,6 +181,20 @@ MUTANTS += [
     ("qevict.py", "codes = 2 * n_kv_heads * head_dim * 2 // 8", "codes = n_kv_heads * head_dim * 2 // 8",
      "value codes left out of the footprint"),
     ("qevict.py", "nw = (L0 - ns) // W", "nw = L0 // W", "windows counted from position 0"),
+    # rotary positions
+    ("qevict.py", "        ya = (a * c).astype(np.float32) + (b * s).astype(np.float32)\n",
+     "        ya = (a * c).astype(np.float32) - (b * s).astype(np.float32)\n",
+     "rotation back with the forward sine"),
+    ("qevict.py", "    a, b = x[..., :h], x[..., h:]", "    a, b = x[..., 0::2], x[..., 1::2]",
+     "rotation pairs adjacent channels"),
+    ("qevict.py", "k, v = dequantize_window(w.ledger, cs=window_cs(P, w.wid))",
+     "k, v = dequantize_window(w.ledger)", "promoted keys not rotated forward"),
+    ("qevict.py", "w.ledger = quantize_window(w.K, w.V, P.group, window_cs(P, w.wid))",
+     "w.ledger = quantize_window(w.K, w.V, P.group)", "keys quantized after rotation"),
+    ("qevict.py", "                k = _bits_to_f32(_f32_to_bf16_bits(k))\n",
+     "                k = k\n", "reconstructed keys not rounded to bf16"),
+    ("qevict.py", "                v = _bits_to_f32(_f32_to_bf16_bits(v))\n",
+     "                v = v\n", "reconstructed values not rounded to bf16"),
 ]
 
 

@@ -232,3 +232,140 @@ def test_evicted_window_no_longer_attended_and_quantized_one_is():
     n = 1 + 32 + 2
     assert out[1] == pytest.approx(0.0, abs=1e-15)
     assert out[2] == pytest.approx(np.tile([0.75, 1.5, 3.0, 6.0], 8).sum() / n, rel=1e-12)
+
+
+# ---- rotary positions (Sec. 4.4: pre-rotation quantization, rotation re-applied)
+def _table(n_pos, half, cos, sin):
+    t = np.zeros((n_pos, half, 2), np.float32)
+    t[..., 0], t[..., 1] = cos, sin
+    return t
+
+
+def test_quarter_turn_quantizes_the_swapped_keys():
+    """With every angle a quarter turn (cos 0, sin 1) the key rotated back is
+    (x_{j+d/2}, -x_j): exact in fp32.  So the ledger of a window quantized
+    with that table holds exactly the codes, scales and zeros of the same
+    window with its key halves swapped and the second half negated,
+    quantized without rotation; the values are untouched."""
+    P = _params(k_full=0, k_quant=1, n_recent=1)
+    Pr = _params(k_full=0, k_quant=1, n_recent=1,
+                 rope=_table(1 + 32 + 8, 16, 0.0, 1.0))
+    rng = np.random.default_rng(3)
+    K = _bits(rng.standard_normal((1, 1, 1 + 32 + 1, 32)))
+    V = _bits(rng.standard_normal((1, 1, 1 + 32 + 1, 32)))
+    kf = (K.astype(np.uint32) << 16).view(np.float32)
+    swapped = np.concatenate([kf[..., 16:], -kf[..., :16]], axis=-1)
+    seq_r = QE.QSequence.from_prefill(Pr, K, V)
+    seq_p = QE.QSequence.from_prefill(P, _bits(swapped), V)
+    QE.route(Pr, seq_r)
+    QE.route(P, seq_p)
+    a, b = seq_r.windows[0].ledger, seq_p.windows[0].ledger
+    for k in ("kq", "vq"):
+        assert np.array_equal(a[k], b[k])
+    for k in ("ks", "kz", "vs", "vz"):
+        assert np.array_equal(a[k].view(np.uint16), b[k].view(np.uint16))
+
+
+def test_quarter_turn_promotion_rotates_the_dequantized_keys_forward():
+    """Promoted under a quarter turn, the bf16 key is the forward rotation
+    (-x_{j+d/2}, x_j) of the dequantized pre-rotation key: with the ledger
+    of the swapped keys (previous pin) that is the plain promotion with the
+    halves swapped back and negated."""
+    Pr = _params(k_full=1, k_quant=1, n_recent=1, rope=_table(1 + 64 + 8, 16, 0.0, 1.0))
+    seq = _seq_with_scores(Pr, [0.2, 0.8], tail=1)
+    QE.route(Pr, seq)                        # window 0 -> Q
+    seq.windows[0].m, seq.windows[1].m = 0.9, 0.1
+    QE.route(Pr, seq)                        # promote window 0
+    w0 = seq.windows[0]
+    kd, vd = QE.dequantize_window(w0.ledger)            # no rotation
+    fwd = np.concatenate([-kd[..., 16:], kd[..., :16]], axis=-1)
+    assert w0.tier == "F"
+    assert np.array_equal(w0.K, _bits(fwd)) and np.array_equal(w0.V, _bits(vd))
+
+
+def test_rotation_round_trip_and_pair_norms():
+    """Any angle: back then forward returns the key within fp32 rounding,
+    and each (j, j + d/2) pair keeps its length."""
+    rng = np.random.default_rng(5)
+    ang = rng.uniform(0, 2 * np.pi, (64, 16))
+    cs = np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
+    x = rng.standard_normal((3, 64, 32)).astype(np.float32)
+    y = QE.rotate(x, cs)
+    back = QE.rotate(y, cs, back=True)
+    assert np.abs(back - x).max() <= 1e-6 * np.abs(x).max()
+    n0 = x[..., :16] ** 2 + x[..., 16:] ** 2
+    n1 = y[..., :16].astype(np.float64) ** 2 + y[..., 16:].astype(np.float64) ** 2
+    assert np.allclose(n1, n0, rtol=1e-6)
+
+
+def test_identity_table_routes_and_quantizes_as_without_rotation():
+    """cos 1, sin 0 everywhere: the same tiers and ledgers as without a
+    table, and the same promoted pages."""
+    P = _params(k_full=1, k_quant=1, n_recent=1)
+    Pr = _params(k_full=1, k_quant=1, n_recent=1, rope=_table(1 + 64 + 8, 16, 1.0, 0.0))
+    seq_p = _seq_with_scores(P, [0.2, 0.8], tail=1)
+    seq_r = _seq_with_scores(Pr, [0.2, 0.8], tail=1)
+    for m in ((0.2, 0.8), (0.9, 0.1)):
+        for s_ in (seq_p, seq_r):
+            s_.windows[0].m, s_.windows[1].m = m
+        QE.route(P, seq_p)
+        QE.route(Pr, seq_r)
+        assert seq_p.tiers() == seq_r.tiers()
+    for a, b in zip(seq_p.windows, seq_r.windows):
+        if a.K is not None:
+            assert np.array_equal(a.K, b.K) and np.array_equal(a.V, b.V)
+        if a.ledger is not None:
+            assert np.array_equal(a.ledger["kq"], b.ledger["kq"])
+
+
+def test_reconstructed_int2_window_is_attended_in_bf16():
+    """With a table, attention sees an INT2 window as its reconstruction in
+    bf16.  All keys 0 give every token the same weight, so the output is the
+    mean of the values: a value group holding 0 and 1 has scale
+    fp16(1/3) = 0.333251953125 and dequantizes to 0, s, 2 s, 3 s, which bf16
+    rounds to 0, 0.333984375, 0.66796875, 1.0; without a table the fp32
+    values are attended."""
+    d = 32
+    K = np.zeros((1, 1, 1 + 32 + 1, d), np.float32)
+    V = np.zeros_like(K)
+    V[0, 0, 1:33, :] = np.tile([0.0, 1.0], 16)[None, :]    # every value group spans [0, 1]
+    V[0, 0, 1:33, 0] = np.tile([0.0, 1.0 / 3, 2.0 / 3, 1.0], 8)
+    out = {}
+    for name, rope in (("plain", None), ("rope", _table(64, 16, 1.0, 0.0))):
+        P = _params(k_full=0, k_quant=1, n_recent=1, rope=rope)
+        seq = QE.QSequence.from_prefill(P, _bits(K), _bits(V))
+        QE.route(P, seq)
+        assert seq.tiers() == ["Q"]
+        z = np.zeros((1, 1, d), np.float32)
+        out[name] = QE.step(P, seq, 2, _bits(z), _bits(z), _bits(z))["out"][0, 0, 0]
+    led_codes = [0, 1, 2, 3] * 8                    # channel 0 per token: 0, 1/3, 2/3, 1
+    s32 = np.float32(np.float16(np.float32(1.0) / np.float32(3.0)))
+    deq = np.array([np.float32(c) * s32 for c in led_codes], np.float32)
+    bf = {0: 0.0, 1: 0.333984375, 2: 0.66796875, 3: 1.0}
+    n = 1 + 32 + 2                                  # sink, window, tail token, new token
+    assert out["rope"] == pytest.approx(sum(bf[c] for c in led_codes) / n, rel=1e-12)
+    assert out["plain"] == pytest.approx(float(deq.astype(np.float64).sum()) / n, rel=1e-12)
+
+
+def test_reconstructed_keys_are_bf16_in_the_logits():
+    """Key channel 0 of an INT2 window spans [0, 1] (scale fp16(1/3), codes
+    0-3); the query reads only that channel.  With a table the logits use the
+    bf16 reconstruction 0, 0.333984375, 0.66796875, 1.0 of the dequantized
+    keys, and the values (code 3 of scale fp16(1/3)) are bf16(0.999755859375)
+    = 1.0; every other token has key 0 and value 0.  Closed form: out_1 =
+    sum_i e^(8 k_i / sqrt(32)) / (sum_i e^(8 k_i / sqrt(32)) + 3)."""
+    d = 32
+    K = np.zeros((1, 1, 1 + 32 + 1, d), np.float32)
+    V = np.zeros_like(K)
+    K[0, 0, 1:33, 0] = np.tile([0.0, 1.0 / 3, 2.0 / 3, 1.0], 8)
+    V[0, 0, 1:33, 1] = 1.0
+    P = _params(k_full=0, k_quant=1, n_recent=1, rope=_table(64, 16, 1.0, 0.0))
+    seq = QE.QSequence.from_prefill(P, _bits(K), _bits(V))
+    QE.route(P, seq)
+    q = np.zeros((1, 1, d), np.float32)
+    q[0, 0, 0] = 8.0
+    z = np.zeros((1, 1, d), np.float32)
+    out = QE.step(P, seq, 2, _bits(q), _bits(z), _bits(z))["out"][0, 0, 1]
+    k = np.tile([0.0, 0.333984375, 0.66796875, 1.0], 8)
+    w = np.exp(8.0 * k / np.sqrt(32.0))
+    assert out == pytest.approx(w.sum() / (w.sum() + 3.0), rel=1e-12)
