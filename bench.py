@@ -514,7 +514,7 @@ def main():
         return
     if args.workload == "tiers":
         bench_tiers(args, rank, world, local_rank, omega=args.omega,
-                    omega_sweep=() if args.no_sweep else (1, 32))
+                    omega_sweep=() if args.no_sweep else (1, 32), rotary=not args.no_sweep)
         finish_dist(world)
         return
 
@@ -1164,7 +1164,7 @@ def bench_paged(args, rank, world, local_rank, md=False, steps=None, quiet=False
 
 
 def bench_tiers(args, rank, world, local_rank, steps=None, omega=None, quiet=False,
-                omega_sweep=(1, 32), sweep_steps=96):
+                omega_sweep=(1, 32), sweep_steps=96, rotary=True):
     """Two-tier run: 4 sequences of 131072 tokens in 128-token windows, K_f
     51 bf16 windows, K_q 204 INT2 windows, routing every omega = 8 steps.
     Timed: K consecutive decode steps from step 1 of a fresh run (steps 1-7
@@ -1172,8 +1172,10 @@ def bench_tiers(args, rank, world, local_rank, steps=None, omega=None, quiet=Fal
     per sequence, later steps attend ~6.6k bf16 and ~26k INT2 tokens per
     sequence); the steady state (steps after the first event) is reported
     beside it, with the memory the tiers hold (bf16 pages, INT2 ledger) per
-    step, and short runs at other routing intervals (omega_sweep).  Returns
-    the JSON record (rank 0) or None."""
+    step, and short runs at other routing intervals (omega_sweep) and in
+    rotary mode (rotary: INT2 windows attended as bf16 reconstructions with
+    keys rotated forward, rebuilt after each routing event).  Returns the
+    JSON record (rank 0) or None."""
     import torch
     dist = init_dist(world, local_rank)
     kvev = load_kvev()
@@ -1190,7 +1192,8 @@ def bench_tiers(args, rank, world, local_rank, steps=None, omega=None, quiet=Fal
     n_steps = steps if steps is not None else args.steps
     max_ctx = L0 + max(n_steps, args.warmup, sweep_steps) + 16
     wl = TierDeviceWorkload(0, n_layers=Ly, batch=b, prefill=L0)
-    pps = wl.n_pages + 16 + 8 * W["k_full"]
+    # bf16 pages: prefill, promotions and, in rotary mode, the reconstructions
+    pps = wl.n_pages + 16 + 8 * W["k_full"] + (8 * W["k_quant"] if rotary else 0)
     tp = kvev.TierEvictionPass(Ly, W["n_q_heads"], W["n_kv_heads"], W["head_dim"], b, max_ctx,
                                pps, W["k_full"], W["k_quant"], W["omega"], W["alpha"])
     wl.fill(torch, tp.k_pool, tp.v_pool, pps)
@@ -1339,6 +1342,38 @@ def bench_tiers(args, rank, world, local_rank, steps=None, omega=None, quiet=Fal
                       "after_first_route_us": round(sum(sm[om:]) / max(1, len(sm) - om) * 1e3, 1),
                       "quant_windows_end": int((tp.tier.cpu().numpy() == kvev.KVEV_TIER_QUANT).sum()),
                       "ledger_bytes_end": int(tp.has_codes.cpu().numpy().astype(bool).sum()) * ledger_entry})
+    # rotary mode over the same steps: its cost does not depend on the key
+    # values, so the drawn keys stand in for rotated ones
+    rot = None
+    if rotary:
+        from workloads import rope_table
+        table = torch.from_numpy(rope_table(max_ctx, W["head_dim"], 10000.0)).to("cuda")
+        kvev.kvev_set_rope(tp.ctx, table, max_ctx)
+        restart()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(sweep_steps + 1)]
+        ev[0].record(stream)
+        for t in range(1, sweep_steps + 1):
+            tp.step(*inputs[t - 1], stream)
+            ev[t].record(stream)
+        torch.cuda.synchronize()
+        kvev.kvev_sync(tp.ctx)
+        kvev.kvev_set_rope(tp.ctx, None, 0)
+        sm = [ev[t - 1].elapsed_time(ev[t]) for t in range(1, sweep_steps + 1)]
+        om = W["omega"]
+        # steps after the first routing event; the first step after each event rebuilds
+        after = range(om + 1, sweep_steps + 1)
+        rebuild = [sm[t - 1] for t in after if (t - 1) % om == 0]
+        plain = [sm[t - 1] for t in after if (t - 1) % om != 0 and t % om != 0]
+        rot = {"steps": sweep_steps, "omega": om, "rope_base": 10000.0,
+               "mean_us": round(sum(sm) / len(sm) * 1e3, 1),
+               "after_first_route_us": round(sum(sm[om:]) / max(1, len(sm) - om) * 1e3, 1),
+               "rebuild_step_us": round(sum(rebuild) / max(1, len(rebuild)) * 1e3, 1),
+               "plain_step_us": round(sum(plain) / max(1, len(plain)) * 1e3, 1),
+               "note": "INT2 windows attended as bf16 reconstructions (keys rotated forward), "
+                       "rebuilt on the first step after each routing event; routing steps aside "
+                       "in plain_step_us"}
+        del table
     restart()
 
     cpu = None
@@ -1364,6 +1399,7 @@ def bench_tiers(args, rank, world, local_rank, steps=None, omega=None, quiet=Fal
             "first_steps_us": [round(x * 1e3, 1) for x in step_ms[:first + 1]],
             "memory": memory,
             "omega_sweep": sweep,
+            "rotary": rot,
             "roofline": {"bound": "hbm", "kernel": "attention (bf16 pages + INT2 windows)",
                          "achieved": round(attn_achieved, 2) if attn_achieved else None,
                          "peak": peak, "unit": "GB/s",

@@ -314,6 +314,14 @@ struct kvev_ctx {
     int k_full = 0, k_quant = 0, omega = 8;
     int int2_grid = 0, int2_warps = 0;
     int t_nw = 0, t_tl = 0, t_first_u = 0, t_nf = 0, t_nq = 0;
+    // rotary positions: the model's (cos, sin) table of the run (null: off)
+    // and the one kvev_set_rope gave for the next run, the pages at the end
+    // of each sequence's range that hold the INT2 windows' bf16
+    // reconstructions, and whether they match the current INT2 list
+    const float* rope = nullptr;
+    const float* rope_next = nullptr;
+    int t_scratch = 0;
+    bool t_recon_valid = false;
     int32_t len = 0, prefill_len = 0;
     std::vector<int32_t> ub_blocks;   // block mode: upper bound of each sequence's live blocks
     int64_t step = 0;
@@ -1344,6 +1352,8 @@ TierArgs tier_args(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_tier_state
     a.lir_streak = c->ws.lir_streak;
     a.lir_counters = c->lir_counters;
     a.lir_sustain = c->lir_sustain;
+    a.rope = c->rope;
+    a.scratch = c->t_scratch;
     return a;
 }
 
@@ -1381,9 +1391,28 @@ kvev_status kvev_set_tiers(kvev_ctx* c, int64_t k_full, int64_t k_quant, int32_t
     const int mw = tier_max_windows(c->lay);
     if (k_full < 0 || k_quant < 0 || k_full > mw || k_quant > mw || omega < 1)
         return fail(KVEV_EINVAL, "K_f, K_q must be in [0, %d] and omega >= 1", mw);
+    if (c->rope && c->begun && (int)k_quant * (kTierW / kTile) > c->t_scratch)
+        return fail(KVEV_ESTATE, "with rotary positions K_q cannot grow past %d after "
+                    "kvev_tier_begin (its reconstruction pages are set aside there)",
+                    c->t_scratch / (kTierW / kTile));
     c->k_full = (int)k_full;
     c->k_quant = (int)k_quant;
     c->omega = omega;
+    return KVEV_OK;
+}
+
+kvev_status kvev_set_rope(kvev_ctx* c, const float* table, int32_t n_pos) {
+    if (!c) return fail(KVEV_EINVAL, "ctx is NULL");
+    if (c->lay.page_tokens != kTierW)
+        return fail(KVEV_ESTATE, "not a two-tier context (layout.page_tokens must be %d)", kTierW);
+    if (table) {
+        if (c->lay.head_dim != 128) return fail(KVEV_EINVAL, "rotary mode needs head_dim 128");
+        if (!aligned16(table)) return fail(KVEV_EINVAL, "the table must be 16-byte aligned");
+        if (n_pos < c->lay.max_ctx)
+            return fail(KVEV_EINVAL, "table of %d positions < max_ctx %d", n_pos,
+                        c->lay.max_ctx);
+    }
+    c->rope_next = table;
     return KVEV_OK;
 }
 
@@ -1396,10 +1425,14 @@ kvev_status kvev_tier_begin(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_t
                     kTierSinks);
     const int hist = prefill_tokens - kTierSinks;
     const int used = 1 + (hist + kTile - 1) / kTile;
-    if (used + 1 > tc->pages_per_seq)
-        return fail(KVEV_EINVAL, "pages_per_seq %d too small for a %d-token prefill",
-                    tc->pages_per_seq, prefill_tokens);
+    const int scratch = c->rope_next ? c->k_quant * (kTierW / kTile) : 0;
+    if (used + 1 > tc->pages_per_seq - scratch)
+        return fail(KVEV_EINVAL, "pages_per_seq %d too small for a %d-token prefill%s",
+                    tc->pages_per_seq, prefill_tokens,
+                    scratch ? " and the INT2 windows' reconstruction pages" : "");
     cudaStream_t s = (cudaStream_t)stream;
+    c->rope = c->rope_next;
+    c->t_scratch = scratch;
     const TierArgs a = tier_args(c, tc, ts, 0);
     rc = timed_launch(c, kProfInit, s, "tier begin",
                       [&] { return launch_tier_begin(a, prefill_tokens, s); });
@@ -1415,6 +1448,7 @@ kvev_status kvev_tier_begin(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_t
     c->t_tl = hist % kTierW;
     c->t_first_u = 0;
     c->t_nf = c->t_nq = 0;
+    c->t_recon_valid = false;
     c->len = prefill_tokens;
     c->prefill_len = prefill_tokens;
     c->step = 0;
@@ -1464,9 +1498,9 @@ kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const 
         c->t_nw = saved_nw;
         c->t_tl = saved_tl;
         const int prom = routing ? std::min(c->t_nq, nf2) : 0;
-        if (used + PW * prom > pps)
+        if (used + PW * prom > pps - c->t_scratch)
             return fail(KVEV_EINVAL, "pages_per_seq %d too small: %d bf16 pages needed", pps,
-                        used + PW * prom);
+                        used + PW * prom + c->t_scratch);
     }
     cudaStream_t s = (cudaStream_t)stream;
     const kvev_layout& Ly = c->lay;
@@ -1476,9 +1510,21 @@ kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const 
         return launch_tier_append(ta, (const uint16_t*)k_new, (const uint16_t*)v_new, s);
     });
     if (rc != KVEV_OK) return rc;
+    // rotary positions: the INT2 windows are attended as bf16 reconstructions
+    // (keys rotated forward), rebuilt when the INT2 list has changed
+    const bool recon = c->rope != nullptr;
+    if (recon && c->t_nq > 0 && !c->t_recon_valid) {
+        TierArgs ra = ta;
+        ra.recon = 1;
+        rc = timed_launch(c, kProfCompact, s, "reconstruct",
+                          [&] { return launch_tier_promote(ra, c->t_nq, c->num_sms, s); });
+        if (rc != KVEV_OK) return rc;
+        c->t_recon_valid = true;
+    }
 
     const int64_t rows = (int64_t)Ly.n_layers * Ly.batch * Ly.n_kv_heads;
-    const int n_bf = 1 + PW * (nw - c->t_first_u + c->t_nf) + (tl + kTile - 1) / kTile;
+    const int n_bf = 1 + PW * (nw - c->t_first_u + c->t_nf) + (tl + kTile - 1) / kTile +
+                     (recon ? PW * c->t_nq : 0);
     AttnArgs at{};
     at.k = (const uint16_t*)tc->k_pool;
     at.v = (const uint16_t*)tc->v_pool;
@@ -1518,7 +1564,7 @@ kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const 
     cb.sp.row0 = 0;
     cb.sp.total_warps = at.total_warps;
     cb.sp.tiles_per_row = n_bf;
-    if (c->t_nq > 0) {
+    if (c->t_nq > 0 && !recon) {
         Int2Args ia{};
         ia.ledger = (const unsigned char*)tc->ledger;
         ia.max_windows = tc->max_windows;
@@ -1585,6 +1631,7 @@ kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const 
         c->t_first_u += n_aged;
         c->t_nf = nf2;
         c->t_nq = nq2;
+        c->t_recon_valid = false;   // the INT2 list may have changed
     }
     c->t_nw = nw;
     c->t_tl = tl;
@@ -1625,7 +1672,7 @@ kvev_status kvev_launch_count(const kvev_ctx* c, int64_t* launches) {
 namespace {
 
 constexpr uint32_t kBlobMagic = 0x5645564bu;   // "KVEV"
-constexpr uint32_t kBlobVersion = 2;
+constexpr uint32_t kBlobVersion = 3;
 
 struct BlobHead {
     uint32_t magic, version;
@@ -1637,7 +1684,7 @@ struct BlobHead {
     int32_t k_full, k_quant, omega;
     int32_t begun, len, prefill_len;
     int64_t step;
-    int32_t t_nw, t_tl, t_first_u, t_nf, t_nq;
+    int32_t t_nw, t_tl, t_first_u, t_nf, t_nq, t_scratch;
     int32_t n_ub, n_pin;          // then n_ub + n_pin int32 values
 };
 
@@ -1681,6 +1728,7 @@ kvev_status kvev_export_state(const kvev_ctx* c, void* host, size_t* bytes) {
     h.t_first_u = c->t_first_u;
     h.t_nf = c->t_nf;
     h.t_nq = c->t_nq;
+    h.t_scratch = c->t_scratch;
     h.n_ub = (int32_t)c->ub_blocks.size();
     h.n_pin = (int32_t)c->pin_blocks.size();
     char* out = static_cast<char*>(host);
@@ -1723,6 +1771,14 @@ kvev_status kvev_import_state(kvev_ctx* c, const void* host, size_t bytes, void*
                in_range(h.t_nw, 0, mw) && in_range(h.t_first_u, 0, h.t_nw) &&
                in_range(h.t_tl, 0, kTierW - 1) && in_range(h.t_nf, 0, mw) &&
                in_range(h.t_nq, 0, mw);
+        // rotary positions: the reconstruction pages set aside at the
+        // exporter's kvev_tier_begin; a context without a table takes none
+        constexpr int PW = kTierW / kTile;
+        sane = sane && (c->rope_next ? in_range(h.t_scratch, PW * (int64_t)h.k_quant,
+                                                PW * (int64_t)mw) && h.t_scratch % PW == 0
+                                     : h.t_scratch == 0);
+    } else {
+        sane = sane && h.t_scratch == 0;
     }
     const char* in = static_cast<const char*>(host);
     for (int32_t i = 0; sane && i < h.n_ub + h.n_pin; ++i) {
@@ -1750,6 +1806,9 @@ kvev_status kvev_import_state(kvev_ctx* c, const void* host, size_t bytes, void*
     c->t_first_u = h.t_first_u;
     c->t_nf = h.t_nf;
     c->t_nq = h.t_nq;
+    c->rope = c->rope_next;
+    c->t_scratch = h.t_scratch;
+    c->t_recon_valid = false;   // reconstructions are rebuilt from the ledger
     c->ub_blocks.assign(h.n_ub, 0);
     c->pin_blocks.assign(h.n_pin, 0);
     c->diag_flags_valid = false;   // the raw-set flags are not part of a checkpoint

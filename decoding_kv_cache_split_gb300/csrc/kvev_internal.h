@@ -428,6 +428,13 @@ struct TierArgs {
     int32_t* lir_streak;   // [b][max_windows]
     int32_t* lir_counters; // [b][3]
     int32_t lir_sustain;
+    // Rotary positions ("QEvict" review Sec. 4.4): keys are quantized rotated
+    // back by their positions and rotated forward again on promotion; the
+    // INT2 windows are attended as a bf16 reconstruction in the last
+    // `scratch` pages of each sequence's range (null rope: off, scratch 0)
+    const float* rope;     // [positions][D/2][2] fp32 (cos, sin)
+    int32_t scratch;
+    int32_t recon;         // tier_promote_kernel: 1 = reconstruct the INT2 list into scratch
 };
 
 // ---- programmatic dependent launch ----------------------------------------

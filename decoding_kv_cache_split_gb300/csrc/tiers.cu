@@ -93,10 +93,11 @@ __global__ void __launch_bounds__(kBook) tier_begin_kernel(const TierArgs a, int
     for (int i = threadIdx.x; i < kTierW / kTile; i += blockDim.x)
         a.st.tail_pages[(size_t)b * (kTierW / kTile) + i] =
             i < n_tail_pages ? base + 1 + nw * (kTierW / kTile) + i : -1;
-    for (int k = threadIdx.x; k < pps - used; k += blockDim.x)   // lowest free page on top
-        a.c.free_pages[(size_t)base + k] = base + pps - 1 - k;
+    const int avail = pps - a.scratch;   // the last `scratch` pages hold reconstructions
+    for (int k = threadIdx.x; k < avail - used; k += blockDim.x)   // lowest free page on top
+        a.c.free_pages[(size_t)base + k] = base + avail - 1 - k;
     if (threadIdx.x == 0) {
-        a.c.n_free[b] = pps - used;
+        a.c.n_free[b] = avail - used;
         a.st.n_windows[b] = nw;
         a.st.tail_len[b] = tl;
         a.seq_len[b] = n0;
@@ -223,8 +224,21 @@ __global__ void __launch_bounds__(kBook) tier_append_kernel(const TierArgs a,
         bpos[j0 + i] = kTierSinks + nw * kTierW + i * kTile;
         blen[j0 + i] = min(kTile, tl - i * kTile);
     }
+    int n_rec = 0;
+    if (a.rope) {   // rotary mode: the INT2 windows' bf16 reconstructions, list order
+        __syncthreads();   // the INT2 list is complete
+        const int jq = j0 + n_tail, sbase = b * pps + pps - a.scratch;
+        for (int u = threadIdx.x; u < n_q * PW; u += blockDim.x) {
+            const int k = u / PW, i = u % PW;
+            const int w = a.qlist[(size_t)b * MW + k];
+            bt[jq + u] = sbase + u;
+            bpos[jq + u] = kTierSinks + w * kTierW + i * kTile;
+            blen[jq + u] = kTile;
+        }
+        n_rec = n_q * PW;
+    }
     if (threadIdx.x == 0) {
-        a.nblk[b] = j0 + n_tail;
+        a.nblk[b] = j0 + n_tail + n_rec;
         a.nq[b] = n_q;
     }
 }
@@ -502,13 +516,34 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
             const int p = 8 * s8 + 4 * h + t;   // channel pair 2p, 2p + 1
             const __nv_bfloat162* col =
                 reinterpret_cast<const __nv_bfloat162*>(xt + grp * kQGroup * XS) + p;
-            __nv_bfloat162 mn2 = col[0], mx2 = col[0];
+            // the pair at `row` of the group as quantized: with rotary positions
+            // rotated back by the row's position (the partner pair 2p +- D/2 is
+            // lane ^ 4's), fp32 products and sums in the oracle's order
+            const bool first_half = 2 * p < D / 2;
+            const float4* cs_row = a.rope
+                ? reinterpret_cast<const float4*>(a.rope) +
+                      ((size_t)(kTierSinks + w * kTierW + grp * kQGroup) * (D / 2) +
+                       ((2 * p) & (D / 2 - 1))) / 2
+                : nullptr;
+            auto key_at = [&](int row) -> float2 {
+                const float2 x = __bfloat1622float2(col[row * (XS / 2)]);
+                if (!a.rope) return x;
+                const float yx = __shfl_xor_sync(0xffffffffu, x.x, 4);
+                const float yy = __shfl_xor_sync(0xffffffffu, x.y, 4);
+                const float4 cs = __ldg(cs_row + (size_t)row * (D / 4));   // cos, sin of j, j + 1
+                return first_half
+                    ? make_float2(__fadd_rn(__fmul_rn(x.x, cs.x), __fmul_rn(yx, cs.y)),
+                                  __fadd_rn(__fmul_rn(x.y, cs.z), __fmul_rn(yy, cs.w)))
+                    : make_float2(__fsub_rn(__fmul_rn(x.x, cs.x), __fmul_rn(yx, cs.y)),
+                                  __fsub_rn(__fmul_rn(x.y, cs.z), __fmul_rn(yy, cs.w)));
+            };
+            float2 mn = key_at(0), mx = mn;
 #pragma unroll
             for (int r = 1; r < kQGroup; ++r) {
-                mn2 = __hmin2(mn2, col[r * (XS / 2)]);
-                mx2 = __hmax2(mx2, col[r * (XS / 2)]);
+                const float2 x = key_at(r);
+                mn = make_float2(fminf(mn.x, x.x), fminf(mn.y, x.y));
+                mx = make_float2(fmaxf(mx.x, x.x), fmaxf(mx.y, x.y));
             }
-            const float2 mn = __bfloat1622float2(mn2), mx = __bfloat1622float2(mx2);
             const __half2 z16 = __floats2half2_rn(mn.x, mn.y);
             const __half2 s16 = __floats2half2_rn(__fdiv_rn(__fsub_rn(mx.x, mn.x), 3.0f),
                                                   __fdiv_rn(__fsub_rn(mx.y, mn.y), 3.0f));
@@ -526,7 +561,7 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
                 for (int gg = 0; gg < 8; ++gg)
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
-                        const float2 x = __bfloat1622float2(col[(16 * tt + 8 * i + gg) * (XS / 2)]);
+                        const float2 x = key_at(16 * tt + 8 * i + gg);
                         const uint32_t c0 = sc.x == 0.f ? 0u : int2_code(x.x, z.x, sc.x, r0);
                         const uint32_t c1 = sc.y == 0.f ? 0u : int2_code(x.y, z.y, sc.y, r1);
                         uint32_t word = (c0 << b0) | (c1 << (b0 + 16));
@@ -623,15 +658,21 @@ __global__ void __launch_bounds__(kPromThreads) tier_promote_kernel(const TierAr
     griddep_release();
     (void)max_items;
     const int LG = a.n_layers * a.n_kv, MW = a.c.max_windows;
-    const int64_t total = 2 * item_count(a.n_prom, a.batch, LG);
+    // promotion: the routing event's promoted windows into their new pages;
+    // reconstruction (rotary mode): every INT2 window, list entry e into the
+    // scratch pages pps - scratch + e PW .. + PW - 1 of its sequence
+    const int32_t* counts = a.recon ? a.nq : a.n_prom;
+    const int32_t* list = a.recon ? a.qlist : a.prom_list;
+    const int64_t total = 2 * item_count(counts, a.batch, LG);
     const int tid = threadIdx.x;
     for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
         const int kv = (int)(it & 1);
         int b, e, lg;
-        item_at(a.n_prom, a.batch, LG, it >> 1, &b, &e, &lg);
-        const int w = a.prom_list[(size_t)b * MW + e];
+        item_at(counts, a.batch, LG, it >> 1, &b, &e, &lg);
+        const int w = list[(size_t)b * MW + e];
         const int l = lg / a.n_kv, g = lg % a.n_kv;
         const int32_t* pages = a.st.win_pages + ((size_t)b * MW + w) * PW;
+        const int rec0 = b * a.c.pages_per_seq + a.c.pages_per_seq - a.scratch + e * PW;
         const uint4* led = reinterpret_cast<const uint4*>(
             reinterpret_cast<const unsigned char*>(a.c.ledger) +
             ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES +
@@ -648,24 +689,42 @@ __global__ void __launch_bounds__(kPromThreads) tier_promote_kernel(const TierAr
         const int q4 = tid >> 6;  // key group / quarter of the window: pages 2 q4, 2 q4 + 1
 #pragma unroll
         for (int pg = 0; pg < 2; ++pg) {
-            const int page = pages[2 * q4 + pg];
+            const int page = a.recon ? rec0 + 2 * q4 + pg : pages[2 * q4 + pg];
             if (page < 0) continue;   // no page could be taken for this promotion
             uint32_t* dst = pool + ((((int64_t)page * a.n_layers + l) * a.n_kv + g) * kTile) * D / 2 + p;
             const uint32_t* cwt = cw + (2 * q4 + pg) * D;   // code words of this 16-token tile
             if (kv == 0) {
                 // keys: channels 2p, 2p + 1 (one field, halves 0 and 1) of the
-                // tokens 16 (2 q4 + pg) + r, read from their ledger fields
-                const int k = Lay::key_scale_index(q4, 2 * p);
-                const float2 sf = __half22float2(sc2[k / 2]), zf = __half22float2(zc2[k / 2]);
-#pragma unroll
-                for (int r = 0; r < kTile; ++r) {
+                // tokens 16 (2 q4 + pg) + r, read from their ledger fields; with
+                // rotary positions rotated forward by the token's position with
+                // the pair 2p +- D/2 (decoded here too), fp32 products and sums
+                // in the oracle's order
+                auto deq = [&](int pp, int r) -> float2 {
+                    const int k = Lay::key_scale_index(q4, 2 * pp);
+                    const float2 sf = __half22float2(sc2[k / 2]), zf = __half22float2(zc2[k / 2]);
                     int word, field, half;
-                    Lay::key_place(16 * (2 * q4 + pg) + r, 2 * p, &word, &field, &half);
+                    Lay::key_place(16 * (2 * q4 + pg) + r, 2 * pp, &word, &field, &half);
                     const uint32_t wd = cw[word];
                     const float c0 = (float)((wd >> Lay::key_bit(field, 0)) & 3u);
                     const float c1 = (float)((wd >> Lay::key_bit(field, 1)) & 3u);
-                    const __nv_bfloat162 bb = __floats2bfloat162_rn(fmaf(c0, sf.x, zf.x),
-                                                                    fmaf(c1, sf.y, zf.y));
+                    return make_float2(fmaf(c0, sf.x, zf.x), fmaf(c1, sf.y, zf.y));
+                };
+                const bool first_half = 2 * p < D / 2;
+#pragma unroll
+                for (int r = 0; r < kTile; ++r) {
+                    float2 x = deq(p, r);
+                    if (a.rope) {
+                        const float2 y = deq(p ^ (D / 4), r);   // the partner pair
+                        const int pos = kTierSinks + w * kTierW + 16 * (2 * q4 + pg) + r;
+                        const float4 cs = __ldg(reinterpret_cast<const float4*>(a.rope) +
+                                                ((size_t)pos * (D / 2) + ((2 * p) & (D / 2 - 1))) / 2);
+                        x = first_half
+                            ? make_float2(__fsub_rn(__fmul_rn(x.x, cs.x), __fmul_rn(y.x, cs.y)),
+                                          __fsub_rn(__fmul_rn(x.y, cs.z), __fmul_rn(y.y, cs.w)))
+                            : make_float2(__fadd_rn(__fmul_rn(x.x, cs.x), __fmul_rn(y.x, cs.y)),
+                                          __fadd_rn(__fmul_rn(x.y, cs.z), __fmul_rn(y.y, cs.w)));
+                    }
+                    const __nv_bfloat162 bb = __floats2bfloat162_rn(x.x, x.y);
                     dst[r * (D / 2)] = *reinterpret_cast<const uint32_t*>(&bb);
                 }
             } else {

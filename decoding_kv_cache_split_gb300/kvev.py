@@ -52,7 +52,7 @@ EXPORTS = ["kvev_create", "kvev_destroy", "kvev_last_error", "kvev_workspace_siz
            "kvev_profile", "kvev_profile_read", "kvev_launch_count", "kvev_test_wait_timeout",
            "kvev_check_scratch", "kvev_sync",
            "kvev_paged_begin", "kvev_paged_step", "kvev_readmit", "kvev_set_tiers",
-           "kvev_tier_diagnostics",
+           "kvev_tier_diagnostics", "kvev_set_rope",
            "kvev_tier_begin", "kvev_tier_step", "kvev_export_state", "kvev_import_state",
            "kvev_attend_noalloc"]
 
@@ -178,6 +178,7 @@ def lib():
             "kvev_readmit": ([P, P, P, I32, I32, I32, P], I32),
             "kvev_set_tiers": ([P, I64, I64, I32], I32),
             "kvev_tier_diagnostics": ([P, I32, P, P], I32),
+            "kvev_set_rope": ([P, P, I32], I32),
             "kvev_tier_begin": ([P, P, P, I32, P], I32),
             "kvev_tier_step": ([P, P, P, P, P, P, I64, P, P], I32),
             "kvev_export_state": ([P, P, P], I32),
@@ -368,6 +369,12 @@ def kvev_set_tiers(ctx, k_full: int, k_quant: int, omega: int) -> None:
 
 def kvev_tier_diagnostics(ctx, sustain: int, counters=None, stream=None) -> None:
     _check(lib().kvev_tier_diagnostics(ctx, int(sustain), _ptr(counters), _stream(stream)), ctx)
+
+
+def kvev_set_rope(ctx, table, n_pos: int) -> None:
+    """table: the model's (cos, sin) cache [n_pos][d/2][2] fp32 on the device
+    (kept alive by the caller), or None to turn rotary mode off."""
+    _check(lib().kvev_set_rope(ctx, _ptr(table), int(n_pos)), ctx)
 
 
 def kvev_tier_begin(ctx, cache: kvev_tier_cache, state: kvev_tier_state, prefill_tokens: int,
@@ -582,7 +589,8 @@ class TierEvictionPass:
     tensors on the current CUDA device."""
 
     def __init__(self, n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, pages_per_seq,
-                 k_full, k_quant, omega, alpha, aggregation=KVEV_AGG_EMA, device="cuda"):
+                 k_full, k_quant, omega, alpha, aggregation=KVEV_AGG_EMA, rope=None,
+                 device="cuda"):
         import torch
         self.torch = torch
         self.pps, self.max_ctx = int(pages_per_seq), int(max_ctx)
@@ -592,6 +600,10 @@ class TierEvictionPass:
         self.ctx = kvev_create(self.layout, k_full, KVEV_TIER_WINDOW, alpha, 0.0)
         kvev_set_tiers(self.ctx, k_full, k_quant, omega)
         kvev_set_scorer(self.ctx, aggregation, 0)
+        self.rope = None
+        if rope is not None:   # [positions][d/2][2] (cos, sin): rotated keys in the pools
+            self.rope = torch.as_tensor(rope, dtype=torch.float32).to(device).contiguous()
+            kvev_set_rope(self.ctx, self.rope, self.rope.shape[0])
         i32 = dict(dtype=torch.int32, device=device)
         pshape = (batch * self.pps, n_layers, n_kv_heads, 16, head_dim)
         self.k_pool = torch.zeros(pshape, dtype=torch.bfloat16, device=device)

@@ -525,6 +525,28 @@ kvev_status kvev_set_tiers(kvev_ctx* ctx, int64_t k_full, int64_t k_quant, int32
 kvev_status kvev_tier_diagnostics(kvev_ctx* ctx, int32_t sustain, int32_t* counters,
                                   void* stream);
 
+/* Rotary positions (the QEvict review, Sec. 4.4 "Positional handling for
+ * promoted keys"): the cached keys are the model's rotated keys, and
+ * `table` ([n_pos][head_dim/2][2] fp32 (cos, sin) of position p and
+ * frequency j, device, 16-byte aligned, n_pos >= layout->max_ctx; the
+ * caller keeps it alive while the context steps) is the model's own
+ * rotation.  A window is quantized in the pre-rotation domain: each key of
+ * position p is rotated back by p before the codec, channel pairs
+ * (j, j + 64), every product and sum rounded to fp32:
+ *     x_j = y_j cos + y_{j+64} sin,  x_{j+64} = y_{j+64} cos - y_j sin;
+ * every use of an INT2 window rotates the dequantized key forward again
+ * (y_j = x_j cos - x_{j+64} sin, y_{j+64} = x_{j+64} cos + x_j sin):
+ * a promoted window's bf16 key is that value rounded to bf16, and the INT2
+ * windows are attended as bf16 reconstructions (keys rotated, keys and
+ * values rounded to bf16), rebuilt after each routing event into the last
+ * 8 K_q pages of each sequence's range, which kvev_tier_begin sets aside
+ * (pages_per_seq must hold them too; K_q cannot grow past that value later).
+ * table = NULL turns the mode off.  Two-tier contexts with head_dim 128
+ * only; takes effect at the next kvev_tier_begin or kvev_import_state (a
+ * blob imports only into a context whose table is set as the exporter's
+ * was, else KVEV_EINVAL). */
+kvev_status kvev_set_rope(kvev_ctx* ctx, const float* table, int32_t n_pos);
+
 /* Start a tiered run over a prefill of `prefill_tokens` (>= 5) tokens that
  * the caller wrote into the pool: tokens 0..4 in rows 0..4 of page b*pps,
  * token 5 + 16 i + r in row r of page b*pps + 1 + i.  All complete windows

@@ -110,6 +110,7 @@ NULL_CTX_CALLS = {
     "kvev_readmit": lambda L: L.kvev_readmit(None, None, None, 0, 0, 1, None),
     "kvev_set_tiers": lambda L: L.kvev_set_tiers(None, 1, 1, 8),
     "kvev_tier_diagnostics": lambda L: L.kvev_tier_diagnostics(None, 4, None, None),
+    "kvev_set_rope": lambda L: L.kvev_set_rope(None, None, 0),
     "kvev_tier_begin": lambda L: L.kvev_tier_begin(None, None, None, 0, None),
     "kvev_tier_step": lambda L: L.kvev_tier_step(None, None, None, None, None, None, 1, None, None),
     "kvev_export_state": lambda L: L.kvev_export_state(None, None, _out()),

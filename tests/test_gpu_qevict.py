@@ -139,17 +139,40 @@ def compare(tp, P, seqs, b, t, q, kn, vn, stats, check_windows=None, lir=None):
             stats["ledgers"] += 1
 
 
+def check_reconstructions(tp, P, seq, b):
+    """Rotary mode: the last 8 K_q pages of sequence b hold, in ascending
+    window order, the INT2 windows dequantized with keys rotated forward,
+    keys and values rounded to bf16, bit for bit (the oracle's
+    dequantize_window with the window's (cos, sin) rows)."""
+    base = b * tp.pps + tp.pps - 8 * P.k_quant
+    n = 0
+    for e, w in enumerate([w for w in seq.windows if w.tier == "Q"]):
+        k, v = QE.dequantize_window(w.ledger, cs=QE.window_cs(P, w.wid))
+        kb, vb = QE._f32_to_bf16_bits(k), QE._f32_to_bf16_bits(v)
+        for i in range(8):
+            page = base + 8 * e + i
+            assert np.array_equal(_bits(tp.k_pool[page]), kb[:, :, 16 * i:16 * i + 16]), \
+                f"reconstructed keys of window {w.wid}, page {i}"
+            assert np.array_equal(_bits(tp.v_pool[page]), vb[:, :, 16 * i:16 * i + 16]), \
+                f"reconstructed values of window {w.wid}, page {i}"
+        n += 1
+    return n
+
+
 def run_tiers(wl, k_full, k_quant, omega, steps, alpha=0.05, pps_slack=24, cumulative=False,
               sustain=None):
-    """sustain: check the Global LIR counts with that span length."""
+    """sustain: check the Global LIR counts with that span length.  With
+    wl.rope_base set the run is in rotary mode (the workload's table), and
+    on steps without a routing event the reconstruction pages are checked."""
     g = wl.geom
     L0 = wl.L0
     max_ctx = L0 + steps + 8
-    pps = 1 + -(-(L0 - 5) // 16) + pps_slack
+    rope = None if wl.rope_base is None else wl.rope_table(max_ctx)
+    pps = 1 + -(-(L0 - 5) // 16) + pps_slack + (0 if rope is None else 8 * k_quant)
     tp = kvev.TierEvictionPass(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, g.batch,
                                max_ctx, pps, k_full, k_quant, omega, alpha,
                                aggregation=kvev.KVEV_AGG_CUMULATIVE if cumulative
-                               else kvev.KVEV_AGG_EMA)
+                               else kvev.KVEV_AGG_EMA, rope=rope)
     lir = None
     if sustain is not None:
         from oracle import diagnostics as D
@@ -160,16 +183,18 @@ def run_tiers(wl, k_full, k_quant, omega, steps, alpha=0.05, pps_slack=24, cumul
     load(tp, K, V, L0)
     tp.begin(L0)
     P = QE.QParams(g.n_layers, g.n_q_heads, g.n_kv_heads, g.head_dim, k_full, k_quant,
-                   alpha=alpha, omega=omega, cumulative=cumulative)
+                   alpha=alpha, omega=omega, cumulative=cumulative, rope=rope)
     seqs = [QE.QSequence.from_prefill(P, K[:, b], V[:, b]) for b in range(g.batch)]
     stats = {"swaps": 0, "out_rel": 0.0, "m_abs": 0.0, "ledgers": 0, "promoted": 0,
-             "redemoted": 0}
+             "redemoted": 0, "recon": 0}
     for t in range(1, steps + 1):
         q, kn, vn = wl.step_inputs(t)
         tp.step(to_dev_bf16(q), to_dev_bf16(kn), to_dev_bf16(vn))
         kvev.kvev_sync(tp.ctx)
         for b in range(g.batch):
             compare(tp, P, seqs, b, t, q[b], kn[b], vn[b], stats, lir=lir)
+            if rope is not None and t % omega != 0:
+                stats["recon"] += check_reconstructions(tp, P, seqs[b], b)
     if lir is not None:
         stats["lir"] = [(c.events, c.revivals, c.spans) for c in lir[0]]
     kvev.kvev_check_scratch(tp.ctx)   # no scratch region overran its guard band
@@ -202,6 +227,20 @@ def test_tiers_cumulative_window_score_and_global_lir():
     st = run_tiers(wl, 2, 3, 4, 100, sustain=2)
     print("tiers EMA + LIR:", st)
     assert any(r > 0 for _, r, _ in st["lir"]), "no revival in 100 steps of needle drift"
+
+
+def test_tiers_rotary_positions():
+    """Rotary mode (the review's Sec. 4.4): the cache holds rotated keys
+    (rope base 10000); windows are quantized rotated back by position (the
+    ledger bit-exact against the oracle), promoted windows come back rotated
+    forward (bf16 pages bit-exact), the INT2 windows are attended through
+    bf16 reconstructions (checked bit for bit on steps without a routing
+    event), and the outputs stay within the attention tolerance."""
+    wl = Workload(Geometry(2, 32, 8, 128, 2), 5 + 128 * 10 + 40, seed=7, outliers=4, needle=16,
+                  needle_period=16, rope_base=10000.0)
+    st = run_tiers(wl, 2, 3, 4, 60)
+    print("tiers rotary:", st)
+    assert st["ledgers"] > 0 and st["promoted"] > 0 and st["recon"] > 0
 
 
 def test_tiers_no_quantized_tier_and_large_capacity():

@@ -95,3 +95,22 @@ def test_named_workloads_have_the_stated_shapes():
 def test_steps_are_numbered_from_one(step):
     with pytest.raises(ValueError):
         tiny_workload().step_inputs(step)
+
+
+def test_rotary_keys_keep_position_zero_and_pair_norms():
+    """With rope_base the cache holds rotated keys: position 0 is the drawn
+    key itself (angle 0), every (j, j + d/2) pair keeps its length up to the
+    bf16 rounding, and the table is cos / sin of p * base^(-2 j / d)."""
+    from workloads import Geometry, Workload, bf16_bits_to_f32
+    g = Geometry(1, 4, 1, 64, 1)
+    plain = Workload(g, 40, seed=4)
+    rot = Workload(g, 40, seed=4, rope_base=10000.0)
+    kp = bf16_bits_to_f32(plain.prefill()[0]).astype(np.float64)
+    kr = bf16_bits_to_f32(rot.prefill()[0]).astype(np.float64)
+    assert np.array_equal(kp[..., 0, :], kr[..., 0, :])
+    np_, nr = kp[..., :32] ** 2 + kp[..., 32:] ** 2, kr[..., :32] ** 2 + kr[..., 32:] ** 2
+    assert np.allclose(nr, np_, rtol=2e-2, atol=1e-3)
+    t = rot.rope_table(41)
+    assert t.shape == (41, 32, 2) and t.dtype == np.float32
+    assert t[7, 5, 0] == np.float32(np.cos(7 * 10000.0 ** (-10 / 64)))
+    assert t[7, 5, 1] == np.float32(np.sin(7 * 10000.0 ** (-10 / 64)))

@@ -10,6 +10,7 @@ from .gen import (  # noqa: F401
     Workload,
     bf16_bits_to_f32,
     f32_to_bf16_bits,
+    rope_table,
     tiny_workload,
     llama8b_workload,
     needle_blocks,

@@ -39,6 +39,14 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32)
 
 
+def rope_table(n_pos: int, head_dim: int, base: float) -> np.ndarray:
+    """[n_pos][head_dim/2][2] fp32 (cos, sin) of p * base^(-2 j / head_dim),
+    formed in fp64 and rounded once (a model's rotary cache)."""
+    inv = float(base) ** (-2.0 * np.arange(head_dim // 2, dtype=np.float64) / head_dim)
+    ang = np.arange(n_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
+
+
 def _rng(seed: int, family: int, index: int = 0) -> np.random.Generator:
     ss = np.random.SeedSequence(entropy=seed, spawn_key=(family, index))
     return np.random.Generator(np.random.PCG64(ss))
@@ -68,13 +76,17 @@ class Workload:
       needle        number of prefill positions whose mean key, times
                     ``needle_weight``, is added to every query; the set is
                     re-drawn at steps 1, 1+P, 1+2P, ... (P = ``needle_period``)
+      rope_base     rotary positions: every key (prefill and new) is the drawn
+                    key rotated by its position with the table of
+                    ``rope_table`` (pairs (j, j + d/2), the rotation in fp64,
+                    then rounded to bf16), as a model's cache holds them
     """
 
     def __init__(self, geom: Geometry, prefill_len: int, seed: int = 0, *,
                  outliers: int = 0, outlier_sigma: float = 8.0,
                  heavy: int = 0, heavy_scale: float = 4.0,
                  needle: int = 0, needle_period: int = 50,
-                 needle_weight: float = 0.5):
+                 needle_weight: float = 0.5, rope_base: float = None):
         self.geom = geom
         self.L0 = int(prefill_len)
         self.seed = int(seed)
@@ -83,6 +95,7 @@ class Workload:
         self.needle_weight = float(needle_weight)
         self.outlier_sigma = float(outlier_sigma)
         self.heavy_scale = float(heavy_scale)
+        self.rope_base = None if rope_base is None else float(rope_base)
         d = geom.head_dim
         if outliers:
             ch = _rng(seed, _F_OUTLIER).choice(d, size=outliers, replace=False)
@@ -105,6 +118,18 @@ class Workload:
             x[..., self.outlier_channels] *= np.float32(self.outlier_sigma)
         return x
 
+    def rope_table(self, n_pos: int) -> np.ndarray:
+        """The rotary table of this workload's keys (see ``rope_table``)."""
+        return rope_table(n_pos, self.geom.head_dim, self.rope_base)
+
+    def _rotate(self, x: np.ndarray, pos: np.ndarray) -> np.ndarray:
+        """Keys x [..., n, d] rotated by the table rows of positions pos [n]."""
+        cs = self.rope_table(int(pos.max()) + 1)[pos].astype(np.float64)
+        h = x.shape[-1] // 2
+        a, b = x[..., :h].astype(np.float64), x[..., h:].astype(np.float64)
+        c, s_ = cs[..., 0], cs[..., 1]
+        return np.concatenate([a * c - b * s_, b * c + a * s_], axis=-1).astype(np.float32)
+
     def prefill_layer(self, layer: int):
         """bf16 bits of (K, V) for one layer: each [batch][n_kv][L0][d]."""
         g = self.geom
@@ -112,6 +137,8 @@ class Workload:
         k = self._key_block(_rng(self.seed, _F_K, layer), shape)
         if self.heavy_positions.size:
             k[:, :, self.heavy_positions, :] *= np.float32(self.heavy_scale)
+        if self.rope_base is not None:
+            k = self._rotate(k, np.arange(self.L0))
         v = _rng(self.seed, _F_V, layer).standard_normal(shape, dtype=np.float32)
         return f32_to_bf16_bits(k), f32_to_bf16_bits(v)
 
@@ -159,6 +186,8 @@ class Workload:
             q = q + np.float32(self.needle_weight) * nm
         kv_shape = (g.batch, g.n_layers, g.n_kv_heads, g.head_dim)
         kn = self._key_block(_rng(self.seed, _F_KNEW, step), kv_shape)
+        if self.rope_base is not None:   # the new token sits at position L0 + step - 1
+            kn = self._rotate(kn[..., None, :], np.array([self.L0 + step - 1]))[..., 0, :]
         vn = _rng(self.seed, _F_VNEW, step).standard_normal(kv_shape, dtype=np.float32)
         return f32_to_bf16_bits(q), f32_to_bf16_bits(kn), f32_to_bf16_bits(vn)
 
