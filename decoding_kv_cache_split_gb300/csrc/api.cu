@@ -104,6 +104,11 @@ struct Workspace {
     float* part_o2 = nullptr;         // INT2 attention partials
     float* part_ml2 = nullptr;
     int32_t* lir_streak = nullptr;    // [batch][max_windows] Global LIR streaks
+    int32_t* t_rslot = nullptr;       // rotary mode: [batch][max_windows] reconstruction slots,
+    int32_t* t_rfree = nullptr;       // free-slot stacks and the windows to reconstruct
+    int32_t* t_nrfree = nullptr;
+    int32_t* t_rlist = nullptr;
+    int32_t* t_nrlist = nullptr;
     // token mode, scorer weightings (VNorm, entropy)
     float* part_e = nullptr;          // [slots][G]
     float* part_vn = nullptr;         // [slots]
@@ -218,6 +223,11 @@ Workspace carve(const kvev_layout& L, int64_t budget, int64_t slots, char* base,
         w.part_o2 = (float*)take((size_t)slots2 * G * L.head_dim * 4, "part_o2");
         w.part_ml2 = (float*)take((size_t)slots2 * G * 2 * 4, "part_ml2");
         w.lir_streak = (int32_t*)take(B * MW * 4, "lir_streak");
+        w.t_rslot = (int32_t*)take(B * MW * 4, "t_rslot");
+        w.t_rfree = (int32_t*)take(B * MW * 4, "t_rfree");
+        w.t_nrfree = (int32_t*)take(B * 4, "t_nrfree");
+        w.t_rlist = (int32_t*)take(B * MW * 4, "t_rlist");
+        w.t_nrlist = (int32_t*)take(B * 4, "t_nrlist");
     }
     w.bytes = off;
     return w;
@@ -317,7 +327,8 @@ struct kvev_ctx {
     // rotary positions: the model's (cos, sin) table of the run (null: off)
     // and the one kvev_set_rope gave for the next run, the pages at the end
     // of each sequence's range that hold the INT2 windows' bf16
-    // reconstructions, and whether they match the current INT2 list
+    // reconstructions, and whether the device's slot map is current (it is
+    // not kept in a checkpoint: after an import the next step rebuilds it)
     const float* rope = nullptr;
     const float* rope_next = nullptr;
     int t_scratch = 0;
@@ -1354,6 +1365,11 @@ TierArgs tier_args(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_tier_state
     a.lir_sustain = c->lir_sustain;
     a.rope = c->rope;
     a.scratch = c->t_scratch;
+    a.rslot = c->ws.t_rslot;
+    a.rfree = c->ws.t_rfree;
+    a.n_rfree = c->ws.t_nrfree;
+    a.rlist = c->ws.t_rlist;
+    a.n_rlist = c->ws.t_nrlist;
     return a;
 }
 
@@ -1448,7 +1464,7 @@ kvev_status kvev_tier_begin(kvev_ctx* c, const kvev_tier_cache* tc, const kvev_t
     c->t_tl = hist % kTierW;
     c->t_first_u = 0;
     c->t_nf = c->t_nq = 0;
-    c->t_recon_valid = false;
+    c->t_recon_valid = true;   // the begin kernel frees every reconstruction slot
     c->len = prefill_tokens;
     c->prefill_len = prefill_tokens;
     c->step = 0;
@@ -1506,14 +1522,18 @@ kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const 
     const kvev_layout& Ly = c->lay;
     const int G = c->group;
     TierArgs ta = tier_args(c, tc, ts, t);
+    // rotary positions: the INT2 windows are attended as bf16 reconstructions
+    // (keys rotated forward), made when a window enters the tier; after an
+    // import the append gives every INT2 window a slot and all are rebuilt
+    const bool recon = c->rope != nullptr;
+    const bool rebuild = recon && !c->t_recon_valid;
+    TierArgs tb = ta;
+    tb.rebuild = rebuild ? 1 : 0;
     rc = timed_launch(c, kProfAppend, s, "tier append", [&] {
-        return launch_tier_append(ta, (const uint16_t*)k_new, (const uint16_t*)v_new, s);
+        return launch_tier_append(tb, (const uint16_t*)k_new, (const uint16_t*)v_new, s);
     });
     if (rc != KVEV_OK) return rc;
-    // rotary positions: the INT2 windows are attended as bf16 reconstructions
-    // (keys rotated forward), rebuilt when the INT2 list has changed
-    const bool recon = c->rope != nullptr;
-    if (recon && c->t_nq > 0 && !c->t_recon_valid) {
+    if (rebuild) {
         TierArgs ra = ta;
         ra.recon = 1;
         rc = timed_launch(c, kProfCompact, s, "reconstruct",
@@ -1622,6 +1642,12 @@ kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const 
             rc = timed_launch(c, kProfCompact, s, "promote", [&] {
                 return launch_tier_promote(ta, n_prom_max, c->num_sms, s);
             });
+        if (rc == KVEV_OK && recon) {   // the windows entering the INT2 tier (codes written)
+            TierArgs ra = ta;
+            ra.recon = 1;
+            rc = timed_launch(c, kProfCompact, s, "reconstruct",
+                              [&] { return launch_tier_promote(ra, nq2, c->num_sms, s); });
+        }
         if (rc == KVEV_OK)
             rc = timed_launch(c, kProfCompact, s, "finish",
                               [&] { return launch_tier_finish(ta, s); });
@@ -1631,7 +1657,6 @@ kvev_status kvev_tier_step(kvev_ctx* c, const void* q, const void* k_new, const 
         c->t_first_u += n_aged;
         c->t_nf = nf2;
         c->t_nq = nq2;
-        c->t_recon_valid = false;   // the INT2 list may have changed
     }
     c->t_nw = nw;
     c->t_tl = tl;

@@ -430,11 +430,20 @@ struct TierArgs {
     int32_t lir_sustain;
     // Rotary positions ("QEvict" review Sec. 4.4): keys are quantized rotated
     // back by their positions and rotated forward again on promotion; the
-    // INT2 windows are attended as a bf16 reconstruction in the last
-    // `scratch` pages of each sequence's range (null rope: off, scratch 0)
+    // INT2 windows are attended as bf16 reconstructions in the last
+    // `scratch` pages of each sequence's range, PW pages per reconstruction
+    // slot (null rope: off, scratch 0).  A window holds a slot while it is
+    // INT2: routing frees the slots of windows leaving the tier and gives
+    // the entering ones a slot and a reconstruction.
     const float* rope;     // [positions][D/2][2] fp32 (cos, sin)
     int32_t scratch;
-    int32_t recon;         // tier_promote_kernel: 1 = reconstruct the INT2 list into scratch
+    int32_t* rslot;        // [b][max_windows] reconstruction slot (-1: none)
+    int32_t* rfree;        // [b][max_windows] free-slot stacks
+    int32_t* n_rfree;      // [b]
+    int32_t* rlist;        // [b][max_windows] windows to reconstruct + counts
+    int32_t* n_rlist;
+    int32_t recon;         // tier_promote_kernel: 1 = reconstruct the windows of rlist
+    int32_t rebuild;       // tier_append_kernel: 1 = slots and rlist anew from the INT2 list
 };
 
 // ---- programmatic dependent launch ----------------------------------------

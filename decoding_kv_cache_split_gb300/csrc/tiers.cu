@@ -96,6 +96,17 @@ __global__ void __launch_bounds__(kBook) tier_begin_kernel(const TierArgs a, int
     const int avail = pps - a.scratch;   // the last `scratch` pages hold reconstructions
     for (int k = threadIdx.x; k < avail - used; k += blockDim.x)   // lowest free page on top
         a.c.free_pages[(size_t)base + k] = base + avail - 1 - k;
+    if (a.rope) {   // no INT2 window yet: every reconstruction slot is free, lowest on top
+        const int n_slots = a.scratch / (kTierW / kTile);
+        for (int w = threadIdx.x; w < MW; w += blockDim.x) {
+            a.rslot[(size_t)b * MW + w] = -1;
+            if (w < n_slots) a.rfree[(size_t)b * MW + w] = n_slots - 1 - w;
+        }
+        if (threadIdx.x == 0) {
+            a.n_rfree[b] = n_slots;
+            a.n_rlist[b] = 0;
+        }
+    }
     if (threadIdx.x == 0) {
         a.c.n_free[b] = avail - used;
         a.st.n_windows[b] = nw;
@@ -225,13 +236,33 @@ __global__ void __launch_bounds__(kBook) tier_append_kernel(const TierArgs a,
         blen[j0 + i] = min(kTile, tl - i * kTile);
     }
     int n_rec = 0;
-    if (a.rope) {   // rotary mode: the INT2 windows' bf16 reconstructions, list order
+    if (a.rope) {   // rotary mode: the INT2 windows' bf16 reconstructions
         __syncthreads();   // the INT2 list is complete
+        const int n_slots = a.scratch / PW;
+        int32_t* rslot = a.rslot + (size_t)b * MW;
+        if (a.rebuild) {   // slot e for the e-th INT2 window; all of them to reconstruct
+            for (int w = threadIdx.x; w < MW; w += blockDim.x) rslot[w] = -1;
+            __syncthreads();
+            for (int k = threadIdx.x; k < n_q; k += blockDim.x) {
+                const int w = a.qlist[(size_t)b * MW + k];
+                rslot[w] = k < n_slots ? k : -1;   // (k_q never exceeds the slots)
+                a.rlist[(size_t)b * MW + k] = w;
+            }
+            for (int k = threadIdx.x; k < n_slots - n_q; k += blockDim.x)
+                a.rfree[(size_t)b * MW + k] = n_slots - 1 - k;
+            if (threadIdx.x == 0) {
+                a.n_rfree[b] = max(n_slots - n_q, 0);
+                a.n_rlist[b] = n_q;
+            }
+            __syncthreads();
+        }
         const int jq = j0 + n_tail, sbase = b * pps + pps - a.scratch;
         for (int u = threadIdx.x; u < n_q * PW; u += blockDim.x) {
             const int k = u / PW, i = u % PW;
             const int w = a.qlist[(size_t)b * MW + k];
-            bt[jq + u] = sbase + u;
+            const int slot = rslot[w];
+            // a window without a slot (flagged by the routing) reads the sink page
+            bt[jq + u] = slot >= 0 && slot < n_slots ? sbase + slot * PW + i : b * pps;
             bpos[jq + u] = kTierSinks + w * kTierW + i * kTile;
             blen[jq + u] = kTile;
         }
@@ -306,6 +337,7 @@ __global__ void __launch_bounds__(256) tier_score_kernel(const TierArgs a) {
 __global__ void __launch_bounds__(kBook) tier_route_kernel(const TierArgs a) {
     __shared__ unsigned long long keys[kTierRouteCap];
     __shared__ uint8_t nt[kTierRouteCap];
+    __shared__ uint8_t enters[kTierRouteCap];   // rotary mode: the window enters the INT2 tier
     __shared__ int red[32];
     griddep_wait();
     griddep_release();
@@ -358,9 +390,12 @@ __global__ void __launch_bounds__(kBook) tier_route_kernel(const TierArgs a) {
         }
     }
     __syncthreads();
-    // transitions: lists for quantization, promotion and freeing
-    int nq = 0, np = 0, nf = 0;
+    // transitions: lists for quantization, promotion and freeing; in rotary
+    // mode the reconstruction slots of windows leaving the INT2 tier return
+    // to their stack
+    int nq = 0, np = 0, nf = 0, nl = 0;
     const int free0 = a.c.n_free[b];
+    const int rfree0 = a.rope ? a.n_rfree[b] : 0;
     for (int w0 = 0; w0 < nw; w0 += blockDim.x) {
         const int w = w0 + threadIdx.x;
         uint8_t o = KVEV_TIER_NONE, t = KVEV_TIER_NONE;
@@ -373,12 +408,21 @@ __global__ void __launch_bounds__(kBook) tier_route_kernel(const TierArgs a) {
         const bool quant = is_bf16_tier(o) && t == KVEV_TIER_QUANT && !codes;
         const bool prom = o == KVEV_TIER_QUANT && t == KVEV_TIER_FULL;
         const bool frees = is_bf16_tier(o) && (t == KVEV_TIER_QUANT || t == KVEV_TIER_EVICTED);
-        int tq, tp, tf;
+        const bool leaves = a.rope && o == KVEV_TIER_QUANT && t != KVEV_TIER_QUANT;
+        int tq, tp, tf, tl;
         const int oq = scan_excl(quant ? 1 : 0, red, &tq);
         const int op = scan_excl(prom ? 1 : 0, red, &tp);
         const int of = scan_excl(frees ? 1 : 0, red, &tf);
+        const int ol = a.rope ? scan_excl(leaves ? 1 : 0, red, &tl) : (tl = 0, 0);
         if (w < nw) {
             const size_t wi = (size_t)b * MW + w;
+            if (a.rope) {
+                enters[w] = o != KVEV_TIER_QUANT && t == KVEV_TIER_QUANT;
+                if (leaves) {
+                    if (rfree0 + nl + ol < MW) a.rfree[(size_t)b * MW + rfree0 + nl + ol] = a.rslot[wi];
+                    a.rslot[wi] = -1;
+                }
+            }
             if (quant) a.quant_list[(size_t)b * MW + nq + oq] = w;
             if (frees) a.free_list[(size_t)b * MW + nf + of] = w;
             if (prom) {   // 8 pages from the top of the free stack (pages freed before this event)
@@ -397,6 +441,32 @@ __global__ void __launch_bounds__(kBook) tier_route_kernel(const TierArgs a) {
         nq += tq;
         np += tp;
         nf += tf;
+        nl += tl;
+    }
+    if (a.rope) {   // entering windows pop slots (the top first) and are listed for reconstruction
+        __syncthreads();
+        const int top = rfree0 + nl;
+        int ne = 0;
+        for (int w0 = 0; w0 < nw; w0 += blockDim.x) {
+            const int w = w0 + threadIdx.x;
+            const bool e = w < nw && enters[w];
+            int te;
+            const int oe = scan_excl(e ? 1 : 0, red, &te);
+            if (e) {
+                const int k = ne + oe, at = top - 1 - k;
+                // every INT2 window holds one slot and there are at least K_q:
+                // the stack cannot run dry
+                const bool ok = at >= 0 && at < MW;
+                if (!ok) atomicOr(a.status, kStatusNoPage);
+                a.rslot[(size_t)b * MW + w] = ok ? a.rfree[(size_t)b * MW + at] : -1;
+                a.rlist[(size_t)b * MW + k] = w;
+            }
+            ne += te;
+        }
+        if (threadIdx.x == 0) {
+            a.n_rfree[b] = max(top - ne, 0);
+            a.n_rlist[b] = ne;
+        }
     }
     if (threadIdx.x == 0) {
         a.n_quant[b] = nq;
@@ -659,12 +729,13 @@ __global__ void __launch_bounds__(kPromThreads) tier_promote_kernel(const TierAr
     (void)max_items;
     const int LG = a.n_layers * a.n_kv, MW = a.c.max_windows;
     // promotion: the routing event's promoted windows into their new pages;
-    // reconstruction (rotary mode): every INT2 window, list entry e into the
-    // scratch pages pps - scratch + e PW .. + PW - 1 of its sequence
-    const int32_t* counts = a.recon ? a.nq : a.n_prom;
-    const int32_t* list = a.recon ? a.qlist : a.prom_list;
+    // reconstruction (rotary mode): the windows of rlist into the scratch
+    // pages pps - scratch + slot PW .. + PW - 1 of their sequence
+    const int32_t* counts = a.recon ? a.n_rlist : a.n_prom;
+    const int32_t* list = a.recon ? a.rlist : a.prom_list;
     const int64_t total = 2 * item_count(counts, a.batch, LG);
     const int tid = threadIdx.x;
+    const int n_slots = a.scratch / PW;
     for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
         const int kv = (int)(it & 1);
         int b, e, lg;
@@ -672,7 +743,9 @@ __global__ void __launch_bounds__(kPromThreads) tier_promote_kernel(const TierAr
         const int w = list[(size_t)b * MW + e];
         const int l = lg / a.n_kv, g = lg % a.n_kv;
         const int32_t* pages = a.st.win_pages + ((size_t)b * MW + w) * PW;
-        const int rec0 = b * a.c.pages_per_seq + a.c.pages_per_seq - a.scratch + e * PW;
+        const int slot = a.recon ? a.rslot[(size_t)b * MW + w] : 0;
+        if (a.recon && (slot < 0 || slot >= n_slots)) continue;   // (flagged by the routing)
+        const int rec0 = b * a.c.pages_per_seq + a.c.pages_per_seq - a.scratch + slot * PW;
         const uint4* led = reinterpret_cast<const uint4*>(
             reinterpret_cast<const unsigned char*>(a.c.ledger) +
             ((((size_t)b * MW + w) * a.n_layers + l) * a.n_kv + g) * Lay::BYTES +
@@ -687,43 +760,61 @@ __global__ void __launch_bounds__(kPromThreads) tier_promote_kernel(const TierAr
         uint32_t* pool = reinterpret_cast<uint32_t*>(kv ? a.c.v_pool : a.c.k_pool);
         const int p = tid & 63;   // channel pair 2p, 2p + 1
         const int q4 = tid >> 6;  // key group / quarter of the window: pages 2 q4, 2 q4 + 1
+        auto page_of = [&](int i) { return a.recon ? rec0 + i : pages[i]; };
+        auto row_ptr = [&](int page, int pair) {
+            return pool + ((((int64_t)page * a.n_layers + l) * a.n_kv + g) * kTile) * D / 2 + pair;
+        };
+        // key channels 2 pp, 2 pp + 1 of token 16 ti + r (one field, halves 0 and 1)
+        auto deq = [&](int pp, int ti, int r) -> float2 {
+            const int k = Lay::key_scale_index(q4, 2 * pp);
+            const float2 sf = __half22float2(sc2[k / 2]), zf = __half22float2(zc2[k / 2]);
+            int word, field, half;
+            Lay::key_place(16 * ti + r, 2 * pp, &word, &field, &half);
+            const uint32_t wd = cw[word];
+            const float c0 = (float)((wd >> Lay::key_bit(field, 0)) & 3u);
+            const float c1 = (float)((wd >> Lay::key_bit(field, 1)) & 3u);
+            return make_float2(fmaf(c0, sf.x, zf.x), fmaf(c1, sf.y, zf.y));
+        };
+        if (kv == 0 && a.rope) {
+            // keys with rotary positions: thread (q4, p) takes page 2 q4 + p / 32
+            // and the pairs pp = p mod 32 and pp + D/4 (channels j, j + 1 and
+            // j + D/2, j + D/2 + 1 for j = 2 pp), which rotate together by the
+            // token's position, fp32 products and sums in the oracle's order
+            const int pp = p & (D / 4 - 1), ti = 2 * q4 + (p >> 5);
+            const int page = page_of(ti);
+            if (page >= 0) {
+                uint32_t* dst = row_ptr(page, pp);
+                const float4* cs_row = reinterpret_cast<const float4*>(a.rope) +
+                                       ((size_t)(kTierSinks + w * kTierW + 16 * ti) * (D / 2) + 2 * pp) / 2;
+#pragma unroll 4
+                for (int r = 0; r < kTile; ++r) {
+                    const float2 x = deq(pp, ti, r), y = deq(pp + D / 4, ti, r);
+                    const float4 cs = __ldg(cs_row + (size_t)r * (D / 4));   // cos, sin of j, j + 1
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(
+                        __fsub_rn(__fmul_rn(x.x, cs.x), __fmul_rn(y.x, cs.y)),
+                        __fsub_rn(__fmul_rn(x.y, cs.z), __fmul_rn(y.y, cs.w)));
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(
+                        __fadd_rn(__fmul_rn(y.x, cs.x), __fmul_rn(x.x, cs.y)),
+                        __fadd_rn(__fmul_rn(y.y, cs.z), __fmul_rn(x.y, cs.w)));
+                    dst[r * (D / 2)] = *reinterpret_cast<const uint32_t*>(&lo);
+                    dst[r * (D / 2) + D / 4] = *reinterpret_cast<const uint32_t*>(&hi);
+                }
+            }
+            __syncthreads();
+            continue;
+        }
 #pragma unroll
         for (int pg = 0; pg < 2; ++pg) {
-            const int page = a.recon ? rec0 + 2 * q4 + pg : pages[2 * q4 + pg];
+            const int page = page_of(2 * q4 + pg);
             if (page < 0) continue;   // no page could be taken for this promotion
-            uint32_t* dst = pool + ((((int64_t)page * a.n_layers + l) * a.n_kv + g) * kTile) * D / 2 + p;
+            uint32_t* dst = row_ptr(page, p);
             const uint32_t* cwt = cw + (2 * q4 + pg) * D;   // code words of this 16-token tile
             if (kv == 0) {
-                // keys: channels 2p, 2p + 1 (one field, halves 0 and 1) of the
-                // tokens 16 (2 q4 + pg) + r, read from their ledger fields; with
-                // rotary positions rotated forward by the token's position with
-                // the pair 2p +- D/2 (decoded here too), fp32 products and sums
-                // in the oracle's order
-                auto deq = [&](int pp, int r) -> float2 {
-                    const int k = Lay::key_scale_index(q4, 2 * pp);
-                    const float2 sf = __half22float2(sc2[k / 2]), zf = __half22float2(zc2[k / 2]);
-                    int word, field, half;
-                    Lay::key_place(16 * (2 * q4 + pg) + r, 2 * pp, &word, &field, &half);
-                    const uint32_t wd = cw[word];
-                    const float c0 = (float)((wd >> Lay::key_bit(field, 0)) & 3u);
-                    const float c1 = (float)((wd >> Lay::key_bit(field, 1)) & 3u);
-                    return make_float2(fmaf(c0, sf.x, zf.x), fmaf(c1, sf.y, zf.y));
-                };
-                const bool first_half = 2 * p < D / 2;
+                // keys: channels 2p, 2p + 1 of the tokens 16 (2 q4 + pg) + r,
+                // read from their ledger fields
 #pragma unroll
                 for (int r = 0; r < kTile; ++r) {
-                    float2 x = deq(p, r);
-                    if (a.rope) {
-                        const float2 y = deq(p ^ (D / 4), r);   // the partner pair
-                        const int pos = kTierSinks + w * kTierW + 16 * (2 * q4 + pg) + r;
-                        const float4 cs = __ldg(reinterpret_cast<const float4*>(a.rope) +
-                                                ((size_t)pos * (D / 2) + ((2 * p) & (D / 2 - 1))) / 2);
-                        x = first_half
-                            ? make_float2(__fsub_rn(__fmul_rn(x.x, cs.x), __fmul_rn(y.x, cs.y)),
-                                          __fsub_rn(__fmul_rn(x.y, cs.z), __fmul_rn(y.y, cs.w)))
-                            : make_float2(__fadd_rn(__fmul_rn(x.x, cs.x), __fmul_rn(y.x, cs.y)),
-                                          __fadd_rn(__fmul_rn(x.y, cs.z), __fmul_rn(y.y, cs.w)));
-                    }
+                    const float2 x = deq(p, 2 * q4 + pg, r);
                     const __nv_bfloat162 bb = __floats2bfloat162_rn(x.x, x.y);
                     dst[r * (D / 2)] = *reinterpret_cast<const uint32_t*>(&bb);
                 }

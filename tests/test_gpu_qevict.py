@@ -140,30 +140,38 @@ def compare(tp, P, seqs, b, t, q, kn, vn, stats, check_windows=None, lir=None):
 
 
 def check_reconstructions(tp, P, seq, b):
-    """Rotary mode: the last 8 K_q pages of sequence b hold, in ascending
-    window order, the INT2 windows dequantized with keys rotated forward,
-    keys and values rounded to bf16, bit for bit (the oracle's
-    dequantize_window with the window's (cos, sin) rows)."""
-    base = b * tp.pps + tp.pps - 8 * P.k_quant
-    n = 0
-    for e, w in enumerate([w for w in seq.windows if w.tier == "Q"]):
+    """Rotary mode: each INT2 window of sequence b has a reconstruction slot
+    of its own among the last 8 K_q pages of the sequence's range, holding
+    the window dequantized with keys rotated forward, keys and values rounded
+    to bf16, bit for bit (the oracle's dequantize_window with the window's
+    (cos, sin) rows).  Slots are the device's to assign: each window's is
+    found by its content."""
+    n_slots = P.k_quant
+    base = b * tp.pps + tp.pps - 8 * n_slots
+    kp = _bits(tp.k_pool[base:base + 8 * n_slots])    # [slot * 8 + i][Ly][Hkv][16][d]
+    vp = _bits(tp.v_pool[base:base + 8 * n_slots])
+    used = set()
+    for w in [w for w in seq.windows if w.tier == "Q"]:
         k, v = QE.dequantize_window(w.ledger, cs=QE.window_cs(P, w.wid))
         kb, vb = QE._f32_to_bf16_bits(k), QE._f32_to_bf16_bits(v)
-        for i in range(8):
-            page = base + 8 * e + i
-            assert np.array_equal(_bits(tp.k_pool[page]), kb[:, :, 16 * i:16 * i + 16]), \
-                f"reconstructed keys of window {w.wid}, page {i}"
-            assert np.array_equal(_bits(tp.v_pool[page]), vb[:, :, 16 * i:16 * i + 16]), \
-                f"reconstructed values of window {w.wid}, page {i}"
-        n += 1
-    return n
+        want_k = kb.reshape(P.n_layers, P.n_kv_heads, 8, 16, -1).transpose(2, 0, 1, 3, 4)
+        want_v = vb.reshape(P.n_layers, P.n_kv_heads, 8, 16, -1).transpose(2, 0, 1, 3, 4)
+        slots = [s_ for s_ in range(n_slots)
+                 if np.array_equal(kp[8 * s_:8 * s_ + 8], want_k)]
+        assert slots, f"no slot holds the reconstructed keys of window {w.wid}"
+        s_ = slots[0]
+        assert s_ not in used, f"window {w.wid} shares slot {s_}"
+        used.add(s_)
+        assert np.array_equal(vp[8 * s_:8 * s_ + 8], want_v), \
+            f"reconstructed values of window {w.wid}"
+    return len(used)
 
 
 def run_tiers(wl, k_full, k_quant, omega, steps, alpha=0.05, pps_slack=24, cumulative=False,
               sustain=None):
     """sustain: check the Global LIR counts with that span length.  With
     wl.rope_base set the run is in rotary mode (the workload's table), and
-    on steps without a routing event the reconstruction pages are checked."""
+    after every step the reconstruction pages are checked."""
     g = wl.geom
     L0 = wl.L0
     max_ctx = L0 + steps + 8
@@ -193,7 +201,7 @@ def run_tiers(wl, k_full, k_quant, omega, steps, alpha=0.05, pps_slack=24, cumul
         kvev.kvev_sync(tp.ctx)
         for b in range(g.batch):
             compare(tp, P, seqs, b, t, q[b], kn[b], vn[b], stats, lir=lir)
-            if rope is not None and t % omega != 0:
+            if rope is not None:
                 stats["recon"] += check_reconstructions(tp, P, seqs[b], b)
     if lir is not None:
         stats["lir"] = [(c.events, c.revivals, c.spans) for c in lir[0]]
@@ -234,8 +242,9 @@ def test_tiers_rotary_positions():
     (rope base 10000); windows are quantized rotated back by position (the
     ledger bit-exact against the oracle), promoted windows come back rotated
     forward (bf16 pages bit-exact), the INT2 windows are attended through
-    bf16 reconstructions (checked bit for bit on steps without a routing
-    event), and the outputs stay within the attention tolerance."""
+    bf16 reconstructions, made as windows enter the INT2 tier (checked bit
+    for bit after every step), and the outputs stay within the attention
+    tolerance."""
     wl = Workload(Geometry(2, 32, 8, 128, 2), 5 + 128 * 10 + 40, seed=7, outliers=4, needle=16,
                   needle_period=16, rope_base=10000.0)
     st = run_tiers(wl, 2, 3, 4, 60)
