@@ -497,6 +497,9 @@ def main():
                     help="two-tier workload: routing interval")
     ap.add_argument("--no-sweep", action="store_true",
                     help="two-tier workload: skip the routing-interval sweep")
+    ap.add_argument("--rope", action="store_true",
+                    help="two-tier workload: the whole run in rotary mode (rope base 10000; "
+                         "INT2 windows attended as bf16 reconstructions)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1184,18 +1187,28 @@ def bench_tiers(args, rank, world, local_rank, steps=None, omega=None, quiet=Fal
     W = dict(TIERS)
     if omega is not None:
         W["omega"] = int(omega)
+    rope_main = bool(getattr(args, "rope", False))
+    if rope_main:   # the rotary record below would repeat the main run
+        rotary = False
     if args.layers != WORKLOAD["n_layers"] or args.prefill != WORKLOAD["prefill"]:
         pre = args.prefill if args.prefill != WORKLOAD["prefill"] else W["prefill"]
         W.update(workload=f"profiling case: {args.layers} layers, {W['batch']} x {pre} tokens",
                  n_layers=args.layers, prefill=pre)
+    if rope_main:
+        W["workload"] += ", rotary positions (rope base 10000)"
     Ly, b, L0 = W["n_layers"], W["batch"], W["prefill"]
     n_steps = steps if steps is not None else args.steps
     max_ctx = L0 + max(n_steps, args.warmup, sweep_steps) + 16
     wl = TierDeviceWorkload(0, n_layers=Ly, batch=b, prefill=L0)
     # bf16 pages: prefill, promotions and, in rotary mode, the reconstructions
-    pps = wl.n_pages + 16 + 8 * W["k_full"] + (8 * W["k_quant"] if rotary else 0)
+    pps = wl.n_pages + 16 + 8 * W["k_full"] + (8 * W["k_quant"] if rotary or rope_main else 0)
+    rope_main_table = None
+    if rope_main:
+        from workloads import rope_table
+        rope_main_table = rope_table(max_ctx, W["head_dim"], 10000.0)
     tp = kvev.TierEvictionPass(Ly, W["n_q_heads"], W["n_kv_heads"], W["head_dim"], b, max_ctx,
-                               pps, W["k_full"], W["k_quant"], W["omega"], W["alpha"])
+                               pps, W["k_full"], W["k_quant"], W["omega"], W["alpha"],
+                               rope=rope_main_table)
     wl.fill(torch, tp.k_pool, tp.v_pool, pps)
     last = max(n_steps, args.warmup, sweep_steps if omega_sweep else 0)
     inputs = [wl.step_inputs(torch, t, tp.k_pool, pps) for t in range(1, last + 1)]

@@ -717,7 +717,7 @@ __device__ __forceinline__ float2 reg_codes(uint32_t x) {   // x rotated to slot
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPromThreads) tier_promote_kernel(const TierArgs a,
+__global__ void __launch_bounds__(kPromThreads, 4) tier_promote_kernel(const TierArgs a,
                                                                     int max_items) {
     using Lay = LedgerLayout<D>;
     static_assert(D == 128, "ledger registers are laid out for head_dim 128");
@@ -957,7 +957,7 @@ cudaError_t launch_tier_promote(const TierArgs& a, int max_items, int num_sms, c
     if (max_items <= 0) return cudaSuccess;
     if (a.head_dim != 128) return cudaErrorInvalidValue;
     const int64_t items = 2LL * a.batch * max_items * a.n_layers * a.n_kv;
-    const int grid = (int)std::min<int64_t>(items, 8LL * num_sms);
+    const int grid = (int)std::min<int64_t>(items, 4LL * num_sms);
     return launch_pdl(tier_promote_kernel<128>, dim3(grid), dim3(kPromThreads), 0, s, a,
                       max_items);
 }
