@@ -538,9 +538,12 @@ kvev_status kvev_tier_diagnostics(kvev_ctx* ctx, int32_t sustain, int32_t* count
  * (y_j = x_j cos - x_{j+64} sin, y_{j+64} = x_{j+64} cos + x_j sin):
  * a promoted window's bf16 key is that value rounded to bf16, and the INT2
  * windows are attended as bf16 reconstructions (keys rotated, keys and
- * values rounded to bf16), rebuilt after each routing event into the last
- * 8 K_q pages of each sequence's range, which kvev_tier_begin sets aside
- * (pages_per_seq must hold them too; K_q cannot grow past that value later).
+ * values rounded to bf16).  These live in the last 8 K_q pages of each
+ * sequence's range, which kvev_tier_begin sets aside (pages_per_seq must
+ * hold them too; K_q cannot grow past that value later): 8 pages per INT2
+ * window, written at the routing event where the window enters the INT2
+ * tier and kept while it stays there; the first step after
+ * kvev_import_state writes them all again.
  * table = NULL turns the mode off.  Two-tier contexts with head_dim 128
  * only; takes effect at the next kvev_tier_begin or kvev_import_state (a
  * blob imports only into a context whose table is set as the exporter's
