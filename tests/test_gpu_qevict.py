@@ -331,3 +331,67 @@ def test_tiers_full_size_three_routing_events():
     assert stats["ledgers"] > 0
     kvev.kvev_check_scratch(tp.ctx)   # no scratch region overran its guard band
     tp.close()
+
+
+@pytest.mark.slow
+def test_tiers_full_size_rotary_two_routing_events():
+    """Rotary mode on the full two-tier workload: 32 layers, 4 sequences of
+    131072 tokens (positions up to 131087 in the table), K_f 51, K_q 204,
+    routing every 8 steps; steps 1-16 of sequence 0 against the oracle with
+    the same table: the first routing event quantizes 204 windows rotated
+    back and reconstructs them rotated forward, the second moves windows
+    between the tiers (promotions rotated forward, reconstructions of the
+    windows entering INT2).  Ledger entries, bf16 pages and reconstructions
+    are compared bit for bit on sampled windows, outputs within 2e-3.  The
+    device draws of the keys carry no rotation: the rotation's arithmetic
+    is the same for any key values."""
+    from workloads import rope_table
+    from workloads.device import TierDeviceWorkload
+    L0, batch, Ly = 131072, 4, 32
+    max_ctx = L0 + 32
+    rope = rope_table(max_ctx, 128, 10000.0)
+    wl = TierDeviceWorkload(0, n_layers=Ly, batch=batch, prefill=L0)
+    pps = wl.n_pages + 16 + 8 * 51 + 8 * 204
+    tp = kvev.TierEvictionPass(Ly, 32, 8, 128, batch, max_ctx, pps, 51, 204, 8, 0.05, rope=rope)
+    wl.fill(torch, tp.k_pool, tp.v_pool, pps)
+    T = 16
+    inputs = [wl.step_inputs(torch, t, tp.k_pool, pps) for t in range(1, T + 1)]
+    hist = L0 - 5
+    pages = slice(0, wl.n_pages)
+    kp, vp = _bits(tp.k_pool[pages]), _bits(tp.v_pool[pages])
+    def tokens(p):
+        rest = p[1:].transpose(1, 2, 0, 3, 4).reshape(Ly, 8, -1, 128)[:, :, :hist]
+        return np.concatenate([p[0, :, :, :5], rest], axis=2)
+    P = QE.QParams(Ly, 32, 8, 128, 51, 204, alpha=0.05, omega=8, rope=rope)
+    seqs = [QE.QSequence.from_prefill(P, tokens(kp), tokens(vp))]
+    del kp, vp
+    tp.begin(L0)
+    sample = set(range(0, 1023, 61))
+    stats = {"swaps": 0, "out_rel": 0.0, "m_abs": 0.0, "ledgers": 0, "promoted": 0,
+             "redemoted": 0, "recon": 0}
+    base = tp.pps - 8 * 204                      # sequence 0's reconstruction slots
+    for t in range(1, T + 1):
+        q, kn, vn = inputs[t - 1]
+        tp.step(q, kn, vn)
+        kvev.kvev_sync(tp.ctx)
+        compare(tp, P, seqs, 0, t, _bits(q[0]), _bits(kn[0]), _bits(vn[0]), stats,
+                check_windows=sample)
+        if t % 8 == 0:   # sampled INT2 windows: a slot holds the reconstruction
+            probe = _bits(tp.k_pool[base:base + 8 * 204:8, 0, 0])   # first page, layer 0, head 0
+            for w in seqs[0].windows:
+                if w.tier != "Q" or w.wid not in sample:
+                    continue
+                k, v = QE.dequantize_window(w.ledger, cs=QE.window_cs(P, w.wid))
+                kb, vb = QE._f32_to_bf16_bits(k), QE._f32_to_bf16_bits(v)
+                hits = [s_ for s_ in range(204) if np.array_equal(probe[s_], kb[0, 0, :16])]
+                assert hits, f"step {t}: no slot holds window {w.wid}"
+                s_ = hits[0]
+                for i in range(8):
+                    page = base + 8 * s_ + i
+                    assert np.array_equal(_bits(tp.k_pool[page]), kb[:, :, 16 * i:16 * i + 16])
+                    assert np.array_equal(_bits(tp.v_pool[page]), vb[:, :, 16 * i:16 * i + 16])
+                stats["recon"] += 1
+    print("tiers full size rotary:", stats)
+    assert stats["ledgers"] > 0 and stats["recon"] > 0
+    kvev.kvev_check_scratch(tp.ctx)   # no scratch region overran its guard band
+    tp.close()
