@@ -216,7 +216,7 @@ def to_dev(bits, torch):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
 
-def cpu_baseline(wl, n_layers_sample: int, min_seconds: float = 10.0, max_reps: int = 8):
+def cpu_baseline(wl, n_layers_sample: int, min_seconds: float = 10.0, max_reps: int = 32):
     """The fp64 oracle (single thread) on the first `n_layers_sample` layers
     of the same step, repeated until about `min_seconds` of CPU work (at most
     `max_reps` times; the step rewrites the same slots, so each repetition
@@ -759,9 +759,9 @@ def main():
             import oracle as O
             n_cores, model = host_cpu()
             O.set_threads(1)
-            val1, secs1, sample = cpu_baseline(wl, min(args.cpu_layers, W["n_layers"]))
+            val1, secs1, _ = cpu_baseline(wl, min(args.cpu_layers, W["n_layers"]))
             used = O.set_threads(n_cores)
-            valn, secsn, _ = cpu_baseline(wl, min(args.cpu_layers, W["n_layers"]))
+            valn, secsn, sample = cpu_baseline(wl, min(args.cpu_layers, W["n_layers"]))
             cpu = {"value": round(valn, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
                    "cpu": model, "sample": sample + f"; the attention's query heads on {used} "
                    "threads (OpenMP)", "seconds": round(secsn, 2),
@@ -865,19 +865,21 @@ def host_cpu():
     return os.cpu_count() or 1, model
 
 
-def timed_reps(fn, min_seconds: float, max_reps: int):
+def timed_reps(fn, min_seconds: float, max_reps: int, prepare=None):
     """Run fn until about min_seconds of wall time (at least once); returns
-    (repetitions, seconds)."""
+    (repetitions, seconds).  With `prepare`, each repetition runs
+    fn(prepare()) and only fn is timed (a fresh copy of a state, say)."""
     total, reps = 0.0, 0
     while reps < 1 or (total < min_seconds and reps < max_reps):
+        arg = prepare() if prepare is not None else None
         t0 = time.perf_counter()
-        fn()
+        fn(arg) if prepare is not None else fn()
         total += time.perf_counter() - t0
         reps += 1
     return reps, total
 
 
-def cpu_baseline_block(kind, W, seq_K, seq_V, inputs1, labels=None, min_seconds=8.0):
+def cpu_baseline_block(kind, W, seq_K, seq_V, inputs1, labels=None, min_seconds=10.0):
     """The oracle of a block workload (oracle/paged.py or oracle/memdecay.py)
     on one sequence of the batch, decode step 1 over its whole prefill,
     repeated to about `min_seconds`; the sequences are independent, so one
@@ -895,15 +897,16 @@ def cpu_baseline_block(kind, W, seq_K, seq_V, inputs1, labels=None, min_seconds=
                         base=(1.0,) * len(lam), lam=lam, pinned=REGION_PINNED,
                         decode_region=DECODE_REGION)
         seq0 = MD.MDSequence.from_prefill(seq_K, seq_V, labels, W["page"])
-        fn = lambda: MD.step(P, seq0.copy(), 1, True, q, kn, vn)
+        fn = lambda s: MD.step(P, s, 1, True, q, kn, vn)
     else:
         from oracle import paged as PG
         P = O.OracleParams(Ly, W["n_q_heads"], W["n_kv_heads"], d, W["budget_blocks"],
                            W["alpha"], W["beta"], O.AGE_SINCE_ACCESS, False)
         seq0 = PG.PagedSequence.from_prefill(seq_K, seq_V, W["page"])
-        fn = lambda: PG.step(P, seq0.copy(), 1, True, q, kn, vn)
+        fn = lambda s: PG.step(P, s, 1, True, q, kn, vn)
     threads = O.set_threads(os.cpu_count() or 1)
-    reps, secs = timed_reps(fn, min_seconds, 4)
+    # each repetition steps a fresh copy of the prefill state (the copy untimed)
+    reps, secs = timed_reps(fn, min_seconds, 64, prepare=seq0.copy)
     row = 2 * d * 2 * W["n_kv_heads"] * Ly
     nbytes = (W["prefill"] + 1) * row
     cores, model = host_cpu()
@@ -1435,7 +1438,7 @@ def bench_tiers(args, rank, world, local_rank, steps=None, omega=None, quiet=Fal
     return line
 
 
-def cpu_baseline_tiers(tp, wl, W, inputs1, n_layers_sample=2, min_seconds=8.0):
+def cpu_baseline_tiers(tp, wl, W, inputs1, n_layers_sample=2, min_seconds=10.0):
     """The two-tier oracle (oracle/qevict.py) on sequence 0 of the batch,
     its first `n_layers_sample` layers, decode step 1 over the whole bf16
     prefill, repeated to about `min_seconds`."""
@@ -1461,8 +1464,9 @@ def cpu_baseline_tiers(tp, wl, W, inputs1, n_layers_sample=2, min_seconds=8.0):
     q, kn, vn = (bits(x[0, :Ly]) for x in inputs1)
     import copy
     threads = O.set_threads(os.cpu_count() or 1)
-    reps, secs = timed_reps(lambda: QE.step(P, copy.deepcopy(seq0), 1, q, kn, vn),
-                            min_seconds, 4)
+    # each repetition steps a fresh copy of the prefill state (the copy untimed)
+    reps, secs = timed_reps(lambda s: QE.step(P, s, 1, q, kn, vn), min_seconds, 32,
+                            prepare=lambda: copy.deepcopy(seq0))
     nbytes = (L0 + 1) * 2 * d * 2 * Hkv * Ly
     cores, model = host_cpu()
     return {"value": round(nbytes * reps / secs / 1e9, 4), "unit": "GB/s",
