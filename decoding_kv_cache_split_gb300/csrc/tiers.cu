@@ -506,23 +506,15 @@ __device__ __forceinline__ void item_at(const int32_t* n, int batch, int LG, int
 // the quotient is divided out exactly (out of line: the rare path stays out
 // of the unrolled loops).
 __device__ __noinline__ float exact_quotient(float d, float sc) { return __fdiv_rn(d, sc); }
-__device__ __forceinline__ uint32_t int2_code(float x, float z, float sc, float r) {
+__device__ __forceinline__ float int2_quotient(float x, float z, float sc, float r) {
     const float d = __fsub_rn(x, z);
-    float y = __fmul_rn(d, r);
+    const float y = __fmul_rn(d, r);
     const float dc = fabsf(y - 1.5f);
-    if (dc <= 0x1p-16f || fabsf(dc - 1.f) <= 0x1p-16f) y = exact_quotient(d, sc);
+    return dc <= 0x1p-16f || fabsf(dc - 1.f) <= 0x1p-16f ? exact_quotient(d, sc) : y;
+}
+__device__ __forceinline__ uint32_t int2_code(float x, float z, float sc, float r) {
+    const float y = int2_quotient(x, z, sc, r);
     return (uint32_t)(y > 0.5f) + (uint32_t)(y >= 1.5f) + (uint32_t)(y > 2.5f);
-}
-// A value code's sign / magnitude bits: bit 0 code <= 1, bit 1 code 0 or 3.
-__device__ __forceinline__ uint32_t sign_mag(uint32_t c) {
-    return (uint32_t)(c <= 1u) | ((uint32_t)(c == 0u || c == 3u) << 1);
-}
-// A pair of codes as bytes (bits 0, 1: first code; 8, 9: second) -> the
-// pair's sign bits at 15, 31 and magnitude bits at 6, 22 (a multiply places
-// both halves; the cross terms land on bits the masks drop).
-__device__ __forceinline__ uint32_t pair_reg_bits(uint32_t x) {
-    return (((x & 0x0101u) * 0x00808000u) & 0x80008000u) |
-           (((x & 0x0202u) * 0x00002020u) & 0x00400040u);
 }
 
 // Quantization of one half (keys or values) of a (window, layer, KV head)
@@ -677,7 +669,16 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
                 reinterpret_cast<__half*>(led + Lay::VZ)[Lay::value_scale_index(tok, cg)] = z16;
                 const float r = sc == 0.f ? 0.f : __frcp_rn(sc);
                 // channel 32 cg + 8 jj + gg -> register 2 (4 cg + jj) + hh: word cg,
-                // slot 2 jj + hh, half e2
+                // slot 2 jj + hh, half e2: the code's sign bit (code <= 1, i.e. the
+                // quotient y < 1.5) at 15 + 16 e2 + 2 slot and its magnitude bit
+                // (code 0 or 3: y <= 0.5 or y > 2.5) 9 below, both mod 32; a zero
+                // scale gives code 0
+                uint32_t sbit[4], mbit[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    sbit[jj] = 1u << ((15 + 16 * e2 + 2 * (2 * jj + hh)) & 31);
+                    mbit[jj] = 1u << ((6 + 16 * e2 + 2 * (2 * jj + hh)) & 31);
+                }
 #pragma unroll
                 for (int gg = 0; gg < 8; ++gg) {
                     uint32_t word = 0;
@@ -685,9 +686,8 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
                     for (int jj = 0; jj < 4; ++jj) {
                         const int c = 8 * jj + gg;
                         const float x = (c & 1) ? __high2float(v2[c >> 1]) : __low2float(v2[c >> 1]);
-                        const uint32_t code = sc == 0.f ? 0u : int2_code(x, z, sc, r);
-                        const uint32_t bits = pair_reg_bits(sign_mag(code) << (8 * e2));
-                        word |= __funnelshift_l(bits, bits, 2 * (2 * jj + hh));
+                        const float y = sc == 0.f ? 0.f : int2_quotient(x, z, sc, r);
+                        word |= (y < 1.5f ? sbit[jj] : 0u) | (y <= 0.5f || y > 2.5f ? mbit[jj] : 0u);
                     }
                     word |= __shfl_xor_sync(0xffffffffu, word, 1);
                     word |= __shfl_xor_sync(0xffffffffu, word, 8);
