@@ -530,9 +530,8 @@ __device__ __forceinline__ uint32_t int2_code(float x, float z, float sc, float 
 constexpr int kQuantThreads = 256;
 constexpr int kRowPad = 8;     // bf16 elements of padding per staged row
 
-template <int D>
-__global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const TierArgs a,
-                                                                      int max_items) {
+template <int D, bool ROPE>
+__device__ __forceinline__ void quantize_items(const TierArgs& a, int max_items) {
     using Lay = LedgerLayout<D>;
     static_assert(D == 128, "ledger registers are laid out for head_dim 128");
     constexpr int PW = kTierW / kTile, WPL = Lay::WORDS_PER_LANE;
@@ -582,29 +581,52 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
             // rotated back by the row's position (the partner pair 2p +- D/2 is
             // lane ^ 4's), fp32 products and sums in the oracle's order
             const bool first_half = 2 * p < D / 2;
-            const float4* cs_row = a.rope
+            const float4* cs_row = ROPE
                 ? reinterpret_cast<const float4*>(a.rope) +
                       ((size_t)(kTierSinks + w * kTierW + grp * kQGroup) * (D / 2) +
                        ((2 * p) & (D / 2 - 1))) / 2
                 : nullptr;
-            auto key_at = [&](int row) -> float2 {
+            // the (cos, sin) of channels j, j + 1 at 8 rows row0 + k step, loaded
+            // together so that their latencies overlap
+            auto load_cs = [&](float4 (&cs)[8], int row0, int step) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) cs[k] = __ldg(cs_row + (size_t)(row0 + k * step) * (D / 4));
+            };
+            auto key_at = [&](int row, const float4& cs) -> float2 {
                 const float2 x = __bfloat1622float2(col[row * (XS / 2)]);
-                if (!a.rope) return x;
+                if (!ROPE) return x;
                 const float yx = __shfl_xor_sync(0xffffffffu, x.x, 4);
                 const float yy = __shfl_xor_sync(0xffffffffu, x.y, 4);
-                const float4 cs = __ldg(cs_row + (size_t)row * (D / 4));   // cos, sin of j, j + 1
                 return first_half
                     ? make_float2(__fadd_rn(__fmul_rn(x.x, cs.x), __fmul_rn(yx, cs.y)),
                                   __fadd_rn(__fmul_rn(x.y, cs.z), __fmul_rn(yy, cs.w)))
                     : make_float2(__fsub_rn(__fmul_rn(x.x, cs.x), __fmul_rn(yx, cs.y)),
                                   __fsub_rn(__fmul_rn(x.y, cs.z), __fmul_rn(yy, cs.w)));
             };
-            float2 mn = key_at(0), mx = mn;
+            float4 cs[8];
+            float2 mn, mx;
+            if constexpr (ROPE) {
+                mn = make_float2(INFINITY, INFINITY);
+                mx = make_float2(-INFINITY, -INFINITY);
 #pragma unroll
-            for (int r = 1; r < kQGroup; ++r) {
-                const float2 x = key_at(r);
-                mn = make_float2(fminf(mn.x, x.x), fminf(mn.y, x.y));
-                mx = make_float2(fmaxf(mx.x, x.x), fmaxf(mx.y, x.y));
+                for (int r0 = 0; r0 < kQGroup; r0 += 8) {
+                    load_cs(cs, r0, 1);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float2 x = key_at(r0 + k, cs[k]);
+                        mn = make_float2(fminf(mn.x, x.x), fminf(mn.y, x.y));
+                        mx = make_float2(fmaxf(mx.x, x.x), fmaxf(mx.y, x.y));
+                    }
+                }
+            } else {
+                mn = key_at(0, cs[0]);
+                mx = mn;
+#pragma unroll
+                for (int r = 1; r < kQGroup; ++r) {
+                    const float2 x = key_at(r, cs[0]);
+                    mn = make_float2(fminf(mn.x, x.x), fminf(mn.y, x.y));
+                    mx = make_float2(fmaxf(mx.x, x.x), fmaxf(mx.y, x.y));
+                }
             }
             const __half2 z16 = __floats2half2_rn(mn.x, mn.y);
             const __half2 s16 = __floats2half2_rn(__fdiv_rn(__fsub_rn(mx.x, mn.x), 3.0f),
@@ -616,14 +638,17 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
             const float r0 = sc.x == 0.f ? 0.f : __frcp_rn(sc.x);
             const float r1 = sc.y == 0.f ? 0.f : __frcp_rn(sc.y);
             const int b0 = Lay::key_bit(Lay::key_field(s8), 0);   // field of k-step s8
-            // token 8 i + gg of tile 2 grp + tt: word 2 i + h of lane 4 gg + t
+            // token 8 i + gg of tile 2 grp + tt: word 2 i + h of lane 4 gg + t (with
+            // rotary positions the 8 rows of one (tt, i) share a batch of loads)
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
-                for (int gg = 0; gg < 8; ++gg)
+                for (int io = 0; io < (ROPE ? 2 : 8); ++io) {
+                    if constexpr (ROPE) load_cs(cs, 16 * tt + 8 * io, 1);
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const float2 x = key_at(16 * tt + 8 * i + gg);
+                    for (int ii = 0; ii < (ROPE ? 8 : 2); ++ii) {
+                        const int gg = ROPE ? ii : io, i = ROPE ? io : ii;
+                        const float2 x = key_at(16 * tt + 8 * i + gg, cs[ROPE ? ii : 0]);
                         const uint32_t c0 = sc.x == 0.f ? 0u : int2_code(x.x, z.x, sc.x, r0);
                         const uint32_t c1 = sc.y == 0.f ? 0u : int2_code(x.y, z.y, sc.y, r1);
                         uint32_t word = (c0 << b0) | (c1 << (b0 + 16));
@@ -633,6 +658,7 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
                         if (s8 == 0)
                             words[(2 * grp + tt) * D + (4 * gg + t) * WPL + 2 * i + h] = word;
                     }
+                }
         } else {
             // values: token tok over channel groups cg and cg + 2; the codes of
             // channel 8 j + gg sit in register 2 j + h of lane 4 gg + t, half e,
@@ -698,6 +724,19 @@ __global__ void __launch_bounds__(kQuantThreads) tier_quantize_kernel(const Tier
         }
         __syncthreads();
     }
+}
+
+// The plain quantizer at 4 CTAs per SM; the rotary one without a register cap
+// (its batches of table loads want the registers).
+template <int D>
+__global__ void __launch_bounds__(kQuantThreads, 4) tier_quantize_kernel(const TierArgs a,
+                                                                         int max_items) {
+    quantize_items<D, false>(a, max_items);
+}
+template <int D>
+__global__ void __launch_bounds__(kQuantThreads) tier_quantize_rope_kernel(const TierArgs a,
+                                                                           int max_items) {
+    quantize_items<D, true>(a, max_items);
 }
 
 // Promotion of one half (keys or values) of a (window, layer, KV head) item:
@@ -944,7 +983,7 @@ cudaError_t launch_tier_route(const TierArgs& a, cudaStream_t s) {
 cudaError_t launch_tier_quantize(const TierArgs& a, int max_items, int num_sms, cudaStream_t s) {
     if (max_items <= 0) return cudaSuccess;
     if (a.head_dim != 128) return cudaErrorInvalidValue;
-    auto kern = tier_quantize_kernel<128>;
+    auto kern = a.rope ? tier_quantize_rope_kernel<128> : tier_quantize_kernel<128>;
     const int smem = kTierW * (128 + kRowPad) * 2;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
