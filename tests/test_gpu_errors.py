@@ -109,3 +109,31 @@ def test_scratch_that_cannot_be_allocated_is_reported():
     assert err.value.status in (kvev.KVEV_ENOMEM, kvev.KVEV_EINVAL)
     x = torch.ones(1024, device="cuda")
     assert float(x.sum()) == 1024.0
+
+
+def test_rotary_table_refusals():
+    """kvev_set_rope refuses a token-granular context (KVEV_ESTATE), a table
+    shorter than max_ctx or not 16-byte aligned (KVEV_EINVAL); in rotary mode
+    kvev_tier_begin refuses a page range without room for the 8 K_q
+    reconstruction pages, and after it K_q cannot grow past them (KVEV_ESTATE)
+    while it may shrink."""
+    L0 = 5 + 128 * 3 + 20
+    max_ctx = L0 + 16
+    table = torch.zeros((max_ctx, 64, 2), dtype=torch.float32, device="cuda")
+    ep = kvev.EvictionPass(2, 8, 2, 128, 1, 64, 32, 0.05, 0.001)
+    assert _status(kvev.kvev_set_rope, ep.ctx, table, max_ctx) == kvev.KVEV_ESTATE
+    ep.close()
+    used = 1 + -(-(L0 - 5) // 16)
+    tight = kvev.TierEvictionPass(2, 32, 8, 128, 1, max_ctx, used + 4, 1, 2, 4, 0.05)
+    assert _status(kvev.kvev_set_rope, tight.ctx, table, max_ctx - 1) == kvev.KVEV_EINVAL
+    assert _status(kvev.kvev_set_rope, tight.ctx, table.data_ptr() + 4, max_ctx) == kvev.KVEV_EINVAL
+    kvev.kvev_set_rope(tight.ctx, table, max_ctx)
+    assert _status(tight.begin, L0) == kvev.KVEV_EINVAL          # no room for 16 scratch pages
+    tight.close()
+    tp = kvev.TierEvictionPass(2, 32, 8, 128, 1, max_ctx, used + 4 + 16, 1, 2, 4, 0.05,
+                               rope=table)
+    tp.begin(L0)
+    assert _status(kvev.kvev_set_tiers, tp.ctx, 1, 3, 4) == kvev.KVEV_ESTATE
+    kvev.kvev_set_tiers(tp.ctx, 1, 1, 4)                         # shrinking is allowed
+    kvev.kvev_sync(tp.ctx)
+    tp.close()
