@@ -526,7 +526,9 @@ __device__ __forceinline__ uint32_t int2_code(float x, float z, float sc, float 
 // Values: a thread per token and 32-channel group; each turns its codes into
 // the sign / magnitude bits of their ledger registers, and the threads whose
 // bits share a word OR them together with two shuffles.  One thread of a
-// word stores it.
+// word stores it.  With rotary positions (ROPE) a key pair is first rotated
+// back in fp32 with its partner pair, the table's cos / sin of 8 rows loaded
+// together.
 constexpr int kQuantThreads = 256;
 constexpr int kRowPad = 8;     // bf16 elements of padding per staged row
 
