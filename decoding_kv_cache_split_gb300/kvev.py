@@ -586,7 +586,10 @@ class TierEvictionPass:
     sinks, page b*pps + 1 + i tokens 5 + 16 i ..); the INT2 ledger
     [batch][max_windows][Ly][Hkv][12288] bytes; per-window score, tier,
     ledger flag and pages; outputs out [b][Ly][Hq][d] fp32.  All torch
-    tensors on the current CUDA device."""
+    tensors on the current CUDA device.  rope: the model's rotary table
+    [positions >= max_ctx][d/2][2] (cos, sin) for rotary mode (the pools
+    then hold rotated keys, and pages_per_seq must also hold the 8 k_quant
+    reconstruction pages at the end of each sequence's range)."""
 
     def __init__(self, n_layers, n_q_heads, n_kv_heads, head_dim, batch, max_ctx, pages_per_seq,
                  k_full, k_quant, omega, alpha, aggregation=KVEV_AGG_EMA, rope=None,
