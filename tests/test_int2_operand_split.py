@@ -151,3 +151,44 @@ def test_value_bias_centres_as_fp16_hi_and_lo():
     assert np.all(err[~big] <= 2.0 ** -33)
     assert np.all(zero < 0) and np.all(scale > 0)
     assert 0.3 < np.mean(mid > 0) < 0.7
+
+
+def test_fp16_operands_alone_would_be_too_coarse():
+    """Why the key-side A operand is a bf16 hi + lo pair rather than one fp16
+    value (11 significant bits, which would save the split): over 8192 INT2
+    tokens with the workload's key statistics (N(0,1) keys, 4 outlier
+    channels of std 8, the query pulled towards 16 keys), rounding each q_c s_c
+    to fp16 moves the attention output by more than 5e-4 relative (the whole
+    INT2 path holds 5e-4 at full size against the 2e-3 tolerance; here
+    1.5e-3), while the hi + lo pair of the same products (16 significant bits)
+    stays below 1e-4 (4.2e-5)."""
+    rng = np.random.default_rng(5)
+    n, d, G = 8192, 128, 4
+    K = rng.standard_normal((n, d)).astype(F)
+    K[:, rng.choice(d, 4, replace=False)] *= F(8)
+    q = (rng.standard_normal((G, d)) + 0.5 * K[rng.choice(n, 16)].mean(0)).astype(F)
+    Kg = K.reshape(-1, 32, d)                                 # 32-token key groups
+    mn, mx = Kg.min(1, keepdims=True), Kg.max(1, keepdims=True)
+    z = mn.astype(np.float16).astype(F)
+    s = ((mx - mn) / F(3)).astype(np.float16).astype(F)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        c = np.where(s == 0, 0, np.clip(np.rint((Kg - z) / s), 0, 3))
+    bias = (q.astype(np.float64) @ z[:, 0].T.astype(np.float64)).repeat(32, 1)   # sum q z
+    qs = (q[:, None, None, :] * s[None]).astype(F)           # [G][group][1][d] fp32
+    hi, lo = split(qs)
+
+    def logits(a):
+        return np.einsum("hgxd,gtd->hgt", a.astype(np.float64), c).reshape(G, n) + bias
+
+    ref = q.astype(np.float64) @ (c * s + z).astype(F).astype(np.float64).reshape(n, d).T
+    V = rng.standard_normal((n, d))
+
+    def out(lg):
+        lg = lg / np.sqrt(d)
+        p = np.exp(lg - lg.max(1, keepdims=True))
+        return (p / p.sum(1, keepdims=True)) @ V
+
+    o_ref = out(ref)
+    rel = lambda o: float((np.abs(o - o_ref).max(1) / np.abs(o_ref).max(1)).max())
+    assert rel(out(logits(qs.astype(np.float16)))) > 5e-4
+    assert rel(out(logits(hi.astype(np.float64) + lo.astype(np.float64)))) < 1e-4
