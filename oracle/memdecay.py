@@ -21,7 +21,7 @@ Cache Eviction for Efficient LLM Agent Inference":
     pinning protects whole pages).
 
 Parity unpinned: the per-region base priorities b_r.  The page prints the
-caption of its Table I without the values; this build reads b_r = 1 for every
+caption of its Table I without the values; this oracle reads b_r = 1 for every
 region (any b_r enters the same Eq. (4), whose structure the pins check), so
 no test can tie the values themselves to the page.
 

@@ -13,7 +13,7 @@ Attention-Drift-Robust Long-Context Decoding" (the review page), Sec. 4:
     (the inner sums of Eq. (1)), folded per step into an EMA with weight
     alpha on the new value, layer after layer in ascending order, kept
     across steps (the LRFU EMA of the kv-cache-docs figure "ema-eviction",
-    the reading this build takes for "EMA accumulated-attention score"); or,
+    the reading taken here of "EMA accumulated-attention score"); or,
     with `cumulative`, Sec. 4.2 Eq. (1) itself: the head-averaged window
     attention added up over steps and, since one routing decision covers
     every layer, over layers too (a sum that never forgets);
@@ -31,7 +31,7 @@ Parity unpinned: the window geometry and routing interval (sinks 5, recent
 32, windows of 128 tokens on the grid after the sinks, routing every Omega = 8
 steps at the end of the step).  The page gives the sink and recent counts and
 Omega but not where windows start or when in a step routing happens; these
-are this build's readings, and no pin ties them to the page beyond the
+are the readings taken here, and no pin ties them to the page beyond the
 capacity example of Eq. (3).
 
 INT2 codec (asymmetric, as the page's KIVI-style scheme: per-channel keys,
